@@ -1,0 +1,125 @@
+"""fp64 CPU oracle for the KLA recurrence -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never calls it and
+shares no code with it.
+
+``kla_oracle_forward`` wraps the plain sequential C loop in ``kla_oracle.c``
+(fp64, program order, no fast-math).  It follows "KLA: Kaczmarz Linear
+Attention" (gist.science/ko/paper/2605.08587), section "KLA update rule":
+beta_t = eta_t / (||k_t||^2 + eps), S_t = S~_{t-1} + beta_t k_t e_t^T with
+e_t = v_t - S~_{t-1}^T k_t, S~_{t-1} = exp(g_t) S_{t-1}, and o_t = S_t^T q_t.
+The decode-step oracle is the same loop with T = 1 and h0 = S.
+
+Pins (all in ``tests/test_oracle_*.py``): the projection constraint
+S_t^T k_t = v_t at eta=1, eps=0 (section "Theoretical derivation"); the
+minimum-Frobenius-norm property against a least-squares solve; the exact
+line search and the normalised-SGD step (section "Key properties"); the
+beta=0 closed form; the no-erase mode against brute-force masked attention;
+and a hand-worked two-token fixture under ``tests/golden/``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kla_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libkla_oracle.so")
+
+NO_ERASE = 1
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain IEEE fp64, no fast-math)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           "-pthread", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            f = lib.kla_oracle_forward
+            dp = ctypes.POINTER(ctypes.c_double)
+            i64 = ctypes.c_int64
+            f.argtypes = [dp, dp, dp, dp, dp, ctypes.c_double, dp, dp, dp, dp,
+                          i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int]
+            f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor -> numpy on the host
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def kla_oracle_forward(q, k, v, g, eta, eps, h0=None, *, no_erase=False,
+                       return_states=False, threads=0):
+    """Sequential fp64 forward over t for every (b, h).
+
+    Shapes: q,k [B,T,H,dk]; v [B,T,H,dv]; g,eta [B,T,H]; h0 [B,H,dk,dv] or None.
+    Returns (o [B,T,H,dv], hT [B,H,dk,dv]) and, with ``return_states``, also
+    states [B,H,T,dk,dv] with states[b,h,t] = S_t (small inputs only).
+    """
+    q, k, v, g, eta, h0 = map(_f64, (q, k, v, g, eta, h0))
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    assert q.shape == (B, T, H, dk) and v.shape == (B, T, H, dv)
+    assert g.shape == (B, T, H) and eta.shape == (B, T, H)
+    if h0 is not None:
+        assert h0.shape == (B, H, dk, dv)
+    o = np.zeros((B, T, H, dv), np.float64)
+    hT = np.zeros((B, H, dk, dv), np.float64)
+    states = np.zeros((B, H, T, dk, dv), np.float64) if return_states else None
+    rc = _load().kla_oracle_forward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(eta), float(eps), _ptr(h0),
+        _ptr(o), _ptr(hT), _ptr(states), B, T, H, dk, dv,
+        NO_ERASE if no_erase else 0, int(threads))
+    if rc != 0:
+        raise RuntimeError(f"kla_oracle_forward failed with code {rc}")
+    if return_states:
+        return o, hT, states
+    return o, hT
+
+
+def kla_oracle_decode_step(q, k, v, g, eta, eps, S):
+    """One recurrent decode step: the forward loop with T = 1, h0 = S.
+
+    Shapes: q,k [B,H,dk]; v [B,H,dv]; g,eta [B,H]; S [B,H,dk,dv].
+    Returns (o [B,H,dv], S_new [B,H,dk,dv]).
+    """
+    q, k, v, g, eta, S = map(_f64, (q, k, v, g, eta, S))
+    o, hT = kla_oracle_forward(q[:, None], k[:, None], v[:, None], g[:, None],
+                               eta[:, None], eps, S)
+    return o[:, 0], hT
+
+
+__all__ = ["build", "kla_oracle_forward", "kla_oracle_decode_step", "NO_ERASE"]
