@@ -1,0 +1,401 @@
+#!/usr/bin/env python3
+"""Throughput of the KLA hot path on one GB300 (or N independent replicas).
+
+Headline workload: the training-shape prefill (B=8, H=8, T=4096,
+d_k=d_v=128, bf16 q/k/v/o, fp32 gates, chunk 64) through kla_chunk_fwd:
+one step = one call over that batch.  The long-context prefill
+(B=1, H=16, T=131072) and the decode loop (B=64, H=16, d=128, fp32 state,
+kla_decode_step) are timed in the same run and reported under "secondary".
+
+Timing: W untimed warm-up steps, then exactly K timed steps, each between
+CUDA events on the launching stream; L2 is flushed (a 512 MiB write) between
+timed steps, outside the events; barrier + synchronize on both sides; max
+over ranks.  SM clocks are sampled with nvidia-smi during the run.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (rank 0 only).
+
+Prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import kla_inputs  # noqa: E402
+
+METRIC = "prefill tokens/s & % roofline at T=4K/131K; decode tokens/s & HBM GB/s"
+FLUSH_BYTES = 512 << 20
+
+
+# --------------------------------------------------------------- work model
+
+def prefill_work(case):
+    """Algorithmic bytes and flops of one prefill call (per launch)."""
+    C, dk, dv = case.chunk, case.dk, case.dv
+    esz = 2 if case.io == "bf16" else 4
+    th = case.B * case.T * case.H
+    per_tok_bytes = esz * (2 * dk + 2 * dv) + 8          # q, k, v, o + g, eta
+    state_bytes = case.B * case.H * dk * dv * 4          # hT written (h0 absent)
+    if case.h0_std > 0:
+        state_bytes *= 2
+    flops_tok = 4 * C * dk + 2 * C * (dk + dv) + 2 * C * dv + 6 * dk * dv
+    return dict(bytes=th * per_tok_bytes + state_bytes, flops=th * flops_tok,
+                token_heads=th, tokens=case.B * case.T,
+                per_token_head_bytes=per_tok_bytes, per_token_head_flops=flops_tok)
+
+
+def decode_work(case):
+    heads = case.B * case.H
+    esz = 2 if case.io == "bf16" else 4
+    per_head = 2 * case.dk * case.dv * 4 + esz * (2 * case.dk + 2 * case.dv) + 8
+    return dict(bytes=heads * per_head, flops=heads * (6 * case.dk * case.dv + 4 * case.dk),
+                tokens=case.B, per_head_bytes=per_head)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def roofline(work, seconds, peaks):
+    t_mem = work["bytes"] / (peaks["hbm"] * 1e9)
+    t_flop = work["flops"] / (peaks["bf16"] * 1e12)
+    if t_mem >= t_flop:
+        ach = work["bytes"] / seconds / 1e9
+        return dict(bound="hbm", achieved=round(ach, 1), peak=peaks["hbm"], unit="GB/s",
+                    frac=round(ach / peaks["hbm"], 4), traffic=None,
+                    peak_source=peaks["source"], roofline_us=round(t_mem * 1e6, 2))
+    ach = work["flops"] / seconds / 1e12
+    return dict(bound="tensor", achieved=round(ach, 2), peak=peaks["bf16"], unit="TFLOP/s",
+                frac=round(ach / peaks["bf16"], 4), traffic=None,
+                peak_source=peaks["source"], roofline_us=round(t_flop * 1e6, 2))
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.proc = None
+        self.out = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}",
+                    "--format=csv,noheader,nounits", "-lms", "200"]
+
+    def start(self):
+        try:
+            self.out = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(self.cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(self.NAMES, r[5:9]):
+                if "Active" in val and "Not" not in val:
+                    reasons.add(name)
+        loaded = [s for s, p in zip(sm, pw) if pw and p >= 0.5 * max(pw)] or sm
+        return dict(sm_mhz=statistics.median(loaded) if loaded else None,
+                    sm_max_mhz=max(mx) if mx else None, reasons=sorted(reasons),
+                    samples=len(rows), power_w_max=max(pw) if pw else None)
+
+
+# ------------------------------------------------------------------- timing
+
+def timed_steps(step, K, W, flush_buf, stream):
+    """W warm-up steps, then K steps each bracketed by events on `stream`."""
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    for a, b in evs:
+        if flush_buf is not None:
+            flush_buf.add_(1)
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]  # ms
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float) -> float:
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+    return x
+
+
+# ------------------------------------------------------------- native arm
+
+# Kernels of ours launched per ABI call, by dispatch: kla_chunk_fwd launches
+# one prefill kernel (plus a 256-byte cudaMemsetAsync of the error record,
+# not a kernel of ours); kla_decode_step launches one kernel.
+LAUNCHES_PER_PREFILL = 1
+LAUNCHES_PER_DECODE = 1
+
+
+def bench_prefill(case, K, W, flush, peaks, stream):
+    import chunked_delta_rule_kla_gb300 as kla
+    inp = kla_inputs.make_prefill(case, device="cuda")
+    B, T, H, dk, dv = case.B, case.T, case.H, case.dk, case.dv
+    o = torch.empty((B, T, H, dv), dtype=inp["q"].dtype, device="cuda")
+    hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
+    ws = kla.alloc_workspace(B, T, H, dk, dv, case.chunk, kla.KLA_IO_BF16 if case.io == "bf16" else kla.KLA_IO_FP32)
+
+    def step():
+        kla.kla_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["eta"], inp["eps"], inp["h0"],
+                          o, hT, ws, case.chunk, stream)
+
+    barrier()
+    ms = timed_steps(step, K, W, flush, stream)
+    barrier()
+    assert kla.kla_workspace_check(ws, stream) == kla.KLA_OK
+    work = prefill_work(case)
+    mean_ms = max_over_ranks(sum(ms) / len(ms))
+    res = dict(ms_per_step=mean_ms, tokens_per_s=work["tokens"] / (mean_ms * 1e-3),
+               tflops=work["flops"] / (mean_ms * 1e-3) / 1e12,
+               gbps=work["bytes"] / (mean_ms * 1e-3) / 1e9,
+               roofline=roofline(work, mean_ms * 1e-3, peaks), work=work,
+               launches=K * LAUNCHES_PER_PREFILL, min_ms=min(ms))
+
+    # end to end through the public API: pinned host inputs -> device -> call -> host
+    host = {n: inp[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "eta")}
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h_h = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
+    dev = {n: torch.empty_like(inp[n]) for n in host}
+
+    def e2e_step():
+        for n in host:
+            dev[n].copy_(host[n], non_blocking=True)
+        kla.kla_chunk_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["eta"], inp["eps"], None,
+                          o, hT, ws, case.chunk, stream)
+        o_h.copy_(o, non_blocking=True)
+        h_h.copy_(hT, non_blocking=True)
+
+    Ke = max(3, min(K, 20))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(Ke):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / Ke)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_h.numel() * o_h.element_size() + h_h.numel() * h_h.element_size()
+    res["e2e"] = dict(value=work["tokens"] / e2e_s, unit="tokens/s", h2d_bytes_per_step=h2d,
+                      d2h_bytes_per_step=d2h, ms_per_step=e2e_s * 1e3, steps=Ke)
+    del inp, o, hT, host, dev
+    return res
+
+
+def bench_decode(case, K_loops, W_loops, peaks, stream, n_states=4):
+    """Times `steps` consecutive kla_decode_step calls per loop.  The calls
+    rotate over n_states independent state buffers (like the layers of a
+    model), so the state working set (n_states x 64 MiB) exceeds L2."""
+    import chunked_delta_rule_kla_gb300 as kla
+    steps = case.steps
+    inp = kla_inputs.make_decode(case, device="cuda")
+    states = [inp["S"].clone() for _ in range(n_states)]
+    o = torch.empty((case.B, case.H, case.dv), dtype=inp["q"].dtype, device="cuda")
+
+    def loop():
+        for t in range(steps):
+            kla.kla_decode_step(inp["q"][t], inp["k"][t], inp["v"][t], inp["g"][t], inp["eta"][t],
+                                inp["eps"], states[t % n_states], o, stream)
+
+    barrier()
+    ms = timed_steps(loop, K_loops, W_loops, None, stream)
+    barrier()
+    work = decode_work(case)
+    per_call_s = max_over_ranks(sum(ms) / len(ms) / steps * 1e-3)
+    res = dict(ms_per_call=per_call_s * 1e3, tokens_per_s=work["tokens"] / per_call_s,
+               gbps=work["bytes"] / per_call_s / 1e9, roofline=roofline(work, per_call_s, peaks),
+               work=work, launches=K_loops * steps * LAUNCHES_PER_DECODE, calls_per_loop=steps,
+               states_rotated=n_states)
+
+    # end to end: per call, pinned host q/k/v/g/eta -> device, step, o -> host
+    hq = {n: inp[n][:64].cpu().pin_memory() for n in ("q", "k", "v", "g", "eta")}
+    dq = {n: torch.empty_like(hq[n][0], device="cuda") for n in hq}
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    n_e2e = 64
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for t in range(n_e2e):
+        for n in hq:
+            dq[n].copy_(hq[n][t], non_blocking=True)
+        kla.kla_decode_step(dq["q"], dq["k"], dq["v"], dq["g"], dq["eta"], inp["eps"],
+                            states[t % n_states], o, stream)
+        o_h.copy_(o, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e)
+    res["e2e"] = dict(value=case.B / e2e_s, unit="tokens/s",
+                      h2d_bytes_per_step=sum(t[0].numel() * t.element_size() for t in hq.values()),
+                      d2h_bytes_per_step=o_h.numel() * o_h.element_size(), ms_per_step=e2e_s * 1e3)
+    del inp, states
+    return res
+
+
+def cpu_baseline_prefill(case, max_heads=16):
+    """The fp64 oracle as it stands, on the host cores, on a bounded sample:
+    the first `max_heads` heads of the workload over the full sequence."""
+    import oracle
+    inp = kla_inputs.make_prefill(case.with_(B=1, H=max_heads), device="cpu")
+    cores = os.cpu_count() or 1
+    threads = min(cores, max_heads)
+    t0 = time.perf_counter()
+    oracle.kla_oracle_forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["eta"], inp["eps"],
+                              inp["h0"], threads=threads)
+    dt = time.perf_counter() - t0
+    th = case.T * max_heads
+    tokens_equiv = th / case.H  # tokens of the workload whose all H heads this sample covers
+    return dict(value=tokens_equiv / dt, unit="tokens/s", cores=threads, kind="oracle",
+                sample=f"{max_heads} heads x T={case.T} of {case.name} ({th} token-heads), "
+                       f"{dt:.2f} s wall, fp64 sequential loop, one thread per head")
+
+
+# ------------------------------------------------------------------- main
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    case = kla_inputs.TRAIN
+    per = []
+    for _ in range(args.warmup):
+        cpu_baseline_prefill(case, max_heads=args.ref_heads)
+    for _ in range(args.steps):
+        per.append(cpu_baseline_prefill(case, max_heads=args.ref_heads))
+    val = statistics.median(p["value"] for p in per)
+    line = dict(impl="reference", metric=METRIC, value=val, unit="tokens/s", n_gpus=args.gpus,
+                steps=args.steps, warmup=args.warmup, ms_per_step=case.B * case.T / val * 1e3,
+                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
+                data="synthetic", config=dict(workload=case.name, B=case.B, T=case.T, H=case.H,
+                                              dk=case.dk, dv=case.dv, chunk=case.chunk),
+                cpu_baseline=dict(per[0], value=val),
+                e2e=dict(value=val, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-secondary", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-heads", type=int, default=16)
+    ap.add_argument("--decode-loops", type=int, default=3)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank)
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import chunked_delta_rule_kla_gb300 as kla
+    kla.load_library()
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    clocks = ClockSampler(torch.cuda.current_device()).start()
+
+    main_case = kla_inputs.TRAIN
+    head = bench_prefill(main_case, args.steps, args.warmup, flush, peaks, stream)
+    secondary = {}
+    if not args.no_secondary:
+        lc = kla_inputs.LONG
+        lr = bench_prefill(lc, max(3, args.steps // 10), 3, flush, peaks, stream)
+        secondary["long_prefill"] = dict(workload=lc.name, tokens_per_s=lr["tokens_per_s"],
+                                         ms_per_step=lr["ms_per_step"], roofline=lr["roofline"],
+                                         tflops=lr["tflops"], e2e=lr["e2e"])
+        dc = kla_inputs.DECODE
+        dr = bench_decode(dc, args.decode_loops, 3, peaks, stream)
+        secondary["decode"] = dict(workload=dc.name, tokens_per_s=dr["tokens_per_s"],
+                                   hbm_gbs=dr["gbps"], us_per_call=dr["ms_per_call"] * 1e3,
+                                   roofline=dr["roofline"], e2e=dr["e2e"],
+                                   states_rotated=dr["states_rotated"])
+    clk = clocks.stop()
+    if rank != 0:
+        return
+    n = world
+    line = dict(
+        metric=METRIC, value=head["tokens_per_s"] * n, unit="tokens/s", n_gpus=n,
+        steps=args.steps, warmup=args.warmup, ms_per_step=head["ms_per_step"],
+        higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
+        data="synthetic",
+        config=dict(workload=main_case.name, B=main_case.B, T=main_case.T, H=main_case.H,
+                    dk=main_case.dk, dv=main_case.dv, chunk=main_case.chunk, io="bf16",
+                    l2="flushed between timed steps (512 MiB write, outside the events)",
+                    parallelism=f"replicas x{n}" if n > 1 else "single GPU"),
+        tflops=head["tflops"], hbm_gbs_algorithmic=head["gbps"],
+        roofline=head["roofline"], e2e=dict(head["e2e"], value=head["e2e"]["value"] * n),
+        gpu_launches=head["launches"], clocks=clk, secondary=secondary,
+    )
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_prefill(main_case, max_heads=args.ref_heads)
+    print(json.dumps(line), flush=True)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

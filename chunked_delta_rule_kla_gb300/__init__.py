@@ -1,0 +1,214 @@
+"""Python binding of libkla (the KLA chunkwise prefill and decode step).
+
+Thin ctypes marshalling over the C ABI in ``include/kla.h``: the functions
+below carry the ABI's names and hand device pointers, sizes and the current
+CUDA stream to the library; every step of the computation runs in the
+library's CUDA kernels.  PyTorch only provides device memory and streams.
+
+The library is loaded on first use from ``_build/libkla.so`` (built by
+``__graft_entry__.build()`` or ``python -m chunked_delta_rule_kla_gb300._build``).
+If it is missing, every op raises: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+KLA_OK = 0
+KLA_ERR_INVALID_ARG = 1
+KLA_ERR_UNSUPPORTED = 2
+KLA_ERR_WORKSPACE = 3
+KLA_ERR_CUDA = 4
+KLA_ERR_DEVICE_TIMEOUT = 5
+
+KLA_IO_BF16 = 0
+KLA_IO_FP32 = 1
+
+# Every symbol include/kla.h declares (checked by the ABI tests).
+EXPORTED_SYMBOLS = (
+    "kla_chunk_fwd_workspace_bytes",
+    "kla_chunk_fwd",
+    "kla_decode_step",
+    "kla_workspace_check",
+    "kla_status_string",
+)
+
+
+class KlaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {kla_status_string(code)} ({code})")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libkla.so (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or _build.LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"libkla.so is not built ({p}); run `python -c \"import __graft_entry__ as g; g.build()\"`")
+        lib = ctypes.CDLL(p)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.kla_chunk_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+        lib.kla_chunk_fwd_workspace_bytes.restype = sz
+        lib.kla_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp,
+                                      i, i, i, i, i, i, i, vp, sz, vp]
+        lib.kla_chunk_fwd.restype = i
+        lib.kla_decode_step.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp]
+        lib.kla_decode_step.restype = i
+        lib.kla_workspace_check.argtypes = [vp, sz, vp]
+        lib.kla_workspace_check.restype = i
+        lib.kla_status_string.argtypes = [i]
+        lib.kla_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def kla_status_string(code: int) -> str:
+    return load_library().kla_status_string(int(code)).decode()
+
+
+def _io_of(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KLA_IO_BF16
+    if t.dtype == torch.float32:
+        return KLA_IO_FP32
+    raise TypeError(f"q/k/v/o must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t, name, dtype=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr() or None
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def kla_chunk_fwd_workspace_bytes(B, T, H, dk, dv, chunk=64, io=KLA_IO_BF16) -> int:
+    return int(load_library().kla_chunk_fwd_workspace_bytes(B, T, H, dk, dv, chunk, io))
+
+
+def kla_chunk_fwd(q, k, v, g, eta, eps, h0, o, hT, workspace, chunk=64, stream=None) -> None:
+    """Enqueue the chunkwise prefill (see include/kla.h) on ``stream``.
+
+    q, k [B,T,H,dk]; v, o [B,T,H,dv] (bf16 or fp32, same dtype); g, eta
+    [B,T,H] fp32; h0, hT [B,H,dk,dv] fp32 or None; workspace a uint8 CUDA
+    tensor of at least kla_chunk_fwd_workspace_bytes(...) bytes.
+    """
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    io = _io_of(q)
+    for name, t in (("k", k), ("v", v), ("o", o)):
+        if t.dtype != q.dtype:
+            raise TypeError(f"{name} must have q's dtype {q.dtype}")
+    if q.shape != k.shape or v.shape[:3] != k.shape[:3] or o.shape != v.shape:
+        raise ValueError("shape mismatch among q, k, v, o")
+    if g.shape != (B, T, H) or eta.shape != (B, T, H):
+        raise ValueError("g and eta must be [B,T,H]")
+    for name, t in (("h0", h0), ("hT", hT)):
+        if t is not None and tuple(t.shape) != (B, H, dk, dv):
+            raise ValueError(f"{name} must be [B,H,dk,dv]")
+    rc = load_library().kla_chunk_fwd(
+        _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g", torch.float32),
+        _ptr(eta, "eta", torch.float32), float(eps), _ptr(h0, "h0", torch.float32),
+        _ptr(o, "o"), _ptr(hT, "hT", torch.float32), B, T, H, dk, dv, int(chunk), io,
+        _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    if rc != KLA_OK:
+        raise KlaError(rc, "kla_chunk_fwd")
+
+
+def kla_decode_step(q, k, v, g, eta, eps, S, o, stream=None) -> None:
+    """Enqueue one decode step (see include/kla.h); S [B,H,dk,dv] is updated in place.
+
+    q, k [B,H,dk]; v, o [B,H,dv] (bf16 or fp32); g, eta [B,H] fp32.
+    """
+    B, H, dk = k.shape
+    dv = v.shape[-1]
+    io = _io_of(q)
+    for name, t in (("k", k), ("v", v), ("o", o)):
+        if t.dtype != q.dtype:
+            raise TypeError(f"{name} must have q's dtype {q.dtype}")
+    if q.shape != k.shape or v.shape[:2] != k.shape[:2] or o.shape != v.shape:
+        raise ValueError("shape mismatch among q, k, v, o")
+    if g.shape != (B, H) or eta.shape != (B, H) or tuple(S.shape) != (B, H, dk, dv):
+        raise ValueError("g, eta must be [B,H] and S [B,H,dk,dv]")
+    rc = load_library().kla_decode_step(
+        _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g", torch.float32),
+        _ptr(eta, "eta", torch.float32), float(eps), _ptr(S, "S", torch.float32),
+        _ptr(o, "o"), B, H, dk, dv, io, _stream(stream))
+    if rc != KLA_OK:
+        raise KlaError(rc, "kla_decode_step")
+
+
+def kla_workspace_check(workspace, stream=None) -> int:
+    """Synchronise and read the workspace's device error record (status code)."""
+    return int(load_library().kla_workspace_check(
+        _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+# ---- allocation helpers (torch memory only; the compute is the ABI call) ----
+
+def alloc_workspace(B, T, H, dk, dv, chunk=64, io=KLA_IO_BF16, device="cuda") -> torch.Tensor:
+    n = kla_chunk_fwd_workspace_bytes(B, T, H, dk, dv, chunk, io)
+    if n == 0:
+        raise KlaError(KLA_ERR_UNSUPPORTED, "kla_chunk_fwd_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def chunk_fwd(q, k, v, g, eta, eps=1e-6, h0=None, output_final_state=True, chunk=64,
+              workspace=None, stream=None):
+    """Allocate o (and hT) and run kla_chunk_fwd.  Returns (o, hT or None)."""
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device) if output_final_state else None
+    if workspace is None:
+        workspace = alloc_workspace(B, T, H, dk, dv, chunk, _io_of(q), q.device)
+    kla_chunk_fwd(q, k, v, g, eta, eps, h0, o, hT, workspace, chunk, stream)
+    return o, hT
+
+
+def decode_step(q, k, v, g, eta, S, eps=1e-6, stream=None):
+    """Run kla_decode_step; S is updated in place.  Returns o."""
+    o = torch.empty(v.shape, dtype=q.dtype, device=q.device)
+    kla_decode_step(q, k, v, g, eta, eps, S, o, stream)
+    return o
+
+
+__all__ = [
+    "kla_chunk_fwd_workspace_bytes", "kla_chunk_fwd", "kla_decode_step", "kla_workspace_check",
+    "kla_status_string", "chunk_fwd", "decode_step", "alloc_workspace", "load_library",
+    "KlaError", "EXPORTED_SYMBOLS", "KLA_IO_BF16", "KLA_IO_FP32",
+]

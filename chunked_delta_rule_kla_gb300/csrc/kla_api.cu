@@ -1,0 +1,115 @@
+// C ABI of libkla (declared in include/kla.h): argument validation, workspace
+// sizing, dispatch to the kernels.  No device memory is allocated here.
+#include "kla.h"
+#include "kla_internal.cuh"
+
+#include <cstdint>
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dim_ok(int d) { return d == 64 || d == 128; }
+
+kla_status check_io(kla_io_dtype io) {
+    return (io == KLA_IO_BF16 || io == KLA_IO_FP32) ? KLA_OK : KLA_ERR_INVALID_ARG;
+}
+
+kla_status to_status(cudaError_t e) { return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA; }
+
+// Problems are addressed with 64-bit offsets, but each dimension must fit the
+// launch grid and the total element counts must fit in int64.
+bool sizes_fit(int B, int T, int H, int dk, int dv) {
+    if (B > 65535 || H > 65535) return false;
+    const int64_t toks = (int64_t)B * T * H;
+    return toks <= (int64_t(1) << 46) / (dk > dv ? dk : dv);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kla_status_string(kla_status s) {
+    switch (s) {
+        case KLA_OK: return "KLA_OK";
+        case KLA_ERR_INVALID_ARG: return "KLA_ERR_INVALID_ARG";
+        case KLA_ERR_UNSUPPORTED: return "KLA_ERR_UNSUPPORTED";
+        case KLA_ERR_WORKSPACE: return "KLA_ERR_WORKSPACE";
+        case KLA_ERR_CUDA: return "KLA_ERR_CUDA";
+        case KLA_ERR_DEVICE_TIMEOUT: return "KLA_ERR_DEVICE_TIMEOUT";
+    }
+    return "KLA_ERR_UNKNOWN";
+}
+
+size_t kla_chunk_fwd_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk,
+                                     kla_io_dtype io) {
+    if (B < 0 || T < 0 || H < 0 || check_io(io) != KLA_OK) return 0;
+    if (!dim_ok(dk) || !dim_ok(dv) || chunk != 64) return 0;
+    if (!sizes_fit(B, T, H, dk, dv)) return 0;
+    return kla::kErrorRecordBytes;
+}
+
+kla_status kla_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* eta, float eps, const float* h0, void* o, float* hT,
+                         int B, int T, int H, int dk, int dv, int chunk, kla_io_dtype io,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+    if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || chunk <= 0) return KLA_ERR_INVALID_ARG;
+    if (check_io(io) != KLA_OK) return KLA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f)) return KLA_ERR_INVALID_ARG;  // also rejects NaN
+    if (!dim_ok(dk) || !dim_ok(dv) || chunk != 64) return KLA_ERR_UNSUPPORTED;
+    if (!sizes_fit(B, T, H, dk, dv)) return KLA_ERR_UNSUPPORTED;
+    const bool have_tokens = (int64_t)B * H * T > 0;
+    if (have_tokens && (!q || !k || !v || !g || !eta || !o)) return KLA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, eta, h0, o, hT};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return KLA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kla::kErrorRecordBytes) return KLA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KLA_ERR_WORKSPACE;
+    if ((int64_t)B * H == 0) return KLA_OK;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, kla::kErrorRecordBytes, st);
+    if (e != cudaSuccess) return KLA_ERR_CUDA;
+    if (T == 0) {
+        if (!hT) return KLA_OK;
+        const size_t bytes = sizeof(float) * (size_t)B * H * dk * dv;
+        if (h0) {
+            if (h0 == hT) return KLA_OK;
+            return to_status(cudaMemcpyAsync(hT, h0, bytes, cudaMemcpyDeviceToDevice, st));
+        }
+        return to_status(cudaMemsetAsync(hT, 0, bytes, st));
+    }
+    const bool bf16 = io == KLA_IO_BF16;
+    return to_status(kla::launch_chunk_fwd_simt(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dk,
+                                                dv, bf16, st));
+}
+
+kla_status kla_decode_step(const void* q, const void* k, const void* v, const float* g,
+                           const float* eta, float eps, float* S, void* o, int B, int H, int dk,
+                           int dv, kla_io_dtype io, void* stream) {
+    if (B < 0 || H < 0 || dk <= 0 || dv <= 0) return KLA_ERR_INVALID_ARG;
+    if (check_io(io) != KLA_OK) return KLA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f)) return KLA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return KLA_ERR_UNSUPPORTED;
+    if (B > 65535 || H > 65535) return KLA_ERR_UNSUPPORTED;
+    if ((int64_t)B * H == 0) return KLA_OK;
+    if (!q || !k || !v || !g || !eta || !S || !o) return KLA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, eta, S, o};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KLA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return to_status(kla::launch_decode_step(q, k, v, g, eta, eps, S, o, B, H, dk, dv,
+                                             io == KLA_IO_BF16, st));
+}
+
+kla_status kla_workspace_check(const void* workspace, size_t workspace_bytes, void* stream) {
+    if (!workspace || workspace_bytes < kla::kErrorRecordBytes) return KLA_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return KLA_ERR_CUDA;
+    kla::DeviceErrorRecord rec;
+    if (cudaMemcpy(&rec, workspace, sizeof(rec), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return KLA_ERR_CUDA;
+    return rec.code != 0 ? KLA_ERR_DEVICE_TIMEOUT : KLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// Internal declarations shared by the CUDA translation units of libkla.
+// Nothing here is part of the public C ABI (include/kla.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace kla {
+
+// First 256 bytes of every kla_chunk_fwd workspace: the device error record.
+// A kernel whose bounded wait gives up writes code != 0 (first writer wins)
+// and returns; the host reads the record in kla_workspace_check.
+struct DeviceErrorRecord {
+    unsigned int code;    // 0 = no error, 1 = bounded wait timed out
+    unsigned int where;   // kernel-specific site id of the wait
+    unsigned int block;   // linear CTA index that gave up
+    unsigned int detail;  // kernel-specific (e.g. the chunk index)
+    unsigned int pad[60];
+};
+static_assert(sizeof(DeviceErrorRecord) == 256, "error record is 256 bytes");
+
+constexpr size_t kErrorRecordBytes = 256;
+
+__device__ __forceinline__ void record_error(DeviceErrorRecord* rec, unsigned where,
+                                             unsigned detail) {
+    if (rec == nullptr) return;
+    if (atomicCAS(&rec->code, 0u, 1u) == 0u) {
+        rec->where = where;
+        rec->block = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+        rec->detail = detail;
+    }
+}
+
+// ---- launchers (each returns the cudaError_t of its launch) --------------
+
+// Decode step, fp32 math, S read once and written once (kla_decode.cu).
+cudaError_t launch_decode_step(const void* q, const void* k, const void* v, const float* g,
+                               const float* eta, float eps, float* S, void* o, int B, int H,
+                               int dk, int dv, bool bf16, cudaStream_t stream);
+
+// Chunkwise prefill on CUDA cores in fp32 (kla_chunk_simt.cu).  Any T >= 1,
+// dk, dv in {64,128}, chunk 64.
+cudaError_t launch_chunk_fwd_simt(const void* q, const void* k, const void* v, const float* g,
+                                  const float* eta, float eps, const float* h0, void* o,
+                                  float* hT, int B, int T, int H, int dk, int dv, bool bf16,
+                                  cudaStream_t stream);
+
+}  // namespace kla

@@ -1,0 +1,135 @@
+/*
+ * kla.h -- C ABI of the Kaczmarz Linear Attention (KLA) GPU library
+ * (libkla.so, sm_103a).
+ *
+ * The operation is the gated delta rule with the Kaczmarz step size from
+ * "KLA: Kaczmarz Linear Attention" (gist.science/ko/paper/2605.08587),
+ * section "KLA update rule", for every (batch b, head h) independently:
+ *
+ *   a_t    = exp(g_t)                        decay gate, g_t <= 0 a log-decay
+ *   beta_t = eta_t / (||k_t||_2^2 + eps)     Kaczmarz coefficient
+ *   S~     = a_t S_{t-1}
+ *   e_t    = v_t - S~^T k_t                  residual
+ *   S_t    = S~ + beta_t k_t e_t^T           state, d_k x d_v (section
+ *                                            "Implementation": GDN state shape)
+ *   o_t    = S_t^T q_t                       readout after the update
+ *
+ * q and k are used as given: no 1/sqrt(d_k) scaling and no normalisation.
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers into caller-owned memory.  The
+ *    library allocates no device memory, keeps no state between calls and
+ *    never synchronises the stream; every call is asynchronous on `stream`
+ *    (a cudaStream_t passed as void*, NULL = the legacy default stream).
+ *  - Tensors are contiguous and row-major.  Token-major layouts:
+ *      q, k : [B, T, H, dk]    v, o : [B, T, H, dv]    g, eta : [B, T, H]
+ *      h0, hT, S : [B, H, dk, dv]
+ *    q, k, v, o use the I/O dtype (`io`); g, eta and every state are fp32.
+ *  - Pointers must be aligned to 16 bytes.
+ *  - Argument and shape errors are reported synchronously, before any work is
+ *    enqueued.  A failed launch returns KLA_ERR_CUDA.  Device-side bounded
+ *    waits record a timeout in the workspace; kla_workspace_check reads it.
+ *  - Calls are thread-safe.  Outputs must not alias inputs (o with q/k/v,
+ *    hT with h0 is allowed only when they are the same pointer).
+ */
+#ifndef KLA_H_
+#define KLA_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define KLA_API __attribute__((visibility("default")))
+#else
+#define KLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kla_status {
+    KLA_OK = 0,
+    KLA_ERR_INVALID_ARG = 1,    /* null pointer, negative size, bad enum, misalignment */
+    KLA_ERR_UNSUPPORTED = 2,    /* well-formed but not implemented (dk, dv, chunk) */
+    KLA_ERR_WORKSPACE = 3,      /* workspace missing or smaller than required */
+    KLA_ERR_CUDA = 4,           /* a CUDA runtime call or kernel launch failed */
+    KLA_ERR_DEVICE_TIMEOUT = 5  /* a bounded device-side wait gave up */
+} kla_status;
+
+typedef enum kla_io_dtype {
+    KLA_IO_BF16 = 0,            /* q, k, v, o in bfloat16 */
+    KLA_IO_FP32 = 1             /* q, k, v, o in float32 */
+} kla_io_dtype;
+
+/*
+ * Bytes of device workspace kla_chunk_fwd needs for this problem (always at
+ * least 256: the first 256 bytes hold the device error record).  Returns 0 if
+ * the arguments are invalid or unsupported.
+ */
+KLA_API size_t kla_chunk_fwd_workspace_bytes(int B, int T, int H, int dk, int dv,
+                                     int chunk, kla_io_dtype io);
+
+/*
+ * Chunkwise-parallel prefill: runs the recurrence above over T tokens for all
+ * B*H heads and writes every o_t and (optionally) the final state.
+ *
+ * The chunkwise form follows the page's section "Implementation": the GDN
+ * chunkwise-parallel algorithm is kept and only the diagonal coefficient
+ * matrix B = Diag(beta_1..beta_C) inside the chunk solver changes.  Per chunk
+ * of C tokens the library forms beta and the decay cumsum, the WY/UT
+ * transform (I + tril(diag(beta) K K^T, -1) with decay)^{-1}, the masked
+ * intra-chunk Q K^T, and carries the fp32 state across chunks.
+ *
+ *  q, k, v : inputs, I/O dtype, shapes above.
+ *  g, eta  : fp32 [B, T, H]; g is the log-decay (a_t = exp(g_t)).
+ *  eps     : added to ||k_t||^2 in the denominator of beta.  With eps = 0 a
+ *            zero key gives 0/0 (a non-finite result); the data is not checked.
+ *  h0      : fp32 [B, H, dk, dv] initial state, or NULL for zeros.
+ *  o       : output [B, T, H, dv], I/O dtype.
+ *  hT      : fp32 [B, H, dk, dv] final state, or NULL to skip.
+ *  chunk   : chunk length C; 64 is supported for every shape.
+ *  dk, dv  : 64 or 128 each.
+ *  workspace, workspace_bytes : device scratch of at least
+ *            kla_chunk_fwd_workspace_bytes(...) bytes, 256-byte aligned,
+ *            owned by the caller, not shared by calls that run concurrently.
+ *  T = 0 is valid: o is empty and hT receives h0 (or zeros).
+ */
+KLA_API kla_status kla_chunk_fwd(const void* q, const void* k, const void* v,
+                         const float* g, const float* eta, float eps,
+                         const float* h0, void* o, float* hT,
+                         int B, int T, int H, int dk, int dv, int chunk,
+                         kla_io_dtype io, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/*
+ * One recurrent decode step for B*H heads (the same recurrence with T = 1;
+ * the page's section "Efficiency" reports decode throughput for this step).
+ * The state is read once and written once, in place.
+ *
+ *  q, k : [B, H, dk] I/O dtype;  v, o : [B, H, dv] I/O dtype
+ *  g, eta : fp32 [B, H]
+ *  S : fp32 [B, H, dk, dv], read as S_{t-1} and overwritten with S_t.
+ *      S must not overlap any other argument.
+ *  dk, dv : 64 or 128 each.
+ */
+KLA_API kla_status kla_decode_step(const void* q, const void* k, const void* v,
+                           const float* g, const float* eta, float eps,
+                           float* S, void* o, int B, int H, int dk, int dv,
+                           kla_io_dtype io, void* stream);
+
+/*
+ * Synchronises `stream` and reads the device error record in `workspace`.
+ * Returns KLA_ERR_DEVICE_TIMEOUT if a bounded device wait gave up during an
+ * earlier kla_chunk_fwd on this workspace, KLA_OK otherwise.
+ */
+KLA_API kla_status kla_workspace_check(const void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* Static, human-readable name of a status code. */
+KLA_API const char* kla_status_string(kla_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KLA_H_ */

@@ -1,0 +1,134 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments with a status code before any
+CUDA call (so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunked_delta_rule_kla_gb300 as kla
+from chunked_delta_rule_kla_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return kla.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"KLA_API\s+[\w\s\*]*?\b(kla_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(kla.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    names = {0: "KLA_OK", 1: "KLA_ERR_INVALID_ARG", 2: "KLA_ERR_UNSUPPORTED",
+             3: "KLA_ERR_WORKSPACE", 4: "KLA_ERR_CUDA", 5: "KLA_ERR_DEVICE_TIMEOUT"}
+    for code, name in names.items():
+        assert kla.kla_status_string(code) == name
+    assert kla.kla_status_string(99) == "KLA_ERR_UNKNOWN"
+
+
+def test_workspace_bytes(lib):
+    n = lib.kla_chunk_fwd_workspace_bytes(8, 4096, 8, 128, 128, 64, kla.KLA_IO_BF16)
+    assert n >= 256 and n % 256 == 0
+    assert lib.kla_chunk_fwd_workspace_bytes(1, 1, 1, 128, 128, 64, kla.KLA_IO_FP32) >= 256
+    assert lib.kla_chunk_fwd_workspace_bytes(1, 0, 1, 64, 64, 64, kla.KLA_IO_FP32) >= 256
+    assert lib.kla_chunk_fwd_workspace_bytes(1, 16, 1, 96, 128, 64, 0) == 0   # dk unsupported
+    assert lib.kla_chunk_fwd_workspace_bytes(1, 16, 1, 128, 128, 32, 0) == 0  # chunk unsupported
+    assert lib.kla_chunk_fwd_workspace_bytes(-1, 16, 1, 128, 128, 64, 0) == 0
+    assert lib.kla_chunk_fwd_workspace_bytes(1, 16, 1, 128, 128, 64, 7) == 0  # bad io enum
+
+
+# Fake, 256-byte aligned, never dereferenced "device" addresses: every call
+# below must fail validation before touching them.
+P = 0x10000000
+WS = 0x20000000
+
+
+def _fwd(lib, **kw):
+    a = dict(q=P, k=P, v=P, g=P, eta=P, eps=1e-6, h0=None, o=P, hT=None, B=1, T=64, H=1,
+             dk=128, dv=128, chunk=64, io=kla.KLA_IO_BF16, ws=WS, wsb=256, stream=None)
+    a.update(kw)
+    return lib.kla_chunk_fwd(a["q"], a["k"], a["v"], a["g"], a["eta"], a["eps"], a["h0"], a["o"],
+                             a["hT"], a["B"], a["T"], a["H"], a["dk"], a["dv"], a["chunk"],
+                             a["io"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), kla.KLA_ERR_INVALID_ARG),
+    (dict(k=None), kla.KLA_ERR_INVALID_ARG),
+    (dict(v=None), kla.KLA_ERR_INVALID_ARG),
+    (dict(g=None), kla.KLA_ERR_INVALID_ARG),
+    (dict(eta=None), kla.KLA_ERR_INVALID_ARG),
+    (dict(o=None), kla.KLA_ERR_INVALID_ARG),
+    (dict(B=-1), kla.KLA_ERR_INVALID_ARG),
+    (dict(T=-5), kla.KLA_ERR_INVALID_ARG),
+    (dict(io=3), kla.KLA_ERR_INVALID_ARG),
+    (dict(eps=-1.0), kla.KLA_ERR_INVALID_ARG),
+    (dict(eps=float("nan")), kla.KLA_ERR_INVALID_ARG),
+    (dict(q=P + 4), kla.KLA_ERR_INVALID_ARG),            # misaligned
+    (dict(dk=96), kla.KLA_ERR_UNSUPPORTED),
+    (dict(dv=256), kla.KLA_ERR_UNSUPPORTED),
+    (dict(chunk=32), kla.KLA_ERR_UNSUPPORTED),
+    (dict(H=70000), kla.KLA_ERR_UNSUPPORTED),
+    (dict(ws=None), kla.KLA_ERR_WORKSPACE),
+    (dict(wsb=128), kla.KLA_ERR_WORKSPACE),
+    (dict(ws=WS + 16), kla.KLA_ERR_WORKSPACE),
+])
+def test_chunk_fwd_rejects(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+
+
+def _dec(lib, **kw):
+    a = dict(q=P, k=P, v=P, g=P, eta=P, eps=1e-6, S=P, o=P, B=2, H=2, dk=128, dv=128,
+             io=kla.KLA_IO_BF16, stream=None)
+    a.update(kw)
+    return lib.kla_decode_step(a["q"], a["k"], a["v"], a["g"], a["eta"], a["eps"], a["S"],
+                               a["o"], a["B"], a["H"], a["dk"], a["dv"], a["io"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(S=None), kla.KLA_ERR_INVALID_ARG),
+    (dict(o=None), kla.KLA_ERR_INVALID_ARG),
+    (dict(q=None), kla.KLA_ERR_INVALID_ARG),
+    (dict(H=-1), kla.KLA_ERR_INVALID_ARG),
+    (dict(io=9), kla.KLA_ERR_INVALID_ARG),
+    (dict(S=P + 8), kla.KLA_ERR_INVALID_ARG),
+    (dict(eps=-0.5), kla.KLA_ERR_INVALID_ARG),
+    (dict(dk=32), kla.KLA_ERR_UNSUPPORTED),
+    (dict(dv=100), kla.KLA_ERR_UNSUPPORTED),
+])
+def test_decode_rejects(lib, kw, code):
+    assert _dec(lib, **kw) == code
+
+
+def test_empty_problems_are_no_ops(lib):
+    # B*H == 0: nothing to do, no CUDA call, OK even with null tensors.
+    assert _fwd(lib, B=0, q=None, k=None, v=None, g=None, eta=None, o=None) == kla.KLA_OK
+    assert _dec(lib, H=0, q=None, k=None, v=None, g=None, eta=None, S=None, o=None) == kla.KLA_OK
+
+
+def test_workspace_check_rejects_small(lib):
+    assert lib.kla_workspace_check(None, 256, None) == kla.KLA_ERR_WORKSPACE
+    assert lib.kla_workspace_check(WS, 16, None) == kla.KLA_ERR_WORKSPACE
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import importlib
+    mod = importlib.import_module("chunked_delta_rule_kla_gb300")
+    monkeypatch.setattr(mod, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        mod.load_library(str(tmp_path / "missing.so"))
