@@ -8,6 +8,7 @@
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 bool dim_ok(int d) { return d == 64 || d == 128; }
 
@@ -60,9 +61,10 @@ kla_status kla_chunk_fwd(const void* q, const void* k, const void* v, const floa
     if (!sizes_fit(B, T, H, dk, dv)) return KLA_ERR_UNSUPPORTED;
     const bool have_tokens = (int64_t)B * H * T > 0;
     if (have_tokens && (!q || !k || !v || !g || !eta || !o)) return KLA_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, g, eta, h0, o, hT};
+    const void* ptrs[] = {q, k, v, h0, o, hT};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return KLA_ERR_INVALID_ARG;
+    if ((g && !aligned4(g)) || (eta && !aligned4(eta))) return KLA_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < kla::kErrorRecordBytes) return KLA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KLA_ERR_WORKSPACE;
     if ((int64_t)B * H == 0) return KLA_OK;
@@ -94,9 +96,10 @@ kla_status kla_decode_step(const void* q, const void* k, const void* v, const fl
     if (B > 65535 || H > 65535) return KLA_ERR_UNSUPPORTED;
     if ((int64_t)B * H == 0) return KLA_OK;
     if (!q || !k || !v || !g || !eta || !S || !o) return KLA_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, g, eta, S, o};
+    const void* ptrs[] = {q, k, v, S, o};
     for (const void* p : ptrs)
         if (!aligned16(p)) return KLA_ERR_INVALID_ARG;
+    if (!aligned4(g) || !aligned4(eta)) return KLA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     return to_status(kla::launch_decode_step(q, k, v, g, eta, eps, S, o, B, H, dk, dv,
                                              io == KLA_IO_BF16, st));

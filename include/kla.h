@@ -25,7 +25,8 @@
  *      q, k : [B, T, H, dk]    v, o : [B, T, H, dv]    g, eta : [B, T, H]
  *      h0, hT, S : [B, H, dk, dv]
  *    q, k, v, o use the I/O dtype (`io`); g, eta and every state are fp32.
- *  - Pointers must be aligned to 16 bytes.
+ *  - q, k, v, o and the fp32 states must be aligned to 16 bytes; g and eta
+ *    to 4 bytes.
  *  - Argument and shape errors are reported synchronously, before any work is
  *    enqueued.  A failed launch returns KLA_ERR_CUDA.  Device-side bounded
  *    waits record a timeout in the workspace; kla_workspace_check reads it.

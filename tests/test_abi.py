@@ -80,6 +80,7 @@ def _fwd(lib, **kw):
     (dict(eps=-1.0), kla.KLA_ERR_INVALID_ARG),
     (dict(eps=float("nan")), kla.KLA_ERR_INVALID_ARG),
     (dict(q=P + 4), kla.KLA_ERR_INVALID_ARG),            # misaligned
+    (dict(g=P + 2), kla.KLA_ERR_INVALID_ARG),
     (dict(dk=96), kla.KLA_ERR_UNSUPPORTED),
     (dict(dv=256), kla.KLA_ERR_UNSUPPORTED),
     (dict(chunk=32), kla.KLA_ERR_UNSUPPORTED),
