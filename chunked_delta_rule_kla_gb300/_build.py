@@ -22,6 +22,7 @@ SOURCES = [
     "kla_api.cu",
     "kla_decode.cu",
     "kla_chunk_simt.cu",
+    "kla_chunk_tc.cu",
 ]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

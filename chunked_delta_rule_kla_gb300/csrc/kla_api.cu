@@ -81,9 +81,13 @@ kla_status kla_chunk_fwd(const void* q, const void* k, const void* v, const floa
         }
         return to_status(cudaMemsetAsync(hT, 0, bytes, st));
     }
-    const bool bf16 = io == KLA_IO_BF16;
+    if (io == KLA_IO_BF16) {
+        auto* rec = reinterpret_cast<kla::DeviceErrorRecord*>(workspace);
+        return to_status(kla::launch_chunk_fwd_tc(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dk, dv,
+                                                  rec, st));
+    }
     return to_status(kla::launch_chunk_fwd_simt(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dk,
-                                                dv, bf16, st));
+                                                dv, false, st));
 }
 
 kla_status kla_decode_step(const void* q, const void* k, const void* v, const float* g,
