@@ -2,7 +2,7 @@
 //
 // One CTA owns one (b, h) head and a 64-column slice of its d_k x d_v state,
 // and walks the head's chunks of C = 64 tokens in order, carrying the fp32
-// state on chip.  Per chunk (local inclusive log-decay cumsum gam_r,
+// state in TMEM.  Per chunk (local inclusive log-decay cumsum gam_r,
 // Gam_r = exp(gam_r), start state S0; "KLA: Kaczmarz Linear Attention",
 // section "Implementation": the GDN chunk solver with B = Diag(beta)):
 //
@@ -15,19 +15,28 @@
 //   QS = Q S0,  O = diag(Gam) QS + P W           tcgen05, M=64
 //   S1 = Gam_C S0 + K^T diag(exp(gam_C - gam_r)) W   tcgen05, M=dk
 //
-// Roles: warp 0 lane 0 issues TMA loads of K, Q and the V slice (two
-// stages); warp 1 owns TMEM and its lane 0 issues every tcgen05.mma; warps
-// 2..5 (the compute warpgroup, 128 threads) do everything that is not a
-// dense contraction: beta, the decay cumsum, the masked P, the triangular
-// inverse, TMEM -> bf16 operand conversions, the fp32 state update (the
-// master state lives in registers, one state row per thread) and the output
-// epilogue.  Every mbarrier wait is bounded; on timeout the CTA records the
-// error in the workspace, stops issuing work and exits.
+// Roles (10 warps):
+//   warp 0      lane 0 issues TMA loads of K, Q and the V slice (2 stages);
+//   warp 1      owns TMEM; lane 0 issues every tcgen05.mma;
+//   warps 2..5  carry warpgroup: TMEM -> bf16 operand tiles for Wk and W,
+//               the fp32 state update (master state in TMEM) and the output
+//               epilogue of chunk c;
+//   warps 6..9  prep warpgroup: beta, the decay cumsum, masked A and P, the
+//               triangular inverse and the T diag(beta), T diag(beta Gam)
+//               operand tiles of chunk c+1, overlapping the carry of chunk c.
+// Every mbarrier wait is bounded; on timeout the CTA records the error in the
+// workspace, stops issuing work and exits.  Decisions that follow a wait are
+// made uniform across each warpgroup with a barrier-reduction.
 //
-// The triangular inverse: the four 16x16 diagonal blocks by forward
-// substitution (fp32, one column per thread), then the off-diagonal blocks
-// by block-column recurrence T_IJ = -T_II sum_{J<=M<I} A_IM T_MJ with
-// warp-level tf32 mma.sync (16x16 blocks are below tcgen05's minimum M).
+// Decay factors: exp(gam_r - gam_s) = u_r w_s with u_r = exp(gam_r - gam_m),
+// w_s = exp(gam_m - gam_s) for the chunk's middle token m, when the chunk's
+// total decay span gam_0 - gam_63 is at most 80 (no fp32 overflow); otherwise
+// each factor is computed as one exponential.
+//
+// The triangular inverse: the four 16x16 diagonal blocks by right-looking
+// substitution (fp32, one column per thread), then the off-diagonal blocks by
+// block-column recurrence T_IJ = -T_II sum_{J<=M<I} A_IM T_MJ with warp-level
+// tf32 mma.sync (16x16 blocks are below tcgen05's minimum M).
 #include "kla_internal.cuh"
 #include "tc_common.cuh"
 
@@ -42,44 +51,55 @@ using namespace kla::tc;
 
 constexpr int C = 64;          // chunk length
 constexpr int DVS = 64;        // state columns per CTA
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kThreads = 320;  // 10 warps
 constexpr int kStages = 2;
-constexpr int LDF = 68;        // fp32 row stride of A / T / scratch (bank-conflict free for mma fragments)
+constexpr int LDF = 68;        // fp32 row stride of A / T / scratch (conflict-free mma fragments)
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s per wait
+constexpr uint32_t kSuspendNs = 100000;          // try_wait suspension hint
+constexpr float kSpanMax = 80.f;                 // largest decay span factorised
 
-// TMEM column map (512 columns allocated)
+// TMEM column map (512 columns)
 constexpr uint32_t TM_GQ = 0;     // M=128 N=64: rows 0..63 K K^T, 64..127 Q K^T
 constexpr uint32_t TM_W = 64;     // M=64 N=64: U, then W
 constexpr uint32_t TM_WK = 128;   // M=64 N=dk
 constexpr uint32_t TM_QS = 256;   // M=64 N=64
 constexpr uint32_t TM_PW = 320;   // M=64 N=64
-constexpr uint32_t TM_S = 384;    // M=dk N=64
+constexpr uint32_t TM_S = 384;    // M=dk N=64: K^T Wt
+constexpr uint32_t TM_SM = 448;   // M=dk N=64: fp32 master state
 constexpr uint32_t kTmemCols = 512;
 
 enum : unsigned { kWhereFull = 1, kWhereEmpty, kWhereGQ, kWhereT, kWhereWK, kWhereWKR, kWhereSR,
-                  kWhereW, kWhereWR, kWhereS };
+                  kWhereW, kWhereWR, kWhereS, kWhereDrain };
+
+// Per-chunk scalars written by the prep warpgroup, double-buffered by chunk
+// parity.
+struct ChunkScalars {
+    float gam[C];   // inclusive cumsum of g
+    float bet[C];   // beta (0 past T)
+    float betg[C];  // beta * Gam
+    float w[C];     // decay factor w_s (factorised mode)
+};
 
 template <int DK>
 struct Layout {
-    static constexpr int KB = DK / 64;                 // 64-wide boxes along d_k
-    static constexpr uint32_t kStageBytes = (2 * KB + 1) * 8192;  // [K0 Q0 (K1 Q1)] V
+    static constexpr int KB = DK / 64;                             // 64-wide boxes along d_k
+    static constexpr uint32_t kStageBytes = (2 * KB + 1) * 8192;   // [K0 Q0 (K1 Q1)] V
     static constexpr uint32_t kStage0 = 0;
-    static constexpr uint32_t kP = kStages * kStageBytes;
-    static constexpr uint32_t kTb = kP + 8192;
+    static constexpr uint32_t kP = kStages * kStageBytes;          // 2 x 8 KB (chunk parity)
+    static constexpr uint32_t kTb = kP + 2 * 8192;
     static constexpr uint32_t kTg = kTb + 8192;
-    static constexpr uint32_t kWk = kTg + 8192;              // KB boxes
+    static constexpr uint32_t kWk = kTg + 8192;                    // KB boxes
     static constexpr uint32_t kWb = kWk + KB * 8192;
     static constexpr uint32_t kWt = kWb + 8192;
-    static constexpr uint32_t kSb = kWt + 8192;              // [DK][64] bf16
-    static constexpr uint32_t kAf = kSb + DK * 128;          // fp32 [64][LDF]
-    static constexpr uint32_t kTf = kAf + C * LDF * 4;       // fp32 [64][LDF]
-    static constexpr uint32_t kRw = kTf + C * LDF * 4;       // fp32 4 x [16][LDF]
-    static constexpr uint32_t kGam = kRw + 4 * 16 * LDF * 4; // fp32 [64]
-    static constexpr uint32_t kBeta = kGam + 256;
-    static constexpr uint32_t kMisc = kBeta + 256;           // scan totals, flags
-    static constexpr uint32_t kBars = kMisc + 64;            // mbarriers
+    static constexpr uint32_t kSb = kWt + 8192;                    // [DK][64] bf16
+    static constexpr uint32_t kAf = kSb + DK * 128;                // fp32 [64][LDF]
+    static constexpr uint32_t kTf = kAf + C * LDF * 4;             // fp32 [64][LDF]
+    static constexpr uint32_t kRw = kTf + C * LDF * 4;             // fp32 3 x [16][LDF]
+    static constexpr uint32_t kScal = kRw + 3 * 16 * LDF * 4;      // 2 x ChunkScalars
+    static constexpr uint32_t kMisc = kScal + 2 * sizeof(ChunkScalars);
+    static constexpr uint32_t kBars = kMisc + 64;
     static constexpr uint32_t kEnd = kBars + 32 * 8;
-    static constexpr size_t kSmemBytes = kEnd + 1024;        // + alignment slack
+    static constexpr size_t kSmemBytes = kEnd + 1024;              // + alignment slack
 };
 
 struct Params {
@@ -93,21 +113,22 @@ struct Params {
     int T, H, dv;
 };
 
-// mbarrier slots
+// mbarrier slots (all with arrival count 1)
 enum { B_FULL0 = 0, B_EMPTY0 = B_FULL0 + kStages, B_GQ = B_EMPTY0 + kStages, B_T, B_WK, B_WKR,
        B_SR, B_W, B_WR, B_S, B_DRAIN, B_COUNT };
 
-__device__ __forceinline__ void named_sync_compute() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ void named_sync_rows() { asm volatile("bar.sync 2, 64;" ::: "memory"); }
-// Barrier over the compute warpgroup that also ORs a predicate across it, so
-// that every compute thread takes the same branch afterwards.
-__device__ __forceinline__ bool named_sync_or(bool pred) {
+// Named barriers: 1/2 carry warpgroup (sync / or-reduction), 3/4 prep
+// warpgroup, 5 the two prep warps holding rows 0..63.
+__device__ __forceinline__ void bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 3, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)pred)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
         : "memory");
     return r != 0;
 }
@@ -145,19 +166,19 @@ __device__ __forceinline__ void warp_store16(float* D, const float (&d)[2][4], f
     const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-        D[gq * LDF + nt * 8 + 2 * tq] = scale * d[nt][0];
-        D[gq * LDF + nt * 8 + 2 * tq + 1] = scale * d[nt][1];
-        D[(gq + 8) * LDF + nt * 8 + 2 * tq] = scale * d[nt][2];
-        D[(gq + 8) * LDF + nt * 8 + 2 * tq + 1] = scale * d[nt][3];
+        *reinterpret_cast<float2*>(&D[gq * LDF + nt * 8 + 2 * tq]) =
+            make_float2(scale * d[nt][0], scale * d[nt][1]);
+        *reinterpret_cast<float2*>(&D[(gq + 8) * LDF + nt * 8 + 2 * tq]) =
+            make_float2(scale * d[nt][2], scale * d[nt][3]);
     }
 }
 
-// Store 8 consecutive bf16 (one 16-byte chunk) of row `row`, columns
-// [col8*8, col8*8+8) of a swizzled [rows][64] tile.
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&p);
 }
+// Store 8 consecutive bf16 (one 16-byte chunk) of row `row`, columns
+// [col8*8, col8*8+8) of a swizzled [rows][64] tile.
 __device__ __forceinline__ void st_chunk8(uint8_t* tile, int row, int col8, float v0, float v1,
                                           float v2, float v3, float v4, float v5, float v6,
                                           float v7) {
@@ -168,7 +189,7 @@ __device__ __forceinline__ void st_chunk8(uint8_t* tile, int row, int col8, floa
     pk.w = pack2(v6, v7);
     *reinterpret_cast<uint4*>(tile + sw128_offset(row, col8 * 8)) = pk;
 }
-#define ST_CHUNK(tile, row, col8, a, o) \
+#define ST_CHUNK(tile, row, col8, a, o)                                                         \
     st_chunk8(tile, row, col8, (a)[(o)], (a)[(o) + 1], (a)[(o) + 2], (a)[(o) + 3], (a)[(o) + 4], \
               (a)[(o) + 5], (a)[(o) + 6], (a)[(o) + 7])
 
@@ -181,14 +202,10 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBars);
-    float* gam = reinterpret_cast<float*>(sm + L::kGam);
-    float* bet = reinterpret_cast<float*>(sm + L::kBeta);
+    ChunkScalars* scal = reinterpret_cast<ChunkScalars*>(sm + L::kScal);
     float* misc = reinterpret_cast<float*>(sm + L::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 32);
     uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(sm + L::kMisc + 48);
-    float* Af = reinterpret_cast<float*>(sm + L::kAf);
-    float* Tf = reinterpret_cast<float*>(sm + L::kTf);
-    float* Rw = reinterpret_cast<float*>(sm + L::kRw);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int slice = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -215,18 +232,31 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         record_error(p.err, where, (unsigned)c);
         *abort_flag = 1;
     };
-    auto wait = [&](int slot, uint32_t parity, unsigned where, int c) -> bool {
+    // Single-thread bounded wait (TMA and MMA roles).
+    auto wait1 = [&](int slot, uint32_t parity, unsigned where, int c) -> bool {
         if (*abort_flag) return false;
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(&bars[slot], parity)) {
+        while (!mbar_try_wait_sleep(&bars[slot], parity, kSuspendNs)) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > kTimeoutNs) { fail(where, c); return false; }
         }
         return true;
     };
+    // Warpgroup bounded wait with a uniform outcome (barrier-reduction `bid`).
+    auto waitg = [&](int slot, uint32_t parity, unsigned where, int c, int bid) -> bool {
+        bool bad = *abort_flag != 0;
+        if (!bad) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait_sleep(&bars[slot], parity, kSuspendNs)) {
+                if (*abort_flag) { bad = true; break; }
+                if (globaltimer_ns() - t0 > kTimeoutNs) { fail(where, c); bad = true; break; }
+            }
+        }
+        return !bar_or(bid, 128, bad);
+    };
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+        // ================================================================ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
@@ -234,7 +264,7 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             int issued = 0;
             for (int c = 0; c < nchunks; ++c) {
                 const int s = c % kStages;
-                if (c >= kStages && !wait(B_EMPTY0 + s, ((c / kStages) - 1) & 1, kWhereEmpty, c)) break;
+                if (c >= kStages && !wait1(B_EMPTY0 + s, ((c / kStages) - 1) & 1, kWhereEmpty, c)) break;
                 uint8_t* st = sm + L::kStage0 + s * L::kStageBytes;
                 uint64_t* full = &bars[B_FULL0 + s];
                 mbar_arrive_expect_tx(full, L::kStageBytes);
@@ -247,17 +277,16 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 tma_load_4d(st + KB * 16384, &tm_v, full, j0, h, t0, b);
                 issued = c + 1;
             }
-            // drain: every issued load must land before the CTA may exit
+            // every issued load must land before the CTA may exit
             for (int c = (issued > kStages ? issued - kStages : 0); c < issued; ++c) {
-                const int s = c % kStages;
                 const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(&bars[B_FULL0 + s], (c / kStages) & 1)) {
+                while (!mbar_try_wait_sleep(&bars[B_FULL0 + c % kStages], (c / kStages) & 1, kSuspendNs)) {
                     if (globaltimer_ns() - t0 > kTimeoutNs) { fail(kWhereFull, c); break; }
                 }
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ================================================================ MMA issuer
         if (lane == 0) {
             const uint32_t st0 = smem_u32(sm + L::kStage0);
             const uint32_t sP = smem_u32(sm + L::kP), sTb = smem_u32(sm + L::kTb),
@@ -273,7 +302,7 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             constexpr uint32_t id_pw = idesc_bf16(64, 64, false, true);
             auto issue_gq = [&](int c) -> bool {
                 const int s = c % kStages;
-                if (!wait(B_FULL0 + s, (c / kStages) & 1, kWhereFull, c)) return false;
+                if (!wait1(B_FULL0 + s, (c / kStages) & 1, kWhereFull, c)) return false;
                 tc_fence_after();
                 const uint32_t sb = st0 + s * L::kStageBytes;
 #pragma unroll
@@ -285,14 +314,14 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 mma_commit(&bars[B_GQ]);
                 return true;
             };
-            bool ok = nchunks > 0 ? issue_gq(0) : true;
+            bool ok = issue_gq(0);
             for (int c = 0; ok && c < nchunks; ++c) {
                 const int s = c % kStages;
                 const uint32_t par = c & 1;
                 const uint32_t sb = st0 + s * L::kStageBytes;
                 const uint32_t sV = sb + KB * 16384;
-                // U = Tb V, Wk = Tg K
-                if (!(ok = wait(B_T, par, kWhereT, c))) break;
+                // U = Tb V, Wk = Tg K   (prep of chunk c done)
+                if (!(ok = wait1(B_T, par, kWhereT, c))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
@@ -303,9 +332,11 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     mma_bf16(tmem + TM_WK, sdesc_sw128(sTg + k * 32, 16, 1024),
                              sdesc_sw128(sb + k * 2048, 16384, 1024), id_wk, k > 0);
                 mma_commit(&bars[B_WK]);
+                // next chunk's Gram products run while the carry of this one proceeds
+                if (c + 1 < nchunks && !(ok = issue_gq(c + 1))) break;
                 // W = U - Wk S0, QS = Q S0
-                if (!(ok = wait(B_WKR, par, kWhereWKR, c))) break;
-                if (!(ok = wait(B_SR, par, kWhereSR, c))) break;
+                if (!(ok = wait1(B_WKR, par, kWhereWKR, c))) break;
+                if (!(ok = wait1(B_SR, par, kWhereSR, c))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < DK / 16; ++k) {
@@ -321,78 +352,193 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 }
                 mma_commit(&bars[B_W]);
                 // S_acc = K^T Wt, PW = P Wb
-                if (!(ok = wait(B_WR, par, kWhereWR, c))) break;
+                if (!(ok = wait1(B_WR, par, kWhereWR, c))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_bf16(tmem + TM_S, sdesc_sw128(sb + k * 2048, 16384, 1024),
                              sdesc_sw128(sWt + k * 2048, 8192, 1024), id_s, k > 0);
+                const uint32_t sPc = sP + par * 8192;
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_bf16(tmem + TM_PW, sdesc_sw128(sP + k * 32, 16, 1024),
+                    mma_bf16(tmem + TM_PW, sdesc_sw128(sPc + k * 32, 16, 1024),
                              sdesc_sw128(sWb + k * 2048, 8192, 1024), id_pw, k > 0);
                 mma_commit(&bars[B_S]);
                 mma_commit(&bars[B_EMPTY0 + s]);
-                if (c + 1 < nchunks) ok = issue_gq(c + 1);
             }
-            // drain: wait until every issued MMA has completed before TMEM is freed
+            // every issued MMA must complete before TMEM is released
             mma_commit(&bars[B_DRAIN]);
             const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(&bars[B_DRAIN], 0)) {
-                if (globaltimer_ns() - t0 > kTimeoutNs) { fail(kWhereS, -1); break; }
+            while (!mbar_try_wait_sleep(&bars[B_DRAIN], 0, kSuspendNs)) {
+                if (globaltimer_ns() - t0 > kTimeoutNs) { fail(kWhereDrain, -1); break; }
             }
         }
-    } else {
-        // ------------------------------------------------------------ compute warpgroup
+    } else if (warp < 6) {
+        // ================================================================ carry warpgroup
         const int q = warp & 3;              // TMEM lane quadrant this warp may access
         const int r128 = q * 32 + lane;      // row of an M=128 accumulator
         const bool m64 = lane < 16;          // holds a row of an M=64 accumulator
         const int r64 = q * 16 + lane;       // that row
-        const uint32_t lane_field = (uint32_t)(q * 32) << 16;
-        uint8_t* Pt = sm + L::kP;
-        uint8_t* Tbt = sm + L::kTb;
-        uint8_t* Tgt = sm + L::kTg;
+        const uint32_t lf = (uint32_t)(q * 32) << 16;
+        const int ct = tid - 64;
+        const bool own_s = (DK == 128) ? true : m64;
+        const int srow = (DK == 128) ? r128 : r64;
         uint8_t* Wkt = sm + L::kWk;
         uint8_t* Wbt = sm + L::kWb;
         uint8_t* Wtt = sm + L::kWt;
         uint8_t* Sbt = sm + L::kSb;
-        const int ct = tid - 64;             // 0..127
-        // Bounded wait whose outcome is the same for all 128 compute threads.
-        auto cwait = [&](int slot, uint32_t parity, unsigned where, int c) -> bool {
-            bool bad = *abort_flag != 0;
-            if (!bad) {
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(&bars[slot], parity)) {
-                    if (*abort_flag) { bad = true; break; }
-                    if (globaltimer_ns() - t0 > kTimeoutNs) { fail(where, c); bad = true; break; }
-                }
-            }
-            return !named_sync_or(bad);
-        };
 
-        // state row owned by this thread: M=DK accumulator rows
-        const bool own_s = (DK == 128) ? true : m64;
-        const int srow = (DK == 128) ? r128 : r64;
-        float S[DVS];
-        if (own_s) {
-            const float* src = p.h0 ? p.h0 + head * DK * dv + (size_t)srow * dv + j0 : nullptr;
+        // master state <- h0 (or zeros); bf16 copy for the first chunk
 #pragma unroll
-            for (int j = 0; j < DVS; j += 4) {
-                float4 v4 = src ? *reinterpret_cast<const float4*>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-                S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
+        for (int half = 0; half < 2; ++half) {
+            float v[32];
+            const float* src = (p.h0 && own_s) ? p.h0 + head * DK * dv + (size_t)srow * dv + j0 + 32 * half : nullptr;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                const float4 v4 = src ? *reinterpret_cast<const float4*>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[j] = v4.x; v[j + 1] = v4.y; v[j + 2] = v4.z; v[j + 3] = v4.w;
             }
+            tmem_st_32x32b_x32(tmem + lf + TM_SM + 32 * half, v);
+            if (own_s) {
 #pragma unroll
-            for (int c8 = 0; c8 < DVS / 8; ++c8) ST_CHUNK(Sbt, srow, c8, S, c8 * 8);
+                for (int u = 0; u < 4; ++u) ST_CHUNK(Sbt, srow, 4 * half + u, v, 8 * u);
+            }
         }
+        tmem_st_wait();
         fence_proxy_async_smem();
-        named_sync_compute();
+        tc_fence_before();
+        bar_sync(1, 128);
         if (ct == 0) mbar_arrive(&bars[B_SR]);
 
-        // gates of this thread's chunk row (rows 0..63 live in quadrants 0, 1)
-        const bool grow = q < 2;
-        const int gr = r128;  // 0..63 for grow
+        for (int c = 0; c < nchunks; ++c) {
+            const uint32_t par = c & 1;
+            const int t0 = c * C;
+            const int nvalid = min(C, T - t0);
+            const ChunkScalars& cs = scal[par];
+
+            // ---- Wk (M=64, N=DK) -> bf16 K-major tile
+            if (!waitg(B_WK, par, kWhereWK, c, 2)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < DK; cc += 32) {
+                float t32[32];
+                tmem_ld_32x32b_x32(tmem + lf + TM_WK + cc, t32);
+                tmem_ld_wait();
+                if (m64) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) ST_CHUNK(Wkt + (cc / 64) * 8192, r64, (cc % 64) / 8 + u, t32, 8 * u);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            bar_sync(1, 128);
+            if (ct == 0) mbar_arrive(&bars[B_WKR]);
+
+            // ---- W (M=64) -> bf16 tiles W and Wt = diag(exp(gC - gam)) W.
+            // Everything this chunk needs from the prep scalars is read here:
+            // the buffer is rewritten two chunks later.
+            if (!waitg(B_W, par, kWhereW, c, 2)) break;
+            tc_fence_after();
+            const float gC = cs.gam[C - 1];
+            const float gr = m64 ? cs.gam[r64] : 0.f;
+            const float Gr = __expf(gr);
+            const float GC = __expf(gC);
+            {
+                const float sc = __expf(gC - gr);
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 32) {
+                    float t32[32];
+                    tmem_ld_32x32b_x32(tmem + lf + TM_W + cc, t32);
+                    tmem_ld_wait();
+                    if (m64) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) ST_CHUNK(Wbt, r64, cc / 8 + u, t32, 8 * u);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) t32[i] *= sc;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) ST_CHUNK(Wtt, r64, cc / 8 + u, t32, 8 * u);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            bar_sync(1, 128);
+            if (ct == 0) mbar_arrive(&bars[B_WR]);
+
+            // ---- state update S1 = Gam_C S0 + K^T Wt (master in TMEM, bf16 copy in smem)
+            if (!waitg(B_S, par, kWhereS, c, 2)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float acc[32], sm32[32];
+                tmem_ld_32x32b_x32(tmem + lf + TM_S + 32 * half, acc);
+                tmem_ld_32x32b_x32(tmem + lf + TM_SM + 32 * half, sm32);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sm32[i] = fmaf(GC, sm32[i], acc[i]);
+                tmem_st_32x32b_x32(tmem + lf + TM_SM + 32 * half, sm32);
+                if (own_s) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) ST_CHUNK(Sbt, srow, 4 * half + u, sm32, 8 * u);
+                }
+            }
+            // output rows o = Gam_r QS + PW (TMEM read before QS/PW are reused)
+            uint32_t opk[32];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float a32[32], b32[32];
+                tmem_ld_32x32b_x32(tmem + lf + TM_QS + 32 * half, a32);
+                tmem_ld_32x32b_x32(tmem + lf + TM_PW + 32 * half, b32);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    opk[16 * half + i] = pack2(fmaf(Gr, a32[2 * i], b32[2 * i]),
+                                               fmaf(Gr, a32[2 * i + 1], b32[2 * i + 1]));
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            bar_sync(1, 128);
+            if (ct == 0) mbar_arrive(&bars[B_SR]);
+            if (m64 && r64 < nvalid) {
+                uint4* orow = reinterpret_cast<uint4*>(p.o + (((size_t)b * T + t0 + r64) * H + h) * dv + j0);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    orow[u] = make_uint4(opk[4 * u], opk[4 * u + 1], opk[4 * u + 2], opk[4 * u + 3]);
+            }
+        }
+        // final state
+        const bool aborted = bar_or(2, 128, *abort_flag != 0);
+        if (p.hT && !aborted) {
+            tc_fence_after();
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float v[32];
+                tmem_ld_32x32b_x32(tmem + lf + TM_SM + 32 * half, v);
+                tmem_ld_wait();
+                if (own_s) {
+                    float* dst = p.hT + head * DK * dv + (size_t)srow * dv + j0 + 32 * half;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                }
+            }
+        }
+    } else {
+        // ================================================================ prep warpgroup
+        const int q = warp & 3;
+        const int r128 = q * 32 + lane;
+        const uint32_t lf = (uint32_t)(q * 32) << 16;
+        const int pt = tid - 192;            // 0..127
+        const bool grow = q < 2;             // holds a K K^T row (rows 0..63)
+        float* Af = reinterpret_cast<float*>(sm + L::kAf);
+        float* Tf = reinterpret_cast<float*>(sm + L::kTf);
+        float* Rw = reinterpret_cast<float*>(sm + L::kRw);
+        uint8_t* Tbt = sm + L::kTb;
+        uint8_t* Tgt = sm + L::kTg;
+
         auto load_gates = [&](int c, float& gv, float& ev) {
-            const int t = c * C + gr;
+            const int t = c * C + r128;
             if (grow && c < nchunks && t < T) {
                 const size_t off = ((size_t)b * T + t) * H + h;
                 gv = p.g[off];
@@ -407,24 +553,25 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
         for (int c = 0; c < nchunks; ++c) {
             const uint32_t par = c & 1;
-            const int t0 = c * C;
-            const int nvalid = min(C, T - t0);
+            const int nvalid = min(C, T - c * C);
+            ChunkScalars& cs = scal[par];
             const float g_cur = g_next, e_cur = e_next;
             load_gates(c + 1, g_next, e_next);
 
-            // ---- 1. K K^T / Q K^T ready
-            if (!cwait(B_GQ, par, kWhereGQ, c)) break;
+            // ---- Gram rows: K K^T (quadrants 0,1) and Q K^T (quadrants 2,3)
+            if (!waitg(B_GQ, par, kWhereGQ, c, 4)) break;
             tc_fence_after();
             float row[64];
+            {
+                float lo[32], hi[32];
+                tmem_ld_32x32b_x32(tmem + lf + TM_GQ, lo);
+                tmem_ld_32x32b_x32(tmem + lf + TM_GQ + 32, hi);
+                tmem_ld_wait();
 #pragma unroll
-            for (int cc = 0; cc < 64; cc += 16) {
-                float tmp[16];
-                tmem_ld_32x32b_x16(tmem + lane_field + TM_GQ + cc, tmp);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) row[cc + i] = tmp[i];
+                for (int i = 0; i < 32; ++i) { row[i] = lo[i]; row[32 + i] = hi[i]; }
             }
-            tmem_ld_wait();
-            // ---- 2. decay cumsum and beta (rows 0..63: quadrants 0 and 1)
+            tc_fence_before();
+            // ---- decay cumsum and beta (rows 0..63)
             if (grow) {
                 float s = g_cur;
 #pragma unroll
@@ -433,11 +580,10 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     if (lane >= off) s += n;
                 }
                 if (q == 0 && lane == 31) misc[0] = s;
-                named_sync_rows();
+                bar_sync(5, 64);
                 if (q == 1) s += misc[0];
-                gam[gr] = s;
-                // ||k_r||^2 = (K K^T)_rr: column gr of this thread's row.  The
-                // quadrant is warp-uniform, so every register index is static.
+                // ||k_r||^2 = (K K^T)_rr; the quadrant is warp-uniform, so
+                // every register index below is static.
                 float kk = 0.f;
                 if (q == 0) {
 #pragma unroll
@@ -446,57 +592,83 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
                     for (int j = 0; j < 32; ++j) kk = (lane == j) ? row[32 + j] : kk;
                 }
-                bet[gr] = (gr < nvalid) ? e_cur / (kk + p.eps) : 0.f;
+                const float beta = (r128 < nvalid) ? e_cur / (kk + p.eps) : 0.f;
+                cs.gam[r128] = s;
+                cs.bet[r128] = beta;
+                cs.betg[r128] = beta * __expf(s);
             }
-            named_sync_compute();
-            const float gC = gam[C - 1];
-            // ---- 3. A rows (quadrants 0,1) and P rows (quadrants 2,3)
+            bar_sync(3, 128);
+            const float gam0 = cs.gam[0], gamm = cs.gam[C / 2 - 1], gamL = cs.gam[C - 1];
+            const bool fact = (gam0 - gamL) <= kSpanMax;
+            if (grow) cs.w[r128] = __expf(gamm - cs.gam[r128]);
+            bar_sync(3, 128);
+            // ---- A rows (quadrants 0,1) and P rows (quadrants 2,3)
             if (grow) {
-                const float gr_ = gam[gr], br = bet[gr];
-                float* arow = Af + gr * LDF;
+                const int r = r128;
+                const float gr = cs.gam[r];
+                const float br = cs.bet[r];
+                const float ur = fact ? br * __expf(gr - gamm) : 0.f;
+                float* arow = Af + r * LDF;
 #pragma unroll
-                for (int s2 = 0; s2 < 64; ++s2)
-                    arow[s2] = (s2 < gr) ? br * __expf(gr_ - gam[s2]) * row[s2] : 0.f;
+                for (int s4 = 0; s4 < 64; s4 += 4) {
+                    const float4 w4 = *reinterpret_cast<const float4*>(&cs.w[s4]);
+                    const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+                    float out[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int s2 = s4 + i;
+                        const float d = fact ? ur * wv[i] : br * __expf(gr - cs.gam[s2]);
+                        out[i] = (s2 < r) ? d * row[s2] : 0.f;
+                    }
+                    *reinterpret_cast<float4*>(arow + s4) = make_float4(out[0], out[1], out[2], out[3]);
+                }
             } else {
-                const int pr = r128 - 64;
-                const float gp = gam[pr];
+                const int r = r128 - 64;
+                const float gr = cs.gam[r];
+                const float ur = fact ? __expf(gr - gamm) : 0.f;
+                uint8_t* Pt = sm + L::kP + par * 8192;
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
+                    const float4 wa = *reinterpret_cast<const float4*>(&cs.w[c8 * 8]);
+                    const float4 wb = *reinterpret_cast<const float4*>(&cs.w[c8 * 8 + 4]);
+                    const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
                     float v[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int s2 = c8 * 8 + i;
-                        v[i] = (s2 <= pr) ? __expf(gp - gam[s2]) * row[s2] : 0.f;
+                        const float d = fact ? ur * wv[i] : __expf(gr - cs.gam[s2]);
+                        v[i] = (s2 <= r) ? d * row[s2] : 0.f;
                     }
-                    ST_CHUNK(Pt, pr, c8, v, 0);
+                    ST_CHUNK(Pt, r, c8, v, 0);
                 }
             }
-            named_sync_compute();
-            // ---- 4. T = (I + A)^{-1}: diagonal 16x16 blocks (threads 0..63)
-            if (ct < 64) {
-                const int I = ct >> 4, j = ct & 15;
+            bar_sync(3, 128);
+            // ---- T = (I + A)^{-1}: diagonal 16x16 blocks, right-looking
+            if (pt < 64) {
+                const int I = pt >> 4, j = pt & 15;
                 const float* a = Af + (16 * I) * LDF + 16 * I;
                 float x[16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    float acc = (r == j) ? 1.f : 0.f;
+                for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
 #pragma unroll
-                    for (int s2 = 0; s2 < r; ++s2) acc = fmaf(-a[r * LDF + s2], x[s2], acc);
-                    x[r] = acc;
+                for (int s2 = 0; s2 < 15; ++s2) {
+                    const float xs = x[s2];
+#pragma unroll
+                    for (int r = s2 + 1; r < 16; ++r) x[r] = fmaf(-a[r * LDF + s2], xs, x[r]);
                 }
                 float* t = Tf + (16 * I) * LDF + 16 * I + j;
 #pragma unroll
                 for (int r = 0; r < 16; ++r) t[r * LDF] = x[r];
             }
-            named_sync_compute();
-            // off-diagonal blocks, one warp per block, by distance d = I - J
+            bar_sync(3, 128);
+            // off-diagonal blocks by distance d = I - J, one warp per block
             {
-                const int wi = warp - 2;  // 0..3
-                float* R = Rw + wi * 16 * LDF;
+                const int wi = warp - 6;  // 0..3
 #pragma unroll 1
                 for (int d = 1; d < 4; ++d) {
                     if (wi < 4 - d) {
                         const int J = wi, I = wi + d;
+                        float* R = Rw + wi * 16 * LDF;
                         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
                         for (int M = J; M < I; ++M)
                             warp_mma16(Af + (16 * I) * LDF + 16 * M, Tf + (16 * M) * LDF + 16 * J, acc);
@@ -507,138 +679,38 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                         warp_store16(Tf + (16 * I) * LDF + 16 * J, acc2, -1.f);
                         __syncwarp();
                     }
-                    named_sync_compute();
+                    bar_sync(3, 128);
                 }
             }
-            // ---- 5. Tb = T diag(beta), Tg = T diag(beta Gam) as bf16 operand tiles
+            // ---- Tb = T diag(beta), Tg = T diag(beta Gam) as bf16 operand tiles
             {
-                const int r = ct >> 1, half = ct & 1;
+                const int r = pt >> 1, half = pt & 1;
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) {
                     const int col8 = half * 4 + c8;
+                    const float4 t0 = *reinterpret_cast<const float4*>(&Tf[r * LDF + col8 * 8]);
+                    const float4 t1 = *reinterpret_cast<const float4*>(&Tf[r * LDF + col8 * 8 + 4]);
+                    const float4 b0 = *reinterpret_cast<const float4*>(&cs.bet[col8 * 8]);
+                    const float4 b1 = *reinterpret_cast<const float4*>(&cs.bet[col8 * 8 + 4]);
+                    const float4 e0 = *reinterpret_cast<const float4*>(&cs.betg[col8 * 8]);
+                    const float4 e1 = *reinterpret_cast<const float4*>(&cs.betg[col8 * 8 + 4]);
+                    const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+                    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                    const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
                     float vb[8], vg[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const int s2 = col8 * 8 + i;
-                        const float t = (s2 <= r) ? Tf[r * LDF + s2] : 0.f;
-                        const float bs = bet[s2];
-                        vb[i] = t * bs;
-                        vg[i] = t * bs * __expf(gam[s2]);
+                        const float t = (col8 * 8 + i <= r) ? tv[i] : 0.f;
+                        vb[i] = t * bv[i];
+                        vg[i] = t * ev[i];
                     }
                     ST_CHUNK(Tbt, r, col8, vb, 0);
                     ST_CHUNK(Tgt, r, col8, vg, 0);
                 }
             }
             fence_proxy_async_smem();
-            named_sync_compute();
-            if (ct == 0) mbar_arrive(&bars[B_T]);
-
-            // ---- 6. Wk (M=64, N=DK) -> bf16 K-major tile
-            if (!cwait(B_WK, par, kWhereWK, c)) break;
-            tc_fence_after();
-#pragma unroll
-            for (int cc = 0; cc < DK; cc += 16) {
-                float tmp[16];
-                tmem_ld_32x32b_x16(tmem + lane_field + TM_WK + cc, tmp);
-                tmem_ld_wait();
-                if (m64) {
-                    ST_CHUNK(Wkt + (cc / 64) * 8192, r64, (cc % 64) / 8, tmp, 0);
-                    ST_CHUNK(Wkt + (cc / 64) * 8192, r64, (cc % 64) / 8 + 1, tmp, 8);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_sync_compute();
-            if (ct == 0) mbar_arrive(&bars[B_WKR]);
-
-            // ---- 7. W (M=64) -> bf16 tiles W and Wt = diag(exp(gC - gam)) W
-            if (!cwait(B_W, par, kWhereW, c)) break;
-            tc_fence_after();
-            {
-                const float sc = m64 ? __expf(gC - gam[r64]) : 0.f;
-#pragma unroll
-                for (int cc = 0; cc < 64; cc += 16) {
-                    float tmp[16];
-                    tmem_ld_32x32b_x16(tmem + lane_field + TM_W + cc, tmp);
-                    tmem_ld_wait();
-                    if (m64) {
-                        ST_CHUNK(Wbt, r64, cc / 8, tmp, 0);
-                        ST_CHUNK(Wbt, r64, cc / 8 + 1, tmp, 8);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) tmp[i] *= sc;
-                        ST_CHUNK(Wtt, r64, cc / 8, tmp, 0);
-                        ST_CHUNK(Wtt, r64, cc / 8 + 1, tmp, 8);
-                    }
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_sync_compute();
-            if (ct == 0) mbar_arrive(&bars[B_WR]);
-
-            // ---- 8. state update S1 = Gam_C S0 + K^T Wt
-            if (!cwait(B_S, par, kWhereS, c)) break;
-            tc_fence_after();
-            {
-                const float GC = __expf(gC);
-#pragma unroll
-                for (int cc = 0; cc < DVS; cc += 16) {
-                    float tmp[16];
-                    tmem_ld_32x32b_x16(tmem + lane_field + TM_S + cc, tmp);
-                    tmem_ld_wait();
-                    if (own_s) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) S[cc + i] = fmaf(GC, S[cc + i], tmp[i]);
-                        ST_CHUNK(Sbt, srow, cc / 8, S, cc);
-                        ST_CHUNK(Sbt, srow, cc / 8 + 1, S, cc + 8);
-                    }
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_sync_compute();
-            if (ct == 0) mbar_arrive(&bars[B_SR]);
-
-            // ---- 9. output rows: o = Gam_r QS + PW
-            {
-                const float Gr = m64 ? __expf(gam[r64]) : 0.f;
-                __nv_bfloat16* orow = p.o + (((size_t)b * T + t0 + r64) * H + h) * dv + j0;
-#pragma unroll
-                for (int cc = 0; cc < 64; cc += 16) {
-                    float a16[16], b16[16];
-                    tmem_ld_32x32b_x16(tmem + lane_field + TM_QS + cc, a16);
-                    tmem_ld_32x32b_x16(tmem + lane_field + TM_PW + cc, b16);
-                    tmem_ld_wait();
-                    if (m64 && r64 < nvalid) {
-                        float v[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = fmaf(Gr, a16[i], b16[i]);
-                        uint4 pk[2];
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            __nv_bfloat162 x0 = __floats2bfloat162_rn(v[8 * hh + 0], v[8 * hh + 1]);
-                            __nv_bfloat162 x1 = __floats2bfloat162_rn(v[8 * hh + 2], v[8 * hh + 3]);
-                            __nv_bfloat162 x2 = __floats2bfloat162_rn(v[8 * hh + 4], v[8 * hh + 5]);
-                            __nv_bfloat162 x3 = __floats2bfloat162_rn(v[8 * hh + 6], v[8 * hh + 7]);
-                            pk[hh].x = *reinterpret_cast<uint32_t*>(&x0);
-                            pk[hh].y = *reinterpret_cast<uint32_t*>(&x1);
-                            pk[hh].z = *reinterpret_cast<uint32_t*>(&x2);
-                            pk[hh].w = *reinterpret_cast<uint32_t*>(&x3);
-                        }
-                        *reinterpret_cast<uint4*>(orow + cc) = pk[0];
-                        *reinterpret_cast<uint4*>(orow + cc + 8) = pk[1];
-                    }
-                }
-            }
-            tc_fence_before();
-        }
-        // final state
-        const bool aborted = named_sync_or(*abort_flag != 0);
-        if (p.hT && own_s && !aborted) {
-            float* dst = p.hT + head * DK * dv + (size_t)srow * dv + j0;
-#pragma unroll
-            for (int j = 0; j < DVS; j += 4)
-                *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+            bar_sync(3, 128);
+            if (pt == 0) mbar_arrive(&bars[B_T]);
         }
     }
     tc_fence_before();
