@@ -33,6 +33,7 @@ KLA_IO_FP32 = 1
 EXPORTED_SYMBOLS = (
     "kla_chunk_fwd_workspace_bytes",
     "kla_chunk_fwd",
+    "kla_chunk_fwd_noalloc",
     "kla_decode_step",
     "kla_workspace_check",
     "kla_status_string",
@@ -70,6 +71,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kla_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp,
                                       i, i, i, i, i, i, i, vp, sz, vp]
         lib.kla_chunk_fwd.restype = i
+        lib.kla_chunk_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp,
+                                              i, i, i, i, i, i, i, vp]
+        lib.kla_chunk_fwd_noalloc.restype = i
         lib.kla_decode_step.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp]
         lib.kla_decode_step.restype = i
         lib.kla_workspace_check.argtypes = [vp, sz, vp]
@@ -148,6 +152,32 @@ def kla_chunk_fwd(q, k, v, g, eta, eps, h0, o, hT, workspace, chunk=64, stream=N
         raise KlaError(rc, "kla_chunk_fwd")
 
 
+def kla_chunk_fwd_noalloc(q, k, v, g, eta, eps, h0, o, hT, chunk=64, stream=None) -> None:
+    """kla_chunk_fwd without a workspace, for callers that must not allocate
+    device memory: the scratch is an array built into the library (see
+    include/kla.h).  Allocates nothing; outputs are the caller's tensors."""
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    io = _io_of(q)
+    for name, t in (("k", k), ("v", v), ("o", o)):
+        if t.dtype != q.dtype:
+            raise TypeError(f"{name} must have q's dtype {q.dtype}")
+    if q.shape != k.shape or v.shape[:3] != k.shape[:3] or o.shape != v.shape:
+        raise ValueError("shape mismatch among q, k, v, o")
+    if g.shape != (B, T, H) or eta.shape != (B, T, H):
+        raise ValueError("g and eta must be [B,T,H]")
+    for name, t in (("h0", h0), ("hT", hT)):
+        if t is not None and tuple(t.shape) != (B, H, dk, dv):
+            raise ValueError(f"{name} must be [B,H,dk,dv]")
+    rc = load_library().kla_chunk_fwd_noalloc(
+        _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g", torch.float32),
+        _ptr(eta, "eta", torch.float32), float(eps), _ptr(h0, "h0", torch.float32),
+        _ptr(o, "o"), _ptr(hT, "hT", torch.float32), B, T, H, dk, dv, int(chunk), io,
+        _stream(stream))
+    if rc != KLA_OK:
+        raise KlaError(rc, "kla_chunk_fwd_noalloc")
+
+
 def kla_decode_step(q, k, v, g, eta, eps, S, o, stream=None) -> None:
     """Enqueue one decode step (see include/kla.h); S [B,H,dk,dv] is updated in place.
 
@@ -208,7 +238,8 @@ def decode_step(q, k, v, g, eta, S, eps=1e-6, stream=None):
 
 
 __all__ = [
-    "kla_chunk_fwd_workspace_bytes", "kla_chunk_fwd", "kla_decode_step", "kla_workspace_check",
+    "kla_chunk_fwd_workspace_bytes", "kla_chunk_fwd", "kla_chunk_fwd_noalloc", "kla_decode_step",
+    "kla_workspace_check",
     "kla_status_string", "chunk_fwd", "decode_step", "alloc_workspace", "load_library",
     "KlaError", "EXPORTED_SYMBOLS", "KLA_IO_BF16", "KLA_IO_FP32",
 ]

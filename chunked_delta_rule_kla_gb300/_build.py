@@ -23,6 +23,7 @@ SOURCES = [
     "kla_decode.cu",
     "kla_chunk_simt.cu",
     "kla_chunk_tc.cu",
+    "kla_noalloc.cu",
 ]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

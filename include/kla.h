@@ -119,6 +119,31 @@ KLA_API kla_status kla_decode_step(const void* q, const void* k, const void* v,
                            kla_io_dtype io, void* stream);
 
 /*
+ * kla_chunk_fwd for callers that must not allocate device memory.  The paper
+ * has no counterpart of this call; it exists for callers such as a plugin
+ * inside a host framework that owns every device allocation, or a serving
+ * loop that fixes its memory budget at start-up, which cannot provide the
+ * workspace kla_chunk_fwd asks for.
+ *
+ * Same arguments, semantics and errors as kla_chunk_fwd, without the
+ * workspace: the scratch lives in a 64 KiB array built into the library,
+ * held on every GPU that loads it until the process exits.  Problems whose
+ * kla_chunk_fwd_workspace_bytes exceeds 64 KiB are rejected with
+ * KLA_ERR_WORKSPACE.  No device memory is allocated.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call shares the array and it keeps the last call's contents; the
+ *    call clears what must start at zero.  Calls that overlap on the GPU
+ *    (other streams or host threads) race on it.
+ *  - A device-side wait timeout recorded in the array is not reported back.
+ */
+KLA_API kla_status kla_chunk_fwd_noalloc(const void* q, const void* k, const void* v,
+                                         const float* g, const float* eta, float eps,
+                                         const float* h0, void* o, float* hT,
+                                         int B, int T, int H, int dk, int dv, int chunk,
+                                         kla_io_dtype io, void* stream);
+
+/*
  * Synchronises `stream` and reads the device error record in `workspace`.
  * Returns KLA_ERR_DEVICE_TIMEOUT if a bounded device wait gave up during an
  * earlier kla_chunk_fwd on this workspace, KLA_OK otherwise.
