@@ -69,7 +69,8 @@ constexpr uint32_t TM_SM = 448;   // M=dk N=64: fp32 master state
 constexpr uint32_t kTmemCols = 512;
 
 enum : unsigned { kWhereFull = 1, kWhereEmpty, kWhereGQ, kWhereT, kWhereWK, kWhereWKR, kWhereSR,
-                  kWhereW, kWhereWR, kWhereS, kWhereDrain };
+                  kWhereW, kWhereWR, kWhereS, kWhereDrain, kWhereGQF, kWhereWKP, kWhereQS,
+                  kWherePW, kWhereEPI };
 
 // Per-chunk scalars written by the prep warpgroup, double-buffered by chunk
 // parity.
@@ -95,7 +96,8 @@ struct Layout {
     static constexpr uint32_t kAf = kSb + DK * 128;                // fp32 [64][LDF]
     static constexpr uint32_t kTf = kAf + C * LDF * 4;             // fp32 [64][LDF]
     static constexpr uint32_t kRw = kTf + C * LDF * 4;             // fp32 3 x [16][LDF]
-    static constexpr uint32_t kScal = kRw + 3 * 16 * LDF * 4;      // 2 x ChunkScalars
+    static constexpr uint32_t kAdT = kRw + 3 * 16 * LDF * 4;       // fp32 4 x [16][16] (A_II^T)
+    static constexpr uint32_t kScal = kAdT + 4 * 256 * 4;          // 2 x ChunkScalars
     static constexpr uint32_t kMisc = kScal + 2 * sizeof(ChunkScalars);
     static constexpr uint32_t kBars = kMisc + 64;
     static constexpr uint32_t kEnd = kBars + 32 * 8;
@@ -114,8 +116,8 @@ struct Params {
 };
 
 // mbarrier slots (all with arrival count 1)
-enum { B_FULL0 = 0, B_EMPTY0 = B_FULL0 + kStages, B_GQ = B_EMPTY0 + kStages, B_T, B_WK, B_WKR,
-       B_SR, B_W, B_WR, B_S, B_DRAIN, B_COUNT };
+enum { B_FULL0 = 0, B_EMPTY0 = B_FULL0 + kStages, B_GQ = B_EMPTY0 + kStages, B_GQF, B_T, B_WK,
+       B_WKR, B_SR, B_W, B_QS, B_WR, B_S, B_PW, B_EPI, B_DRAIN, B_COUNT };
 
 // Named barriers: 1/2 carry warpgroup (sync / or-reduction), 3/4 prep
 // warpgroup, 5 the two prep warps holding rows 0..63.
@@ -287,24 +289,42 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
     } else if (warp == 1) {
         // ================================================================ MMA issuer
-        if (lane == 0) {
-            const uint32_t st0 = smem_u32(sm + L::kStage0);
-            const uint32_t sP = smem_u32(sm + L::kP), sTb = smem_u32(sm + L::kTb),
-                           sTg = smem_u32(sm + L::kTg), sWk = smem_u32(sm + L::kWk),
-                           sWb = smem_u32(sm + L::kWb), sWt = smem_u32(sm + L::kWt),
-                           sSb = smem_u32(sm + L::kSb);
-            constexpr uint32_t id_gq = idesc_bf16(128, 64, false, false);
-            constexpr uint32_t id_u = idesc_bf16(64, 64, false, true);
-            constexpr uint32_t id_wk = idesc_bf16(64, DK, false, true);
-            constexpr uint32_t id_w = idesc_bf16(64, 64, false, true, true);
-            constexpr uint32_t id_qs = idesc_bf16(64, 64, false, true);
-            constexpr uint32_t id_s = idesc_bf16(DK, 64, true, true);
-            constexpr uint32_t id_pw = idesc_bf16(64, 64, false, true);
-            auto issue_gq = [&](int c) -> bool {
-                const int s = c % kStages;
-                if (!wait1(B_FULL0 + s, (c / kStages) & 1, kWhereFull, c)) return false;
-                tc_fence_after();
-                const uint32_t sb = st0 + s * L::kStageBytes;
+        // The whole warp runs the schedule so that descriptors and addresses
+        // stay warp-uniform; one elected lane issues each group of MMAs and
+        // its commit.
+        auto waitw = [&](int slot, uint32_t parity, unsigned where, int c) -> bool {
+            bool bad = *abort_flag != 0;
+            if (!bad) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait_sleep(&bars[slot], parity, kSuspendNs)) {
+                    if (*abort_flag) { bad = true; break; }
+                    if (globaltimer_ns() - t0 > kTimeoutNs) {
+                        if (lane == 0) fail(where, c);
+                        bad = true;
+                        break;
+                    }
+                }
+            }
+            return !__any_sync(0xffffffffu, bad);
+        };
+        const uint32_t st0 = smem_u32(sm + L::kStage0);
+        const uint32_t sP = smem_u32(sm + L::kP), sTb = smem_u32(sm + L::kTb),
+                       sTg = smem_u32(sm + L::kTg), sWk = smem_u32(sm + L::kWk),
+                       sWb = smem_u32(sm + L::kWb), sWt = smem_u32(sm + L::kWt),
+                       sSb = smem_u32(sm + L::kSb);
+        constexpr uint32_t id_gq = idesc_bf16(128, 64, false, false);
+        constexpr uint32_t id_u = idesc_bf16(64, 64, false, true);
+        constexpr uint32_t id_wk = idesc_bf16(64, DK, false, true);
+        constexpr uint32_t id_w = idesc_bf16(64, 64, false, true, true);
+        constexpr uint32_t id_qs = idesc_bf16(64, 64, false, true);
+        constexpr uint32_t id_s = idesc_bf16(DK, 64, true, true);
+        constexpr uint32_t id_pw = idesc_bf16(64, 64, false, true);
+        auto issue_gq = [&](int c) -> bool {
+            const int s = c % kStages;
+            if (!waitw(B_FULL0 + s, (c / kStages) & 1, kWhereFull, c)) return false;
+            tc_fence_after();
+            const uint32_t sb = st0 + s * L::kStageBytes;
+            if (elect_one()) {
 #pragma unroll
                 for (int k = 0; k < DK / 16; ++k) {
                     const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
@@ -312,17 +332,26 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                              sdesc_sw128(sb + off, 16, 1024), id_gq, k > 0);
                 }
                 mma_commit(&bars[B_GQ]);
-                return true;
-            };
-            bool ok = issue_gq(0);
-            for (int c = 0; ok && c < nchunks; ++c) {
-                const int s = c % kStages;
-                const uint32_t par = c & 1;
-                const uint32_t sb = st0 + s * L::kStageBytes;
-                const uint32_t sV = sb + KB * 16384;
-                // U = Tb V, Wk = Tg K   (prep of chunk c done)
-                if (!(ok = wait1(B_T, par, kWhereT, c))) break;
-                tc_fence_after();
+            }
+            __syncwarp();
+            return true;
+        };
+        bool ok = issue_gq(0);
+        for (int c = 0; ok && c < nchunks; ++c) {
+            const int s = c % kStages;
+            const uint32_t par = c & 1;
+            const uint32_t sb = st0 + s * L::kStageBytes;
+            const uint32_t sV = sb + KB * 16384;
+            // the prep has copied this chunk's Gram rows out of TMEM: the
+            // next chunk's Gram products can start right away
+            if (c + 1 < nchunks) {
+                if (!(ok = waitw(B_GQF, par, kWhereGQF, c))) break;
+                if (!(ok = issue_gq(c + 1))) break;
+            }
+            // U = Tb V, Wk = Tg K   (prep of chunk c done)
+            if (!(ok = waitw(B_T, par, kWhereT, c))) break;
+            tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_bf16(tmem + TM_W, sdesc_sw128(sTb + k * 32, 16, 1024),
@@ -332,47 +361,63 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     mma_bf16(tmem + TM_WK, sdesc_sw128(sTg + k * 32, 16, 1024),
                              sdesc_sw128(sb + k * 2048, 16384, 1024), id_wk, k > 0);
                 mma_commit(&bars[B_WK]);
-                // next chunk's Gram products run while the carry of this one proceeds
-                if (c + 1 < nchunks && !(ok = issue_gq(c + 1))) break;
-                // W = U - Wk S0, QS = Q S0
-                if (!(ok = wait1(B_WKR, par, kWhereWKR, c))) break;
-                if (!(ok = wait1(B_SR, par, kWhereSR, c))) break;
-                tc_fence_after();
+            }
+            __syncwarp();
+            // W = U - Wk S0 (on the state path: committed on its own)
+            if (!(ok = waitw(B_WKR, par, kWhereWKR, c))) break;
+            if (!(ok = waitw(B_SR, par, kWhereSR, c))) break;
+            tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
                 for (int k = 0; k < DK / 16; ++k) {
                     const uint32_t aoff = (k / 4) * 8192 + (k % 4) * 32;
                     mma_bf16(tmem + TM_W, sdesc_sw128(sWk + aoff, 16, 1024),
                              sdesc_sw128(sSb + k * 2048, 8192, 1024), id_w, 1);
                 }
+                mma_commit(&bars[B_W]);
+            }
+            __syncwarp();
+            // QS = Q S0 once the previous chunk's epilogue has read QS and PW
+            if (c > 0 && !(ok = waitw(B_EPI, par ^ 1u, kWhereEPI, c))) break;
+            tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
                 for (int k = 0; k < DK / 16; ++k) {
                     const uint32_t aoff = 8192 + (k / 4) * 16384 + (k % 4) * 32;
                     mma_bf16(tmem + TM_QS, sdesc_sw128(sb + aoff, 16, 1024),
                              sdesc_sw128(sSb + k * 2048, 8192, 1024), id_qs, k > 0);
                 }
-                mma_commit(&bars[B_W]);
-                // S_acc = K^T Wt, PW = P Wb
-                if (!(ok = wait1(B_WR, par, kWhereWR, c))) break;
-                tc_fence_after();
+                mma_commit(&bars[B_QS]);
+            }
+            __syncwarp();
+            // S_acc = K^T Wt (on the state path), then PW = P Wb
+            if (!(ok = waitw(B_WR, par, kWhereWR, c))) break;
+            tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_bf16(tmem + TM_S, sdesc_sw128(sb + k * 2048, 16384, 1024),
                              sdesc_sw128(sWt + k * 2048, 8192, 1024), id_s, k > 0);
+                mma_commit(&bars[B_S]);
                 const uint32_t sPc = sP + par * 8192;
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_bf16(tmem + TM_PW, sdesc_sw128(sPc + k * 32, 16, 1024),
                              sdesc_sw128(sWb + k * 2048, 8192, 1024), id_pw, k > 0);
-                mma_commit(&bars[B_S]);
+                mma_commit(&bars[B_PW]);
                 mma_commit(&bars[B_EMPTY0 + s]);
             }
-            // every issued MMA must complete before TMEM is released
+            __syncwarp();
+        }
+        // every issued MMA must complete before TMEM is released
+        if (elect_one()) {
             mma_commit(&bars[B_DRAIN]);
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait_sleep(&bars[B_DRAIN], 0, kSuspendNs)) {
                 if (globaltimer_ns() - t0 > kTimeoutNs) { fail(kWhereDrain, -1); break; }
             }
         }
+        __syncwarp();
     } else if (warp < 6) {
         // ================================================================ carry warpgroup
         const int q = warp & 3;              // TMEM lane quadrant this warp may access
@@ -465,24 +510,34 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             bar_sync(1, 128);
             if (ct == 0) mbar_arrive(&bars[B_WR]);
 
-            // ---- state update S1 = Gam_C S0 + K^T Wt (master in TMEM, bf16 copy in smem)
+            // ---- state update S1 = Gam_C S0 + K^T Wt: the bf16 copy for the
+            // next chunk's products is published first, then the fp32 master
+            // (TMEM) is rewritten.
             if (!waitg(B_S, par, kWhereS, c, 2)) break;
             tc_fence_after();
+            float snew[2][32];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                float acc[32], sm32[32];
+                float acc[32];
                 tmem_ld_32x32b_x32(tmem + lf + TM_S + 32 * half, acc);
-                tmem_ld_32x32b_x32(tmem + lf + TM_SM + 32 * half, sm32);
+                tmem_ld_32x32b_x32(tmem + lf + TM_SM + 32 * half, snew[half]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) sm32[i] = fmaf(GC, sm32[i], acc[i]);
-                tmem_st_32x32b_x32(tmem + lf + TM_SM + 32 * half, sm32);
+                for (int i = 0; i < 32; ++i) snew[half][i] = fmaf(GC, snew[half][i], acc[i]);
                 if (own_s) {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) ST_CHUNK(Sbt, srow, 4 * half + u, sm32, 8 * u);
+                    for (int u = 0; u < 4; ++u) ST_CHUNK(Sbt, srow, 4 * half + u, snew[half], 8 * u);
                 }
             }
-            // output rows o = Gam_r QS + PW (TMEM read before QS/PW are reused)
+            fence_proxy_async_smem();
+            tc_fence_before();
+            bar_sync(1, 128);
+            if (ct == 0) mbar_arrive(&bars[B_SR]);
+            tmem_st_32x32b_x32(tmem + lf + TM_SM, snew[0]);
+            tmem_st_32x32b_x32(tmem + lf + TM_SM + 32, snew[1]);
+            // ---- output rows o = Gam_r QS + PW
+            if (!waitg(B_PW, par, kWherePW, c, 2)) break;  // PW is issued after QS
+            tc_fence_after();
             uint32_t opk[32];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -496,10 +551,9 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                                                fmaf(Gr, a32[2 * i + 1], b32[2 * i + 1]));
             }
             tmem_st_wait();
-            fence_proxy_async_smem();
             tc_fence_before();
             bar_sync(1, 128);
-            if (ct == 0) mbar_arrive(&bars[B_SR]);
+            if (ct == 0) mbar_arrive(&bars[B_EPI]);
             if (m64 && r64 < nvalid) {
                 uint4* orow = reinterpret_cast<uint4*>(p.o + (((size_t)b * T + t0 + r64) * H + h) * dv + j0);
 #pragma unroll
@@ -507,6 +561,7 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     orow[u] = make_uint4(opk[4 * u], opk[4 * u + 1], opk[4 * u + 2], opk[4 * u + 3]);
             }
         }
+        tmem_st_wait();  // no TMEM store may be in flight when the CTA leaves
         // final state
         const bool aborted = bar_or(2, 128, *abort_flag != 0);
         if (p.hT && !aborted) {
@@ -534,6 +589,7 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         float* Af = reinterpret_cast<float*>(sm + L::kAf);
         float* Tf = reinterpret_cast<float*>(sm + L::kTf);
         float* Rw = reinterpret_cast<float*>(sm + L::kRw);
+        float* AdT = reinterpret_cast<float*>(sm + L::kAdT);
         uint8_t* Tbt = sm + L::kTb;
         uint8_t* Tgt = sm + L::kTg;
 
@@ -558,6 +614,19 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const float g_cur = g_next, e_cur = e_next;
             load_gates(c + 1, g_next, e_next);
 
+            // ---- decay cumsum (rows 0..63), before the Gram products are needed
+            float gsum = g_cur;
+            if (grow) {
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float n = __shfl_up_sync(0xffffffffu, gsum, off);
+                    if (lane >= off) gsum += n;
+                }
+                if (q == 0 && lane == 31) misc[0] = gsum;
+                bar_sync(5, 64);
+                if (q == 1) gsum += misc[0];
+            }
+
             // ---- Gram rows: K K^T (quadrants 0,1) and Q K^T (quadrants 2,3)
             if (!waitg(B_GQ, par, kWhereGQ, c, 4)) break;
             tc_fence_after();
@@ -571,17 +640,10 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 for (int i = 0; i < 32; ++i) { row[i] = lo[i]; row[32 + i] = hi[i]; }
             }
             tc_fence_before();
-            // ---- decay cumsum and beta (rows 0..63)
+            bar_sync(3, 128);
+            if (pt == 0) mbar_arrive(&bars[B_GQF]);
+            // ---- beta (rows 0..63)
             if (grow) {
-                float s = g_cur;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float n = __shfl_up_sync(0xffffffffu, s, off);
-                    if (lane >= off) s += n;
-                }
-                if (q == 0 && lane == 31) misc[0] = s;
-                bar_sync(5, 64);
-                if (q == 1) s += misc[0];
                 // ||k_r||^2 = (K K^T)_rr; the quadrant is warp-uniform, so
                 // every register index below is static.
                 float kk = 0.f;
@@ -593,68 +655,101 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     for (int j = 0; j < 32; ++j) kk = (lane == j) ? row[32 + j] : kk;
                 }
                 const float beta = (r128 < nvalid) ? e_cur / (kk + p.eps) : 0.f;
-                cs.gam[r128] = s;
+                cs.gam[r128] = gsum;
                 cs.bet[r128] = beta;
-                cs.betg[r128] = beta * __expf(s);
+                cs.betg[r128] = beta * __expf(gsum);
             }
             bar_sync(3, 128);
             const float gam0 = cs.gam[0], gamm = cs.gam[C / 2 - 1], gamL = cs.gam[C - 1];
             const bool fact = (gam0 - gamL) <= kSpanMax;
             if (grow) cs.w[r128] = __expf(gamm - cs.gam[r128]);
             bar_sync(3, 128);
-            // ---- A rows (quadrants 0,1) and P rows (quadrants 2,3)
+            // ---- A rows (quadrants 0,1) and P rows (quadrants 2,3); the
+            // decay-factor mode is uniform over the chunk.
             if (grow) {
                 const int r = r128;
                 const float gr = cs.gam[r];
                 const float br = cs.bet[r];
-                const float ur = fact ? br * __expf(gr - gamm) : 0.f;
                 float* arow = Af + r * LDF;
+                float dg[16];  // this row's entries inside its diagonal 16x16 block
+                if (fact) {
+                    const float ur = br * __expf(gr - gamm);
 #pragma unroll
-                for (int s4 = 0; s4 < 64; s4 += 4) {
-                    const float4 w4 = *reinterpret_cast<const float4*>(&cs.w[s4]);
-                    const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
-                    float out[4];
+                    for (int s4 = 0; s4 < 64; s4 += 4) {
+                        const float4 w4 = *reinterpret_cast<const float4*>(&cs.w[s4]);
+                        const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+                        float out[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int s2 = s4 + i;
-                        const float d = fact ? ur * wv[i] : br * __expf(gr - cs.gam[s2]);
-                        out[i] = (s2 < r) ? d * row[s2] : 0.f;
+                        for (int i = 0; i < 4; ++i) out[i] = (s4 + i < r) ? ur * wv[i] * row[s4 + i] : 0.f;
+                        *reinterpret_cast<float4*>(arow + s4) = make_float4(out[0], out[1], out[2], out[3]);
                     }
-                    *reinterpret_cast<float4*>(arow + s4) = make_float4(out[0], out[1], out[2], out[3]);
+                } else {
+#pragma unroll
+                    for (int s4 = 0; s4 < 64; s4 += 4) {
+                        float out[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            out[i] = (s4 + i < r) ? br * __expf(gr - cs.gam[s4 + i]) * row[s4 + i] : 0.f;
+                        *reinterpret_cast<float4*>(arow + s4) = make_float4(out[0], out[1], out[2], out[3]);
+                    }
                 }
+                __syncwarp();
+                // transposed copy of the diagonal block: AdT[I][s][r mod 16]
+                const int I = r >> 4, rl = r & 15;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) dg[i] = arow[16 * I + i];
+                float* adt = AdT + I * 256 + rl;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) adt[i * 16] = dg[i];
             } else {
                 const int r = r128 - 64;
                 const float gr = cs.gam[r];
-                const float ur = fact ? __expf(gr - gamm) : 0.f;
                 uint8_t* Pt = sm + L::kP + par * 8192;
+                if (fact) {
+                    const float ur = __expf(gr - gamm);
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    const float4 wa = *reinterpret_cast<const float4*>(&cs.w[c8 * 8]);
-                    const float4 wb = *reinterpret_cast<const float4*>(&cs.w[c8 * 8 + 4]);
-                    const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-                    float v[8];
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const float4 wa = *reinterpret_cast<const float4*>(&cs.w[c8 * 8]);
+                        const float4 wb = *reinterpret_cast<const float4*>(&cs.w[c8 * 8 + 4]);
+                        const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+                        float v[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int s2 = c8 * 8 + i;
-                        const float d = fact ? ur * wv[i] : __expf(gr - cs.gam[s2]);
-                        v[i] = (s2 <= r) ? d * row[s2] : 0.f;
+                        for (int i = 0; i < 8; ++i) v[i] = (c8 * 8 + i <= r) ? ur * wv[i] * row[c8 * 8 + i] : 0.f;
+                        ST_CHUNK(Pt, r, c8, v, 0);
                     }
-                    ST_CHUNK(Pt, r, c8, v, 0);
+                } else {
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        float v[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int s2 = c8 * 8 + i;
+                            v[i] = (s2 <= r) ? __expf(gr - cs.gam[s2]) * row[s2] : 0.f;
+                        }
+                        ST_CHUNK(Pt, r, c8, v, 0);
+                    }
                 }
             }
             bar_sync(3, 128);
-            // ---- T = (I + A)^{-1}: diagonal 16x16 blocks, right-looking
+            // ---- T = (I + A)^{-1}: diagonal 16x16 blocks, right-looking, one
+            // column per thread; column s of A_II is contiguous in AdT.
             if (pt < 64) {
                 const int I = pt >> 4, j = pt & 15;
-                const float* a = Af + (16 * I) * LDF + 16 * I;
+                const float* at = AdT + I * 256;
                 float x[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
 #pragma unroll
                 for (int s2 = 0; s2 < 15; ++s2) {
+                    float a[16];
+#pragma unroll
+                    for (int r4 = (s2 + 1) & ~3; r4 < 16; r4 += 4) {
+                        const float4 v4 = *reinterpret_cast<const float4*>(at + s2 * 16 + r4);
+                        a[r4] = v4.x; a[r4 + 1] = v4.y; a[r4 + 2] = v4.z; a[r4 + 3] = v4.w;
+                    }
                     const float xs = x[s2];
 #pragma unroll
-                    for (int r = s2 + 1; r < 16; ++r) x[r] = fmaf(-a[r * LDF + s2], xs, x[r]);
+                    for (int r = s2 + 1; r < 16; ++r) x[r] = fmaf(-a[r], xs, x[r]);
                 }
                 float* t = Tf + (16 * I) * LDF + 16 * I + j;
 #pragma unroll
@@ -682,7 +777,9 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     bar_sync(3, 128);
                 }
             }
-            // ---- Tb = T diag(beta), Tg = T diag(beta Gam) as bf16 operand tiles
+            // ---- Tb = T diag(beta), Tg = T diag(beta Gam) as bf16 operand tiles;
+            // the previous chunk's U and Wk products must have read them.
+            if (c > 0 && !waitg(B_WK, par ^ 1u, kWhereWKP, c, 4)) break;
             {
                 const int r = pt >> 1, half = pt & 1;
 #pragma unroll

@@ -182,6 +182,17 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// One lane of the (fully active) warp returns true.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .b32 rx;\n\t.reg .pred px;\n\telect.sync rx|px, %1;\n\t"
+        "selp.b32 %0, 1, 0, px;\n\t}"
+        : "=r"(pred)
+        : "r"(0xffffffffu));
+    return pred != 0;
+}
+
 // ---------------------------------------------------------------- MMA
 // Shared-memory matrix descriptor, 128-byte swizzle.  Addresses and byte
 // offsets are encoded >> 4.  K-major tiles: SBO = byte distance between
