@@ -185,7 +185,7 @@ LAUNCHES_PER_PREFILL = 1
 LAUNCHES_PER_DECODE = 1
 
 
-def bench_prefill(case, K, W, flush, peaks, stream):
+def bench_prefill(case, K, W, flush, peaks, stream, e2e=True):
     import chunked_delta_rule_kla_gb300 as kla
     inp = kla_inputs.make_prefill(case, device="cuda")
     B, T, H, dk, dv = case.B, case.T, case.H, case.dk, case.dv
@@ -209,6 +209,9 @@ def bench_prefill(case, K, W, flush, peaks, stream):
                roofline=roofline(work, mean_ms * 1e-3, peaks), work=work,
                launches=K * LAUNCHES_PER_PREFILL, min_ms=min(ms))
 
+    if not e2e:
+        del inp, o, hT
+        return res
     # end to end through the public API: pinned host inputs -> device -> call -> host
     host = {n: inp[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "eta")}
     o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
@@ -241,7 +244,7 @@ def bench_prefill(case, K, W, flush, peaks, stream):
     return res
 
 
-def bench_decode(case, K_loops, W_loops, peaks, stream, n_states=4):
+def bench_decode(case, K_loops, W_loops, peaks, stream, n_states=4, e2e=True):
     """Times `steps` consecutive kla_decode_step calls per loop.  The calls
     rotate over n_states independent state buffers (like the layers of a
     model), so the state working set (n_states x 64 MiB) exceeds L2."""
@@ -266,6 +269,9 @@ def bench_decode(case, K_loops, W_loops, peaks, stream, n_states=4):
                work=work, launches=K_loops * steps * LAUNCHES_PER_DECODE, calls_per_loop=steps,
                states_rotated=n_states)
 
+    if not e2e:
+        del inp, states
+        return res
     # end to end: per call, pinned host q/k/v/g/eta -> device, step, o -> host
     hq = {n: inp[n][:64].cpu().pin_memory() for n in ("q", "k", "v", "g", "eta")}
     dq = {n: torch.empty_like(hq[n][0], device="cuda") for n in hq}
@@ -338,6 +344,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-heads", type=int, default=16)
     ap.add_argument("--decode-loops", type=int, default=3)
+    ap.add_argument("--only", choices=["train", "long", "decode"], default=None,
+                    help="time one workload only (profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -358,20 +367,36 @@ def main():
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     clocks = ClockSampler(torch.cuda.current_device()).start()
 
+    e2e = not args.no_e2e
+    if args.only is not None:
+        if args.only == "decode":
+            dr = bench_decode(kla_inputs.DECODE, args.decode_loops, args.warmup, peaks, stream, e2e=e2e)
+            line = dict(workload=kla_inputs.DECODE.name, tokens_per_s=dr["tokens_per_s"],
+                        us_per_call=dr["ms_per_call"] * 1e3, roofline=dr["roofline"],
+                        gpu_launches=dr["launches"])
+        else:
+            case = kla_inputs.TRAIN if args.only == "train" else kla_inputs.LONG
+            r = bench_prefill(case, args.steps, args.warmup, flush, peaks, stream, e2e=e2e)
+            line = dict(workload=case.name, tokens_per_s=r["tokens_per_s"], ms_per_step=r["ms_per_step"],
+                        roofline=r["roofline"], gpu_launches=r["launches"])
+        clocks.stop()
+        if rank == 0:
+            print(json.dumps(dict(only=args.only, **line)), flush=True)
+        return
     main_case = kla_inputs.TRAIN
-    head = bench_prefill(main_case, args.steps, args.warmup, flush, peaks, stream)
+    head = bench_prefill(main_case, args.steps, args.warmup, flush, peaks, stream, e2e=e2e)
     secondary = {}
     if not args.no_secondary:
         lc = kla_inputs.LONG
-        lr = bench_prefill(lc, max(3, args.steps // 10), 3, flush, peaks, stream)
+        lr = bench_prefill(lc, max(3, args.steps // 10), 3, flush, peaks, stream, e2e=e2e)
         secondary["long_prefill"] = dict(workload=lc.name, tokens_per_s=lr["tokens_per_s"],
                                          ms_per_step=lr["ms_per_step"], roofline=lr["roofline"],
-                                         tflops=lr["tflops"], e2e=lr["e2e"])
+                                         tflops=lr["tflops"], e2e=lr.get("e2e"))
         dc = kla_inputs.DECODE
-        dr = bench_decode(dc, args.decode_loops, 3, peaks, stream)
+        dr = bench_decode(dc, args.decode_loops, 3, peaks, stream, e2e=e2e)
         secondary["decode"] = dict(workload=dc.name, tokens_per_s=dr["tokens_per_s"],
                                    hbm_gbs=dr["gbps"], us_per_call=dr["ms_per_call"] * 1e3,
-                                   roofline=dr["roofline"], e2e=dr["e2e"],
+                                   roofline=dr["roofline"], e2e=dr.get("e2e"),
                                    states_rotated=dr["states_rotated"])
     clk = clocks.stop()
     if rank != 0:
@@ -387,7 +412,8 @@ def main():
                     l2="flushed between timed steps (512 MiB write, outside the events)",
                     parallelism=f"replicas x{n}" if n > 1 else "single GPU"),
         tflops=head["tflops"], hbm_gbs_algorithmic=head["gbps"],
-        roofline=head["roofline"], e2e=dict(head["e2e"], value=head["e2e"]["value"] * n),
+        roofline=head["roofline"],
+        e2e=dict(head["e2e"], value=head["e2e"]["value"] * n) if "e2e" in head else None,
         gpu_launches=head["launches"], clocks=clk, secondary=secondary,
     )
     if not args.no_cpu_baseline:
