@@ -33,10 +33,11 @@
 // total decay span gam_0 - gam_63 is at most 80 (no fp32 overflow); otherwise
 // each factor is computed as one exponential.
 //
-// The triangular inverse: the four 16x16 diagonal blocks by right-looking
-// substitution (fp32, one column per thread), then the off-diagonal blocks by
-// block-column recurrence T_IJ = -T_II sum_{J<=M<I} A_IM T_MJ with warp-level
-// tf32 mma.sync (16x16 blocks are below tcgen05's minimum M).
+// The triangular inverse, fp32 on CUDA cores: the four 16x16 diagonal blocks
+// by right-looking substitution (one column per thread), then
+//   T_10 = -T_11 A_10 T_00,  T_32 = -T_33 A_32 T_22      (16x16 blocks)
+//   T_ba = -T_b A_ba T_a                                   (32x32 blocks)
+// where a, b are the leading and trailing 32-token halves of the chunk.
 #include "kla_internal.cuh"
 #include "tc_common.cuh"
 
@@ -135,46 +136,6 @@ __device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
     return r != 0;
 }
 
-__device__ __forceinline__ uint32_t f2tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-// D(16x16, two m16n8 fragments) += X(16x16) * Y(16x16); X, Y fp32 in shared
-// memory with row stride LDF.  One warp.
-__device__ __forceinline__ void warp_mma16(const float* X, const float* Y, float (&d)[2][4]) {
-    const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-        const uint32_t a0 = f2tf32(X[gq * LDF + kk * 8 + tq]);
-        const uint32_t a1 = f2tf32(X[(gq + 8) * LDF + kk * 8 + tq]);
-        const uint32_t a2 = f2tf32(X[gq * LDF + kk * 8 + tq + 4]);
-        const uint32_t a3 = f2tf32(X[(gq + 8) * LDF + kk * 8 + tq + 4]);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const uint32_t b0 = f2tf32(Y[(kk * 8 + tq) * LDF + nt * 8 + gq]);
-            const uint32_t b1 = f2tf32(Y[(kk * 8 + tq + 4) * LDF + nt * 8 + gq]);
-            asm volatile(
-                "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, "
-                "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-                : "+f"(d[nt][0]), "+f"(d[nt][1]), "+f"(d[nt][2]), "+f"(d[nt][3])
-                : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-        }
-    }
-}
-
-__device__ __forceinline__ void warp_store16(float* D, const float (&d)[2][4], float scale) {
-    const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        *reinterpret_cast<float2*>(&D[gq * LDF + nt * 8 + 2 * tq]) =
-            make_float2(scale * d[nt][0], scale * d[nt][1]);
-        *reinterpret_cast<float2*>(&D[(gq + 8) * LDF + nt * 8 + 2 * tq]) =
-            make_float2(scale * d[nt][2], scale * d[nt][3]);
-    }
-}
-
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&p);
@@ -202,7 +163,9 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     using L = Layout<DK>;
     constexpr int KB = L::KB;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived by pointer arithmetic on the shared
+    // array so that every access below stays a shared-memory access.
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBars);
     ChunkScalars* scal = reinterpret_cast<ChunkScalars*>(sm + L::kScal);
     float* misc = reinterpret_cast<float*>(sm + L::kMisc);
@@ -593,6 +556,9 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         uint8_t* Tbt = sm + L::kTb;
         uint8_t* Tgt = sm + L::kTg;
 
+        // The blocks of T above the diagonal stay zero for the whole kernel.
+        for (int i = pt; i < C * LDF; i += 128) Tf[i] = 0.f;
+        bar_sync(3, 128);
         auto load_gates = [&](int c, float& gv, float& ev) {
             const int t = c * C + r128;
             if (grow && c < nchunks && t < T) {
@@ -756,27 +722,84 @@ chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 for (int r = 0; r < 16; ++r) t[r * LDF] = x[r];
             }
             bar_sync(3, 128);
-            // off-diagonal blocks by distance d = I - J, one warp per block
-            {
-                const int wi = warp - 6;  // 0..3
-#pragma unroll 1
-                for (int d = 1; d < 4; ++d) {
-                    if (wi < 4 - d) {
-                        const int J = wi, I = wi + d;
-                        float* R = Rw + wi * 16 * LDF;
-                        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                        for (int M = J; M < I; ++M)
-                            warp_mma16(Af + (16 * I) * LDF + 16 * M, Tf + (16 * M) * LDF + 16 * J, acc);
-                        warp_store16(R, acc, 1.f);
-                        __syncwarp();
-                        float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                        warp_mma16(Tf + (16 * I) * LDF + 16 * I, R, acc2);
-                        warp_store16(Tf + (16 * I) * LDF + 16 * J, acc2, -1.f);
-                        __syncwarp();
-                    }
-                    bar_sync(3, 128);
+            // ---- T_10 = -T_11 (A_10 T_00) and T_32 = -T_33 (A_32 T_22):
+            // 64 threads, 2x4 outputs each (T's blocks above the diagonal
+            // are zero, so full 16-term sums need no masking)
+            if (pt < 64) {
+                const int bs = pt >> 5, rem = pt & 31, r0 = (rem >> 2) * 2, c0 = (rem & 3) * 4;
+                const int J = 2 * bs, I = J + 1;
+                float* R = Rw + bs * 16 * LDF;
+                float y[2][4] = {};
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const float a0 = Af[(16 * I + r0) * LDF + 16 * J + m];
+                    const float a1 = Af[(16 * I + r0 + 1) * LDF + 16 * J + m];
+                    const float4 t4 = *reinterpret_cast<const float4*>(&Tf[(16 * J + m) * LDF + 16 * J + c0]);
+                    y[0][0] = fmaf(a0, t4.x, y[0][0]); y[0][1] = fmaf(a0, t4.y, y[0][1]);
+                    y[0][2] = fmaf(a0, t4.z, y[0][2]); y[0][3] = fmaf(a0, t4.w, y[0][3]);
+                    y[1][0] = fmaf(a1, t4.x, y[1][0]); y[1][1] = fmaf(a1, t4.y, y[1][1]);
+                    y[1][2] = fmaf(a1, t4.z, y[1][2]); y[1][3] = fmaf(a1, t4.w, y[1][3]);
                 }
+                *reinterpret_cast<float4*>(&R[r0 * LDF + c0]) = make_float4(y[0][0], y[0][1], y[0][2], y[0][3]);
+                *reinterpret_cast<float4*>(&R[(r0 + 1) * LDF + c0]) = make_float4(y[1][0], y[1][1], y[1][2], y[1][3]);
             }
+            bar_sync(3, 128);
+            if (pt < 64) {
+                const int bs = pt >> 5, rem = pt & 31, r0 = (rem >> 2) * 2, c0 = (rem & 3) * 4;
+                const int J = 2 * bs, I = J + 1;
+                const float* R = Rw + bs * 16 * LDF;
+                float z[2][4] = {};
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const float t0 = Tf[(16 * I + r0) * LDF + 16 * I + m];
+                    const float t1 = Tf[(16 * I + r0 + 1) * LDF + 16 * I + m];
+                    const float4 y4 = *reinterpret_cast<const float4*>(&R[m * LDF + c0]);
+                    z[0][0] = fmaf(t0, y4.x, z[0][0]); z[0][1] = fmaf(t0, y4.y, z[0][1]);
+                    z[0][2] = fmaf(t0, y4.z, z[0][2]); z[0][3] = fmaf(t0, y4.w, z[0][3]);
+                    z[1][0] = fmaf(t1, y4.x, z[1][0]); z[1][1] = fmaf(t1, y4.y, z[1][1]);
+                    z[1][2] = fmaf(t1, y4.z, z[1][2]); z[1][3] = fmaf(t1, y4.w, z[1][3]);
+                }
+                *reinterpret_cast<float4*>(&Tf[(16 * I + r0) * LDF + 16 * J + c0]) =
+                    make_float4(-z[0][0], -z[0][1], -z[0][2], -z[0][3]);
+                *reinterpret_cast<float4*>(&Tf[(16 * I + r0 + 1) * LDF + 16 * J + c0]) =
+                    make_float4(-z[1][0], -z[1][1], -z[1][2], -z[1][3]);
+            }
+            bar_sync(3, 128);
+            // ---- T_ba = -T_b (A_ba T_a) for the 32x32 block (rows 32..63,
+            // columns 0..31): 128 threads, 2x4 outputs each
+            {
+                const int r0 = (pt >> 3) * 2, c0 = (pt & 7) * 4;
+                float y[2][4] = {};
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const float a0 = Af[(32 + r0) * LDF + m];
+                    const float a1 = Af[(33 + r0) * LDF + m];
+                    const float4 t4 = *reinterpret_cast<const float4*>(&Tf[m * LDF + c0]);
+                    y[0][0] = fmaf(a0, t4.x, y[0][0]); y[0][1] = fmaf(a0, t4.y, y[0][1]);
+                    y[0][2] = fmaf(a0, t4.z, y[0][2]); y[0][3] = fmaf(a0, t4.w, y[0][3]);
+                    y[1][0] = fmaf(a1, t4.x, y[1][0]); y[1][1] = fmaf(a1, t4.y, y[1][1]);
+                    y[1][2] = fmaf(a1, t4.z, y[1][2]); y[1][3] = fmaf(a1, t4.w, y[1][3]);
+                }
+                *reinterpret_cast<float4*>(&Rw[r0 * LDF + c0]) = make_float4(y[0][0], y[0][1], y[0][2], y[0][3]);
+                *reinterpret_cast<float4*>(&Rw[(r0 + 1) * LDF + c0]) = make_float4(y[1][0], y[1][1], y[1][2], y[1][3]);
+                bar_sync(3, 128);
+                float z[2][4] = {};
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const float t0 = Tf[(32 + r0) * LDF + 32 + m];
+                    const float t1 = Tf[(33 + r0) * LDF + 32 + m];
+                    const float4 y4 = *reinterpret_cast<const float4*>(&Rw[m * LDF + c0]);
+                    z[0][0] = fmaf(t0, y4.x, z[0][0]); z[0][1] = fmaf(t0, y4.y, z[0][1]);
+                    z[0][2] = fmaf(t0, y4.z, z[0][2]); z[0][3] = fmaf(t0, y4.w, z[0][3]);
+                    z[1][0] = fmaf(t1, y4.x, z[1][0]); z[1][1] = fmaf(t1, y4.y, z[1][1]);
+                    z[1][2] = fmaf(t1, y4.z, z[1][2]); z[1][3] = fmaf(t1, y4.w, z[1][3]);
+                }
+                *reinterpret_cast<float4*>(&Tf[(32 + r0) * LDF + c0]) =
+                    make_float4(-z[0][0], -z[0][1], -z[0][2], -z[0][3]);
+                *reinterpret_cast<float4*>(&Tf[(33 + r0) * LDF + c0]) =
+                    make_float4(-z[1][0], -z[1][1], -z[1][2], -z[1][3]);
+            }
+            bar_sync(3, 128);
             // ---- Tb = T diag(beta), Tg = T diag(beta Gam) as bf16 operand tiles;
             // the previous chunk's U and Wk products must have read them.
             if (c > 0 && !waitg(B_WK, par ^ 1u, kWhereWKP, c, 4)) break;
