@@ -47,7 +47,9 @@ size_t kla_chunk_fwd_workspace_bytes(int B, int T, int H, int dk, int dv, int ch
     if (B < 0 || T < 0 || H < 0 || check_io(io) != KLA_OK) return 0;
     if (!dim_ok(dk) || !dim_ok(dv) || chunk != 64) return 0;
     if (!sizes_fit(B, T, H, dk, dv)) return 0;
-    return kla::kErrorRecordBytes;
+    size_t n = kla::kErrorRecordBytes;
+    if (io == KLA_IO_BF16) n += kla::chunk_fwd_tc_record_bytes(B, T, H);
+    return n;
 }
 
 kla_status kla_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
@@ -68,6 +70,8 @@ kla_status kla_chunk_fwd(const void* q, const void* k, const void* v, const floa
     if (!workspace || workspace_bytes < kla::kErrorRecordBytes) return KLA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KLA_ERR_WORKSPACE;
     if ((int64_t)B * H == 0) return KLA_OK;
+    if (workspace_bytes < kla_chunk_fwd_workspace_bytes(B, T, H, dk, dv, chunk, io))
+        return KLA_ERR_WORKSPACE;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(workspace, 0, kla::kErrorRecordBytes, st);
@@ -83,8 +87,9 @@ kla_status kla_chunk_fwd(const void* q, const void* k, const void* v, const floa
     }
     if (io == KLA_IO_BF16) {
         auto* rec = reinterpret_cast<kla::DeviceErrorRecord*>(workspace);
+        uint8_t* records = reinterpret_cast<uint8_t*>(workspace) + kla::kErrorRecordBytes;
         return to_status(kla::launch_chunk_fwd_tc(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dk, dv,
-                                                  rec, st));
+                                                  rec, records, st));
     }
     return to_status(kla::launch_chunk_fwd_simt(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dk,
                                                 dv, false, st));

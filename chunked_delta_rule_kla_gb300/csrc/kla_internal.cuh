@@ -48,12 +48,14 @@ cudaError_t launch_chunk_fwd_simt(const void* q, const void* k, const void* v, c
                                   cudaStream_t stream);
 
 // Chunkwise prefill on the tensor cores (tcgen05 + TMA + TMEM), bf16 I/O,
-// dk, dv in {64,128}, chunk 64 (kla_chunk_tc.cu).  `err` is the device error
-// record at the start of the caller's workspace.
+// dk, dv in {64,128}, chunk 64 (kla_chunk_tc.cu): a prep kernel over every
+// (chunk, head) writes per-chunk records to `records` (chunk_fwd_tc_record_bytes
+// bytes), then the carry kernel walks the chunks of each head.  `err` is the
+// device error record at the start of the caller's workspace.
 cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, const float* g,
                                 const float* eta, float eps, const float* h0, void* o, float* hT,
                                 int B, int T, int H, int dk, int dv, DeviceErrorRecord* err,
-                                cudaStream_t stream);
-size_t chunk_fwd_tc_smem_bytes(int dk);
+                                uint8_t* records, cudaStream_t stream);
+size_t chunk_fwd_tc_record_bytes(int B, int T, int H);
 
 }  // namespace kla

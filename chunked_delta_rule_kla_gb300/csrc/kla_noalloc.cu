@@ -5,12 +5,13 @@
 // plugin inside a host framework that owns every device allocation, or a
 // serving loop that fixes its memory budget at start-up and forbids any
 // allocation afterwards.  This entry point keeps the prefill's scratch (the
-// device error record that kla_chunk_fwd otherwise expects in the caller's
-// workspace) in a fixed array that is part of the library image, so the
-// caller passes only its inputs and outputs.
+// device error record and the per-chunk records that kla_chunk_fwd otherwise
+// expects in the caller's workspace) in a fixed array that is part of the
+// library image, so the caller passes only its inputs and outputs.
 //
-// The array is kNoAllocScratchBytes (64 KiB) on every GPU that loads the
-// library and stays resident until the process exits.  All calls share it:
+// The array is kNoAllocScratchBytes (16 MiB) on every GPU that loads the
+// library and stays resident until the process exits; with bf16 I/O that
+// covers about a thousand (batch, head, 64-token chunk) triples.  All calls share it:
 // it keeps the last call's contents, the call clears what must start at zero
 // before launching, and calls that run at the same time on the GPU (other
 // streams or other host threads) race on it.
@@ -21,7 +22,7 @@
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = 64 * 1024;
+constexpr size_t kNoAllocScratchBytes = 16u << 20;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

@@ -63,9 +63,11 @@ typedef enum kla_io_dtype {
 } kla_io_dtype;
 
 /*
- * Bytes of device workspace kla_chunk_fwd needs for this problem (always at
- * least 256: the first 256 bytes hold the device error record).  Returns 0 if
- * the arguments are invalid or unsupported.
+ * Bytes of device workspace kla_chunk_fwd needs for this problem: 256 bytes
+ * of device error record, plus, with bf16 I/O, one 16,640-byte record per
+ * (batch, head, 64-token chunk) that carries the chunk's state-independent
+ * operands from the first kernel to the second.  Returns 0 if the arguments
+ * are invalid or unsupported.
  */
 KLA_API size_t kla_chunk_fwd_workspace_bytes(int B, int T, int H, int dk, int dv,
                                      int chunk, kla_io_dtype io);
@@ -126,9 +128,10 @@ KLA_API kla_status kla_decode_step(const void* q, const void* k, const void* v,
  * workspace kla_chunk_fwd asks for.
  *
  * Same arguments, semantics and errors as kla_chunk_fwd, without the
- * workspace: the scratch lives in a 64 KiB array built into the library,
+ * workspace: the scratch lives in a 16 MiB array built into the library,
  * held on every GPU that loads it until the process exits.  Problems whose
- * kla_chunk_fwd_workspace_bytes exceeds 64 KiB are rejected with
+ * kla_chunk_fwd_workspace_bytes exceeds 16 MiB (with bf16 I/O, more than
+ * about a thousand (batch, head, 64-token chunk) triples) are rejected with
  * KLA_ERR_WORKSPACE.  No device memory is allocated.
  *  - The first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
