@@ -48,7 +48,7 @@ size_t kla_chunk_fwd_workspace_bytes(int B, int T, int H, int dk, int dv, int ch
     if (!dim_ok(dk) || !dim_ok(dv) || chunk != 64) return 0;
     if (!sizes_fit(B, T, H, dk, dv)) return 0;
     size_t n = kla::kErrorRecordBytes;
-    if (io == KLA_IO_BF16) n += kla::chunk_fwd_tc_record_bytes(B, T, H);
+    if (io == KLA_IO_BF16) n += kla::chunk_fwd_tc_record_bytes(B, T, H, dk);
     return n;
 }
 

@@ -17,14 +17,15 @@
 //
 //  chunk_prep_kernel   one CTA per (chunk, head), every chunk in parallel.
 //                      K K^T on tcgen05 (M=64), beta, the decay cumsum, A
-//                      and the triangular inverse on CUDA cores; writes the
-//                      bf16 operand tiles T diag(beta), T diag(beta Gam) and
+//                      and the triangular inverse on CUDA cores, then
+//                      Wk = T diag(beta Gam) K on tcgen05; writes the bf16
+//                      operand tiles T diag(beta), T diag(beta Gam), Wk and
 //                      gam to a record in the workspace.
 //  chunk_carry_kernel  one CTA per (head, 64-column state slice), chunks in
 //                      order, fp32 state in TMEM.  TMA brings K, Q, the V
 //                      slice and the chunk's record; tcgen05 computes Q K^T,
-//                      U, Wk, W, Q S0, K^T Wt and P W.  An aux warpgroup forms
-//                      P, converts Wk and writes the outputs; the carry
+//                      U, W, Q S0, K^T Wt and P W.  An aux warpgroup forms
+//                      P and writes the outputs; the carry
 //                      warpgroup does only the state path (W -> Wt, the
 //                      state update).
 //
@@ -62,12 +63,17 @@ constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s per wait
 constexpr uint32_t kSuspendNs = 100000;          // try_wait suspension hint
 constexpr float kSpanMax = 80.f;                 // largest decay span factorised
 
-// Workspace record of one (b, h, chunk): two swizzled bf16 64x64 tiles and
-// the decay cumsum.
-constexpr uint32_t kRecTb = 0;
-constexpr uint32_t kRecTg = 8192;
-constexpr uint32_t kRecGam = 16384;
-constexpr uint32_t kRecBytes = 16384 + 256;
+// Workspace record of one (b, h, chunk): the swizzled bf16 operand tiles
+// T diag(beta) (64x64), T diag(beta Gam) (64x64) and Wk = T diag(beta Gam) K
+// (64 x dk, as 64-column boxes), then the decay cumsum (64 floats).
+template <int DK>
+struct Rec {
+    static constexpr uint32_t kTb = 0;
+    static constexpr uint32_t kTg = 8192;
+    static constexpr uint32_t kWk = 16384;
+    static constexpr uint32_t kGam = kWk + (DK / 64) * 8192;
+    static constexpr uint32_t kBytes = kGam + 256;
+};
 
 enum : unsigned { kWhereFull = 1, kWhereEmpty, kWhereGQ, kWhereT, kWhereWK, kWhereWKR, kWhereSR,
                   kWhereW, kWhereEPI, kWhereWR, kWhereWB, kWhereS, kWherePW, kWherePR, kWhereDrain,
@@ -149,11 +155,12 @@ template <int DK>
 struct PrepLayout {
     static constexpr int KB = DK / 64;
     static constexpr uint32_t kK = 0;                          // KB boxes of [64][64] bf16
-    static constexpr uint32_t kTb = kK + KB * 8192;            // record image: Tb, Tg, gam
-    static constexpr uint32_t kTg = kTb + 8192;
-    static constexpr uint32_t kGam = kTg + 8192;               // 64 floats (record tail)
-    static constexpr uint32_t kRec = kTb;
-    static constexpr uint32_t kAf = kGam + 256;                // fp32 [64][LDF]
+    static constexpr uint32_t kRec = kK + KB * 8192;           // record image (Rec<DK>)
+    static constexpr uint32_t kTb = kRec + Rec<DK>::kTb;
+    static constexpr uint32_t kTg = kRec + Rec<DK>::kTg;
+    static constexpr uint32_t kWk = kRec + Rec<DK>::kWk;
+    static constexpr uint32_t kGam = kRec + Rec<DK>::kGam;
+    static constexpr uint32_t kAf = kRec + Rec<DK>::kBytes;    // fp32 [64][LDF]
     static constexpr uint32_t kTf = kAf + C * LDF * 4;         // fp32 [64][LDF]
     static constexpr uint32_t kRw = kTf + C * LDF * 4;         // fp32 [32][LDF]
     static constexpr uint32_t kAdT = kRw + 32 * LDF * 4;       // fp32 4 x [16][16]
@@ -180,7 +187,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
     constexpr int KB = L::KB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBars);  // 0: K loaded, 1: K K^T done
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBars);  // 0: K loaded, 1: K K^T, 2: Wk
     float* misc = reinterpret_cast<float*>(sm + L::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 32);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kMisc + 48);
@@ -203,11 +210,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
     if (tid == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
+        mbar_init(&bars[2], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, 64);
+        tmem_alloc(tmem_slot, 256);  // K K^T at column 0, Wk at column 64
         tmem_relinquish();
     }
     tc_fence_before();
@@ -464,9 +472,38 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
         }
         fence_proxy_async_smem();
         bar_sync(1, 128);
+        // ---- Wk = Tg K (M=64, N=dk; K as the MN-major B operand)
         if (pt == 0) {
-            uint8_t* dst = p.rec + (((size_t)b * H + h) * p.nchunks + c) * kRecBytes;
-            bulk_store(dst, sm + L::kRec, kRecBytes);
+            tc_fence_after();
+            constexpr uint32_t id_wk = idesc_bf16(64, DK, false, true);
+            const uint32_t sTg = smem_u32(sm + L::kTg), sK = smem_u32(sm + L::kK);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16(tmem + 64, sdesc_sw128(sTg + k * 32, 16, 1024),
+                         sdesc_sw128(sK + k * 2048, 8192, 1024), id_wk, k > 0);
+            mma_commit(&bars[2]);
+        }
+        if (!wt.group(2, 0, kWherePrepG, c, 3, 128)) goto prep_done;
+        tc_fence_after();
+        {
+            uint8_t* Wkt = sm + L::kWk;
+#pragma unroll
+            for (int cc = 0; cc < DK; cc += 32) {
+                float t32[32];
+                tmem_ld_32x32b_x32(tmem + lf + 64 + cc, t32);
+                tmem_ld_wait();
+                if (m64) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) ST_CHUNK(Wkt + (cc / 64) * 8192, r, (cc % 64) / 8 + u, t32, 8 * u);
+                }
+            }
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        bar_sync(1, 128);
+        if (pt == 0) {
+            uint8_t* dst = p.rec + (((size_t)b * H + h) * p.nchunks + c) * Rec<DK>::kBytes;
+            bulk_store(dst, sm + L::kRec, Rec<DK>::kBytes);
             bulk_commit();
             bulk_wait_all();
         }
@@ -475,7 +512,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 64);
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ============================================================================
@@ -504,11 +541,10 @@ template <int DK>
 struct CarryLayout {
     static constexpr int KB = DK / 64;
     static constexpr uint32_t kTmaBytes = (2 * KB + 1) * 8192;     // [K0 Q0 (K1 Q1)] V
-    static constexpr uint32_t kRecOff = kTmaBytes;                  // record: Tb, Tg, gam
-    static constexpr uint32_t kStageBytes = ((kTmaBytes + kRecBytes + 1023) / 1024) * 1024;
+    static constexpr uint32_t kRecOff = kTmaBytes;                  // record (Rec<DK>)
+    static constexpr uint32_t kStageBytes = ((kTmaBytes + Rec<DK>::kBytes + 1023) / 1024) * 1024;
     static constexpr uint32_t kP = kStages * kStageBytes;           // 2 x 8 KB (chunk parity)
-    static constexpr uint32_t kWk = kP + 2 * 8192;                  // KB boxes
-    static constexpr uint32_t kWb = kWk + KB * 8192;
+    static constexpr uint32_t kWb = kP + 2 * 8192;
     static constexpr uint32_t kWt = kWb + 8192;
     static constexpr uint32_t kSb = kWt + 8192;                     // [DK][64] bf16
     static constexpr uint32_t kMisc = kSb + DK * 128;
@@ -576,7 +612,7 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 if (c >= kStages && !wt.poll(B_EMPTY0 + s, ((c / kStages) - 1) & 1, kWhereEmpty, c)) break;
                 uint8_t* st = sm + s * L::kStageBytes;
                 uint64_t* full = &bars[B_FULL0 + s];
-                mbar_arrive_expect_tx(full, L::kTmaBytes + kRecBytes);
+                mbar_arrive_expect_tx(full, L::kTmaBytes + Rec<DK>::kBytes);
                 const int t0 = c * C;
 #pragma unroll
                 for (int kb = 0; kb < KB; ++kb) {
@@ -584,7 +620,7 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     tma_load_4d(st + kb * 16384 + 8192, &tm_q, full, kb * 64, h, t0, b);
                 }
                 tma_load_4d(st + KB * 16384, &tm_v, full, j0, h, t0, b);
-                bulk_load(st + L::kRecOff, p.rec + (head * nchunks + c) * kRecBytes, kRecBytes, full);
+                bulk_load(st + L::kRecOff, p.rec + (head * nchunks + c) * Rec<DK>::kBytes, Rec<DK>::kBytes, full);
                 issued = c + 1;
             }
             // every issued load must land before the CTA may exit
@@ -598,12 +634,10 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     } else if (warp == 1) {
         // ================================================================ MMA schedule
         const uint32_t st0 = smem_u32(sm);
-        const uint32_t sP = smem_u32(sm + L::kP), sWk = smem_u32(sm + L::kWk),
-                       sWb = smem_u32(sm + L::kWb), sWt = smem_u32(sm + L::kWt),
-                       sSb = smem_u32(sm + L::kSb);
+        const uint32_t sP = smem_u32(sm + L::kP), sWb = smem_u32(sm + L::kWb),
+                       sWt = smem_u32(sm + L::kWt), sSb = smem_u32(sm + L::kSb);
         constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);
         constexpr uint32_t id_u = idesc_bf16(64, 64, false, true);
-        constexpr uint32_t id_wk = idesc_bf16(64, DK, false, true);
         constexpr uint32_t id_w = idesc_bf16(64, 64, false, true, true);
         constexpr uint32_t id_qs = idesc_bf16(64, 64, false, true);
         constexpr uint32_t id_s = idesc_bf16(DK, 64, true, true);
@@ -614,8 +648,8 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const uint32_t par = c & 1;
             const uint32_t sb = st0 + s * L::kStageBytes;
             const uint32_t sV = sb + KB * 16384;
-            const uint32_t sTb = sb + L::kRecOff + kRecTb, sTg = sb + L::kRecOff + kRecTg;
-            // Q K^T, U = Tb V, Wk = Tg K   (inputs and record of chunk c landed)
+            const uint32_t sTb = sb + L::kRecOff + Rec<DK>::kTb, sWk = sb + L::kRecOff + Rec<DK>::kWk;
+            // Q K^T and U = Tb V   (inputs and record of chunk c landed)
             if (!(ok = wt.warp(B_FULL0 + s, (c / kStages) & 1, kWhereFull, c))) break;
             tc_fence_after();
             if (elect_one()) {
@@ -630,15 +664,9 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 for (int k = 0; k < 4; ++k)
                     mma_bf16(tmem + TM_W, sdesc_sw128(sTb + k * 32, 16, 1024),
                              sdesc_sw128(sV + k * 2048, 8192, 1024), id_u, k > 0);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_bf16(tmem + TM_WK, sdesc_sw128(sTg + k * 32, 16, 1024),
-                             sdesc_sw128(sb + k * 2048, 16384, 1024), id_wk, k > 0);
-                mma_commit(&bars[B_WK]);
             }
             __syncwarp();
-            // W = U - Wk S0  (state path)
-            if (!(ok = wt.warp(B_WKR, par, kWhereWKR, c))) break;
+            // W = U - Wk S0  (state path; Wk comes with the record)
             if (!(ok = wt.warp(B_SR, par, kWhereSR, c))) break;
             tc_fence_after();
             if (elect_one()) {
@@ -737,7 +765,7 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
         for (int c = 0; c < nchunks; ++c) {
             const uint32_t par = c & 1;
-            const float* gam = reinterpret_cast<const float*>(sm + (c % kStages) * L::kStageBytes + L::kRecOff + kRecGam);
+            const float* gam = reinterpret_cast<const float*>(sm + (c % kStages) * L::kStageBytes + L::kRecOff + Rec<DK>::kGam);
 
             // ---- W (M=64) -> Wt = diag(exp(gC - gam)) W first (the state
             // product needs it), then W itself (for P W).  The record is read
@@ -828,12 +856,11 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int r64 = q * 16 + lane;
         const uint32_t lf = (uint32_t)(q * 32) << 16;
         const int at = tid - 192;            // 0..127
-        uint8_t* Wkt = sm + L::kWk;
         for (int c = 0; c < nchunks; ++c) {
             const uint32_t par = c & 1;
             const int t0 = c * C;
             const int nvalid = min(C, T - t0);
-            const float* gam = reinterpret_cast<const float*>(sm + (c % kStages) * L::kStageBytes + L::kRecOff + kRecGam);
+            const float* gam = reinterpret_cast<const float*>(sm + (c % kStages) * L::kStageBytes + L::kRecOff + Rec<DK>::kGam);
 
             // ---- P = mask(exp(gam_r - gam_s) Q K^T) -> bf16 tile (parity buffer)
             if (!wt.group(B_QKB, par, kWherePR, c, 4, 128)) break;
@@ -870,24 +897,6 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tc_fence_before();
             bar_sync(3, 128);
             if (at == 0) mbar_arrive(&bars[B_PR]);
-
-            // ---- Wk (M=64, N=DK) -> bf16 K-major tile
-            if (!wt.group(B_WK, par, kWhereWK, c, 4, 128)) break;
-            tc_fence_after();
-#pragma unroll
-            for (int cc = 0; cc < DK; cc += 32) {
-                float t32[32];
-                tmem_ld_32x32b_x32(tmem + lf + TM_WK + cc, t32);
-                tmem_ld_wait();
-                if (m64) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) ST_CHUNK(Wkt + (cc / 64) * 8192, r64, (cc % 64) / 8 + u, t32, 8 * u);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            bar_sync(3, 128);
-            if (at == 0) mbar_arrive(&bars[B_WKR]);
 
             // ---- outputs o = Gam_r QS + PW
             if (!wt.group(B_PW, par, kWherePW, c, 4, 128)) break;  // PW is issued after QS
@@ -982,9 +991,9 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
 
 }  // namespace
 
-size_t chunk_fwd_tc_record_bytes(int B, int T, int H) {
+size_t chunk_fwd_tc_record_bytes(int B, int T, int H, int dk) {
     const size_t nchunks = (size_t)((T + C - 1) / C);
-    return (size_t)B * H * nchunks * kRecBytes;
+    return (size_t)B * H * nchunks * (dk == 128 ? Rec<128>::kBytes : Rec<64>::kBytes);
 }
 
 cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, const float* g,

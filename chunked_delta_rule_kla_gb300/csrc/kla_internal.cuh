@@ -56,6 +56,6 @@ cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, con
                                 const float* eta, float eps, const float* h0, void* o, float* hT,
                                 int B, int T, int H, int dk, int dv, DeviceErrorRecord* err,
                                 uint8_t* records, cudaStream_t stream);
-size_t chunk_fwd_tc_record_bytes(int B, int T, int H);
+size_t chunk_fwd_tc_record_bytes(int B, int T, int H, int dk);
 
 }  // namespace kla
