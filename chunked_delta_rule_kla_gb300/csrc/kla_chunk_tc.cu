@@ -155,20 +155,25 @@ template <int DK>
 struct PrepLayout {
     static constexpr int KB = DK / 64;
     static constexpr uint32_t kK = 0;                          // KB boxes of [64][64] bf16
-    static constexpr uint32_t kRec = kK + KB * 8192;           // record image (Rec<DK>)
-    static constexpr uint32_t kTb = kRec + Rec<DK>::kTb;
-    static constexpr uint32_t kTg = kRec + Rec<DK>::kTg;
-    static constexpr uint32_t kWk = kRec + Rec<DK>::kWk;
-    static constexpr uint32_t kGam = kRec + Rec<DK>::kGam;
-    static constexpr uint32_t kAf = kRec + Rec<DK>::kBytes;    // fp32 [64][LDF]
+    // Region X: A and T (fp32) while the inverse is formed; afterwards the
+    // outgoing record body (Tb, Tg, Wk) is written over it.
+    static constexpr uint32_t kX = kK + KB * 8192;
+    static constexpr uint32_t kAf = kX;                        // fp32 [64][LDF]
     static constexpr uint32_t kTf = kAf + C * LDF * 4;         // fp32 [64][LDF]
-    static constexpr uint32_t kRw = kTf + C * LDF * 4;         // fp32 [32][LDF]
+    static constexpr uint32_t kTb = kX + Rec<DK>::kTb;         // written after A is dead
+    static constexpr uint32_t kTg = kX + Rec<DK>::kTg;
+    static constexpr uint32_t kWk = kX + Rec<DK>::kWk;         // written after T is dead
+    static constexpr uint32_t kXEnd = (kTf + C * LDF * 4 > kX + Rec<DK>::kGam) ? kTf + C * LDF * 4
+                                                                               : kX + Rec<DK>::kGam;
+    static constexpr uint32_t kRw = kXEnd;                     // fp32 [32][LDF]
     static constexpr uint32_t kAdT = kRw + 32 * LDF * 4;       // fp32 4 x [16][16]
-    static constexpr uint32_t kBet = kAdT + 4 * 256 * 4;       // beta[64], betg[64], w[64]
+    static constexpr uint32_t kGam = kAdT + 4 * 256 * 4;       // 64 floats (record tail)
+    static constexpr uint32_t kBet = kGam + 256;               // beta[64], betg[64], w[64]
     static constexpr uint32_t kMisc = kBet + 3 * 256;
     static constexpr uint32_t kBars = kMisc + 64;
     static constexpr uint32_t kEnd = kBars + 4 * 8;
     static constexpr size_t kSmemBytes = kEnd + 1024;
+    static_assert(Rec<DK>::kTg + 8192 <= C * LDF * 4, "Tb, Tg fit in A's space");
 };
 
 struct PrepParams {
@@ -181,7 +186,7 @@ struct PrepParams {
 };
 
 template <int DK>
-__global__ void __launch_bounds__(kPrepThreads, 2)
+__global__ void __launch_bounds__(kPrepThreads, 3)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) {
     using L = PrepLayout<DK>;
     constexpr int KB = L::KB;
@@ -215,7 +220,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, 256);  // K K^T at column 0, Wk at column 64
+        tmem_alloc(tmem_slot, 128);  // K K^T, later Wk (the Gram rows are consumed first)
         tmem_relinquish();
     }
     tc_fence_before();
@@ -479,7 +484,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
             const uint32_t sTg = smem_u32(sm + L::kTg), sK = smem_u32(sm + L::kK);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                mma_bf16(tmem + 64, sdesc_sw128(sTg + k * 32, 16, 1024),
+                mma_bf16(tmem, sdesc_sw128(sTg + k * 32, 16, 1024),
                          sdesc_sw128(sK + k * 2048, 8192, 1024), id_wk, k > 0);
             mma_commit(&bars[2]);
         }
@@ -490,7 +495,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
 #pragma unroll
             for (int cc = 0; cc < DK; cc += 32) {
                 float t32[32];
-                tmem_ld_32x32b_x32(tmem + lf + 64 + cc, t32);
+                tmem_ld_32x32b_x32(tmem + lf + cc, t32);
                 tmem_ld_wait();
                 if (m64) {
 #pragma unroll
@@ -503,7 +508,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
         bar_sync(1, 128);
         if (pt == 0) {
             uint8_t* dst = p.rec + (((size_t)b * H + h) * p.nchunks + c) * Rec<DK>::kBytes;
-            bulk_store(dst, sm + L::kRec, Rec<DK>::kBytes);
+            bulk_store(dst, sm + L::kX, Rec<DK>::kGam);
+            bulk_store(dst + Rec<DK>::kGam, sm + L::kGam, 256);
             bulk_commit();
             bulk_wait_all();
         }
@@ -512,7 +518,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 // ============================================================================
