@@ -33,6 +33,9 @@ KLA_IO_FP32 = 1
 EXPORTED_SYMBOLS = (
     "kla_chunk_fwd_workspace_bytes",
     "kla_chunk_fwd",
+    "kla_chunk_fwd_scan_workspace_bytes",
+    "kla_chunk_fwd_scan",
+    "kla_chunk_fwd_auto_segments",
     "kla_chunk_fwd_noalloc",
     "kla_decode_step",
     "kla_workspace_check",
@@ -71,6 +74,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kla_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp,
                                       i, i, i, i, i, i, i, vp, sz, vp]
         lib.kla_chunk_fwd.restype = i
+        lib.kla_chunk_fwd_scan_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+        lib.kla_chunk_fwd_scan_workspace_bytes.restype = sz
+        lib.kla_chunk_fwd_scan.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp,
+                                           i, i, i, i, i, i, i, i, vp, sz, vp]
+        lib.kla_chunk_fwd_scan.restype = i
+        lib.kla_chunk_fwd_auto_segments.argtypes = [i, i, i, i, i, i, i]
+        lib.kla_chunk_fwd_auto_segments.restype = i
         lib.kla_chunk_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp,
                                               i, i, i, i, i, i, i, vp]
         lib.kla_chunk_fwd_noalloc.restype = i
@@ -122,16 +132,17 @@ def kla_chunk_fwd_workspace_bytes(B, T, H, dk, dv, chunk=64, io=KLA_IO_BF16) -> 
     return int(load_library().kla_chunk_fwd_workspace_bytes(B, T, H, dk, dv, chunk, io))
 
 
-def kla_chunk_fwd(q, k, v, g, eta, eps, h0, o, hT, workspace, chunk=64, stream=None) -> None:
-    """Enqueue the chunkwise prefill (see include/kla.h) on ``stream``.
+def kla_chunk_fwd_scan_workspace_bytes(B, T, H, dk, dv, chunk=64, io=KLA_IO_BF16, segments=0) -> int:
+    return int(load_library().kla_chunk_fwd_scan_workspace_bytes(B, T, H, dk, dv, chunk, io, segments))
 
-    q, k [B,T,H,dk]; v, o [B,T,H,dv] (bf16 or fp32, same dtype); g, eta
-    [B,T,H] fp32; h0, hT [B,H,dk,dv] fp32 or None; workspace a uint8 CUDA
-    tensor of at least kla_chunk_fwd_workspace_bytes(...) bytes.
-    """
+
+def kla_chunk_fwd_auto_segments(B, T, H, dk, dv, chunk=64, io=KLA_IO_BF16) -> int:
+    return int(load_library().kla_chunk_fwd_auto_segments(B, T, H, dk, dv, chunk, io))
+
+
+def _check_prefill_args(q, k, v, g, eta, h0, o, hT):
     B, T, H, dk = k.shape
     dv = v.shape[-1]
-    io = _io_of(q)
     for name, t in (("k", k), ("v", v), ("o", o)):
         if t.dtype != q.dtype:
             raise TypeError(f"{name} must have q's dtype {q.dtype}")
@@ -142,6 +153,17 @@ def kla_chunk_fwd(q, k, v, g, eta, eps, h0, o, hT, workspace, chunk=64, stream=N
     for name, t in (("h0", h0), ("hT", hT)):
         if t is not None and tuple(t.shape) != (B, H, dk, dv):
             raise ValueError(f"{name} must be [B,H,dk,dv]")
+    return B, T, H, dk, dv, _io_of(q)
+
+
+def kla_chunk_fwd(q, k, v, g, eta, eps, h0, o, hT, workspace, chunk=64, stream=None) -> None:
+    """Enqueue the chunkwise prefill (see include/kla.h) on ``stream``.
+
+    q, k [B,T,H,dk]; v, o [B,T,H,dv] (bf16 or fp32, same dtype); g, eta
+    [B,T,H] fp32; h0, hT [B,H,dk,dv] fp32 or None; workspace a uint8 CUDA
+    tensor of at least kla_chunk_fwd_workspace_bytes(...) bytes.
+    """
+    B, T, H, dk, dv, io = _check_prefill_args(q, k, v, g, eta, h0, o, hT)
     rc = load_library().kla_chunk_fwd(
         _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g", torch.float32),
         _ptr(eta, "eta", torch.float32), float(eps), _ptr(h0, "h0", torch.float32),
@@ -152,23 +174,27 @@ def kla_chunk_fwd(q, k, v, g, eta, eps, h0, o, hT, workspace, chunk=64, stream=N
         raise KlaError(rc, "kla_chunk_fwd")
 
 
+def kla_chunk_fwd_scan(q, k, v, g, eta, eps, h0, o, hT, workspace, segments, chunk=64,
+                       stream=None) -> None:
+    """kla_chunk_fwd with the chunk-level scan's segment count given (see
+    include/kla.h): 0 = automatic, 1 = no scan.  workspace holds at least
+    kla_chunk_fwd_scan_workspace_bytes(..., segments) bytes."""
+    B, T, H, dk, dv, io = _check_prefill_args(q, k, v, g, eta, h0, o, hT)
+    rc = load_library().kla_chunk_fwd_scan(
+        _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g", torch.float32),
+        _ptr(eta, "eta", torch.float32), float(eps), _ptr(h0, "h0", torch.float32),
+        _ptr(o, "o"), _ptr(hT, "hT", torch.float32), B, T, H, dk, dv, int(chunk), io,
+        int(segments), _ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != KLA_OK:
+        raise KlaError(rc, "kla_chunk_fwd_scan")
+
+
 def kla_chunk_fwd_noalloc(q, k, v, g, eta, eps, h0, o, hT, chunk=64, stream=None) -> None:
     """kla_chunk_fwd without a workspace, for callers that must not allocate
     device memory: the scratch is an array built into the library (see
     include/kla.h).  Allocates nothing; outputs are the caller's tensors."""
-    B, T, H, dk = k.shape
-    dv = v.shape[-1]
-    io = _io_of(q)
-    for name, t in (("k", k), ("v", v), ("o", o)):
-        if t.dtype != q.dtype:
-            raise TypeError(f"{name} must have q's dtype {q.dtype}")
-    if q.shape != k.shape or v.shape[:3] != k.shape[:3] or o.shape != v.shape:
-        raise ValueError("shape mismatch among q, k, v, o")
-    if g.shape != (B, T, H) or eta.shape != (B, T, H):
-        raise ValueError("g and eta must be [B,T,H]")
-    for name, t in (("h0", h0), ("hT", hT)):
-        if t is not None and tuple(t.shape) != (B, H, dk, dv):
-            raise ValueError(f"{name} must be [B,H,dk,dv]")
+    B, T, H, dk, dv, io = _check_prefill_args(q, k, v, g, eta, h0, o, hT)
     rc = load_library().kla_chunk_fwd_noalloc(
         _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g", torch.float32),
         _ptr(eta, "eta", torch.float32), float(eps), _ptr(h0, "h0", torch.float32),
@@ -210,8 +236,10 @@ def kla_workspace_check(workspace, stream=None) -> int:
 
 # ---- allocation helpers (torch memory only; the compute is the ABI call) ----
 
-def alloc_workspace(B, T, H, dk, dv, chunk=64, io=KLA_IO_BF16, device="cuda") -> torch.Tensor:
-    n = kla_chunk_fwd_workspace_bytes(B, T, H, dk, dv, chunk, io)
+def alloc_workspace(B, T, H, dk, dv, chunk=64, io=KLA_IO_BF16, device="cuda",
+                    segments=0) -> torch.Tensor:
+    """Workspace for kla_chunk_fwd (segments=0) or kla_chunk_fwd_scan."""
+    n = kla_chunk_fwd_scan_workspace_bytes(B, T, H, dk, dv, chunk, io, segments)
     if n == 0:
         raise KlaError(KLA_ERR_UNSUPPORTED, "kla_chunk_fwd_workspace_bytes")
     return torch.empty(n, dtype=torch.uint8, device=device)
@@ -239,6 +267,7 @@ def decode_step(q, k, v, g, eta, S, eps=1e-6, stream=None):
 
 __all__ = [
     "kla_chunk_fwd_workspace_bytes", "kla_chunk_fwd", "kla_chunk_fwd_noalloc", "kla_decode_step",
+    "kla_chunk_fwd_scan", "kla_chunk_fwd_scan_workspace_bytes", "kla_chunk_fwd_auto_segments",
     "kla_workspace_check",
     "kla_status_string", "chunk_fwd", "decode_step", "alloc_workspace", "load_library",
     "KlaError", "EXPORTED_SYMBOLS", "KLA_IO_BF16", "KLA_IO_FP32",

@@ -42,25 +42,43 @@ const char* kla_status_string(kla_status s) {
     return "KLA_ERR_UNKNOWN";
 }
 
-size_t kla_chunk_fwd_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk,
-                                     kla_io_dtype io) {
+int kla_chunk_fwd_auto_segments(int B, int T, int H, int dk, int dv, int chunk, kla_io_dtype io) {
     if (B < 0 || T < 0 || H < 0 || check_io(io) != KLA_OK) return 0;
     if (!dim_ok(dk) || !dim_ok(dv) || chunk != 64) return 0;
     if (!sizes_fit(B, T, H, dk, dv)) return 0;
+    if (io != KLA_IO_BF16) return 1;
+    return kla::chunk_fwd_tc_auto_segments(B, T, H, dk, dv);
+}
+
+size_t kla_chunk_fwd_scan_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk,
+                                          kla_io_dtype io, int segments) {
+    if (B < 0 || T < 0 || H < 0 || segments < 0 || check_io(io) != KLA_OK) return 0;
+    if (!dim_ok(dk) || !dim_ok(dv) || chunk != 64) return 0;
+    if (!sizes_fit(B, T, H, dk, dv)) return 0;
     size_t n = kla::kErrorRecordBytes;
-    if (io == KLA_IO_BF16) n += kla::chunk_fwd_tc_record_bytes(B, T, H, dk);
+    if (io != KLA_IO_BF16) return segments <= 1 ? n : 0;
+    if (segments == 0) segments = kla::chunk_fwd_tc_auto_segments(B, T, H, dk, dv);
+    n += kla::chunk_fwd_tc_record_bytes(B, T, H, dk);
+    n += kla::chunk_fwd_tc_scan_bytes(B, H, dk, dv, kla::chunk_fwd_tc_scan_shape(T, segments).nseg);
     return n;
 }
 
-kla_status kla_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
-                         const float* eta, float eps, const float* h0, void* o, float* hT,
-                         int B, int T, int H, int dk, int dv, int chunk, kla_io_dtype io,
-                         void* workspace, size_t workspace_bytes, void* stream) {
-    if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || chunk <= 0) return KLA_ERR_INVALID_ARG;
+size_t kla_chunk_fwd_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk,
+                                     kla_io_dtype io) {
+    return kla_chunk_fwd_scan_workspace_bytes(B, T, H, dk, dv, chunk, io, 0);
+}
+
+kla_status kla_chunk_fwd_scan(const void* q, const void* k, const void* v, const float* g,
+                              const float* eta, float eps, const float* h0, void* o, float* hT,
+                              int B, int T, int H, int dk, int dv, int chunk, kla_io_dtype io,
+                              int segments, void* workspace, size_t workspace_bytes, void* stream) {
+    if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || chunk <= 0 || segments < 0)
+        return KLA_ERR_INVALID_ARG;
     if (check_io(io) != KLA_OK) return KLA_ERR_INVALID_ARG;
     if (!(eps >= 0.f)) return KLA_ERR_INVALID_ARG;  // also rejects NaN
     if (!dim_ok(dk) || !dim_ok(dv) || chunk != 64) return KLA_ERR_UNSUPPORTED;
     if (!sizes_fit(B, T, H, dk, dv)) return KLA_ERR_UNSUPPORTED;
+    if (io != KLA_IO_BF16 && segments > 1) return KLA_ERR_UNSUPPORTED;
     const bool have_tokens = (int64_t)B * H * T > 0;
     if (have_tokens && (!q || !k || !v || !g || !eta || !o)) return KLA_ERR_INVALID_ARG;
     const void* ptrs[] = {q, k, v, h0, o, hT};
@@ -70,7 +88,8 @@ kla_status kla_chunk_fwd(const void* q, const void* k, const void* v, const floa
     if (!workspace || workspace_bytes < kla::kErrorRecordBytes) return KLA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KLA_ERR_WORKSPACE;
     if ((int64_t)B * H == 0) return KLA_OK;
-    if (workspace_bytes < kla_chunk_fwd_workspace_bytes(B, T, H, dk, dv, chunk, io))
+    if (segments == 0) segments = kla_chunk_fwd_auto_segments(B, T, H, dk, dv, chunk, io);
+    if (workspace_bytes < kla_chunk_fwd_scan_workspace_bytes(B, T, H, dk, dv, chunk, io, segments))
         return KLA_ERR_WORKSPACE;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -89,10 +108,18 @@ kla_status kla_chunk_fwd(const void* q, const void* k, const void* v, const floa
         auto* rec = reinterpret_cast<kla::DeviceErrorRecord*>(workspace);
         uint8_t* records = reinterpret_cast<uint8_t*>(workspace) + kla::kErrorRecordBytes;
         return to_status(kla::launch_chunk_fwd_tc(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dk, dv,
-                                                  rec, records, st));
+                                                  segments, rec, records, st));
     }
     return to_status(kla::launch_chunk_fwd_simt(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dk,
                                                 dv, false, st));
+}
+
+kla_status kla_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* eta, float eps, const float* h0, void* o, float* hT,
+                         int B, int T, int H, int dk, int dv, int chunk, kla_io_dtype io,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+    return kla_chunk_fwd_scan(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dk, dv, chunk, io, 0,
+                              workspace, workspace_bytes, stream);
 }
 
 kla_status kla_decode_step(const void* q, const void* k, const void* v, const float* g,

@@ -64,15 +64,16 @@ constexpr uint32_t kSuspendNs = 100000;          // try_wait suspension hint
 constexpr float kSpanMax = 80.f;                 // largest decay span factorised
 
 // Workspace record of one (b, h, chunk): the swizzled bf16 operand tiles
-// T diag(beta) (64x64), T diag(beta Gam) (64x64) and Wk = T diag(beta Gam) K
-// (64 x dk, as 64-column boxes), then the decay cumsum (64 floats).
+// T diag(beta) (64x64) and Wk = T diag(beta Gam) K (64 x dk, as 64-column
+// boxes), then the decay cumsum gam (64 floats) and the decay factors
+// w_s = exp(gam_m - gam_s) about the chunk's middle token m (64 floats).
 template <int DK>
 struct Rec {
     static constexpr uint32_t kTb = 0;
-    static constexpr uint32_t kTg = 8192;
-    static constexpr uint32_t kWk = 16384;
+    static constexpr uint32_t kWk = 8192;
     static constexpr uint32_t kGam = kWk + (DK / 64) * 8192;
-    static constexpr uint32_t kBytes = kGam + 256;
+    static constexpr uint32_t kWf = kGam + 256;
+    static constexpr uint32_t kBytes = kWf + 256;
 };
 
 enum : unsigned { kWhereFull = 1, kWhereEmpty, kWhereGQ, kWhereT, kWhereWK, kWhereWKR, kWhereSR,
@@ -156,24 +157,27 @@ struct PrepLayout {
     static constexpr int KB = DK / 64;
     static constexpr uint32_t kK = 0;                          // KB boxes of [64][64] bf16
     // Region X: A and T (fp32) while the inverse is formed; afterwards the
-    // outgoing record body (Tb, Tg, Wk) is written over it.
+    // outgoing record body (Tb, Wk) is written over it.  Tg = T diag(beta
+    // Gam), the A operand of Wk = Tg K, sits where Wk goes: it is written
+    // with Tb once A is dead and read by the MMA before Wk replaces it.
     static constexpr uint32_t kX = kK + KB * 8192;
     static constexpr uint32_t kAf = kX;                        // fp32 [64][LDF]
     static constexpr uint32_t kTf = kAf + C * LDF * 4;         // fp32 [64][LDF]
     static constexpr uint32_t kTb = kX + Rec<DK>::kTb;         // written after A is dead
-    static constexpr uint32_t kTg = kX + Rec<DK>::kTg;
-    static constexpr uint32_t kWk = kX + Rec<DK>::kWk;         // written after T is dead
+    static constexpr uint32_t kTg = kX + Rec<DK>::kWk;
+    static constexpr uint32_t kWk = kX + Rec<DK>::kWk;         // written after T and Tg are dead
     static constexpr uint32_t kXEnd = (kTf + C * LDF * 4 > kX + Rec<DK>::kGam) ? kTf + C * LDF * 4
                                                                                : kX + Rec<DK>::kGam;
     static constexpr uint32_t kRw = kXEnd;                     // fp32 [32][LDF]
     static constexpr uint32_t kAdT = kRw + 32 * LDF * 4;       // fp32 4 x [16][16]
-    static constexpr uint32_t kGam = kAdT + 4 * 256 * 4;       // 64 floats (record tail)
-    static constexpr uint32_t kBet = kGam + 256;               // beta[64], betg[64], w[64]
-    static constexpr uint32_t kMisc = kBet + 3 * 256;
+    static constexpr uint32_t kGam = kAdT + 4 * 256 * 4;       // gam[64], w[64] (record tail)
+    static constexpr uint32_t kWf = kGam + 256;
+    static constexpr uint32_t kBet = kWf + 256;                // beta[64], betg[64]
+    static constexpr uint32_t kMisc = kBet + 2 * 256;
     static constexpr uint32_t kBars = kMisc + 64;
     static constexpr uint32_t kEnd = kBars + 4 * 8;
     static constexpr size_t kSmemBytes = kEnd + 1024;
-    static_assert(Rec<DK>::kTg + 8192 <= C * LDF * 4, "Tb, Tg fit in A's space");
+    static_assert(Rec<DK>::kWk + 8192 <= C * LDF * 4, "Tb, Tg fit in A's space");
 };
 
 struct PrepParams {
@@ -199,7 +203,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
     float* gam = reinterpret_cast<float*>(sm + L::kGam);
     float* bet = reinterpret_cast<float*>(sm + L::kBet);
     float* betg = bet + C;
-    float* wf = bet + 2 * C;
+    float* wf = reinterpret_cast<float*>(sm + L::kWf);
     float* Af = reinterpret_cast<float*>(sm + L::kAf);
     float* Tf = reinterpret_cast<float*>(sm + L::kTf);
     float* Rw = reinterpret_cast<float*>(sm + L::kRw);
@@ -509,7 +513,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
         if (pt == 0) {
             uint8_t* dst = p.rec + (((size_t)b * H + h) * p.nchunks + c) * Rec<DK>::kBytes;
             bulk_store(dst, sm + L::kX, Rec<DK>::kGam);
-            bulk_store(dst + Rec<DK>::kGam, sm + L::kGam, 256);
+            bulk_store(dst + Rec<DK>::kGam, sm + L::kGam, 512);
             bulk_commit();
             bulk_wait_all();
         }
@@ -534,9 +538,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
 constexpr int kCarryThreads = 320;
 
 // TMEM column map (512 columns)
-constexpr uint32_t TM_QK = 0;     // M=64 N=64: Q K^T
+constexpr uint32_t TM_QK = 0;     // M=64 N=64: Q K^T, chunk parity 0 (parity 1 at +TM_QK1)
 constexpr uint32_t TM_W = 64;     // M=64 N=64: U, then W
-constexpr uint32_t TM_WK = 128;   // M=64 N=dk
+constexpr uint32_t TM_QK1 = 128;  // offset of the parity-1 Q K^T buffer
 constexpr uint32_t TM_QS = 256;   // M=64 N=64
 constexpr uint32_t TM_PW = 320;   // M=64 N=64
 constexpr uint32_t TM_S = 384;    // M=dk N=64: K^T Wt
@@ -559,20 +563,30 @@ struct CarryLayout {
     static constexpr size_t kSmemBytes = kEnd + 1024;
 };
 
+// Chunks of a head are split into nseg segments of seg_chunks chunks (the
+// last may be shorter); blockIdx.z = b * nseg + segment.
 struct CarryParams {
-    const float* h0;
+    const float* s_in;      // output mode: start states [B][H][nseg][DK][dv] (null: zeros)
     const uint8_t* rec;
     __nv_bfloat16* o;
-    float* hT;
+    float* s_out;           // output mode: hT [B][H][DK][dv] (null: not written), written by the
+                            // last segment; summary mode: [B][H][nseg][DK][dv + DK]
     DeviceErrorRecord* err;
     int T, H, dv, nchunks;
+    int nseg, seg_chunks;
 };
 
 // mbarrier slots (all with arrival count 1)
-enum { B_FULL0 = 0, B_EMPTY0 = B_FULL0 + kStages, B_QKB = B_EMPTY0 + kStages, B_PR, B_WK, B_WKR,
-       B_SR, B_W, B_QS, B_WR, B_WB, B_S, B_PW, B_EPI, B_DRAIN, B_COUNT };
+// B_QKB + p: Q K^T of the chunks of parity p has landed (one barrier per
+// TMEM buffer, so a phase can never be overtaken before it is waited for).
+enum { B_FULL0 = 0, B_EMPTY0 = B_FULL0 + kStages, B_QKB = B_EMPTY0 + kStages, B_QKB1, B_PR,
+       B_SR, B_W, B_WR, B_WB, B_S, B_PW, B_EPI, B_DRAIN, B_COUNT };
 
-template <int DK>
+// SUMMARY: the segment's affine state map S_end = M S_start + N instead of
+// outputs.  The CTA runs the same state path on [N | M] (DK x (dv + DK))
+// from [0 | I]: slices of N see the chunk's values, slices of M see V = 0
+// (U = 0).  No Q, no P, no outputs.
+template <int DK, bool SUMMARY>
 __global__ void __launch_bounds__(kCarryThreads, 1)
 chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const CarryParams p) {
@@ -585,10 +599,14 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kMisc + 48);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int slice = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int slice = blockIdx.x, h = blockIdx.y;
+    const int b = blockIdx.z / p.nseg, seg = blockIdx.z % p.nseg;
     const int j0 = slice * DVS;
     const int T = p.T, H = p.H, dv = p.dv;
     const int nchunks = p.nchunks;
+    const int c0 = seg * p.seg_chunks;                  // first chunk of the segment
+    const int nch = min(p.seg_chunks, nchunks - c0);    // its chunks (>= 1)
+    const bool vslice = !SUMMARY || j0 < dv;            // columns that see V
     const size_t head = (size_t)b * H + h;
     Waiter wt{bars, abort_flag, p.err};
 
@@ -613,20 +631,23 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             int issued = 0;
-            for (int c = 0; c < nchunks; ++c) {
+            constexpr uint32_t kQKBytes = (SUMMARY ? 1 : 2) * KB * 8192;
+            const uint32_t bytes = kQKBytes + (vslice ? 8192u : 0u) + Rec<DK>::kBytes;
+            for (int c = 0; c < nch; ++c) {
                 const int s = c % kStages;
                 if (c >= kStages && !wt.poll(B_EMPTY0 + s, ((c / kStages) - 1) & 1, kWhereEmpty, c)) break;
                 uint8_t* st = sm + s * L::kStageBytes;
                 uint64_t* full = &bars[B_FULL0 + s];
-                mbar_arrive_expect_tx(full, L::kTmaBytes + Rec<DK>::kBytes);
-                const int t0 = c * C;
+                mbar_arrive_expect_tx(full, bytes);
+                const int cg = c0 + c;
+                const int t0 = cg * C;
 #pragma unroll
                 for (int kb = 0; kb < KB; ++kb) {
                     tma_load_4d(st + kb * 16384, &tm_k, full, kb * 64, h, t0, b);
-                    tma_load_4d(st + kb * 16384 + 8192, &tm_q, full, kb * 64, h, t0, b);
+                    if (!SUMMARY) tma_load_4d(st + kb * 16384 + 8192, &tm_q, full, kb * 64, h, t0, b);
                 }
-                tma_load_4d(st + KB * 16384, &tm_v, full, j0, h, t0, b);
-                bulk_load(st + L::kRecOff, p.rec + (head * nchunks + c) * Rec<DK>::kBytes, Rec<DK>::kBytes, full);
+                if (vslice) tma_load_4d(st + KB * 16384, &tm_v, full, j0, h, t0, b);
+                bulk_load(st + L::kRecOff, p.rec + (head * nchunks + cg) * Rec<DK>::kBytes, Rec<DK>::kBytes, full);
                 issued = c + 1;
             }
             // every issued load must land before the CTA may exit
@@ -648,31 +669,85 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         constexpr uint32_t id_qs = idesc_bf16(64, 64, false, true);
         constexpr uint32_t id_s = idesc_bf16(DK, 64, true, true);
         constexpr uint32_t id_pw = idesc_bf16(64, 64, false, true);
-        bool ok = true;
-        for (int c = 0; ok && c < nchunks; ++c) {
+        // Issue order per chunk c puts the two state-path products first:
+        //   W(c) (needs S_c), Q S_c, K^T Wt(c) (needs Wt), then work for
+        //   other chunks: Q K^T of chunk c+1 (double-buffered), P W(c), and
+        //   U of chunk c+1 (into W's accumulator, free once Wt(c) is read).
+        auto issue_qk = [&](int cc) {
+            const uint32_t sb = st0 + (cc % kStages) * L::kStageBytes;
+#pragma unroll
+            for (int k = 0; k < DK / 16; ++k) {
+                const uint32_t koff = (k / 4) * 16384 + (k % 4) * 32;
+                mma_bf16(tmem + TM_QK + (cc & 1) * TM_QK1, sdesc_sw128(sb + 8192 + koff, 16, 1024),
+                         sdesc_sw128(sb + koff, 16, 1024), id_qk, k > 0);
+            }
+            mma_commit(&bars[B_QKB + (cc & 1)]);
+        };
+        auto issue_u = [&](int cc) {
+            const uint32_t sb = st0 + (cc % kStages) * L::kStageBytes;
+            const uint32_t sTb = sb + L::kRecOff + Rec<DK>::kTb, sV = sb + KB * 16384;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16(tmem + TM_W, sdesc_sw128(sTb + k * 32, 16, 1024),
+                         sdesc_sw128(sV + k * 2048, 8192, 1024), id_u, k > 0);
+        };
+        bool ok = wt.warp(B_FULL0, 0, kWhereFull, 0);
+        if (SUMMARY) {
+            // state path only: [U(c)] W(c), K^T Wt(c); M slices start W from 0
+            if (ok && vslice) {
+                tc_fence_after();
+                if (elect_one()) issue_u(0);
+                __syncwarp();
+            }
+            for (int c = 0; ok && c < nch; ++c) {
+                const int s = c % kStages;
+                const uint32_t par = c & 1;
+                const uint32_t sb = st0 + s * L::kStageBytes;
+                const uint32_t sWk = sb + L::kRecOff + Rec<DK>::kWk;
+                if (!(ok = wt.warp(B_SR, par, kWhereSR, c))) break;
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int k = 0; k < DK / 16; ++k) {
+                        const uint32_t aoff = (k / 4) * 8192 + (k % 4) * 32;
+                        mma_bf16(tmem + TM_W, sdesc_sw128(sWk + aoff, 16, 1024),
+                                 sdesc_sw128(sSb + k * 2048, 8192, 1024), id_w, (vslice || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&bars[B_W]);
+                }
+                __syncwarp();
+                if (!(ok = wt.warp(B_WR, par, kWhereWR, c))) break;
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(tmem + TM_S, sdesc_sw128(sb + k * 2048, 16384, 1024),
+                                 sdesc_sw128(sWt + k * 2048, 8192, 1024), id_s, k > 0);
+                    mma_commit(&bars[B_S]);
+                    mma_commit(&bars[B_EMPTY0 + s]);
+                }
+                __syncwarp();
+                if (c + 1 < nch) {
+                    if (!(ok = wt.warp(B_FULL0 + (c + 1) % kStages, ((c + 1) / kStages) & 1, kWhereFull, c + 1))) break;
+                    tc_fence_after();
+                    if (vslice) {
+                        if (elect_one()) issue_u(c + 1);
+                        __syncwarp();
+                    }
+                }
+            }
+        } else {
+        if (ok) {
+            tc_fence_after();
+            if (elect_one()) { issue_qk(0); issue_u(0); }
+            __syncwarp();
+        }
+        for (int c = 0; ok && c < nch; ++c) {
             const int s = c % kStages;
             const uint32_t par = c & 1;
             const uint32_t sb = st0 + s * L::kStageBytes;
-            const uint32_t sV = sb + KB * 16384;
-            const uint32_t sTb = sb + L::kRecOff + Rec<DK>::kTb, sWk = sb + L::kRecOff + Rec<DK>::kWk;
-            // Q K^T and U = Tb V   (inputs and record of chunk c landed)
-            if (!(ok = wt.warp(B_FULL0 + s, (c / kStages) & 1, kWhereFull, c))) break;
-            tc_fence_after();
-            if (elect_one()) {
-#pragma unroll
-                for (int k = 0; k < DK / 16; ++k) {
-                    const uint32_t koff = (k / 4) * 16384 + (k % 4) * 32;
-                    mma_bf16(tmem + TM_QK, sdesc_sw128(sb + 8192 + koff, 16, 1024),
-                             sdesc_sw128(sb + koff, 16, 1024), id_qk, k > 0);
-                }
-                mma_commit(&bars[B_QKB]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_bf16(tmem + TM_W, sdesc_sw128(sTb + k * 32, 16, 1024),
-                             sdesc_sw128(sV + k * 2048, 8192, 1024), id_u, k > 0);
-            }
-            __syncwarp();
-            // W = U - Wk S0  (state path; Wk comes with the record)
+            const uint32_t sWk = sb + L::kRecOff + Rec<DK>::kWk;
+            // W = U - Wk S0  (state path)
             if (!(ok = wt.warp(B_SR, par, kWhereSR, c))) break;
             tc_fence_after();
             if (elect_one()) {
@@ -695,10 +770,9 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     mma_bf16(tmem + TM_QS, sdesc_sw128(sb + aoff, 16, 1024),
                              sdesc_sw128(sSb + k * 2048, 8192, 1024), id_qs, k > 0);
                 }
-                mma_commit(&bars[B_QS]);
             }
             __syncwarp();
-            // S_acc = K^T Wt  (state path)
+            // S_acc = K^T Wt  (state path); the stage is free once it completes
             if (!(ok = wt.warp(B_WR, par, kWhereWR, c))) break;
             tc_fence_after();
             if (elect_one()) {
@@ -707,8 +781,17 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     mma_bf16(tmem + TM_S, sdesc_sw128(sb + k * 2048, 16384, 1024),
                              sdesc_sw128(sWt + k * 2048, 8192, 1024), id_s, k > 0);
                 mma_commit(&bars[B_S]);
+                mma_commit(&bars[B_EMPTY0 + s]);
             }
             __syncwarp();
+            // Q K^T of the next chunk; its buffer was last read for P(c-1),
+            // which P W(c-1) has already waited for.
+            if (c + 1 < nch) {
+                if (!(ok = wt.warp(B_FULL0 + (c + 1) % kStages, ((c + 1) / kStages) & 1, kWhereFull, c + 1))) break;
+                tc_fence_after();
+                if (elect_one()) issue_qk(c + 1);
+                __syncwarp();
+            }
             // PW = P Wb
             if (!(ok = wt.warp(B_WB, par, kWhereWB, c))) break;
             if (!(ok = wt.warp(B_PR, par, kWherePR, c))) break;
@@ -720,9 +803,10 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     mma_bf16(tmem + TM_PW, sdesc_sw128(sPc + k * 32, 16, 1024),
                              sdesc_sw128(sWb + k * 2048, 8192, 1024), id_pw, k > 0);
                 mma_commit(&bars[B_PW]);
-                mma_commit(&bars[B_EMPTY0 + s]);
+                if (c + 1 < nch) issue_u(c + 1);
             }
             __syncwarp();
+        }
         }
         // every issued MMA must complete before TMEM is released
         if (elect_one()) {
@@ -751,11 +835,17 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             float v[32];
-            const float* src = (p.h0 && own_s) ? p.h0 + head * DK * dv + (size_t)srow * dv + j0 + 32 * half : nullptr;
+            const float* src = (!SUMMARY && p.s_in && own_s)
+                                   ? p.s_in + (((size_t)head * p.nseg + seg) * DK + srow) * dv + j0 + 32 * half
+                                   : nullptr;
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
                 const float4 v4 = src ? *reinterpret_cast<const float4*>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
                 v[j] = v4.x; v[j + 1] = v4.y; v[j + 2] = v4.z; v[j + 3] = v4.w;
+            }
+            if (SUMMARY && !vslice) {  // M columns start at the identity
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = (srow == j0 - dv + 32 * half + j) ? 1.f : 0.f;
             }
             tmem_st_32x32b_x32(tmem + lf + TM_SM + 32 * half, v);
             if (own_s) {
@@ -769,7 +859,7 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         bar_sync(1, 128);
         if (ct == 0) mbar_arrive(&bars[B_SR]);
 
-        for (int c = 0; c < nchunks; ++c) {
+        for (int c = 0; c < nch; ++c) {
             const uint32_t par = c & 1;
             const float* gam = reinterpret_cast<const float*>(sm + (c % kStages) * L::kStageBytes + L::kRecOff + Rec<DK>::kGam);
 
@@ -802,13 +892,15 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tc_fence_before();
             bar_sync(1, 128);
             if (ct == 0) mbar_arrive(&bars[B_WR]);
-            if (m64) {
+            if (!SUMMARY) {
+                if (m64) {
 #pragma unroll
-                for (int u = 0; u < 8; ++u) ST_CHUNK(Wbt, r64, u, w64, 8 * u);
+                    for (int u = 0; u < 8; ++u) ST_CHUNK(Wbt, r64, u, w64, 8 * u);
+                }
+                fence_proxy_async_smem();
+                bar_sync(1, 128);
+                if (ct == 0) mbar_arrive(&bars[B_WB]);
             }
-            fence_proxy_async_smem();
-            bar_sync(1, 128);
-            if (ct == 0) mbar_arrive(&bars[B_WB]);
 
             // ---- state update S1 = Gam_C S0 + K^T Wt: the bf16 copy for the
             // next chunk's products is published first, then the fp32 master
@@ -840,7 +932,8 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         tmem_st_wait();  // no TMEM store may be in flight when the CTA leaves
         // final state
         const bool aborted = bar_or(2, 128, *abort_flag != 0);
-        if (p.hT && !aborted) {
+        const bool write_final = SUMMARY || (p.s_out && seg == p.nseg - 1);
+        if (write_final && !aborted) {
             tc_fence_after();
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -848,34 +941,36 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 tmem_ld_32x32b_x32(tmem + lf + TM_SM + 32 * half, v);
                 tmem_ld_wait();
                 if (own_s) {
-                    float* dst = p.hT + head * DK * dv + (size_t)srow * dv + j0 + 32 * half;
+                    float* dst = SUMMARY ? p.s_out + (((size_t)head * p.nseg + seg) * DK + srow) * (dv + DK) + j0 + 32 * half
+                                         : p.s_out + ((size_t)head * DK + srow) * dv + j0 + 32 * half;
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
                         *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
                 }
             }
         }
-    } else {
+    } else if (!SUMMARY) {
         // ================================================================ aux warpgroup
         const int q = warp & 3;
         const bool m64 = lane < 16;
         const int r64 = q * 16 + lane;
         const uint32_t lf = (uint32_t)(q * 32) << 16;
         const int at = tid - 192;            // 0..127
-        for (int c = 0; c < nchunks; ++c) {
+        for (int c = 0; c < nch; ++c) {
             const uint32_t par = c & 1;
-            const int t0 = c * C;
+            const int t0 = (c0 + c) * C;
             const int nvalid = min(C, T - t0);
             const float* gam = reinterpret_cast<const float*>(sm + (c % kStages) * L::kStageBytes + L::kRecOff + Rec<DK>::kGam);
+            const float* wfac = gam + C;  // w_s = exp(gam_m - gam_s)
 
             // ---- P = mask(exp(gam_r - gam_s) Q K^T) -> bf16 tile (parity buffer)
-            if (!wt.group(B_QKB, par, kWherePR, c, 4, 128)) break;
+            if (!wt.group(B_QKB + par, (c >> 1) & 1, kWherePR, c, 4, 128)) break;
             tc_fence_after();
             float qk[64];
             {
                 float lo[32], hi[32];
-                tmem_ld_32x32b_x32(tmem + lf + TM_QK, lo);
-                tmem_ld_32x32b_x32(tmem + lf + TM_QK + 32, hi);
+                tmem_ld_32x32b_x32(tmem + lf + TM_QK + par * TM_QK1, lo);
+                tmem_ld_32x32b_x32(tmem + lf + TM_QK + par * TM_QK1 + 32, hi);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) { qk[i] = lo[i]; qk[32 + i] = hi[i]; }
@@ -886,17 +981,29 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const float gamm = gam[C / 2 - 1];
                 const bool fact = (gam[0] - gam[C - 1]) <= kSpanMax;
                 uint8_t* Pt = sm + L::kP + par * 8192;
-                const float ur = __expf(gr - gamm);
+                if (fact) {
+                    const float ur = __expf(gr - gamm);
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    float v[8];
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const float4 w0 = *reinterpret_cast<const float4*>(wfac + c8 * 8);
+                        const float4 w1 = *reinterpret_cast<const float4*>(wfac + c8 * 8 + 4);
+                        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                        float v[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int s2 = c8 * 8 + i;
-                        const float d = fact ? ur * __expf(gamm - gam[s2]) : __expf(gr - gam[s2]);
-                        v[i] = (s2 <= r64) ? d * qk[s2] : 0.f;
+                        for (int i = 0; i < 8; ++i) v[i] = (c8 * 8 + i <= r64) ? ur * wv[i] * qk[c8 * 8 + i] : 0.f;
+                        ST_CHUNK(Pt, r64, c8, v, 0);
                     }
-                    ST_CHUNK(Pt, r64, c8, v, 0);
+                } else {
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        float v[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int s2 = c8 * 8 + i;
+                            v[i] = (s2 <= r64) ? __expf(gr - gam[s2]) * qk[s2] : 0.f;
+                        }
+                        ST_CHUNK(Pt, r64, c8, v, 0);
+                    }
                 }
             }
             fence_proxy_async_smem();
@@ -936,6 +1043,56 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ============================================================================
+// segment_combine_kernel: the sequential pass over segment maps.  For each
+// head, S_start[0] = h0 (or 0) and S_start[j+1] = M_j S_start[j] + N_j, where
+// [N_j | M_j] (DK x (dv + DK)) is segment j's summary.  fp32 on CUDA cores;
+// one CTA per (16-column block, head), thread (i, half) owns row i and eight
+// columns.  M_j is staged in shared memory (rows padded to DK + 1 floats).
+// ============================================================================
+template <int DK>
+__global__ void __launch_bounds__(2 * DK)
+segment_combine_kernel(const float* __restrict__ X, const float* __restrict__ h0,
+                       float* __restrict__ S_start, int H, int nseg, int dv) {
+    extern __shared__ float csm[];
+    float* Ms = csm;                      // [DK][DK + 1]
+    float* Ss = csm + DK * (DK + 1);      // [DK][16]
+    const int col0 = blockIdx.x * 16, h = blockIdx.y, b = blockIdx.z;
+    const size_t head = (size_t)b * H + h;
+    const int tid = threadIdx.x, i = tid >> 1, cb = (tid & 1) * 8;
+    const int ldx = dv + DK;
+    float sv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sv[j] = h0 ? h0[(head * DK + i) * dv + col0 + cb + j] : 0.f;
+    for (int seg = 0;; ++seg) {
+        float* dst = S_start + ((head * nseg + seg) * DK + i) * dv + col0 + cb;
+        *reinterpret_cast<float4*>(dst) = make_float4(sv[0], sv[1], sv[2], sv[3]);
+        *reinterpret_cast<float4*>(dst + 4) = make_float4(sv[4], sv[5], sv[6], sv[7]);
+        if (seg == nseg - 1) break;
+        const float* Xs = X + (head * nseg + seg) * DK * (size_t)ldx;
+        __syncthreads();  // the previous step's reads of Ms and Ss are done
+        for (int e = tid; e < DK * DK; e += 2 * DK) Ms[(e / DK) * (DK + 1) + e % DK] = Xs[(e / DK) * (size_t)ldx + dv + e % DK];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) Ss[i * 16 + cb + j] = sv[j];
+        __syncthreads();
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = Xs[(size_t)i * ldx + col0 + cb + j];
+#pragma unroll 4
+        for (int kk = 0; kk < DK; ++kk) {
+            const float m = Ms[i * (DK + 1) + kk];
+            const float4 s0 = *reinterpret_cast<const float4*>(&Ss[kk * 16 + cb]);
+            const float4 s1 = *reinterpret_cast<const float4*>(&Ss[kk * 16 + cb + 4]);
+            acc[0] = fmaf(m, s0.x, acc[0]); acc[1] = fmaf(m, s0.y, acc[1]);
+            acc[2] = fmaf(m, s0.z, acc[2]); acc[3] = fmaf(m, s0.w, acc[3]);
+            acc[4] = fmaf(m, s1.x, acc[4]); acc[5] = fmaf(m, s1.y, acc[5]);
+            acc[6] = fmaf(m, s1.z, acc[6]); acc[7] = fmaf(m, s1.w, acc[7]);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sv[j] = acc[j];
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -969,20 +1126,28 @@ bool make_map(CUtensorMap* map, const void* base, int B, int T, int H, int D) {
 template <int DK>
 cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* g, const float* eta,
                       float eps, const float* h0, void* o, float* hT, int B, int T, int H, int dv,
-                      DeviceErrorRecord* err, uint8_t* rec, cudaStream_t stream) {
+                      DeviceErrorRecord* err, uint8_t* rec, int nseg, int seg_chunks, float* seg_x,
+                      float* seg_start, cudaStream_t stream) {
     CUtensorMap mq, mk, mv;
     if (!make_map(&mq, q, B, T, H, DK) || !make_map(&mk, k, B, T, H, DK) ||
         !make_map(&mv, v, B, T, H, dv))
         return cudaErrorInvalidValue;
     auto prep = chunk_prep_kernel<DK>;
-    auto carry = chunk_carry_kernel<DK>;
+    auto carry = chunk_carry_kernel<DK, false>;
+    auto summary = chunk_carry_kernel<DK, true>;
+    auto combine = segment_combine_kernel<DK>;
     const size_t smem_prep = PrepLayout<DK>::kSmemBytes, smem_carry = CarryLayout<DK>::kSmemBytes;
+    const size_t smem_comb = sizeof(float) * (DK * (DK + 1) + DK * 16);
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_prep);
         if (attr_err == cudaSuccess)
             attr_err = cudaFuncSetAttribute(carry, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_carry);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(summary, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_carry);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_comb);
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int nchunks = (T + C - 1) / C;
@@ -990,8 +1155,21 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
     prep<<<dim3(nchunks, H, B), kPrepThreads, smem_prep, stream>>>(mk, pp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    CarryParams cp{h0, rec, reinterpret_cast<__nv_bfloat16*>(o), hT, err, T, H, dv, nchunks};
-    carry<<<dim3(dv / DVS, H, B), kCarryThreads, smem_carry, stream>>>(mq, mk, mv, cp);
+    auto* ob = reinterpret_cast<__nv_bfloat16*>(o);
+    if (nseg == 1) {
+        CarryParams cp{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks};
+        carry<<<dim3(dv / DVS, H, B), kCarryThreads, smem_carry, stream>>>(mq, mk, mv, cp);
+        return cudaGetLastError();
+    }
+    // chunk-level scan: segment summaries, the sequential combine, then each
+    // segment's outputs from its true start state
+    CarryParams c1{nullptr, rec, nullptr, seg_x, err, T, H, dv, nchunks, nseg, seg_chunks};
+    summary<<<dim3((dv + DK) / DVS, H, B * nseg), kCarryThreads, smem_carry, stream>>>(mq, mk, mv, c1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    combine<<<dim3(dv / 16, H, B), 2 * DK, smem_comb, stream>>>(seg_x, h0, seg_start, H, nseg, dv);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    CarryParams c3{seg_start, rec, ob, hT, err, T, H, dv, nchunks, nseg, seg_chunks};
+    carry<<<dim3(dv / DVS, H, B * nseg), kCarryThreads, smem_carry, stream>>>(mq, mk, mv, c3);
     return cudaGetLastError();
 }
 
@@ -1002,13 +1180,43 @@ size_t chunk_fwd_tc_record_bytes(int B, int T, int H, int dk) {
     return (size_t)B * H * nchunks * (dk == 128 ? Rec<128>::kBytes : Rec<64>::kBytes);
 }
 
+ScanShape chunk_fwd_tc_scan_shape(int T, int segments) {
+    const int nchunks = (T + C - 1) / C;
+    ScanShape sh{1, nchunks > 0 ? nchunks : 1};
+    if (segments <= 1 || nchunks <= 1) return sh;
+    sh.seg_chunks = (nchunks + segments - 1) / segments;
+    sh.nseg = (nchunks + sh.seg_chunks - 1) / sh.seg_chunks;
+    if (sh.nseg == 1) sh.seg_chunks = nchunks;
+    return sh;
+}
+
+size_t chunk_fwd_tc_scan_bytes(int B, int H, int dk, int dv, int nseg) {
+    if (nseg <= 1) return 0;
+    return sizeof(float) * (size_t)B * H * nseg * dk * ((size_t)(dv + dk) + dv);
+}
+
+int chunk_fwd_tc_auto_segments(int B, int T, int H, int dk, int dv) {
+    const int nchunks = (T + C - 1) / C;
+    const long long base = (long long)B * H * (dv / DVS);        // carry CTAs without a scan
+    if (base * 2 > kScanTargetCtas) return 1;
+    const long long per_seg = (long long)B * H * ((dv + dk) / DVS);  // summary CTAs per segment
+    long long nseg = kScanTargetCtas / per_seg;
+    if (nseg > nchunks / kScanMinSegChunks) nseg = nchunks / kScanMinSegChunks;
+    return nseg > 1 ? (int)nseg : 1;
+}
+
 cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, const float* g,
                                 const float* eta, float eps, const float* h0, void* o, float* hT,
-                                int B, int T, int H, int dk, int dv, DeviceErrorRecord* err,
-                                uint8_t* records, cudaStream_t stream) {
+                                int B, int T, int H, int dk, int dv, int segments,
+                                DeviceErrorRecord* err, uint8_t* records, cudaStream_t stream) {
+    const ScanShape sh = chunk_fwd_tc_scan_shape(T, segments);
+    float* seg_x = reinterpret_cast<float*>(records + chunk_fwd_tc_record_bytes(B, T, H, dk));
+    float* seg_start = seg_x + (size_t)B * H * sh.nseg * dk * (dv + dk);
     if (dk == 128)
-        return launch_dk<128>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, err, records, stream);
-    return launch_dk<64>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, err, records, stream);
+        return launch_dk<128>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, err, records, sh.nseg,
+                              sh.seg_chunks, seg_x, seg_start, stream);
+    return launch_dk<64>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, err, records, sh.nseg,
+                         sh.seg_chunks, seg_x, seg_start, stream);
 }
 
 }  // namespace kla

@@ -50,12 +50,29 @@ cudaError_t launch_chunk_fwd_simt(const void* q, const void* k, const void* v, c
 // Chunkwise prefill on the tensor cores (tcgen05 + TMA + TMEM), bf16 I/O,
 // dk, dv in {64,128}, chunk 64 (kla_chunk_tc.cu): a prep kernel over every
 // (chunk, head) writes per-chunk records to `records` (chunk_fwd_tc_record_bytes
-// bytes), then the carry kernel walks the chunks of each head.  `err` is the
-// device error record at the start of the caller's workspace.
+// bytes), then the carry kernel walks the chunks of each head.  With
+// `segments` > 1 the chunks of each head are split into segments (the
+// chunk-level scan): a summary pass gives each segment's affine state map, a
+// sequential combine gives each segment's start state, and the carry kernel
+// then runs every segment in parallel.  The scan's buffers
+// (chunk_fwd_tc_scan_bytes) follow the records.  `err` is the device error
+// record at the start of the caller's workspace.
+struct ScanShape {
+    int nseg;        // segments per head
+    int seg_chunks;  // chunks per segment (the last one may hold fewer)
+};
+// GB300 SM count the automatic segment count aims to fill, and the shortest
+// segment it makes.
+constexpr int kScanTargetCtas = 152;
+constexpr int kScanMinSegChunks = 32;
+
 cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, const float* g,
                                 const float* eta, float eps, const float* h0, void* o, float* hT,
-                                int B, int T, int H, int dk, int dv, DeviceErrorRecord* err,
-                                uint8_t* records, cudaStream_t stream);
+                                int B, int T, int H, int dk, int dv, int segments,
+                                DeviceErrorRecord* err, uint8_t* records, cudaStream_t stream);
 size_t chunk_fwd_tc_record_bytes(int B, int T, int H, int dk);
+ScanShape chunk_fwd_tc_scan_shape(int T, int segments);
+size_t chunk_fwd_tc_scan_bytes(int B, int H, int dk, int dv, int nseg);
+int chunk_fwd_tc_auto_segments(int B, int T, int H, int dk, int dv);
 
 }  // namespace kla

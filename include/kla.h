@@ -64,10 +64,12 @@ typedef enum kla_io_dtype {
 
 /*
  * Bytes of device workspace kla_chunk_fwd needs for this problem: 256 bytes
- * of device error record, plus, with bf16 I/O, one 16,640-byte record per
- * (batch, head, 64-token chunk) that carries the chunk's state-independent
- * operands from the first kernel to the second.  Returns 0 if the arguments
- * are invalid or unsupported.
+ * of device error record, plus, with bf16 I/O, one record of
+ * 8704 + 128*dk bytes (25,088 for dk = 128) per (batch, head, 64-token
+ * chunk) that carries the chunk's state-independent operands from the first
+ * kernel to the second, plus the chunk-level scan's buffers when the
+ * automatic segment count (kla_chunk_fwd_auto_segments) is above 1.
+ * Returns 0 if the arguments are invalid or unsupported.
  */
 KLA_API size_t kla_chunk_fwd_workspace_bytes(int B, int T, int H, int dk, int dv,
                                      int chunk, kla_io_dtype io);
@@ -105,6 +107,52 @@ KLA_API kla_status kla_chunk_fwd(const void* q, const void* k, const void* v,
                          void* stream);
 
 /*
+ * Chunk-level scan.  Over one chunk the state update is affine in the
+ * chunk's start state: S_end = M S_start + N with M (dk x dk) and N
+ * (dk x dv) independent of S_start, and such maps compose associatively.
+ * "Kernelized Linear Attention" (gist.science/ko/paper/2607.17419), section
+ * 2.3, carries the inter-chunk state with an associative scan, and "Higher-
+ * order Linear Attention" (gist.science/ko/paper/2510.27258), section 4,
+ * shows that a scan over segment summaries reproduces the serial
+ * recurrence exactly; here that is applied to the KLA map above.
+ *
+ * kla_chunk_fwd_scan splits the chunks of every head into `segments` runs of
+ * consecutive chunks.  It forms every run's map [N | M] in parallel (the
+ * chunk recurrence started from [0 | I]), walks the runs of each head in
+ * order once to get each run's true start state (S_0 = h0,
+ * S_{j+1} = M_j S_j + N_j, fp32), then forms every run's outputs in
+ * parallel from its start state.  The result equals kla_chunk_fwd's up to
+ * rounding order.
+ *
+ *  segments : 0 = the count kla_chunk_fwd would use (automatic); 1 = no
+ *             scan; larger values are reduced so that every run holds at
+ *             least one chunk.  With fp32 I/O only 0 and 1 are supported
+ *             (KLA_ERR_UNSUPPORTED otherwise).
+ *  Every other argument as in kla_chunk_fwd; the workspace must hold
+ *  kla_chunk_fwd_scan_workspace_bytes(..., segments) bytes: kla_chunk_fwd's
+ *  plus, when more than one run is used, B*H*runs*dk*(2*dv + dk)*4 bytes for
+ *  the runs' maps and start states.
+ */
+KLA_API size_t kla_chunk_fwd_scan_workspace_bytes(int B, int T, int H, int dk, int dv,
+                                                  int chunk, kla_io_dtype io, int segments);
+
+KLA_API kla_status kla_chunk_fwd_scan(const void* q, const void* k, const void* v,
+                                      const float* g, const float* eta, float eps,
+                                      const float* h0, void* o, float* hT,
+                                      int B, int T, int H, int dk, int dv, int chunk,
+                                      kla_io_dtype io, int segments, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
+/*
+ * Segment count kla_chunk_fwd uses for this shape (1 = no scan): with bf16
+ * I/O, when the heads' carry work fills less than half of a GB300's 152
+ * SMs, enough runs of at least 32 chunks to fill them; otherwise 1.
+ * Returns 0 if the arguments are invalid or unsupported.
+ */
+KLA_API int kla_chunk_fwd_auto_segments(int B, int T, int H, int dk, int dv, int chunk,
+                                        kla_io_dtype io);
+
+/*
  * One recurrent decode step for B*H heads (the same recurrence with T = 1;
  * the page's section "Efficiency" reports decode throughput for this step).
  * The state is read once and written once, in place.
@@ -130,9 +178,9 @@ KLA_API kla_status kla_decode_step(const void* q, const void* k, const void* v,
  * Same arguments, semantics and errors as kla_chunk_fwd, without the
  * workspace: the scratch lives in a 16 MiB array built into the library,
  * held on every GPU that loads it until the process exits.  Problems whose
- * kla_chunk_fwd_workspace_bytes exceeds 16 MiB (with bf16 I/O, more than
- * about a thousand (batch, head, 64-token chunk) triples) are rejected with
- * KLA_ERR_WORKSPACE.  No device memory is allocated.
+ * kla_chunk_fwd_workspace_bytes exceeds 16 MiB (with bf16 I/O and dk = 128,
+ * more than about 650 (batch, head, 64-token chunk) triples) are rejected
+ * with KLA_ERR_WORKSPACE.  No device memory is allocated.
  *  - The first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
  *  - Every call shares the array and it keeps the last call's contents; the

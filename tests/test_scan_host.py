@@ -1,0 +1,59 @@
+"""Host-side logic of the chunk-level scan: the automatic run count, the
+workspace it needs and the argument checks (no GPU work)."""
+import pytest
+
+import kla_inputs
+
+
+def _kla():
+    import chunked_delta_rule_kla_gb300 as kla
+    try:
+        kla.load_library()
+    except RuntimeError as e:
+        pytest.skip(str(e))
+    return kla
+
+
+def test_auto_segments_policy():
+    kla = _kla()
+    L, Tr = kla_inputs.LONG, kla_inputs.TRAIN
+    # long context, 16 heads: the carry alone would fill 32 of 152 SMs -> scan
+    assert kla.kla_chunk_fwd_auto_segments(L.B, L.T, L.H, L.dk, L.dv) > 1
+    # training shape, 64 heads x 2 column slices: enough parallelism already
+    assert kla.kla_chunk_fwd_auto_segments(Tr.B, Tr.T, Tr.H, Tr.dk, Tr.dv) == 1
+    # short sequences are never split below 32 chunks per run
+    assert kla.kla_chunk_fwd_auto_segments(1, 64 * 63, 1, 128, 128) == 1
+    assert kla.kla_chunk_fwd_auto_segments(1, 64 * 64, 1, 128, 128) == 2
+    # fp32 I/O has no scan; invalid shapes give 0
+    assert kla.kla_chunk_fwd_auto_segments(1, 1 << 17, 1, 128, 128, io=kla.KLA_IO_FP32) == 1
+    assert kla.kla_chunk_fwd_auto_segments(1, 1024, 1, 96, 128) == 0
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128)])
+def test_scan_workspace_formula(dk, dv):
+    kla = _kla()
+    B, T, H = 2, 1000, 3
+    nchunks = -(-T // 64)
+    base = kla.kla_chunk_fwd_scan_workspace_bytes(B, T, H, dk, dv, segments=1)
+    rec = 8192 + 64 * dk * 2 + 512
+    assert base == 256 + B * H * nchunks * rec
+    for segments in (2, 3, 5, 16, 40):
+        seg_chunks = -(-nchunks // segments)
+        nseg = -(-nchunks // seg_chunks)
+        n = kla.kla_chunk_fwd_scan_workspace_bytes(B, T, H, dk, dv, segments=segments)
+        assert n == base + B * H * nseg * dk * (2 * dv + dk) * 4
+        assert n % 256 == 0
+    assert kla.kla_chunk_fwd_workspace_bytes(B, T, H, dk, dv) == base  # auto = 1 here
+
+
+def test_scan_argument_errors():
+    kla = _kla()
+    lib = kla.load_library()
+    args = [None] * 5 + [1e-6, None, None, None]
+    # fp32 I/O supports no segmentation
+    rc = lib.kla_chunk_fwd_scan(*args, 1, 128, 1, 128, 128, 64, kla.KLA_IO_FP32, 2, None, 0, None)
+    assert rc == kla.KLA_ERR_UNSUPPORTED
+    rc = lib.kla_chunk_fwd_scan(*args, 1, 128, 1, 128, 128, 64, kla.KLA_IO_BF16, -1, None, 0, None)
+    assert rc == kla.KLA_ERR_INVALID_ARG
+    assert kla.kla_chunk_fwd_scan_workspace_bytes(1, 128, 1, 128, 128, io=kla.KLA_IO_FP32, segments=2) == 0
+    assert kla.kla_chunk_fwd_scan_workspace_bytes(1, 128, 1, 128, 128, segments=-1) == 0
