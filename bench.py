@@ -163,26 +163,51 @@ def timed_steps(step, K, W, flush_buf, stream):
     return [a.elapsed_time(b) for a, b in evs]  # ms
 
 
+def _dist_on() -> bool:
+    return torch.distributed.is_available() and torch.distributed.is_initialized()
+
+
 def barrier():
-    if torch.distributed.is_available() and torch.distributed.is_initialized():
+    if _dist_on():
         torch.distributed.barrier()
 
 
+def world_size() -> int:
+    return torch.distributed.get_world_size() if _dist_on() else 1
+
+
 def max_over_ranks(x: float) -> float:
-    if torch.distributed.is_available() and torch.distributed.is_initialized():
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    """Largest x over the ranks (x itself without a process group).  NCCL
+    reduces a device tensor, gloo a host tensor."""
+    if _dist_on():
+        dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         return float(t.item())
     return x
 
 
+def job_throughput(units_per_rank: float, local_seconds: float) -> tuple[float, float]:
+    """Whole-job rate for replicas that each process `units_per_rank` units:
+    the units of all ranks divided by the slowest rank's time.  Returns
+    (units/s over the job, that slowest time in seconds)."""
+    slowest = max_over_ranks(local_seconds)
+    return units_per_rank * world_size() / slowest, slowest
+
+
 # ------------------------------------------------------------- native arm
 
-# Kernels of ours launched per ABI call, by dispatch: kla_chunk_fwd launches
-# one prefill kernel (plus a 256-byte cudaMemsetAsync of the error record,
-# not a kernel of ours); kla_decode_step launches one kernel.
-LAUNCHES_PER_PREFILL = 1
+# Kernels of ours launched per ABI call.  kla_chunk_fwd: chunk_prep_kernel
+# and chunk_carry_kernel, or, when it splits the chunks into runs (the
+# chunk-level scan), chunk_prep_kernel, the summary pass, the combine and
+# chunk_carry_kernel; plus a 256-byte cudaMemsetAsync of the error record
+# (not a kernel of ours).  kla_decode_step launches one kernel.
 LAUNCHES_PER_DECODE = 1
+
+
+def prefill_launches(kla, case) -> int:
+    segs = kla.kla_chunk_fwd_auto_segments(case.B, case.T, case.H, case.dk, case.dv, case.chunk)
+    return 2 if segs == 1 else 4
 
 
 def bench_prefill(case, K, W, flush, peaks, stream, e2e=True):
@@ -202,12 +227,15 @@ def bench_prefill(case, K, W, flush, peaks, stream, e2e=True):
     barrier()
     assert kla.kla_workspace_check(ws, stream) == kla.KLA_OK
     work = prefill_work(case)
-    mean_ms = max_over_ranks(sum(ms) / len(ms))
+    job_tps, slowest_s = job_throughput(work["tokens"], sum(ms) / len(ms) * 1e-3)
+    mean_ms = slowest_s * 1e3
     res = dict(ms_per_step=mean_ms, tokens_per_s=work["tokens"] / (mean_ms * 1e-3),
+               job_tokens_per_s=job_tps,
                tflops=work["flops"] / (mean_ms * 1e-3) / 1e12,
                gbps=work["bytes"] / (mean_ms * 1e-3) / 1e9,
                roofline=roofline(work, mean_ms * 1e-3, peaks), work=work,
-               launches=K * LAUNCHES_PER_PREFILL, min_ms=min(ms))
+               launches=K * prefill_launches(kla, case), min_ms=min(ms),
+               segments=kla.kla_chunk_fwd_auto_segments(B, T, H, dk, dv, case.chunk))
 
     if not e2e:
         del inp, o, hT
@@ -235,10 +263,10 @@ def bench_prefill(case, K, W, flush, peaks, stream, e2e=True):
     for _ in range(Ke):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_s = max_over_ranks((time.perf_counter() - t0) / Ke)
+    e2e_job, e2e_s = job_throughput(work["tokens"], (time.perf_counter() - t0) / Ke)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = o_h.numel() * o_h.element_size() + h_h.numel() * h_h.element_size()
-    res["e2e"] = dict(value=work["tokens"] / e2e_s, unit="tokens/s", h2d_bytes_per_step=h2d,
+    res["e2e"] = dict(value=e2e_job, unit="tokens/s", h2d_bytes_per_step=h2d,
                       d2h_bytes_per_step=d2h, ms_per_step=e2e_s * 1e3, steps=Ke)
     del inp, o, hT, host, dev
     return res
@@ -403,7 +431,7 @@ def main():
         return
     n = world
     line = dict(
-        metric=METRIC, value=head["tokens_per_s"] * n, unit="tokens/s", n_gpus=n,
+        metric=METRIC, value=head["job_tokens_per_s"], unit="tokens/s", n_gpus=n,
         steps=args.steps, warmup=args.warmup, ms_per_step=head["ms_per_step"],
         higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
         data="synthetic",
@@ -413,7 +441,7 @@ def main():
                     parallelism=f"replicas x{n}" if n > 1 else "single GPU"),
         tflops=head["tflops"], hbm_gbs_algorithmic=head["gbps"],
         roofline=head["roofline"],
-        e2e=dict(head["e2e"], value=head["e2e"]["value"] * n) if "e2e" in head else None,
+        e2e=head.get("e2e"),
         gpu_launches=head["launches"], clocks=clk, secondary=secondary,
     )
     if not args.no_cpu_baseline:
