@@ -65,15 +65,17 @@ constexpr float kSpanMax = 80.f;                 // largest decay span factorise
 
 // Workspace record of one (b, h, chunk): the swizzled bf16 operand tiles
 // T diag(beta) (64x64) and Wk = T diag(beta Gam) K (64 x dk, as 64-column
-// boxes), then the decay cumsum gam (64 floats) and the decay factors
-// w_s = exp(gam_m - gam_s) about the chunk's middle token m (64 floats).
+// boxes), then three float[64] vectors: the decay cumsum gam, the decay
+// factors w_s = exp(gam_m - gam_s) about the chunk's middle token m, and
+// sc_r = exp(gam_C - gam_r), the decay from token r to the chunk's end.
 template <int DK>
 struct Rec {
     static constexpr uint32_t kTb = 0;
     static constexpr uint32_t kWk = 8192;
     static constexpr uint32_t kGam = kWk + (DK / 64) * 8192;
     static constexpr uint32_t kWf = kGam + 256;
-    static constexpr uint32_t kBytes = kWf + 256;
+    static constexpr uint32_t kSc = kWf + 256;
+    static constexpr uint32_t kBytes = kSc + 256;
 };
 
 enum : unsigned { kWhereFull = 1, kWhereEmpty, kWhereGQ, kWhereT, kWhereWK, kWhereWKR, kWhereSR,
@@ -170,9 +172,10 @@ struct PrepLayout {
                                                                                : kX + Rec<DK>::kGam;
     static constexpr uint32_t kRw = kXEnd;                     // fp32 [32][LDF]
     static constexpr uint32_t kAdT = kRw + 32 * LDF * 4;       // fp32 4 x [16][16]
-    static constexpr uint32_t kGam = kAdT + 4 * 256 * 4;       // gam[64], w[64] (record tail)
+    static constexpr uint32_t kGam = kAdT + 4 * 256 * 4;       // gam[64], w[64], sc[64] (record tail)
     static constexpr uint32_t kWf = kGam + 256;
-    static constexpr uint32_t kBet = kWf + 256;                // beta[64], betg[64]
+    static constexpr uint32_t kSc = kWf + 256;
+    static constexpr uint32_t kBet = kSc + 256;                // beta[64], betg[64]
     static constexpr uint32_t kMisc = kBet + 2 * 256;
     static constexpr uint32_t kBars = kMisc + 64;
     static constexpr uint32_t kEnd = kBars + 4 * 8;
@@ -323,7 +326,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
                 betg[r] = br * __expf(gr);
             }
             const float gamm = gam[C / 2 - 1];
-            if (pt < C) wf[pt] = __expf(gamm - gam[pt]);
+            if (pt < C) {
+                wf[pt] = __expf(gamm - gam[pt]);
+                reinterpret_cast<float*>(sm + L::kSc)[pt] = __expf(gam[C - 1] - gam[pt]);
+            }
             bar_sync(1, 128);
             const bool fact = (gam[0] - gam[C - 1]) <= kSpanMax;
             // ---- A rows (64 threads) and the transposed diagonal blocks
@@ -513,7 +519,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
         if (pt == 0) {
             uint8_t* dst = p.rec + (((size_t)b * H + h) * p.nchunks + c) * Rec<DK>::kBytes;
             bulk_store(dst, sm + L::kX, Rec<DK>::kGam);
-            bulk_store(dst + Rec<DK>::kGam, sm + L::kGam, 512);
+            bulk_store(dst + Rec<DK>::kGam, sm + L::kGam, 768);
             bulk_commit();
             bulk_wait_all();
         }
@@ -772,7 +778,7 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 }
             }
             __syncwarp();
-            // S_acc = K^T Wt  (state path); the stage is free once it completes
+            // S_acc = K^T Wt  (state path)
             if (!(ok = wt.warp(B_WR, par, kWhereWR, c))) break;
             tc_fence_after();
             if (elect_one()) {
@@ -781,7 +787,6 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     mma_bf16(tmem + TM_S, sdesc_sw128(sb + k * 2048, 16384, 1024),
                              sdesc_sw128(sWt + k * 2048, 8192, 1024), id_s, k > 0);
                 mma_commit(&bars[B_S]);
-                mma_commit(&bars[B_EMPTY0 + s]);
             }
             __syncwarp();
             // Q K^T of the next chunk; its buffer was last read for P(c-1),
@@ -803,6 +808,9 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     mma_bf16(tmem + TM_PW, sdesc_sw128(sPc + k * 32, 16, 1024),
                              sdesc_sw128(sWb + k * 2048, 8192, 1024), id_pw, k > 0);
                 mma_commit(&bars[B_PW]);
+                // the stage is free: every MMA reading it is issued, and the
+                // aux warps have read the chunk's decay vectors (P(c) is built)
+                mma_commit(&bars[B_EMPTY0 + s]);
                 if (c + 1 < nch) issue_u(c + 1);
             }
             __syncwarp();
@@ -1044,6 +1052,530 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 }
 
 // ============================================================================
+// chunk_state_kernel: the carry for d_k = d_v = 128, one CTA per (head, run),
+// with the state held transposed: TMEM lane j holds column j of S, so every
+// state product is an M = 128 tcgen05 MMA whose A operand (S0^T, Wt^T, Wb^T)
+// is written to TMEM as bf16 by the state warps and read from there.
+//
+//   [-U^T | 0]                 = -(V^T [Tb ; 0]^T)        A = V^T (smem, MN-major)
+//   [-W^T | S0^T Q^T]         += S0^T [Wk ; Q]^T          one N = 128 product
+//   S_acc                      = Wt^T K,   Wt = diag(exp(gam_C - gam_r)) W
+//   S1^T                       = Gam_C S0^T + S_acc       (fp32 master in registers)
+//   o_r                        = Gam_r (S0^T Q^T)[., r] + (Wb^T P^T)[., r]
+//
+// Roles (14 warps):
+//   warps 0..3   aux: P from Q K^T; the S0^T Q^T half read out early; the
+//                outputs (TMEM -> swizzled smem tile -> TMA store)
+//   warps 4..11  state: -W^T -> bf16 Wt^T (the chain) and Wb^T; the update
+//   warp 12      TMA producer (K, [Wk ; Q], V, [Tb ; 0], the record's vectors)
+//   warp 13      owns TMEM; issues the MMAs from a polling scheduler that
+//                puts the two state-path products first
+// SUMMARY: the run's affine map instead of outputs.  blockIdx.x = 0 carries
+// N (the values enter), blockIdx.x = 1 carries M (V = 0, start at I).
+// ============================================================================
+constexpr int kStateThreads = 448;
+
+// TMEM columns
+constexpr uint32_t TS_D = 0;       // [-W^T | S0^T Q^T] (fp32, M=128 N=128)
+constexpr uint32_t TS_QK = 128;    // Q K^T (fp32, M=64 N=64)
+constexpr uint32_t TS_WTB = 192;   // Wt^T (bf16 pairs, 32 columns)
+constexpr uint32_t TS_WBB = 224;   // Wb^T (bf16 pairs)
+constexpr uint32_t TS_S0B = 256;   // S0^T (bf16 pairs, 64 columns)
+constexpr uint32_t TS_SA = 320;    // S_acc (fp32, M=128 N=128)
+constexpr uint32_t TS_PW = 448;    // Wb^T P^T (fp32, M=128 N=64)
+
+struct StateLayout {
+    // one stage; rows of every tile are tokens, 128-byte swizzle
+    static constexpr uint32_t kK = 0;         // K boxes (d 0..63, 64..127)
+    static constexpr uint32_t kWQ = 16384;    // [Wk box kb | Q box kb] at kWQ + 16384 kb
+    static constexpr uint32_t kV = 49152;     // V boxes
+    static constexpr uint32_t kTZ = 65536;    // [T diag(beta) | zeros]
+    static constexpr uint32_t kVec = 81920;   // gam, w, sc (float[64] each)
+    static constexpr uint32_t kStageBytes = ((kVec + 768 + 1023) / 1024) * 1024;
+    static constexpr uint32_t kP = 2 * kStageBytes;       // 2 x [64][64] bf16 (chunk parity)
+    static constexpr uint32_t kO = kP + 2 * 8192;         // 2 x 2 boxes [64 tok][64] bf16
+    static constexpr uint32_t kG = kO + 2 * 16384;        // 2 x 64 floats: Gam_r for the epilogue
+    static constexpr uint32_t kMisc = kG + 512;
+    static constexpr uint32_t kBars = kMisc + 64;
+    static constexpr uint32_t kEnd = kBars + 32 * 8;
+    static constexpr size_t kSmemBytes = kEnd + 1024;
+};
+
+enum { SB_FULL0 = 0, SB_EMPTY0 = SB_FULL0 + kStages, SB_QKB = SB_EMPTY0 + kStages, SB_PR, SB_SR, SB_W,
+       SB_WCT, SB_WCB, SB_QSR, SB_S, SB_PW, SB_DRAIN, SB_COUNT };
+
+template <bool SUMMARY>
+__global__ void __launch_bounds__(kStateThreads, 1)
+chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const CarryParams p) {
+    using L = StateLayout;
+    using R = Rec<128>;
+    constexpr int DK = 128;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 32);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kMisc + 48);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.y;
+    const int b = blockIdx.z / p.nseg, seg = blockIdx.z % p.nseg;
+    const bool vhalf = !SUMMARY || blockIdx.x == 0;     // the values enter this state
+    const int T = p.T, H = p.H, dv = p.dv;
+    const int nchunks = p.nchunks;
+    const int c0 = seg * p.seg_chunks;
+    const int nch = min(p.seg_chunks, nchunks - c0);
+    const size_t head = (size_t)b * H + h;
+    Waiter wt{bars, abort_flag, p.err};
+
+    if (tid == 0) {
+        for (int i = 0; i < SB_COUNT; ++i) mbar_init(&bars[i], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (!SUMMARY) {  // the zero halves of [T diag(beta) | 0], never loaded
+        for (int i = tid; i < kStages * 2048; i += kStateThreads) {
+            const int s = i / 2048, e = i % 2048;
+            reinterpret_cast<uint32_t*>(sm + s * L::kStageBytes + L::kTZ + 8192)[e] = 0u;
+        }
+        fence_proxy_async_smem();
+    }
+    if (warp == 13) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 12) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_k);
+            if (!SUMMARY) tma_prefetch_desc(&tm_q);
+            if (vhalf) tma_prefetch_desc(&tm_v);
+            const uint32_t bytes = 16384u + (SUMMARY ? 0u : 16384u) + (vhalf ? 16384u : 0u) + 8192u + 16384u + 768u;
+            int issued = 0;
+            for (int c = 0; c < nch; ++c) {
+                const int s = c % kStages;
+                if (c >= kStages && !wt.poll(SB_EMPTY0 + s, ((c / kStages) - 1) & 1, kWhereEmpty, c)) break;
+                uint8_t* st = sm + s * L::kStageBytes;
+                uint64_t* full = &bars[SB_FULL0 + s];
+                mbar_arrive_expect_tx(full, bytes);
+                const int cg = c0 + c;
+                const int t0 = cg * C;
+                const uint8_t* rec = p.rec + (head * nchunks + cg) * R::kBytes;
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+                    tma_load_4d(st + L::kK + kb * 8192, &tm_k, full, kb * 64, h, t0, b);
+                    if (!SUMMARY) tma_load_4d(st + L::kWQ + kb * 16384 + 8192, &tm_q, full, kb * 64, h, t0, b);
+                    if (vhalf) tma_load_4d(st + L::kV + kb * 8192, &tm_v, full, kb * 64, h, t0, b);
+                    bulk_load(st + L::kWQ + kb * 16384, rec + R::kWk + kb * 8192, 8192, full);
+                }
+                bulk_load(st + L::kTZ, rec + R::kTb, 8192, full);
+                bulk_load(st + L::kVec, rec + R::kGam, 768, full);
+                issued = c + 1;
+            }
+            for (int c = (issued > kStages ? issued - kStages : 0); c < issued; ++c) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait_sleep(&bars[SB_FULL0 + c % kStages], (c / kStages) & 1, kSuspendNs)) {
+                    if (globaltimer_ns() - t0 > kTimeoutNs) { wt.fail(kWhereFull, c); break; }
+                }
+            }
+        }
+    } else if (warp == 13) {
+        // ================================================================ MMA schedule
+        const uint32_t st0 = smem_u32(sm), sP = smem_u32(sm + L::kP);
+        constexpr int NW = SUMMARY ? 64 : 128;   // [Wk ; Q] rows
+        constexpr uint32_t id_u = idesc_bf16(128, NW, true, false, true);   // -(V^T [Tb ; 0]^T)
+        constexpr uint32_t id_w = idesc_bf16(128, NW, false, false);        // S0^T [Wk ; Q]^T
+        constexpr uint32_t id_s = idesc_bf16(128, 128, false, true);        // Wt^T K
+        constexpr uint32_t id_pw = idesc_bf16(128, 64, false, false);       // Wb^T P^T
+        constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);
+        auto stage = [&](int cc) { return st0 + (cc % kStages) * L::kStageBytes; };
+        auto issue_u = [&](int cc) {
+            const uint32_t sb = stage(cc);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16(tmem + TS_D, sdesc_sw128(sb + L::kV + k * 2048, 8192, 1024),
+                         sdesc_sw128(sb + L::kTZ + k * 32, 16, 1024), id_u, k > 0);
+        };
+        auto issue_w = [&](int cc) {
+            const uint32_t sb = stage(cc);
+#pragma unroll
+            for (int k = 0; k < DK / 16; ++k)
+                mma_bf16_ta(tmem + TS_D, tmem + TS_S0B + k * 8,
+                            sdesc_sw128(sb + L::kWQ + (k / 4) * 16384 + (k % 4) * 32, 16, 1024), id_w,
+                            (vhalf || k > 0) ? 1u : 0u);
+            mma_commit(&bars[SB_W]);
+        };
+        auto issue_s = [&](int cc) {
+            const uint32_t sb = stage(cc);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16_ta(tmem + TS_SA, tmem + TS_WTB + k * 8, sdesc_sw128(sb + L::kK + k * 2048, 8192, 1024),
+                            id_s, k > 0);
+            mma_commit(&bars[SB_S]);
+        };
+        auto issue_qk = [&](int cc) {
+            const uint32_t sb = stage(cc);
+#pragma unroll
+            for (int k = 0; k < DK / 16; ++k)
+                mma_bf16(tmem + TS_QK, sdesc_sw128(sb + L::kWQ + (k / 4) * 16384 + 8192 + (k % 4) * 32, 16, 1024),
+                         sdesc_sw128(sb + L::kK + (k / 4) * 8192 + (k % 4) * 32, 16, 1024), id_qk, k > 0);
+            mma_commit(&bars[SB_QKB]);
+        };
+        auto issue_pw = [&](int cc) {
+            const uint32_t sPc = sP + (cc & 1) * 8192;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16_ta(tmem + TS_PW, tmem + TS_WBB + k * 8, sdesc_sw128(sPc + k * 32, 16, 1024), id_pw, k > 0);
+            mma_commit(&bars[SB_PW]);
+        };
+        // warp-uniform non-blocking test of a barrier phase
+        auto ready = [&](int slot, uint32_t parity) {
+            const bool r = mbar_test_wait(&bars[slot], parity);
+            return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+        };
+        bool ok = wt.warp(SB_FULL0, 0, kWhereFull, 0);
+        if (ok) {
+            tc_fence_after();
+            if (elect_one()) {
+                if (vhalf) issue_u(0);
+                if (!SUMMARY) issue_qk(0);
+            }
+            __syncwarp();
+        }
+        if (SUMMARY) {
+            for (int c = 0; ok && c < nch; ++c) {
+                const uint32_t par = c & 1;
+                if (!(ok = wt.warp(SB_SR, par, kWhereSR, c))) break;
+                tc_fence_after();
+                if (elect_one()) issue_w(c);
+                __syncwarp();
+                if (!(ok = wt.warp(SB_WCT, par, kWhereWR, c))) break;
+                tc_fence_after();
+                if (elect_one()) {
+                    issue_s(c);
+                    mma_commit(&bars[SB_EMPTY0 + c % kStages]);
+                }
+                __syncwarp();
+                if (c + 1 < nch) {
+                    if (!(ok = wt.warp(SB_FULL0 + (c + 1) % kStages, ((c + 1) / kStages) & 1, kWhereFull, c + 1))) break;
+                    tc_fence_after();
+                    if (vhalf) {
+                        if (elect_one()) issue_u(c + 1);
+                        __syncwarp();
+                    }
+                }
+            }
+        } else {
+            // Per chunk c: W(c) [S_c ready] and S(c) [Wt ready] first; then
+            // U(c+1) [-W^T and S0^T Q^T read], P W(c) [P(c) and Wb ready],
+            // Q K^T(c+1) [Q K^T(c) read], and the stage release.
+            int c = 0;
+            bool fW = false, fS = false, fU = false, fPW = false, fQK = false, fE = false;
+            uint32_t idle = 0;
+            uint64_t t_last = globaltimer_ns();
+            while (ok && c < nch) {
+                const uint32_t par = c & 1;
+                const int s1 = (c + 1) % kStages;
+                const uint32_t p1 = ((c + 1) / kStages) & 1;
+                bool prog = false;
+                if (!fW && ready(SB_SR, par)) {
+                    tc_fence_after();
+                    if (elect_one()) issue_w(c);
+                    __syncwarp();
+                    fW = prog = true;
+                }
+                if (fW && !fS && ready(SB_WCT, par)) {
+                    tc_fence_after();
+                    if (elect_one()) issue_s(c);
+                    __syncwarp();
+                    fS = prog = true;
+                }
+                if (fS && !fU) {
+                    if (c + 1 >= nch) {
+                        fU = true;
+                    } else if (ready(SB_QSR, par) && ready(SB_FULL0 + s1, p1)) {
+                        tc_fence_after();
+                        if (elect_one()) issue_u(c + 1);
+                        __syncwarp();
+                        fU = prog = true;
+                    }
+                }
+                if (fW && !fPW && ready(SB_PR, par) && ready(SB_WCB, par)) {
+                    tc_fence_after();
+                    if (elect_one()) issue_pw(c);
+                    __syncwarp();
+                    fPW = prog = true;
+                }
+                if (fPW && !fQK) {
+                    if (c + 1 >= nch) {
+                        fQK = true;
+                    } else if (ready(SB_FULL0 + s1, p1)) {
+                        tc_fence_after();
+                        if (elect_one()) issue_qk(c + 1);
+                        __syncwarp();
+                        fQK = prog = true;
+                    }
+                }
+                if (fS && fPW && !fE) {
+                    if (elect_one()) mma_commit(&bars[SB_EMPTY0 + c % kStages]);
+                    __syncwarp();
+                    fE = prog = true;
+                }
+                if (fW && fS && fU && fPW && fQK && fE) {
+                    ++c;
+                    fW = fS = fU = fPW = fQK = fE = false;
+                    idle = 0;
+                    t_last = globaltimer_ns();
+                } else if (!prog) {
+                    // nothing issuable: sleep until the next state-path
+                    // barrier completes (or briefly), then look again
+                    if (!fW) mbar_try_wait_sleep(&bars[SB_SR], par, 1000);
+                    else if (!fS) mbar_try_wait_sleep(&bars[SB_WCT], par, 1000);
+                    __syncwarp();
+                    if ((++idle & 15) == 0) {
+                        if (*abort_flag) { ok = false; break; }
+                        if (globaltimer_ns() - t_last > kTimeoutNs) { wt.fail(kWhereSR, c); ok = false; break; }
+                    }
+                }
+            }
+        }
+        if (elect_one()) {
+            mma_commit(&bars[SB_DRAIN]);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait_sleep(&bars[SB_DRAIN], 0, kSuspendNs)) {
+                if (globaltimer_ns() - t0 > kTimeoutNs) { wt.fail(kWhereDrain, -1); break; }
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ================================================================ state warps
+        const int q = warp & 3, hh = (warp - 4) >> 2;
+        const int j = q * 32 + lane;                      // state column (TMEM lane)
+        const uint32_t lf = (uint32_t)(q * 32) << 16;
+        const int st_id = tid - 128;                      // 0..255
+        float master[64];                                 // S^T[j][64 hh + i]
+        {
+            const float* src = SUMMARY ? nullptr
+                                       : (p.s_in ? p.s_in + ((size_t)head * p.nseg + seg) * DK * dv : nullptr);
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const int d = 64 * hh + i;
+                master[i] = SUMMARY ? ((!vhalf && d == j) ? 1.f : 0.f) : (src ? src[(size_t)d * dv + j] : 0.f);
+            }
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                uint32_t pk[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) pk[i] = pack2(master[16 * qq + 2 * i], master[16 * qq + 2 * i + 1]);
+                tmem_st_32x32b_x8u(tmem + lf + TS_S0B + 32 * hh + 8 * qq, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            bar_sync(1, 256);
+            if (st_id == 0) mbar_arrive(&bars[SB_SR]);
+        }
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t par = c & 1;
+            const float* vec = reinterpret_cast<const float*>(sm + (c % kStages) * L::kStageBytes + L::kVec);
+            const float* sc = vec + 2 * C;                // exp(gam_C - gam_r)
+            // ---- -W^T -> Wt^T = W^T diag(exp(gam_C - gam_r)) (bf16, TMEM): the chain
+            if (!wt.group(SB_W, par, kWhereW, c, 3, 256)) break;
+            tc_fence_after();
+            const float GC = __expf(vec[C - 1]);
+            uint32_t pb[16];
+            {
+                float v[32];
+                tmem_ld_32x32b_x16(tmem + lf + TS_D + 32 * hh, *reinterpret_cast<float(*)[16]>(v));
+                tmem_ld_32x32b_x16(tmem + lf + TS_D + 32 * hh + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+                tmem_ld_wait();
+#pragma unroll
+                for (int qq = 0; qq < 2; ++qq) {
+                    uint32_t pt[8];
+#pragma unroll
+                    for (int i4 = 0; i4 < 4; ++i4) {
+                        const int i = 16 * qq + 4 * i4;
+                        const float4 s4 = *reinterpret_cast<const float4*>(sc + 32 * hh + i);
+                        const float w0 = -v[i], w1 = -v[i + 1], w2 = -v[i + 2], w3 = -v[i + 3];
+                        pt[2 * i4] = pack2(w0 * s4.x, w1 * s4.y);
+                        pt[2 * i4 + 1] = pack2(w2 * s4.z, w3 * s4.w);
+                        pb[8 * qq + 2 * i4] = pack2(w0, w1);
+                        pb[8 * qq + 2 * i4 + 1] = pack2(w2, w3);
+                    }
+                    tmem_st_32x32b_x8u(tmem + lf + TS_WTB + 16 * hh + 8 * qq, pt);
+                }
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            bar_sync(1, 256);
+            if (st_id == 0) mbar_arrive(&bars[SB_WCT]);
+            // ---- Wb^T, once P W of the previous chunk has read the last one
+            if (!SUMMARY) {
+                if (c > 0 && !wt.group(SB_PW, par ^ 1u, kWherePW, c, 3, 256)) break;
+                tc_fence_after();
+                tmem_st_32x32b_x16u(tmem + lf + TS_WBB + 16 * hh, pb);
+                tmem_st_wait();
+                tc_fence_before();
+                bar_sync(1, 256);
+                if (st_id == 0) mbar_arrive(&bars[SB_WCB]);
+            }
+            // ---- S1^T = Gam_C S0^T + S_acc; bf16 copy for the next chunk
+            if (!wt.group(SB_S, par, kWhereS, c, 3, 256)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int hq = 0; hq < 2; ++hq) {
+                float acc[32];
+                tmem_ld_32x32b_x16(tmem + lf + TS_SA + 64 * hh + 32 * hq, *reinterpret_cast<float(*)[16]>(acc));
+                tmem_ld_32x32b_x16(tmem + lf + TS_SA + 64 * hh + 32 * hq + 16, *reinterpret_cast<float(*)[16]>(acc + 16));
+                tmem_ld_wait();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) master[32 * hq + i] = fmaf(GC, master[32 * hq + i], acc[i]);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pk[i] = pack2(master[32 * hq + 2 * i], master[32 * hq + 2 * i + 1]);
+                tmem_st_32x32b_x16u(tmem + lf + TS_S0B + 32 * hh + 16 * hq, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            bar_sync(1, 256);
+            if (st_id == 0) mbar_arrive(&bars[SB_SR]);
+        }
+        const bool aborted = bar_or(3, 256, *abort_flag != 0);
+        const bool write_final = SUMMARY || (p.s_out && seg == p.nseg - 1);
+        if (write_final && !aborted) {
+            float* dst = SUMMARY ? p.s_out + ((size_t)head * p.nseg + seg) * DK * (dv + DK) + (vhalf ? j : dv + j)
+                                 : p.s_out + (size_t)head * DK * dv + j;
+            const size_t ld = SUMMARY ? (size_t)(dv + DK) : (size_t)dv;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) dst[(size_t)(64 * hh + i) * ld] = master[i];
+        }
+    } else if (!SUMMARY) {
+        // ================================================================ aux warps
+        const int q = warp;                               // TMEM lane quadrant
+        const bool m64 = lane < 16;
+        const int r64 = q * 16 + lane;                    // row of the M=64 Q K^T
+        const int j = q * 32 + lane;                      // output column (M=128 lane)
+        const uint32_t lf = (uint32_t)(q * 32) << 16;
+        const int at = tid;                               // 0..127
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t par = c & 1;
+            const int t0 = (c0 + c) * C;
+            const float* gam = reinterpret_cast<const float*>(sm + (c % kStages) * L::kStageBytes + L::kVec);
+            const float* wfac = gam + C;
+            float* Gp = reinterpret_cast<float*>(sm + L::kG) + par * C;
+            // ---- P = mask(exp(gam_r - gam_s) Q K^T) -> bf16 tile; Gam_r kept for the epilogue
+            if (!wt.group(SB_QKB, par, kWherePR, c, 4, 128)) break;
+            tc_fence_after();
+            {
+                float qk[64];
+                {
+                    float lo[32], hi[32];
+                    tmem_ld_32x32b_x32(tmem + lf + TS_QK, lo);
+                    tmem_ld_32x32b_x32(tmem + lf + TS_QK + 32, hi);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) { qk[i] = lo[i]; qk[32 + i] = hi[i]; }
+                }
+                if (at < C) Gp[at] = __expf(gam[at]);
+                if (m64) {
+                    const float gr = gam[r64];
+                    const float gamm = gam[C / 2 - 1];
+                    const bool fact = (gam[0] - gam[C - 1]) <= kSpanMax;
+                    uint8_t* Pt = sm + L::kP + par * 8192;
+                    if (fact) {
+                        const float ur = __expf(gr - gamm);
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8) {
+                            const float4 w0 = *reinterpret_cast<const float4*>(wfac + c8 * 8);
+                            const float4 w1 = *reinterpret_cast<const float4*>(wfac + c8 * 8 + 4);
+                            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                            float v[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) v[i] = (c8 * 8 + i <= r64) ? ur * wv[i] * qk[c8 * 8 + i] : 0.f;
+                            ST_CHUNK(Pt, r64, c8, v, 0);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8) {
+                            float v[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int s2 = c8 * 8 + i;
+                                v[i] = (s2 <= r64) ? __expf(gr - gam[s2]) * qk[s2] : 0.f;
+                            }
+                            ST_CHUNK(Pt, r64, c8, v, 0);
+                        }
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            bar_sync(2, 128);
+            if (at == 0) mbar_arrive(&bars[SB_PR]);
+            // ---- S0^T Q^T (the right half of the W product), read out early
+            if (!wt.group(SB_W, par, kWhereW, c, 4, 128)) break;
+            tc_fence_after();
+            float qs[64];  // Gam_r (S0^T Q^T)[j][r]
+            tmem_ld_32x32b_x32(tmem + lf + TS_D + 64, *reinterpret_cast<float(*)[32]>(qs));
+            tmem_ld_32x32b_x32(tmem + lf + TS_D + 96, *reinterpret_cast<float(*)[32]>(qs + 32));
+            tmem_ld_wait();
+            tc_fence_before();
+            bar_sync(2, 128);
+            if (at == 0) mbar_arrive(&bars[SB_QSR]);
+#pragma unroll
+            for (int r4 = 0; r4 < 16; ++r4) {
+                const float4 g4 = *reinterpret_cast<const float4*>(Gp + 4 * r4);
+                qs[4 * r4] *= g4.x; qs[4 * r4 + 1] *= g4.y; qs[4 * r4 + 2] *= g4.z; qs[4 * r4 + 3] *= g4.w;
+            }
+            // ---- o_r = Gam_r (S0^T Q^T)[., r] + (Wb^T P^T)[., r]: TMEM -> smem tile -> TMA store
+            if (!wt.group(SB_PW, par, kWherePW, c, 4, 128)) break;
+            tc_fence_after();
+            if (at == 0) bulk_wait_read_le1();  // the store that last used this tile has read it
+            bar_sync(2, 128);
+            // o[r][j] goes to byte r*128 + ((j8 ^ (r & 7)) << 4) + (j & 7)*2 of
+            // the tile holding columns (j & ~63)..+63 (128-byte swizzle)
+            const uint32_t obase = smem_u32(sm + L::kO + par * 16384 + (j >> 6) * 8192) + (uint32_t)(j & 7) * 2u;
+            const uint32_t j8 = (uint32_t)(j & 63) >> 3;
+            uint32_t oaddr[8];
+#pragma unroll
+            for (int r8 = 0; r8 < 8; ++r8) oaddr[r8] = obase + (((j8 ^ (uint32_t)r8) & 7u) << 4);
+#pragma unroll
+            for (int hq = 0; hq < 2; ++hq) {
+                float b32[32];
+                tmem_ld_32x32b_x32(tmem + lf + TS_PW + 32 * hq, b32);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int r = 32 * hq + i;
+                    const __nv_bfloat16 ov = __float2bfloat16_rn(qs[r] + b32[i]);
+                    asm volatile("st.shared.b16 [%0], %1;" ::"r"(oaddr[r & 7] + (uint32_t)r * 128u),
+                                 "h"(*reinterpret_cast<const unsigned short*>(&ov))
+                                 : "memory");
+                }
+            }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            bar_sync(2, 128);
+            if (at == 0) {
+                tma_store_4d(&tm_o, sm + L::kO + par * 16384, 0, h, t0, b);
+                tma_store_4d(&tm_o, sm + L::kO + par * 16384 + 8192, 64, h, t0, b);
+                bulk_commit();
+            }
+        }
+        if (at == 0) bulk_wait_all();  // stores must finish reading shared memory before exit
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 13) tmem_dealloc(tmem, 512);
+}
+
+// ============================================================================
 // segment_combine_kernel: the sequential pass over segment maps.  For each
 // head, S_start[0] = h0 (or 0) and S_start[j+1] = M_j S_start[j] + N_j, where
 // [N_j | M_j] (DK x (dv + DK)) is segment j's summary.  fp32 on CUDA cores;
@@ -1156,6 +1688,35 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto* ob = reinterpret_cast<__nv_bfloat16*>(o);
+    if (DK == 128 && dv == 128) {
+        // transposed-state carry: one CTA per (head, run)
+        CUtensorMap mo;
+        if (!make_map(&mo, o, B, T, H, dv)) return cudaErrorInvalidValue;
+        auto state = chunk_state_kernel<false>;
+        auto state_sum = chunk_state_kernel<true>;
+        constexpr size_t smem_state = StateLayout::kSmemBytes;
+        static std::once_flag once_s;
+        static cudaError_t attr_s = cudaSuccess;
+        std::call_once(once_s, [&] {
+            attr_s = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_state);
+            if (attr_s == cudaSuccess)
+                attr_s = cudaFuncSetAttribute(state_sum, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_state);
+        });
+        if (attr_s != cudaSuccess) return attr_s;
+        if (nseg == 1) {
+            CarryParams cp{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks};
+            state<<<dim3(1, H, B), kStateThreads, smem_state, stream>>>(mq, mk, mv, mo, cp);
+            return cudaGetLastError();
+        }
+        CarryParams c1{nullptr, rec, nullptr, seg_x, err, T, H, dv, nchunks, nseg, seg_chunks};
+        state_sum<<<dim3(2, H, B * nseg), kStateThreads, smem_state, stream>>>(mq, mk, mv, mo, c1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        combine<<<dim3(dv / 16, H, B), 2 * DK, smem_comb, stream>>>(seg_x, h0, seg_start, H, nseg, dv);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        CarryParams c3{seg_start, rec, ob, hT, err, T, H, dv, nchunks, nseg, seg_chunks};
+        state<<<dim3(1, H, B * nseg), kStateThreads, smem_state, stream>>>(mq, mk, mv, mo, c3);
+        return cudaGetLastError();
+    }
     if (nseg == 1) {
         CarryParams cp{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks};
         carry<<<dim3(dv / DVS, H, B), kCarryThreads, smem_carry, stream>>>(mq, mk, mv, cp);
@@ -1197,9 +1758,12 @@ size_t chunk_fwd_tc_scan_bytes(int B, int H, int dk, int dv, int nseg) {
 
 int chunk_fwd_tc_auto_segments(int B, int T, int H, int dk, int dv) {
     const int nchunks = (T + C - 1) / C;
-    const long long base = (long long)B * H * (dv / DVS);        // carry CTAs without a scan
+    // carry CTAs without a scan, and summary CTAs per run: one per head (two
+    // per run) for d_k = d_v = 128, one per 64-column slice otherwise
+    const bool wide = dk == 128 && dv == 128;
+    const long long base = (long long)B * H * (wide ? 1 : dv / DVS);
     if (base * 2 > kScanTargetCtas) return 1;
-    const long long per_seg = (long long)B * H * ((dv + dk) / DVS);  // summary CTAs per segment
+    const long long per_seg = (long long)B * H * (wide ? 2 : (dv + dk) / DVS);
     long long nseg = kScanTargetCtas / per_seg;
     if (nseg > nchunks / kScanMinSegChunks) nseg = nchunks / kScanMinSegChunks;
     return nseg > 1 ? (int)nseg : 1;

@@ -65,7 +65,7 @@ typedef enum kla_io_dtype {
 /*
  * Bytes of device workspace kla_chunk_fwd needs for this problem: 256 bytes
  * of device error record, plus, with bf16 I/O, one record of
- * 8704 + 128*dk bytes (25,088 for dk = 128) per (batch, head, 64-token
+ * 8960 + 128*dk bytes (25,344 for dk = 128) per (batch, head, 64-token
  * chunk) that carries the chunk's state-independent operands from the first
  * kernel to the second, plus the chunk-level scan's buffers when the
  * automatic segment count (kla_chunk_fwd_auto_segments) is above 1.

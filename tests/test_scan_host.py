@@ -35,7 +35,7 @@ def test_scan_workspace_formula(dk, dv):
     B, T, H = 2, 1000, 3
     nchunks = -(-T // 64)
     base = kla.kla_chunk_fwd_scan_workspace_bytes(B, T, H, dk, dv, segments=1)
-    rec = 8192 + 64 * dk * 2 + 512
+    rec = 8192 + 64 * dk * 2 + 768
     assert base == 256 + B * H * nchunks * rec
     for segments in (2, 3, 5, 16, 40):
         seg_chunks = -(-nchunks // segments)
