@@ -197,17 +197,39 @@ def job_throughput(units_per_rank: float, local_seconds: float) -> tuple[float, 
 
 # ------------------------------------------------------------- native arm
 
-# Kernels of ours launched per ABI call.  kla_chunk_fwd: chunk_prep_kernel
-# and chunk_carry_kernel, or, when it splits the chunks into runs (the
-# chunk-level scan), chunk_prep_kernel, the summary pass, the combine and
-# chunk_carry_kernel; plus a 256-byte cudaMemsetAsync of the error record
-# (not a kernel of ours).  kla_decode_step launches one kernel.
+# Kernels of ours launched per ABI call.  kla_chunk_fwd, by dispatch:
+#  - chunk-level scan (few heads, long sequences): chunk_prep_kernel, the
+#    summary pass, the combine and the carry: 4;
+#  - d_k = d_v = 128 with >= 32 chunks and free SMs: chunk ranges, each a
+#    prep and a carry launch (the prep of range r+1 overlaps the carry of
+#    range r): 2 per range;
+#  - otherwise chunk_prep_kernel and the carry: 2;
+# plus a 256-byte cudaMemsetAsync of the error record (not a kernel of
+# ours).  kla_decode_step launches one kernel.
 LAUNCHES_PER_DECODE = 1
+MAX_RANGES, RANGE_MIN_CHUNKS, GB300_SMS = 8, 32, 152
+
+
+def chunk_ranges(nchunks: int) -> int:
+    """Number of chunk ranges the library uses (first nchunks/8, at least 4
+    chunks, then about 1.25x each; at most MAX_RANGES)."""
+    n, lo, size = 0, 0, max(nchunks // 8, 4)
+    while lo < nchunks and n < MAX_RANGES:
+        lo = nchunks if (n == MAX_RANGES - 1 or lo + size >= nchunks) else lo + size
+        n += 1
+        size = (size * 5 + 3) // 4
+    return n
 
 
 def prefill_launches(kla, case) -> int:
     segs = kla.kla_chunk_fwd_auto_segments(case.B, case.T, case.H, case.dk, case.dv, case.chunk)
-    return 2 if segs == 1 else 4
+    if segs > 1:
+        return 4
+    nchunks = -(-case.T // case.chunk)
+    if (case.dk == 128 and case.dv == 128 and nchunks >= RANGE_MIN_CHUNKS
+            and case.B * case.H + 16 <= GB300_SMS):
+        return 2 * chunk_ranges(nchunks)
+    return 2
 
 
 def bench_prefill(case, K, W, flush, peaks, stream, e2e=True):

@@ -59,7 +59,7 @@ size_t kla_chunk_fwd_scan_workspace_bytes(int B, int T, int H, int dk, int dv, i
     if (io != KLA_IO_BF16) return segments <= 1 ? n : 0;
     if (segments == 0) segments = kla::chunk_fwd_tc_auto_segments(B, T, H, dk, dv);
     n += kla::chunk_fwd_tc_record_bytes(B, T, H, dk);
-    n += kla::chunk_fwd_tc_scan_bytes(B, H, dk, dv, kla::chunk_fwd_tc_scan_shape(T, segments).nseg);
+    n += kla::chunk_fwd_tc_extra_bytes(B, T, H, dk, dv, kla::chunk_fwd_tc_scan_shape(T, segments).nseg);
     return n;
 }
 

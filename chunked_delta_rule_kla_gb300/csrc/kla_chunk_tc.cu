@@ -153,32 +153,33 @@ struct Waiter {
 // compute beta, gam, A, T and the two operand tiles.
 // ============================================================================
 constexpr int kPrepThreads = 160;
+constexpr int kPrepPerSm = 4;   // resident prep CTAs per SM (49 KB shared memory, 128 TMEM columns each)
 
 template <int DK>
 struct PrepLayout {
     static constexpr int KB = DK / 64;
     static constexpr uint32_t kK = 0;                          // KB boxes of [64][64] bf16
-    // Region X: A and T (fp32) while the inverse is formed; afterwards the
-    // outgoing record body (Tb, Wk) is written over it.  Tg = T diag(beta
-    // Gam), the A operand of Wk = Tg K, sits where Wk goes: it is written
-    // with Tb once A is dead and read by the MMA before Wk replaces it.
+    // Region X: A (fp32), over which T is formed in place, and the scratch
+    // Rw; afterwards the outgoing record body (Tb, Wk) is written over it.
+    // Tg = T diag(beta Gam), the A operand of Wk = Tg K, sits where Wk goes:
+    // it is written with Tb once T is in registers and read by the MMA
+    // before Wk replaces it.
     static constexpr uint32_t kX = kK + KB * 8192;
-    static constexpr uint32_t kAf = kX;                        // fp32 [64][LDF]
-    static constexpr uint32_t kTf = kAf + C * LDF * 4;         // fp32 [64][LDF]
-    static constexpr uint32_t kTb = kX + Rec<DK>::kTb;         // written after A is dead
+    static constexpr uint32_t kAf = kX;                        // fp32 [64][LDF]: A, then T
+    static constexpr uint32_t kRw = kAf + C * LDF * 4;         // fp32 [32][LDF]
+    static constexpr uint32_t kTb = kX + Rec<DK>::kTb;
     static constexpr uint32_t kTg = kX + Rec<DK>::kWk;
-    static constexpr uint32_t kWk = kX + Rec<DK>::kWk;         // written after T and Tg are dead
-    static constexpr uint32_t kXEnd = (kTf + C * LDF * 4 > kX + Rec<DK>::kGam) ? kTf + C * LDF * 4
-                                                                               : kX + Rec<DK>::kGam;
-    static constexpr uint32_t kRw = kXEnd;                     // fp32 [32][LDF]
-    static constexpr uint32_t kAdT = kRw + 32 * LDF * 4;       // fp32 4 x [16][16]
+    static constexpr uint32_t kWk = kX + Rec<DK>::kWk;
+    static constexpr uint32_t kXEnd = (kRw + 32 * LDF * 4 > kX + Rec<DK>::kGam) ? kRw + 32 * LDF * 4
+                                                                              : kX + Rec<DK>::kGam;
+    static constexpr uint32_t kAdT = kXEnd;                    // fp32 4 x [16][16]
     static constexpr uint32_t kGam = kAdT + 4 * 256 * 4;       // gam[64], w[64], sc[64] (record tail)
     static constexpr uint32_t kWf = kGam + 256;
     static constexpr uint32_t kSc = kWf + 256;
     static constexpr uint32_t kBet = kSc + 256;                // beta[64], betg[64]
     static constexpr uint32_t kMisc = kBet + 2 * 256;
     static constexpr uint32_t kBars = kMisc + 64;
-    static constexpr uint32_t kEnd = kBars + 4 * 8;
+    static constexpr uint32_t kEnd = kBars + 6 * 8;
     static constexpr size_t kSmemBytes = kEnd + 1024;
     static_assert(Rec<DK>::kWk + 8192 <= C * LDF * 4, "Tb, Tg fit in A's space");
 };
@@ -190,16 +191,22 @@ struct PrepParams {
     DeviceErrorRecord* err;
     float eps;
     int T, H, nchunks;
+    int B, c_lo, c_hi;      // work items: chunks [c_lo, c_hi) of every (b, h), chunk-major
+    int pdl_wait;           // launched as a programmatic dependent: wait for the primary at exit
 };
 
+// Persistent: each CTA walks items blockIdx.x, blockIdx.x + gridDim.x, ...;
+// warp 0 fetches the next item's K tile as soon as the current Wk product
+// has read the tile.
 template <int DK>
-__global__ void __launch_bounds__(kPrepThreads, 3)
+__global__ void __launch_bounds__(kPrepThreads, kPrepPerSm)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) {
     using L = PrepLayout<DK>;
     constexpr int KB = L::KB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBars);  // 0: K loaded, 1: K K^T, 2: Wk
+    // 0: K loaded, 1: K K^T, 2: Wk, 3: TMEM read (Wk converted), 4, 5: drains
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBars);
     float* misc = reinterpret_cast<float*>(sm + L::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 32);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kMisc + 48);
@@ -208,23 +215,21 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
     float* betg = bet + C;
     float* wf = reinterpret_cast<float*>(sm + L::kWf);
     float* Af = reinterpret_cast<float*>(sm + L::kAf);
-    float* Tf = reinterpret_cast<float*>(sm + L::kTf);
+    float* Tf = Af;  // T is formed in place: each block of T replaces the block of A it no longer needs
     float* Rw = reinterpret_cast<float*>(sm + L::kRw);
     float* AdT = reinterpret_cast<float*>(sm + L::kAdT);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int T = p.T, H = p.H;
-    const int t0 = c * C;
-    const int nvalid = min(C, T - t0);
+    const int nheads = p.B * H;
+    const int total = (p.c_hi - p.c_lo) * nheads;
     Waiter wt{bars, abort_flag, p.err};
 
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        mbar_init(&bars[2], 1);
+        for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
     if (warp == 0) {
         tmem_alloc(tmem_slot, 128);  // K K^T, later Wk (the Gram rows are consumed first)
@@ -237,12 +242,28 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
 
     if (warp == 0) {
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[0], KB * 8192);
+            int loads = 0;          // K tiles requested so far
+            bool inflight = false;  // a requested tile not yet waited for
+            auto load = [&](int item) {
+                const int c = p.c_lo + item / nheads, hd = item % nheads;
+                mbar_arrive_expect_tx(&bars[0], KB * 8192);
 #pragma unroll
-            for (int kb = 0; kb < KB; ++kb) tma_load_4d(sm + L::kK + kb * 8192, &tm_k, &bars[0], kb * 64, h, t0, b);
-            // K K^T (M=64, N=64) once the tile has landed
-            if (wt.poll(0, 0, kWherePrepK, c)) {
+                for (int kb = 0; kb < KB; ++kb)
+                    tma_load_4d(sm + L::kK + kb * 8192, &tm_k, &bars[0], kb * 64, hd % H, c * C, hd / H);
+                ++loads;
+                inflight = true;
+            };
+            int it = 0;
+            if ((int)blockIdx.x < total) load(blockIdx.x);
+            for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
+                const uint32_t ph = it & 1;
+                const int c = p.c_lo + item / nheads;
+                if (!wt.poll(0, ph, kWherePrepK, c)) break;
+                inflight = false;
+                // the previous item's Wk has been read out of TMEM
+                if (it > 0 && !wt.poll(3, ph ^ 1u, kWherePrepG, c)) break;
                 tc_fence_after();
+                // K K^T (M=64, N=64)
                 constexpr uint32_t id_g = idesc_bf16(64, 64, false, false);
                 const uint32_t sK = smem_u32(sm + L::kK);
 #pragma unroll
@@ -251,15 +272,20 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
                     mma_bf16(tmem, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), id_g, k > 0);
                 }
                 mma_commit(&bars[1]);
-                const uint64_t tw = globaltimer_ns();  // MMAs must finish before TMEM is freed
-                while (!mbar_try_wait_sleep(&bars[1], 0, kSuspendNs))
-                    if (globaltimer_ns() - tw > kTimeoutNs) { wt.fail(kWhereDrain, c); break; }
-            } else {
-                // the TMA copy must land before the CTA exits
+                // Wk = Tg K has read the tile: fetch the next one
+                if (!wt.poll(2, ph, kWherePrepG, c)) break;
+                if (item + (int)gridDim.x < total) load(item + gridDim.x);
+            }
+            // in-flight copies and MMAs must finish before the CTA exits
+            if (inflight) {
                 const uint64_t tw = globaltimer_ns();
-                while (!mbar_try_wait_sleep(&bars[0], 0, kSuspendNs))
+                while (!mbar_try_wait_sleep(&bars[0], (loads - 1) & 1, kSuspendNs))
                     if (globaltimer_ns() - tw > kTimeoutNs) break;
             }
+            mma_commit(&bars[4]);
+            const uint64_t tw = globaltimer_ns();
+            while (!mbar_try_wait_sleep(&bars[4], 0, kSuspendNs))
+                if (globaltimer_ns() - tw > kTimeoutNs) { wt.fail(kWhereDrain, -1); break; }
         }
         __syncwarp();
     } else {
@@ -270,9 +296,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
         const uint32_t lf = (uint32_t)(q * 32) << 16;
         uint8_t* Tbt = sm + L::kTb;
         uint8_t* Tgt = sm + L::kTg;
+        int it = 0;
+        for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
+        const uint32_t ph = it & 1;
+        const int c = p.c_lo + item / nheads, hd = item % nheads;
+        const int h = hd % H, b = hd / H;
+        const int t0 = c * C;
+        const int nvalid = min(C, T - t0);
 
-        // T's blocks above the diagonal stay zero.
-        for (int i = pt; i < C * LDF; i += 128) Tf[i] = 0.f;
+        // (T's blocks above the diagonal are A's zeros.)
         // ---- gates and the decay cumsum (threads 0..63 hold rows 0..63)
         float gv = 0.f, ev = 0.f;
         if (pt < C && pt < nvalid) {
@@ -294,7 +326,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
             bet[pt] = ev;  // eta for now; beta below
         }
         // ---- K K^T rows
-        if (!wt.group(1, 0, kWherePrepG, c, 3, 128)) goto prep_done;
+        if (!wt.group(1, ph, kWherePrepG, c, 3, 128)) break;
         tc_fence_after();
         {
             float row[64];
@@ -460,14 +492,22 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
             *reinterpret_cast<float4*>(&Tf[(33 + r0) * LDF + c0]) = make_float4(-z[1][0], -z[1][1], -z[1][2], -z[1][3]);
         }
         bar_sync(1, 128);
-        // ---- Tb = T diag(beta), Tg = T diag(beta Gam): 128 threads, 2 x 8 columns each
+        // ---- Tb = T diag(beta), Tg = T diag(beta Gam): 128 threads, 2 x 8 columns each.
+        // The tiles overwrite T, so each thread first takes its half-row.
         {
             const int rr = pt >> 1, col8 = (pt & 1) * 4;
+            float4 ta[4][2];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                ta[u][0] = *reinterpret_cast<const float4*>(&Tf[rr * LDF + (col8 + u) * 8]);
+                ta[u][1] = *reinterpret_cast<const float4*>(&Tf[rr * LDF + (col8 + u) * 8 + 4]);
+            }
+            bar_sync(1, 128);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int c8 = col8 + u;
-                const float4 a0 = *reinterpret_cast<const float4*>(&Tf[rr * LDF + c8 * 8]);
-                const float4 a1 = *reinterpret_cast<const float4*>(&Tf[rr * LDF + c8 * 8 + 4]);
+                const float4 a0 = ta[u][0];
+                const float4 a1 = ta[u][1];
                 const float4 b0 = *reinterpret_cast<const float4*>(&bet[c8 * 8]);
                 const float4 b1 = *reinterpret_cast<const float4*>(&bet[c8 * 8 + 4]);
                 const float4 e0 = *reinterpret_cast<const float4*>(&betg[c8 * 8]);
@@ -498,7 +538,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
                          sdesc_sw128(sK + k * 2048, 8192, 1024), id_wk, k > 0);
             mma_commit(&bars[2]);
         }
-        if (!wt.group(2, 0, kWherePrepG, c, 3, 128)) goto prep_done;
+        if (!wt.group(2, ph, kWherePrepG, c, 3, 128)) break;
         tc_fence_after();
         {
             uint8_t* Wkt = sm + L::kWk;
@@ -517,18 +557,28 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
         fence_proxy_async_smem();
         bar_sync(1, 128);
         if (pt == 0) {
+            mbar_arrive(&bars[3]);  // TMEM free for the next item's K K^T
             uint8_t* dst = p.rec + (((size_t)b * H + h) * p.nchunks + c) * Rec<DK>::kBytes;
             bulk_store(dst, sm + L::kX, Rec<DK>::kGam);
             bulk_store(dst + Rec<DK>::kGam, sm + L::kGam, 768);
             bulk_commit();
             bulk_wait_all();
         }
-    prep_done:;
+        bar_sync(1, 128);  // the record has left shared memory
+        }
+        if (pt == 0) {     // this thread's Wk MMAs must finish before TMEM is freed
+            mma_commit(&bars[5]);
+            const uint64_t tw = globaltimer_ns();
+            while (!mbar_try_wait_sleep(&bars[5], 0, kSuspendNs))
+                if (globaltimer_ns() - tw > kTimeoutNs) { wt.fail(kWhereDrain, -1); break; }
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 128);
+    // a programmatic dependent launch ends only after its primary grid
+    if (p.pdl_wait && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ============================================================================
@@ -569,8 +619,9 @@ struct CarryLayout {
     static constexpr size_t kSmemBytes = kEnd + 1024;
 };
 
-// Chunks of a head are split into nseg segments of seg_chunks chunks (the
-// last may be shorter); blockIdx.z = b * nseg + segment.
+// The launch covers chunks [c_begin, c_end) of every head, split into nseg
+// segments of seg_chunks chunks (the last may be shorter); blockIdx.z =
+// b * nseg + segment.
 struct CarryParams {
     const float* s_in;      // output mode: start states [B][H][nseg][DK][dv] (null: zeros)
     const uint8_t* rec;
@@ -580,6 +631,7 @@ struct CarryParams {
     DeviceErrorRecord* err;
     int T, H, dv, nchunks;
     int nseg, seg_chunks;
+    int c_begin, c_end;
 };
 
 // mbarrier slots (all with arrival count 1)
@@ -610,8 +662,8 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int j0 = slice * DVS;
     const int T = p.T, H = p.H, dv = p.dv;
     const int nchunks = p.nchunks;
-    const int c0 = seg * p.seg_chunks;                  // first chunk of the segment
-    const int nch = min(p.seg_chunks, nchunks - c0);    // its chunks (>= 1)
+    const int c0 = p.c_begin + seg * p.seg_chunks;      // first chunk of the segment
+    const int nch = min(p.seg_chunks, p.c_end - c0);    // its chunks (>= 1)
     const bool vslice = !SUMMARY || j0 < dv;            // columns that see V
     const size_t head = (size_t)b * H + h;
     Waiter wt{bars, abort_flag, p.err};
@@ -1124,8 +1176,8 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const bool vhalf = !SUMMARY || blockIdx.x == 0;     // the values enter this state
     const int T = p.T, H = p.H, dv = p.dv;
     const int nchunks = p.nchunks;
-    const int c0 = seg * p.seg_chunks;
-    const int nch = min(p.seg_chunks, nchunks - c0);
+    const int c0 = p.c_begin + seg * p.seg_chunks;
+    const int nch = min(p.seg_chunks, p.c_end - c0);
     const size_t head = (size_t)b * H + h;
     Waiter wt{bars, abort_flag, p.err};
 
@@ -1133,6 +1185,9 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         for (int i = 0; i < SB_COUNT; ++i) mbar_init(&bars[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
+        // a programmatic dependent (the next chunk range's prep) may start
+        // on the SMs this grid leaves free
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
     if (!SUMMARY) {  // the zero halves of [T diag(beta) | 0], never loaded
         for (int i = tid; i < kStages * 2048; i += kStateThreads) {
@@ -1149,6 +1204,10 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // launched as a programmatic dependent of a prep grid: its records (and,
+    // through it, the previous range's state) are complete after this wait;
+    // a no-op for an ordinary launch
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 12) {
         // ================================================================ TMA producer
@@ -1655,11 +1714,26 @@ bool make_map(CUtensorMap* map, const void* base, int B, int T, int H, int D) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// SM count of the current device (cached per device).
+int sm_count() {
+    static std::mutex mu;
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kScanTargetCtas;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev] == 0) {
+        int n = 0;
+        cached[dev] = (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+                          ? n : kScanTargetCtas;
+    }
+    return cached[dev];
+}
+
 template <int DK>
 cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* g, const float* eta,
                       float eps, const float* h0, void* o, float* hT, int B, int T, int H, int dv,
                       DeviceErrorRecord* err, uint8_t* rec, int nseg, int seg_chunks, float* seg_x,
-                      float* seg_start, cudaStream_t stream) {
+                      float* seg_start, float* handoff, cudaStream_t stream) {
     CUtensorMap mq, mk, mv;
     if (!make_map(&mq, q, B, T, H, DK) || !make_map(&mk, k, B, T, H, DK) ||
         !make_map(&mv, v, B, T, H, dv))
@@ -1683,10 +1757,32 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int nchunks = (T + C - 1) / C;
-    PrepParams pp{g, eta, rec, err, eps, T, H, nchunks};
-    prep<<<dim3(nchunks, H, B), kPrepThreads, smem_prep, stream>>>(mk, pp);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    const int sms = sm_count();
+    // persistent prep over chunks [c_lo, c_hi) of every head on up to
+    // max_ctas CTAs; as a programmatic dependent it overlaps the running grid
+    auto launch_prep = [&](int c_lo, int c_hi, int max_ctas, bool pdl) -> cudaError_t {
+        const int total = (c_hi - c_lo) * B * H;
+        const int grid = total < max_ctas ? total : max_ctas;
+        PrepParams pp{g, eta, rec, err, eps, T, H, nchunks, B, c_lo, c_hi, pdl ? 1 : 0};
+        if (!pdl) {
+            prep<<<grid, kPrepThreads, smem_prep, stream>>>(mk, pp);
+            return cudaGetLastError();
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kPrepThreads);
+        cfg.dynamicSmemBytes = smem_prep;
+        cfg.stream = stream;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, prep, mk, pp);
+    };
+    cudaError_t e = cudaSuccess;
+    const int ranges = (DK == 128 && dv == 128) ? chunk_ranges(B, H, nchunks, nseg) : 1;  // >= 1
+    if (ranges == 1 && (e = launch_prep(0, nchunks, kPrepPerSm * sms, false)) != cudaSuccess) return e;
     auto* ob = reinterpret_cast<__nv_bfloat16*>(o);
     if (DK == 128 && dv == 128) {
         // transposed-state carry: one CTA per (head, run)
@@ -1703,33 +1799,66 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
                 attr_s = cudaFuncSetAttribute(state_sum, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_state);
         });
         if (attr_s != cudaSuccess) return attr_s;
-        if (nseg == 1) {
-            CarryParams cp{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks};
+        if (nseg == 1 && ranges == 1) {
+            CarryParams cp{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks, 0, nchunks};
             state<<<dim3(1, H, B), kStateThreads, smem_state, stream>>>(mq, mk, mv, mo, cp);
             return cudaGetLastError();
         }
-        CarryParams c1{nullptr, rec, nullptr, seg_x, err, T, H, dv, nchunks, nseg, seg_chunks};
+        if (nseg == 1) {
+            // chunk ranges: the carry of range r runs while the prep of range
+            // r+1 fills the other SMs; the state passes between ranges
+            // through `handoff`.  Ranges grow so that each prep fits under
+            // the previous carry; each carry is a programmatic dependent of
+            // its prep so that its launch overlaps the prep.
+            auto launch_state = [&](const CarryParams& cp, bool pdl) -> cudaError_t {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(1, H, B);
+                cfg.blockDim = dim3(kStateThreads);
+                cfg.dynamicSmemBytes = smem_state;
+                cfg.stream = stream;
+                cudaLaunchAttribute at[1];
+                at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                at[0].val.programmaticStreamSerializationAllowed = 1;
+                cfg.attrs = at;
+                cfg.numAttrs = pdl ? 1 : 0;
+                return cudaLaunchKernelEx(&cfg, state, mq, mk, mv, mo, cp);
+            };
+            int bounds[kMaxRanges + 1];
+            const int nr = chunk_range_bounds(nchunks, bounds);
+            const int free_sms = sms - B * H > 8 ? sms - B * H : 8;
+            if ((e = launch_prep(bounds[0], bounds[1], kPrepPerSm * sms, false)) != cudaSuccess) return e;
+            for (int r = 0; r < nr; ++r) {
+                const bool last = r == nr - 1;
+                CarryParams cp{r == 0 ? h0 : handoff, rec, ob, last ? hT : handoff, err, T, H, dv, nchunks,
+                               1, bounds[r + 1] - bounds[r], bounds[r], bounds[r + 1]};
+                if ((e = launch_state(cp, r > 0)) != cudaSuccess) return e;
+                if (!last && (e = launch_prep(bounds[r + 1], bounds[r + 2], kPrepPerSm * free_sms, true)) != cudaSuccess)
+                    return e;
+            }
+            return cudaSuccess;
+        }
+        CarryParams c1{nullptr, rec, nullptr, seg_x, err, T, H, dv, nchunks, nseg, seg_chunks, 0, nchunks};
         state_sum<<<dim3(2, H, B * nseg), kStateThreads, smem_state, stream>>>(mq, mk, mv, mo, c1);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         combine<<<dim3(dv / 16, H, B), 2 * DK, smem_comb, stream>>>(seg_x, h0, seg_start, H, nseg, dv);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        CarryParams c3{seg_start, rec, ob, hT, err, T, H, dv, nchunks, nseg, seg_chunks};
+        CarryParams c3{seg_start, rec, ob, hT, err, T, H, dv, nchunks, nseg, seg_chunks, 0, nchunks};
         state<<<dim3(1, H, B * nseg), kStateThreads, smem_state, stream>>>(mq, mk, mv, mo, c3);
         return cudaGetLastError();
     }
     if (nseg == 1) {
-        CarryParams cp{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks};
+        CarryParams cp{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks, 0, nchunks};
         carry<<<dim3(dv / DVS, H, B), kCarryThreads, smem_carry, stream>>>(mq, mk, mv, cp);
         return cudaGetLastError();
     }
     // chunk-level scan: segment summaries, the sequential combine, then each
     // segment's outputs from its true start state
-    CarryParams c1{nullptr, rec, nullptr, seg_x, err, T, H, dv, nchunks, nseg, seg_chunks};
+    CarryParams c1{nullptr, rec, nullptr, seg_x, err, T, H, dv, nchunks, nseg, seg_chunks, 0, nchunks};
     summary<<<dim3((dv + DK) / DVS, H, B * nseg), kCarryThreads, smem_carry, stream>>>(mq, mk, mv, c1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     combine<<<dim3(dv / 16, H, B), 2 * DK, smem_comb, stream>>>(seg_x, h0, seg_start, H, nseg, dv);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    CarryParams c3{seg_start, rec, ob, hT, err, T, H, dv, nchunks, nseg, seg_chunks};
+    CarryParams c3{seg_start, rec, ob, hT, err, T, H, dv, nchunks, nseg, seg_chunks, 0, nchunks};
     carry<<<dim3(dv / DVS, H, B * nseg), kCarryThreads, smem_carry, stream>>>(mq, mk, mv, c3);
     return cudaGetLastError();
 }
@@ -1751,9 +1880,31 @@ ScanShape chunk_fwd_tc_scan_shape(int T, int segments) {
     return sh;
 }
 
-size_t chunk_fwd_tc_scan_bytes(int B, int H, int dk, int dv, int nseg) {
-    if (nseg <= 1) return 0;
-    return sizeof(float) * (size_t)B * H * nseg * dk * ((size_t)(dv + dk) + dv);
+int chunk_ranges(int B, int H, int nchunks, int nseg) {
+    const long long heads = (long long)B * H;
+    if (!(nseg == 1 && nchunks >= kRangeMinChunks && heads + 16 <= kScanTargetCtas)) return 1;
+    int bounds[kMaxRanges + 1];
+    return chunk_range_bounds(nchunks, bounds);
+}
+
+int chunk_range_bounds(int nchunks, int* bounds) {
+    // first range nchunks/8 (at least 4) chunks, then each about 1.25x the last
+    int n = 0, size = nchunks / 8 > 4 ? nchunks / 8 : 4;
+    bounds[0] = 0;
+    while (bounds[n] < nchunks && n < kMaxRanges) {
+        const int hi = (n == kMaxRanges - 1 || bounds[n] + size >= nchunks) ? nchunks : bounds[n] + size;
+        bounds[++n] = hi;
+        size = (size * 5 + 3) / 4;
+    }
+    return n;
+}
+
+size_t chunk_fwd_tc_extra_bytes(int B, int T, int H, int dk, int dv, int nseg) {
+    if (nseg > 1) return sizeof(float) * (size_t)B * H * nseg * dk * ((size_t)(dv + dk) + dv);
+    const int nchunks = (T + C - 1) / C;
+    if (dk == 128 && dv == 128 && chunk_ranges(B, H, nchunks, nseg) > 1)
+        return sizeof(float) * (size_t)B * H * dk * dv;  // state handed between chunk ranges
+    return 0;
 }
 
 int chunk_fwd_tc_auto_segments(int B, int T, int H, int dk, int dv) {
@@ -1774,13 +1925,16 @@ cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, con
                                 int B, int T, int H, int dk, int dv, int segments,
                                 DeviceErrorRecord* err, uint8_t* records, cudaStream_t stream) {
     const ScanShape sh = chunk_fwd_tc_scan_shape(T, segments);
+    // after the records: the scan's maps and start states, or (without a
+    // scan) the state handed between chunk ranges
     float* seg_x = reinterpret_cast<float*>(records + chunk_fwd_tc_record_bytes(B, T, H, dk));
     float* seg_start = seg_x + (size_t)B * H * sh.nseg * dk * (dv + dk);
+    float* handoff = seg_x;
     if (dk == 128)
         return launch_dk<128>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, err, records, sh.nseg,
-                              sh.seg_chunks, seg_x, seg_start, stream);
+                              sh.seg_chunks, seg_x, seg_start, handoff, stream);
     return launch_dk<64>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, err, records, sh.nseg,
-                         sh.seg_chunks, seg_x, seg_start, stream);
+                         sh.seg_chunks, seg_x, seg_start, handoff, stream);
 }
 
 }  // namespace kla

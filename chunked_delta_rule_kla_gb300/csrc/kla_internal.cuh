@@ -54,9 +54,12 @@ cudaError_t launch_chunk_fwd_simt(const void* q, const void* k, const void* v, c
 // `segments` > 1 the chunks of each head are split into segments (the
 // chunk-level scan): a summary pass gives each segment's affine state map, a
 // sequential combine gives each segment's start state, and the carry kernel
-// then runs every segment in parallel.  The scan's buffers
-// (chunk_fwd_tc_scan_bytes) follow the records.  `err` is the device error
-// record at the start of the caller's workspace.
+// then runs every segment in parallel.  Without a scan and with enough free
+// SMs, the chunks are split into up to kMaxRanges ranges whose carries run one after
+// another while the next range's prep overlaps them.  The scan's buffers, or
+// the state handed between ranges (chunk_fwd_tc_extra_bytes), follow the
+// records.  `err` is the device error record at the start of the caller's
+// workspace.
 struct ScanShape {
     int nseg;        // segments per head
     int seg_chunks;  // chunks per segment (the last one may hold fewer)
@@ -65,6 +68,9 @@ struct ScanShape {
 // segment it makes.
 constexpr int kScanTargetCtas = 152;
 constexpr int kScanMinSegChunks = 32;
+// chunk ranges of the unsegmented d_k = d_v = 128 path
+constexpr int kMaxRanges = 8;
+constexpr int kRangeMinChunks = 32;
 
 cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, const float* g,
                                 const float* eta, float eps, const float* h0, void* o, float* hT,
@@ -72,7 +78,11 @@ cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, con
                                 DeviceErrorRecord* err, uint8_t* records, cudaStream_t stream);
 size_t chunk_fwd_tc_record_bytes(int B, int T, int H, int dk);
 ScanShape chunk_fwd_tc_scan_shape(int T, int segments);
-size_t chunk_fwd_tc_scan_bytes(int B, int H, int dk, int dv, int nseg);
+size_t chunk_fwd_tc_extra_bytes(int B, int T, int H, int dk, int dv, int nseg);
+int chunk_ranges(int B, int H, int nchunks, int nseg);
+// Fills bounds[0..n] with the chunk-range limits (bounds[0] = 0,
+// bounds[n] = nchunks) and returns n <= kMaxRanges.
+int chunk_range_bounds(int nchunks, int* bounds);
 int chunk_fwd_tc_auto_segments(int B, int T, int H, int dk, int dv);
 
 }  // namespace kla
