@@ -1909,13 +1909,19 @@ size_t chunk_fwd_tc_extra_bytes(int B, int T, int H, int dk, int dv, int nseg) {
 
 int chunk_fwd_tc_auto_segments(int B, int T, int H, int dk, int dv) {
     const int nchunks = (T + C - 1) / C;
-    // carry CTAs without a scan, and summary CTAs per run: one per head (two
-    // per run) for d_k = d_v = 128, one per 64-column slice otherwise
-    const bool wide = dk == 128 && dv == 128;
-    const long long base = (long long)B * H * (wide ? 1 : dv / DVS);
-    if (base * 2 > kScanTargetCtas) return 1;
-    const long long per_seg = (long long)B * H * (wide ? 2 : (dv + dk) / DVS);
-    long long nseg = kScanTargetCtas / per_seg;
+    const long long heads = (long long)B * H;
+    long long nseg;
+    if (dk == 128 && dv == 128) {
+        // one carry CTA per (head, run): enough runs for one full wave of the
+        // output pass (the summary pass, two CTAs per run, takes about two)
+        if (heads * 4 > kScanTargetCtas) return 1;
+        nseg = kScanTargetCtas / heads;
+    } else {
+        // one carry CTA per 64-column slice: fill one wave of summary CTAs
+        const long long base = heads * (dv / DVS);
+        if (base * 2 > kScanTargetCtas) return 1;
+        nseg = kScanTargetCtas / (heads * ((dv + dk) / DVS));
+    }
     if (nseg > nchunks / kScanMinSegChunks) nseg = nchunks / kScanMinSegChunks;
     return nseg > 1 ? (int)nseg : 1;
 }

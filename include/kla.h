@@ -144,10 +144,13 @@ KLA_API kla_status kla_chunk_fwd_scan(const void* q, const void* k, const void* 
                                       size_t workspace_bytes, void* stream);
 
 /*
- * Segment count kla_chunk_fwd uses for this shape (1 = no scan): with bf16
- * I/O, when the heads' carry work fills less than half of a GB300's 152
- * SMs, enough runs of at least 32 chunks to fill them; otherwise 1.
- * Returns 0 if the arguments are invalid or unsupported.
+ * Segment count kla_chunk_fwd uses for this shape (1 = no scan).  With bf16
+ * I/O and dk = dv = 128, when 4*B*H <= 152 (a GB300's SMs), it is
+ * floor(152 / (B*H)): one full wave of per-(head, run) carry CTAs.  For the
+ * other head dimensions, when the carry's 64-column slices fill less than
+ * half of the SMs, it is as many runs as give one wave of summary CTAs.
+ * Runs hold at least 32 chunks.  Returns 0 if the arguments are invalid or
+ * unsupported.
  */
 KLA_API int kla_chunk_fwd_auto_segments(int B, int T, int H, int dk, int dv, int chunk,
                                         kla_io_dtype io);
