@@ -1648,27 +1648,46 @@ segment_combine_kernel(const float* __restrict__ X, const float* __restrict__ h0
     extern __shared__ float csm[];
     float* Ms = csm;                      // [DK][DK + 1]
     float* Ss = csm + DK * (DK + 1);      // [DK][16]
+    constexpr int kM4 = DK / 8;           // float4 of M_j per thread
     const int col0 = blockIdx.x * 16, h = blockIdx.y, b = blockIdx.z;
     const size_t head = (size_t)b * H + h;
     const int tid = threadIdx.x, i = tid >> 1, cb = (tid & 1) * 8;
     const int ldx = dv + DK;
+    // M_j (the right DK columns of run j's map) is fetched into registers one
+    // step ahead, so its load overlaps the previous step's products
+    float4 mpre[kM4];
+    auto fetch_m = [&](int seg) {
+        const float* Xs = X + (head * nseg + seg) * DK * (size_t)ldx + dv;
+#pragma unroll
+        for (int u = 0; u < kM4; ++u) {
+            const int e4 = tid + u * 2 * DK, row = e4 / (DK / 4), c4 = e4 % (DK / 4);
+            mpre[u] = *reinterpret_cast<const float4*>(Xs + (size_t)row * ldx + 4 * c4);
+        }
+    };
     float sv[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) sv[j] = h0 ? h0[(head * DK + i) * dv + col0 + cb + j] : 0.f;
+    if (nseg > 1) fetch_m(0);
     for (int seg = 0;; ++seg) {
         float* dst = S_start + ((head * nseg + seg) * DK + i) * dv + col0 + cb;
         *reinterpret_cast<float4*>(dst) = make_float4(sv[0], sv[1], sv[2], sv[3]);
         *reinterpret_cast<float4*>(dst + 4) = make_float4(sv[4], sv[5], sv[6], sv[7]);
         if (seg == nseg - 1) break;
-        const float* Xs = X + (head * nseg + seg) * DK * (size_t)ldx;
         __syncthreads();  // the previous step's reads of Ms and Ss are done
-        for (int e = tid; e < DK * DK; e += 2 * DK) Ms[(e / DK) * (DK + 1) + e % DK] = Xs[(e / DK) * (size_t)ldx + dv + e % DK];
+#pragma unroll
+        for (int u = 0; u < kM4; ++u) {
+            const int e4 = tid + u * 2 * DK, row = e4 / (DK / 4), c4 = e4 % (DK / 4);
+            float* m = Ms + row * (DK + 1) + 4 * c4;
+            m[0] = mpre[u].x; m[1] = mpre[u].y; m[2] = mpre[u].z; m[3] = mpre[u].w;
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) Ss[i * 16 + cb + j] = sv[j];
         __syncthreads();
-        float acc[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = Xs[(size_t)i * ldx + col0 + cb + j];
+        if (seg + 1 < nseg - 1) fetch_m(seg + 1);
+        const float* Nrow = X + ((head * nseg + seg) * DK + i) * (size_t)ldx + col0 + cb;
+        const float4 n0 = *reinterpret_cast<const float4*>(Nrow);
+        const float4 n1 = *reinterpret_cast<const float4*>(Nrow + 4);
+        float acc[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
 #pragma unroll 4
         for (int kk = 0; kk < DK; ++kk) {
             const float m = Ms[i * (DK + 1) + kk];
