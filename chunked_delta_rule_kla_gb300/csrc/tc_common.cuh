@@ -142,6 +142,10 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void*
 __device__ __forceinline__ void bulk_wait_read_le1() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
+// Waits until no committed bulk group still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_le0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until every committed bulk store of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
