@@ -296,6 +296,20 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
         const uint32_t lf = (uint32_t)(q * 32) << 16;
         uint8_t* Tbt = sm + L::kTb;
         uint8_t* Tgt = sm + L::kTg;
+        // gates of an item, fetched one item ahead (threads 0..63, one token each)
+        auto fetch_gates = [&](int item, float& gq, float& eq) {
+            gq = 0.f; eq = 0.f;
+            if (pt < C && item < total) {
+                const int c = p.c_lo + item / nheads, hd = item % nheads;
+                if (c * C + pt < T) {
+                    const size_t off = ((size_t)(hd / H) * T + c * C + pt) * H + (hd % H);
+                    gq = p.g[off];
+                    eq = p.eta[off];
+                }
+            }
+        };
+        float gnext, enext;
+        fetch_gates(blockIdx.x, gnext, enext);
         int it = 0;
         for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
         const uint32_t ph = it & 1;
@@ -303,15 +317,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
         const int h = hd % H, b = hd / H;
         const int t0 = c * C;
         const int nvalid = min(C, T - t0);
+        const float gv = gnext, ev = enext;
+        fetch_gates(item + gridDim.x, gnext, enext);
 
         // (T's blocks above the diagonal are A's zeros.)
         // ---- gates and the decay cumsum (threads 0..63 hold rows 0..63)
-        float gv = 0.f, ev = 0.f;
-        if (pt < C && pt < nvalid) {
-            const size_t off = ((size_t)b * T + t0 + pt) * H + h;
-            gv = p.g[off];
-            ev = p.eta[off];
-        }
         if (pt < C) {
             float s = gv;
 #pragma unroll
@@ -562,11 +572,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
             bulk_store(dst, sm + L::kX, Rec<DK>::kGam);
             bulk_store(dst + Rec<DK>::kGam, sm + L::kGam, 768);
             bulk_commit();
+            bulk_wait_read_le0();
+        }
+        bar_sync(1, 128);  // the record has been read out of shared memory
+        }
+        if (pt == 0) {     // this thread's stores complete and its Wk MMAs finish before TMEM is freed
             bulk_wait_all();
-        }
-        bar_sync(1, 128);  // the record has left shared memory
-        }
-        if (pt == 0) {     // this thread's Wk MMAs must finish before TMEM is freed
             mma_commit(&bars[5]);
             const uint64_t tw = globaltimer_ns();
             while (!mbar_try_wait_sleep(&bars[5], 0, kSuspendNs))
