@@ -1122,12 +1122,16 @@ chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 //
 //   [-U^T | 0]                 = -(V^T [Tb ; 0]^T)        A = V^T (smem, MN-major)
 //   [-W^T | S0^T Q^T]         += S0^T [Wk ; Q]^T          one N = 128 product
-//   S_acc                      = Wt^T K,   Wt = diag(exp(gam_C - gam_r)) W
+//   [S_acc | (P W)^T]          = Wt^T [K | P'^T]          one N = 192 product
+//         Wt = diag(exp(gam_C - gam_r)) W,  P'_rs = exp(gam_r - gam_C) (q_r . k_s), s <= r,
+//         so that P' Wt = P W; used when the chunk's decay span is at most
+//         80.  Otherwise S_acc = Wt^T K and (P W)^T = Wb^T P^T with P built
+//         from one exponential per entry and Wb = W in bf16.
 //   S1^T                       = Gam_C S0^T + S_acc       (fp32 master in registers)
-//   o_r                        = Gam_r (S0^T Q^T)[., r] + (Wb^T P^T)[., r]
+//   o_r                        = Gam_r (S0^T Q^T)[., r] + (P W)^T[., r]
 //
 // Roles (14 warps):
-//   warps 0..3   aux: P from Q K^T; the S0^T Q^T half read out early; the
+//   warps 0..3   aux: P'^T (or P) from K Q^T; the S0^T Q^T half read out early; the
 //                outputs (TMEM -> swizzled smem tile -> TMA store)
 //   warps 4..11  state: -W^T -> bf16 Wt^T (the chain) and Wb^T; the update
 //   warp 12      TMA producer (K, [Wk ; Q], V, [Tb ; 0], the record's vectors)
@@ -1150,19 +1154,22 @@ constexpr uint32_t TS_PW = 448;    // Wb^T P^T (fp32, M=128 N=64)
 struct StateLayout {
     // one stage; rows of every tile are tokens, 128-byte swizzle
     static constexpr uint32_t kK = 0;         // K boxes (d 0..63, 64..127)
-    static constexpr uint32_t kWQ = 16384;    // [Wk box kb | Q box kb] at kWQ + 16384 kb
-    static constexpr uint32_t kV = 49152;     // V boxes
-    static constexpr uint32_t kTZ = 65536;    // [T diag(beta) | zeros]
-    static constexpr uint32_t kVec = 81920;   // gam, w, sc (float[64] each)
+    static constexpr uint32_t kPT = 16384;    // P'^T [s][r] (third N block after K) or P [r][s]
+    static constexpr uint32_t kWQ = 24576;    // [Wk box kb | Q box kb] at kWQ + 16384 kb
+    static constexpr uint32_t kV = 57344;     // V boxes
+    static constexpr uint32_t kTZ = 73728;    // [T diag(beta) | zeros]
+    static constexpr uint32_t kVec = 90112;   // gam, w, sc (float[64] each)
     static constexpr uint32_t kStageBytes = ((kVec + 768 + 1023) / 1024) * 1024;
-    static constexpr uint32_t kP = 2 * kStageBytes;       // 2 x [64][64] bf16 (chunk parity)
-    static constexpr uint32_t kO = kP + 2 * 8192;         // 2 x 2 boxes [64 tok][64] bf16
-    static constexpr uint32_t kG = kO + 2 * 16384;        // 2 x 64 floats: Gam_r for the epilogue
-    static constexpr uint32_t kMisc = kG + 512;
+    static constexpr uint32_t kO = 2 * kStageBytes;       // 2 x 2 boxes [64 tok][64] bf16
+    static constexpr uint32_t kG = kO + 2 * 16384;        // 2 x (Gam_r, exp(gam_r - gam_C)) floats[64]
+    static constexpr uint32_t kMisc = kG + 1024;
     static constexpr uint32_t kBars = kMisc + 64;
     static constexpr uint32_t kEnd = kBars + 32 * 8;
     static constexpr size_t kSmemBytes = kEnd + 1024;
 };
+
+// the chunk's decay span allows the factorised forms (every factor finite)
+__device__ __forceinline__ bool span_ok(const float* gam) { return (gam[0] - gam[C - 1]) <= kSpanMax; }
 
 enum { SB_FULL0 = 0, SB_EMPTY0 = SB_FULL0 + kStages, SB_QKB = SB_EMPTY0 + kStages, SB_PR, SB_SR, SB_W,
        SB_WCT, SB_WCB, SB_QSR, SB_S, SB_PW, SB_DRAIN, SB_COUNT };
@@ -1185,7 +1192,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int h = blockIdx.y;
     const int b = blockIdx.z / p.nseg, seg = blockIdx.z % p.nseg;
     const bool vhalf = !SUMMARY || blockIdx.x == 0;     // the values enter this state
-    const int T = p.T, H = p.H, dv = p.dv;
+    const int H = p.H, dv = p.dv;
     const int nchunks = p.nchunks;
     const int c0 = p.c_begin + seg * p.seg_chunks;
     const int nch = min(p.seg_chunks, p.c_end - c0);
@@ -1257,11 +1264,12 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
     } else if (warp == 13) {
         // ================================================================ MMA schedule
-        const uint32_t st0 = smem_u32(sm), sP = smem_u32(sm + L::kP);
+        const uint32_t st0 = smem_u32(sm);
         constexpr int NW = SUMMARY ? 64 : 128;   // [Wk ; Q] rows
         constexpr uint32_t id_u = idesc_bf16(128, NW, true, false, true);   // -(V^T [Tb ; 0]^T)
         constexpr uint32_t id_w = idesc_bf16(128, NW, false, false);        // S0^T [Wk ; Q]^T
         constexpr uint32_t id_s = idesc_bf16(128, 128, false, true);        // Wt^T K
+        constexpr uint32_t id_sp = idesc_bf16(128, 192, false, true);       // Wt^T [K | P'^T]
         constexpr uint32_t id_pw = idesc_bf16(128, 64, false, false);       // Wb^T P^T
         constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);
         auto stage = [&](int cc) { return st0 + (cc % kStages) * L::kStageBytes; };
@@ -1281,28 +1289,33 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                             (vhalf || k > 0) ? 1u : 0u);
             mma_commit(&bars[SB_W]);
         };
-        auto issue_s = [&](int cc) {
+        // S_acc (and with `merged`, (P W)^T in the next 64 columns)
+        auto issue_s = [&](int cc, bool merged) {
             const uint32_t sb = stage(cc);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 mma_bf16_ta(tmem + TS_SA, tmem + TS_WTB + k * 8, sdesc_sw128(sb + L::kK + k * 2048, 8192, 1024),
-                            id_s, k > 0);
+                            merged ? id_sp : id_s, k > 0);
             mma_commit(&bars[SB_S]);
+            if (merged) mma_commit(&bars[SB_PW]);
         };
-        auto issue_qk = [&](int cc) {
+        auto issue_qk = [&](int cc) {  // K Q^T (rows s, columns r)
             const uint32_t sb = stage(cc);
 #pragma unroll
             for (int k = 0; k < DK / 16; ++k)
-                mma_bf16(tmem + TS_QK, sdesc_sw128(sb + L::kWQ + (k / 4) * 16384 + 8192 + (k % 4) * 32, 16, 1024),
-                         sdesc_sw128(sb + L::kK + (k / 4) * 8192 + (k % 4) * 32, 16, 1024), id_qk, k > 0);
+                mma_bf16(tmem + TS_QK, sdesc_sw128(sb + L::kK + (k / 4) * 8192 + (k % 4) * 32, 16, 1024),
+                         sdesc_sw128(sb + L::kWQ + (k / 4) * 16384 + 8192 + (k % 4) * 32, 16, 1024), id_qk, k > 0);
             mma_commit(&bars[SB_QKB]);
         };
         auto issue_pw = [&](int cc) {
-            const uint32_t sPc = sP + (cc & 1) * 8192;
+            const uint32_t sPc = stage(cc) + L::kPT;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 mma_bf16_ta(tmem + TS_PW, tmem + TS_WBB + k * 8, sdesc_sw128(sPc + k * 32, 16, 1024), id_pw, k > 0);
             mma_commit(&bars[SB_PW]);
+        };
+        auto chunk_span_ok = [&](int cc) {
+            return span_ok(reinterpret_cast<const float*>(sm + (cc % kStages) * L::kStageBytes + L::kVec));
         };
         // warp-uniform non-blocking test of a barrier phase
         auto ready = [&](int slot, uint32_t parity) {
@@ -1328,7 +1341,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 if (!(ok = wt.warp(SB_WCT, par, kWhereWR, c))) break;
                 tc_fence_after();
                 if (elect_one()) {
-                    issue_s(c);
+                    issue_s(c, false);
                     mma_commit(&bars[SB_EMPTY0 + c % kStages]);
                 }
                 __syncwarp();
@@ -1360,11 +1373,13 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     __syncwarp();
                     fW = prog = true;
                 }
-                if (fW && !fS && ready(SB_WCT, par)) {
+                const bool merged = chunk_span_ok(c);
+                if (fW && !fS && ready(SB_WCT, par) && (!merged || ready(SB_PR, par))) {
                     tc_fence_after();
-                    if (elect_one()) issue_s(c);
+                    if (elect_one()) issue_s(c, merged);
                     __syncwarp();
                     fS = prog = true;
+                    if (merged) fPW = true;
                 }
                 if (fS && !fU) {
                     if (c + 1 >= nch) {
@@ -1376,7 +1391,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         fU = prog = true;
                     }
                 }
-                if (fW && !fPW && ready(SB_PR, par) && ready(SB_WCB, par)) {
+                if (fW && !fPW && !merged && ready(SB_PR, par) && ready(SB_WCB, par)) {
                     tc_fence_after();
                     if (elect_one()) issue_pw(c);
                     __syncwarp();
@@ -1484,14 +1499,16 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tc_fence_before();
             bar_sync(1, 256);
             if (st_id == 0) mbar_arrive(&bars[SB_WCT]);
-            // ---- Wb^T, once P W of the previous chunk has read the last one
+            // ---- Wb^T (strong decay only), once P W of the previous chunk has read the last one
             if (!SUMMARY) {
-                if (c > 0 && !wt.group(SB_PW, par ^ 1u, kWherePW, c, 3, 256)) break;
-                tc_fence_after();
-                tmem_st_32x32b_x16u(tmem + lf + TS_WBB + 16 * hh, pb);
-                tmem_st_wait();
-                tc_fence_before();
-                bar_sync(1, 256);
+                if (!span_ok(vec)) {
+                    if (c > 0 && !wt.group(SB_PW, par ^ 1u, kWherePW, c, 3, 256)) break;
+                    tc_fence_after();
+                    tmem_st_32x32b_x16u(tmem + lf + TS_WBB + 16 * hh, pb);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    bar_sync(1, 256);
+                }
                 if (st_id == 0) mbar_arrive(&bars[SB_WCB]);
             }
             // ---- S1^T = Gam_C S0^T + S_acc; bf16 copy for the next chunk
@@ -1536,49 +1553,49 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const uint32_t par = c & 1;
             const int t0 = (c0 + c) * C;
             const float* gam = reinterpret_cast<const float*>(sm + (c % kStages) * L::kStageBytes + L::kVec);
-            const float* wfac = gam + C;
-            float* Gp = reinterpret_cast<float*>(sm + L::kG) + par * C;
-            // ---- P = mask(exp(gam_r - gam_s) Q K^T) -> bf16 tile; Gam_r kept for the epilogue
+            float* Gp = reinterpret_cast<float*>(sm + L::kG) + par * C;  // Gam_r
+            // ---- from K Q^T (lane row s): P'^T [s][r] = exp(gam_r - gam_C) (k_s . q_r) for s <= r,
+            // rows written whole; with strong decay P [r][s] = exp(gam_r - gam_s) (q_r . k_s),
+            // columns written element by element.  Gam_r is kept for the epilogue.
             if (!wt.group(SB_QKB, par, kWherePR, c, 4, 128)) break;
             tc_fence_after();
+            float* Fr = reinterpret_cast<float*>(sm + L::kG) + 2 * C + par * C;  // exp(gam_r - gam_C)
             {
-                float qk[64];
+                float kq[64];
                 {
                     float lo[32], hi[32];
                     tmem_ld_32x32b_x32(tmem + lf + TS_QK, lo);
                     tmem_ld_32x32b_x32(tmem + lf + TS_QK + 32, hi);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) { qk[i] = lo[i]; qk[32 + i] = hi[i]; }
+                    for (int i = 0; i < 32; ++i) { kq[i] = lo[i]; kq[32 + i] = hi[i]; }
                 }
-                if (at < C) Gp[at] = __expf(gam[at]);
+                const bool fact = span_ok(gam);
+                if (at < C) {
+                    Gp[at] = __expf(gam[at]);
+                    Fr[at] = __expf(gam[at] - gam[C - 1]);
+                }
+                bar_sync(2, 128);
+                uint8_t* Pt = sm + (c % kStages) * L::kStageBytes + L::kPT;
                 if (m64) {
-                    const float gr = gam[r64];
-                    const float gamm = gam[C / 2 - 1];
-                    const bool fact = (gam[0] - gam[C - 1]) <= kSpanMax;
-                    uint8_t* Pt = sm + L::kP + par * 8192;
+                    const int sr = r64;  // this lane's row s
                     if (fact) {
-                        const float ur = __expf(gr - gamm);
 #pragma unroll
                         for (int c8 = 0; c8 < 8; ++c8) {
-                            const float4 w0 = *reinterpret_cast<const float4*>(wfac + c8 * 8);
-                            const float4 w1 = *reinterpret_cast<const float4*>(wfac + c8 * 8 + 4);
-                            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                            float v[8];
+                            const float4 f0 = *reinterpret_cast<const float4*>(Fr + c8 * 8);
+                            const float4 f1 = *reinterpret_cast<const float4*>(Fr + c8 * 8 + 4);
+                            const float fv[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+                            float vv[8];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) v[i] = (c8 * 8 + i <= r64) ? ur * wv[i] * qk[c8 * 8 + i] : 0.f;
-                            ST_CHUNK(Pt, r64, c8, v, 0);
+                            for (int i = 0; i < 8; ++i) vv[i] = (sr <= c8 * 8 + i) ? fv[i] * kq[c8 * 8 + i] : 0.f;
+                            ST_CHUNK(Pt, sr, c8, vv, 0);
                         }
                     } else {
+                        const float gs = gam[sr];
 #pragma unroll
-                        for (int c8 = 0; c8 < 8; ++c8) {
-                            float v[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const int s2 = c8 * 8 + i;
-                                v[i] = (s2 <= r64) ? __expf(gr - gam[s2]) * qk[s2] : 0.f;
-                            }
-                            ST_CHUNK(Pt, r64, c8, v, 0);
+                        for (int rr = 0; rr < C; ++rr) {
+                            const float pv = (sr <= rr) ? __expf(gam[rr] - gs) * kq[rr] : 0.f;
+                            *reinterpret_cast<__nv_bfloat16*>(Pt + sw128_offset(rr, sr)) = __float2bfloat16_rn(pv);
                         }
                     }
                 }
