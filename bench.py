@@ -77,17 +77,28 @@ def load_peaks():
         return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
-def roofline(work, seconds, peaks):
+# DRAM bytes (read + write) per call, from one ncu capture of the same
+# command (profiles/): every launch of one call, serialised with cold caches,
+# so writes still in L2 when a launch ends are not counted.  Refresh these
+# whenever the kernels change.
+TRAFFIC_BYTES = {
+    "train_prefill_bf16_B8H8T4096d128": 398.5e6,
+    "long_prefill_bf16_B1H16T131072d128": 6223.6e6,
+    "decode_bf16_B64H16d128_x1024": 71.7e6,
+}
+
+
+def roofline(work, seconds, peaks, traffic=None):
     t_mem = work["bytes"] / (peaks["hbm"] * 1e9)
     t_flop = work["flops"] / (peaks["bf16"] * 1e12)
     if t_mem >= t_flop:
         ach = work["bytes"] / seconds / 1e9
         return dict(bound="hbm", achieved=round(ach, 1), peak=peaks["hbm"], unit="GB/s",
-                    frac=round(ach / peaks["hbm"], 4), traffic=None,
+                    frac=round(ach / peaks["hbm"], 4), traffic=traffic,
                     peak_source=peaks["source"], roofline_us=round(t_mem * 1e6, 2))
     ach = work["flops"] / seconds / 1e12
     return dict(bound="tensor", achieved=round(ach, 2), peak=peaks["bf16"], unit="TFLOP/s",
-                frac=round(ach / peaks["bf16"], 4), traffic=None,
+                frac=round(ach / peaks["bf16"], 4), traffic=traffic,
                 peak_source=peaks["source"], roofline_us=round(t_flop * 1e6, 2))
 
 
@@ -255,7 +266,9 @@ def bench_prefill(case, K, W, flush, peaks, stream, e2e=True):
                job_tokens_per_s=job_tps,
                tflops=work["flops"] / (mean_ms * 1e-3) / 1e12,
                gbps=work["bytes"] / (mean_ms * 1e-3) / 1e9,
-               roofline=roofline(work, mean_ms * 1e-3, peaks), work=work,
+               roofline=dict(roofline(work, mean_ms * 1e-3, peaks, TRAFFIC_BYTES.get(case.name)),
+                             scope="one kla_chunk_fwd call: all its launches (prep and carry kernels)",
+                             peak_kind="burst copy bandwidth"), work=work,
                launches=K * prefill_launches(kla, case), min_ms=min(ms),
                segments=kla.kla_chunk_fwd_auto_segments(B, T, H, dk, dv, case.chunk))
 
@@ -315,7 +328,10 @@ def bench_decode(case, K_loops, W_loops, peaks, stream, n_states=4, e2e=True):
     work = decode_work(case)
     per_call_s = max_over_ranks(sum(ms) / len(ms) / steps * 1e-3)
     res = dict(ms_per_call=per_call_s * 1e3, tokens_per_s=work["tokens"] / per_call_s,
-               gbps=work["bytes"] / per_call_s / 1e9, roofline=roofline(work, per_call_s, peaks),
+               gbps=work["bytes"] / per_call_s / 1e9,
+               roofline=dict(roofline(work, per_call_s, peaks, TRAFFIC_BYTES.get(case.name)),
+                             scope="one kla_decode_step call (decode_tma_kernel)",
+                             peak_kind="burst copy bandwidth"),
                work=work, launches=K_loops * steps * LAUNCHES_PER_DECODE, calls_per_loop=steps,
                states_rotated=n_states)
 
