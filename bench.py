@@ -237,6 +237,8 @@ def prefill_launches(kla, case) -> int:
     if segs > 1:
         return 4
     nchunks = -(-case.T // case.chunk)
+    if case.dk == 128 and case.dv == 128 and 2 * case.B * case.H <= GB300_SMS:
+        return 1   # prep and carry in one cooperative grid
     if (case.dk == 128 and case.dv == 128 and nchunks >= RANGE_MIN_CHUNKS
             and case.B * case.H + 16 <= GB300_SMS):
         return 2 * chunk_ranges(nchunks)

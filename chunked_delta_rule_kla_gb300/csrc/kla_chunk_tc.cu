@@ -80,7 +80,7 @@ struct Rec {
 
 enum : unsigned { kWhereFull = 1, kWhereEmpty, kWhereGQ, kWhereT, kWhereWK, kWhereWKR, kWhereSR,
                   kWhereW, kWhereEPI, kWhereWR, kWhereWB, kWhereS, kWherePW, kWherePR, kWhereDrain,
-                  kWherePrepK, kWherePrepG };
+                  kWherePrepK, kWherePrepG, kWhereFlag };
 
 // Named barriers used in both kernels (id 0 is __syncthreads).
 __device__ __forceinline__ void bar_sync(int id, int n) {
@@ -195,21 +195,49 @@ struct PrepParams {
     int pdl_wait;           // launched as a programmatic dependent: wait for the primary at exit
 };
 
-// Persistent: each CTA walks items blockIdx.x, blockIdx.x + gridDim.x, ...;
-// warp 0 fetches the next item's K tile as soon as the current Wk product
-// has read the tile.
+// Ready flags between the prep and the carry inside one grid: the prep's
+// record store completes, is ordered before the flag's release, and the
+// carry's bulk copies of the record follow the flag's acquire.
+__device__ __forceinline__ void publish_ready(int* flag) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
+}
+__device__ __forceinline__ int load_acquire(const int* flag) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    return v;
+}
+
+// One prep lane: 5 warps (160 threads) over one PrepLayout region of shared
+// memory and 128 TMEM columns, walking items item0, item0 + istride, ...
+// (chunk-major).  Warp 0 fetches the next item's K tile as soon as the
+// current Wk product has read the tile.
+struct PrepLane {
+    int tid;            // 0..159 within the lane
+    int wbase;          // CTA warp index of the lane's warp 0 (TMEM lane quadrants follow it)
+    int bar0;           // first of the lane's three named barriers
+    int item0, istride;
+    int* flags;         // per-(head, chunk) ready flags, published once a record is stored; or null
+};
+
+// barriers 0: K loaded, 1: K K^T, 2: Wk, 3: TMEM read (Wk converted), 4, 5: drains
 template <int DK>
-__global__ void __launch_bounds__(kPrepThreads, kPrepPerSm)
-chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) {
+__device__ __forceinline__ void prep_lane_init(uint8_t* sm) {
+    using L = PrepLayout<DK>;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBars);
+    for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
+    *reinterpret_cast<volatile int*>(sm + L::kMisc + 32) = 0;
+    fence_mbar_init();
+}
+
+template <int DK>
+__device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepParams& p, uint8_t* sm,
+                                          const uint32_t tmem, const PrepLane& ln) {
     using L = PrepLayout<DK>;
     constexpr int KB = L::KB;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    // 0: K loaded, 1: K K^T, 2: Wk, 3: TMEM read (Wk converted), 4, 5: drains
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBars);
     float* misc = reinterpret_cast<float*>(sm + L::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 32);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kMisc + 48);
     float* gam = reinterpret_cast<float*>(sm + L::kGam);
     float* bet = reinterpret_cast<float*>(sm + L::kBet);
     float* betg = bet + C;
@@ -219,26 +247,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
     float* Rw = reinterpret_cast<float*>(sm + L::kRw);
     float* AdT = reinterpret_cast<float*>(sm + L::kAdT);
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = ln.tid, warp = tid >> 5, lane = tid & 31;
     const int T = p.T, H = p.H;
     const int nheads = p.B * H;
     const int total = (p.c_hi - p.c_lo) * nheads;
+    const int item0 = ln.item0, istride = ln.istride;
+    const int B1 = ln.bar0, B2 = ln.bar0 + 1, B3 = ln.bar0 + 2;   // 128, 64 and 128 threads
     Waiter wt{bars, abort_flag, p.err};
-
-    if (tid == 0) {
-        for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    }
-    if (warp == 0) {
-        tmem_alloc(tmem_slot, 128);  // K K^T, later Wk (the Gram rows are consumed first)
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -249,13 +264,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
                 mbar_arrive_expect_tx(&bars[0], KB * 8192);
 #pragma unroll
                 for (int kb = 0; kb < KB; ++kb)
-                    tma_load_4d(sm + L::kK + kb * 8192, &tm_k, &bars[0], kb * 64, hd % H, c * C, hd / H);
+                    tma_load_4d(sm + L::kK + kb * 8192, tm_kp, &bars[0], kb * 64, hd % H, c * C, hd / H);
                 ++loads;
                 inflight = true;
             };
             int it = 0;
-            if ((int)blockIdx.x < total) load(blockIdx.x);
-            for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
+            if (item0 < total) load(item0);
+            for (int item = item0; item < total; item += istride, ++it) {
                 const uint32_t ph = it & 1;
                 const int c = p.c_lo + item / nheads;
                 if (!wt.poll(0, ph, kWherePrepK, c)) break;
@@ -274,7 +289,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
                 mma_commit(&bars[1]);
                 // Wk = Tg K has read the tile: fetch the next one
                 if (!wt.poll(2, ph, kWherePrepG, c)) break;
-                if (item + (int)gridDim.x < total) load(item + gridDim.x);
+                if (item + istride < total) load(item + istride);
             }
             // in-flight copies and MMAs must finish before the CTA exits
             if (inflight) {
@@ -290,7 +305,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
         __syncwarp();
     } else {
         const int pt = tid - 32;                 // 0..127
-        const int q = warp & 3;                  // TMEM lane quadrant
+        const int q = (ln.wbase + warp) & 3;     // TMEM lane quadrant of this warp
         const bool m64 = lane < 16;              // holds a row of the M=64 Gram product
         const int r = q * 16 + lane;             // that row
         const uint32_t lf = (uint32_t)(q * 32) << 16;
@@ -309,16 +324,21 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
             }
         };
         float gnext, enext;
-        fetch_gates(blockIdx.x, gnext, enext);
+        fetch_gates(item0, gnext, enext);
+        int pending = -1;  // (thread 0) item whose record store is not yet published
+        auto publish = [&](int item) {
+            const int c = p.c_lo + item / nheads, hd = item % nheads;
+            publish_ready(ln.flags + (size_t)hd * p.nchunks + c);
+        };
         int it = 0;
-        for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
+        for (int item = item0; item < total; item += istride, ++it) {
         const uint32_t ph = it & 1;
         const int c = p.c_lo + item / nheads, hd = item % nheads;
         const int h = hd % H, b = hd / H;
         const int t0 = c * C;
         const int nvalid = min(C, T - t0);
         const float gv = gnext, ev = enext;
-        fetch_gates(item + gridDim.x, gnext, enext);
+        fetch_gates(item + istride, gnext, enext);
 
         // (T's blocks above the diagonal are A's zeros.)
         // ---- gates and the decay cumsum (threads 0..63 hold rows 0..63)
@@ -330,13 +350,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
                 if (lane >= off) s += n;
             }
             if (pt == 31) misc[0] = s;
-            bar_sync(2, 64);
+            bar_sync(B2, 64);
             if (pt >= 32) s += misc[0];
             gam[pt] = s;
             bet[pt] = ev;  // eta for now; beta below
         }
         // ---- K K^T rows
-        if (!wt.group(1, ph, kWherePrepG, c, 3, 128)) break;
+        if (!wt.group(1, ph, kWherePrepG, c, B3, 128)) break;
         tc_fence_after();
         {
             float row[64];
@@ -362,7 +382,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
                 gr = gam[r];
                 br = (r < nvalid) ? bet[r] / (kk + p.eps) : 0.f;
             }
-            bar_sync(1, 128);  // every thread has read eta from bet[]
+            bar_sync(B1, 128);  // every thread has read eta from bet[]
             if (m64) {
                 bet[r] = br;
                 betg[r] = br * __expf(gr);
@@ -372,7 +392,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
                 wf[pt] = __expf(gamm - gam[pt]);
                 reinterpret_cast<float*>(sm + L::kSc)[pt] = __expf(gam[C - 1] - gam[pt]);
             }
-            bar_sync(1, 128);
+            bar_sync(B1, 128);
             const bool fact = (gam[0] - gam[C - 1]) <= kSpanMax;
             // ---- A rows (64 threads) and the transposed diagonal blocks
             if (m64) {
@@ -404,7 +424,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
                 for (int i = 0; i < 16; ++i) adt[i * 16] = arow[16 * I + i];
             }
         }
-        bar_sync(1, 128);
+        bar_sync(B1, 128);
+        if (pt == 0 && pending >= 0) {  // that store has long completed; publish it
+            bulk_wait_all();
+            publish(pending);
+            pending = -1;
+        }
         // ---- T = (I + A)^{-1}: diagonal 16x16 blocks, right-looking
         if (pt < 64) {
             const int I = pt >> 4, j = pt & 15;
@@ -428,7 +453,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) t[rr * LDF] = x[rr];
         }
-        bar_sync(1, 128);
+        bar_sync(B1, 128);
         // ---- T_10 = -T_11 (A_10 T_00), T_32 = -T_33 (A_32 T_22): 64 threads, 2x4 each
         if (pt < 64) {
             const int bs = pt >> 5, rem = pt & 31, r0 = (rem >> 2) * 2, c0 = (rem & 3) * 4;
@@ -448,7 +473,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
             *reinterpret_cast<float4*>(&R[r0 * LDF + c0]) = make_float4(y[0][0], y[0][1], y[0][2], y[0][3]);
             *reinterpret_cast<float4*>(&R[(r0 + 1) * LDF + c0]) = make_float4(y[1][0], y[1][1], y[1][2], y[1][3]);
         }
-        bar_sync(1, 128);
+        bar_sync(B1, 128);
         if (pt < 64) {
             const int bs = pt >> 5, rem = pt & 31, r0 = (rem >> 2) * 2, c0 = (rem & 3) * 4;
             const int J = 2 * bs, I = J + 1;
@@ -469,7 +494,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
             *reinterpret_cast<float4*>(&Tf[(16 * I + r0 + 1) * LDF + 16 * J + c0]) =
                 make_float4(-z[1][0], -z[1][1], -z[1][2], -z[1][3]);
         }
-        bar_sync(1, 128);
+        bar_sync(B1, 128);
         // ---- T_ba = -T_b (A_ba T_a): 128 threads, 2x4 each
         {
             const int r0 = (pt >> 3) * 2, c0 = (pt & 7) * 4;
@@ -486,7 +511,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
             }
             *reinterpret_cast<float4*>(&Rw[r0 * LDF + c0]) = make_float4(y[0][0], y[0][1], y[0][2], y[0][3]);
             *reinterpret_cast<float4*>(&Rw[(r0 + 1) * LDF + c0]) = make_float4(y[1][0], y[1][1], y[1][2], y[1][3]);
-            bar_sync(1, 128);
+            bar_sync(B1, 128);
             float z[2][4] = {};
 #pragma unroll
             for (int m = 0; m < 32; ++m) {
@@ -501,7 +526,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
             *reinterpret_cast<float4*>(&Tf[(32 + r0) * LDF + c0]) = make_float4(-z[0][0], -z[0][1], -z[0][2], -z[0][3]);
             *reinterpret_cast<float4*>(&Tf[(33 + r0) * LDF + c0]) = make_float4(-z[1][0], -z[1][1], -z[1][2], -z[1][3]);
         }
-        bar_sync(1, 128);
+        bar_sync(B1, 128);
         // ---- Tb = T diag(beta), Tg = T diag(beta Gam): 128 threads, 2 x 8 columns each.
         // The tiles overwrite T, so each thread first takes its half-row.
         {
@@ -512,7 +537,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
                 ta[u][0] = *reinterpret_cast<const float4*>(&Tf[rr * LDF + (col8 + u) * 8]);
                 ta[u][1] = *reinterpret_cast<const float4*>(&Tf[rr * LDF + (col8 + u) * 8 + 4]);
             }
-            bar_sync(1, 128);
+            bar_sync(B1, 128);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int c8 = col8 + u;
@@ -536,7 +561,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
             }
         }
         fence_proxy_async_smem();
-        bar_sync(1, 128);
+        bar_sync(B1, 128);
         // ---- Wk = Tg K (M=64, N=dk; K as the MN-major B operand)
         if (pt == 0) {
             tc_fence_after();
@@ -548,7 +573,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
                          sdesc_sw128(sK + k * 2048, 8192, 1024), id_wk, k > 0);
             mma_commit(&bars[2]);
         }
-        if (!wt.group(2, ph, kWherePrepG, c, 3, 128)) break;
+        if (!wt.group(2, ph, kWherePrepG, c, B3, 128)) break;
         tc_fence_after();
         {
             uint8_t* Wkt = sm + L::kWk;
@@ -565,7 +590,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
         }
         tc_fence_before();
         fence_proxy_async_smem();
-        bar_sync(1, 128);
+        bar_sync(B1, 128);
         if (pt == 0) {
             mbar_arrive(&bars[3]);  // TMEM free for the next item's K K^T
             uint8_t* dst = p.rec + (((size_t)b * H + h) * p.nchunks + c) * Rec<DK>::kBytes;
@@ -573,17 +598,43 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
             bulk_store(dst + Rec<DK>::kGam, sm + L::kGam, 768);
             bulk_commit();
             bulk_wait_read_le0();
+            if (ln.flags) pending = item;
         }
-        bar_sync(1, 128);  // the record has been read out of shared memory
+        bar_sync(B1, 128);  // the record has been read out of shared memory
         }
         if (pt == 0) {     // this thread's stores complete and its Wk MMAs finish before TMEM is freed
             bulk_wait_all();
+            if (pending >= 0) publish(pending);
             mma_commit(&bars[5]);
             const uint64_t tw = globaltimer_ns();
             while (!mbar_try_wait_sleep(&bars[5], 0, kSuspendNs))
                 if (globaltimer_ns() - tw > kTimeoutNs) { wt.fail(kWhereDrain, -1); break; }
         }
     }
+}
+
+// Persistent prep grid: one lane per CTA; CTA i walks items i, i + gridDim.x, ...
+template <int DK>
+__global__ void __launch_bounds__(kPrepThreads, kPrepPerSm)
+chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) {
+    using L = PrepLayout<DK>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kMisc + 48);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    if (tid == 0) {
+        prep_lane_init<DK>(sm);
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 128);  // K K^T, later Wk (the Gram rows are consumed first)
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    prep_lane<DK>(&tm_k, p, sm, tmem, PrepLane{tid, 0, 1, (int)blockIdx.x, (int)gridDim.x, nullptr});
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1172,26 +1223,27 @@ struct StateLayout {
 __device__ __forceinline__ bool span_ok(const float* gam) { return (gam[0] - gam[C - 1]) <= kSpanMax; }
 
 enum { SB_FULL0 = 0, SB_EMPTY0 = SB_FULL0 + kStages, SB_QKB = SB_EMPTY0 + kStages, SB_PR, SB_SR, SB_W,
-       SB_WCT, SB_WCB, SB_QSR, SB_S, SB_PW, SB_DRAIN, SB_COUNT };
+       SB_WCT, SB_WCB, SB_QSR, SB_S, SB_PW, SB_DRAIN, SB_SLD, SB_SFREE, SB_COUNT };
 
+// One carry CTA: warps 0..13 take the roles above; any further warp only
+// joins the CTA-wide barriers.  (bx, h, bz) play the roles of the grid
+// coordinates (x: the SUMMARY half, y: head, z: batch * runs + run).  With
+// `flags`, the record of a chunk is copied only once its flag is set.
 template <bool SUMMARY>
-__global__ void __launch_bounds__(kStateThreads, 1)
-chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                   const CarryParams p) {
+__device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                          const CUtensorMap& tm_v, const CUtensorMap& tm_o,
+                                          const CarryParams& p, uint8_t* sm, const int bx, const int h,
+                                          const int bz, const int* flags) {
     using L = StateLayout;
     using R = Rec<128>;
     constexpr int DK = 128;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 32);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kMisc + 48);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.y;
-    const int b = blockIdx.z / p.nseg, seg = blockIdx.z % p.nseg;
-    const bool vhalf = !SUMMARY || blockIdx.x == 0;     // the values enter this state
+    const int b = bz / p.nseg, seg = bz % p.nseg;
+    const bool vhalf = !SUMMARY || bx == 0;             // the values enter this state
     const int H = p.H, dv = p.dv;
     const int nchunks = p.nchunks;
     const int c0 = p.c_begin + seg * p.seg_chunks;
@@ -1208,7 +1260,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
     if (!SUMMARY) {  // the zero halves of [T diag(beta) | 0], never loaded
-        for (int i = tid; i < kStages * 2048; i += kStateThreads) {
+        for (int i = tid; i < kStages * 2048; i += (int)blockDim.x) {
             const int s = i / 2048, e = i % 2048;
             reinterpret_cast<uint32_t*>(sm + s * L::kStageBytes + L::kTZ + 8192)[e] = 0u;
         }
@@ -1222,6 +1274,50 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+
+    // Stage c holds chunk c0 + c: its K, Q, V tiles (inputs of the call) and
+    // its record (written by the prep grid).  One arrive with the stage's
+    // whole byte count, then the two groups of copies.
+    const uint32_t stage_bytes = 16384u + (SUMMARY ? 0u : 16384u) + (vhalf ? 16384u : 0u) + 8192u + 16384u + 768u;
+    auto load_inputs = [&](int c) {
+        uint8_t* st = sm + (c % kStages) * L::kStageBytes;
+        uint64_t* full = &bars[SB_FULL0 + c % kStages];
+        const int t0 = (c0 + c) * C;
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            tma_load_4d(st + L::kK + kb * 8192, &tm_k, full, kb * 64, h, t0, b);
+            if (!SUMMARY) tma_load_4d(st + L::kWQ + kb * 16384 + 8192, &tm_q, full, kb * 64, h, t0, b);
+            if (vhalf) tma_load_4d(st + L::kV + kb * 8192, &tm_v, full, kb * 64, h, t0, b);
+        }
+    };
+    auto load_record = [&](int c) {
+        uint8_t* st = sm + (c % kStages) * L::kStageBytes;
+        uint64_t* full = &bars[SB_FULL0 + c % kStages];
+        const uint8_t* rec = p.rec + (head * nchunks + c0 + c) * R::kBytes;
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) bulk_load(st + L::kWQ + kb * 16384, rec + R::kWk + kb * 8192, 8192, full);
+        bulk_load(st + L::kTZ, rec + R::kTb, 8192, full);
+        bulk_load(st + L::kVec, rec + R::kGam, 768, full);
+    };
+    // The start state (fp32 [DK][dv], 64 KB) comes in through stage 1 with a
+    // bulk copy: plain loads of it by the state warps were limited by the
+    // loads one SM keeps in flight.  Stage 1 is filled with its chunk once
+    // the state warps have read the state (SB_SFREE).
+    const float* s_start = (!SUMMARY && p.s_in) ? p.s_in + ((size_t)head * p.nseg + seg) * DK * dv : nullptr;
+    constexpr uint32_t kStartBytes = DK * 128 * 4;   // dv = 128 here
+    const int first = s_start ? (nch < 1 ? nch : 1) : (nch < kStages ? nch : kStages);
+    if (warp == 12 && lane == 0) {
+        // No grid of this call writes q, k or v, so the first stages' input
+        // tiles are requested before the dependency wait below and arrive
+        // while the grids before this one finish.
+        tma_prefetch_desc(&tm_k);
+        if (!SUMMARY) tma_prefetch_desc(&tm_q);
+        if (vhalf) tma_prefetch_desc(&tm_v);
+        for (int c = 0; c < first; ++c) {
+            mbar_arrive_expect_tx(&bars[SB_FULL0 + c], stage_bytes);
+            load_inputs(c);
+        }
+    }
     // launched as a programmatic dependent of a prep grid: its records (and,
     // through it, the previous range's state) are complete after this wait;
     // a no-op for an ordinary launch
@@ -1230,30 +1326,42 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (warp == 12) {
         // ================================================================ TMA producer
         if (lane == 0) {
-            tma_prefetch_desc(&tm_k);
-            if (!SUMMARY) tma_prefetch_desc(&tm_q);
-            if (vhalf) tma_prefetch_desc(&tm_v);
-            const uint32_t bytes = 16384u + (SUMMARY ? 0u : 16384u) + (vhalf ? 16384u : 0u) + 8192u + 16384u + 768u;
+            if (s_start) {
+                mbar_arrive_expect_tx(&bars[SB_SLD], kStartBytes);
+#pragma unroll
+                for (int part = 0; part < 4; ++part)
+                    bulk_load(sm + L::kStageBytes + part * (kStartBytes / 4), s_start + part * (kStartBytes / 16),
+                              kStartBytes / 4, &bars[SB_SLD]);
+            }
             int issued = 0;
             for (int c = 0; c < nch; ++c) {
-                const int s = c % kStages;
-                if (c >= kStages && !wt.poll(SB_EMPTY0 + s, ((c / kStages) - 1) & 1, kWhereEmpty, c)) break;
-                uint8_t* st = sm + s * L::kStageBytes;
-                uint64_t* full = &bars[SB_FULL0 + s];
-                mbar_arrive_expect_tx(full, bytes);
-                const int cg = c0 + c;
-                const int t0 = cg * C;
-                const uint8_t* rec = p.rec + (head * nchunks + cg) * R::kBytes;
-#pragma unroll
-                for (int kb = 0; kb < 2; ++kb) {
-                    tma_load_4d(st + L::kK + kb * 8192, &tm_k, full, kb * 64, h, t0, b);
-                    if (!SUMMARY) tma_load_4d(st + L::kWQ + kb * 16384 + 8192, &tm_q, full, kb * 64, h, t0, b);
-                    if (vhalf) tma_load_4d(st + L::kV + kb * 8192, &tm_v, full, kb * 64, h, t0, b);
-                    bulk_load(st + L::kWQ + kb * 16384, rec + R::kWk + kb * 8192, 8192, full);
+                if (c >= first) {
+                    const int s = c % kStages;
+                    const bool freed = c >= kStages ? wt.poll(SB_EMPTY0 + s, ((c / kStages) - 1) & 1, kWhereEmpty, c)
+                                                    : wt.poll(SB_SFREE, 0, kWhereEmpty, c);   // held the start state
+                    if (!freed) break;
+                    mbar_arrive_expect_tx(&bars[SB_FULL0 + s], stage_bytes);
+                    load_inputs(c);
                 }
-                bulk_load(st + L::kTZ, rec + R::kTb, 8192, full);
-                bulk_load(st + L::kVec, rec + R::kGam, 768, full);
+                // the record is copied even after a failed flag wait so that
+                // every armed stage completes; the abort flag stops the rest
+                bool ready = true;
+                if (flags) {
+                    const int* f = flags + head * nchunks + c0 + c;
+                    const uint64_t t0 = globaltimer_ns();
+                    while (load_acquire(f) == 0) {
+                        if (*abort_flag || globaltimer_ns() - t0 > kTimeoutNs) {
+                            wt.fail(kWhereFlag, c);
+                            ready = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
+                load_record(c);
                 issued = c + 1;
+                if (!ready) break;
             }
             for (int c = (issued > kStages ? issued - kStages : 0); c < issued; ++c) {
                 const uint64_t t0 = globaltimer_ns();
@@ -1438,7 +1546,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 12) {
         // ================================================================ state warps
         const int q = warp & 3, hh = (warp - 4) >> 2;
         const int j = q * 32 + lane;                      // state column (TMEM lane)
@@ -1446,12 +1554,13 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int st_id = tid - 128;                      // 0..255
         float master[64];                                 // S^T[j][64 hh + i]
         {
-            const float* src = SUMMARY ? nullptr
-                                       : (p.s_in ? p.s_in + ((size_t)head * p.nseg + seg) * DK * dv : nullptr);
+            // a failed wait leaves zeros; the abort flag then ends every loop
+            const bool staged = s_start && wt.group(SB_SLD, 0, kWhereFull, -1, 3, 256);
+            const float* sst = reinterpret_cast<const float*>(sm + L::kStageBytes);   // [DK][128]
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
                 const int d = 64 * hh + i;
-                master[i] = SUMMARY ? ((!vhalf && d == j) ? 1.f : 0.f) : (src ? src[(size_t)d * dv + j] : 0.f);
+                master[i] = SUMMARY ? ((!vhalf && d == j) ? 1.f : 0.f) : (staged ? sst[d * 128 + j] : 0.f);
             }
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
@@ -1463,7 +1572,10 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tmem_st_wait();
             tc_fence_before();
             bar_sync(1, 256);
-            if (st_id == 0) mbar_arrive(&bars[SB_SR]);
+            if (st_id == 0) {
+                mbar_arrive(&bars[SB_SR]);
+                if (s_start) mbar_arrive(&bars[SB_SFREE]);
+            }
         }
         for (int c = 0; c < nch; ++c) {
             const uint32_t par = c & 1;
@@ -1541,7 +1653,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
             for (int i = 0; i < 64; ++i) dst[(size_t)(64 * hh + i) * ld] = master[i];
         }
-    } else if (!SUMMARY) {
+    } else if (!SUMMARY && warp < 4) {
         // ================================================================ aux warps
         const int q = warp;                               // TMEM lane quadrant
         const bool m64 = lane < 16;
@@ -1660,6 +1772,72 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __syncthreads();
     tc_fence_after();
     if (warp == 13) tmem_dealloc(tmem, 512);
+}
+
+template <bool SUMMARY>
+__global__ void __launch_bounds__(kStateThreads, 1)
+chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const CarryParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    state_cta<SUMMARY>(tm_q, tm_k, tm_v, tm_o, p, sm, blockIdx.x, blockIdx.y, blockIdx.z, nullptr);
+}
+
+// ============================================================================
+// chunk_fused_kernel: prep and carry of every chunk in one grid (d_k = d_v =
+// 128, one run per head).  The grid holds one CTA per SM and is launched
+// cooperatively, so all of its CTAs are resident together.  `ncarry` CTAs
+// (one per head; every `stride`-th CTA among the first ncarry * stride) run
+// state_cta over all chunks; every other CTA runs three prep lanes.  Lanes
+// take items chunk-major, so the records arrive roughly in the order the
+// carries consume them; each record's flag is published once its store has
+// completed, and a carry copies a record only after its flag is set.
+// ============================================================================
+constexpr int kFusedLanes = 3;
+constexpr int kFusedCarryStride = 1;
+constexpr int kFusedThreads = kFusedLanes * kPrepThreads;   // 480: 15 warps
+constexpr uint32_t kPrepLaneBytes = (uint32_t)((PrepLayout<128>::kSmemBytes - 1024 + 1023) / 1024) * 1024;
+constexpr size_t kFusedSmemBytes =
+    (StateLayout::kSmemBytes > kFusedLanes * kPrepLaneBytes + 1024) ? StateLayout::kSmemBytes
+                                                                    : kFusedLanes * kPrepLaneBytes + 1024;
+
+// register budget of a 14-warp carry: 128 per thread (65536 / 512)
+__global__ void __launch_bounds__(512, 1)
+chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const CarryParams cp, const PrepParams pp, int* flags, const int ncarry, const int stride) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int bx = blockIdx.x;
+    const int span = ncarry * stride;   // CTAs among which the carries are interleaved
+    if (bx < span && bx % stride == 0) {
+        const int hd = bx / stride;
+        state_cta<false>(tm_q, tm_k, tm_v, tm_o, cp, sm, 0, hd % cp.H, hd / cp.H, flags);
+        return;
+    }
+    const int pidx = bx < span ? (bx / stride) * (stride - 1) + bx % stride - 1 : bx - ncarry;
+    const int nprep = (int)gridDim.x - ncarry;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int ln = warp / 5;                           // lane 0..2
+    uint8_t* lsm = sm + ln * kPrepLaneBytes;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PrepLayout<128>::kMisc + 48);
+    if (tid % kPrepThreads == 0) prep_lane_init<128>(lsm);
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 512);   // 128 columns per lane
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    prep_lane<128>(&tm_k, pp, lsm, tmem + 128u * ln,
+                   PrepLane{tid - ln * kPrepThreads, ln * 5, 1 + 3 * ln, pidx * kFusedLanes + ln,
+                            nprep * kFusedLanes, flags});
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // ============================================================================
@@ -1828,9 +2006,46 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
         return cudaLaunchKernelEx(&cfg, prep, mk, pp);
     };
     cudaError_t e = cudaSuccess;
+    auto* ob = reinterpret_cast<__nv_bfloat16*>(o);
+    static std::once_flag once_f;
+    static int fused_per_sm = 0;   // resident fused CTAs per SM (0: the grid cannot be formed)
+    if (DK == 128 && dv == 128 && chunk_fused(B, H, DK, dv, nseg)) {
+        std::call_once(once_f, [&] {
+            if (cudaFuncSetAttribute(chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kFusedSmemBytes) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fused_per_sm, chunk_fused_kernel, kFusedThreads,
+                                                              kFusedSmemBytes) != cudaSuccess)
+                fused_per_sm = 0;
+            (void)cudaGetLastError();
+        });
+    }
+    // otherwise the prep grid and then one carry grid (the workspace holds no
+    // range hand-off when chunk_fused holds)
+    if (DK == 128 && dv == 128 && chunk_fused(B, H, DK, dv, nseg) && fused_per_sm >= 1 && sms >= 2 * B * H) {
+        // one cooperative grid: a carry CTA per head, prep lanes on the rest
+        CUtensorMap mo;
+        if (!make_map(&mo, o, B, T, H, dv)) return cudaErrorInvalidValue;
+        int* flags = reinterpret_cast<int*>(handoff);
+        if ((e = cudaMemsetAsync(flags, 0, sizeof(int) * (size_t)B * H * nchunks, stream)) != cudaSuccess)
+            return e;
+        CarryParams cp{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks, 0, nchunks};
+        PrepParams pp{g, eta, rec, err, eps, T, H, nchunks, B, 0, nchunks, 0};
+        int ncarry = B * H, stride = kFusedCarryStride;
+        if (ncarry * stride > sms) stride = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(sms);
+        cfg.blockDim = dim3(kFusedThreads);
+        cfg.dynamicSmemBytes = kFusedSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeCooperative;
+        at[0].val.cooperative = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, chunk_fused_kernel, mq, mk, mv, mo, cp, pp, flags, ncarry, stride);
+    }
     const int ranges = (DK == 128 && dv == 128) ? chunk_ranges(B, H, nchunks, nseg) : 1;  // >= 1
     if (ranges == 1 && (e = launch_prep(0, nchunks, kPrepPerSm * sms, false)) != cudaSuccess) return e;
-    auto* ob = reinterpret_cast<__nv_bfloat16*>(o);
     if (DK == 128 && dv == 128) {
         // transposed-state carry: one CTA per (head, run)
         CUtensorMap mo;
@@ -1867,6 +2082,8 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
                 at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
                 at[0].val.programmaticStreamSerializationAllowed = 1;
                 cfg.attrs = at;
+                // the first carry is an ordinary launch: its CTAs then spread
+                // over an idle GPU instead of taking the SMs the prep frees first
                 cfg.numAttrs = pdl ? 1 : 0;
                 return cudaLaunchKernelEx(&cfg, state, mq, mk, mv, mo, cp);
             };
@@ -1927,8 +2144,14 @@ ScanShape chunk_fwd_tc_scan_shape(int T, int segments) {
     return sh;
 }
 
+bool chunk_fused(int B, int H, int dk, int dv, int nseg) {
+    const long long heads = (long long)B * H;
+    return dk == 128 && dv == 128 && nseg == 1 && heads >= 1 && 2 * heads <= kScanTargetCtas;
+}
+
 int chunk_ranges(int B, int H, int nchunks, int nseg) {
     const long long heads = (long long)B * H;
+    if (chunk_fused(B, H, 128, 128, nseg)) return 1;
     if (!(nseg == 1 && nchunks >= kRangeMinChunks && heads + 16 <= kScanTargetCtas)) return 1;
     int bounds[kMaxRanges + 1];
     return chunk_range_bounds(nchunks, bounds);
@@ -1949,6 +2172,8 @@ int chunk_range_bounds(int nchunks, int* bounds) {
 size_t chunk_fwd_tc_extra_bytes(int B, int T, int H, int dk, int dv, int nseg) {
     if (nseg > 1) return sizeof(float) * (size_t)B * H * nseg * dk * ((size_t)(dv + dk) + dv);
     const int nchunks = (T + C - 1) / C;
+    if (chunk_fused(B, H, dk, dv, nseg))  // ready flags, rounded up to 256 bytes
+        return (sizeof(int) * (size_t)B * H * nchunks + 255) / 256 * 256;
     if (dk == 128 && dv == 128 && chunk_ranges(B, H, nchunks, nseg) > 1)
         return sizeof(float) * (size_t)B * H * dk * dv;  // state handed between chunk ranges
     return 0;

@@ -57,8 +57,8 @@ cudaError_t launch_chunk_fwd_simt(const void* q, const void* k, const void* v, c
 // then runs every segment in parallel.  Without a scan and with enough free
 // SMs, the chunks are split into up to kMaxRanges ranges whose carries run one after
 // another while the next range's prep overlaps them.  The scan's buffers, or
-// the state handed between ranges (chunk_fwd_tc_extra_bytes), follow the
-// records.  `err` is the device error record at the start of the caller's
+// the state handed between ranges, or the fused grid's ready flags
+// (chunk_fwd_tc_extra_bytes), follow the records.  `err` is the device error record at the start of the caller's
 // workspace.
 struct ScanShape {
     int nseg;        // segments per head
@@ -79,6 +79,9 @@ cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, con
 size_t chunk_fwd_tc_record_bytes(int B, int T, int H, int dk);
 ScanShape chunk_fwd_tc_scan_shape(int T, int segments);
 size_t chunk_fwd_tc_extra_bytes(int B, int T, int H, int dk, int dv, int nseg);
+// Unsegmented d_k = d_v = 128 with at most kScanTargetCtas / 2 heads: prep and
+// carry run in one cooperative grid (per-chunk ready flags in the workspace).
+bool chunk_fused(int B, int H, int dk, int dv, int nseg);
 int chunk_ranges(int B, int H, int nchunks, int nseg);
 // Fills bounds[0..n] with the chunk-range limits (bounds[0] = 0,
 // bounds[n] = nchunks) and returns n <= kMaxRanges.
