@@ -82,8 +82,6 @@ def load_peaks():
 # so writes still in L2 when a launch ends are not counted.  Refresh these
 # whenever the kernels change.
 TRAFFIC_BYTES = {
-    "train_prefill_bf16_B8H8T4096d128": 398.5e6,
-    "long_prefill_bf16_B1H16T131072d128": 6223.6e6,
     "decode_bf16_B64H16d128_x1024": 71.7e6,
 }
 

@@ -149,10 +149,10 @@ struct Waiter {
 
 // ============================================================================
 // chunk_prep_kernel: state-independent part of one chunk of one head.
-// 5 warps: warp 0 owns TMEM, loads the K tile and issues K K^T; warps 1..4
-// compute beta, gam, A, T and the two operand tiles.
+// 4 warps compute beta, gam, A, T and the two operand tiles; thread 0 also
+// issues the K tile copies and the two MMAs (K K^T and Wk).
 // ============================================================================
-constexpr int kPrepThreads = 160;
+constexpr int kPrepThreads = 128;
 constexpr int kPrepPerSm = 4;   // resident prep CTAs per SM (49 KB shared memory, 128 TMEM columns each)
 
 template <int DK>
@@ -208,19 +208,18 @@ __device__ __forceinline__ int load_acquire(const int* flag) {
     return v;
 }
 
-// One prep lane: 5 warps (160 threads) over one PrepLayout region of shared
+// One prep lane: 4 warps (128 threads) over one PrepLayout region of shared
 // memory and 128 TMEM columns, walking items item0, item0 + istride, ...
-// (chunk-major).  Warp 0 fetches the next item's K tile as soon as the
-// current Wk product has read the tile.
+// (chunk-major).
 struct PrepLane {
-    int tid;            // 0..159 within the lane
+    int tid;            // 0..127 within the lane
     int wbase;          // CTA warp index of the lane's warp 0 (TMEM lane quadrants follow it)
     int bar0;           // first of the lane's three named barriers
     int item0, istride;
     int* flags;         // per-(head, chunk) ready flags, published once a record is stored; or null
 };
 
-// barriers 0: K loaded, 1: K K^T, 2: Wk, 3: TMEM read (Wk converted), 4, 5: drains
+// barriers 0: K loaded, 1: K K^T, 2: Wk, 4, 5: drains
 template <int DK>
 __device__ __forceinline__ void prep_lane_init(uint8_t* sm) {
     using L = PrepLayout<DK>;
@@ -255,62 +254,45 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
     const int B1 = ln.bar0, B2 = ln.bar0 + 1, B3 = ln.bar0 + 2;   // 128, 64 and 128 threads
     Waiter wt{bars, abort_flag, p.err};
 
-    if (warp == 0) {
-        if (lane == 0) {
-            int loads = 0;          // K tiles requested so far
-            bool inflight = false;  // a requested tile not yet waited for
-            auto load = [&](int item) {
-                const int c = p.c_lo + item / nheads, hd = item % nheads;
-                mbar_arrive_expect_tx(&bars[0], KB * 8192);
+    const int pt = tid;                      // 0..127
+    const int q = (ln.wbase + warp) & 3;     // TMEM lane quadrant of this warp
+    const bool m64 = lane < 16;              // holds a row of the M=64 Gram product
+    const int r = q * 16 + lane;             // that row
+    const uint32_t lf = (uint32_t)(q * 32) << 16;
+    uint8_t* Tbt = sm + L::kTb;
+    uint8_t* Tgt = sm + L::kTg;
+    {
+        // Thread 0 issues the K copies and the MMAs: the next item's K as
+        // soon as this item's Wk product has read the tile, and the next
+        // item's K K^T as soon as this item's Wk is out of TMEM.
+        int loads = 0, waited = 0;   // (thread 0) K tiles requested / waited for
+        auto load_k = [&](int item) {
+            const int c = p.c_lo + item / nheads, hd = item % nheads;
+            mbar_arrive_expect_tx(&bars[0], KB * 8192);
 #pragma unroll
-                for (int kb = 0; kb < KB; ++kb)
-                    tma_load_4d(sm + L::kK + kb * 8192, tm_kp, &bars[0], kb * 64, hd % H, c * C, hd / H);
-                ++loads;
-                inflight = true;
-            };
-            int it = 0;
-            if (item0 < total) load(item0);
-            for (int item = item0; item < total; item += istride, ++it) {
-                const uint32_t ph = it & 1;
-                const int c = p.c_lo + item / nheads;
-                if (!wt.poll(0, ph, kWherePrepK, c)) break;
-                inflight = false;
-                // the previous item's Wk has been read out of TMEM
-                if (it > 0 && !wt.poll(3, ph ^ 1u, kWherePrepG, c)) break;
-                tc_fence_after();
-                // K K^T (M=64, N=64)
-                constexpr uint32_t id_g = idesc_bf16(64, 64, false, false);
-                const uint32_t sK = smem_u32(sm + L::kK);
+            for (int kb = 0; kb < KB; ++kb)
+                tma_load_4d(sm + L::kK + kb * 8192, tm_kp, &bars[0], kb * 64, hd % H, c * C, hd / H);
+            ++loads;
+        };
+        // K K^T (M=64, N=64) of the item whose tile was requested last
+        auto issue_gram = [&](int c) -> bool {
+            if (!wt.poll(0, waited & 1, kWherePrepK, c)) return false;
+            ++waited;
+            tc_fence_after();
+            constexpr uint32_t id_g = idesc_bf16(64, 64, false, false);
+            const uint32_t sK = smem_u32(sm + L::kK);
 #pragma unroll
-                for (int k = 0; k < DK / 16; ++k) {
-                    const uint32_t off = (k / 4) * 8192 + (k % 4) * 32;
-                    mma_bf16(tmem, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), id_g, k > 0);
-                }
-                mma_commit(&bars[1]);
-                // Wk = Tg K has read the tile: fetch the next one
-                if (!wt.poll(2, ph, kWherePrepG, c)) break;
-                if (item + istride < total) load(item + istride);
+            for (int k = 0; k < DK / 16; ++k) {
+                const uint32_t off = (k / 4) * 8192 + (k % 4) * 32;
+                mma_bf16(tmem, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), id_g, k > 0);
             }
-            // in-flight copies and MMAs must finish before the CTA exits
-            if (inflight) {
-                const uint64_t tw = globaltimer_ns();
-                while (!mbar_try_wait_sleep(&bars[0], (loads - 1) & 1, kSuspendNs))
-                    if (globaltimer_ns() - tw > kTimeoutNs) break;
-            }
-            mma_commit(&bars[4]);
-            const uint64_t tw = globaltimer_ns();
-            while (!mbar_try_wait_sleep(&bars[4], 0, kSuspendNs))
-                if (globaltimer_ns() - tw > kTimeoutNs) { wt.fail(kWhereDrain, -1); break; }
+            mma_commit(&bars[1]);
+            return true;
+        };
+        if (pt == 0 && item0 < total) {
+            load_k(item0);
+            issue_gram(p.c_lo + item0 / nheads);
         }
-        __syncwarp();
-    } else {
-        const int pt = tid - 32;                 // 0..127
-        const int q = (ln.wbase + warp) & 3;     // TMEM lane quadrant of this warp
-        const bool m64 = lane < 16;              // holds a row of the M=64 Gram product
-        const int r = q * 16 + lane;             // that row
-        const uint32_t lf = (uint32_t)(q * 32) << 16;
-        uint8_t* Tbt = sm + L::kTb;
-        uint8_t* Tgt = sm + L::kTg;
         // gates of an item, fetched one item ahead (threads 0..63, one token each)
         auto fetch_gates = [&](int item, float& gq, float& eq) {
             gq = 0.f; eq = 0.f;
@@ -325,7 +307,11 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
         };
         float gnext, enext;
         fetch_gates(item0, gnext, enext);
-        int pending = -1;  // (thread 0) item whose record store is not yet published
+        // Thread kStorer stores the records and publishes their flags; its
+        // warp is idle while T's diagonal blocks are inverted, which is when
+        // it waits for the previous record's store to complete.
+        constexpr int kStorer = 64;
+        int pending = -1;  // (kStorer) item whose record store is not yet published
         auto publish = [&](int item) {
             const int c = p.c_lo + item / nheads, hd = item % nheads;
             publish_ready(ln.flags + (size_t)hd * p.nchunks + c);
@@ -425,7 +411,7 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
             }
         }
         bar_sync(B1, 128);
-        if (pt == 0 && pending >= 0) {  // that store has long completed; publish it
+        if (pt == kStorer && pending >= 0) {  // stored an item ago: publish it
             bulk_wait_all();
             publish(pending);
             pending = -1;
@@ -575,6 +561,7 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
         }
         if (!wt.group(2, ph, kWherePrepG, c, B3, 128)) break;
         tc_fence_after();
+        if (pt == 0 && item + istride < total) load_k(item + istride);   // Wk has read the tile
         {
             uint8_t* Wkt = sm + L::kWk;
 #pragma unroll
@@ -591,8 +578,9 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
         tc_fence_before();
         fence_proxy_async_smem();
         bar_sync(B1, 128);
-        if (pt == 0) {
-            mbar_arrive(&bars[3]);  // TMEM free for the next item's K K^T
+        // Wk is out of TMEM: the next item's K K^T may overwrite it
+        if (pt == 0 && item + istride < total) issue_gram(p.c_lo + (item + istride) / nheads);
+        if (pt == kStorer) {
             uint8_t* dst = p.rec + (((size_t)b * H + h) * p.nchunks + c) * Rec<DK>::kBytes;
             bulk_store(dst, sm + L::kX, Rec<DK>::kGam);
             bulk_store(dst + Rec<DK>::kGam, sm + L::kGam, 768);
@@ -602,9 +590,16 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
         }
         bar_sync(B1, 128);  // the record has been read out of shared memory
         }
-        if (pt == 0) {     // this thread's stores complete and its Wk MMAs finish before TMEM is freed
+        if (pt == kStorer) {   // the last store completes (and is published) before exit
             bulk_wait_all();
             if (pending >= 0) publish(pending);
+        }
+        if (pt == 0) {     // this thread's copies and MMAs finish before TMEM is freed
+            for (; waited < loads; ++waited) {   // a tile left in flight by an abort
+                const uint64_t tw = globaltimer_ns();
+                while (!mbar_try_wait_sleep(&bars[0], waited & 1, kSuspendNs))
+                    if (globaltimer_ns() - tw > kTimeoutNs) break;
+            }
             mma_commit(&bars[5]);
             const uint64_t tw = globaltimer_ns();
             while (!mbar_try_wait_sleep(&bars[5], 0, kSuspendNs))
@@ -694,6 +689,12 @@ struct CarryParams {
     int T, H, dv, nchunks;
     int nseg, seg_chunks;
     int c_begin, c_end;
+    // transposed carry: refill a stage's group A as soon as it is released
+    // (about a chunk earlier than group B).  Set for the carries that run
+    // beside prep lanes, where it removed most stage waits; with every SM
+    // carrying, as in the scan's passes, the earlier requests only added to
+    // the memory traffic in flight and the passes ran slower.
+    int early_a;
 };
 
 // mbarrier slots (all with arrival count 1)
@@ -1222,7 +1223,8 @@ struct StateLayout {
 // the chunk's decay span allows the factorised forms (every factor finite)
 __device__ __forceinline__ bool span_ok(const float* gam) { return (gam[0] - gam[C - 1]) <= kSpanMax; }
 
-enum { SB_FULL0 = 0, SB_EMPTY0 = SB_FULL0 + kStages, SB_QKB = SB_EMPTY0 + kStages, SB_PR, SB_SR, SB_W,
+enum { SB_FULLA0 = 0, SB_FULLB0 = SB_FULLA0 + kStages, SB_EMPTYA0 = SB_FULLB0 + kStages,
+       SB_EMPTYB0 = SB_EMPTYA0 + kStages, SB_QKB = SB_EMPTYB0 + kStages, SB_PR, SB_SR, SB_W,
        SB_WCT, SB_WCB, SB_QSR, SB_S, SB_PW, SB_DRAIN, SB_SLD, SB_SFREE, SB_COUNT };
 
 // One carry CTA: warps 0..13 take the roles above; any further warp only
@@ -1275,29 +1277,40 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // Stage c holds chunk c0 + c: its K, Q, V tiles (inputs of the call) and
-    // its record (written by the prep grid).  One arrive with the stage's
-    // whole byte count, then the two groups of copies.
-    const uint32_t stage_bytes = 16384u + (SUMMARY ? 0u : 16384u) + (vhalf ? 16384u : 0u) + 8192u + 16384u + 768u;
-    auto load_inputs = [&](int c) {
+    // Stage c holds chunk c0 + c in two groups, each with its own full and
+    // empty barriers.  Group A: the Q and V tiles (inputs of the call) and
+    // Wk and T diag(beta) (the chunk's record, written by the prep); U, Q K^T
+    // and W read it, and all three are issued by the start of the chunk, so
+    // it is released early and (with p.early_a) refilled then, two chunks
+    // ahead.  Group B: the K tiles and the gate vectors, read until the
+    // chunk's S and P W.
+    const uint32_t a_bytes = (SUMMARY ? 0u : 16384u) + (vhalf ? 16384u : 0u) + 16384u + 8192u;
+    const uint32_t b_bytes = 16384u + 768u;
+    auto load_inputs = [&](int c, bool group_a) {
         uint8_t* st = sm + (c % kStages) * L::kStageBytes;
-        uint64_t* full = &bars[SB_FULL0 + c % kStages];
+        uint64_t* full = &bars[(group_a ? SB_FULLA0 : SB_FULLB0) + c % kStages];
         const int t0 = (c0 + c) * C;
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-            tma_load_4d(st + L::kK + kb * 8192, &tm_k, full, kb * 64, h, t0, b);
+            if (!group_a) {
+                tma_load_4d(st + L::kK + kb * 8192, &tm_k, full, kb * 64, h, t0, b);
+                continue;
+            }
             if (!SUMMARY) tma_load_4d(st + L::kWQ + kb * 16384 + 8192, &tm_q, full, kb * 64, h, t0, b);
             if (vhalf) tma_load_4d(st + L::kV + kb * 8192, &tm_v, full, kb * 64, h, t0, b);
         }
     };
-    auto load_record = [&](int c) {
+    auto load_record = [&](int c, bool group_a) {
         uint8_t* st = sm + (c % kStages) * L::kStageBytes;
-        uint64_t* full = &bars[SB_FULL0 + c % kStages];
+        uint64_t* full = &bars[(group_a ? SB_FULLA0 : SB_FULLB0) + c % kStages];
         const uint8_t* rec = p.rec + (head * nchunks + c0 + c) * R::kBytes;
+        if (!group_a) {
+            bulk_load(st + L::kVec, rec + R::kGam, 768, full);
+            return;
+        }
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) bulk_load(st + L::kWQ + kb * 16384, rec + R::kWk + kb * 8192, 8192, full);
         bulk_load(st + L::kTZ, rec + R::kTb, 8192, full);
-        bulk_load(st + L::kVec, rec + R::kGam, 768, full);
     };
     // The start state (fp32 [DK][dv], 64 KB) comes in through stage 1 with a
     // bulk copy: plain loads of it by the state warps were limited by the
@@ -1314,8 +1327,10 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
         if (!SUMMARY) tma_prefetch_desc(&tm_q);
         if (vhalf) tma_prefetch_desc(&tm_v);
         for (int c = 0; c < first; ++c) {
-            mbar_arrive_expect_tx(&bars[SB_FULL0 + c], stage_bytes);
-            load_inputs(c);
+            mbar_arrive_expect_tx(&bars[SB_FULLA0 + c], a_bytes);
+            load_inputs(c, true);
+            mbar_arrive_expect_tx(&bars[SB_FULLB0 + c], b_bytes);
+            load_inputs(c, false);
         }
     }
     // launched as a programmatic dependent of a prep grid: its records (and,
@@ -1333,18 +1348,22 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                     bulk_load(sm + L::kStageBytes + part * (kStartBytes / 4), s_start + part * (kStartBytes / 16),
                               kStartBytes / 4, &bars[SB_SLD]);
             }
-            int issued = 0;
+            // A group is armed only when all of its copies follow; every
+            // armed group completes (after a failed flag wait the record is
+            // still copied; the abort flag stops the rest).
+            int issued_a = 0, issued_b = 0;
             for (int c = 0; c < nch; ++c) {
+                const int s = c % kStages;
+                const uint32_t pe = ((c / kStages) - 1) & 1;
+                const bool b_first = !p.early_a && c >= first && c >= kStages;   // group A waits for B's release
+                if (b_first && !wt.poll(SB_EMPTYB0 + s, pe, kWhereEmpty, c)) break;
                 if (c >= first) {
-                    const int s = c % kStages;
-                    const bool freed = c >= kStages ? wt.poll(SB_EMPTY0 + s, ((c / kStages) - 1) & 1, kWhereEmpty, c)
+                    const bool freed = c >= kStages ? wt.poll(SB_EMPTYA0 + s, pe, kWhereEmpty, c)
                                                     : wt.poll(SB_SFREE, 0, kWhereEmpty, c);   // held the start state
                     if (!freed) break;
-                    mbar_arrive_expect_tx(&bars[SB_FULL0 + s], stage_bytes);
-                    load_inputs(c);
+                    mbar_arrive_expect_tx(&bars[SB_FULLA0 + s], a_bytes);
+                    load_inputs(c, true);
                 }
-                // the record is copied even after a failed flag wait so that
-                // every armed stage completes; the abort flag stops the rest
                 bool ready = true;
                 if (flags) {
                     const int* f = flags + head * nchunks + c0 + c;
@@ -1359,14 +1378,26 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                     }
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                 }
-                load_record(c);
-                issued = c + 1;
+                load_record(c, true);
+                issued_a = c + 1;
+                if (c >= first) {
+                    if (c >= kStages && !b_first && !wt.poll(SB_EMPTYB0 + s, pe, kWhereEmpty, c)) break;
+                    mbar_arrive_expect_tx(&bars[SB_FULLB0 + s], b_bytes);
+                    load_inputs(c, false);
+                }
+                load_record(c, false);
+                issued_b = c + 1;
                 if (!ready) break;
             }
-            for (int c = (issued > kStages ? issued - kStages : 0); c < issued; ++c) {
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait_sleep(&bars[SB_FULL0 + c % kStages], (c / kStages) & 1, kSuspendNs)) {
-                    if (globaltimer_ns() - t0 > kTimeoutNs) { wt.fail(kWhereFull, c); break; }
+            // copies still in flight finish before the CTA exits
+            for (int g = 0; g < 2; ++g) {
+                const int issued = g == 0 ? issued_a : issued_b;
+                for (int c = (issued > kStages ? issued - kStages : 0); c < issued; ++c) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait_sleep(&bars[(g == 0 ? SB_FULLA0 : SB_FULLB0) + c % kStages],
+                                                (c / kStages) & 1, kSuspendNs)) {
+                        if (globaltimer_ns() - t0 > kTimeoutNs) { wt.fail(kWhereFull, c); break; }
+                    }
                 }
             }
         }
@@ -1430,7 +1461,8 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
             const bool r = mbar_test_wait(&bars[slot], parity);
             return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
         };
-        bool ok = wt.warp(SB_FULL0, 0, kWhereFull, 0);
+        bool ok = nch > 0 && wt.warp(SB_FULLA0, 0, kWhereFull, 0);
+        if (ok && !SUMMARY) ok = wt.warp(SB_FULLB0, 0, kWhereFull, 0);   // Q K^T(0) reads K
         if (ok) {
             tc_fence_after();
             if (elect_one()) {
@@ -1444,17 +1476,21 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                 const uint32_t par = c & 1;
                 if (!(ok = wt.warp(SB_SR, par, kWhereSR, c))) break;
                 tc_fence_after();
-                if (elect_one()) issue_w(c);
+                if (elect_one()) {
+                    issue_w(c);
+                    mma_commit(&bars[SB_EMPTYA0 + c % kStages]);   // U(c) and W(c) read group A
+                }
                 __syncwarp();
                 if (!(ok = wt.warp(SB_WCT, par, kWhereWR, c))) break;
+                if (!(ok = wt.warp(SB_FULLB0 + c % kStages, (c / kStages) & 1, kWhereFull, c))) break;
                 tc_fence_after();
                 if (elect_one()) {
                     issue_s(c, false);
-                    mma_commit(&bars[SB_EMPTY0 + c % kStages]);
+                    mma_commit(&bars[SB_EMPTYB0 + c % kStages]);
                 }
                 __syncwarp();
                 if (c + 1 < nch) {
-                    if (!(ok = wt.warp(SB_FULL0 + (c + 1) % kStages, ((c + 1) / kStages) & 1, kWhereFull, c + 1))) break;
+                    if (!(ok = wt.warp(SB_FULLA0 + (c + 1) % kStages, ((c + 1) / kStages) & 1, kWhereFull, c + 1))) break;
                     tc_fence_after();
                     if (vhalf) {
                         if (elect_one()) issue_u(c + 1);
@@ -1463,9 +1499,10 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                 }
             }
         } else {
-            // Per chunk c: W(c) [S_c ready] and S(c) [Wt ready] first; then
-            // U(c+1) [-W^T and S0^T Q^T read], P W(c) [P(c) and Wb ready],
-            // Q K^T(c+1) [Q K^T(c) read], and the stage release.
+            // Per chunk c: W(c) [S_c ready] with the release of group A, and
+            // S(c) [Wt ready] first; then U(c+1) [-W^T and S0^T Q^T read],
+            // P W(c) [P(c) and Wb ready], Q K^T(c+1) [Q K^T(c) read], and the
+            // release of group B.
             int c = 0;
             bool fW = false, fS = false, fU = false, fPW = false, fQK = false, fE = false;
             uint32_t idle = 0;
@@ -1477,7 +1514,11 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                 bool prog = false;
                 if (!fW && ready(SB_SR, par)) {
                     tc_fence_after();
-                    if (elect_one()) issue_w(c);
+                    if (elect_one()) {
+                        issue_w(c);
+                        // U(c), Q K^T(c) and W(c) are the readers of group A
+                        mma_commit(&bars[SB_EMPTYA0 + c % kStages]);
+                    }
                     __syncwarp();
                     fW = prog = true;
                 }
@@ -1492,7 +1533,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                 if (fS && !fU) {
                     if (c + 1 >= nch) {
                         fU = true;
-                    } else if (ready(SB_QSR, par) && ready(SB_FULL0 + s1, p1)) {
+                    } else if (ready(SB_QSR, par) && ready(SB_FULLA0 + s1, p1)) {
                         tc_fence_after();
                         if (elect_one()) issue_u(c + 1);
                         __syncwarp();
@@ -1508,7 +1549,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                 if (fPW && !fQK) {
                     if (c + 1 >= nch) {
                         fQK = true;
-                    } else if (ready(SB_FULL0 + s1, p1)) {
+                    } else if (ready(SB_FULLA0 + s1, p1) && ready(SB_FULLB0 + s1, p1)) {
                         tc_fence_after();
                         if (elect_one()) issue_qk(c + 1);
                         __syncwarp();
@@ -1516,7 +1557,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                     }
                 }
                 if (fS && fPW && !fE) {
-                    if (elect_one()) mma_commit(&bars[SB_EMPTY0 + c % kStages]);
+                    if (elect_one()) mma_commit(&bars[SB_EMPTYB0 + c % kStages]);
                     __syncwarp();
                     fE = prog = true;
                 }
@@ -1788,38 +1829,59 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 // chunk_fused_kernel: prep and carry of every chunk in one grid (d_k = d_v =
 // 128, one run per head).  The grid holds one CTA per SM and is launched
 // cooperatively, so all of its CTAs are resident together.  `ncarry` CTAs
-// (one per head; every `stride`-th CTA among the first ncarry * stride) run
-// state_cta over all chunks; every other CTA runs three prep lanes.  Lanes
+// (one per head) run state_cta over all chunks; every other CTA runs four
+// prep lanes.  Roles go by SM: the CTAs on SM ids below ncarry run the
+// carries, so that (with the usual contiguous numbering) the two SMs of a
+// TPC hold two carries or two preps; a carry whose TPC neighbour runs prep
+// lanes was measured about 25% slower.  Each CTA takes a ticket from one of
+// two counters (zeroed with the flags): a carry ticket is the head, a prep
+// ticket the prep index; prep tickets past the prep count turn into carry
+// tickets, so every head gets exactly one carry whatever the SM numbering.
+// Lanes
 // take items chunk-major, so the records arrive roughly in the order the
 // carries consume them; each record's flag is published once its store has
 // completed, and a carry copies a record only after its flag is set.
 // ============================================================================
-constexpr int kFusedLanes = 3;
-constexpr int kFusedCarryStride = 1;
-constexpr int kFusedThreads = kFusedLanes * kPrepThreads;   // 480: 15 warps
+constexpr int kFusedLanes = 4;
+constexpr int kFusedThreads = kFusedLanes * kPrepThreads;   // 512: 16 warps
 constexpr uint32_t kPrepLaneBytes = (uint32_t)((PrepLayout<128>::kSmemBytes - 1024 + 1023) / 1024) * 1024;
 constexpr size_t kFusedSmemBytes =
     (StateLayout::kSmemBytes > kFusedLanes * kPrepLaneBytes + 1024) ? StateLayout::kSmemBytes
                                                                     : kFusedLanes * kPrepLaneBytes + 1024;
 
+// more than half of an SM's shared memory: one CTA per SM, so the SM ids of
+// a full grid are distinct
+static_assert(kFusedSmemBytes > 116 * 1024, "the fused grid relies on one CTA per SM");
 // register budget of a 14-warp carry: 128 per thread (65536 / 512)
 __global__ void __launch_bounds__(512, 1)
 chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                   const CarryParams cp, const PrepParams pp, int* flags, const int ncarry, const int stride) {
+                   const CarryParams cp, const PrepParams pp, int* tickets, int* flags, const int ncarry) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const int bx = blockIdx.x;
-    const int span = ncarry * stride;   // CTAs among which the carries are interleaved
-    if (bx < span && bx % stride == 0) {
-        const int hd = bx / stride;
+    const int nprep = (int)gridDim.x - ncarry;
+    __shared__ int role[2];   // carry?, head or prep index
+    if (threadIdx.x == 0) {
+        uint32_t sid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sid));
+        int carry = (int)sid < ncarry, t = 0;
+        if (!carry) {
+            t = atomicAdd(&tickets[1], 1);
+            carry = t >= nprep;
+        }
+        if (carry) t = atomicAdd(&tickets[0], 1);
+        role[0] = carry;
+        role[1] = t;
+    }
+    __syncthreads();
+    if (role[0]) {
+        const int hd = role[1];
         state_cta<false>(tm_q, tm_k, tm_v, tm_o, cp, sm, 0, hd % cp.H, hd / cp.H, flags);
         return;
     }
-    const int pidx = bx < span ? (bx / stride) * (stride - 1) + bx % stride - 1 : bx - ncarry;
-    const int nprep = (int)gridDim.x - ncarry;
+    const int pidx = role[1];
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int ln = warp / 5;                           // lane 0..2
+    const int ln = warp / 4;                           // lane 0..3
     uint8_t* lsm = sm + ln * kPrepLaneBytes;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PrepLayout<128>::kMisc + 48);
     if (tid % kPrepThreads == 0) prep_lane_init<128>(lsm);
@@ -1832,7 +1894,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     prep_lane<128>(&tm_k, pp, lsm, tmem + 128u * ln,
-                   PrepLane{tid - ln * kPrepThreads, ln * 5, 1 + 3 * ln, pidx * kFusedLanes + ln,
+                   PrepLane{tid - ln * kPrepThreads, ln * 4, 1 + 3 * ln, pidx * kFusedLanes + ln,
                             nprep * kFusedLanes, flags});
     tc_fence_before();
     __syncthreads();
@@ -2025,13 +2087,13 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
         // one cooperative grid: a carry CTA per head, prep lanes on the rest
         CUtensorMap mo;
         if (!make_map(&mo, o, B, T, H, dv)) return cudaErrorInvalidValue;
-        int* flags = reinterpret_cast<int*>(handoff);
-        if ((e = cudaMemsetAsync(flags, 0, sizeof(int) * (size_t)B * H * nchunks, stream)) != cudaSuccess)
+        int* tickets = reinterpret_cast<int*>(handoff);   // 2 role counters, then the flags
+        int* flags = tickets + 2;
+        if ((e = cudaMemsetAsync(tickets, 0, sizeof(int) * (2 + (size_t)B * H * nchunks), stream)) != cudaSuccess)
             return e;
-        CarryParams cp{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks, 0, nchunks};
+        CarryParams cp{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks, 0, nchunks, 1};
         PrepParams pp{g, eta, rec, err, eps, T, H, nchunks, B, 0, nchunks, 0};
-        int ncarry = B * H, stride = kFusedCarryStride;
-        if (ncarry * stride > sms) stride = 1;
+        const int ncarry = B * H;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(sms);
         cfg.blockDim = dim3(kFusedThreads);
@@ -2042,7 +2104,7 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
         at[0].val.cooperative = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, chunk_fused_kernel, mq, mk, mv, mo, cp, pp, flags, ncarry, stride);
+        return cudaLaunchKernelEx(&cfg, chunk_fused_kernel, mq, mk, mv, mo, cp, pp, tickets, flags, ncarry);
     }
     const int ranges = (DK == 128 && dv == 128) ? chunk_ranges(B, H, nchunks, nseg) : 1;  // >= 1
     if (ranges == 1 && (e = launch_prep(0, nchunks, kPrepPerSm * sms, false)) != cudaSuccess) return e;
@@ -2172,8 +2234,8 @@ int chunk_range_bounds(int nchunks, int* bounds) {
 size_t chunk_fwd_tc_extra_bytes(int B, int T, int H, int dk, int dv, int nseg) {
     if (nseg > 1) return sizeof(float) * (size_t)B * H * nseg * dk * ((size_t)(dv + dk) + dv);
     const int nchunks = (T + C - 1) / C;
-    if (chunk_fused(B, H, dk, dv, nseg))  // ready flags, rounded up to 256 bytes
-        return (sizeof(int) * (size_t)B * H * nchunks + 255) / 256 * 256;
+    if (chunk_fused(B, H, dk, dv, nseg))  // 2 role counters and the ready flags, rounded up to 256 bytes
+        return (sizeof(int) * (2 + (size_t)B * H * nchunks) + 255) / 256 * 256;
     if (dk == 128 && dv == 128 && chunk_ranges(B, H, nchunks, nseg) > 1)
         return sizeof(float) * (size_t)B * H * dk * dv;  // state handed between chunk ranges
     return 0;

@@ -36,8 +36,9 @@ def test_scan_workspace_formula(dk, dv):
     nchunks = -(-T // 64)
     base = kla.kla_chunk_fwd_scan_workspace_bytes(B, T, H, dk, dv, segments=1)
     rec = 8192 + 64 * dk * 2 + 768
-    # d_k = d_v = 128 with few heads and no scan: one grid with per-chunk ready flags
-    flags = -(-B * H * nchunks * 4 // 256) * 256 if (dk, dv) == (128, 128) else 0
+    # d_k = d_v = 128 with few heads and no scan: one grid with two role counters
+    # and per-chunk ready flags
+    flags = -(-(2 + B * H * nchunks) * 4 // 256) * 256 if (dk, dv) == (128, 128) else 0
     assert base == 256 + B * H * nchunks * rec + flags
     assert base % 256 == 0
     base -= flags
