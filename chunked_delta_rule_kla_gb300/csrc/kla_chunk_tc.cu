@@ -195,6 +195,48 @@ struct PrepParams {
     int pdl_wait;           // launched as a programmatic dependent: wait for the primary at exit
 };
 
+// D = P Q for a 16 x 16 tile of D with K = 8 * KS: P (16 x K) and Q (K x 16)
+// row-major fp32 in shared memory with row stride LDF, rounded to tf32 for
+// mma.sync m16n8k8 (one warp, fp32 accumulation).  The fragments follow the
+// PTX layout of that shape: lane = 4 g + t holds P[g | g + 8][t | t + 4],
+// Q[t | t + 4][n], and D[g | g + 8][2 t | 2 t + 1] of each 8-column half n.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+template <int KS>
+__device__ __forceinline__ void mma_tile16_tf32(float (&d)[2][4], const float* P, const float* Q, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int n = 0; n < 2; ++n) d[n][0] = d[n][1] = d[n][2] = d[n][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        const int k0 = 8 * ks;
+        const uint32_t a0 = to_tf32(P[g * LDF + k0 + t]), a1 = to_tf32(P[(g + 8) * LDF + k0 + t]);
+        const uint32_t a2 = to_tf32(P[g * LDF + k0 + t + 4]), a3 = to_tf32(P[(g + 8) * LDF + k0 + t + 4]);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const uint32_t b0 = to_tf32(Q[(k0 + t) * LDF + 8 * n + g]);
+            const uint32_t b1 = to_tf32(Q[(k0 + t + 4) * LDF + 8 * n + g]);
+            asm volatile(
+                "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                "{%8, %9}, {%0, %1, %2, %3};"
+                : "+f"(d[n][0]), "+f"(d[n][1]), "+f"(d[n][2]), "+f"(d[n][3])
+                : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        }
+    }
+}
+// writes s * D (the tile of mma_tile16_tf32) row-major with row stride LDF
+__device__ __forceinline__ void store_tile16(float* dst, const float (&d)[2][4], float s, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+        *reinterpret_cast<float2*>(dst + g * LDF + 8 * n + 2 * t) = make_float2(s * d[n][0], s * d[n][1]);
+        *reinterpret_cast<float2*>(dst + (g + 8) * LDF + 8 * n + 2 * t) = make_float2(s * d[n][2], s * d[n][3]);
+    }
+}
+
 // Ready flags between the prep and the carry inside one grid: the prep's
 // record store completes, is ordered before the flag's release, and the
 // carry's bulk copies of the record follow the flag's acquire.
@@ -438,79 +480,31 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
             float* t = Tf + (16 * I) * LDF + 16 * I + j;
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) t[rr * LDF] = x[rr];
+            // ---- T_10 = -T_11 (A_10 T_00) on warp 0, T_32 = -T_33 (A_32 T_22)
+            // on warp 1: each warp formed the two diagonal blocks it uses.
+            // The products run on mma.sync with tf32 operands: T is used only
+            // after rounding to bf16 (T diag(beta), T diag(beta Gam)).
+            __syncwarp();
+            const int J = 2 * warp, I1 = J + 1;
+            float* R = Rw + warp * 16 * LDF;
+            float d[2][4];
+            mma_tile16_tf32<2>(d, Af + 16 * I1 * LDF + 16 * J, Tf + 16 * J * LDF + 16 * J, lane);
+            store_tile16(R, d, 1.f, lane);
+            __syncwarp();
+            mma_tile16_tf32<2>(d, Tf + 16 * I1 * LDF + 16 * I1, R, lane);
+            store_tile16(Tf + 16 * I1 * LDF + 16 * J, d, -1.f, lane);
         }
         bar_sync(B1, 128);
-        // ---- T_10 = -T_11 (A_10 T_00), T_32 = -T_33 (A_32 T_22): 64 threads, 2x4 each
-        if (pt < 64) {
-            const int bs = pt >> 5, rem = pt & 31, r0 = (rem >> 2) * 2, c0 = (rem & 3) * 4;
-            const int J = 2 * bs, I = J + 1;
-            float* R = Rw + bs * 16 * LDF;
-            float y[2][4] = {};
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const float a0 = Af[(16 * I + r0) * LDF + 16 * J + m];
-                const float a1 = Af[(16 * I + r0 + 1) * LDF + 16 * J + m];
-                const float4 t4 = *reinterpret_cast<const float4*>(&Tf[(16 * J + m) * LDF + 16 * J + c0]);
-                y[0][0] = fmaf(a0, t4.x, y[0][0]); y[0][1] = fmaf(a0, t4.y, y[0][1]);
-                y[0][2] = fmaf(a0, t4.z, y[0][2]); y[0][3] = fmaf(a0, t4.w, y[0][3]);
-                y[1][0] = fmaf(a1, t4.x, y[1][0]); y[1][1] = fmaf(a1, t4.y, y[1][1]);
-                y[1][2] = fmaf(a1, t4.z, y[1][2]); y[1][3] = fmaf(a1, t4.w, y[1][3]);
-            }
-            *reinterpret_cast<float4*>(&R[r0 * LDF + c0]) = make_float4(y[0][0], y[0][1], y[0][2], y[0][3]);
-            *reinterpret_cast<float4*>(&R[(r0 + 1) * LDF + c0]) = make_float4(y[1][0], y[1][1], y[1][2], y[1][3]);
-        }
-        bar_sync(B1, 128);
-        if (pt < 64) {
-            const int bs = pt >> 5, rem = pt & 31, r0 = (rem >> 2) * 2, c0 = (rem & 3) * 4;
-            const int J = 2 * bs, I = J + 1;
-            const float* R = Rw + bs * 16 * LDF;
-            float z[2][4] = {};
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const float t0v = Tf[(16 * I + r0) * LDF + 16 * I + m];
-                const float t1v = Tf[(16 * I + r0 + 1) * LDF + 16 * I + m];
-                const float4 y4 = *reinterpret_cast<const float4*>(&R[m * LDF + c0]);
-                z[0][0] = fmaf(t0v, y4.x, z[0][0]); z[0][1] = fmaf(t0v, y4.y, z[0][1]);
-                z[0][2] = fmaf(t0v, y4.z, z[0][2]); z[0][3] = fmaf(t0v, y4.w, z[0][3]);
-                z[1][0] = fmaf(t1v, y4.x, z[1][0]); z[1][1] = fmaf(t1v, y4.y, z[1][1]);
-                z[1][2] = fmaf(t1v, y4.z, z[1][2]); z[1][3] = fmaf(t1v, y4.w, z[1][3]);
-            }
-            *reinterpret_cast<float4*>(&Tf[(16 * I + r0) * LDF + 16 * J + c0]) =
-                make_float4(-z[0][0], -z[0][1], -z[0][2], -z[0][3]);
-            *reinterpret_cast<float4*>(&Tf[(16 * I + r0 + 1) * LDF + 16 * J + c0]) =
-                make_float4(-z[1][0], -z[1][1], -z[1][2], -z[1][3]);
-        }
-        bar_sync(B1, 128);
-        // ---- T_ba = -T_b (A_ba T_a): 128 threads, 2x4 each
+        // ---- T_ba = -T_b (A_ba T_a) for the 32 x 32 blocks: warp w forms the
+        // 16 x 16 tile (w / 2, w % 2) of Y = A_ba T_a, then of -T_b Y
         {
-            const int r0 = (pt >> 3) * 2, c0 = (pt & 7) * 4;
-            float y[2][4] = {};
-#pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                const float a0 = Af[(32 + r0) * LDF + m];
-                const float a1 = Af[(33 + r0) * LDF + m];
-                const float4 t4 = *reinterpret_cast<const float4*>(&Tf[m * LDF + c0]);
-                y[0][0] = fmaf(a0, t4.x, y[0][0]); y[0][1] = fmaf(a0, t4.y, y[0][1]);
-                y[0][2] = fmaf(a0, t4.z, y[0][2]); y[0][3] = fmaf(a0, t4.w, y[0][3]);
-                y[1][0] = fmaf(a1, t4.x, y[1][0]); y[1][1] = fmaf(a1, t4.y, y[1][1]);
-                y[1][2] = fmaf(a1, t4.z, y[1][2]); y[1][3] = fmaf(a1, t4.w, y[1][3]);
-            }
-            *reinterpret_cast<float4*>(&Rw[r0 * LDF + c0]) = make_float4(y[0][0], y[0][1], y[0][2], y[0][3]);
-            *reinterpret_cast<float4*>(&Rw[(r0 + 1) * LDF + c0]) = make_float4(y[1][0], y[1][1], y[1][2], y[1][3]);
+            const int ti = warp >> 1, tj = warp & 1;
+            float d[2][4];
+            mma_tile16_tf32<4>(d, Af + (32 + 16 * ti) * LDF, Tf + 16 * tj, lane);
+            store_tile16(Rw + 16 * ti * LDF + 16 * tj, d, 1.f, lane);
             bar_sync(B1, 128);
-            float z[2][4] = {};
-#pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                const float t0v = Tf[(32 + r0) * LDF + 32 + m];
-                const float t1v = Tf[(33 + r0) * LDF + 32 + m];
-                const float4 y4 = *reinterpret_cast<const float4*>(&Rw[m * LDF + c0]);
-                z[0][0] = fmaf(t0v, y4.x, z[0][0]); z[0][1] = fmaf(t0v, y4.y, z[0][1]);
-                z[0][2] = fmaf(t0v, y4.z, z[0][2]); z[0][3] = fmaf(t0v, y4.w, z[0][3]);
-                z[1][0] = fmaf(t1v, y4.x, z[1][0]); z[1][1] = fmaf(t1v, y4.y, z[1][1]);
-                z[1][2] = fmaf(t1v, y4.z, z[1][2]); z[1][3] = fmaf(t1v, y4.w, z[1][3]);
-            }
-            *reinterpret_cast<float4*>(&Tf[(32 + r0) * LDF + c0]) = make_float4(-z[0][0], -z[0][1], -z[0][2], -z[0][3]);
-            *reinterpret_cast<float4*>(&Tf[(33 + r0) * LDF + c0]) = make_float4(-z[1][0], -z[1][1], -z[1][2], -z[1][3]);
+            mma_tile16_tf32<4>(d, Tf + (32 + 16 * ti) * LDF + 32, Rw + 16 * tj, lane);
+            store_tile16(Tf + (32 + 16 * ti) * LDF + 16 * tj, d, -1.f, lane);
         }
         bar_sync(B1, 128);
         // ---- Tb = T diag(beta), Tg = T diag(beta Gam): 128 threads, 2 x 8 columns each.
