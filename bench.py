@@ -82,6 +82,8 @@ def load_peaks():
 # so writes still in L2 when a launch ends are not counted.  Refresh these
 # whenever the kernels change.
 TRAFFIC_BYTES = {
+    "train_prefill_bf16_B8H8T4096d128": 445.8e6,
+    "long_prefill_bf16_B1H16T131072d128": 6223.7e6,
     "decode_bf16_B64H16d128_x1024": 71.7e6,
 }
 
@@ -267,7 +269,7 @@ def bench_prefill(case, K, W, flush, peaks, stream, e2e=True):
                tflops=work["flops"] / (mean_ms * 1e-3) / 1e12,
                gbps=work["bytes"] / (mean_ms * 1e-3) / 1e9,
                roofline=dict(roofline(work, mean_ms * 1e-3, peaks, TRAFFIC_BYTES.get(case.name)),
-                             scope="one kla_chunk_fwd call: all its launches (prep and carry kernels)",
+                             scope="one kla_chunk_fwd call: all its launches (one fused prep-and-carry grid, or the prep, carry and combine kernels)",
                              peak_kind="burst copy bandwidth"), work=work,
                launches=K * prefill_launches(kla, case), min_ms=min(ms),
                segments=kla.kla_chunk_fwd_auto_segments(B, T, H, dk, dv, case.chunk))

@@ -579,8 +579,15 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
             bulk_store(dst, sm + L::kX, Rec<DK>::kGam);
             bulk_store(dst + Rec<DK>::kGam, sm + L::kGam, 768);
             bulk_commit();
-            bulk_wait_read_le0();
-            if (ln.flags) pending = item;
+            if (ln.flags && it == 0) {
+                // the first round's records are what the carries wait for
+                // at the start: publish at once
+                bulk_wait_all();
+                publish(item);
+            } else {
+                bulk_wait_read_le0();
+                if (ln.flags) pending = item;
+            }
         }
         bar_sync(B1, 128);  // the record has been read out of shared memory
         }
