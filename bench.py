@@ -362,7 +362,7 @@ def bench_decode(case, K_loops, W_loops, peaks, stream, n_states=4, e2e=True):
     return res
 
 
-def cpu_baseline_prefill(case, max_heads=16):
+def cpu_baseline_prefill(case, max_heads=64):
     """The fp64 oracle as it stands, on the host cores, on a bounded sample:
     the first `max_heads` heads of the workload over the full sequence."""
     import oracle
@@ -410,7 +410,7 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-secondary", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-heads", type=int, default=16)
+    ap.add_argument("--ref-heads", type=int, default=64)
     ap.add_argument("--decode-loops", type=int, default=3)
     ap.add_argument("--only", choices=["train", "long", "decode"], default=None,
                     help="time one workload only (profiling runs)")
