@@ -66,9 +66,15 @@ typedef enum kla_io_dtype {
  * Bytes of device workspace kla_chunk_fwd needs for this problem: 256 bytes
  * of device error record, plus, with bf16 I/O, one record of
  * 8960 + 128*dk bytes (25,344 for dk = 128) per (batch, head, 64-token
- * chunk) that carries the chunk's state-independent operands from the first
- * kernel to the second, plus the chunk-level scan's buffers when the
- * automatic segment count (kla_chunk_fwd_auto_segments) is above 1.
+ * chunk) that carries the chunk's state-independent operands from the prep
+ * to the carry, plus one of:
+ *  - the chunk-level scan's buffers, when the automatic segment count
+ *    (kla_chunk_fwd_auto_segments) is above 1;
+ *  - with dk = dv = 128, no scan and B*H <= 76: two int32 counters and one
+ *    int32 ready flag per (batch, head, chunk), rounded up to 256 bytes,
+ *    for the single grid that runs prep and carry together;
+ *  - with dk = dv = 128, no scan, 77 <= B*H <= 136 and at least 32 chunks:
+ *    one fp32 dk x dv state per head, handed between chunk ranges.
  * Returns 0 if the arguments are invalid or unsupported.
  */
 KLA_API size_t kla_chunk_fwd_workspace_bytes(int B, int T, int H, int dk, int dv,
