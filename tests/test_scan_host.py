@@ -62,3 +62,23 @@ def test_scan_argument_errors():
     assert rc == kla.KLA_ERR_INVALID_ARG
     assert kla.kla_chunk_fwd_scan_workspace_bytes(1, 128, 1, 128, 128, io=kla.KLA_IO_FP32, segments=2) == 0
     assert kla.kla_chunk_fwd_scan_workspace_bytes(1, 128, 1, 128, 128, segments=-1) == 0
+
+
+@pytest.mark.parametrize("B,H,nchunks,extra", [
+    (4, 19, 40, "flags"),      # 76 heads: prep lanes and carries in one grid
+    (1, 77, 40, "handoff"),    # 77 heads, >= 32 chunks: chunk ranges hand the state over
+    (1, 77, 31, "none"),       # 77 heads, < 32 chunks: one prep grid, then one carry grid
+    (2, 68, 40, "handoff"),    # 136 heads: still chunk ranges
+    (1, 137, 40, "none"),      # more heads: no ranges
+])
+def test_unsegmented_path_workspace(B, H, nchunks, extra):
+    # d_k = d_v = 128 without a scan: the workspace names the path the call takes
+    kla = _kla()
+    T = 64 * nchunks - 5
+    assert kla.kla_chunk_fwd_auto_segments(B, T, H, 128, 128) == 1
+    n = kla.kla_chunk_fwd_workspace_bytes(B, T, H, 128, 128)
+    base = 256 + B * H * nchunks * (8960 + 128 * 128)
+    want = {"flags": -(-(2 + B * H * nchunks) * 4 // 256) * 256,
+            "handoff": B * H * 128 * 128 * 4,
+            "none": 0}[extra]
+    assert n == base + want
