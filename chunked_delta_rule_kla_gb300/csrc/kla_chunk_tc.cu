@@ -2105,7 +2105,11 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
         at[0].val.cooperative = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, chunk_fused_kernel, mq, mk, mv, mo, cp, pp, tickets, flags, ncarry);
+        e = cudaLaunchKernelEx(&cfg, chunk_fused_kernel, mq, mk, mv, mo, cp, pp, tickets, flags, ncarry);
+        if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+        // fewer SMs usable than the device has (another context holds some):
+        // the prep grid and then one carry grid instead
+        (void)cudaGetLastError();
     }
     const int ranges = (DK == 128 && dv == 128) ? chunk_ranges(B, H, nchunks, nseg) : 1;  // >= 1
     if (ranges == 1 && (e = launch_prep(0, nchunks, kPrepPerSm * sms, false)) != cudaSuccess) return e;
