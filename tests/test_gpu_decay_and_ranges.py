@@ -7,7 +7,7 @@
 - One fused grid: d_k = d_v = 128 without a scan and with at most 76 heads
   runs prep lanes and carries in one cooperative grid, the carries waiting
   on per-chunk ready flags; here with a nonzero h0, with and without hT,
-  and with 76 heads (the most the grid takes).
+  with 76 heads (the most the grid takes) and with a single head.
 - Chunk ranges: with 77 to 136 heads and >= 32 chunks the carry runs in
   growing chunk ranges, the state passing between ranges through the
   workspace; here with a nonzero h0 and without hT (the handoff buffer)
@@ -106,3 +106,13 @@ def test_chunk_ranges_with_h0(want_hT):
     assert rel_err(o, o_ref) <= TOL["bf16"]
     if want_hT:
         assert rel_err(hT, h_ref) <= TOL["bf16"]
+
+
+def test_fused_grid_single_head():
+    # one carry CTA beside 151 prep CTAs, most of whose lanes get no item
+    case = kla_inputs.TINY.with_(B=1, H=1, T=64 * 5 + 7, dk=128, dv=128, io="bf16", h0_std=0.05, seed=97)
+    inp = kla_inputs.make_prefill(case, device="cuda")
+    o, hT = _run(inp)
+    o_ref, h_ref = oracle_prefill(inp)
+    assert rel_err(o, o_ref) <= TOL["bf16"]
+    assert rel_err(hT, h_ref) <= TOL["bf16"]
