@@ -449,7 +449,13 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
                 const int I = r >> 4;
                 float* adt = AdT + I * 256 + (r & 15);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) adt[i * 16] = arow[16 * I + i];
+                for (int u = 0; u < 4; ++u) {   // 16-byte reads of the row just written
+                    const float4 a4 = *reinterpret_cast<const float4*>(arow + 16 * I + 4 * u);
+                    adt[(4 * u) * 16] = a4.x;
+                    adt[(4 * u + 1) * 16] = a4.y;
+                    adt[(4 * u + 2) * 16] = a4.z;
+                    adt[(4 * u + 3) * 16] = a4.w;
+                }
             }
         }
         bar_sync(B1, 128);
