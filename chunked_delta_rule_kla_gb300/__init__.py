@@ -29,6 +29,9 @@ KLA_ERR_DEVICE_TIMEOUT = 5
 KLA_IO_BF16 = 0
 KLA_IO_FP32 = 1
 
+KLA_BETA_KACZMARZ = 0   # beta_t = eta_t / (||k_t||^2 + eps)
+KLA_BETA_DIRECT = 1     # beta_t = eta_t (the learned-scalar rule; DeltaNet with g = 0)
+
 # Every symbol include/kla.h declares (checked by the ABI tests).
 EXPORTED_SYMBOLS = (
     "kla_chunk_fwd_workspace_bytes",
@@ -37,7 +40,9 @@ EXPORTED_SYMBOLS = (
     "kla_chunk_fwd_scan",
     "kla_chunk_fwd_auto_segments",
     "kla_chunk_fwd_noalloc",
+    "kla_chunk_fwd_ex",
     "kla_decode_step",
+    "kla_decode_step_ex",
     "kla_workspace_check",
     "kla_status_string",
 )
@@ -86,6 +91,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kla_chunk_fwd_noalloc.restype = i
         lib.kla_decode_step.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp]
         lib.kla_decode_step.restype = i
+        lib.kla_chunk_fwd_ex.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp,
+                                         i, i, i, i, i, i, i, i, i, vp, sz, vp]
+        lib.kla_chunk_fwd_ex.restype = i
+        lib.kla_decode_step_ex.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, i, vp]
+        lib.kla_decode_step_ex.restype = i
         lib.kla_workspace_check.argtypes = [vp, sz, vp]
         lib.kla_workspace_check.restype = i
         lib.kla_status_string.argtypes = [i]
@@ -190,6 +200,21 @@ def kla_chunk_fwd_scan(q, k, v, g, eta, eps, h0, o, hT, workspace, segments, chu
         raise KlaError(rc, "kla_chunk_fwd_scan")
 
 
+def kla_chunk_fwd_ex(q, k, v, g, eta, eps, h0, o, hT, workspace, beta=KLA_BETA_KACZMARZ,
+                     segments=0, chunk=64, stream=None) -> None:
+    """kla_chunk_fwd_scan with the step size chosen by ``beta`` (KLA_BETA_KACZMARZ or
+    KLA_BETA_DIRECT, see include/kla.h)."""
+    B, T, H, dk, dv, io = _check_prefill_args(q, k, v, g, eta, h0, o, hT)
+    rc = load_library().kla_chunk_fwd_ex(
+        _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g", torch.float32),
+        _ptr(eta, "eta", torch.float32), float(eps), _ptr(h0, "h0", torch.float32),
+        _ptr(o, "o"), _ptr(hT, "hT", torch.float32), B, T, H, dk, dv, int(chunk), io,
+        int(beta), int(segments), _ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != KLA_OK:
+        raise KlaError(rc, "kla_chunk_fwd_ex")
+
+
 def kla_chunk_fwd_noalloc(q, k, v, g, eta, eps, h0, o, hT, chunk=64, stream=None) -> None:
     """kla_chunk_fwd without a workspace, for callers that must not allocate
     device memory: the scratch is an array built into the library (see
@@ -204,10 +229,11 @@ def kla_chunk_fwd_noalloc(q, k, v, g, eta, eps, h0, o, hT, chunk=64, stream=None
         raise KlaError(rc, "kla_chunk_fwd_noalloc")
 
 
-def kla_decode_step(q, k, v, g, eta, eps, S, o, stream=None) -> None:
+def kla_decode_step(q, k, v, g, eta, eps, S, o, stream=None, beta=KLA_BETA_KACZMARZ) -> None:
     """Enqueue one decode step (see include/kla.h); S [B,H,dk,dv] is updated in place.
 
-    q, k [B,H,dk]; v, o [B,H,dv] (bf16 or fp32); g, eta [B,H] fp32.
+    q, k [B,H,dk]; v, o [B,H,dv] (bf16 or fp32); g, eta [B,H] fp32.  A ``beta``
+    other than KLA_BETA_KACZMARZ goes through kla_decode_step_ex.
     """
     B, H, dk = k.shape
     dv = v.shape[-1]
@@ -219,12 +245,15 @@ def kla_decode_step(q, k, v, g, eta, eps, S, o, stream=None) -> None:
         raise ValueError("shape mismatch among q, k, v, o")
     if g.shape != (B, H) or eta.shape != (B, H) or tuple(S.shape) != (B, H, dk, dv):
         raise ValueError("g, eta must be [B,H] and S [B,H,dk,dv]")
-    rc = load_library().kla_decode_step(
-        _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g", torch.float32),
-        _ptr(eta, "eta", torch.float32), float(eps), _ptr(S, "S", torch.float32),
-        _ptr(o, "o"), B, H, dk, dv, io, _stream(stream))
+    args = (_ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g", torch.float32),
+            _ptr(eta, "eta", torch.float32), float(eps), _ptr(S, "S", torch.float32),
+            _ptr(o, "o"), B, H, dk, dv, io)
+    if beta == KLA_BETA_KACZMARZ:
+        rc, name = load_library().kla_decode_step(*args, _stream(stream)), "kla_decode_step"
+    else:
+        rc, name = load_library().kla_decode_step_ex(*args, int(beta), _stream(stream)), "kla_decode_step_ex"
     if rc != KLA_OK:
-        raise KlaError(rc, "kla_decode_step")
+        raise KlaError(rc, name)
 
 
 def kla_workspace_check(workspace, stream=None) -> int:
@@ -246,28 +275,35 @@ def alloc_workspace(B, T, H, dk, dv, chunk=64, io=KLA_IO_BF16, device="cuda",
 
 
 def chunk_fwd(q, k, v, g, eta, eps=1e-6, h0=None, output_final_state=True, chunk=64,
-              workspace=None, stream=None):
-    """Allocate o (and hT) and run kla_chunk_fwd.  Returns (o, hT or None)."""
+              workspace=None, stream=None, beta=KLA_BETA_KACZMARZ):
+    """Allocate o (and hT) and run kla_chunk_fwd (kla_chunk_fwd_ex when ``beta`` is
+    KLA_BETA_DIRECT: eta is then the step size itself).  Returns (o, hT or None)."""
     B, T, H, dk = k.shape
     dv = v.shape[-1]
     o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device) if output_final_state else None
     if workspace is None:
         workspace = alloc_workspace(B, T, H, dk, dv, chunk, _io_of(q), q.device)
-    kla_chunk_fwd(q, k, v, g, eta, eps, h0, o, hT, workspace, chunk, stream)
+    if beta == KLA_BETA_KACZMARZ:
+        kla_chunk_fwd(q, k, v, g, eta, eps, h0, o, hT, workspace, chunk, stream)
+    else:
+        kla_chunk_fwd_ex(q, k, v, g, eta, eps, h0, o, hT, workspace, beta=beta, chunk=chunk,
+                         stream=stream)
     return o, hT
 
 
-def decode_step(q, k, v, g, eta, S, eps=1e-6, stream=None):
-    """Run kla_decode_step; S is updated in place.  Returns o."""
+def decode_step(q, k, v, g, eta, S, eps=1e-6, stream=None, beta=KLA_BETA_KACZMARZ):
+    """Run kla_decode_step (with the step size chosen by ``beta``); S is updated in
+    place.  Returns o."""
     o = torch.empty(v.shape, dtype=q.dtype, device=q.device)
-    kla_decode_step(q, k, v, g, eta, eps, S, o, stream)
+    kla_decode_step(q, k, v, g, eta, eps, S, o, stream, beta=beta)
     return o
 
 
 __all__ = [
     "kla_chunk_fwd_workspace_bytes", "kla_chunk_fwd", "kla_chunk_fwd_noalloc", "kla_decode_step",
     "kla_chunk_fwd_scan", "kla_chunk_fwd_scan_workspace_bytes", "kla_chunk_fwd_auto_segments",
+    "kla_chunk_fwd_ex", "kla_decode_step_ex", "KLA_BETA_KACZMARZ", "KLA_BETA_DIRECT",
     "kla_workspace_check",
     "kla_status_string", "chunk_fwd", "decode_step", "alloc_workspace", "load_library",
     "KlaError", "EXPORTED_SYMBOLS", "KLA_IO_BF16", "KLA_IO_FP32",

@@ -68,13 +68,16 @@ size_t kla_chunk_fwd_workspace_bytes(int B, int T, int H, int dk, int dv, int ch
     return kla_chunk_fwd_scan_workspace_bytes(B, T, H, dk, dv, chunk, io, 0);
 }
 
-kla_status kla_chunk_fwd_scan(const void* q, const void* k, const void* v, const float* g,
-                              const float* eta, float eps, const float* h0, void* o, float* hT,
-                              int B, int T, int H, int dk, int dv, int chunk, kla_io_dtype io,
-                              int segments, void* workspace, size_t workspace_bytes, void* stream) {
+kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,
+                            const float* eta, float eps, const float* h0, void* o, float* hT,
+                            int B, int T, int H, int dk, int dv, int chunk, kla_io_dtype io,
+                            kla_beta_mode beta, int segments, void* workspace,
+                            size_t workspace_bytes, void* stream) {
     if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || chunk <= 0 || segments < 0)
         return KLA_ERR_INVALID_ARG;
     if (check_io(io) != KLA_OK) return KLA_ERR_INVALID_ARG;
+    if (beta != KLA_BETA_KACZMARZ && beta != KLA_BETA_DIRECT) return KLA_ERR_INVALID_ARG;
+    const bool direct = beta == KLA_BETA_DIRECT;
     if (!(eps >= 0.f)) return KLA_ERR_INVALID_ARG;  // also rejects NaN
     if (!dim_ok(dk) || !dim_ok(dv) || chunk != 64) return KLA_ERR_UNSUPPORTED;
     if (!sizes_fit(B, T, H, dk, dv)) return KLA_ERR_UNSUPPORTED;
@@ -108,10 +111,18 @@ kla_status kla_chunk_fwd_scan(const void* q, const void* k, const void* v, const
         auto* rec = reinterpret_cast<kla::DeviceErrorRecord*>(workspace);
         uint8_t* records = reinterpret_cast<uint8_t*>(workspace) + kla::kErrorRecordBytes;
         return to_status(kla::launch_chunk_fwd_tc(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dk, dv,
-                                                  segments, rec, records, st));
+                                                  segments, direct, rec, records, st));
     }
     return to_status(kla::launch_chunk_fwd_simt(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dk,
-                                                dv, false, st));
+                                                dv, false, direct, st));
+}
+
+kla_status kla_chunk_fwd_scan(const void* q, const void* k, const void* v, const float* g,
+                              const float* eta, float eps, const float* h0, void* o, float* hT,
+                              int B, int T, int H, int dk, int dv, int chunk, kla_io_dtype io,
+                              int segments, void* workspace, size_t workspace_bytes, void* stream) {
+    return kla_chunk_fwd_ex(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dk, dv, chunk, io,
+                            KLA_BETA_KACZMARZ, segments, workspace, workspace_bytes, stream);
 }
 
 kla_status kla_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
@@ -122,11 +133,12 @@ kla_status kla_chunk_fwd(const void* q, const void* k, const void* v, const floa
                               workspace, workspace_bytes, stream);
 }
 
-kla_status kla_decode_step(const void* q, const void* k, const void* v, const float* g,
-                           const float* eta, float eps, float* S, void* o, int B, int H, int dk,
-                           int dv, kla_io_dtype io, void* stream) {
+kla_status kla_decode_step_ex(const void* q, const void* k, const void* v, const float* g,
+                              const float* eta, float eps, float* S, void* o, int B, int H, int dk,
+                              int dv, kla_io_dtype io, kla_beta_mode beta, void* stream) {
     if (B < 0 || H < 0 || dk <= 0 || dv <= 0) return KLA_ERR_INVALID_ARG;
     if (check_io(io) != KLA_OK) return KLA_ERR_INVALID_ARG;
+    if (beta != KLA_BETA_KACZMARZ && beta != KLA_BETA_DIRECT) return KLA_ERR_INVALID_ARG;
     if (!(eps >= 0.f)) return KLA_ERR_INVALID_ARG;
     if (!dim_ok(dk) || !dim_ok(dv)) return KLA_ERR_UNSUPPORTED;
     if (B > 65535 || H > 65535) return KLA_ERR_UNSUPPORTED;
@@ -138,7 +150,14 @@ kla_status kla_decode_step(const void* q, const void* k, const void* v, const fl
     if (!aligned4(g) || !aligned4(eta)) return KLA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     return to_status(kla::launch_decode_step(q, k, v, g, eta, eps, S, o, B, H, dk, dv,
-                                             io == KLA_IO_BF16, st));
+                                             io == KLA_IO_BF16, beta == KLA_BETA_DIRECT, st));
+}
+
+kla_status kla_decode_step(const void* q, const void* k, const void* v, const float* g,
+                           const float* eta, float eps, float* S, void* o, int B, int H, int dk,
+                           int dv, kla_io_dtype io, void* stream) {
+    return kla_decode_step_ex(q, k, v, g, eta, eps, S, o, B, H, dk, dv, io, KLA_BETA_KACZMARZ,
+                              stream);
 }
 
 kla_status kla_workspace_check(const void* workspace, size_t workspace_bytes, void* stream) {

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_fwd_simt_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __restrict__ v,
                       const float* __restrict__ g, const float* __restrict__ eta, float eps,
                       const float* __restrict__ h0, IO* __restrict__ o, float* __restrict__ hT,
-                      int T, int H, int dv) {
+                      int T, int H, int dv, int beta_direct) {
     using L = Smem<DK>;
     constexpr int KLD = L::KLD, PLD = L::PLD;
     extern __shared__ float smem[];
@@ -97,7 +97,8 @@ chunk_fwd_simt_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const 
             bet[tid] = ok ? eta[off] : 0.f;
         }
         __syncthreads();
-        // ---- 2. beta_r = eta_r / (||k_r||^2 + eps); gam = inclusive cumsum of g
+        // ---- 2. beta_r = eta_r / (||k_r||^2 + eps) (or eta_r with beta_direct);
+        //         gam = inclusive cumsum of g
         {
             const int warp = tid >> 5, lane = tid & 31;
             for (int r = warp; r < C; r += kThreads / 32) {
@@ -105,7 +106,7 @@ chunk_fwd_simt_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const 
                 for (int d = lane; d < DK; d += 32) s = fmaf(Ks[r * KLD + d], Ks[r * KLD + d], s);
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-                if (lane == 0) bet[r] = r < nvalid ? bet[r] / (s + eps) : 0.f;
+                if (lane == 0) bet[r] = r < nvalid ? (beta_direct ? bet[r] : bet[r] / (s + eps)) : 0.f;
             }
             if (warp == 0) {
                 // two entries per lane: (2l, 2l+1)
@@ -278,14 +279,14 @@ chunk_fwd_simt_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const 
 template <typename IO, int DK>
 cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* g,
                       const float* eta, float eps, const float* h0, void* o, float* hT, int B,
-                      int T, int H, int dv, cudaStream_t stream) {
+                      int T, int H, int dv, bool beta_direct, cudaStream_t stream) {
     auto kern = chunk_fwd_simt_kernel<IO, DK>;
     const size_t smem = Smem<DK>::kBytes;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     dim3 grid(dv / DVS, H, B);
     kern<<<grid, kThreads, smem, stream>>>((const IO*)q, (const IO*)k, (const IO*)v, g, eta, eps,
-                                           h0, (IO*)o, hT, T, H, dv);
+                                           h0, (IO*)o, hT, T, H, dv, beta_direct ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -294,13 +295,14 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
 cudaError_t launch_chunk_fwd_simt(const void* q, const void* k, const void* v, const float* g,
                                   const float* eta, float eps, const float* h0, void* o,
                                   float* hT, int B, int T, int H, int dk, int dv, bool bf16,
-                                  cudaStream_t stream) {
+                                  bool beta_direct, cudaStream_t stream) {
+    const bool bd = beta_direct;
     if (bf16) {
-        if (dk == 128) return launch_dk<__nv_bfloat16, 128>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, stream);
-        return launch_dk<__nv_bfloat16, 64>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, stream);
+        if (dk == 128) return launch_dk<__nv_bfloat16, 128>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, bd, stream);
+        return launch_dk<__nv_bfloat16, 64>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, bd, stream);
     }
-    if (dk == 128) return launch_dk<float, 128>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, stream);
-    return launch_dk<float, 64>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, stream);
+    if (dk == 128) return launch_dk<float, 128>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, bd, stream);
+    return launch_dk<float, 64>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, bd, stream);
 }
 
 }  // namespace kla

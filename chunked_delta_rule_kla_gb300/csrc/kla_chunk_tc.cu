@@ -193,6 +193,7 @@ struct PrepParams {
     int T, H, nchunks;
     int B, c_lo, c_hi;      // work items: chunks [c_lo, c_hi) of every (b, h), chunk-major
     int pdl_wait;           // launched as a programmatic dependent: wait for the primary at exit
+    int beta_direct;        // beta_t = eta_t instead of eta_t / (||k_t||^2 + eps)
 };
 
 // D = P Q for a 16 x 16 tile of D with K = 8 * KS: P (16 x K) and Q (K x 16)
@@ -408,7 +409,7 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
             float gr = 0.f, br = 0.f;
             if (m64) {
                 gr = gam[r];
-                br = (r < nvalid) ? bet[r] / (kk + p.eps) : 0.f;
+                br = (r < nvalid) ? (p.beta_direct ? bet[r] : bet[r] / (kk + p.eps)) : 0.f;
             }
             bar_sync(B1, 128);  // every thread has read eta from bet[]
             if (m64) {
@@ -2027,7 +2028,7 @@ template <int DK>
 cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* g, const float* eta,
                       float eps, const float* h0, void* o, float* hT, int B, int T, int H, int dv,
                       DeviceErrorRecord* err, uint8_t* rec, int nseg, int seg_chunks, float* seg_x,
-                      float* seg_start, float* handoff, cudaStream_t stream) {
+                      float* seg_start, float* handoff, bool beta_direct, cudaStream_t stream) {
     CUtensorMap mq, mk, mv;
     if (!make_map(&mq, q, B, T, H, DK) || !make_map(&mk, k, B, T, H, DK) ||
         !make_map(&mv, v, B, T, H, dv))
@@ -2057,7 +2058,7 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
     auto launch_prep = [&](int c_lo, int c_hi, int max_ctas, bool pdl) -> cudaError_t {
         const int total = (c_hi - c_lo) * B * H;
         const int grid = total < max_ctas ? total : max_ctas;
-        PrepParams pp{g, eta, rec, err, eps, T, H, nchunks, B, c_lo, c_hi, pdl ? 1 : 0};
+        PrepParams pp{g, eta, rec, err, eps, T, H, nchunks, B, c_lo, c_hi, pdl ? 1 : 0, beta_direct ? 1 : 0};
         if (!pdl) {
             prep<<<grid, kPrepThreads, smem_prep, stream>>>(mk, pp);
             return cudaGetLastError();
@@ -2099,7 +2100,7 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
         if ((e = cudaMemsetAsync(tickets, 0, sizeof(int) * (2 + (size_t)B * H * nchunks), stream)) != cudaSuccess)
             return e;
         CarryParams cp{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks, 0, nchunks, 1};
-        PrepParams pp{g, eta, rec, err, eps, T, H, nchunks, B, 0, nchunks, 0};
+        PrepParams pp{g, eta, rec, err, eps, T, H, nchunks, B, 0, nchunks, 0, beta_direct ? 1 : 0};
         const int ncarry = B * H;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(sms);
@@ -2273,7 +2274,7 @@ int chunk_fwd_tc_auto_segments(int B, int T, int H, int dk, int dv) {
 
 cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, const float* g,
                                 const float* eta, float eps, const float* h0, void* o, float* hT,
-                                int B, int T, int H, int dk, int dv, int segments,
+                                int B, int T, int H, int dk, int dv, int segments, bool beta_direct,
                                 DeviceErrorRecord* err, uint8_t* records, cudaStream_t stream) {
     const ScanShape sh = chunk_fwd_tc_scan_shape(T, segments);
     // after the records: the scan's maps and start states, or (without a
@@ -2283,9 +2284,9 @@ cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, con
     float* handoff = seg_x;
     if (dk == 128)
         return launch_dk<128>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, err, records, sh.nseg,
-                              sh.seg_chunks, seg_x, seg_start, handoff, stream);
+                              sh.seg_chunks, seg_x, seg_start, handoff, beta_direct, stream);
     return launch_dk<64>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, err, records, sh.nseg,
-                         sh.seg_chunks, seg_x, seg_start, handoff, stream);
+                         sh.seg_chunks, seg_x, seg_start, handoff, beta_direct, stream);
 }
 
 }  // namespace kla

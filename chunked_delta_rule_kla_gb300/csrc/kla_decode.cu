@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kThreads, kTmaCtasPerSm)
 decode_tma_kernel(const __grid_constant__ CUtensorMap tm_s, const IO* __restrict__ q,
                   const IO* __restrict__ k, const IO* __restrict__ v, const float* __restrict__ g,
                   const float* __restrict__ eta, float eps, IO* __restrict__ o, int H, int dv,
-                  int items) {
+                  int items, int beta_direct) {
     constexpr int RPT = DK / 16;
     constexpr uint32_t kTileBytes = DK * kCols * 4;
     extern __shared__ uint8_t smem_raw[];
@@ -142,7 +142,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_s, const IO* __restrict
             y.x += b4.x; y.y += b4.y; y.z += b4.z; y.w += b4.w;
         }
         const float a = expf(gv);
-        const float beta = ev / (scal[0] + eps);
+        const float beta = beta_direct ? ev : ev / (scal[0] + eps);
         const float bkq = beta * scal[1];
         float e[4], xv[4] = {x.x, x.y, x.z, x.w}, yv[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
@@ -207,7 +207,7 @@ PFN_cuTensorMapEncodeTiled_v12000 decode_encode_fn() {
 template <typename IO>
 cudaError_t launch_io(const void* q, const void* k, const void* v, const float* g,
                       const float* eta, float eps, float* S, void* o, int B, int H, int dk,
-                      int dv, cudaStream_t stream) {
+                      int dv, bool beta_direct, cudaStream_t stream) {
     auto fn = decode_encode_fn();
     if (!fn) return cudaErrorInitializationError;
     // S [B][H][dk][dv] fp32 as 4-D (dv, dk, H, B); box 64 x dk x 1 x 1
@@ -248,18 +248,18 @@ cudaError_t launch_io(const void* q, const void* k, const void* v, const float* 
     cfg.numAttrs = 1;
     if (dk == 128)
         return cudaLaunchKernelEx(&cfg, decode_tma_kernel<IO, 128>, map, (const IO*)q, (const IO*)k,
-                                  (const IO*)v, g, eta, eps, (IO*)o, H, dv, items);
+                                  (const IO*)v, g, eta, eps, (IO*)o, H, dv, items, beta_direct ? 1 : 0);
     return cudaLaunchKernelEx(&cfg, decode_tma_kernel<IO, 64>, map, (const IO*)q, (const IO*)k, (const IO*)v,
-                              g, eta, eps, (IO*)o, H, dv, items);
+                              g, eta, eps, (IO*)o, H, dv, items, beta_direct ? 1 : 0);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_step(const void* q, const void* k, const void* v, const float* g,
                                const float* eta, float eps, float* S, void* o, int B, int H,
-                               int dk, int dv, bool bf16, cudaStream_t stream) {
-    if (bf16) return launch_io<__nv_bfloat16>(q, k, v, g, eta, eps, S, o, B, H, dk, dv, stream);
-    return launch_io<float>(q, k, v, g, eta, eps, S, o, B, H, dk, dv, stream);
+                               int dk, int dv, bool bf16, bool beta_direct, cudaStream_t stream) {
+    if (bf16) return launch_io<__nv_bfloat16>(q, k, v, g, eta, eps, S, o, B, H, dk, dv, beta_direct, stream);
+    return launch_io<float>(q, k, v, g, eta, eps, S, o, B, H, dk, dv, beta_direct, stream);
 }
 
 }  // namespace kla

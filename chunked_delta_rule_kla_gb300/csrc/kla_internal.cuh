@@ -36,16 +36,18 @@ __device__ __forceinline__ void record_error(DeviceErrorRecord* rec, unsigned wh
 // ---- launchers (each returns the cudaError_t of its launch) --------------
 
 // Decode step, fp32 math, S read once and written once (kla_decode.cu).
+// beta_direct: beta_t = eta_t (the learned-scalar rule) instead of
+// eta_t / (||k_t||^2 + eps); the same flag in every launcher below.
 cudaError_t launch_decode_step(const void* q, const void* k, const void* v, const float* g,
                                const float* eta, float eps, float* S, void* o, int B, int H,
-                               int dk, int dv, bool bf16, cudaStream_t stream);
+                               int dk, int dv, bool bf16, bool beta_direct, cudaStream_t stream);
 
 // Chunkwise prefill on CUDA cores in fp32 (kla_chunk_simt.cu).  Any T >= 1,
 // dk, dv in {64,128}, chunk 64.
 cudaError_t launch_chunk_fwd_simt(const void* q, const void* k, const void* v, const float* g,
                                   const float* eta, float eps, const float* h0, void* o,
                                   float* hT, int B, int T, int H, int dk, int dv, bool bf16,
-                                  cudaStream_t stream);
+                                  bool beta_direct, cudaStream_t stream);
 
 // Chunkwise prefill on the tensor cores (tcgen05 + TMA + TMEM), bf16 I/O,
 // dk, dv in {64,128}, chunk 64 (kla_chunk_tc.cu): a prep kernel over every
@@ -74,7 +76,7 @@ constexpr int kRangeMinChunks = 32;
 
 cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, const float* g,
                                 const float* eta, float eps, const float* h0, void* o, float* hT,
-                                int B, int T, int H, int dk, int dv, int segments,
+                                int B, int T, int H, int dk, int dv, int segments, bool beta_direct,
                                 DeviceErrorRecord* err, uint8_t* records, cudaStream_t stream);
 size_t chunk_fwd_tc_record_bytes(int B, int T, int H, int dk);
 ScanShape chunk_fwd_tc_scan_shape(int T, int segments);

@@ -63,6 +63,22 @@ typedef enum kla_io_dtype {
 } kla_io_dtype;
 
 /*
+ * The step size of the update (the _ex calls take it; every other call uses
+ * KLA_BETA_KACZMARZ).
+ *  KLA_BETA_KACZMARZ  beta_t = eta_t / (||k_t||^2 + eps): KLA itself.
+ *  KLA_BETA_DIRECT    beta_t = eta_t; eps is not used.  This is the learned
+ *                     scalar of Gated DeltaNet that KLA replaces ("KLA:
+ *                     Kaczmarz Linear Attention", sections "Problem
+ *                     statement" and "Methodology"); with g = 0 it is the
+ *                     ungated delta rule (DeltaNet).  Stable when
+ *                     beta_t ||k_t||^2 < 2, e.g. unit-norm keys and eta in (0, 1].
+ */
+typedef enum kla_beta_mode {
+    KLA_BETA_KACZMARZ = 0,
+    KLA_BETA_DIRECT = 1
+} kla_beta_mode;
+
+/*
  * Bytes of device workspace kla_chunk_fwd needs for this problem: 256 bytes
  * of device error record, plus, with bf16 I/O, one record of
  * 8960 + 128*dk bytes (25,344 for dk = 128) per (batch, head, 64-token
@@ -150,6 +166,18 @@ KLA_API kla_status kla_chunk_fwd_scan(const void* q, const void* k, const void* 
                                       size_t workspace_bytes, void* stream);
 
 /*
+ * kla_chunk_fwd_scan with the step size chosen by `beta` (kla_beta_mode;
+ * KLA_ERR_INVALID_ARG for other values).  Same workspace
+ * (kla_chunk_fwd_scan_workspace_bytes), same paths and errors.
+ */
+KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
+                                    const float* g, const float* eta, float eps,
+                                    const float* h0, void* o, float* hT,
+                                    int B, int T, int H, int dk, int dv, int chunk,
+                                    kla_io_dtype io, kla_beta_mode beta, int segments,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Segment count kla_chunk_fwd uses for this shape (1 = no scan).  With bf16
  * I/O and dk = dv = 128, when 4*B*H <= 152 (a GB300's SMs), it is
  * floor(152 / (B*H)): one full wave of per-(head, run) carry CTAs.  For the
@@ -176,6 +204,12 @@ KLA_API kla_status kla_decode_step(const void* q, const void* k, const void* v,
                            const float* g, const float* eta, float eps,
                            float* S, void* o, int B, int H, int dk, int dv,
                            kla_io_dtype io, void* stream);
+
+/* kla_decode_step with the step size chosen by `beta` (kla_beta_mode). */
+KLA_API kla_status kla_decode_step_ex(const void* q, const void* k, const void* v,
+                                      const float* g, const float* eta, float eps,
+                                      float* S, void* o, int B, int H, int dk, int dv,
+                                      kla_io_dtype io, kla_beta_mode beta, void* stream);
 
 /*
  * kla_chunk_fwd for callers that must not allocate device memory.  The paper

@@ -33,6 +33,7 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libkla_oracle.so")
 
 NO_ERASE = 1
+BETA_DIRECT = 2
 
 _lib = None
 _lock = threading.Lock()
@@ -82,8 +83,12 @@ def _ptr(a):
 
 
 def kla_oracle_forward(q, k, v, g, eta, eps, h0=None, *, no_erase=False,
-                       return_states=False, threads=0):
+                       return_states=False, threads=0, beta_direct=False):
     """Sequential fp64 forward over t for every (b, h).
+
+    ``beta_direct``: beta_t = eta_t as given (the learned-scalar step size of
+    Gated DeltaNet that the KLA page's sections "Problem statement" and
+    "Methodology" contrast with the Kaczmarz step); eps is then unused.
 
     Shapes: q,k [B,T,H,dk]; v [B,T,H,dv]; g,eta [B,T,H]; h0 [B,H,dk,dv] or None.
     Returns (o [B,T,H,dv], hT [B,H,dk,dv]) and, with ``return_states``, also
@@ -102,7 +107,7 @@ def kla_oracle_forward(q, k, v, g, eta, eps, h0=None, *, no_erase=False,
     rc = _load().kla_oracle_forward(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(eta), float(eps), _ptr(h0),
         _ptr(o), _ptr(hT), _ptr(states), B, T, H, dk, dv,
-        NO_ERASE if no_erase else 0, int(threads))
+        (NO_ERASE if no_erase else 0) | (BETA_DIRECT if beta_direct else 0), int(threads))
     if rc != 0:
         raise RuntimeError(f"kla_oracle_forward failed with code {rc}")
     if return_states:
@@ -110,7 +115,7 @@ def kla_oracle_forward(q, k, v, g, eta, eps, h0=None, *, no_erase=False,
     return o, hT
 
 
-def kla_oracle_decode_step(q, k, v, g, eta, eps, S):
+def kla_oracle_decode_step(q, k, v, g, eta, eps, S, *, beta_direct=False):
     """One recurrent decode step: the forward loop with T = 1, h0 = S.
 
     Shapes: q,k [B,H,dk]; v [B,H,dv]; g,eta [B,H]; S [B,H,dk,dv].
@@ -118,8 +123,8 @@ def kla_oracle_decode_step(q, k, v, g, eta, eps, S):
     """
     q, k, v, g, eta, S = map(_f64, (q, k, v, g, eta, S))
     o, hT = kla_oracle_forward(q[:, None], k[:, None], v[:, None], g[:, None],
-                               eta[:, None], eps, S)
+                               eta[:, None], eps, S, beta_direct=beta_direct)
     return o[:, 0], hT
 
 
-__all__ = ["build", "kla_oracle_forward", "kla_oracle_decode_step", "NO_ERASE"]
+__all__ = ["build", "kla_oracle_forward", "kla_oracle_decode_step", "NO_ERASE", "BETA_DIRECT"]

@@ -25,6 +25,12 @@
  *   - no 1/sqrt(d_k) scaling of q and no extra normalisation of q or k;
  *   - eps is added to ||k_t||^2 inside the denominator.
  *
+ * KLA_ORACLE_BETA_DIRECT takes beta_t = eta_t as given (eps unused): the
+ * learned scalar coefficient of Gated DeltaNet that the same page's sections
+ * "Problem statement" and "Methodology" name as what KLA replaces; with
+ * g = 0 it is the ungated delta rule.  The library exposes this step size
+ * as KLA_BETA_DIRECT.
+ *
  * Test hook (never exported by the CUDA library): KLA_ORACLE_NO_ERASE drops
  * the erase term and uses unit write strength, S_t = a_t S_{t-1} + k_t v_t^T,
  * i.e. plain gated linear attention, so that a brute-force masked-attention
@@ -45,6 +51,7 @@
 #include <string.h>
 
 #define KLA_ORACLE_NO_ERASE 1
+#define KLA_ORACLE_BETA_DIRECT 2
 
 typedef struct {
     const double *q, *k, *v, *g, *eta, *h0;
@@ -80,10 +87,13 @@ static void run_head(job_t *J, int64_t b, int64_t h, double *S, double *x) {
             for (int64_t i = 0; i < dk; ++i)
                 for (int64_t j = 0; j < dv; ++j) S[i * dv + j] += kt[i] * vt[j];
         } else {
-            /* beta = eta / (||k||^2 + eps) */
-            double kk = 0.0;
-            for (int64_t i = 0; i < dk; ++i) kk += kt[i] * kt[i];
-            const double beta = J->eta[tok] / (kk + J->eps);
+            /* beta = eta / (||k||^2 + eps), or eta as given */
+            double beta = J->eta[tok];
+            if (!(J->flags & KLA_ORACLE_BETA_DIRECT)) {
+                double kk = 0.0;
+                for (int64_t i = 0; i < dk; ++i) kk += kt[i] * kt[i];
+                beta = J->eta[tok] / (kk + J->eps);
+            }
             /* e = v - S~^T k */
             for (int64_t j = 0; j < dv; ++j) x[j] = 0.0;
             for (int64_t i = 0; i < dk; ++i)

@@ -25,8 +25,11 @@ MUTATIONS = {
     "update_sign": ("S[i * dv + j] += bk * x[j];", "S[i * dv + j] -= bk * x[j];"),
     "residual_from_undecayed_state": ("x[j] = vt[j] - x[j];", "x[j] = vt[j] - x[j] / a;"),
     "readout_with_key": ("ot[j] += S[i * dv + j] * qt[i];", "ot[j] += S[i * dv + j] * kt[i];"),
-    "eta_ignored": ("const double beta = J->eta[tok] / (kk + J->eps);",
-                    "const double beta = 1.0 / (kk + J->eps);"),
+    "eta_ignored": ("beta = J->eta[tok] / (kk + J->eps);",
+                    "beta = 1.0 / (kk + J->eps);"),
+    "direct_beta_normalised": ("if (!(J->flags & KLA_ORACLE_BETA_DIRECT)) {", "if (1) {"),
+    "direct_beta_flag_inverted": ("if (!(J->flags & KLA_ORACLE_BETA_DIRECT)) {",
+                                  "if (J->flags & KLA_ORACLE_BETA_DIRECT) {"),
 }
 
 PINS = [
@@ -36,6 +39,7 @@ PINS = [
     pins.test_beta_zero_closed_form,
     lambda: pins.test_no_erase_equals_masked_attention(True),
     lambda: pins.test_normalised_sgd_step(0.37),
+    pins.test_direct_beta_hand_worked_two_tokens,
 ]
 
 

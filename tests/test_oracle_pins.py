@@ -256,3 +256,58 @@ def test_empty_sequence_returns_h0():
     o, hT = oracle.kla_oracle_forward(q, k, v, g, eta, 1e-6, h0)
     assert o.shape == (1, 0, 2, 3)
     np.testing.assert_array_equal(hT, h0)
+
+
+# ---- the direct step size beta_t = eta_t (the learned scalar of Gated
+# DeltaNet that the page's sections "Problem statement" and "Methodology" say
+# KLA replaces; with g = 0, the ungated delta rule)
+
+def test_direct_beta_hand_worked_two_tokens():
+    # d_k = 2, d_v = 1, h0 = 0.  Token 0: k = (1, 0), v = 2, q = (1, 1),
+    # g = 0, eta = 0.5.  Token 1: k = (1, 1), v = 3, q = (0, 2), g = log 0.5,
+    # eta = 0.25.
+    #   direct:   S_1 = 0.5 * (1,0) * 2 = (1, 0);              o_0 = 1
+    #             S~ = (0.5, 0), e = 3 - 0.5 = 2.5,
+    #             S_2 = (0.5, 0) + 0.25 * (1,1) * 2.5 = (1.125, 0.625); o_1 = 1.25
+    #   Kaczmarz (eps = 0): token 0 is the same (||k||^2 = 1); token 1 has
+    #             beta = 0.25 / 2, S_2 = (0.8125, 0.3125), o_1 = 0.625
+    q = np.array([[1.0, 1.0], [0.0, 2.0]]).reshape(1, 2, 1, 2)
+    k = np.array([[1.0, 0.0], [1.0, 1.0]]).reshape(1, 2, 1, 2)
+    v = np.array([2.0, 3.0]).reshape(1, 2, 1, 1)
+    g = np.array([0.0, math.log(0.5)]).reshape(1, 2, 1)
+    eta = np.array([0.5, 0.25]).reshape(1, 2, 1)
+    o, hT = oracle.kla_oracle_forward(q, k, v, g, eta, 0.0, beta_direct=True)
+    np.testing.assert_allclose(o.ravel(), [1.0, 1.25], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(hT.ravel(), [1.125, 0.625], rtol=0, atol=1e-15)
+    o, hT = oracle.kla_oracle_forward(q, k, v, g, eta, 0.0)
+    np.testing.assert_allclose(o.ravel(), [1.0, 0.625], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(hT.ravel(), [0.8125, 0.3125], rtol=0, atol=1e-15)
+
+
+def test_direct_beta_equals_kaczmarz_for_unit_keys():
+    # ||k_t|| = 1 and eps = 0 make eta_t / (||k_t||^2 + eps) = eta_t
+    rng = np.random.default_rng(31)
+    q, k, v, g, eta, h0 = _rand_inputs(rng, 2, 40, 3, 8, 5, knorm=(1.0, 1.0), h0_std=0.3)
+    o_d, h_d = oracle.kla_oracle_forward(q, k, v, g, eta, 0.0, h0, beta_direct=True)
+    o_k, h_k = oracle.kla_oracle_forward(q, k, v, g, eta, 0.0, h0)
+    np.testing.assert_allclose(o_d, o_k, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(h_d, h_k, rtol=1e-12, atol=1e-12)
+    # and with other key norms the two differ
+    q, k, v, g, eta, h0 = _rand_inputs(rng, 1, 40, 2, 8, 5, knorm=(2.0, 3.0))
+    o_d, _ = oracle.kla_oracle_forward(q, k, v, g, eta, 0.0, h0, beta_direct=True)
+    o_k, _ = oracle.kla_oracle_forward(q, k, v, g, eta, 0.0, h0)
+    assert np.max(np.abs(o_d - o_k)) > 1e-2
+
+
+def test_delta_rule_projection_with_unit_keys():
+    # g = 0, beta = 1, ||k|| = 1: the delta rule writes S_t^T k_t = v_t exactly
+    rng = np.random.default_rng(32)
+    B, T, H, dk, dv = 1, 30, 2, 6, 4
+    q, k, v, _, _, h0 = _rand_inputs(rng, B, T, H, dk, dv, knorm=(1.0, 1.0), h0_std=0.5)
+    g = np.zeros((B, T, H))
+    eta = np.ones((B, T, H))
+    _, _, states = oracle.kla_oracle_forward(q, k, v, g, eta, 0.0, h0, beta_direct=True,
+                                             return_states=True)
+    for t in range(T):
+        for h in range(H):
+            np.testing.assert_allclose(states[0, h, t].T @ k[0, t, h], v[0, t, h], rtol=0, atol=1e-12)

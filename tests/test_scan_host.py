@@ -82,3 +82,17 @@ def test_unsegmented_path_workspace(B, H, nchunks, extra):
             "handoff": B * H * 128 * 128 * 4,
             "none": 0}[extra]
     assert n == base + want
+
+
+def test_beta_mode_argument_errors():
+    # an unknown step-size rule is refused before any device work
+    kla = _kla()
+    lib = kla.load_library()
+    args = [None] * 5 + [1e-6, None, None, None]
+    for bad in (-1, 2, 7):
+        rc = lib.kla_chunk_fwd_ex(*args, 1, 128, 1, 128, 128, 64, kla.KLA_IO_BF16, bad, 0, None, 0,
+                                  None)
+        assert rc == kla.KLA_ERR_INVALID_ARG
+        rc = lib.kla_decode_step_ex(None, None, None, None, None, 1e-6, None, None, 1, 1, 128, 128,
+                                    kla.KLA_IO_BF16, bad, None)
+        assert rc == kla.KLA_ERR_INVALID_ARG
