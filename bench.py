@@ -5,7 +5,9 @@ Headline workload: the training-shape prefill (B=8, H=8, T=4096,
 d_k=d_v=128, bf16 q/k/v/o, fp32 gates, chunk 64) through kla_chunk_fwd:
 one step = one call over that batch.  The long-context prefill
 (B=1, H=16, T=131072) and the decode loop (B=64, H=16, d=128, fp32 state,
-kla_decode_step) are timed in the same run and reported under "secondary".
+kla_decode_step) are timed in the same run and reported under "secondary", with
+the training shape under Gated DeltaNet's step-size rule (kla_chunk_fwd_ex with
+KLA_BETA_DIRECT, unit-norm keys).
 
 Timing: W untimed warm-up steps, then exactly K timed steps, each between
 CUDA events on the launching stream; L2 is flushed (a 512 MiB write) between
@@ -82,8 +84,9 @@ def load_peaks():
 # so writes still in L2 when a launch ends are not counted.  Refresh these
 # whenever the kernels change.
 TRAFFIC_BYTES = {
-    "train_prefill_bf16_B8H8T4096d128": 450.9e6,
-    "long_prefill_bf16_B1H16T131072d128": 6224.6e6,
+    "train_prefill_bf16_B8H8T4096d128": 451.0e6,
+    "gdn_train_prefill_bf16_B8H8T4096d128_unitkeys": 452.5e6,
+    "long_prefill_bf16_B1H16T131072d128": 6223.7e6,
     "decode_bf16_B64H16d128_x1024": 71.7e6,
 }
 
@@ -245,7 +248,9 @@ def prefill_launches(kla, case) -> int:
     return 2
 
 
-def bench_prefill(case, K, W, flush, peaks, stream, e2e=True):
+def bench_prefill(case, K, W, flush, peaks, stream, e2e=True, direct=False):
+    """Time kla_chunk_fwd on ``case`` (kla_chunk_fwd_ex with KLA_BETA_DIRECT when
+    ``direct``: the same call under Gated DeltaNet's step-size rule)."""
     import chunked_delta_rule_kla_gb300 as kla
     inp = kla_inputs.make_prefill(case, device="cuda")
     B, T, H, dk, dv = case.B, case.T, case.H, case.dk, case.dv
@@ -254,8 +259,13 @@ def bench_prefill(case, K, W, flush, peaks, stream, e2e=True):
     ws = kla.alloc_workspace(B, T, H, dk, dv, case.chunk, kla.KLA_IO_BF16 if case.io == "bf16" else kla.KLA_IO_FP32)
 
     def step():
-        kla.kla_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["eta"], inp["eps"], inp["h0"],
-                          o, hT, ws, case.chunk, stream)
+        if direct:
+            kla.kla_chunk_fwd_ex(inp["q"], inp["k"], inp["v"], inp["g"], inp["eta"], inp["eps"],
+                                 inp["h0"], o, hT, ws, beta=kla.KLA_BETA_DIRECT, chunk=case.chunk,
+                                 stream=stream)
+        else:
+            kla.kla_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["eta"], inp["eps"],
+                              inp["h0"], o, hT, ws, case.chunk, stream)
 
     barrier()
     ms = timed_steps(step, K, W, flush, stream)
@@ -412,7 +422,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-heads", type=int, default=64)
     ap.add_argument("--decode-loops", type=int, default=3)
-    ap.add_argument("--only", choices=["train", "long", "decode"], default=None,
+    ap.add_argument("--only", choices=["train", "long", "gdn", "decode"], default=None,
                     help="time one workload only (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
     args = ap.parse_args()
@@ -443,8 +453,10 @@ def main():
                         us_per_call=dr["ms_per_call"] * 1e3, roofline=dr["roofline"],
                         gpu_launches=dr["launches"])
         else:
-            case = kla_inputs.TRAIN if args.only == "train" else kla_inputs.LONG
-            r = bench_prefill(case, args.steps, args.warmup, flush, peaks, stream, e2e=e2e)
+            case = {"train": kla_inputs.TRAIN, "long": kla_inputs.LONG,
+                    "gdn": kla_inputs.GDN_TRAIN}[args.only]
+            r = bench_prefill(case, args.steps, args.warmup, flush, peaks, stream, e2e=e2e,
+                              direct=args.only == "gdn")
             line = dict(workload=case.name, tokens_per_s=r["tokens_per_s"], ms_per_step=r["ms_per_step"],
                         roofline=r["roofline"], gpu_launches=r["launches"])
         clocks.stop()
@@ -460,6 +472,13 @@ def main():
         secondary["long_prefill"] = dict(workload=lc.name, tokens_per_s=lr["tokens_per_s"],
                                          ms_per_step=lr["ms_per_step"], roofline=lr["roofline"],
                                          tflops=lr["tflops"], e2e=lr.get("e2e"))
+        gc = kla_inputs.GDN_TRAIN
+        gr = bench_prefill(gc, max(5, args.steps // 2), 3, flush, peaks, stream, e2e=False,
+                           direct=True)
+        secondary["gdn_train_prefill"] = dict(workload=gc.name, beta="direct (eta as given)",
+                                              tokens_per_s=gr["tokens_per_s"],
+                                              ms_per_step=gr["ms_per_step"],
+                                              roofline=gr["roofline"])
         dc = kla_inputs.DECODE
         dr = bench_decode(dc, args.decode_loops, 3, peaks, stream, e2e=e2e)
         secondary["decode"] = dict(workload=dc.name, tokens_per_s=dr["tokens_per_s"],

@@ -78,6 +78,11 @@ TRAIN = PrefillCase("train_prefill_bf16_B8H8T4096d128", B=8, T=4096, H=8,
                     dk=128, dv=128, io="bf16", eps=1e-6, seed=2)
 LONG = PrefillCase("long_prefill_bf16_B1H16T131072d128", B=1, T=131072, H=16,
                    dk=128, dv=128, io="bf16", eps=1e-6, seed=3)
+# The training shape under the direct step size (Gated DeltaNet's rule): unit-norm
+# keys, as that rule is used with L2-normalised keys, so that eta in (0, 1) keeps
+# every step contractive.
+GDN_TRAIN = TRAIN.with_(name="gdn_train_prefill_bf16_B8H8T4096d128_unitkeys", knorm=(1.0, 1.0),
+                        seed=5)
 DECODE = DecodeCase("decode_bf16_B64H16d128_x1024", B=64, H=16, dk=128, dv=128,
                     steps=1024, io="bf16", eps=1e-6, seed=4)
 
@@ -157,4 +162,4 @@ def make_decode(case: DecodeCase, device="cpu", steps: Optional[int] = None) -> 
 
 
 __all__ = ["PrefillCase", "DecodeCase", "TINY", "PROJECTION", "TRAIN", "LONG",
-           "DECODE", "PREFILL_CASES", "make_prefill", "make_decode", "io_torch_dtype"]
+           "GDN_TRAIN", "DECODE", "PREFILL_CASES", "make_prefill", "make_decode", "io_torch_dtype"]
