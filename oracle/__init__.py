@@ -17,6 +17,10 @@ minimum-Frobenius-norm property against a least-squares solve; the exact
 line search and the normalised-SGD step (section "Key properties"); the
 beta=0 closed form; the no-erase mode against brute-force masked attention;
 and a hand-worked two-token fixture under ``tests/golden/``.
+
+``kla_oracle_backward`` is the reverse-mode derivative of the same loop
+(every state kept, the step undone operation by operation), pinned by central
+finite differences of ``kla_oracle_forward`` and by torch autograd.
 """
 from __future__ import annotations
 
@@ -64,6 +68,11 @@ def _load():
             f.argtypes = [dp, dp, dp, dp, dp, ctypes.c_double, dp, dp, dp, dp,
                           i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int]
             f.restype = ctypes.c_int
+            fb = lib.kla_oracle_backward
+            fb.argtypes = [dp, dp, dp, dp, dp, ctypes.c_double, dp, dp, dp,
+                           dp, dp, dp, dp, dp, dp,
+                           i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int]
+            fb.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -127,4 +136,31 @@ def kla_oracle_decode_step(q, k, v, g, eta, eps, S, *, beta_direct=False):
     return o[:, 0], hT
 
 
-__all__ = ["build", "kla_oracle_forward", "kla_oracle_decode_step", "NO_ERASE", "BETA_DIRECT"]
+def kla_oracle_backward(q, k, v, g, eta, eps, h0, dout, dhT=None, *, beta_direct=False,
+                        threads=0):
+    """Gradients of ``kla_oracle_forward`` (fp64, sequential reverse mode).
+
+    ``dout`` is dL/do [B,T,H,dv]; ``dhT`` is dL/dh_T [B,H,dk,dv] or None (zero).
+    Returns a dict with dq, dk [B,T,H,dk], dv [B,T,H,dv], dg, deta [B,T,H] and
+    dh0 [B,H,dk,dv] (the gradient of the start state, zero-state included).
+    """
+    q, k, v, g, eta, h0, dout, dhT = map(_f64, (q, k, v, g, eta, h0, dout, dhT))
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    assert q.shape == (B, T, H, dk) and v.shape == (B, T, H, dv) and dout.shape == v.shape
+    assert g.shape == (B, T, H) and eta.shape == (B, T, H)
+    for s_ in (h0, dhT):
+        assert s_ is None or s_.shape == (B, H, dk, dv)
+    out = dict(dq=np.zeros((B, T, H, dk)), dk=np.zeros((B, T, H, dk)), dv=np.zeros((B, T, H, dv)),
+               dg=np.zeros((B, T, H)), deta=np.zeros((B, T, H)), dh0=np.zeros((B, H, dk, dv)))
+    rc = _load().kla_oracle_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(eta), float(eps), _ptr(h0), _ptr(dout), _ptr(dhT),
+        _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]), _ptr(out["deta"]),
+        _ptr(out["dh0"]), B, T, H, dk, dv, BETA_DIRECT if beta_direct else 0, int(threads))
+    if rc != 0:
+        raise RuntimeError(f"kla_oracle_backward failed with code {rc}")
+    return out
+
+
+__all__ = ["build", "kla_oracle_forward", "kla_oracle_decode_step", "kla_oracle_backward",
+           "NO_ERASE", "BETA_DIRECT"]

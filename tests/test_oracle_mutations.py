@@ -47,9 +47,13 @@ PINS = [
 def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
     old, new = MUTATIONS[name]
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    # the mistakes are planted in the forward loop only (the reverse mode, after
+    # the marker, recomputes the forward with its own copy of these lines)
+    cut = src.index("/* Reverse mode.")
+    fwd, rest = src[:cut], src[cut:]
+    assert fwd.count(old) == 1, f"mutation anchor for {name} not found exactly once"
     mutated = tmp_path / "kla_oracle_mut.c"
-    mutated.write_text(src.replace(old, new))
+    mutated.write_text(fwd.replace(old, new) + rest)
     so = tmp_path / "libmut.so"
     if shutil.which("gcc") is None:
         pytest.skip("gcc not available")
