@@ -43,6 +43,8 @@ EXPORTED_SYMBOLS = (
     "kla_chunk_fwd_ex",
     "kla_decode_step",
     "kla_decode_step_ex",
+    "kla_chunk_bwd_workspace_bytes",
+    "kla_chunk_bwd",
     "kla_workspace_check",
     "kla_status_string",
 )
@@ -96,6 +98,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kla_chunk_fwd_ex.restype = i
         lib.kla_decode_step_ex.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, i, vp]
         lib.kla_decode_step_ex.restype = i
+        lib.kla_chunk_bwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+        lib.kla_chunk_bwd_workspace_bytes.restype = sz
+        lib.kla_chunk_bwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp,
+                                      vp, vp, vp, vp, vp, vp,
+                                      i, i, i, i, i, i, i, i, vp, sz, vp]
+        lib.kla_chunk_bwd.restype = i
         lib.kla_workspace_check.argtypes = [vp, sz, vp]
         lib.kla_workspace_check.restype = i
         lib.kla_status_string.argtypes = [i]
@@ -215,6 +223,38 @@ def kla_chunk_fwd_ex(q, k, v, g, eta, eps, h0, o, hT, workspace, beta=KLA_BETA_K
         raise KlaError(rc, "kla_chunk_fwd_ex")
 
 
+def kla_chunk_bwd_workspace_bytes(B, T, H, dk, dv, chunk=64, io=KLA_IO_BF16) -> int:
+    return int(load_library().kla_chunk_bwd_workspace_bytes(B, T, H, dk, dv, chunk, io))
+
+
+def kla_chunk_bwd(q, k, v, g, eta, eps, h0, grad_o, grad_hT, grad_q, grad_k, grad_v, grad_g,
+                  grad_eta, grad_h0, workspace, beta=KLA_BETA_KACZMARZ, chunk=64,
+                  stream=None) -> None:
+    """Enqueue the chunkwise backward (see include/kla.h): the gradients of
+    (o, hT) with respect to q, k, v, g, eta and h0.  grad_q, grad_k, grad_v have
+    the I/O dtype of q; grad_g, grad_eta, grad_h0 are fp32; grad_hT and grad_h0
+    may be None."""
+    B, T, H, dk, dv, io = _check_prefill_args(q, k, v, g, eta, h0, grad_o, grad_hT)
+    for name, t, ref in (("grad_q", grad_q, q), ("grad_k", grad_k, k), ("grad_v", grad_v, v)):
+        if t.shape != ref.shape or t.dtype != ref.dtype:
+            raise ValueError(f"{name} must match the shape and dtype of its input")
+    if grad_g.shape != g.shape or grad_eta.shape != eta.shape:
+        raise ValueError("grad_g and grad_eta must be [B,T,H]")
+    if grad_h0 is not None and tuple(grad_h0.shape) != (B, H, dk, dv):
+        raise ValueError("grad_h0 must be [B,H,dk,dv]")
+    rc = load_library().kla_chunk_bwd(
+        _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g", torch.float32),
+        _ptr(eta, "eta", torch.float32), float(eps), _ptr(h0, "h0", torch.float32),
+        _ptr(grad_o, "grad_o"), _ptr(grad_hT, "grad_hT", torch.float32),
+        _ptr(grad_q, "grad_q"), _ptr(grad_k, "grad_k"), _ptr(grad_v, "grad_v"),
+        _ptr(grad_g, "grad_g", torch.float32), _ptr(grad_eta, "grad_eta", torch.float32),
+        _ptr(grad_h0, "grad_h0", torch.float32), B, T, H, dk, dv, int(chunk), io, int(beta),
+        _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    if rc != KLA_OK:
+        raise KlaError(rc, "kla_chunk_bwd")
+
+
 def kla_chunk_fwd_noalloc(q, k, v, g, eta, eps, h0, o, hT, chunk=64, stream=None) -> None:
     """kla_chunk_fwd without a workspace, for callers that must not allocate
     device memory: the scratch is an array built into the library (see
@@ -292,6 +332,60 @@ def chunk_fwd(q, k, v, g, eta, eps=1e-6, h0=None, output_final_state=True, chunk
     return o, hT
 
 
+def chunk_bwd(q, k, v, g, eta, grad_o, grad_hT=None, eps=1e-6, h0=None, beta=KLA_BETA_KACZMARZ,
+              workspace=None, stream=None):
+    """Allocate the gradients and run kla_chunk_bwd.  Returns a dict with
+    dq, dk, dv, dg, deta and dh0."""
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    out = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+               dg=torch.empty_like(g), deta=torch.empty_like(eta),
+               dh0=torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device))
+    if workspace is None:
+        n = kla_chunk_bwd_workspace_bytes(B, T, H, dk, dv, 64, _io_of(q))
+        if n == 0:
+            raise KlaError(KLA_ERR_UNSUPPORTED, "kla_chunk_bwd_workspace_bytes")
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    kla_chunk_bwd(q, k, v, g, eta, eps, h0, grad_o, grad_hT, out["dq"], out["dk"], out["dv"],
+                  out["dg"], out["deta"], out["dh0"], workspace, beta=beta, stream=stream)
+    return out
+
+
+class KLAChunk(torch.autograd.Function):
+    """(o, hT) = KLA over a chunked sequence, differentiable in every input.
+
+    Forward runs kla_chunk_fwd_ex, backward kla_chunk_bwd; no state is kept
+    between them beyond the inputs."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, g, eta, h0, eps, beta):
+        B, T, H, dk = k.shape
+        dv = v.shape[-1]
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+        ws = alloc_workspace(B, T, H, dk, dv, 64, _io_of(q), q.device)
+        kla_chunk_fwd_ex(q, k, v, g, eta, eps, h0, o, hT, ws, beta=beta)
+        ctx.save_for_backward(q, k, v, g, eta, h0)
+        ctx.eps, ctx.beta = eps, beta
+        return o, hT
+
+    @staticmethod
+    def backward(ctx, do, dhT):
+        q, k, v, g, eta, h0 = ctx.saved_tensors
+        do = torch.zeros_like(q[..., :1].expand(*q.shape[:3], v.shape[-1])) if do is None else do
+        grads = chunk_bwd(q, k, v, g, eta, do.contiguous(),
+                          None if dhT is None else dhT.contiguous(), ctx.eps, h0, ctx.beta)
+        return (grads["dq"], grads["dk"], grads["dv"], grads["dg"], grads["deta"],
+                grads["dh0"] if h0 is not None else None, None, None)
+
+
+def kla_chunk(q, k, v, g, eta, eps=1e-6, h0=None, beta=KLA_BETA_KACZMARZ):
+    """Differentiable chunkwise KLA: returns (o, hT) and supports .backward()."""
+    return KLAChunk.apply(q.contiguous(), k.contiguous(), v.contiguous(), g.contiguous(),
+                          eta.contiguous(), None if h0 is None else h0.contiguous(), float(eps),
+                          int(beta))
+
+
 def decode_step(q, k, v, g, eta, S, eps=1e-6, stream=None, beta=KLA_BETA_KACZMARZ):
     """Run kla_decode_step (with the step size chosen by ``beta``); S is updated in
     place.  Returns o."""
@@ -304,6 +398,7 @@ __all__ = [
     "kla_chunk_fwd_workspace_bytes", "kla_chunk_fwd", "kla_chunk_fwd_noalloc", "kla_decode_step",
     "kla_chunk_fwd_scan", "kla_chunk_fwd_scan_workspace_bytes", "kla_chunk_fwd_auto_segments",
     "kla_chunk_fwd_ex", "kla_decode_step_ex", "KLA_BETA_KACZMARZ", "KLA_BETA_DIRECT",
+    "kla_chunk_bwd", "kla_chunk_bwd_workspace_bytes", "chunk_bwd", "kla_chunk", "KLAChunk",
     "kla_workspace_check",
     "kla_status_string", "chunk_fwd", "decode_step", "alloc_workspace", "load_library",
     "KlaError", "EXPORTED_SYMBOLS", "KLA_IO_BF16", "KLA_IO_FP32",

@@ -24,6 +24,7 @@ SOURCES = [
     "kla_chunk_simt.cu",
     "kla_chunk_tc.cu",
     "kla_noalloc.cu",
+    "kla_bwd.cu",
 ]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -160,6 +160,58 @@ kla_status kla_decode_step(const void* q, const void* k, const void* v, const fl
                               stream);
 }
 
+size_t kla_chunk_bwd_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk,
+                                     kla_io_dtype io) {
+    if (B < 0 || T < 0 || H < 0 || check_io(io) != KLA_OK) return 0;
+    if (!dim_ok(dk) || !dim_ok(dv) || chunk != 64) return 0;
+    if (!sizes_fit(B, T, H, dk, dv) || (int64_t)B * H > 65535) return 0;
+    const size_t body = sizeof(float) * kla::chunk_bwd_workspace_floats(B, T, H, dk, dv);
+    return kla::kErrorRecordBytes + (body + 255) / 256 * 256;
+}
+
+kla_status kla_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* eta, float eps, const float* h0, const void* grad_o,
+                         const float* grad_hT, void* grad_q, void* grad_k, void* grad_v,
+                         float* grad_g, float* grad_eta, float* grad_h0, int B, int T, int H,
+                         int dk, int dv, int chunk, kla_io_dtype io, kla_beta_mode beta,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+    if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || chunk <= 0) return KLA_ERR_INVALID_ARG;
+    if (check_io(io) != KLA_OK) return KLA_ERR_INVALID_ARG;
+    if (beta != KLA_BETA_KACZMARZ && beta != KLA_BETA_DIRECT) return KLA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f)) return KLA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv) || chunk != 64) return KLA_ERR_UNSUPPORTED;
+    if (!sizes_fit(B, T, H, dk, dv) || (int64_t)B * H > 65535) return KLA_ERR_UNSUPPORTED;
+    const bool have_tokens = (int64_t)B * H * T > 0;
+    if (have_tokens && (!q || !k || !v || !g || !eta || !grad_o || !grad_q || !grad_k ||
+                        !grad_v || !grad_g || !grad_eta))
+        return KLA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, h0, grad_o, grad_hT, grad_q, grad_k, grad_v, grad_h0};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return KLA_ERR_INVALID_ARG;
+    const void* vec[] = {g, eta, grad_g, grad_eta};
+    for (const void* p : vec)
+        if (p && !aligned4(p)) return KLA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kla::kErrorRecordBytes) return KLA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KLA_ERR_WORKSPACE;
+    if ((int64_t)B * H == 0) return KLA_OK;
+    if (workspace_bytes < kla_chunk_bwd_workspace_bytes(B, T, H, dk, dv, chunk, io))
+        return KLA_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, kla::kErrorRecordBytes, st);
+    if (e != cudaSuccess) return KLA_ERR_CUDA;
+    if (T == 0) {
+        // nothing happens between h0 and hT
+        if (!grad_h0) return KLA_OK;
+        const size_t bytes = sizeof(float) * (size_t)B * H * dk * dv;
+        if (grad_hT) return to_status(cudaMemcpyAsync(grad_h0, grad_hT, bytes, cudaMemcpyDeviceToDevice, st));
+        return to_status(cudaMemsetAsync(grad_h0, 0, bytes, st));
+    }
+    float* scratch = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kla::kErrorRecordBytes);
+    return to_status(kla::launch_chunk_bwd(q, k, v, g, eta, eps, h0, grad_o, grad_hT, grad_q, grad_k,
+                                           grad_v, grad_g, grad_eta, grad_h0, B, T, H, dk, dv,
+                                           io == KLA_IO_BF16, beta == KLA_BETA_DIRECT, scratch, st));
+}
+
 kla_status kla_workspace_check(const void* workspace, size_t workspace_bytes, void* stream) {
     if (!workspace || workspace_bytes < kla::kErrorRecordBytes) return KLA_ERR_WORKSPACE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -90,4 +90,15 @@ int chunk_ranges(int B, int H, int nchunks, int nseg);
 int chunk_range_bounds(int nchunks, int* bounds);
 int chunk_fwd_tc_auto_segments(int B, int T, int H, int dk, int dv);
 
+// Chunkwise backward (kla_bwd.cu): four launches on `stream` (per-chunk prep,
+// forward state carry, reverse gradient carry, per-chunk gradients).  bf16
+// I/O uses tf32 products; fp32 I/O uses a three-term tf32 split.  `scratch`
+// holds chunk_bwd_workspace_floats floats.
+size_t chunk_bwd_workspace_floats(int B, int T, int H, int dk, int dv);
+cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
+                             const float* eta, float eps, const float* h0, const void* dout,
+                             const float* dhT, void* dq, void* dk, void* dv, float* dg, float* deta,
+                             float* dh0, int B, int T, int H, int DK, int DV, bool bf16,
+                             bool beta_direct, float* scratch, cudaStream_t stream);
+
 }  // namespace kla

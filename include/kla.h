@@ -178,6 +178,40 @@ KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
                                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Chunkwise backward: the gradients of kla_chunk_fwd_ex's outputs (o, hT)
+ * with respect to all of its inputs.  The pages print no backward; this
+ * is the reverse mode of the same chunkwise algorithm ("KLA: Kaczmarz Linear
+ * Attention", section "Implementation": the chunkwise-parallel training
+ * algorithm of Gated DeltaNet is kept).  The forward states are recomputed
+ * inside the call; nothing has to be kept from the forward.
+ *
+ *  q, k, v, g, eta, eps, h0, beta : the forward's inputs (h0 may be NULL)
+ *  grad_o  : dL/do, [B, T, H, dv] I/O dtype
+ *  grad_hT : dL/dhT, fp32 [B, H, dk, dv], or NULL for zero
+ *  grad_q, grad_k : [B, T, H, dk] I/O dtype    grad_v : [B, T, H, dv] I/O dtype
+ *  grad_g, grad_eta : fp32 [B, T, H]
+ *  grad_h0 : fp32 [B, H, dk, dv], or NULL when not wanted
+ *  chunk = 64; dk, dv : 64 or 128 each; B*H <= 65535.
+ *
+ * Products are tf32 tensor-core tiles with fp32 accumulation; with fp32 I/O
+ * each product is split into three tf32 products (fp32-level accuracy).
+ * The workspace (kla_chunk_bwd_workspace_bytes, 256-byte aligned, caller
+ * owned) holds per-chunk records, every chunk's start state and state
+ * gradient: about 312 KB per (batch, head, chunk) at dk = dv = 128.  Errors
+ * are those of kla_chunk_fwd_ex; outputs are undefined unless KLA_OK.
+ */
+KLA_API size_t kla_chunk_bwd_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk,
+                                             kla_io_dtype io);
+KLA_API kla_status kla_chunk_bwd(const void* q, const void* k, const void* v,
+                                 const float* g, const float* eta, float eps,
+                                 const float* h0, const void* grad_o, const float* grad_hT,
+                                 void* grad_q, void* grad_k, void* grad_v, float* grad_g,
+                                 float* grad_eta, float* grad_h0,
+                                 int B, int T, int H, int dk, int dv, int chunk,
+                                 kla_io_dtype io, kla_beta_mode beta,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Segment count kla_chunk_fwd uses for this shape (1 = no scan).  With bf16
  * I/O and dk = dv = 128, when 4*B*H <= 152 (a GB300's SMs), it is
  * floor(152 / (B*H)): one full wave of per-(head, run) carry CTAs.  For the
