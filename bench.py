@@ -7,7 +7,8 @@ one step = one call over that batch.  The long-context prefill
 (B=1, H=16, T=131072) and the decode loop (B=64, H=16, d=128, fp32 state,
 kla_decode_step) are timed in the same run and reported under "secondary", with
 the training shape under Gated DeltaNet's step-size rule (kla_chunk_fwd_ex with
-KLA_BETA_DIRECT, unit-norm keys).
+KLA_BETA_DIRECT, unit-norm keys) and the backward (kla_chunk_bwd) of the
+training shape.
 
 Timing: W untimed warm-up steps, then exactly K timed steps, each between
 CUDA events on the launching stream; L2 is flushed (a 512 MiB write) between
@@ -57,6 +58,23 @@ def prefill_work(case):
     return dict(bytes=th * per_tok_bytes + state_bytes, flops=th * flops_tok,
                 token_heads=th, tokens=case.B * case.T,
                 per_token_head_bytes=per_tok_bytes, per_token_head_flops=flops_tok)
+
+
+def backward_work(case):
+    """Algorithmic bytes of one kla_chunk_bwd call: q, k, v, dO, g, eta read and
+    dq, dk, dv, dg, deta written once per token-head; dhT read and dh0 written
+    (h0 read too when present) once per head."""
+    esz = 2 if case.io == "bf16" else 4
+    C, dk, dv = case.chunk, case.dk, case.dv
+    th = case.B * case.T * case.H
+    per_tok_bytes = esz * (4 * dk + 3 * dv) + 16
+    state_bytes = case.B * case.H * dk * dv * 4 * (3 if case.h0_std > 0 else 2)
+    # products per token-head: prep 2C(3dk + 2dv), the two carries 10 dk dv,
+    # the gradients 2(6C dk + 4C dv + 4 dk dv)
+    flops_tok = 2 * C * (9 * dk + 6 * dv) + 18 * dk * dv
+    return dict(bytes=th * per_tok_bytes + state_bytes, flops=th * flops_tok, token_heads=th,
+                tokens=case.B * case.T, per_token_head_bytes=per_tok_bytes,
+                per_token_head_flops=flops_tok)
 
 
 def decode_work(case):
@@ -319,6 +337,41 @@ def bench_prefill(case, K, W, flush, peaks, stream, e2e=True, direct=False):
     return res
 
 
+def bench_backward(case, K, W, flush, peaks, stream):
+    """Time kla_chunk_bwd (the gradients of o and hT w.r.t. every input) on ``case``."""
+    import chunked_delta_rule_kla_gb300 as kla
+    inp = kla_inputs.make_prefill(case, device="cuda")
+    B, T, H, dk, dv = case.B, case.T, case.H, case.dk, case.dv
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(case.seed + 1000)
+    do = torch.randn((B, T, H, dv), generator=gen, device="cuda").to(inp["q"].dtype)
+    dhT = torch.randn((B, H, dk, dv), generator=gen, device="cuda")
+    io = kla.KLA_IO_BF16 if case.io == "bf16" else kla.KLA_IO_FP32
+    ws = torch.empty(kla.kla_chunk_bwd_workspace_bytes(B, T, H, dk, dv, case.chunk, io),
+                     dtype=torch.uint8, device="cuda")
+    gq, gk, gv = torch.empty_like(inp["q"]), torch.empty_like(inp["k"]), torch.empty_like(inp["v"])
+    gg, ge = torch.empty_like(inp["g"]), torch.empty_like(inp["eta"])
+    gh0 = torch.empty_like(dhT)
+
+    def step():
+        kla.kla_chunk_bwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["eta"], inp["eps"], inp["h0"],
+                          do, dhT, gq, gk, gv, gg, ge, gh0, ws, stream=stream)
+
+    barrier()
+    ms = timed_steps(step, K, W, flush, stream)
+    barrier()
+    work = backward_work(case)
+    _, slowest_s = job_throughput(work["tokens"], sum(ms) / len(ms) * 1e-3)
+    mean_ms = slowest_s * 1e3
+    res = dict(ms_per_step=mean_ms, tokens_per_s=work["tokens"] / (mean_ms * 1e-3),
+               roofline=dict(roofline(work, mean_ms * 1e-3, peaks, TRAFFIC_BYTES.get("bwd_" + case.name)),
+                             scope="one kla_chunk_bwd call: its three launches (prep, the two carries in one grid, gradients)",
+                             peak_kind="burst copy bandwidth"),
+               launches=3 * K, min_ms=min(ms), workspace_bytes=ws.numel())
+    del inp, do, dhT, ws, gq, gk, gv, gg, ge, gh0
+    return res
+
+
 def bench_decode(case, K_loops, W_loops, peaks, stream, n_states=4, e2e=True):
     """Times `steps` consecutive kla_decode_step calls per loop.  The calls
     rotate over n_states independent state buffers (like the layers of a
@@ -422,7 +475,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-heads", type=int, default=64)
     ap.add_argument("--decode-loops", type=int, default=3)
-    ap.add_argument("--only", choices=["train", "long", "gdn", "decode"], default=None,
+    ap.add_argument("--only", choices=["train", "long", "gdn", "decode", "bwd"], default=None,
                     help="time one workload only (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
     args = ap.parse_args()
@@ -447,7 +500,12 @@ def main():
 
     e2e = not args.no_e2e
     if args.only is not None:
-        if args.only == "decode":
+        if args.only == "bwd":
+            br = bench_backward(kla_inputs.TRAIN, args.steps, args.warmup, flush, peaks, stream)
+            line = dict(workload="bwd_" + kla_inputs.TRAIN.name, tokens_per_s=br["tokens_per_s"],
+                        ms_per_step=br["ms_per_step"], roofline=br["roofline"],
+                        gpu_launches=br["launches"])
+        elif args.only == "decode":
             dr = bench_decode(kla_inputs.DECODE, args.decode_loops, args.warmup, peaks, stream, e2e=e2e)
             line = dict(workload=kla_inputs.DECODE.name, tokens_per_s=dr["tokens_per_s"],
                         us_per_call=dr["ms_per_call"] * 1e3, roofline=dr["roofline"],
@@ -479,6 +537,10 @@ def main():
                                               tokens_per_s=gr["tokens_per_s"],
                                               ms_per_step=gr["ms_per_step"],
                                               roofline=gr["roofline"])
+        br = bench_backward(kla_inputs.TRAIN, max(5, args.steps // 4), 3, flush, peaks, stream)
+        secondary["backward_train"] = dict(workload="bwd_" + kla_inputs.TRAIN.name,
+                                           tokens_per_s=br["tokens_per_s"],
+                                           ms_per_step=br["ms_per_step"], roofline=br["roofline"])
         dc = kla_inputs.DECODE
         dr = bench_decode(dc, args.decode_loops, 3, peaks, stream, e2e=e2e)
         secondary["decode"] = dict(workload=dc.name, tokens_per_s=dr["tokens_per_s"],

@@ -19,11 +19,14 @@
 //   dW  = Kt dS1 + P^T dO
 //   dS0 = Gam_C dS1 + (diag(Gam) Q)^T dO - Wk^T dW
 //
-// Four launches:
-//   bwd_prep_kernel       every (chunk, head): beta, gamma, T, Wk, U, P^T dO
-//   bwd_fwd_carry_kernel  every head, chunks in order: S0 of each chunk, W
-//   bwd_rev_carry_kernel  every head, chunks in reverse: dS1 of each chunk, dW
-//   bwd_grad_kernel       every (chunk, head): dq, dk, dv, dg, deta
+// Three launches:
+//   bwd_prep_kernel   every (chunk, head): beta, gamma, T, Wk, U, P^T dO and
+//                     L = (diag(Gam) Q)^T dO
+//   bwd_carry_kernel  every head twice, at the same time: the forward carry
+//                     (chunks in order) keeps S0 and W of each chunk; the
+//                     reverse carry (chunks in reverse, dS0 = Gam_C dS1 + L -
+//                     Wk^T dW) keeps dS1 and dW.  Neither needs the other.
+//   bwd_grad_kernel   every (chunk, head): dq, dk, dv, dg, deta
 //
 // Given S0, dS1, W and dW, the gradient kernel works out the rest:
 //   - dX = T^T dW, dv = diag(beta) dX;
@@ -37,6 +40,8 @@
 // L1/L2.  With fp32 I/O each product is split into three tf32 products
 // (hi*hi + hi*lo + lo*hi), which keeps fp32-level accuracy.
 #include "kla_internal.cuh"
+
+#include <algorithm>
 
 namespace kla {
 namespace {
@@ -71,17 +76,57 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ float warp_sum(float s) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    return s;
+}
+
+// Eight consecutive values of one storage row (16-byte aligned), as fp32.
+template <typename T> __device__ __forceinline__ void ld8(const T* p, float (&x)[8]);
+template <> __device__ __forceinline__ void ld8<float>(const float* p, float (&x)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+template <> __device__ __forceinline__ void ld8<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[8]) {
+    const uint4 r = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
 // One operand of a product: element (i, j) of op(X), where op is the
 // identity or the transpose.  Storage rows at or past `rows` read as zero
 // (the tail of the last chunk).
+//   run8(i, k0, x): x[u] = op(X)(i, k0 + u) for the A operand (M x K), or
+//                   op(X)(k0 + u, i) for the B operand (K x N) with B_ROLE.
+// The eight values are one storage row's 16-byte-aligned run when the
+// operand is stored with k along its rows (A untransposed, B transposed).
 template <typename T, bool TRANS>
 struct Opnd {
     const T* p;
     int ld;
     int rows;
-    __device__ __forceinline__ float at(int i, int j) const {
-        const int r = TRANS ? j : i, c = TRANS ? i : j;
-        return r < rows ? ldf<T>(p + (size_t)r * ld + c) : 0.f;
+    template <bool B_ROLE>
+    __device__ __forceinline__ void run8(int i, int k0, float (&x)[8]) const {
+        constexpr bool contiguous = B_ROLE ? TRANS : !TRANS;
+        if (contiguous) {
+            if (i < rows) {
+                ld8<T>(p + (size_t)i * ld + k0, x);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] = 0.f;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int r = k0 + u;
+                x[u] = r < rows ? ldf<T>(p + (size_t)r * ld + i) : 0.f;
+            }
+        }
     }
 };
 template <bool TRANS, typename T>
@@ -90,10 +135,15 @@ __device__ __forceinline__ Opnd<T, TRANS> opnd(const T* p, int ld, int rows = 1 
 }
 
 // C[m][n] = (acc ? C[m][n] : 0) + alpha * rs[m] * sum_k A(m,k) B(k,n), for an
-// M x N output (M % 16 == 0, N % 32 == 0, K % 8 == 0) computed by every warp
-// of the CTA, one 16 x 32 tile at a time.  rs may be null (1).  No barrier
-// inside: the caller orders the operands' writes before and the result's
-// reads after.
+// M x N output (M % 16 == 0, N % 32 == 0, K % 32 == 0) computed by every warp
+// of the CTA, one 16 x 32 tile at a time.  Within each 32-wide k batch the
+// k index is permuted, the same way for A and B (a sum over k does not
+// depend on its order): in k-step s, lane (g, t) supplies k = 8t + 2s and
+// 8t + 2s + 1 where the MMA's fragment layout names t and t + 4.  A lane's
+// four k-steps thus read eight consecutive k of each of its rows and
+// columns, loaded before the MMAs so that global-memory operands overlap
+// their latencies.  rs may be null (1).  No barrier inside: the caller
+// orders the operands' writes before and the result's reads after.
 template <bool PRECISE, typename OA, typename OB>
 __device__ void mm(int M, int N, int K, const OA& A, const OB& B, float* Cp, int ldc, float alpha,
                    bool acc, const float* rs = nullptr) {
@@ -105,26 +155,32 @@ __device__ void mm(int M, int N, int K, const OA& A, const OB& B, float* Cp, int
         float d[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
-        for (int k0 = 0; k0 < K; k0 += 8) {
-            const float af[4] = {A.at(m0 + g, k0 + t), A.at(m0 + g + 8, k0 + t),
-                                 A.at(m0 + g, k0 + t + 4), A.at(m0 + g + 8, k0 + t + 4)};
-            uint32_t ah[4], al[4];
+        for (int k0 = 0; k0 < K; k0 += 32) {
+            float ar[2][8], br[4][8];
+            A.template run8<false>(m0 + g, k0 + 8 * t, ar[0]);
+            A.template run8<false>(m0 + g + 8, k0 + 8 * t, ar[1]);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                ah[i] = tf32_bits(af[i]);
-                if (PRECISE) al[i] = tf32_bits(af[i] - __uint_as_float(ah[i]));
-            }
+            for (int nt = 0; nt < 4; ++nt) B.template run8<true>(n0 + 8 * nt + g, k0 + 8 * t, br[nt]);
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int n = n0 + 8 * nt + g;
-                const float b0 = B.at(k0 + t, n), b1 = B.at(k0 + t + 4, n);
-                const uint32_t bh0 = tf32_bits(b0), bh1 = tf32_bits(b1);
-                mma_tf32(d[nt], ah, bh0, bh1);
-                if (PRECISE) {
-                    const uint32_t bl0 = tf32_bits(b0 - __uint_as_float(bh0));
-                    const uint32_t bl1 = tf32_bits(b1 - __uint_as_float(bh1));
-                    mma_tf32(d[nt], ah, bl0, bl1);
-                    mma_tf32(d[nt], al, bh0, bh1);
+            for (int ks = 0; ks < 4; ++ks) {
+                const float af[4] = {ar[0][2 * ks], ar[1][2 * ks], ar[0][2 * ks + 1], ar[1][2 * ks + 1]};
+                uint32_t ah[4], al[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    ah[i] = tf32_bits(af[i]);
+                    if (PRECISE) al[i] = tf32_bits(af[i] - __uint_as_float(ah[i]));
+                }
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const float b0 = br[nt][2 * ks], b1 = br[nt][2 * ks + 1];
+                    const uint32_t bh0 = tf32_bits(b0), bh1 = tf32_bits(b1);
+                    mma_tf32(d[nt], ah, bh0, bh1);
+                    if (PRECISE) {
+                        const uint32_t bl0 = tf32_bits(b0 - __uint_as_float(bh0));
+                        const uint32_t bl1 = tf32_bits(b1 - __uint_as_float(bh1));
+                        mma_tf32(d[nt], ah, bl0, bl1);
+                        mma_tf32(d[nt], al, bh0, bh1);
+                    }
                 }
             }
         }
@@ -146,15 +202,16 @@ __device__ void mm(int M, int N, int K, const OA& A, const OB& B, float* Cp, int
 }
 
 // Per-(chunk, head) record written by the prep (fp32):
-//   gamma[64] | beta[64] | kk[64] | T[64][64] | Wk[64][dk] | U[64][dv] | PdO[64][dv]
+//   gamma[64] | beta[64] | kk[64] | T[64][64] | Wk[64][dk] | U[64][dv] | PdO[64][dv] | L[dk][dv]
 struct RecLayout {
-    size_t gamma, beta, kk, T, Wk, U, PdO, floats;
+    size_t gamma, beta, kk, T, Wk, U, PdO, L, floats;
     __host__ __device__ RecLayout(int dk, int dv) {
         gamma = 0; beta = C; kk = 2 * C; T = 3 * C;
         Wk = T + (size_t)C * C;
         U = Wk + (size_t)C * dk;
         PdO = U + (size_t)C * dv;
-        floats = PdO + (size_t)C * dv;
+        L = PdO + (size_t)C * dv;
+        floats = L + (size_t)dk * dv;
     }
 };
 
@@ -184,15 +241,198 @@ __device__ __forceinline__ int chunk_valid(const BwdParams& p, int c) {
     return n < C ? n : C;
 }
 
+// ------------------------------------------------------------ data movement
+// 16-byte vectors: 4 fp32 or 8 bf16 values.
+template <typename T> struct Vec;
+template <> struct Vec<float> {
+    static constexpr int W = 4;
+    __device__ __forceinline__ static void unpack(const uint4& r, float* x) {
+        x[0] = __uint_as_float(r.x); x[1] = __uint_as_float(r.y);
+        x[2] = __uint_as_float(r.z); x[3] = __uint_as_float(r.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float* x) {
+        return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                          __float_as_uint(x[3]));
+    }
+};
+template <> struct Vec<__nv_bfloat16> {
+    static constexpr int W = 8;
+    __device__ __forceinline__ static void unpack(const uint4& r, float* x) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    __device__ __forceinline__ static uint4 pack(const float* x) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
+// For every 16-byte vector of rows [0, rows) x cols of a row-major matrix
+// (row r at src + r * ld), calls f(r, j, x[Vec<T>::W]) with the values as
+// fp32 (zero for rows at or past nvalid).  Four vectors are in flight per
+// thread.
+template <typename T, typename F>
+__device__ __forceinline__ void for_rows(const T* src, size_t ld, int rows, int cols, int nvalid,
+                                         F f) {
+    constexpr int VW = Vec<T>::W;
+    const int vpr = cols / VW, total = rows * vpr;
+    for (int base = threadIdx.x; base < total; base += 4 * blockDim.x) {
+        uint4 raw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int v = base + u * blockDim.x;
+            const int r = v / vpr, j = (v - r * vpr) * VW;
+            raw[u] = (v < total && r < nvalid)
+                         ? __ldg(reinterpret_cast<const uint4*>(src + (size_t)r * ld + j))
+                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int v = base + u * blockDim.x;
+            if (v < total) {
+                const int r = v / vpr, j = (v - r * vpr) * VW;
+                float x[VW];
+                Vec<T>::unpack(raw[u], x);
+                f(r, j, x);
+            }
+        }
+    }
+}
+
+// dst[r][j] = rs[r] * src[r][j] (fp32 in shared memory; rs null: 1)
+template <typename T>
+__device__ __forceinline__ void stage_rows(float* dst, int lds, const T* src, size_t ld, int rows,
+                                           int cols, int nvalid, const float* rs) {
+    for_rows<T>(src, ld, rows, cols, nvalid, [&](int r, int j, const float* x) {
+        const float sc = rs ? rs[r] : 1.f;
+#pragma unroll
+        for (int i = 0; i < Vec<T>::W; i += 4)
+            *reinterpret_cast<float4*>(dst + r * lds + j + i) =
+                make_float4(sc * x[i], sc * x[i + 1], sc * x[i + 2], sc * x[i + 3]);
+    });
+}
+
+// the same rows copied unchanged into shared memory of the source type
+template <typename T>
+__device__ __forceinline__ void copy_rows(T* dst, int lds, const T* src, size_t ld, int rows,
+                                          int cols, int nvalid) {
+    constexpr int VW = Vec<T>::W;
+    const int vpr = cols / VW, total = rows * vpr;
+    for (int base = threadIdx.x; base < total; base += 4 * blockDim.x) {
+        uint4 raw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int v = base + u * blockDim.x;
+            const int r = v / vpr, j = (v - r * vpr) * VW;
+            raw[u] = (v < total && r < nvalid)
+                         ? __ldg(reinterpret_cast<const uint4*>(src + (size_t)r * ld + j))
+                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int v = base + u * blockDim.x;
+            if (v < total) {
+                const int r = v / vpr, j = (v - r * vpr) * VW;
+                *reinterpret_cast<uint4*>(dst + r * lds + j) = raw[u];
+            }
+        }
+    }
+}
+
+// f(i, x[4]) for each float4 i of a contiguous fp32 array of n floats (n % 4 == 0)
+template <typename F>
+__device__ __forceinline__ void for_f4(const float* src, int n, F f) {
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+    const int n4 = n / 4;
+    for (int base = threadIdx.x; base < n4; base += 4 * blockDim.x) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = base + u * blockDim.x;
+            v[u] = idx < n4 ? __ldg(s4 + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = base + u * blockDim.x;
+            if (idx < n4) {
+                const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                f(idx, x);
+            }
+        }
+    }
+}
+
+// f(i, v) for i in [0, n) with v = ld(i) (a float4 read), four reads in
+// flight per thread
+template <typename LD, typename F>
+__device__ __forceinline__ void batched4(int n, LD ld, F f) {
+    for (int base = threadIdx.x; base < n; base += 4 * blockDim.x) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = base + u * blockDim.x;
+            v[u] = idx < n ? ld(idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = base + u * blockDim.x;
+            if (idx < n) f(idx, v[u]);
+        }
+    }
+}
+
+// per-row scalars of the chunk (g or eta) into shared memory, zero past nvalid
+__device__ __forceinline__ void load_row_scalars(float* dst, const float* src, const BwdParams& p,
+                                                 int bh, int c, int nvalid) {
+    for (int r = threadIdx.x; r < C; r += blockDim.x)
+        dst[r] = r < nvalid ? __ldg(src + tok_index(p, bh, c, r)) : 0.f;
+}
+
 // ------------------------------------------------------------------ prep
+// rows x cols of a row-major global matrix, transposed into shared memory:
+// dst[j][r] = rs[r] * src[r][j] (zero for rows at or past nvalid; rs null: 1).
+// Lanes run along r, so the shared-memory writes do not conflict.
+template <typename T>
+__device__ __forceinline__ void stage_cols(float* dst, int ldd, const T* src, size_t ld, int rows,
+                                           int cols, int nvalid, const float* rs) {
+    constexpr int VW = Vec<T>::W;
+    for (int i = threadIdx.x; i < rows * cols / VW; i += blockDim.x) {
+        const int r = i % rows, j = (i / rows) * VW;
+        float x[VW];
+        if (r < nvalid) {
+            Vec<T>::unpack(__ldg(reinterpret_cast<const uint4*>(src + (size_t)r * ld + j)), x);
+        } else {
+#pragma unroll
+            for (int u = 0; u < VW; ++u) x[u] = 0.f;
+        }
+        const float sc = rs ? rs[r] : 1.f;
+#pragma unroll
+        for (int u = 0; u < VW; ++u) dst[(j + u) * ldd + r] = sc * x[u];
+    }
+}
+
+// Every product of the prep reads its operands along k in 16-byte runs:
+// row-major K and Q, and the transposes (beta Gam K)^T, (beta V)^T,
+// (Gam Q)^T and dO^T.
 template <typename TIO, bool PRECISE>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdParams p) {
     extern __shared__ __align__(16) float smf[];
     const int c = blockIdx.x, bh = blockIdx.y;
-    const int DK = p.DK, DV = p.DV, ldK = DK + kPad, ldX = (DK > DV ? DK : DV) + kPad;
-    float* sK = smf;                       // C x DK
-    float* sX = sK + C * ldK;              // C x max(DK, DV)
-    float* sT = sX + C * ldX;              // C x C
+    const int DK = p.DK, DV = p.DV, DM = DK > DV ? DK : DV;
+    const int ldR = DM + kPad;             // row-major C x d tiles
+    const int big = DM * kLdCC > C * ldR ? DM * kLdCC : C * ldR;
+    float* b1 = smf;                       // K (row-major), then (Gam Q)^T
+    float* b2 = b1 + big;                  // (beta Gam K)^T, (beta V)^T, Q (row-major), dO^T
+    float* sT = b2 + big;                  // C x C
     float* sG = sT + C * kLdCC;            // C x C
     float* sgam = sG + C * kLdCC;          // gamma
     float* sbeta = sgam + C;
@@ -201,7 +441,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdParams p) {
     const int tid = threadIdx.x, nt = blockDim.x;
     const int nvalid = chunk_valid(p, c);
     const size_t t0 = tok_index(p, bh, c, 0);
-    const int sH = p.H;
+    const size_t ldk = (size_t)p.H * DK, ldv = (size_t)p.H * DV;
     const TIO* K = static_cast<const TIO*>(p.k) + t0 * DK;
     const TIO* Q = static_cast<const TIO*>(p.q) + t0 * DK;
     const TIO* V = static_cast<const TIO*>(p.v) + t0 * DV;
@@ -209,39 +449,48 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdParams p) {
     const RecLayout L(DK, DV);
     float* rec = p.rec + ((size_t)bh * p.nchunks + c) * L.floats;
 
-    for (int i = tid; i < C * DK; i += nt) {
-        const int r = i / DK, j = i % DK;
-        sK[r * ldK + j] = r < nvalid ? ldf<TIO>(K + (size_t)r * sH * DK + j) : 0.f;
-    }
+    stage_rows<TIO>(b1, ldR, K, ldk, C, DK, nvalid, nullptr);
+    load_row_scalars(sgam, p.g, p, bh, c, nvalid);
+    load_row_scalars(sbeta, p.eta, p, bh, c, nvalid);
     __syncthreads();
     // ||k_r||^2, one warp per row
     for (int r = tid >> 5; r < C; r += nt >> 5) {
         float s = 0.f;
-        for (int j = tid & 31; j < DK; j += 32) s += sK[r * ldK + j] * sK[r * ldK + j];
-#pragma unroll
-        for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        for (int j = tid & 31; j < DK; j += 32) s += b1[r * ldR + j] * b1[r * ldR + j];
+        s = warp_sum(s);
         if ((tid & 31) == 0) skk[r] = s;
     }
     __syncthreads();
-    if (tid == 0) {
-        float acc = 0.f;
-        for (int r = 0; r < C; ++r) {
-            const size_t ti = tok_index(p, bh, c, r);
-            const bool ok = r < nvalid;
-            acc += ok ? p.g[ti] : 0.f;
-            sgam[r] = acc;
-            const float e = ok ? p.eta[ti] : 0.f;
-            sbeta[r] = ok ? (p.beta_direct ? e : e / (skk[r] + p.eps)) : 0.f;
-            sbg[r] = sbeta[r] * __expf(acc);
+    if (tid < 32) {
+        // gamma = inclusive cumulative sum of g: two rows per lane, then a warp scan
+        const float a0 = sgam[2 * tid], a1 = a0 + sgam[2 * tid + 1];
+        float x = a1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, o);
+            if (tid >= o) x += y;
         }
+        const float before = x - a1;
+        sgam[2 * tid] = before + a0;
+        sgam[2 * tid + 1] = x;
+    }
+    if (tid < C) {
+        const float e = sbeta[tid];
+        sbeta[tid] = tid < nvalid ? (p.beta_direct ? e : e / (skk[tid] + p.eps)) : 0.f;
     }
     __syncthreads();
+    if (tid < C) sbg[tid] = sbeta[tid] * __expf(sgam[tid]);
     // G = K K^T -> A = diag(beta) strict_lower(D o G)
-    mm<PRECISE>(C, C, DK, opnd<false>(sK, ldK), opnd<true>(sK, ldK), sG, kLdCC, 1.f, false);
+    mm<PRECISE>(C, C, DK, opnd<false>(b1, ldR), opnd<true>(b1, ldR), sG, kLdCC, 1.f, false);
     __syncthreads();
     for (int i = tid; i < C * C; i += nt) {
-        const int r = i / C, s = i % C;
-        sG[r * kLdCC + s] = s < r ? sbeta[r] * __expf(sgam[r] - sgam[s]) * sG[r * kLdCC + s] : 0.f;
+        const int r = i / C, s2 = i % C;
+        sG[r * kLdCC + s2] = s2 < r ? sbeta[r] * __expf(sgam[r] - sgam[s2]) * sG[r * kLdCC + s2] : 0.f;
+    }
+    // (beta Gam K)^T from the K rows
+    for (int i = tid; i < C * DK; i += nt) {
+        const int r = i % C, j = i / C;
+        b2[j * kLdCC + r] = sbg[r] * b1[r * ldR + j];
     }
     __syncthreads();
     // T = (I + A)^{-1}: column j by four lanes of one warp, forward substitution
@@ -250,7 +499,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdParams p) {
         if (j < C) {
             for (int r = 0; r < C; ++r) {
                 float a = 0.f;
-                for (int s = j + part; s < r; s += 4) a += sG[r * kLdCC + s] * sT[s * kLdCC + j];
+                for (int s2 = j + part; s2 < r; s2 += 4) a += sG[r * kLdCC + s2] * sT[s2 * kLdCC + j];
                 a += __shfl_xor_sync(0xffffffffu, a, 1);
                 a += __shfl_xor_sync(0xffffffffu, a, 2);
                 if (part == 0) sT[r * kLdCC + j] = r == j ? 1.f : (r < j ? 0.f : -a);
@@ -260,32 +509,32 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdParams p) {
     }
     __syncthreads();
     // Wk = T diag(beta Gam) K
-    for (int i = tid; i < C * DK; i += nt) {
-        const int r = i / DK, j = i % DK;
-        sX[r * ldX + j] = sbg[r] * sK[r * ldK + j];
-    }
-    __syncthreads();
-    mm<PRECISE>(C, DK, C, opnd<false>(sT, kLdCC), opnd<false>(sX, ldX), rec + L.Wk, DK, 1.f, false);
+    mm<PRECISE>(C, DK, C, opnd<false>(sT, kLdCC), opnd<true>(b2, kLdCC), rec + L.Wk, DK, 1.f, false);
     __syncthreads();
     // U = T diag(beta) V
-    for (int i = tid; i < C * DV; i += nt) {
-        const int r = i / DV, j = i % DV;
-        sX[r * ldX + j] = r < nvalid ? sbeta[r] * ldf<TIO>(V + (size_t)r * sH * DV + j) : 0.f;
+    stage_cols<TIO>(b2, kLdCC, V, ldv, C, DV, nvalid, sbeta);
+    __syncthreads();
+    mm<PRECISE>(C, DV, C, opnd<false>(sT, kLdCC), opnd<true>(b2, kLdCC), rec + L.U, DV, 1.f, false);
+    __syncthreads();
+    // P^T = upper(D^T o K Q^T), Q row-major in b2
+    stage_rows<TIO>(b2, ldR, Q, ldk, C, DK, nvalid, nullptr);
+    __syncthreads();
+    mm<PRECISE>(C, C, DK, opnd<false>(b1, ldR), opnd<true>(b2, ldR), sG, kLdCC, 1.f, false);
+    __syncthreads();
+    for (int i = tid; i < C * C; i += nt) {      // sG[s][r] = P[r][s]
+        const int s2 = i / C, r = i % C;
+        sG[s2 * kLdCC + r] = s2 <= r ? __expf(sgam[r] - sgam[s2]) * sG[s2 * kLdCC + r] : 0.f;
+    }
+    for (int i = tid; i < C * DK; i += nt) {     // (Gam Q)^T over K (K is no longer needed)
+        const int r = i % C, j = i / C;
+        b1[j * kLdCC + r] = __expf(sgam[r]) * b2[r * ldR + j];
     }
     __syncthreads();
-    mm<PRECISE>(C, DV, C, opnd<false>(sT, kLdCC), opnd<false>(sX, ldX), rec + L.U, DV, 1.f, false);
+    stage_cols<TIO>(b2, kLdCC, dO, ldv, C, DV, nvalid, nullptr);   // dO^T
     __syncthreads();
-    // P = lower(D o Q K^T), then P^T dO
-    mm<PRECISE>(C, C, DK, opnd<false>(Q, sH * DK, nvalid), opnd<true>(sK, ldK), sG, kLdCC, 1.f,
-                false);
-    __syncthreads();
-    for (int i = tid; i < C * C; i += nt) {
-        const int r = i / C, s = i % C;
-        sG[r * kLdCC + s] = s <= r ? __expf(sgam[r] - sgam[s]) * sG[r * kLdCC + s] : 0.f;
-    }
-    __syncthreads();
-    mm<PRECISE>(C, DV, C, opnd<true>(sG, kLdCC), opnd<false>(dO, sH * DV, nvalid), rec + L.PdO, DV,
-                1.f, false);
+    // P^T dO and L = (Gam Q)^T dO
+    mm<PRECISE>(C, DV, C, opnd<false>(sG, kLdCC), opnd<true>(b2, kLdCC), rec + L.PdO, DV, 1.f, false);
+    mm<PRECISE>(DK, DV, C, opnd<false>(b1, kLdCC), opnd<true>(b2, kLdCC), rec + L.L, DV, 1.f, false);
     // vectors and T
     for (int i = tid; i < C; i += nt) {
         rec[L.gamma + i] = sgam[i];
@@ -296,118 +545,171 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdParams p) {
 }
 
 // ------------------------------------------------------------ carries
-// Forward: S0 of every chunk and W = U - Wk S0; S <- Gam_C S + Kt^T W.
+// CTA x < B*H runs the forward carry of head x, CTA B*H + x the reverse carry
+// of the same head; neither reads what the other writes.
+//   forward:  keep S0;  W = U - Wk S0;            S  <- Gam_C S  + Kt^T W
+//   reverse:  keep dS1; dW = Kt dS1 + P^T dO;     dS <- Gam_C dS + L - Wk^T dW
+// Shared memory holds every operand with k along its rows: the state and W
+// transposed (S^T, W^T), one of Wk / Kt row-major (X) and the other
+// transposed (Y^T), so that both products read 16-byte runs:
+//   W^T = -+ S^T X^T      S^T += +- W^T Y     (X, Y) = (Wk, Kt) forward, (Kt, Wk) reverse
 template <typename TIO, bool PRECISE>
-__global__ void __launch_bounds__(512) bwd_fwd_carry_kernel(BwdParams p) {
+__global__ void __launch_bounds__(512) bwd_carry_kernel(BwdParams p) {
     extern __shared__ __align__(16) float smf[];
-    const int bh = blockIdx.x, DK = p.DK, DV = p.DV;
-    const int ldS = DV + kPad, ldK = DK + kPad;
-    float* sS = smf;                 // DK x DV
-    float* sW = sS + DK * ldS;       // C x DV
-    float* sKt = sW + C * ldS;       // C x DK
+    const int heads = p.B * p.H;
+    const bool rev = (int)blockIdx.x >= heads;
+    const int bh = rev ? (int)blockIdx.x - heads : (int)blockIdx.x;
+    const int DK = p.DK, DV = p.DV;
+    const int ldS = DK + kPad;       // rows of S^T and X
+    float* sSt = smf;                // DV x DK: S^T (or dS^T)
+    float* sWt = sSt + DV * ldS;     // DV x C: W^T (or dW^T)
+    float* sX = sWt + DV * kLdCC;    // C x DK: Wk (forward) or Kt (reverse)
+    float* sYt = sX + C * ldS;       // DK x C: Kt^T (forward) or Wk^T (reverse)
+    float* veC = sYt + DK * kLdCC;   // exp(gamma_C - gamma_r)
     const int tid = threadIdx.x, nt = blockDim.x;
     const RecLayout L(DK, DV);
     const size_t SS = (size_t)DK * DV, WS = (size_t)C * DV;
-    for (int i = tid; i < DK * DV; i += nt)
-        sS[(i / DV) * ldS + i % DV] = p.h0 ? p.h0[(size_t)bh * SS + i] : 0.f;
-    for (int c = 0; c < p.nchunks; ++c) {
-        const int nvalid = chunk_valid(p, c);
-        const float* rec = p.rec + ((size_t)bh * p.nchunks + c) * L.floats;
-        const TIO* K = static_cast<const TIO*>(p.k) + tok_index(p, bh, c, 0) * DK;
-        const float gC = rec[L.gamma + C - 1];
-        __syncthreads();
-        float* st = p.states + ((size_t)bh * p.nchunks + c) * SS;
-        for (int i = tid; i < DK * DV; i += nt) st[i] = sS[(i / DV) * ldS + i % DV];
-        for (int i = tid; i < C * DK; i += nt) {
-            const int r = i / DK, j = i % DK;
-            sKt[r * ldK + j] =
-                r < nvalid ? __expf(gC - rec[L.gamma + r]) * ldf<TIO>(K + (size_t)r * p.H * DK + j) : 0.f;
-        }
-        // W = U - Wk S0
-        mm<PRECISE>(C, DV, DK, opnd<false>(rec + L.Wk, DK), opnd<false>(sS, ldS), sW, ldS, -1.f, false);
-        __syncthreads();
-        float* wout = p.wbuf + ((size_t)bh * p.nchunks + c) * WS;
-        for (int i = tid; i < C * DV; i += nt) {
-            const int r = i / DV, j = i % DV;
-            const float w = sW[r * ldS + j] + rec[L.U + i];
-            sW[r * ldS + j] = w;
-            wout[i] = w;
-        }
-        const float GC = __expf(gC);
-        for (int i = tid; i < DK * DV; i += nt) sS[(i / DV) * ldS + i % DV] *= GC;
-        __syncthreads();
-        mm<PRECISE>(DK, DV, C, opnd<true>(sKt, ldK), opnd<false>(sW, ldS), sS, ldS, 1.f, true);
+    const float* init = rev ? p.dhT : p.h0;
+    for (int i = tid; i < DK * DV; i += nt) {
+        const int a = i % DK, b = i / DK;          // S[a][b] into S^T[b][a]
+        sSt[b * ldS + a] = init ? init[(size_t)bh * SS + (size_t)a * DV + b] : 0.f;
     }
-}
-
-// Reverse: dS1 of every chunk and dW = Kt dS1 + P^T dO;
-// dS <- Gam_C dS + (diag(Gam) Q)^T dO - Wk^T dW.
-template <typename TIO, bool PRECISE>
-__global__ void __launch_bounds__(512) bwd_rev_carry_kernel(BwdParams p) {
-    extern __shared__ __align__(16) float smf[];
-    const int bh = blockIdx.x, DK = p.DK, DV = p.DV;
-    const int ldS = DV + kPad, ldK = DK + kPad;
-    float* sD = smf;                 // DK x DV
-    float* sW = sD + DK * ldS;       // C x DV
-    float* sKt = sW + C * ldS;       // C x DK
-    float* sQg = sKt + C * ldK;      // C x DK
-    const int tid = threadIdx.x, nt = blockDim.x;
-    const RecLayout L(DK, DV);
-    const size_t SS = (size_t)DK * DV, WS = (size_t)C * DV;
-    for (int i = tid; i < DK * DV; i += nt)
-        sD[(i / DV) * ldS + i % DV] = p.dhT ? p.dhT[(size_t)bh * SS + i] : 0.f;
-    for (int c = p.nchunks - 1; c >= 0; --c) {
+    float* keep_s = rev ? p.dstates : p.states;
+    float* keep_w = rev ? p.dwbuf : p.wbuf;
+    constexpr int VW = Vec<TIO>::W;
+    for (int it = 0; it < p.nchunks; ++it) {
+        const int c = rev ? p.nchunks - 1 - it : it;
         const int nvalid = chunk_valid(p, c);
-        const float* rec = p.rec + ((size_t)bh * p.nchunks + c) * L.floats;
-        const size_t t0 = tok_index(p, bh, c, 0);
-        const TIO* K = static_cast<const TIO*>(p.k) + t0 * DK;
-        const TIO* Q = static_cast<const TIO*>(p.q) + t0 * DK;
-        const TIO* dO = static_cast<const TIO*>(p.dout) + t0 * DV;
-        const float gC = rec[L.gamma + C - 1];
+        const size_t item = (size_t)bh * p.nchunks + c;
+        const float* rec = p.rec + item * L.floats;
+        const TIO* K = static_cast<const TIO*>(p.k) + tok_index(p, bh, c, 0) * DK;
+        const size_t ldk = (size_t)p.H * DK;
+        const float gC = __ldg(rec + L.gamma + C - 1);
         __syncthreads();
-        float* dst = p.dstates + ((size_t)bh * p.nchunks + c) * SS;
-        for (int i = tid; i < DK * DV; i += nt) dst[i] = sD[(i / DV) * ldS + i % DV];
-        for (int i = tid; i < C * DK; i += nt) {
-            const int r = i / DK, j = i % DK;
-            const bool ok = r < nvalid;
-            const float gr = rec[L.gamma + r];
-            sKt[r * ldK + j] = ok ? __expf(gC - gr) * ldf<TIO>(K + (size_t)r * p.H * DK + j) : 0.f;
-            sQg[r * ldK + j] = ok ? __expf(gr) * ldf<TIO>(Q + (size_t)r * p.H * DK + j) : 0.f;
+        if (tid < C) veC[tid] = __expf(gC - __ldg(rec + L.gamma + tid));
+        // keep the state as [DK][DV]: four columns of one row per thread, lanes
+        // along the rows (conflict-free reads of S^T)
+        float* st = keep_s + item * SS;
+        for (int i = tid; i < DK * DV / 4; i += nt) {
+            const int a = i % DK, b = (i / DK) * 4;
+            *reinterpret_cast<float4*>(st + (size_t)a * DV + b) =
+                make_float4(sSt[b * ldS + a], sSt[(b + 1) * ldS + a], sSt[(b + 2) * ldS + a],
+                            sSt[(b + 3) * ldS + a]);
+        }
+        // Wk into X (forward) or Y^T (reverse; lanes along the chunk rows)
+        if (!rev) {
+            for_f4(rec + L.Wk, C * DK, [&](int i, const float* x) {
+                const int r = (4 * i) / DK, j = (4 * i) % DK;
+                *reinterpret_cast<float4*>(sX + r * ldS + j) = make_float4(x[0], x[1], x[2], x[3]);
+            });
+        } else {
+            const float4* wk4 = reinterpret_cast<const float4*>(rec + L.Wk);
+            for (int i = tid; i < C * DK / 4; i += nt) {
+                const int r = i % C, j = (i / C) * 4;
+                const float4 x = __ldg(wk4 + (r * DK + j) / 4);
+                sYt[j * kLdCC + r] = x.x;
+                sYt[(j + 1) * kLdCC + r] = x.y;
+                sYt[(j + 2) * kLdCC + r] = x.z;
+                sYt[(j + 3) * kLdCC + r] = x.w;
+            }
         }
         __syncthreads();
-        // dW = Kt dS1 + P^T dO
-        mm<PRECISE>(C, DV, DK, opnd<false>(sKt, ldK), opnd<false>(sD, ldS), sW, ldS, 1.f, false);
-        __syncthreads();
-        float* wout = p.dwbuf + ((size_t)bh * p.nchunks + c) * WS;
-        for (int i = tid; i < C * DV; i += nt) {
-            const int r = i / DV, j = i % DV;
-            const float w = sW[r * ldS + j] + rec[L.PdO + i];
-            sW[r * ldS + j] = w;
-            wout[i] = w;
+        // Kt into X (reverse, row-major) or Y^T (forward; lanes along the chunk rows)
+        if (rev) {
+            stage_rows<TIO>(sX, ldS, K, ldk, C, DK, nvalid, veC);
+        } else {
+            for (int i = tid; i < C * DK / VW; i += nt) {
+                const int r = i % C, j = (i / C) * VW;
+                float x[VW];
+                if (r < nvalid) {
+                    Vec<TIO>::unpack(__ldg(reinterpret_cast<const uint4*>(K + (size_t)r * ldk + j)), x);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < VW; ++u) x[u] = 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < VW; ++u) sYt[(j + u) * kLdCC + r] = veC[r] * x[u];
+            }
         }
-        const float GC = __expf(gC);
-        for (int i = tid; i < DK * DV; i += nt) sD[(i / DV) * ldS + i % DV] *= GC;
         __syncthreads();
-        mm<PRECISE>(DK, DV, C, opnd<true>(sQg, ldK), opnd<false>(dO, p.H * DV, nvalid), sD, ldS, 1.f,
-                    true);
+        // W^T = -S^T Wk^T (forward) or dW^T = dS^T Kt^T (reverse)
+        mm<PRECISE>(DV, C, DK, opnd<false>(sSt, ldS), opnd<true>(sX, ldS), sWt, kLdCC,
+                    rev ? 1.f : -1.f, false);
         __syncthreads();
-        mm<PRECISE>(DK, DV, C, opnd<true>(rec + L.Wk, DK), opnd<false>(sW, ldS), sD, ldS, -1.f, true);
+        // + U (forward) or + P^T dO (reverse); keep W (or dW) as [C][DV]
+        {
+            const float* add = rec + (rev ? L.PdO : L.U);
+            float* wout = keep_w + item * WS;
+            batched4(
+                C * DV / 4,
+                [&](int i) {
+                    const int r = i % C, j = (i / C) * 4;
+                    return __ldg(reinterpret_cast<const float4*>(add + r * DV + j));
+                },
+                [&](int i, float4 x) {
+                    const int r = i % C, j = (i / C) * 4;
+                    float4 w;
+                    w.x = sWt[j * kLdCC + r] + x.x;
+                    w.y = sWt[(j + 1) * kLdCC + r] + x.y;
+                    w.z = sWt[(j + 2) * kLdCC + r] + x.z;
+                    w.w = sWt[(j + 3) * kLdCC + r] + x.w;
+                    sWt[j * kLdCC + r] = w.x;
+                    sWt[(j + 1) * kLdCC + r] = w.y;
+                    sWt[(j + 2) * kLdCC + r] = w.z;
+                    sWt[(j + 3) * kLdCC + r] = w.w;
+                    *reinterpret_cast<float4*>(wout + r * DV + j) = w;
+                });
+        }
+        // S^T <- Gam_C S^T (+ L^T in reverse)
+        {
+            const float GC = __expf(gC);
+            const float* Lc = rec + L.L;
+            if (rev) {
+                batched4(
+                    DK * DV / 4,
+                    [&](int i) {
+                        const int a = i % DK, b = (i / DK) * 4;
+                        return __ldg(reinterpret_cast<const float4*>(Lc + (size_t)a * DV + b));
+                    },
+                    [&](int i, float4 x) {
+                        const int a = i % DK, b = (i / DK) * 4;
+                        float* y = sSt + b * ldS + a;
+                        y[0] = GC * y[0] + x.x;
+                        y[ldS] = GC * y[ldS] + x.y;
+                        y[2 * ldS] = GC * y[2 * ldS] + x.z;
+                        y[3 * ldS] = GC * y[3 * ldS] + x.w;
+                    });
+            } else {
+                for (int i = tid; i < DK * DV; i += nt) {
+                    const int a = i % DK, b = i / DK;
+                    sSt[b * ldS + a] *= GC;
+                }
+            }
+        }
+        __syncthreads();
+        // S^T += W^T Kt (forward) or dS^T -= dW^T Wk (reverse)
+        mm<PRECISE>(DV, DK, C, opnd<false>(sWt, kLdCC), opnd<true>(sYt, kLdCC), sSt, ldS,
+                    rev ? -1.f : 1.f, true);
     }
     __syncthreads();
-    if (p.dh0)
-        for (int i = tid; i < DK * DV; i += nt) p.dh0[(size_t)bh * SS + i] = sD[(i / DV) * ldS + i % DV];
+    if (rev && p.dh0)
+        for (int i = tid; i < DK * DV; i += nt) {
+            const int a = i % DK, b = i / DK;
+            p.dh0[(size_t)bh * SS + (size_t)a * DV + b] = sSt[b * ldS + a];
+        }
 }
 
 // ------------------------------------------------------------ gradients
-__device__ __forceinline__ float warp_sum(float s) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    return s;
-}
+
+// Shared memory of the gradient kernel (floats, in order): dX, E, dQ, dK
+// (C x pad rows each), two C x C tiles, the row vectors, then (bf16 I/O only)
+// K, Q and dO as bf16 rows of kLdB elements.
+constexpr int kLdB = 128 + 8;
 
 template <typename TIO, bool PRECISE>
-__global__ void __launch_bounds__(256) bwd_grad_kernel(BwdParams p) {
+__global__ void __launch_bounds__(512) bwd_grad_kernel(BwdParams p) {
     extern __shared__ __align__(16) float smf[];
+    constexpr bool STAGE = sizeof(TIO) == 2;   // inputs kept in shared memory (bf16 I/O)
     const int c = blockIdx.x, bh = blockIdx.y;
     const int DK = p.DK, DV = p.DV, DM = DK > DV ? DK : DV;
     const int ldV = DV + kPad, ldK = DK + kPad, ldM = DM + kPad;
@@ -415,17 +717,19 @@ __global__ void __launch_bounds__(256) bwd_grad_kernel(BwdParams p) {
     float* sE = sDX + C * ldV;         // C x max(DK, DV)
     float* sDQ = sE + C * ldM;         // C x DK
     float* sDK = sDQ + C * ldK;        // C x DK
-    float* sG = sDK + C * ldK;         // C x C: At
-    float* sG2 = sG + C * kLdCC;       // C x C: dP
-    float* sP = sG2 + C * kLdCC;       // C x C: P, then dA
-    float* vgam = sP + C * kLdCC;
+    float* sA = sDK + C * ldK;         // C x C
+    float* sB = sA + C * kLdCC;        // C x C
+    float* vgam = sB + C * kLdCC;
     float* vGam = vgam + C;
     float* vbeta = vGam + C;
     float* veC = vbeta + C;
     float* vdb = veC + C;              // dbeta
     float* vdg = vdb + C;              // dgamma
     float* vrs = vdg + C;              // row scales
-    float* vred = vrs + C;             // [0] dgamma_C, [1..8] block reduction
+    float* vred = vrs + C;             // [0] dgamma_C, [1 + warp] block reduction
+    TIO* sKb = reinterpret_cast<TIO*>(vred + 32);
+    TIO* sQb = sKb + C * kLdB;
+    TIO* sOb = sQb + C * kLdB;
     const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
     const int nvalid = chunk_valid(p, c);
     const RecLayout L(DK, DV);
@@ -437,17 +741,28 @@ __global__ void __launch_bounds__(256) bwd_grad_kernel(BwdParams p) {
     const float* dW = p.dwbuf + item * C * DV;
     const size_t t0 = tok_index(p, bh, c, 0);
     const int sK_ = p.H * DK, sV_ = p.H * DV;
-    const TIO* Q = static_cast<const TIO*>(p.q) + t0 * DK;
-    const TIO* K = static_cast<const TIO*>(p.k) + t0 * DK;
-    const TIO* V = static_cast<const TIO*>(p.v) + t0 * DV;
-    const TIO* dO = static_cast<const TIO*>(p.dout) + t0 * DV;
-    const float gC = rec[L.gamma + C - 1];
+    const TIO* Qg = static_cast<const TIO*>(p.q) + t0 * DK;
+    const TIO* Kg = static_cast<const TIO*>(p.k) + t0 * DK;
+    const TIO* Vg = static_cast<const TIO*>(p.v) + t0 * DV;
+    const TIO* Og = static_cast<const TIO*>(p.dout) + t0 * DV;
+    // the operands K, Q, dO: shared-memory rows (zero past nvalid) or global rows
+    const TIO* Kp = STAGE ? sKb : Kg;
+    const TIO* Qp = STAGE ? sQb : Qg;
+    const TIO* Op = STAGE ? sOb : Og;
+    const int ldKp = STAGE ? kLdB : sK_, ldOp = STAGE ? kLdB : sV_;
+    const int rowsp = STAGE ? C : nvalid;
+    const float gC = __ldg(rec + L.gamma + C - 1);
 
+    if (STAGE) {
+        copy_rows<TIO>(sKb, kLdB, Kg, sK_, C, DK, nvalid);
+        copy_rows<TIO>(sQb, kLdB, Qg, sK_, C, DK, nvalid);
+        copy_rows<TIO>(sOb, kLdB, Og, sV_, C, DV, nvalid);
+    }
     for (int r = tid; r < C; r += nt) {
-        const float gr = rec[L.gamma + r];
+        const float gr = __ldg(rec + L.gamma + r);
         vgam[r] = gr;
         vGam[r] = __expf(gr);
-        vbeta[r] = rec[L.beta + r];
+        vbeta[r] = __ldg(rec + L.beta + r);
         veC[r] = __expf(gC - gr);
         vdb[r] = 0.f;
         vdg[r] = 0.f;
@@ -455,27 +770,36 @@ __global__ void __launch_bounds__(256) bwd_grad_kernel(BwdParams p) {
     if (tid == 0) vred[0] = 0.f;
     __syncthreads();
 
-    // dX = T^T dW; dv = diag(beta) dX
+    // dX = T^T dW;  K S0 (into E);  G = K K^T (into A)
     mm<PRECISE>(C, DV, C, opnd<true>(rec + L.T, C), opnd<false>(dW, DV), sDX, ldV, 1.f, false);
-    // e = V - diag(Gam) K S0 - At W:  K S0 first
-    mm<PRECISE>(C, DV, DK, opnd<false>(K, sK_, nvalid), opnd<false>(S0, DV), sE, ldM, 1.f, false);
-    // G = K K^T
-    mm<PRECISE>(C, C, DK, opnd<false>(K, sK_, nvalid), opnd<true>(K, sK_, nvalid), sG, kLdCC, 1.f,
+    mm<PRECISE>(C, DV, DK, opnd<false>(Kp, ldKp, rowsp), opnd<false>(S0, DV), sE, ldM, 1.f, false);
+    mm<PRECISE>(C, C, DK, opnd<false>(Kp, ldKp, rowsp), opnd<true>(Kp, ldKp, rowsp), sA, kLdCC, 1.f,
                 false);
     __syncthreads();
-    TIO* gv = static_cast<TIO*>(p.dv) + t0 * DV;
-    for (int i = tid; i < C * DV; i += nt) {
-        const int r = i / DV, j = i % DV;
-        if (r < nvalid) stf<TIO>(gv + (size_t)r * sV_ + j, vbeta[r] * sDX[r * ldV + j]);
-        const float vv = r < nvalid ? ldf<TIO>(V + (size_t)r * sV_ + j) : 0.f;
-        sE[r * ldM + j] = vv - vGam[r] * sE[r * ldM + j];
+    // dv = diag(beta) dX;  E = V - diag(Gam) K S0;  A = At = strict_lower(D o G)
+    {
+        TIO* gv = static_cast<TIO*>(p.dv) + t0 * DV;
+        constexpr int VW = Vec<TIO>::W;
+        for (int i = tid; i < C * DV / VW; i += nt) {
+            const int r = (i * VW) / DV, j = (i * VW) % DV;
+            if (r >= nvalid) continue;
+            float x[VW];
+#pragma unroll
+            for (int u = 0; u < VW; ++u) x[u] = vbeta[r] * sDX[r * ldV + j + u];
+            *reinterpret_cast<uint4*>(gv + (size_t)r * sV_ + j) = Vec<TIO>::pack(x);
+        }
+        for_rows<TIO>(Vg, sV_, C, DV, nvalid, [&](int r, int j, const float* x) {
+#pragma unroll
+            for (int u = 0; u < VW; ++u) sE[r * ldM + j + u] = x[u] - vGam[r] * sE[r * ldM + j + u];
+        });
     }
     for (int i = tid; i < C * C; i += nt) {
         const int r = i / C, s = i % C;
-        sG[r * kLdCC + s] = s < r ? __expf(vgam[r] - vgam[s]) * sG[r * kLdCC + s] : 0.f;
+        sA[r * kLdCC + s] = s < r ? __expf(vgam[r] - vgam[s]) * sA[r * kLdCC + s] : 0.f;
     }
     __syncthreads();
-    mm<PRECISE>(C, DV, C, opnd<false>(sG, kLdCC), opnd<false>(W, DV), sE, ldM, -1.f, true);
+    // E -= At W: the residuals e
+    mm<PRECISE>(C, DV, C, opnd<false>(sA, kLdCC), opnd<false>(W, DV), sE, ldM, -1.f, true);
     __syncthreads();
     // dbeta_r = dX_r . e_r
     for (int r = warp; r < C; r += nw) {
@@ -484,32 +808,36 @@ __global__ void __launch_bounds__(256) bwd_grad_kernel(BwdParams p) {
         s = warp_sum(s);
         if (lane == 0) vdb[r] = s;
     }
-    // dq = diag(Gam) dO S0^T;  row scale for the Y term of dk: -Gam beta
+    // dq = diag(Gam) dO S0^T;  row scale of the Y term of dk: -Gam beta
     for (int r = tid; r < C; r += nt) vrs[r] = -vGam[r] * vbeta[r];
-    mm<PRECISE>(C, DK, DV, opnd<false>(dO, sV_, nvalid), opnd<true>(S0, DV), sDQ, ldK, 1.f, false,
-                vGam);
+    mm<PRECISE>(C, DK, DV, opnd<false>(Op, ldOp, rowsp), opnd<true>(S0, DV), sDQ, ldK, 1.f, false, vGam);
     __syncthreads();
-    // dk (Y term) = -diag(Gam beta) dX S0^T;  Kt term into sE: diag(eC) W dS1^T
+    // dk (Y term) = -diag(Gam beta) dX S0^T;  Kt term into E: diag(eC) W dS1^T
     mm<PRECISE>(C, DK, DV, opnd<false>(sDX, ldV), opnd<true>(S0, DV), sDK, ldK, 1.f, false, vrs);
     mm<PRECISE>(C, DK, DV, opnd<false>(W, DV), opnd<true>(dS1, DV), sE, ldM, 1.f, false, veC);
-    // dP = lower(dO W^T);  P = lower(D o Q K^T)
-    mm<PRECISE>(C, C, DV, opnd<false>(dO, sV_, nvalid), opnd<true>(W, DV), sG2, kLdCC, 1.f, false);
-    mm<PRECISE>(C, C, DK, opnd<false>(Q, sK_, nvalid), opnd<true>(K, sK_, nvalid), sP, kLdCC, 1.f,
+    // dP = dO W^T (into A);  P = Q K^T (into B)
+    mm<PRECISE>(C, C, DV, opnd<false>(Op, ldOp, rowsp), opnd<true>(W, DV), sA, kLdCC, 1.f, false);
+    mm<PRECISE>(C, C, DK, opnd<false>(Qp, ldKp, rowsp), opnd<true>(Kp, ldKp, rowsp), sB, kLdCC, 1.f,
                 false);
-    // Gam_C <dS1, S0>, block reduction
+    // <dS1, S0>, block reduction
     {
         float s = 0.f;
-        for (int i = tid; i < DK * DV; i += nt) s += dS1[i] * S0[i];
+        const float4* a4 = reinterpret_cast<const float4*>(dS1);
+        const float4* b4 = reinterpret_cast<const float4*>(S0);
+        for (int i = tid; i < DK * DV / 4; i += nt) {
+            const float4 a = __ldg(a4 + i), b = __ldg(b4 + i);
+            s += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+        }
         s = warp_sum(s);
         if (lane == 0) vred[1 + warp] = s;
     }
     __syncthreads();
-    // dgamma from the O term (q . dq_a), the Y term (k . dk_y) and the Kt term (z)
+    // dgamma from the O term (q . dq), the Y term (k . dk_y) and the Kt term (z)
     for (int r = warp; r < C; r += nw) {
         float a = 0.f, b = 0.f, z = 0.f;
         if (r < nvalid) {
             for (int j = lane; j < DK; j += 32) {
-                const float qv = ldf<TIO>(Q + (size_t)r * sK_ + j), kv = ldf<TIO>(K + (size_t)r * sK_ + j);
+                const float qv = ldf<TIO>(Qp + (size_t)r * ldKp + j), kv = ldf<TIO>(Kp + (size_t)r * ldKp + j);
                 a += qv * sDQ[r * ldK + j];
                 b += kv * sDK[r * ldK + j];
                 z += kv * sE[r * ldM + j];
@@ -535,37 +863,43 @@ __global__ void __launch_bounds__(256) bwd_grad_kernel(BwdParams p) {
     }
     for (int i = tid; i < C * C; i += nt) {
         const int r = i / C, s = i % C;
-        const float d = __expf(vgam[r] - vgam[s]);
-        sP[r * kLdCC + s] = s <= r ? d * sP[r * kLdCC + s] : 0.f;
-        sG2[r * kLdCC + s] = s <= r ? sG2[r * kLdCC + s] : 0.f;
+        const bool low = s <= r;
+        sA[r * kLdCC + s] = low ? sA[r * kLdCC + s] : 0.f;
+        sB[r * kLdCC + s] = low ? __expf(vgam[r] - vgam[s]) * sB[r * kLdCC + s] : 0.f;
     }
     __syncthreads();
-    // dgamma from P: +row sums, -column sums of dP o P
+    // dgamma from P: + row sums, - column sums of dP o P
     for (int i = tid; i < 2 * C; i += nt) {
         const int x = i % C;
         float s = 0.f;
         if (i < C) {
-            for (int y = 0; y <= x; ++y) s += sG2[x * kLdCC + y] * sP[x * kLdCC + y];
+            for (int y = 0; y <= x; ++y) s += sA[x * kLdCC + y] * sB[x * kLdCC + y];
             atomicAdd(&vdg[x], s);
         } else {
-            for (int y = x; y < C; ++y) s += sG2[y * kLdCC + x] * sP[y * kLdCC + x];
+            for (int y = x; y < C; ++y) s += sA[y * kLdCC + x] * sB[y * kLdCC + x];
             atomicAdd(&vdg[x], -s);
         }
     }
     __syncthreads();
-    // dP o D
+    // dP o D;  dq += (dP o D) K;  dk += (dP o D)^T Q
     for (int i = tid; i < C * C; i += nt) {
         const int r = i / C, s = i % C;
-        if (s <= r) sG2[r * kLdCC + s] *= __expf(vgam[r] - vgam[s]);
+        if (s <= r) sA[r * kLdCC + s] *= __expf(vgam[r] - vgam[s]);
     }
-    // dA = -strict_lower(dX W^T) (into sP)
-    mm<PRECISE>(C, C, DV, opnd<false>(sDX, ldV), opnd<true>(W, DV), sP, kLdCC, -1.f, false);
     __syncthreads();
-    mm<PRECISE>(C, DK, C, opnd<false>(sG2, kLdCC), opnd<false>(K, sK_, nvalid), sDQ, ldK, 1.f, true);
-    mm<PRECISE>(C, DK, C, opnd<true>(sG2, kLdCC), opnd<false>(Q, sK_, nvalid), sDK, ldK, 1.f, true);
+    mm<PRECISE>(C, DK, C, opnd<false>(sA, kLdCC), opnd<false>(Kp, ldKp, rowsp), sDQ, ldK, 1.f, true);
+    mm<PRECISE>(C, DK, C, opnd<true>(sA, kLdCC), opnd<false>(Qp, ldKp, rowsp), sDK, ldK, 1.f, true);
+    // dA = -strict_lower(dX W^T) (into B, P is done);  G again (into A, once dP is done)
+    mm<PRECISE>(C, C, DV, opnd<false>(sDX, ldV), opnd<true>(W, DV), sB, kLdCC, -1.f, false);
+    __syncthreads();
+    mm<PRECISE>(C, C, DK, opnd<false>(Kp, ldKp, rowsp), opnd<true>(Kp, ldKp, rowsp), sA, kLdCC, 1.f,
+                false);
+    __syncthreads();
     for (int i = tid; i < C * C; i += nt) {
         const int r = i / C, s = i % C;
-        sP[r * kLdCC + s] = s < r ? sP[r * kLdCC + s] : 0.f;
+        const bool st = s < r;
+        sB[r * kLdCC + s] = st ? sB[r * kLdCC + s] : 0.f;
+        sA[r * kLdCC + s] = st ? __expf(vgam[r] - vgam[s]) * sA[r * kLdCC + s] : 0.f;
     }
     __syncthreads();
     // dgamma from A (A_rs = beta_r At_rs): u = dA o A
@@ -573,23 +907,22 @@ __global__ void __launch_bounds__(256) bwd_grad_kernel(BwdParams p) {
         const int x = i % C;
         float s = 0.f;
         if (i < C) {
-            for (int y = 0; y < x; ++y) s += sP[x * kLdCC + y] * sG[x * kLdCC + y];
+            for (int y = 0; y < x; ++y) s += sB[x * kLdCC + y] * sA[x * kLdCC + y];
             atomicAdd(&vdg[x], vbeta[x] * s);
         } else {
-            for (int y = x + 1; y < C; ++y) s += vbeta[y] * sP[y * kLdCC + x] * sG[y * kLdCC + x];
+            for (int y = x + 1; y < C; ++y) s += vbeta[y] * sB[y * kLdCC + x] * sA[y * kLdCC + x];
             atomicAdd(&vdg[x], -s);
         }
     }
     __syncthreads();
-    // F = diag(beta) (dA o D); dk += F K + F^T K
+    // F = diag(beta) (dA o D);  dk += F K + F^T K
     for (int i = tid; i < C * C; i += nt) {
         const int r = i / C, s = i % C;
-        if (s < r) sP[r * kLdCC + s] *= vbeta[r] * __expf(vgam[r] - vgam[s]);
+        if (s < r) sB[r * kLdCC + s] *= vbeta[r] * __expf(vgam[r] - vgam[s]);
     }
     __syncthreads();
-    mm<PRECISE>(C, DK, C, opnd<false>(sP, kLdCC), opnd<false>(K, sK_, nvalid), sDK, ldK, 1.f, true);
-    __syncthreads();
-    mm<PRECISE>(C, DK, C, opnd<true>(sP, kLdCC), opnd<false>(K, sK_, nvalid), sDK, ldK, 1.f, true);
+    mm<PRECISE>(C, DK, C, opnd<false>(sB, kLdCC), opnd<false>(Kp, ldKp, rowsp), sDK, ldK, 1.f, true);
+    mm<PRECISE>(C, DK, C, opnd<true>(sB, kLdCC), opnd<false>(Kp, ldKp, rowsp), sDK, ldK, 1.f, true);
     __syncthreads();
     // step-size chain, dg = reverse cumulative sum of dgamma, outputs
     if (tid == 0) {
@@ -601,64 +934,67 @@ __global__ void __launch_bounds__(256) bwd_grad_kernel(BwdParams p) {
         }
     }
     for (int r = tid; r < C; r += nt) {
-        const float kk = rec[L.kk + r];
-        const float den = kk + p.eps;
+        const float den = __ldg(rec + L.kk + r) + p.eps;
         // coefficient of k_r in dk_r from beta = eta / (||k||^2 + eps)
         vrs[r] = p.beta_direct ? 0.f : -2.f * vbeta[r] * vdb[r] / den;
         if (r < nvalid) p.deta[t0 + (size_t)r * p.H] = p.beta_direct ? vdb[r] : vdb[r] / den;
     }
     __syncthreads();
-    TIO* gq = static_cast<TIO*>(p.dq) + t0 * DK;
-    TIO* gk = static_cast<TIO*>(p.dk) + t0 * DK;
-    for (int i = tid; i < C * DK; i += nt) {
-        const int r = i / DK, j = i % DK;
-        if (r >= nvalid) continue;
-        stf<TIO>(gq + (size_t)r * sK_ + j, sDQ[r * ldK + j]);
-        const float kv = ldf<TIO>(K + (size_t)r * sK_ + j);
-        stf<TIO>(gk + (size_t)r * sK_ + j, sDK[r * ldK + j] + vrs[r] * kv);
+    {
+        TIO* gq = static_cast<TIO*>(p.dq) + t0 * DK;
+        TIO* gk = static_cast<TIO*>(p.dk) + t0 * DK;
+        constexpr int VW = Vec<TIO>::W;
+        for (int i = tid; i < C * DK / VW; i += nt) {
+            const int r = (i * VW) / DK, j = (i * VW) % DK;
+            if (r >= nvalid) continue;
+            float xq[VW], xk[VW], kv[VW];
+            Vec<TIO>::unpack(*reinterpret_cast<const uint4*>(Kp + (size_t)r * ldKp + j), kv);
+#pragma unroll
+            for (int u = 0; u < VW; ++u) {
+                xq[u] = sDQ[r * ldK + j + u];
+                xk[u] = sDK[r * ldK + j + u] + vrs[r] * kv[u];
+            }
+            *reinterpret_cast<uint4*>(gq + (size_t)r * sK_ + j) = Vec<TIO>::pack(xq);
+            *reinterpret_cast<uint4*>(gk + (size_t)r * sK_ + j) = Vec<TIO>::pack(xk);
+        }
     }
     for (int r = tid; r < nvalid; r += nt) p.dg[t0 + (size_t)r * p.H] = vdg[r];
 }
 
 size_t prep_smem(int DK, int DV) {
     const int DM = DK > DV ? DK : DV;
-    return sizeof(float) * ((size_t)C * (DK + kPad) + (size_t)C * (DM + kPad) + 2 * (size_t)C * kLdCC + 4 * C);
+    const size_t big = std::max((size_t)DM * kLdCC, (size_t)C * (DM + kPad));
+    return sizeof(float) * (2 * big + 2 * (size_t)C * kLdCC + 4 * C);
 }
-size_t fwd_carry_smem(int DK, int DV) {
-    return sizeof(float) * ((size_t)DK * (DV + kPad) + (size_t)C * (DV + kPad) + (size_t)C * (DK + kPad));
+size_t carry_smem(int DK, int DV) {
+    return sizeof(float) * ((size_t)DV * (DK + kPad) + (size_t)DV * kLdCC + (size_t)C * (DK + kPad) +
+                            (size_t)DK * kLdCC + C);
 }
-size_t rev_carry_smem(int DK, int DV) {
-    return fwd_carry_smem(DK, DV) + sizeof(float) * (size_t)C * (DK + kPad);
-}
-size_t grad_smem(int DK, int DV) {
+size_t grad_smem(int DK, int DV, bool bf16) {
     const int DM = DK > DV ? DK : DV;
-    return sizeof(float) * ((size_t)C * (DV + kPad) + (size_t)C * (DM + kPad) + 2 * (size_t)C * (DK + kPad) +
-                            3 * (size_t)C * kLdCC + 8 * C + 16);
+    const size_t f = (size_t)C * (DV + kPad) + (size_t)C * (DM + kPad) + 2 * (size_t)C * (DK + kPad) +
+                     2 * (size_t)C * kLdCC + 7 * C + 32;
+    return sizeof(float) * f + (bf16 ? 3 * sizeof(__nv_bfloat16) * (size_t)C * kLdB : 0);
 }
 
 template <typename TIO, bool PRECISE>
 cudaError_t launch_all(const BwdParams& p, cudaStream_t st) {
-    const size_t s_prep = prep_smem(p.DK, p.DV), s_fwd = fwd_carry_smem(p.DK, p.DV);
-    const size_t s_rev = rev_carry_smem(p.DK, p.DV), s_grad = grad_smem(p.DK, p.DV);
+    const size_t s_prep = prep_smem(p.DK, p.DV), s_carry = carry_smem(p.DK, p.DV);
+    const size_t s_grad = grad_smem(p.DK, p.DV, sizeof(TIO) == 2);
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(bwd_prep_kernel<TIO, PRECISE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)s_prep)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(bwd_fwd_carry_kernel<TIO, PRECISE>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_fwd)) != cudaSuccess)
-        return e;
-    if ((e = cudaFuncSetAttribute(bwd_rev_carry_kernel<TIO, PRECISE>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_rev)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(bwd_carry_kernel<TIO, PRECISE>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_carry)) != cudaSuccess)
         return e;
     if ((e = cudaFuncSetAttribute(bwd_grad_kernel<TIO, PRECISE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)s_grad)) != cudaSuccess) return e;
     const dim3 items(p.nchunks, p.B * p.H);
     bwd_prep_kernel<TIO, PRECISE><<<items, 256, s_prep, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_fwd_carry_kernel<TIO, PRECISE><<<p.B * p.H, 512, s_fwd, st>>>(p);
+    bwd_carry_kernel<TIO, PRECISE><<<2 * p.B * p.H, 512, s_carry, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_rev_carry_kernel<TIO, PRECISE><<<p.B * p.H, 512, s_rev, st>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_grad_kernel<TIO, PRECISE><<<items, 256, s_grad, st>>>(p);
+    bwd_grad_kernel<TIO, PRECISE><<<items, 512, s_grad, st>>>(p);
     return cudaGetLastError();
 }
 

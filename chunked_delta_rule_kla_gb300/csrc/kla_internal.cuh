@@ -90,8 +90,8 @@ int chunk_ranges(int B, int H, int nchunks, int nseg);
 int chunk_range_bounds(int nchunks, int* bounds);
 int chunk_fwd_tc_auto_segments(int B, int T, int H, int dk, int dv);
 
-// Chunkwise backward (kla_bwd.cu): four launches on `stream` (per-chunk prep,
-// forward state carry, reverse gradient carry, per-chunk gradients).  bf16
+// Chunkwise backward (kla_bwd.cu): three launches on `stream` (per-chunk prep,
+// the forward and reverse carries in one grid, per-chunk gradients).  bf16
 // I/O uses tf32 products; fp32 I/O uses a three-term tf32 split.  `scratch`
 // holds chunk_bwd_workspace_floats floats.
 size_t chunk_bwd_workspace_floats(int B, int T, int H, int dk, int dv);

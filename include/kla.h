@@ -197,7 +197,7 @@ KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
  * each product is split into three tf32 products (fp32-level accuracy).
  * The workspace (kla_chunk_bwd_workspace_bytes, 256-byte aligned, caller
  * owned) holds per-chunk records, every chunk's start state and state
- * gradient: about 312 KB per (batch, head, chunk) at dk = dv = 128.  Errors
+ * gradient: about 373 KB per (batch, head, chunk) at dk = dv = 128.  Errors
  * are those of kla_chunk_fwd_ex; outputs are undefined unless KLA_OK.
  */
 KLA_API size_t kla_chunk_bwd_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk,
