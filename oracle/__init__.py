@@ -21,6 +21,10 @@ and a hand-worked two-token fixture under ``tests/golden/``.
 ``kla_oracle_backward`` is the reverse-mode derivative of the same loop
 (every state kept, the step undone operation by operation), pinned by central
 finite differences of ``kla_oracle_forward`` and by torch autograd.
+
+``kla_oracle_psd_features`` is the rank-one PSD feature map of the KATA page
+(psi(u) = u u^T as a vector), under which the same recurrence is DeltaKATA;
+it is pinned by its inner-product identity and by numpy's outer product.
 """
 from __future__ import annotations
 
@@ -162,5 +166,47 @@ def kla_oracle_backward(q, k, v, g, eta, eps, h0, dout, dhT=None, *, beta_direct
     return out
 
 
+def psd_feature_index(p: int):
+    """The (i, j), i <= j, of each feature, row-major over the upper triangle."""
+    return [(i, j) for i in range(p) for j in range(i, p)]
+
+
+def kla_oracle_psd_features(x, d_out):
+    """Rank-one PSD feature of each row u of x (shape [..., p]), as a vector.
+
+    "Kernelized Linear Attention: breaking the capacity wall via symmetric
+    cones", section 2.2: psi(u) = u u^T.  The symmetric matrix is written out
+    as its upper triangle, row-major, with the off-diagonal entries scaled by
+    sqrt(2) (so that the Frobenius inner product of two features is the dot
+    product of their vectors), then padded with zeros to d_out >= p(p+1)/2.
+    """
+    x = _f64(x)
+    p = x.shape[-1]
+    idx = psd_feature_index(p)
+    assert d_out >= len(idx)
+    y = np.zeros(x.shape[:-1] + (d_out,), np.float64)
+    for n, (i, j) in enumerate(idx):
+        y[..., n] = x[..., i] * x[..., j] * (1.0 if i == j else np.sqrt(2.0))
+    return y
+
+
+def kla_oracle_psd_features_bwd(x, dy):
+    """dL/dx given dL/dy for y = kla_oracle_psd_features(x, d_out): for the
+    entry y = c x_i x_j, dx_i += c x_j dy and dx_j += c x_i dy (2 x_i dy on the
+    diagonal)."""
+    x, dy = _f64(x), _f64(dy)
+    p = x.shape[-1]
+    dx = np.zeros_like(x)
+    for n, (i, j) in enumerate(psd_feature_index(p)):
+        if i == j:
+            dx[..., i] += 2.0 * x[..., i] * dy[..., n]
+        else:
+            c = np.sqrt(2.0)
+            dx[..., i] += c * x[..., j] * dy[..., n]
+            dx[..., j] += c * x[..., i] * dy[..., n]
+    return dx
+
+
 __all__ = ["build", "kla_oracle_forward", "kla_oracle_decode_step", "kla_oracle_backward",
+           "kla_oracle_psd_features", "kla_oracle_psd_features_bwd", "psd_feature_index",
            "NO_ERASE", "BETA_DIRECT"]
