@@ -7,8 +7,9 @@ one step = one call over that batch.  The long-context prefill
 (B=1, H=16, T=131072) and the decode loop (B=64, H=16, d=128, fp32 state,
 kla_decode_step) are timed in the same run and reported under "secondary", with
 the training shape under Gated DeltaNet's step-size rule (kla_chunk_fwd_ex with
-KLA_BETA_DIRECT, unit-norm keys) and the backward (kla_chunk_bwd) of the
-training shape.
+KLA_BETA_DIRECT, unit-norm keys), the backward (kla_chunk_bwd) of the
+training shape, and DeltaKATA (PSD features of 15-value q and k, then
+kla_chunk_fwd) on the training shape.
 
 Timing: W untimed warm-up steps, then exactly K timed steps, each between
 CUDA events on the launching stream; L2 is flushed (a 512 MiB write) between
@@ -372,6 +373,56 @@ def bench_backward(case, K, W, flush, peaks, stream):
     return res
 
 
+def deltakata_work(case, p):
+    """Algorithmic bytes of one DeltaKATA prefill from raw inputs: q, k with p
+    values per token-head, v and o with dv, g and eta; hT per head."""
+    esz = 2 if case.io == "bf16" else 4
+    th = case.B * case.T * case.H
+    per_tok = esz * (2 * p + 2 * case.dv) + 8
+    w = prefill_work(case)
+    return dict(bytes=th * per_tok + case.B * case.H * case.dk * case.dv * 4, flops=w["flops"],
+                tokens=case.B * case.T, token_heads=th, per_token_head_bytes=per_tok)
+
+
+def bench_deltakata(case, p, K, W, flush, peaks, stream):
+    """Time DeltaKATA on ``case``: the PSD features of q and k (p values per
+    token-head, case.dk features) and kla_chunk_fwd on them."""
+    import chunked_delta_rule_kla_gb300 as kla
+    inp = kla_inputs.make_prefill(case, device="cuda")
+    B, T, H, dk, dv = case.B, case.T, case.H, case.dk, case.dv
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(case.seed + 2000)
+    dt = inp["q"].dtype
+    q = torch.randn((B, T, H, p), generator=gen, device="cuda").mul(0.4).to(dt)
+    u = torch.randn((B, T, H, p), generator=gen, device="cuda")
+    k = (u / u.norm(dim=-1, keepdim=True)).to(dt)
+    fq = torch.empty((B, T, H, dk), dtype=dt, device="cuda")
+    fk = torch.empty_like(fq)
+    o = torch.empty((B, T, H, dv), dtype=dt, device="cuda")
+    hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
+    ws = kla.alloc_workspace(B, T, H, dk, dv, case.chunk, kla.KLA_IO_BF16 if case.io == "bf16" else kla.KLA_IO_FP32)
+
+    def step():
+        kla.kla_psd_features(q, fq, stream)
+        kla.kla_psd_features(k, fk, stream)
+        kla.kla_chunk_fwd(fq, fk, inp["v"], inp["g"], inp["eta"], inp["eps"], None, o, hT, ws,
+                          case.chunk, stream)
+
+    barrier()
+    ms = timed_steps(step, K, W, flush, stream)
+    barrier()
+    work = deltakata_work(case, p)
+    _, slowest_s = job_throughput(work["tokens"], sum(ms) / len(ms) * 1e-3)
+    mean_ms = slowest_s * 1e3
+    res = dict(ms_per_step=mean_ms, tokens_per_s=work["tokens"] / (mean_ms * 1e-3),
+               roofline=dict(roofline(work, mean_ms * 1e-3, peaks, TRAFFIC_BYTES.get("deltakata_" + case.name)),
+                             scope="two kla_psd_features calls and one kla_chunk_fwd call",
+                             peak_kind="burst copy bandwidth"),
+               launches=K * (2 + prefill_launches(kla, case)))
+    del inp, q, k, fq, fk, o, hT, ws
+    return res
+
+
 def bench_decode(case, K_loops, W_loops, peaks, stream, n_states=4, e2e=True):
     """Times `steps` consecutive kla_decode_step calls per loop.  The calls
     rotate over n_states independent state buffers (like the layers of a
@@ -475,7 +526,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-heads", type=int, default=64)
     ap.add_argument("--decode-loops", type=int, default=3)
-    ap.add_argument("--only", choices=["train", "long", "gdn", "decode", "bwd"], default=None,
+    ap.add_argument("--only", choices=["train", "long", "gdn", "decode", "bwd", "deltakata"], default=None,
                     help="time one workload only (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
     args = ap.parse_args()
@@ -500,7 +551,12 @@ def main():
 
     e2e = not args.no_e2e
     if args.only is not None:
-        if args.only == "bwd":
+        if args.only == "deltakata":
+            kr = bench_deltakata(kla_inputs.TRAIN, 15, args.steps, args.warmup, flush, peaks, stream)
+            line = dict(workload="deltakata_p15_" + kla_inputs.TRAIN.name, tokens_per_s=kr["tokens_per_s"],
+                        ms_per_step=kr["ms_per_step"], roofline=kr["roofline"],
+                        gpu_launches=kr["launches"])
+        elif args.only == "bwd":
             br = bench_backward(kla_inputs.TRAIN, args.steps, args.warmup, flush, peaks, stream)
             line = dict(workload="bwd_" + kla_inputs.TRAIN.name, tokens_per_s=br["tokens_per_s"],
                         ms_per_step=br["ms_per_step"], roofline=br["roofline"],
@@ -541,6 +597,10 @@ def main():
         secondary["backward_train"] = dict(workload="bwd_" + kla_inputs.TRAIN.name,
                                            tokens_per_s=br["tokens_per_s"],
                                            ms_per_step=br["ms_per_step"], roofline=br["roofline"])
+        kr = bench_deltakata(kla_inputs.TRAIN, 15, max(5, args.steps // 2), 3, flush, peaks, stream)
+        secondary["deltakata_train_prefill"] = dict(
+            workload="deltakata_p15_" + kla_inputs.TRAIN.name, p=15, d_feat=kla_inputs.TRAIN.dk,
+            tokens_per_s=kr["tokens_per_s"], ms_per_step=kr["ms_per_step"], roofline=kr["roofline"])
         dc = kla_inputs.DECODE
         dr = bench_decode(dc, args.decode_loops, 3, peaks, stream, e2e=e2e)
         secondary["decode"] = dict(workload=dc.name, tokens_per_s=dr["tokens_per_s"],

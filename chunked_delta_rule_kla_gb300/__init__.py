@@ -45,6 +45,8 @@ EXPORTED_SYMBOLS = (
     "kla_decode_step_ex",
     "kla_chunk_bwd_workspace_bytes",
     "kla_chunk_bwd",
+    "kla_psd_features",
+    "kla_psd_features_bwd",
     "kla_workspace_check",
     "kla_status_string",
 )
@@ -104,6 +106,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                       vp, vp, vp, vp, vp, vp,
                                       i, i, i, i, i, i, i, i, vp, sz, vp]
         lib.kla_chunk_bwd.restype = i
+        i64 = ctypes.c_int64
+        lib.kla_psd_features.argtypes = [vp, vp, i64, i, i, i, vp]
+        lib.kla_psd_features.restype = i
+        lib.kla_psd_features_bwd.argtypes = [vp, vp, vp, i64, i, i, i, vp]
+        lib.kla_psd_features_bwd.restype = i
         lib.kla_workspace_check.argtypes = [vp, sz, vp]
         lib.kla_workspace_check.restype = i
         lib.kla_status_string.argtypes = [i]
@@ -255,6 +262,34 @@ def kla_chunk_bwd(q, k, v, g, eta, eps, h0, grad_o, grad_hT, grad_q, grad_k, gra
         raise KlaError(rc, "kla_chunk_bwd")
 
 
+def kla_psd_features(x, y, stream=None) -> None:
+    """DeltaKATA features (see include/kla.h): x [..., p] -> y [..., d_out], same dtype."""
+    p, d_out = x.shape[-1], y.shape[-1]
+    if y.shape[:-1] != x.shape[:-1] or y.dtype != x.dtype:
+        raise ValueError("y must be [..., d_out] with x's leading shape and dtype")
+    rows = x.numel() // p if p else 0
+    rc = load_library().kla_psd_features(_ptr(x, "x"), _ptr(y, "y"), rows, p, d_out, _io_of(x),
+                                         _stream(stream))
+    if rc != KLA_OK:
+        raise KlaError(rc, "kla_psd_features")
+
+
+def kla_psd_features_bwd(x, grad_y, grad_x, stream=None) -> None:
+    """The derivative of kla_psd_features: grad_y [..., d_out] -> grad_x [..., p]."""
+    p, d_out = x.shape[-1], grad_y.shape[-1]
+    if grad_x.shape != x.shape or grad_y.shape[:-1] != x.shape[:-1]:
+        raise ValueError("shape mismatch among x, grad_y, grad_x")
+    for name, t in (("grad_y", grad_y), ("grad_x", grad_x)):
+        if t.dtype != x.dtype:
+            raise TypeError(f"{name} must have x's dtype")
+    rows = x.numel() // p if p else 0
+    rc = load_library().kla_psd_features_bwd(_ptr(x, "x"), _ptr(grad_y, "grad_y"),
+                                             _ptr(grad_x, "grad_x"), rows, p, d_out, _io_of(x),
+                                             _stream(stream))
+    if rc != KLA_OK:
+        raise KlaError(rc, "kla_psd_features_bwd")
+
+
 def kla_chunk_fwd_noalloc(q, k, v, g, eta, eps, h0, o, hT, chunk=64, stream=None) -> None:
     """kla_chunk_fwd without a workspace, for callers that must not allocate
     device memory: the scratch is an array built into the library (see
@@ -386,6 +421,42 @@ def kla_chunk(q, k, v, g, eta, eps=1e-6, h0=None, beta=KLA_BETA_KACZMARZ):
                           int(beta))
 
 
+def psd_features(x, d_out, stream=None):
+    """Allocate and return the DeltaKATA features of x ([..., p] -> [..., d_out])."""
+    y = torch.empty(x.shape[:-1] + (d_out,), dtype=x.dtype, device=x.device)
+    kla_psd_features(x.contiguous(), y, stream)
+    return y
+
+
+class PSDFeatures(torch.autograd.Function):
+    """psi(u) = u u^T as a vector (kla_psd_features), differentiable."""
+
+    @staticmethod
+    def forward(ctx, x, d_out):
+        x = x.contiguous()
+        ctx.save_for_backward(x)
+        return psd_features(x, d_out)
+
+    @staticmethod
+    def backward(ctx, gy):
+        (x,) = ctx.saved_tensors
+        gx = torch.empty_like(x)
+        kla_psd_features_bwd(x, gy.contiguous(), gx)
+        return gx, None
+
+
+def deltakata(q, k, v, g, eta, eps=1e-6, h0=None, d_feat=None, beta=KLA_BETA_KACZMARZ):
+    """DeltaKATA: the KLA recurrence on the rank-one PSD features of q and k.
+
+    q, k [B,T,H,p] with p(p+1)/2 <= d_feat in {64, 128} (default: the smaller
+    that fits); v [B,T,H,dv].  Differentiable; returns (o, hT)."""
+    p = k.shape[-1]
+    if d_feat is None:
+        d_feat = 64 if p * (p + 1) // 2 <= 64 else 128
+    return kla_chunk(PSDFeatures.apply(q, d_feat), PSDFeatures.apply(k, d_feat), v, g, eta, eps,
+                     h0, beta)
+
+
 def decode_step(q, k, v, g, eta, S, eps=1e-6, stream=None, beta=KLA_BETA_KACZMARZ):
     """Run kla_decode_step (with the step size chosen by ``beta``); S is updated in
     place.  Returns o."""
@@ -399,6 +470,7 @@ __all__ = [
     "kla_chunk_fwd_scan", "kla_chunk_fwd_scan_workspace_bytes", "kla_chunk_fwd_auto_segments",
     "kla_chunk_fwd_ex", "kla_decode_step_ex", "KLA_BETA_KACZMARZ", "KLA_BETA_DIRECT",
     "kla_chunk_bwd", "kla_chunk_bwd_workspace_bytes", "chunk_bwd", "kla_chunk", "KLAChunk",
+    "kla_psd_features", "kla_psd_features_bwd", "psd_features", "PSDFeatures", "deltakata",
     "kla_workspace_check",
     "kla_status_string", "chunk_fwd", "decode_step", "alloc_workspace", "load_library",
     "KlaError", "EXPORTED_SYMBOLS", "KLA_IO_BF16", "KLA_IO_FP32",

@@ -25,6 +25,7 @@ SOURCES = [
     "kla_chunk_tc.cu",
     "kla_noalloc.cu",
     "kla_bwd.cu",
+    "kla_psd.cu",
 ]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

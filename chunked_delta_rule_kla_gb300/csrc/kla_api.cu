@@ -212,6 +212,29 @@ kla_status kla_chunk_bwd(const void* q, const void* k, const void* v, const floa
                                            io == KLA_IO_BF16, beta == KLA_BETA_DIRECT, scratch, st));
 }
 
+kla_status kla_psd_features(const void* x, void* y, int64_t rows, int p, int d_out,
+                            kla_io_dtype io, void* stream) {
+    if (rows < 0 || p < 1 || check_io(io) != KLA_OK) return KLA_ERR_INVALID_ARG;
+    if (!dim_ok(d_out) || p * (p + 1) / 2 > d_out) return KLA_ERR_UNSUPPORTED;
+    if (rows == 0) return KLA_OK;
+    if (!x || !y) return KLA_ERR_INVALID_ARG;
+    if (!aligned4(x) || !aligned4(y)) return KLA_ERR_INVALID_ARG;
+    return to_status(kla::launch_psd_features(x, y, rows, p, d_out, io == KLA_IO_BF16,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kla_status kla_psd_features_bwd(const void* x, const void* grad_y, void* grad_x, int64_t rows,
+                                int p, int d_out, kla_io_dtype io, void* stream) {
+    if (rows < 0 || p < 1 || check_io(io) != KLA_OK) return KLA_ERR_INVALID_ARG;
+    if (!dim_ok(d_out) || p * (p + 1) / 2 > d_out) return KLA_ERR_UNSUPPORTED;
+    if (rows == 0) return KLA_OK;
+    if (!x || !grad_y || !grad_x) return KLA_ERR_INVALID_ARG;
+    if (!aligned4(x) || !aligned4(grad_y) || !aligned4(grad_x)) return KLA_ERR_INVALID_ARG;
+    return to_status(kla::launch_psd_features_bwd(x, grad_y, grad_x, rows, p, d_out,
+                                                  io == KLA_IO_BF16,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kla_status kla_workspace_check(const void* workspace, size_t workspace_bytes, void* stream) {
     if (!workspace || workspace_bytes < kla::kErrorRecordBytes) return KLA_ERR_WORKSPACE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

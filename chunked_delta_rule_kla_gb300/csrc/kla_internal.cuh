@@ -95,6 +95,13 @@ int chunk_fwd_tc_auto_segments(int B, int T, int H, int dk, int dv);
 // I/O uses tf32 products; fp32 I/O uses a three-term tf32 split.  `scratch`
 // holds chunk_bwd_workspace_floats floats.
 size_t chunk_bwd_workspace_floats(int B, int T, int H, int dk, int dv);
+
+// Rank-one PSD features of DeltaKATA and their derivative (kla_psd.cu):
+// rows of p values in, rows of d_out features out (and back).
+cudaError_t launch_psd_features(const void* x, void* y, int64_t rows, int p, int d_out, bool bf16,
+                                cudaStream_t stream);
+cudaError_t launch_psd_features_bwd(const void* x, const void* dy, void* dx, int64_t rows, int p,
+                                    int d_out, bool bf16, cudaStream_t stream);
 cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
                              const float* eta, float eps, const float* h0, const void* dout,
                              const float* dhT, void* dq, void* dk, void* dv, float* dg, float* deta,

@@ -37,6 +37,7 @@
 #define KLA_H_
 
 #include <stddef.h>
+#include <stdint.h>
 
 #if defined(__GNUC__)
 #define KLA_API __attribute__((visibility("default")))
@@ -210,6 +211,28 @@ KLA_API kla_status kla_chunk_bwd(const void* q, const void* k, const void* v,
                                  int B, int T, int H, int dk, int dv, int chunk,
                                  kla_io_dtype io, kla_beta_mode beta,
                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * DeltaKATA's keys and queries: the rank-one PSD feature psi(u) = u u^T of
+ * each row u ("Kernelized Linear Attention: breaking the capacity wall via
+ * symmetric cones", section 2.2; section 4 runs the delta rule on it).
+ * psi(u) is written as the upper triangle of u u^T, row-major, off-diagonal
+ * entries scaled by sqrt(2), then zeros up to d_out, so that
+ * psi(q) . psi(k) = (q . k)^2 and ||psi(k)||^2 = ||k||^4.  Feeding the
+ * features of q and k to kla_chunk_fwd_ex / kla_chunk_bwd gives DeltaKATA.
+ *
+ *  x : [rows, p] I/O dtype;  y : [rows, d_out] I/O dtype (written in full)
+ *  1 <= p, p(p+1)/2 <= d_out, d_out in {64, 128} (p <= 10 or p <= 15)
+ *
+ * kla_psd_features_bwd maps grad_y [rows, d_out] to grad_x [rows, p].  Both
+ * are asynchronous on `stream`; KLA_ERR_INVALID_ARG / KLA_ERR_UNSUPPORTED for
+ * bad arguments or sizes.
+ */
+KLA_API kla_status kla_psd_features(const void* x, void* y, int64_t rows, int p, int d_out,
+                                    kla_io_dtype io, void* stream);
+KLA_API kla_status kla_psd_features_bwd(const void* x, const void* grad_y, void* grad_x,
+                                        int64_t rows, int p, int d_out, kla_io_dtype io,
+                                        void* stream);
 
 /*
  * Segment count kla_chunk_fwd uses for this shape (1 = no scan).  With bf16

@@ -96,3 +96,16 @@ def test_beta_mode_argument_errors():
         rc = lib.kla_decode_step_ex(None, None, None, None, None, 1e-6, None, None, 1, 1, 128, 128,
                                     kla.KLA_IO_BF16, bad, None)
         assert rc == kla.KLA_ERR_INVALID_ARG
+
+
+def test_psd_feature_argument_errors():
+    kla = _kla()
+    lib = kla.load_library()
+    # 16 (16+1)/2 = 136 features do not fit 128; 11 do not fit 64; d_out must be 64 or 128
+    assert lib.kla_psd_features(None, None, 1, 16, 128, kla.KLA_IO_BF16, None) == kla.KLA_ERR_UNSUPPORTED
+    assert lib.kla_psd_features(None, None, 1, 11, 64, kla.KLA_IO_BF16, None) == kla.KLA_ERR_UNSUPPORTED
+    assert lib.kla_psd_features(None, None, 1, 4, 96, kla.KLA_IO_BF16, None) == kla.KLA_ERR_UNSUPPORTED
+    assert lib.kla_psd_features(None, None, 1, 0, 64, kla.KLA_IO_BF16, None) == kla.KLA_ERR_INVALID_ARG
+    assert lib.kla_psd_features(None, None, 1, 4, 64, kla.KLA_IO_BF16, None) == kla.KLA_ERR_INVALID_ARG
+    assert lib.kla_psd_features(None, None, 0, 4, 64, kla.KLA_IO_BF16, None) == kla.KLA_OK
+    assert lib.kla_psd_features_bwd(None, None, None, 1, 15, 64, kla.KLA_IO_FP32, None) == kla.KLA_ERR_UNSUPPORTED
