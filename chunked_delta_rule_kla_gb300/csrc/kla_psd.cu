@@ -10,7 +10,8 @@
 // d_out in {64, 128} the chunked kernels take the features as keys and
 // queries unchanged (zero padding changes no product).
 //
-// Both kernels are one warp per row and stream their rows once (HBM-bound).
+// The forward takes a half-warp per row, the derivative a warp per row; both
+// stream their rows once (HBM-bound).
 #include "kla_internal.cuh"
 
 namespace kla {
@@ -39,34 +40,71 @@ __device__ __forceinline__ void feature_pair(int n, int p, int& i, int& j) {
     j = i + n;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(256) psd_features_kernel(const T* __restrict__ x, T* __restrict__ y,
-                                                           int64_t rows, int p, int d_out) {
-    const int lane = threadIdx.x & 31;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int nf = p * (p + 1) / 2;
-    int fi[4], fj[4];
-    float fs[4];
+// d_out / 16 consecutive features of one row, stored as one vector
+template <typename T, int PER> struct FeatStore;
+template <> struct FeatStore<__nv_bfloat16, 8> {
+    __device__ __forceinline__ static void st(__nv_bfloat16* p, const float* v) {
+        uint32_t w[4];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const int n = lane + 32 * m;
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+template <> struct FeatStore<__nv_bfloat16, 4> {
+    __device__ __forceinline__ static void st(__nv_bfloat16* p, const float* v) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+        *reinterpret_cast<uint2*>(p) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    }
+};
+template <> struct FeatStore<float, 8> {
+    __device__ __forceinline__ static void st(float* p, const float* v) {
+        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+    }
+};
+template <> struct FeatStore<float, 4> {
+    __device__ __forceinline__ static void st(float* p, const float* v) {
+        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+};
+
+// A half-warp per row: lane s of the half loads x[s] (s < p) and writes the
+// features PER*s .. PER*s + PER - 1 (PER = d_out / 16) as one vector.
+template <typename T, int PER>
+__global__ void __launch_bounds__(256) psd_features_kernel(const T* __restrict__ x, T* __restrict__ y,
+                                                           int64_t rows, int p) {
+    constexpr int d_out = 16 * PER;
+    const int lane = threadIdx.x & 31, sub = lane & 15;
+    const unsigned mask = 0xffffu << (lane & 16);
+    const int nf = p * (p + 1) / 2;
+    int fi[PER], fj[PER];
+    float fs[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int n = PER * sub + u;
         if (n < nf) {
-            feature_pair(n, p, fi[m], fj[m]);
-            fs[m] = fi[m] == fj[m] ? 1.f : kSqrt2;
+            feature_pair(n, p, fi[u], fj[u]);
+            fs[u] = fi[u] == fj[u] ? 1.f : kSqrt2;
         } else {
-            fi[m] = fj[m] = 0;
-            fs[m] = 0.f;
+            fi[u] = fj[u] = 0;
+            fs[u] = 0.f;
         }
     }
-    for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < rows; row += nwarps) {
-        const float xv = lane < p ? ldx<T>(x + row * p + lane) : 0.f;
+    const int64_t nhalf = ((int64_t)gridDim.x * blockDim.x) >> 4;
+    for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4; row < rows; row += nhalf) {
+        const float xv = sub < p ? ldx<T>(x + row * p + sub) : 0.f;
+        float v[PER];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float xi = __shfl_sync(0xffffffffu, xv, fi[m]);
-            const float xj = __shfl_sync(0xffffffffu, xv, fj[m]);
-            const int n = lane + 32 * m;
-            if (n < d_out) stx<T>(y + row * d_out + n, fs[m] * xi * xj);
+        for (int u = 0; u < PER; ++u) {
+            const float xi = __shfl_sync(mask, xv, fi[u], 16);
+            const float xj = __shfl_sync(mask, xv, fj[u], 16);
+            v[u] = fs[u] * xi * xj;
         }
+        FeatStore<T, PER>::st(y + row * d_out + PER * sub, v);
     }
 }
 
@@ -111,12 +149,17 @@ int grid_for(int64_t rows) {
 cudaError_t launch_psd_features(const void* x, void* y, int64_t rows, int p, int d_out, bool bf16,
                                 cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
-    if (bf16)
-        psd_features_kernel<__nv_bfloat16><<<grid_for(rows), 256, 0, stream>>>(
-            static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), rows, p, d_out);
+    const int64_t blocks64 = (rows + 15) / 16;         // 16 half-warps per block, a row each
+    const int grid = (int)(blocks64 < 152 * 16 ? blocks64 : 152 * 16);
+    using bf = __nv_bfloat16;
+    if (bf16 && d_out == 128)
+        psd_features_kernel<bf, 8><<<grid, 256, 0, stream>>>(static_cast<const bf*>(x), static_cast<bf*>(y), rows, p);
+    else if (bf16)
+        psd_features_kernel<bf, 4><<<grid, 256, 0, stream>>>(static_cast<const bf*>(x), static_cast<bf*>(y), rows, p);
+    else if (d_out == 128)
+        psd_features_kernel<float, 8><<<grid, 256, 0, stream>>>(static_cast<const float*>(x), static_cast<float*>(y), rows, p);
     else
-        psd_features_kernel<float><<<grid_for(rows), 256, 0, stream>>>(
-            static_cast<const float*>(x), static_cast<float*>(y), rows, p, d_out);
+        psd_features_kernel<float, 4><<<grid, 256, 0, stream>>>(static_cast<const float*>(x), static_cast<float*>(y), rows, p);
     return cudaGetLastError();
 }
 
