@@ -25,6 +25,9 @@ finite differences of ``kla_oracle_forward`` and by torch autograd.
 ``kla_oracle_psd_features`` is the rank-one PSD feature map of the KATA page
 (psi(u) = u u^T as a vector), under which the same recurrence is DeltaKATA;
 it is pinned by its inner-product identity and by numpy's outer product.
+
+``kla_oracle_loglinear_forward`` is the Log-Linear gated delta rule (one
+state per Fenwick bucket, weighted readout), written out by origin token.
 """
 from __future__ import annotations
 
@@ -207,6 +210,61 @@ def kla_oracle_psd_features_bwd(x, dy):
     return dx
 
 
+def loglinear_level(t: int, s: int) -> int:
+    """Fenwick level of token s in the prefix of token t (s <= t): 0 for s = t,
+    else one more than the highest bit in which t and s differ ("Log-Linear
+    Attention", technical summary section 2: the prefix is split into buckets
+    of exponentially growing size, recent tokens in the small ones)."""
+    assert 0 <= s <= t
+    return 0 if s == t else (t ^ s).bit_length()
+
+
+def loglinear_num_levels(T: int) -> int:
+    """Levels a sequence of T tokens uses: 1 + ceil(log2 T) (1 for T <= 1)."""
+    return 1 + (max(T, 1) - 1).bit_length()
+
+
+def kla_oracle_loglinear_forward(q, k, v, g, eta, lam, eps, *, beta_direct=False, no_erase=False):
+    """Log-Linear gated delta rule, written out by origin token.
+
+    "Log-Linear Attention", technical summary section 2: one state per Fenwick
+    bucket and o_t = sum_l lambda_t^(l) q_t^T S_t^(l).  Read with the delta
+    rule's transition A_t = a_t (I - beta_t k_t k_t^T) acting on every bucket
+    and each write beta_s k_s v_s^T kept in the bucket of its token s:
+
+        S_t^(l) = sum_{s <= t, level(t, s) = l} A_t ... A_{s+1} beta_s k_s v_s^T
+
+    so that the buckets sum to the ordinary state.  A write's propagation only
+    changes its key: x_s <- a_t (x_s - beta_t k_t (k_t . x_s)), and
+    o_t = sum_s lambda_t^(level(t, s)) (q_t . x_s) v_s.  With ``no_erase`` the
+    transition is a_t I and beta = 1 (linear attention: o = (Q K^T o M_H) V).
+    Starts from a zero state.  lam: [B, T, H, L] with L >= loglinear_num_levels(T).
+    """
+    q, k, v, g, eta, lam = map(_f64, (q, k, v, g, eta, lam))
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    assert lam.shape[:3] == (B, T, H) and lam.shape[3] >= loglinear_num_levels(T)
+    o = np.zeros((B, T, H, dv))
+    for b in range(B):
+        for h in range(H):
+            X = np.zeros((T, dk))              # propagated keys of tokens 0..t
+            for t in range(T):
+                kt = k[b, t, h]
+                a = np.exp(g[b, t, h])
+                if no_erase:
+                    beta = 1.0
+                    X[:t] *= a
+                else:
+                    beta = eta[b, t, h] if beta_direct else eta[b, t, h] / (kt @ kt + eps)
+                    X[:t] = a * (X[:t] - beta * np.outer(X[:t] @ kt, kt))
+                X[t] = beta * kt
+                lev = np.array([loglinear_level(t, s) for s in range(t + 1)])
+                w = lam[b, t, h][lev] * (X[:t + 1] @ q[b, t, h])
+                o[b, t, h] = w @ v[b, :t + 1, h]
+    return o
+
+
 __all__ = ["build", "kla_oracle_forward", "kla_oracle_decode_step", "kla_oracle_backward",
            "kla_oracle_psd_features", "kla_oracle_psd_features_bwd", "psd_feature_index",
+           "kla_oracle_loglinear_forward", "loglinear_level", "loglinear_num_levels",
            "NO_ERASE", "BETA_DIRECT"]
