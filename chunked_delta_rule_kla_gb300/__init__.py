@@ -47,6 +47,9 @@ EXPORTED_SYMBOLS = (
     "kla_chunk_bwd",
     "kla_psd_features",
     "kla_psd_features_bwd",
+    "kla_loglinear_num_levels",
+    "kla_loglinear_workspace_bytes",
+    "kla_loglinear_fwd",
     "kla_workspace_check",
     "kla_status_string",
 )
@@ -111,6 +114,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kla_psd_features.restype = i
         lib.kla_psd_features_bwd.argtypes = [vp, vp, vp, i64, i, i, i, vp]
         lib.kla_psd_features_bwd.restype = i
+        lib.kla_loglinear_num_levels.argtypes = [i]
+        lib.kla_loglinear_num_levels.restype = i
+        lib.kla_loglinear_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+        lib.kla_loglinear_workspace_bytes.restype = sz
+        lib.kla_loglinear_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, f, vp,
+                                          i, i, i, i, i, i, i, i, vp, sz, vp]
+        lib.kla_loglinear_fwd.restype = i
         lib.kla_workspace_check.argtypes = [vp, sz, vp]
         lib.kla_workspace_check.restype = i
         lib.kla_status_string.argtypes = [i]
@@ -290,6 +300,30 @@ def kla_psd_features_bwd(x, grad_y, grad_x, stream=None) -> None:
         raise KlaError(rc, "kla_psd_features_bwd")
 
 
+def kla_loglinear_num_levels(T) -> int:
+    return int(load_library().kla_loglinear_num_levels(int(T)))
+
+
+def kla_loglinear_workspace_bytes(B, T, H, dk, dv, chunk=64, io=KLA_IO_BF16) -> int:
+    return int(load_library().kla_loglinear_workspace_bytes(B, T, H, dk, dv, chunk, io))
+
+
+def kla_loglinear_fwd(q, k, v, g, eta, lam, eps, o, workspace, beta=KLA_BETA_KACZMARZ, chunk=64,
+                      stream=None) -> None:
+    """Enqueue the Log-Linear gated delta rule (see include/kla.h): lam is
+    [B,T,H,L] fp32 with L >= kla_loglinear_num_levels(T); the state starts at zero."""
+    B, T, H, dk, dv, io = _check_prefill_args(q, k, v, g, eta, None, o, None)
+    if lam.dim() != 4 or tuple(lam.shape[:3]) != (B, T, H):
+        raise ValueError("lam must be [B,T,H,L]")
+    rc = load_library().kla_loglinear_fwd(
+        _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g", torch.float32),
+        _ptr(eta, "eta", torch.float32), _ptr(lam, "lam", torch.float32), int(lam.shape[3]),
+        float(eps), _ptr(o, "o"), B, T, H, dk, dv, int(chunk), io, int(beta),
+        _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != KLA_OK:
+        raise KlaError(rc, "kla_loglinear_fwd")
+
+
 def kla_chunk_fwd_noalloc(q, k, v, g, eta, eps, h0, o, hT, chunk=64, stream=None) -> None:
     """kla_chunk_fwd without a workspace, for callers that must not allocate
     device memory: the scratch is an array built into the library (see
@@ -457,6 +491,21 @@ def deltakata(q, k, v, g, eta, eps=1e-6, h0=None, d_feat=None, beta=KLA_BETA_KAC
                      h0, beta)
 
 
+def loglinear_fwd(q, k, v, g, eta, lam, eps=1e-6, beta=KLA_BETA_KACZMARZ, workspace=None,
+                  stream=None):
+    """Allocate o and run kla_loglinear_fwd.  Returns o."""
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if workspace is None:
+        n = kla_loglinear_workspace_bytes(B, T, H, dk, dv, 64, _io_of(q))
+        if n == 0:
+            raise KlaError(KLA_ERR_UNSUPPORTED, "kla_loglinear_workspace_bytes")
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    kla_loglinear_fwd(q, k, v, g, eta, lam, eps, o, workspace, beta=beta, stream=stream)
+    return o
+
+
 def decode_step(q, k, v, g, eta, S, eps=1e-6, stream=None, beta=KLA_BETA_KACZMARZ):
     """Run kla_decode_step (with the step size chosen by ``beta``); S is updated in
     place.  Returns o."""
@@ -471,6 +520,7 @@ __all__ = [
     "kla_chunk_fwd_ex", "kla_decode_step_ex", "KLA_BETA_KACZMARZ", "KLA_BETA_DIRECT",
     "kla_chunk_bwd", "kla_chunk_bwd_workspace_bytes", "chunk_bwd", "kla_chunk", "KLAChunk",
     "kla_psd_features", "kla_psd_features_bwd", "psd_features", "PSDFeatures", "deltakata",
+    "kla_loglinear_num_levels", "kla_loglinear_workspace_bytes", "kla_loglinear_fwd", "loglinear_fwd",
     "kla_workspace_check",
     "kla_status_string", "chunk_fwd", "decode_step", "alloc_workspace", "load_library",
     "KlaError", "EXPORTED_SYMBOLS", "KLA_IO_BF16", "KLA_IO_FP32",

@@ -26,6 +26,7 @@ SOURCES = [
     "kla_noalloc.cu",
     "kla_bwd.cu",
     "kla_psd.cu",
+    "kla_loglinear.cu",
 ]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

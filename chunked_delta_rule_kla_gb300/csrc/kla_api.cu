@@ -212,6 +212,51 @@ kla_status kla_chunk_bwd(const void* q, const void* k, const void* v, const floa
                                            io == KLA_IO_BF16, beta == KLA_BETA_DIRECT, scratch, st));
 }
 
+int kla_loglinear_num_levels(int T) {
+    if (T < 0) return 0;
+    int bits = 0;
+    while (bits < 31 && (1 << bits) < T) ++bits;      // ceil(log2 T)
+    return 1 + bits;
+}
+
+size_t kla_loglinear_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk,
+                                     kla_io_dtype io) {
+    if (B < 0 || T < 0 || H < 0 || check_io(io) != KLA_OK) return 0;
+    if (!dim_ok(dk) || !dim_ok(dv) || chunk != 64) return 0;
+    if (!sizes_fit(B, T, H, dk, dv) || (int64_t)B * H > 65535) return 0;
+    const size_t body = sizeof(float) * kla::loglinear_workspace_floats(B, T, H, dk, dv);
+    return kla::kErrorRecordBytes + (body + 255) / 256 * 256;
+}
+
+kla_status kla_loglinear_fwd(const void* q, const void* k, const void* v, const float* g,
+                             const float* eta, const float* lambda, int L, float eps, void* o,
+                             int B, int T, int H, int dk, int dv, int chunk, kla_io_dtype io,
+                             kla_beta_mode beta, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+    if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || chunk <= 0) return KLA_ERR_INVALID_ARG;
+    if (check_io(io) != KLA_OK) return KLA_ERR_INVALID_ARG;
+    if (beta != KLA_BETA_KACZMARZ && beta != KLA_BETA_DIRECT) return KLA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f)) return KLA_ERR_INVALID_ARG;
+    if (L < kla_loglinear_num_levels(T)) return KLA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv) || chunk != 64) return KLA_ERR_UNSUPPORTED;
+    if (!sizes_fit(B, T, H, dk, dv) || (int64_t)B * H > 65535) return KLA_ERR_UNSUPPORTED;
+    if ((int64_t)B * H * T == 0) return KLA_OK;
+    if (!q || !k || !v || !g || !eta || !lambda || !o) return KLA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, o};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KLA_ERR_INVALID_ARG;
+    if (!aligned4(g) || !aligned4(eta) || !aligned4(lambda)) return KLA_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KLA_ERR_WORKSPACE;
+    if (workspace_bytes < kla_loglinear_workspace_bytes(B, T, H, dk, dv, chunk, io))
+        return KLA_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, kla::kErrorRecordBytes, st);
+    if (e != cudaSuccess) return KLA_ERR_CUDA;
+    float* scratch = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kla::kErrorRecordBytes);
+    return to_status(kla::launch_loglinear_fwd(q, k, v, g, eta, lambda, L, eps, o, B, T, H, dk, dv,
+                                               io == KLA_IO_BF16, beta == KLA_BETA_DIRECT, scratch, st));
+}
+
 kla_status kla_psd_features(const void* x, void* y, int64_t rows, int p, int d_out,
                             kla_io_dtype io, void* stream) {
     if (rows < 0 || p < 1 || check_io(io) != KLA_OK) return KLA_ERR_INVALID_ARG;

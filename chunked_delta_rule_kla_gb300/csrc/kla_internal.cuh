@@ -96,6 +96,15 @@ int chunk_fwd_tc_auto_segments(int B, int T, int H, int dk, int dv);
 // holds chunk_bwd_workspace_floats floats.
 size_t chunk_bwd_workspace_floats(int B, int T, int H, int dk, int dv);
 
+// Log-Linear gated delta rule (kla_loglinear.cu): a per-chunk kernel, a
+// per-head Fenwick carry of the level states, a per-chunk output kernel.
+int loglinear_state_bits(int T);
+size_t loglinear_workspace_floats(int B, int T, int H, int dk, int dv);
+cudaError_t launch_loglinear_fwd(const void* q, const void* k, const void* v, const float* g,
+                                 const float* eta, const float* lam, int L, float eps, void* o, int B,
+                                 int T, int H, int DK, int DV, bool bf16, bool beta_direct,
+                                 float* scratch, cudaStream_t stream);
+
 // Rank-one PSD features of DeltaKATA and their derivative (kla_psd.cu):
 // rows of p values in, rows of d_out features out (and back).
 cudaError_t launch_psd_features(const void* x, void* y, int64_t rows, int p, int d_out, bool bf16,

@@ -213,6 +213,33 @@ KLA_API kla_status kla_chunk_bwd(const void* q, const void* k, const void* v,
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Log-Linear gated delta rule ("Log-Linear Attention", technical summary
+ * section 2): the prefix of token t is split into Fenwick buckets, token s in
+ * bucket level(t, s) = 0 for s = t, else 1 + floor(log2(t xor s)); each bucket
+ * keeps its own state, and o_t = sum_l lambda_t^(l) S_t^(l)^T q_t.  The
+ * delta rule's transition a_t (I - beta_t k_t k_t^T) acts on every bucket and
+ * each write beta_s k_s v_s^T stays in its token's bucket, so the buckets sum
+ * to the state of kla_chunk_fwd (lambda = 1 gives kla_chunk_fwd's o).
+ *
+ *  q, k, v, g, eta, eps, beta : as kla_chunk_fwd_ex (the state starts at zero)
+ *  lambda : fp32 [B, T, H, L], L >= kla_loglinear_num_levels(T)
+ *  o      : [B, T, H, dv] I/O dtype
+ *  chunk = 64; dk, dv : 64 or 128; B*H <= 65535.
+ *
+ * Cost: O(T log T); the workspace (kla_loglinear_workspace_bytes) holds the
+ * level states at every chunk start, ceil(log2(T / 64)) slots of dk x dv fp32
+ * per (batch, head, chunk).  Errors as kla_chunk_fwd_ex.
+ */
+KLA_API int kla_loglinear_num_levels(int T);
+KLA_API size_t kla_loglinear_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk,
+                                             kla_io_dtype io);
+KLA_API kla_status kla_loglinear_fwd(const void* q, const void* k, const void* v, const float* g,
+                                     const float* eta, const float* lambda, int L, float eps,
+                                     void* o, int B, int T, int H, int dk, int dv, int chunk,
+                                     kla_io_dtype io, kla_beta_mode beta, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/*
  * DeltaKATA's keys and queries: the rank-one PSD feature psi(u) = u u^T of
  * each row u ("Kernelized Linear Attention: breaking the capacity wall via
  * symmetric cones", section 2.2; section 4 runs the delta rule on it).

@@ -258,7 +258,8 @@ def kla_oracle_loglinear_forward(q, k, v, g, eta, lam, eps, *, beta_direct=False
                     beta = eta[b, t, h] if beta_direct else eta[b, t, h] / (kt @ kt + eps)
                     X[:t] = a * (X[:t] - beta * np.outer(X[:t] @ kt, kt))
                 X[t] = beta * kt
-                lev = np.array([loglinear_level(t, s) for s in range(t + 1)])
+                # level(t, s) for s = 0..t: the bit length of t xor s (frexp's exponent)
+                lev = np.frexp((t ^ np.arange(t + 1)).astype(np.float64))[1]
                 w = lam[b, t, h][lev] * (X[:t + 1] @ q[b, t, h])
                 o[b, t, h] = w @ v[b, :t + 1, h]
     return o

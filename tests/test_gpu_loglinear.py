@@ -1,0 +1,81 @@
+"""GPU parity of the Log-Linear gated delta rule (kla_loglinear_fwd) against
+the oracle, which writes the buckets out by origin token."""
+import numpy as np
+import pytest
+import torch
+
+import kla_inputs
+import oracle
+from tests.parity_utils import TOL, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _kla():
+    import chunked_delta_rule_kla_gb300 as kla
+    return kla
+
+
+def _inputs(io, B, T, H, dk, dv, seed):
+    case = kla_inputs.TINY.with_(B=B, T=T, H=H, dk=dk, dv=dv, io=io, seed=seed, knorm=(0.5, 2.0))
+    inp = kla_inputs.make_prefill(case, device="cuda")
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed + 1)
+    L = oracle.loglinear_num_levels(T)
+    lam = torch.empty((B, T, H, L), device="cuda").uniform_(0.2, 1.5, generator=gen)
+    return inp, lam
+
+
+def _check(io, B, T, H, dk, dv, seed, direct=False, heads=None):
+    kla = _kla()
+    inp, lam = _inputs(io, B, T, H, dk, dv, seed)
+    beta = kla.KLA_BETA_DIRECT if direct else kla.KLA_BETA_KACZMARZ
+    if direct:
+        inp["k"] = torch.nn.functional.normalize(inp["k"].float(), dim=-1).to(inp["k"].dtype)
+    o = kla.loglinear_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["eta"], lam, inp["eps"], beta=beta)
+    torch.cuda.synchronize()
+    names = ("q", "k", "v", "g", "eta")
+    sel = {n: inp[n] for n in names}
+    lam_s = lam
+    if heads is not None:
+        idx = torch.as_tensor(heads, device="cuda")
+        sel = {n: t.index_select(2, idx) for n, t in sel.items()}
+        lam_s = lam.index_select(2, idx)
+        o = o.index_select(2, idx)
+    ref = oracle.kla_oracle_loglinear_forward(*(sel[n] for n in names), lam_s, inp["eps"],
+                                              beta_direct=direct)
+    e = rel_err(o, ref)
+    assert e <= TOL[io], f"o rel err {e:.3e} > {TOL[io]}"
+
+
+@pytest.mark.parametrize("io", ["fp32", "bf16"])
+@pytest.mark.parametrize("T", [1, 5, 64, 65, 130, 200, 520])
+def test_loglinear_lengths(io, T):
+    _check(io, 1, T, 2, 128, 128, 600 + T)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64)])
+@pytest.mark.parametrize("io", ["fp32", "bf16"])
+def test_loglinear_head_dims(io, dk, dv):
+    _check(io, 2, 300, 2, dk, dv, 700 + dk + dv)
+
+
+@pytest.mark.parametrize("io", ["fp32", "bf16"])
+def test_loglinear_direct_step_size(io):
+    _check(io, 1, 260, 2, 128, 128, 720, direct=True)
+
+
+def test_loglinear_unit_weights_equal_chunk_fwd():
+    # lambda = 1 sums the buckets back into the ordinary state: kla_chunk_fwd's output
+    kla = _kla()
+    inp, lam = _inputs("fp32", 2, 333, 2, 128, 128, 730)
+    lam = torch.ones_like(lam)
+    o = kla.loglinear_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["eta"], lam, inp["eps"])
+    o2, _ = kla.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["eta"], inp["eps"], None)
+    torch.cuda.synchronize()
+    assert rel_err(o, o2.double().cpu().numpy()) <= 1e-4
+
+
+def test_loglinear_training_shape_sampled_heads():
+    # B1 H4 T4096 d128 bf16: 64 chunks, level states up to bit 5; two heads checked
+    _check("bf16", 1, 4096, 4, 128, 128, 740, heads=[0, 3])

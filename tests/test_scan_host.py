@@ -109,3 +109,19 @@ def test_psd_feature_argument_errors():
     assert lib.kla_psd_features(None, None, 1, 4, 64, kla.KLA_IO_BF16, None) == kla.KLA_ERR_INVALID_ARG
     assert lib.kla_psd_features(None, None, 0, 4, 64, kla.KLA_IO_BF16, None) == kla.KLA_OK
     assert lib.kla_psd_features_bwd(None, None, None, 1, 15, 64, kla.KLA_IO_FP32, None) == kla.KLA_ERR_UNSUPPORTED
+
+
+def test_loglinear_levels_and_errors():
+    kla = _kla()
+    lib = kla.load_library()
+    assert [kla.kla_loglinear_num_levels(T) for T in (1, 2, 64, 65, 4096, 131072)] == [1, 2, 7, 8, 13, 18]
+    args = [None] * 6
+    # too few levels for T = 100 (needs 8)
+    rc = lib.kla_loglinear_fwd(*args, 7, 1e-6, None, 1, 100, 1, 128, 128, 64, kla.KLA_IO_BF16, 0,
+                               None, 0, None)
+    assert rc == kla.KLA_ERR_INVALID_ARG
+    rc = lib.kla_loglinear_fwd(*args, 8, 1e-6, None, 1, 100, 1, 96, 128, 64, kla.KLA_IO_BF16, 0,
+                               None, 0, None)
+    assert rc == kla.KLA_ERR_UNSUPPORTED
+    assert kla.kla_loglinear_workspace_bytes(1, 100, 1, 96, 128) == 0
+    assert kla.kla_loglinear_workspace_bytes(1, 4096, 2, 128, 128) > 0
