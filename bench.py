@@ -8,8 +8,9 @@ one step = one call over that batch.  The long-context prefill
 kla_decode_step) are timed in the same run and reported under "secondary", with
 the training shape under Gated DeltaNet's step-size rule (kla_chunk_fwd_ex with
 KLA_BETA_DIRECT, unit-norm keys), the backward (kla_chunk_bwd) of the
-training shape, and DeltaKATA (PSD features of 15-value q and k, then
-kla_chunk_fwd) on the training shape.
+training shape, DeltaKATA (PSD features of 15-value q and k, then
+kla_chunk_fwd) and the Log-Linear gated delta rule (kla_loglinear_fwd), both
+on the training shape.
 
 Timing: W untimed warm-up steps, then exactly K timed steps, each between
 CUDA events on the launching stream; L2 is flushed (a 512 MiB write) between
@@ -423,6 +424,50 @@ def bench_deltakata(case, p, K, W, flush, peaks, stream):
     return res
 
 
+def loglinear_work(case, L):
+    """Algorithmic bytes of one kla_loglinear_fwd call: q, k, v, o, g, eta and
+    the L level weights once per token-head.  Flops: those of the plain
+    prefill (a lower bound; the level states add O(log T) per chunk)."""
+    w = prefill_work(case)
+    th = case.B * case.T * case.H
+    per_tok = w["per_token_head_bytes"] + 4 * L
+    return dict(bytes=th * per_tok, flops=w["flops"], tokens=case.B * case.T, token_heads=th,
+                per_token_head_bytes=per_tok)
+
+
+def bench_loglinear(case, K, W, flush, peaks, stream):
+    """Time kla_loglinear_fwd on ``case`` with random level weights."""
+    import chunked_delta_rule_kla_gb300 as kla
+    inp = kla_inputs.make_prefill(case, device="cuda")
+    B, T, H, dk, dv = case.B, case.T, case.H, case.dk, case.dv
+    L = kla.kla_loglinear_num_levels(T)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(case.seed + 3000)
+    lam = torch.empty((B, T, H, L), device="cuda").uniform_(0.2, 1.5, generator=gen)
+    o = torch.empty((B, T, H, dv), dtype=inp["q"].dtype, device="cuda")
+    io = kla.KLA_IO_BF16 if case.io == "bf16" else kla.KLA_IO_FP32
+    ws = torch.empty(kla.kla_loglinear_workspace_bytes(B, T, H, dk, dv, case.chunk, io),
+                     dtype=torch.uint8, device="cuda")
+
+    def step():
+        kla.kla_loglinear_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["eta"], lam, inp["eps"], o,
+                              ws, stream=stream)
+
+    barrier()
+    ms = timed_steps(step, K, W, flush, stream)
+    barrier()
+    work = loglinear_work(case, L)
+    _, slowest_s = job_throughput(work["tokens"], sum(ms) / len(ms) * 1e-3)
+    mean_ms = slowest_s * 1e3
+    res = dict(ms_per_step=mean_ms, tokens_per_s=work["tokens"] / (mean_ms * 1e-3), levels=L,
+               roofline=dict(roofline(work, mean_ms * 1e-3, peaks, TRAFFIC_BYTES.get("loglinear_" + case.name)),
+                             scope="one kla_loglinear_fwd call: its three launches (chunk, carry, output)",
+                             peak_kind="burst copy bandwidth"),
+               launches=3 * K, min_ms=min(ms))
+    del inp, lam, o, ws
+    return res
+
+
 def bench_decode(case, K_loops, W_loops, peaks, stream, n_states=4, e2e=True):
     """Times `steps` consecutive kla_decode_step calls per loop.  The calls
     rotate over n_states independent state buffers (like the layers of a
@@ -526,7 +571,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-heads", type=int, default=64)
     ap.add_argument("--decode-loops", type=int, default=3)
-    ap.add_argument("--only", choices=["train", "long", "gdn", "decode", "bwd", "deltakata"], default=None,
+    ap.add_argument("--only", choices=["train", "long", "gdn", "decode", "bwd", "deltakata", "loglinear"],
+                    default=None,
                     help="time one workload only (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
     args = ap.parse_args()
@@ -551,7 +597,12 @@ def main():
 
     e2e = not args.no_e2e
     if args.only is not None:
-        if args.only == "deltakata":
+        if args.only == "loglinear":
+            lr2 = bench_loglinear(kla_inputs.TRAIN, args.steps, args.warmup, flush, peaks, stream)
+            line = dict(workload="loglinear_" + kla_inputs.TRAIN.name, tokens_per_s=lr2["tokens_per_s"],
+                        ms_per_step=lr2["ms_per_step"], roofline=lr2["roofline"],
+                        gpu_launches=lr2["launches"])
+        elif args.only == "deltakata":
             kr = bench_deltakata(kla_inputs.TRAIN, 15, args.steps, args.warmup, flush, peaks, stream)
             line = dict(workload="deltakata_p15_" + kla_inputs.TRAIN.name, tokens_per_s=kr["tokens_per_s"],
                         ms_per_step=kr["ms_per_step"], roofline=kr["roofline"],
@@ -601,6 +652,10 @@ def main():
         secondary["deltakata_train_prefill"] = dict(
             workload="deltakata_p15_" + kla_inputs.TRAIN.name, p=15, d_feat=kla_inputs.TRAIN.dk,
             tokens_per_s=kr["tokens_per_s"], ms_per_step=kr["ms_per_step"], roofline=kr["roofline"])
+        lr2 = bench_loglinear(kla_inputs.TRAIN, max(5, args.steps // 4), 3, flush, peaks, stream)
+        secondary["loglinear_train_prefill"] = dict(
+            workload="loglinear_" + kla_inputs.TRAIN.name, levels=lr2["levels"],
+            tokens_per_s=lr2["tokens_per_s"], ms_per_step=lr2["ms_per_step"], roofline=lr2["roofline"])
         dc = kla_inputs.DECODE
         dr = bench_decode(dc, args.decode_loops, 3, peaks, stream, e2e=e2e)
         secondary["decode"] = dict(workload=dc.name, tokens_per_s=dr["tokens_per_s"],
