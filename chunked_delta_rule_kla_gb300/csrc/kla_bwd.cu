@@ -263,6 +263,20 @@ __global__ void __launch_bounds__(512) bwd_carry_kernel(BwdParams p) {
         const size_t ldk = (size_t)p.H * DK;
         const float gC = __ldg(rec + L.gamma + C - 1);
         __syncthreads();
+        // the next chunk's record and K rows into L2 while this one runs
+        if (it + 1 < p.nchunks) {
+            const int cn = rev ? c - 1 : c + 1;
+            const float* rn = p.rec + ((size_t)bh * p.nchunks + cn) * L.floats;
+            if (tid == 0) {
+                prefetch_l2(rn, sizeof(float) * C);
+                prefetch_l2(rn + L.Wk, sizeof(float) * C * DK);
+                prefetch_l2(rn + (rev ? L.PdO : L.U), sizeof(float) * C * DV);
+                if (rev) prefetch_l2(rn + L.L, sizeof(float) * DK * DV);
+            }
+            const int r = tid - 32;
+            if (r >= 0 && r < min(C, p.T - cn * C))
+                prefetch_l2(static_cast<const TIO*>(p.k) + tok_index(p, bh, cn, r) * DK, sizeof(TIO) * DK);
+        }
         if (tid < C) veC[tid] = __expf(gC - __ldg(rec + L.gamma + tid));
         // keep the state as [DK][DV]: four columns of one row per thread, lanes
         // along the rows (conflict-free reads of S^T)

@@ -203,6 +203,16 @@ __global__ void __launch_bounds__(512) ll_carry_kernel(LLParams p) {
         float* Snext = p.states + (item + 1) * p.nbits * SS;        // slots of chunk c + 1
         const int b = __ffs(c + 1) - 1;                              // lowest set bit of c + 1
         __syncthreads();
+        // the next chunk's record and K rows into L2 while this one runs
+        if (c + 2 < p.nchunks) {
+            const float* rn = rec + RF;
+            if (tid == 0) {
+                prefetch_l2(rn, sizeof(float) * (C + (size_t)C * DK + (size_t)C * DV));
+            }
+            const int r = tid - 32;
+            if (r >= 0 && r < min(C, p.T - (c + 1) * C))
+                prefetch_l2(static_cast<const TIO*>(p.k) + ll_tok(p, bh, c + 1, r) * DK, sizeof(TIO) * DK);
+        }
         if (tid < C) veC[tid] = __expf(gC - __ldg(rec + tid));
         for_f4(rWk, C * DK, [&](int i, const float* x) {
             const int r = (4 * i) / DK, j = (4 * i) % DK;

@@ -335,5 +335,17 @@ __device__ __forceinline__ void stage_cols(float* dst, int ldd, const T* src, si
     }
 }
 
+// Asks L2 to fetch `bytes` (a multiple of 16) from 16-byte-aligned global
+// memory, in pieces of at most 16 KB; nothing waits for it.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    const char* c = static_cast<const char*>(p);
+    for (uint32_t off = 0; off < bytes; off += 16384u) {
+        const uint32_t n = bytes - off < 16384u ? bytes - off : 16384u;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(__cvta_generic_to_global(c + off)),
+                     "r"(n)
+                     : "memory");
+    }
+}
+
 }  // namespace tile
 }  // namespace kla
