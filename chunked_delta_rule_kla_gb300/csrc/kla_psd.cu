@@ -94,17 +94,28 @@ __global__ void __launch_bounds__(256) psd_features_kernel(const T* __restrict__
             fs[u] = 0.f;
         }
     }
+    // four rows per half-warp in flight: their loads go out before any is used
     const int64_t nhalf = ((int64_t)gridDim.x * blockDim.x) >> 4;
-    for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4; row < rows; row += nhalf) {
-        const float xv = sub < p ? ldx<T>(x + row * p + sub) : 0.f;
-        float v[PER];
+    for (int64_t row0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4; row0 < rows;
+         row0 += 4 * nhalf) {
+        float xv[4];
 #pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            const float xi = __shfl_sync(mask, xv, fi[u], 16);
-            const float xj = __shfl_sync(mask, xv, fj[u], 16);
-            v[u] = fs[u] * xi * xj;
+        for (int m = 0; m < 4; ++m) {
+            const int64_t row = row0 + m * nhalf;
+            xv[m] = (sub < p && row < rows) ? ldx<T>(x + row * p + sub) : 0.f;
         }
-        FeatStore<T, PER>::st(y + row * d_out + PER * sub, v);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int64_t row = row0 + m * nhalf;
+            float v[PER];
+#pragma unroll
+            for (int u = 0; u < PER; ++u) {
+                const float xi = __shfl_sync(mask, xv[m], fi[u], 16);
+                const float xj = __shfl_sync(mask, xv[m], fj[u], 16);
+                v[u] = fs[u] * xi * xj;
+            }
+            if (row < rows) FeatStore<T, PER>::st(y + row * d_out + PER * sub, v);
+        }
     }
 }
 
