@@ -199,7 +199,9 @@ __global__ void __launch_bounds__(512) ll_carry_kernel(LLParams p) {
         const TIO* K = static_cast<const TIO*>(p.k) + ll_tok(p, bh, c, 0) * DK;
         const size_t ldk = (size_t)p.H * DK;
         const float gC = __ldg(rec + C - 1), GC = __expf(gC);
-        const float* Scur = p.states + item * p.nbits * SS;         // slots of chunk c
+        // slots of chunk c: written by this kernel one chunk earlier, so read with
+        // ordinary (coherent) loads, never through the read-only path
+        const float* Scur = p.states + item * p.nbits * SS;
         float* Snext = p.states + (item + 1) * p.nbits * SS;        // slots of chunk c + 1
         const int b = __ffs(c + 1) - 1;                              // lowest set bit of c + 1
         __syncthreads();
@@ -241,16 +243,17 @@ __global__ void __launch_bounds__(512) ll_carry_kernel(LLParams p) {
                     const int r = (4 * i) / DK, a = (4 * i) % DK;
                     float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
                     for (int l = 0; l < b; ++l) {
-                        const float4 x = __ldg(reinterpret_cast<const float4*>(Scur + l * SS) + i);
+                        const float4 x = reinterpret_cast<const float4*>(Scur + l * SS)[i];
                         m.x += x.x; m.y += x.y; m.z += x.z; m.w += x.w;
                     }
                     *reinterpret_cast<float4*>(sSt + r * ldS + a) = m;
                 }
             } else {
-                for_f4(Scur + j * SS, DK * DV, [&](int i, const float* x) {
+                const float4* src = reinterpret_cast<const float4*>(Scur + j * SS);
+                for (int i = tid; i < DK * DV / 4; i += nt) {
                     const int r = (4 * i) / DK, a = (4 * i) % DK;
-                    *reinterpret_cast<float4*>(sSt + r * ldS + a) = make_float4(x[0], x[1], x[2], x[3]);
-                });
+                    *reinterpret_cast<float4*>(sSt + r * ldS + a) = src[i];
+                }
             }
             __syncthreads();
             // W^T = -S^T Wk^T (+ U^T for the merged level)

@@ -14,8 +14,20 @@ constexpr int kPad = 4;        // row padding (floats) of shared-memory tiles
 constexpr int kLdCC = C + kPad;
 
 template <typename T> __device__ __forceinline__ float ldf(const T* p);
-template <> __device__ __forceinline__ float ldf<float>(const float* p) { return *p; }
+template <> __device__ __forceinline__ float ldf<float>(const float* p) {
+    if (__isShared(p)) {
+        float v;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"((uint32_t)__cvta_generic_to_shared(p)));
+        return v;
+    }
+    return *p;
+}
 template <> __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16* p) {
+    if (__isShared(p)) {
+        unsigned short v;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"((uint32_t)__cvta_generic_to_shared(p)));
+        return __uint_as_float((uint32_t)v << 16);
+    }
     return __bfloat162float(*p);
 }
 template <typename T> __device__ __forceinline__ void stf(T* p, float x);
@@ -45,14 +57,30 @@ __device__ __forceinline__ float warp_sum(float s) {
     return s;
 }
 
+// 16 bytes at p: with shared-memory addresses through ld.shared, so that the
+// load is not tracked as a generic (global-path) access
+__device__ __forceinline__ uint4 ld16(const void* p) {
+    if (__isShared(p)) {
+        uint4 r;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                     : "r"((uint32_t)__cvta_generic_to_shared(p)));
+        return r;
+    }
+    return *reinterpret_cast<const uint4*>(p);
+}
+
 // Eight consecutive values of one storage row (16-byte aligned), as fp32.
 template <typename T> __device__ __forceinline__ void ld8(const T* p, float (&x)[8]);
 template <> __device__ __forceinline__ void ld8<float>(const float* p, float (&x)[8]) {
-    const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    const uint4 a = ld16(p), b = ld16(p + 4);
+    x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+    x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+    x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+    x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
 }
 template <> __device__ __forceinline__ void ld8<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[8]) {
-    const uint4 r = *reinterpret_cast<const uint4*>(p);
+    const uint4 r = ld16(p);
     const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
