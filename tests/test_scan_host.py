@@ -125,3 +125,30 @@ def test_loglinear_levels_and_errors():
     assert rc == kla.KLA_ERR_UNSUPPORTED
     assert kla.kla_loglinear_workspace_bytes(1, 100, 1, 96, 128) == 0
     assert kla.kla_loglinear_workspace_bytes(1, 4096, 2, 128, 128) > 0
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128)])
+def test_backward_workspace_formula(dk, dv):
+    # per chunk-head: the prep record (gamma, beta, kk, T, Wk, U, P^T dO, L), the
+    # start state and its gradient, W and dW; plus the error record
+    kla = _kla()
+    B, T, H = 2, 1000, 3
+    items = B * H * -(-T // 64)
+    rec = 3 * 64 + 64 * 64 + 64 * dk + 2 * 64 * dv + dk * dv
+    body = 4 * items * (rec + 2 * dk * dv + 2 * 64 * dv)
+    assert kla.kla_chunk_bwd_workspace_bytes(B, T, H, dk, dv) == 256 + -(-body // 256) * 256
+    assert kla.kla_chunk_bwd_workspace_bytes(B, T, H, 96, dv) == 0
+    assert kla.kla_chunk_bwd_workspace_bytes(1, 64, 65536, dk, dv) == 0     # B*H over 65535
+
+
+@pytest.mark.parametrize("T", [1, 64, 65, 4096, 4097])
+def test_loglinear_workspace_formula(T):
+    # per chunk-head: gamma, Wk, U and the chunk's own output, then one state
+    # slot per bit of the largest chunk index
+    kla = _kla()
+    B, H, dk, dv = 1, 2, 128, 64
+    nch = -(-T // 64)
+    bits = max(1, (nch - 1).bit_length())
+    items = B * H * nch
+    body = 4 * items * (64 + 64 * dk + 2 * 64 * dv + bits * dk * dv)
+    assert kla.kla_loglinear_workspace_bytes(B, T, H, dk, dv) == 256 + -(-body // 256) * 256
