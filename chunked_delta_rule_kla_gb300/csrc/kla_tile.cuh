@@ -30,11 +30,6 @@ template <> __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloa
     }
     return __bfloat162float(*p);
 }
-template <typename T> __device__ __forceinline__ void stf(T* p, float x);
-template <> __device__ __forceinline__ void stf<float>(float* p, float x) { *p = x; }
-template <> __device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16* p, float x) {
-    *p = __float2bfloat16_rn(x);
-}
 
 __device__ __forceinline__ uint32_t tf32_bits(float x) {
     uint32_t r;
