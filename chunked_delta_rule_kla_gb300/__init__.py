@@ -50,6 +50,7 @@ EXPORTED_SYMBOLS = (
     "kla_loglinear_num_levels",
     "kla_loglinear_workspace_bytes",
     "kla_loglinear_fwd",
+    "kla_loglinear_decode_step",
     "kla_workspace_check",
     "kla_status_string",
 )
@@ -121,6 +122,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kla_loglinear_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, f, vp,
                                           i, i, i, i, i, i, i, i, vp, sz, vp]
         lib.kla_loglinear_fwd.restype = i
+        lib.kla_loglinear_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i, f, vp, i, vp,
+                                                  i, i, i, i, i, i, vp]
+        lib.kla_loglinear_decode_step.restype = i
         lib.kla_workspace_check.argtypes = [vp, sz, vp]
         lib.kla_workspace_check.restype = i
         lib.kla_status_string.argtypes = [i]
@@ -324,6 +328,23 @@ def kla_loglinear_fwd(q, k, v, g, eta, lam, eps, o, workspace, beta=KLA_BETA_KAC
         raise KlaError(rc, "kla_loglinear_fwd")
 
 
+def kla_loglinear_decode_step(q, k, v, g, eta, lam, eps, states, t, o, beta=KLA_BETA_KACZMARZ,
+                              stream=None) -> None:
+    """One Log-Linear decode step for token ``t`` (see include/kla.h): states
+    [B,H,L,dk,dv] fp32 (zero-filled before t = 0) are updated in place."""
+    B, H, dk = k.shape
+    dv = v.shape[-1]
+    if tuple(states.shape[:2]) != (B, H) or tuple(states.shape[3:]) != (dk, dv) or lam.shape != states.shape[:3]:
+        raise ValueError("states must be [B,H,L,dk,dv] and lam [B,H,L]")
+    rc = load_library().kla_loglinear_decode_step(
+        _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g", torch.float32),
+        _ptr(eta, "eta", torch.float32), _ptr(lam, "lam", torch.float32), int(lam.shape[2]),
+        float(eps), _ptr(states, "states", torch.float32), int(t), _ptr(o, "o"), B, H, dk, dv,
+        _io_of(q), int(beta), _stream(stream))
+    if rc != KLA_OK:
+        raise KlaError(rc, "kla_loglinear_decode_step")
+
+
 def kla_chunk_fwd_noalloc(q, k, v, g, eta, eps, h0, o, hT, chunk=64, stream=None) -> None:
     """kla_chunk_fwd without a workspace, for callers that must not allocate
     device memory: the scratch is an array built into the library (see
@@ -521,6 +542,7 @@ __all__ = [
     "kla_chunk_bwd", "kla_chunk_bwd_workspace_bytes", "chunk_bwd", "kla_chunk", "KLAChunk",
     "kla_psd_features", "kla_psd_features_bwd", "psd_features", "PSDFeatures", "deltakata",
     "kla_loglinear_num_levels", "kla_loglinear_workspace_bytes", "kla_loglinear_fwd", "loglinear_fwd",
+    "kla_loglinear_decode_step",
     "kla_workspace_check",
     "kla_status_string", "chunk_fwd", "decode_step", "alloc_workspace", "load_library",
     "KlaError", "EXPORTED_SYMBOLS", "KLA_IO_BF16", "KLA_IO_FP32",

@@ -257,6 +257,28 @@ kla_status kla_loglinear_fwd(const void* q, const void* k, const void* v, const 
                                                io == KLA_IO_BF16, beta == KLA_BETA_DIRECT, scratch, st));
 }
 
+kla_status kla_loglinear_decode_step(const void* q, const void* k, const void* v, const float* g,
+                                     const float* eta, const float* lambda, int L, float eps,
+                                     float* states, int t, void* o, int B, int H, int dk, int dv,
+                                     kla_io_dtype io, kla_beta_mode beta, void* stream) {
+    if (B < 0 || H < 0 || t < 0 || check_io(io) != KLA_OK) return KLA_ERR_INVALID_ARG;
+    if (beta != KLA_BETA_KACZMARZ && beta != KLA_BETA_DIRECT) return KLA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f)) return KLA_ERR_INVALID_ARG;
+    if (t == INT32_MAX || L < kla_loglinear_num_levels(t + 1) || L > 32) return KLA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return KLA_ERR_UNSUPPORTED;
+    if ((int64_t)B * H > 65535) return KLA_ERR_UNSUPPORTED;
+    if ((int64_t)B * H == 0) return KLA_OK;
+    if (!q || !k || !v || !g || !eta || !lambda || !states || !o) return KLA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, o};
+    for (const void* p : ptrs)
+        if (!aligned4(p)) return KLA_ERR_INVALID_ARG;
+    if (!aligned4(g) || !aligned4(eta) || !aligned4(lambda) || !aligned16(states))
+        return KLA_ERR_INVALID_ARG;
+    return to_status(kla::launch_loglinear_decode(q, k, v, g, eta, lambda, L, eps, states, t, o, B, H, dk,
+                                                  dv, io == KLA_IO_BF16, beta == KLA_BETA_DIRECT,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kla_status kla_psd_features(const void* x, void* y, int64_t rows, int p, int d_out,
                             kla_io_dtype io, void* stream) {
     if (rows < 0 || p < 1 || check_io(io) != KLA_OK) return KLA_ERR_INVALID_ARG;

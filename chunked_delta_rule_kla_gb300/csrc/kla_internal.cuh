@@ -105,6 +105,11 @@ cudaError_t launch_loglinear_fwd(const void* q, const void* k, const void* v, co
                                  int T, int H, int DK, int DV, bool bf16, bool beta_direct,
                                  float* scratch, cudaStream_t stream);
 
+cudaError_t launch_loglinear_decode(const void* q, const void* k, const void* v, const float* g,
+                                    const float* eta, const float* lam, int L, float eps, float* states,
+                                    int t, void* o, int B, int H, int DK, int DV, bool bf16,
+                                    bool beta_direct, cudaStream_t stream);
+
 // Rank-one PSD features of DeltaKATA and their derivative (kla_psd.cu):
 // rows of p values in, rows of d_out features out (and back).
 cudaError_t launch_psd_features(const void* x, void* y, int64_t rows, int p, int d_out, bool bf16,

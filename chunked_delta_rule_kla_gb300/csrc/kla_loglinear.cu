@@ -398,7 +398,148 @@ cudaError_t ll_launch(const LLParams& p, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- decode
+// One token for every head: the O(log T) decode of the Log-Linear page.
+// states [B, H, L, dk, dv] hold the bucket states relative to token t - 1:
+// level 0 is token t - 1 itself and level j + 1 is non-empty when bit j of
+// t - 1 is set.  For token t every non-empty state takes the transition
+// a (I - beta k k^T); with b the lowest set bit of t, levels 0..b merge into
+// level b + 1 (always empty before: bit b of t - 1 is clear) and the write
+// beta k v^T becomes level 0.  o = sum_l lambda^(l) S^(l)^T q.
+// A CTA owns 16 columns of one head; thread (row group, column) holds
+// dk / 16 rows of its column.
+template <typename TIO>
+__global__ void __launch_bounds__(256) ll_decode_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k,
+                                                        const TIO* __restrict__ v, const float* __restrict__ g,
+                                                        const float* __restrict__ eta,
+                                                        const float* __restrict__ lam, int L, float eps,
+                                                        int beta_direct, float* __restrict__ states, int t,
+                                                        TIO* __restrict__ o, int H, int DK, int DV) {
+    __shared__ float sk[128], sq[128], sred[16][17], slam[32];
+    __shared__ float sscal[2];
+    const int bh = blockIdx.y, col0 = blockIdx.x * 16;
+    const int tid = threadIdx.x, col = tid & 15, rg = tid >> 4;
+    const int rows = DK / 16, r0 = rg * rows;
+    for (int i = tid; i < DK; i += blockDim.x) {
+        sk[i] = ldf<TIO>(k + (size_t)bh * DK + i);
+        sq[i] = ldf<TIO>(q + (size_t)bh * DK + i);
+    }
+    for (int i = tid; i < L; i += blockDim.x) slam[i] = lam[(size_t)bh * L + i];
+    __syncthreads();
+    if (tid < 32) {
+        float kk = 0.f, qk = 0.f;
+        for (int i = tid; i < DK; i += 32) {
+            kk += sk[i] * sk[i];
+            qk += sq[i] * sk[i];
+        }
+        kk = warp_sum(kk);
+        qk = warp_sum(qk);
+        if (tid == 0) {
+            const float e = eta[bh];
+            sscal[0] = beta_direct ? e : e / (kk + eps);
+            sscal[1] = qk;
+        }
+    }
+    __syncthreads();
+    const float a = __expf(g[bh]), beta = sscal[0], qk = sscal[1];
+    const size_t SS = (size_t)DK * DV;
+    float* st = states + (size_t)bh * L * SS;
+    // column reduction over the 16 row groups
+    auto colsum = [&](float x) {
+        sred[rg][col] = x;
+        __syncthreads();
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s += sred[i][col];
+        __syncthreads();
+        return s;
+    };
+    float out = 0.f;                       // this thread's column of o (row group 0 keeps it)
+    float merged[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) merged[i] = 0.f;
+    const int b = t > 0 ? __ffs(t) - 1 : -1;
+    if (t > 0) {
+        const int prev = t - 1;
+        for (int l = 0; l < L; ++l) {
+            const bool present = l == 0 || ((prev >> (l - 1)) & 1);
+            if (!present) continue;
+            float* S = st + (size_t)l * SS;
+            float x[8];
+            float dot = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i < rows) {
+                    x[i] = S[(size_t)(r0 + i) * DV + col0 + col];
+                    dot += sk[r0 + i] * x[i];
+                }
+            }
+            const float kx = colsum(dot);
+            float y = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i < rows) {
+                    x[i] = a * (x[i] - beta * sk[r0 + i] * kx);
+                    if (l <= b) merged[i] += x[i];
+                    else y += sq[r0 + i] * x[i];
+                }
+            }
+            if (l > b) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (i < rows) S[(size_t)(r0 + i) * DV + col0 + col] = x[i];
+                out += slam[l] * colsum(y);
+            } else if (l > 0) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (i < rows) S[(size_t)(r0 + i) * DV + col0 + col] = 0.f;   // merged away
+            }
+        }
+        // the merged level b + 1
+        float* S = st + (size_t)(b + 1) * SS;
+        float y = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i < rows) {
+                S[(size_t)(r0 + i) * DV + col0 + col] = merged[i];
+                y += sq[r0 + i] * merged[i];
+            }
+        }
+        out += slam[b + 1] * colsum(y);
+    }
+    // the new write: level 0 = beta k v^T; its readout is beta (q . k) v
+    const float vc = ldf<TIO>(v + (size_t)bh * DV + col0 + col);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (i < rows) st[(size_t)(r0 + i) * DV + col0 + col] = beta * sk[r0 + i] * vc;
+    out += slam[0] * beta * qk * vc;
+    if (rg == 0) {
+        if constexpr (sizeof(TIO) == 2)
+            o[(size_t)bh * DV + col0 + col] = __float2bfloat16_rn(out);
+        else
+            o[(size_t)bh * DV + col0 + col] = out;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_loglinear_decode(const void* q, const void* k, const void* v, const float* g,
+                                    const float* eta, const float* lam, int L, float eps, float* states,
+                                    int t, void* o, int B, int H, int DK, int DV, bool bf16,
+                                    bool beta_direct, cudaStream_t stream) {
+    const dim3 grid(DV / 16, B * H);
+    if (bf16) {
+        using bf = __nv_bfloat16;
+        ll_decode_kernel<bf><<<grid, 256, 0, stream>>>(
+            static_cast<const bf*>(q), static_cast<const bf*>(k), static_cast<const bf*>(v), g, eta, lam, L,
+            eps, beta_direct ? 1 : 0, states, t, static_cast<bf*>(o), H, DK, DV);
+    } else {
+        ll_decode_kernel<float><<<grid, 256, 0, stream>>>(
+            static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v), g, eta,
+            lam, L, eps, beta_direct ? 1 : 0, states, t, static_cast<float*>(o), H, DK, DV);
+    }
+    return cudaGetLastError();
+}
 
 int loglinear_state_bits(int T) {
     const int nch = (T + C - 1) / C;

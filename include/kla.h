@@ -240,6 +240,27 @@ KLA_API kla_status kla_loglinear_fwd(const void* q, const void* k, const void* v
                                      size_t workspace_bytes, void* stream);
 
 /*
+ * One Log-Linear decode step (token t) for B*H heads, O(log T) per token: the
+ * Fenwick update of the Log-Linear page.  `states` [B, H, L, dk, dv] fp32
+ * holds the bucket states relative to token t - 1 (level 0: token t - 1;
+ * level j + 1: non-empty when bit j of t - 1 is set); the caller zero-fills it
+ * before t = 0 and passes t = 0, 1, 2, ... in order.  Every non-empty state
+ * takes the transition a_t (I - beta_t k_t k_t^T); with b the lowest set bit
+ * of t, levels 0..b merge into level b + 1, the write beta_t k_t v_t^T becomes
+ * level 0, and o_t = sum_l lambda_t^(l) S^(l)^T q_t.  Decoding a whole
+ * sequence this way gives kla_loglinear_fwd's outputs.
+ *
+ *  q, k : [B, H, dk];  v, o : [B, H, dv] (I/O dtype);  g, eta : fp32 [B, H]
+ *  lambda : fp32 [B, H, L], kla_loglinear_num_levels(t + 1) <= L <= 32
+ *  dk, dv : 64 or 128; B*H <= 65535.
+ */
+KLA_API kla_status kla_loglinear_decode_step(const void* q, const void* k, const void* v,
+                                             const float* g, const float* eta,
+                                             const float* lambda, int L, float eps, float* states,
+                                             int t, void* o, int B, int H, int dk, int dv,
+                                             kla_io_dtype io, kla_beta_mode beta, void* stream);
+
+/*
  * DeltaKATA's keys and queries: the rank-one PSD feature psi(u) = u u^T of
  * each row u ("Kernelized Linear Attention: breaking the capacity wall via
  * symmetric cones", section 2.2; section 4 runs the delta rule on it).

@@ -79,3 +79,25 @@ def test_loglinear_unit_weights_equal_chunk_fwd():
 def test_loglinear_training_shape_sampled_heads():
     # B1 H4 T4096 d128 bf16: 64 chunks, level states up to bit 5; two heads checked
     _check("bf16", 1, 4096, 4, 128, 128, 740, heads=[0, 3])
+
+
+@pytest.mark.parametrize("io", ["fp32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 128)])
+def test_loglinear_decode_steps_match_oracle(io, dk, dv):
+    # T decode steps from zero states give the Log-Linear outputs of the whole sequence
+    kla = _kla()
+    B, T, H = 2, 150, 3
+    inp, lam = _inputs(io, B, T, H, dk, dv, 750 + dk)
+    L = lam.shape[-1]
+    states = torch.zeros((B, H, L, dk, dv), device="cuda")
+    outs = []
+    for t in range(T):
+        pick = lambda n: inp[n][:, t].contiguous()
+        o = torch.empty((B, H, dv), dtype=inp["q"].dtype, device="cuda")
+        kla.kla_loglinear_decode_step(pick("q"), pick("k"), pick("v"), pick("g"), pick("eta"),
+                                      lam[:, t].contiguous(), inp["eps"], states, t, o)
+        outs.append(o)
+    torch.cuda.synchronize()
+    ref = oracle.kla_oracle_loglinear_forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["eta"], lam,
+                                              inp["eps"])
+    assert rel_err(torch.stack(outs, 1), ref) <= TOL[io]

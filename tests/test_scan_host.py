@@ -152,3 +152,18 @@ def test_loglinear_workspace_formula(T):
     items = B * H * nch
     body = 4 * items * (64 + 64 * dk + 2 * 64 * dv + bits * dk * dv)
     assert kla.kla_loglinear_workspace_bytes(B, T, H, dk, dv) == 256 + -(-body // 256) * 256
+
+
+def test_loglinear_decode_argument_errors():
+    kla = _kla()
+    lib = kla.load_library()
+    args = [None] * 6
+    # token 100 needs 1 + ceil(log2 101) = 8 levels; more than 32 are refused
+    rc = lib.kla_loglinear_decode_step(*args, 7, 1e-6, None, 100, None, 1, 1, 128, 128, kla.KLA_IO_BF16, 0, None)
+    assert rc == kla.KLA_ERR_INVALID_ARG
+    rc = lib.kla_loglinear_decode_step(*args, 33, 1e-6, None, 100, None, 1, 1, 128, 128, kla.KLA_IO_BF16, 0, None)
+    assert rc == kla.KLA_ERR_INVALID_ARG
+    rc = lib.kla_loglinear_decode_step(*args, 8, 1e-6, None, 100, None, 1, 1, 96, 128, kla.KLA_IO_BF16, 0, None)
+    assert rc == kla.KLA_ERR_UNSUPPORTED
+    rc = lib.kla_loglinear_decode_step(*args, 8, 1e-6, None, -1, None, 1, 1, 128, 128, kla.KLA_IO_BF16, 0, None)
+    assert rc == kla.KLA_ERR_INVALID_ARG
