@@ -10,7 +10,8 @@ the training shape under Gated DeltaNet's step-size rule (kla_chunk_fwd_ex with
 KLA_BETA_DIRECT, unit-norm keys), the backward (kla_chunk_bwd) of the
 training shape, DeltaKATA (PSD features of 15-value q and k, then
 kla_chunk_fwd) and the Log-Linear gated delta rule (kla_loglinear_fwd), both
-on the training shape.
+on the training shape, and Log-Linear decoding (kla_loglinear_decode_step,
+1024 tokens of the decode workload's heads).
 
 Timing: W untimed warm-up steps, then exactly K timed steps, each between
 CUDA events on the launching stream; L2 is flushed (a 512 MiB write) between
@@ -468,6 +469,59 @@ def bench_loglinear(case, K, W, flush, peaks, stream):
     return res
 
 
+def bench_loglinear_decode(case, steps, peaks, stream):
+    """Time kla_loglinear_decode_step over tokens 0 .. steps-1 of ``case``'s
+    heads (states zero at token 0).  Algorithmic bytes of token t: each
+    non-empty bucket state read and written (popcount(t-1) + 1 of them for
+    t > 0), the merged and new states written, q, k, v, o, g, eta, lambda."""
+    import chunked_delta_rule_kla_gb300 as kla
+    B, H, dk, dv = case.B, case.H, case.dk, case.dv
+    L = kla.kla_loglinear_num_levels(steps)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(case.seed + 4000)
+    dt = torch.bfloat16 if case.io == "bf16" else torch.float32
+    q = torch.randn((steps, B, H, dk), generator=gen, device="cuda").to(dt)
+    k = torch.nn.functional.normalize(torch.randn((steps, B, H, dk), generator=gen, device="cuda"), dim=-1).to(dt)
+    v = torch.randn((steps, B, H, dv), generator=gen, device="cuda").to(dt)
+    g = torch.nn.functional.logsigmoid(torch.randn((steps, B, H), generator=gen, device="cuda") + 2.0)
+    eta = torch.sigmoid(torch.randn((steps, B, H), generator=gen, device="cuda"))
+    lam = torch.empty((steps, B, H, L), device="cuda").uniform_(0.2, 1.5, generator=gen)
+    states = torch.zeros((B, H, L, dk, dv), device="cuda")
+    o = torch.empty((B, H, dv), dtype=dt, device="cuda")
+    esz = 2 if case.io == "bf16" else 4
+    sbytes = dk * dv * 4
+    total = 0
+    for t in range(steps):
+        touched = (bin(t - 1).count("1") + 1) * 2 * sbytes + sbytes if t > 0 else 0
+        total += B * H * (touched + sbytes + esz * (2 * dk + 2 * dv) + 8 + 4 * L)
+
+    def run():
+        for t in range(steps):
+            kla.kla_loglinear_decode_step(q[t], k[t], v[t], g[t], eta[t], lam[t], 1e-6, states, t, o,
+                                          stream=stream)
+
+    states.zero_()
+    run()                                   # warm-up pass
+    states.zero_()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    sec = e0.elapsed_time(e1) * 1e-3
+    work = dict(bytes=total, flops=0)
+    res = dict(us_per_step=sec / steps * 1e6, tokens_per_s=B * steps / sec, levels=L,
+               roofline=dict(roofline(work, sec, peaks),
+                             scope=f"{steps} kla_loglinear_decode_step calls from token 0, averaged",
+                             peak_kind="burst copy bandwidth"),
+               launches=steps)
+    del q, k, v, g, eta, lam, states, o
+    return res
+
+
 def bench_decode(case, K_loops, W_loops, peaks, stream, n_states=4, e2e=True):
     """Times `steps` consecutive kla_decode_step calls per loop.  The calls
     rotate over n_states independent state buffers (like the layers of a
@@ -571,7 +625,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-heads", type=int, default=64)
     ap.add_argument("--decode-loops", type=int, default=3)
-    ap.add_argument("--only", choices=["train", "long", "gdn", "decode", "bwd", "deltakata", "loglinear"],
+    ap.add_argument("--only", choices=["train", "long", "gdn", "decode", "bwd", "deltakata", "loglinear",
+                                       "lldecode"],
                     default=None,
                     help="time one workload only (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
@@ -597,7 +652,12 @@ def main():
 
     e2e = not args.no_e2e
     if args.only is not None:
-        if args.only == "loglinear":
+        if args.only == "lldecode":
+            dr2 = bench_loglinear_decode(kla_inputs.DECODE, 1024, peaks, stream)
+            line = dict(workload="loglinear_decode_bf16_B64H16d128_x1024", tokens_per_s=dr2["tokens_per_s"],
+                        us_per_step=dr2["us_per_step"], roofline=dr2["roofline"],
+                        gpu_launches=dr2["launches"])
+        elif args.only == "loglinear":
             lr2 = bench_loglinear(kla_inputs.TRAIN, args.steps, args.warmup, flush, peaks, stream)
             line = dict(workload="loglinear_" + kla_inputs.TRAIN.name, tokens_per_s=lr2["tokens_per_s"],
                         ms_per_step=lr2["ms_per_step"], roofline=lr2["roofline"],
@@ -656,6 +716,10 @@ def main():
         secondary["loglinear_train_prefill"] = dict(
             workload="loglinear_" + kla_inputs.TRAIN.name, levels=lr2["levels"],
             tokens_per_s=lr2["tokens_per_s"], ms_per_step=lr2["ms_per_step"], roofline=lr2["roofline"])
+        dr2 = bench_loglinear_decode(kla_inputs.DECODE, 1024, peaks, stream)
+        secondary["loglinear_decode"] = dict(
+            workload="loglinear_decode_bf16_B64H16d128_x1024", levels=dr2["levels"],
+            tokens_per_s=dr2["tokens_per_s"], us_per_step=dr2["us_per_step"], roofline=dr2["roofline"])
         dc = kla_inputs.DECODE
         dr = bench_decode(dc, args.decode_loops, 3, peaks, stream, e2e=e2e)
         secondary["decode"] = dict(workload=dc.name, tokens_per_s=dr["tokens_per_s"],
