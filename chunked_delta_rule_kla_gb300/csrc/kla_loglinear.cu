@@ -22,6 +22,8 @@
 //                      S^(j) <- Gam_C S^(j) - Kt^T (Wk S^(j))   (j > b)
 //   ll_out_kernel    every (chunk, head): o = O_in + sum_j diag(lambda^(7+j))
 //                    (diag(Gam) Q S^(j) - P Wk S^(j))
+// Decoding (kla_loglinear_decode_step) is the same Fenwick update one token at
+// a time: ll_decode_kernel keeps one state per token-level bucket.
 // Products are the CTA-wide tf32 mma.sync tiles of kla_tile.cuh (a three-term
 // split with fp32 I/O).  Level states are kept transposed, [dv][dk], in the
 // workspace.
