@@ -2011,17 +2011,15 @@ bool make_map(CUtensorMap* map, const void* base, int B, int T, int H, int D) {
 
 // SM count of the current device (cached per device).
 int sm_count() {
-    static std::mutex mu;
-    static int cached[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kScanTargetCtas;
-    std::lock_guard<std::mutex> lock(mu);
-    if (cached[dev] == 0) {
-        int n = 0;
-        cached[dev] = (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-                          ? n : kScanTargetCtas;
-    }
-    return cached[dev];
+    static PerDevice cache;
+    int n = 0;
+    const cudaError_t e = cache.run([](int dev, int& v) {
+        int m = 0;
+        v = (cudaDeviceGetAttribute(&m, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && m > 0)
+                ? m : kScanTargetCtas;
+        return cudaSuccess;
+    }, &n);
+    return (e == cudaSuccess && n > 0) ? n : kScanTargetCtas;
 }
 
 template <int DK>
@@ -2039,16 +2037,17 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
     auto combine = segment_combine_kernel<DK>;
     const size_t smem_prep = PrepLayout<DK>::kSmemBytes, smem_carry = CarryLayout<DK>::kSmemBytes;
     const size_t smem_comb = sizeof(float) * (DK * (DK + 1) + DK * 16);
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_prep);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(carry, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_carry);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(summary, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_carry);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_comb);
+    // shared-memory limits, set on each device the first time it launches
+    static PerDevice attrs;
+    const cudaError_t attr_err = attrs.run([&](int, int&) {
+        cudaError_t r = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_prep);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(carry, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_carry);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(summary, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_carry);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_comb);
+        return r;
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int nchunks = (T + C - 1) / C;
@@ -2077,17 +2076,18 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
     };
     cudaError_t e = cudaSuccess;
     auto* ob = reinterpret_cast<__nv_bfloat16*>(o);
-    static std::once_flag once_f;
-    static int fused_per_sm = 0;   // resident fused CTAs per SM (0: the grid cannot be formed)
+    static PerDevice fused_setup;
+    int fused_per_sm = 0;   // resident fused CTAs per SM on this device (0: the grid cannot be formed)
     if (DK == 128 && dv == 128 && chunk_fused(B, H, DK, dv, nseg)) {
-        std::call_once(once_f, [&] {
+        (void)fused_setup.run([&](int, int& per_sm) {
             if (cudaFuncSetAttribute(chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kFusedSmemBytes) != cudaSuccess ||
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fused_per_sm, chunk_fused_kernel, kFusedThreads,
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chunk_fused_kernel, kFusedThreads,
                                                               kFusedSmemBytes) != cudaSuccess)
-                fused_per_sm = 0;
+                per_sm = 0;
             (void)cudaGetLastError();
-        });
+            return cudaSuccess;
+        }, &fused_per_sm);
     }
     // otherwise the prep grid and then one carry grid (the workspace holds no
     // range hand-off when chunk_fused holds)
@@ -2127,12 +2127,12 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
         auto state = chunk_state_kernel<false>;
         auto state_sum = chunk_state_kernel<true>;
         constexpr size_t smem_state = StateLayout::kSmemBytes;
-        static std::once_flag once_s;
-        static cudaError_t attr_s = cudaSuccess;
-        std::call_once(once_s, [&] {
-            attr_s = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_state);
-            if (attr_s == cudaSuccess)
-                attr_s = cudaFuncSetAttribute(state_sum, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_state);
+        static PerDevice state_attrs;
+        const cudaError_t attr_s = state_attrs.run([&](int, int&) {
+            cudaError_t r = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_state);
+            if (r == cudaSuccess)
+                r = cudaFuncSetAttribute(state_sum, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_state);
+            return r;
         });
         if (attr_s != cudaSuccess) return attr_s;
         if (nseg == 1 && ranges == 1) {

@@ -220,19 +220,18 @@ cudaError_t launch_io(const void* q, const void* k, const void* v, const float* 
            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    static int sms = 0;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        int dev = 0, n = 0;
-        sms = (cudaGetDevice(&dev) == cudaSuccess &&
-               cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) ? n : 152;
-        attr_err = cudaFuncSetAttribute(decode_tma_kernel<IO, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        2 * 128 * kCols * 4 + 128);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(decode_tma_kernel<IO, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            2 * 64 * kCols * 4 + 128);
-    });
+    // the SM count and the shared-memory limits, per device
+    static PerDevice setup;
+    int sms = 0;
+    const cudaError_t attr_err = setup.run([](int dev, int& n) {
+        n = (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) ? n : 152;
+        cudaError_t r = cudaFuncSetAttribute(decode_tma_kernel<IO, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             2 * 128 * kCols * 4 + 128);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(decode_tma_kernel<IO, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     2 * 64 * kCols * 4 + 128);
+        return r;
+    }, &sms);
     if (attr_err != cudaSuccess) return attr_err;
     const int items = B * H * (dv / kCols);
     const int grid = items < kTmaCtasPerSm * sms ? items : kTmaCtasPerSm * sms;

@@ -6,8 +6,33 @@
 #include <cuda_bf16.h>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 namespace kla {
+
+// Host-side set-up that CUDA applies to one device at a time (a kernel's
+// shared-memory limit, occupancy, the SM count): run once per device, with
+// that device current, and remembered per device.  `init(dev, slot)` returns
+// the set-up's cudaError_t and may fill `slot` (an int kept for the device).
+constexpr int kMaxDevices = 64;
+struct PerDevice {
+    std::mutex mu;
+    bool done[kMaxDevices] = {};
+    cudaError_t err[kMaxDevices] = {};
+    int value[kMaxDevices] = {};
+    template <typename F>
+    cudaError_t run(F&& init, int* out = nullptr) {
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev]) {
+            err[dev] = init(dev, value[dev]);
+            done[dev] = true;
+        }
+        if (out) *out = value[dev];
+        return err[dev];
+    }
+};
 
 // First 256 bytes of every kla_chunk_fwd workspace: the device error record.
 // A kernel whose bounded wait gives up writes code != 0 (first writer wins)

@@ -10,8 +10,10 @@
 // library image, so the caller passes only its inputs and outputs.
 //
 // The array is kNoAllocScratchBytes (16 MiB) on every GPU that loads the
-// library and stays resident until the process exits; with bf16 I/O that
-// covers about a thousand (batch, head, 64-token chunk) triples.  All calls share it:
+// library and stays resident until the process exits.  With bf16 I/O each
+// (batch, head, 64-token chunk) triple takes a 25,344-byte record for
+// d_k = 128 (17,152 bytes for d_k = 64), so the array covers about 650
+// triples (about 970 for d_k = 64).  All calls share it:
 // it keeps the last call's contents, the call clears what must start at zero
 // before launching, and calls that run at the same time on the GPU (other
 // streams or other host threads) race on it.
@@ -23,7 +25,7 @@
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = 16u << 20;
-constexpr int kMaxDevices = 64;
+using kla::kMaxDevices;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -133,3 +133,35 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(mod, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         mod.load_library(str(tmp_path / "missing.so"))
+
+
+# kla_chunk_fwd_noalloc keeps its scratch in a fixed 16 MiB array: a problem
+# whose workspace would be larger is refused before any CUDA call.
+NOALLOC_MAX = 16 << 20
+
+
+def _noalloc(lib, B, T, H, dk=128, dv=128):
+    return lib.kla_chunk_fwd_noalloc(P, P, P, P, P, ctypes.c_float(1e-6), None, P, None, B, T, H,
+                                     dk, dv, 64, kla.KLA_IO_BF16, None)
+
+
+def _largest_t_under(lib, B, H, limit):
+    lo, hi = 64, 64 * 4096
+    while hi - lo > 64:
+        mid = (lo + hi) // 2 // 64 * 64
+        if lib.kla_chunk_fwd_workspace_bytes(B, mid, H, 128, 128, 64, kla.KLA_IO_BF16) <= limit:
+            lo = mid
+        else:
+            hi = mid
+    return lo
+
+
+@pytest.mark.parametrize("B,H", [(1, 1), (2, 8), (1, 40)])
+def test_noalloc_rejects_beyond_its_array(lib, B, H):
+    t_fit = _largest_t_under(lib, B, H, NOALLOC_MAX)
+    assert lib.kla_chunk_fwd_workspace_bytes(B, t_fit, H, 128, 128, 64, kla.KLA_IO_BF16) <= NOALLOC_MAX
+    t_over = t_fit + 64
+    assert lib.kla_chunk_fwd_workspace_bytes(B, t_over, H, 128, 128, 64, kla.KLA_IO_BF16) > NOALLOC_MAX
+    assert _noalloc(lib, B, t_over, H) == kla.KLA_ERR_WORKSPACE
+    # about 650 records of 25,344 bytes (fewer when the scan's maps share the array)
+    assert B * H * t_fit <= 662 * 64

@@ -17,7 +17,7 @@ def _kla():
 
 
 def _inputs(io, B, T, H, dk, dv, seed):
-    case = kla_inputs.TINY.with_(B=B, T=T, H=H, dk=dk, dv=dv, io=io, seed=seed, knorm=(0.5, 2.0))
+    case = kla_inputs.TINY.with_(B=B, T=T, H=H, dk=dk, dv=dv, io=io, seed=seed)
     inp = kla_inputs.make_prefill(case, device="cuda")
     gen = torch.Generator(device="cuda")
     gen.manual_seed(seed + 1)
