@@ -43,6 +43,7 @@ EXPORTED_SYMBOLS = (
     "kla_chunk_fwd_ex",
     "kla_decode_step",
     "kla_decode_step_ex",
+    "kla_decode_step_checked",
     "kla_chunk_bwd_workspace_bytes",
     "kla_chunk_bwd",
     "kla_psd_features",
@@ -104,6 +105,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kla_chunk_fwd_ex.restype = i
         lib.kla_decode_step_ex.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, i, vp]
         lib.kla_decode_step_ex.restype = i
+        lib.kla_decode_step_checked.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, i, vp, vp]
+        lib.kla_decode_step_checked.restype = i
         lib.kla_chunk_bwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
         lib.kla_chunk_bwd_workspace_bytes.restype = sz
         lib.kla_chunk_bwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp,
@@ -359,11 +362,14 @@ def kla_chunk_fwd_noalloc(q, k, v, g, eta, eps, h0, o, hT, chunk=64, stream=None
         raise KlaError(rc, "kla_chunk_fwd_noalloc")
 
 
-def kla_decode_step(q, k, v, g, eta, eps, S, o, stream=None, beta=KLA_BETA_KACZMARZ) -> None:
+def kla_decode_step(q, k, v, g, eta, eps, S, o, stream=None, beta=KLA_BETA_KACZMARZ,
+                    status=None) -> None:
     """Enqueue one decode step (see include/kla.h); S [B,H,dk,dv] is updated in place.
 
     q, k [B,H,dk]; v, o [B,H,dv] (bf16 or fp32); g, eta [B,H] fp32.  A ``beta``
-    other than KLA_BETA_KACZMARZ goes through kla_decode_step_ex.
+    other than KLA_BETA_KACZMARZ goes through kla_decode_step_ex; a ``status``
+    tensor (>= 256 bytes on the device, cleared by the caller) through
+    kla_decode_step_checked, read back with kla_workspace_check(status).
     """
     B, H, dk = k.shape
     dv = v.shape[-1]
@@ -378,7 +384,12 @@ def kla_decode_step(q, k, v, g, eta, eps, S, o, stream=None, beta=KLA_BETA_KACZM
     args = (_ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(g, "g", torch.float32),
             _ptr(eta, "eta", torch.float32), float(eps), _ptr(S, "S", torch.float32),
             _ptr(o, "o"), B, H, dk, dv, io)
-    if beta == KLA_BETA_KACZMARZ:
+    if status is not None:
+        if status.numel() * status.element_size() < 256:
+            raise ValueError("status must hold at least 256 bytes")
+        rc, name = (load_library().kla_decode_step_checked(*args, int(beta), _ptr(status, "status"),
+                                                            _stream(stream)), "kla_decode_step_checked")
+    elif beta == KLA_BETA_KACZMARZ:
         rc, name = load_library().kla_decode_step(*args, _stream(stream)), "kla_decode_step"
     else:
         rc, name = load_library().kla_decode_step_ex(*args, int(beta), _stream(stream)), "kla_decode_step_ex"

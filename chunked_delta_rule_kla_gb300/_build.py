@@ -57,12 +57,20 @@ def needs_build() -> bool:
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile and link libkla.so if any source is newer; return its path."""
-    if not force and not needs_build():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          build_dir: str | None = None) -> str:
+    """Compile and link libkla.so if any source is newer; return its path.
+
+    ``extra_flags`` and ``build_dir`` make a variant library in a folder of its
+    own (the tests use this for a build whose device waits run out)."""
+    out_dir = build_dir or BUILD_DIR
+    lib_path = os.path.join(out_dir, "libkla.so")
+    if not force and os.path.exists(lib_path):
+        t = os.path.getmtime(lib_path)
+        if not any(os.path.getmtime(f) > t for f in _deps()):
+            return lib_path
     nvcc = _nvcc()
-    obj_dir = os.path.join(BUILD_DIR, "obj")
+    obj_dir = os.path.join(out_dir, "obj")
     os.makedirs(obj_dir, exist_ok=True)
     flags = NVCC_FLAGS + list(extra_flags or [])
 
@@ -80,13 +88,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
 
     with cf.ThreadPoolExecutor(max_workers=min(8, len(SOURCES))) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH_FLAGS, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

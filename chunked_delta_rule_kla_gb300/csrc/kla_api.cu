@@ -133,9 +133,10 @@ kla_status kla_chunk_fwd(const void* q, const void* k, const void* v, const floa
                               workspace, workspace_bytes, stream);
 }
 
-kla_status kla_decode_step_ex(const void* q, const void* k, const void* v, const float* g,
-                              const float* eta, float eps, float* S, void* o, int B, int H, int dk,
-                              int dv, kla_io_dtype io, kla_beta_mode beta, void* stream) {
+kla_status kla_decode_step_checked(const void* q, const void* k, const void* v, const float* g,
+                                   const float* eta, float eps, float* S, void* o, int B, int H,
+                                   int dk, int dv, kla_io_dtype io, kla_beta_mode beta,
+                                   void* status, void* stream) {
     if (B < 0 || H < 0 || dk <= 0 || dv <= 0) return KLA_ERR_INVALID_ARG;
     if (check_io(io) != KLA_OK) return KLA_ERR_INVALID_ARG;
     if (beta != KLA_BETA_KACZMARZ && beta != KLA_BETA_DIRECT) return KLA_ERR_INVALID_ARG;
@@ -148,9 +149,18 @@ kla_status kla_decode_step_ex(const void* q, const void* k, const void* v, const
     for (const void* p : ptrs)
         if (!aligned16(p)) return KLA_ERR_INVALID_ARG;
     if (!aligned4(g) || !aligned4(eta)) return KLA_ERR_INVALID_ARG;
+    if (status && (reinterpret_cast<uintptr_t>(status) & 255u) != 0) return KLA_ERR_WORKSPACE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     return to_status(kla::launch_decode_step(q, k, v, g, eta, eps, S, o, B, H, dk, dv,
-                                             io == KLA_IO_BF16, beta == KLA_BETA_DIRECT, st));
+                                             io == KLA_IO_BF16, beta == KLA_BETA_DIRECT,
+                                             reinterpret_cast<kla::DeviceErrorRecord*>(status), st));
+}
+
+kla_status kla_decode_step_ex(const void* q, const void* k, const void* v, const float* g,
+                              const float* eta, float eps, float* S, void* o, int B, int H, int dk,
+                              int dv, kla_io_dtype io, kla_beta_mode beta, void* stream) {
+    return kla_decode_step_checked(q, k, v, g, eta, eps, S, o, B, H, dk, dv, io, beta, nullptr,
+                                   stream);
 }
 
 kla_status kla_decode_step(const void* q, const void* k, const void* v, const float* g,

@@ -60,6 +60,16 @@ constexpr int DVS = 64;        // state columns per carry CTA
 constexpr int kStages = 2;
 constexpr int LDF = 68;        // fp32 row stride of A / T / scratch
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s per wait
+// A carry's wait for a record's ready flag (another CTA's progress).  A
+// test-only build may shorten it (KLA_TEST_FLAG_WAIT_NS) and name one chunk
+// of head 0 whose flag the prep lanes never publish
+// (KLA_TEST_UNPUBLISHED_CHUNK), so that this wait runs out and the error path
+// (record, stop, drain, exit) is exercised; product builds define neither.
+#ifdef KLA_TEST_FLAG_WAIT_NS
+constexpr uint64_t kFlagWaitNs = KLA_TEST_FLAG_WAIT_NS;
+#else
+constexpr uint64_t kFlagWaitNs = kTimeoutNs;
+#endif
 constexpr uint32_t kSuspendNs = 100000;          // try_wait suspension hint
 constexpr float kSpanMax = 80.f;                 // largest decay span factorised
 
@@ -357,6 +367,9 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
         int pending = -1;  // (kStorer) item whose record store is not yet published
         auto publish = [&](int item) {
             const int c = p.c_lo + item / nheads, hd = item % nheads;
+#ifdef KLA_TEST_UNPUBLISHED_CHUNK
+            if (hd == 0 && c == KLA_TEST_UNPUBLISHED_CHUNK) return;   // test build: a flag nothing sets
+#endif
             publish_ready(ln.flags + (size_t)hd * p.nchunks + c);
         };
         int it = 0;
@@ -1377,7 +1390,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                     const int* f = flags + head * nchunks + c0 + c;
                     const uint64_t t0 = globaltimer_ns();
                     while (load_acquire(f) == 0) {
-                        if (*abort_flag || globaltimer_ns() - t0 > kTimeoutNs) {
+                        if (*abort_flag || globaltimer_ns() - t0 > kFlagWaitNs) {
                             wt.fail(kWhereFlag, c);
                             ready = false;
                             break;

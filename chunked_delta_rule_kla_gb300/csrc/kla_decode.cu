@@ -36,14 +36,18 @@ __device__ __forceinline__ void from_f32(__nv_bfloat16* p, float x) { *p = __flo
 // a step may be placed while the previous one drains, and waits for it to
 // complete before it reads anything.
 constexpr int kTmaCtasPerSm = 3;
-constexpr uint64_t kDecodeTimeoutNs = 1000000000ull;
+constexpr uint64_t kDecodeTimeoutNs = 1000000000ull;   // a tile wait; on expiry the CTA stops
+constexpr uint64_t kDecodeDrainNs = 1000000000ull;     // waits for copies in flight before exit
+constexpr unsigned kWhereDecodeTile = 32;              // error-record site of the tile wait
 
+// On a wait that runs out, the CTA records the error in `err` (when given),
+// stops taking items, waits (bounded) for every copy it requested and exits.
 template <typename IO, int DK>
 __global__ void __launch_bounds__(kThreads, kTmaCtasPerSm)
 decode_tma_kernel(const __grid_constant__ CUtensorMap tm_s, const IO* __restrict__ q,
                   const IO* __restrict__ k, const IO* __restrict__ v, const float* __restrict__ g,
                   const float* __restrict__ eta, float eps, IO* __restrict__ o, int H, int dv,
-                  int items, int beta_direct) {
+                  int items, int beta_direct, DeviceErrorRecord* err) {
     constexpr int RPT = DK / 16;
     constexpr uint32_t kTileBytes = DK * kCols * 4;
     extern __shared__ uint8_t smem_raw[];
@@ -70,8 +74,11 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_s, const IO* __restrict
     // a no-op for an ordinary launch
     asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
+    // (thread 0) copies requested into / waited for from each tile buffer
+    int nload[2] = {0, 0}, nwait[2] = {0, 0};
     auto load = [&](int item, int buf) {  // one thread: the tile and the head's k, q and v block
         const int head = item / nblk, jb = item % nblk;
+        ++nload[buf];
         mbar_arrive_expect_tx(&full[buf], kTileBytes + (2 * DK + kCols) * (uint32_t)sizeof(IO));
         tma_load_4d(tiles + buf * DK * kCols, &tm_s, &full[buf], jb * kCols, 0, head % H, head / H);
         bulk_load(kraw[buf], k + (size_t)head * DK, DK * sizeof(IO), &full[buf]);
@@ -92,8 +99,15 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_s, const IO* __restrict
         const float gv = g[head], ev = eta[head];  // in flight while the tile is awaited
         if (tid == 0) {
             const uint64_t t0 = globaltimer_ns();
+            bool got = true;
             while (!mbar_try_wait(&full[buf], (it >> 1) & 1))
-                if (globaltimer_ns() - t0 > kDecodeTimeoutNs) { stop = 1; break; }
+                if (globaltimer_ns() - t0 > kDecodeTimeoutNs) { got = false; break; }
+            if (got) {
+                ++nwait[buf];
+            } else {
+                record_error(err, kWhereDecodeTile, (unsigned)item);
+                stop = 1;
+            }
         }
         __syncthreads();
         if (stop) break;
@@ -178,13 +192,13 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_s, const IO* __restrict
     if (tid == 0) {
         bulk_wait_all();  // stores complete before exit
         // a requested tile that was never waited for must land before exit
-        if (stop == 0) {
-            // every load issued was waited for in the loop
-        } else {
-            for (int b2 = 0; b2 < 2; ++b2) {
+        // (only after a stop: otherwise every copy was waited for in the loop);
+        // the n-th copy into a buffer completes the barrier's phase of parity n & 1
+        for (int b2 = 0; b2 < 2; ++b2) {
+            for (; nwait[b2] < nload[b2]; ++nwait[b2]) {
                 const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(&full[b2], (it >> 1) & 1))
-                    if (globaltimer_ns() - t0 > kDecodeTimeoutNs) break;
+                while (!mbar_try_wait(&full[b2], nwait[b2] & 1))
+                    if (globaltimer_ns() - t0 > kDecodeDrainNs) break;
             }
         }
     }
@@ -207,7 +221,7 @@ PFN_cuTensorMapEncodeTiled_v12000 decode_encode_fn() {
 template <typename IO>
 cudaError_t launch_io(const void* q, const void* k, const void* v, const float* g,
                       const float* eta, float eps, float* S, void* o, int B, int H, int dk,
-                      int dv, bool beta_direct, cudaStream_t stream) {
+                      int dv, bool beta_direct, DeviceErrorRecord* err, cudaStream_t stream) {
     auto fn = decode_encode_fn();
     if (!fn) return cudaErrorInitializationError;
     // S [B][H][dk][dv] fp32 as 4-D (dv, dk, H, B); box 64 x dk x 1 x 1
@@ -247,18 +261,19 @@ cudaError_t launch_io(const void* q, const void* k, const void* v, const float* 
     cfg.numAttrs = 1;
     if (dk == 128)
         return cudaLaunchKernelEx(&cfg, decode_tma_kernel<IO, 128>, map, (const IO*)q, (const IO*)k,
-                                  (const IO*)v, g, eta, eps, (IO*)o, H, dv, items, beta_direct ? 1 : 0);
+                                  (const IO*)v, g, eta, eps, (IO*)o, H, dv, items, beta_direct ? 1 : 0, err);
     return cudaLaunchKernelEx(&cfg, decode_tma_kernel<IO, 64>, map, (const IO*)q, (const IO*)k, (const IO*)v,
-                              g, eta, eps, (IO*)o, H, dv, items, beta_direct ? 1 : 0);
+                              g, eta, eps, (IO*)o, H, dv, items, beta_direct ? 1 : 0, err);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_step(const void* q, const void* k, const void* v, const float* g,
                                const float* eta, float eps, float* S, void* o, int B, int H,
-                               int dk, int dv, bool bf16, bool beta_direct, cudaStream_t stream) {
-    if (bf16) return launch_io<__nv_bfloat16>(q, k, v, g, eta, eps, S, o, B, H, dk, dv, beta_direct, stream);
-    return launch_io<float>(q, k, v, g, eta, eps, S, o, B, H, dk, dv, beta_direct, stream);
+                               int dk, int dv, bool bf16, bool beta_direct, DeviceErrorRecord* err,
+                               cudaStream_t stream) {
+    if (bf16) return launch_io<__nv_bfloat16>(q, k, v, g, eta, eps, S, o, B, H, dk, dv, beta_direct, err, stream);
+    return launch_io<float>(q, k, v, g, eta, eps, S, o, B, H, dk, dv, beta_direct, err, stream);
 }
 
 }  // namespace kla

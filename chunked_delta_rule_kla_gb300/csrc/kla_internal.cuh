@@ -63,9 +63,11 @@ __device__ __forceinline__ void record_error(DeviceErrorRecord* rec, unsigned wh
 // Decode step, fp32 math, S read once and written once (kla_decode.cu).
 // beta_direct: beta_t = eta_t (the learned-scalar rule) instead of
 // eta_t / (||k_t||^2 + eps); the same flag in every launcher below.
+// `err` (nullable): the error record a timed-out tile wait writes to.
 cudaError_t launch_decode_step(const void* q, const void* k, const void* v, const float* g,
                                const float* eta, float eps, float* S, void* o, int B, int H,
-                               int dk, int dv, bool bf16, bool beta_direct, cudaStream_t stream);
+                               int dk, int dv, bool bf16, bool beta_direct, DeviceErrorRecord* err,
+                               cudaStream_t stream);
 
 // Chunkwise prefill on CUDA cores in fp32 (kla_chunk_simt.cu).  Any T >= 1,
 // dk, dv in {64,128}, chunk 64.

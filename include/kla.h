@@ -317,6 +317,28 @@ KLA_API kla_status kla_decode_step_ex(const void* q, const void* k, const void* 
                                       kla_io_dtype io, kla_beta_mode beta, void* stream);
 
 /*
+ * kla_decode_step_ex with a device error record, so that a bounded wait that
+ * gives up inside the step is reported.  The step streams each state tile
+ * into shared memory and waits (at most 1 s) for the copy; a CTA whose wait
+ * runs out writes the record (first writer wins), waits for its copies in
+ * flight and returns, leaving the items it had not reached unchanged.
+ *
+ *  status : device memory of at least 256 bytes, 256-byte aligned, owned by
+ *           the caller; nullable (then nothing is recorded, as in
+ *           kla_decode_step_ex).  The call does not clear it: clear it once
+ *           (cudaMemsetAsync to 0) before a run of steps, which then share
+ *           it, and read it with kla_workspace_check(status, 256, stream),
+ *           which returns KLA_ERR_DEVICE_TIMEOUT if any step gave up.
+ * Other arguments and errors: kla_decode_step; a misaligned status returns
+ * KLA_ERR_WORKSPACE.
+ */
+KLA_API kla_status kla_decode_step_checked(const void* q, const void* k, const void* v,
+                                           const float* g, const float* eta, float eps,
+                                           float* S, void* o, int B, int H, int dk, int dv,
+                                           kla_io_dtype io, kla_beta_mode beta, void* status,
+                                           void* stream);
+
+/*
  * kla_chunk_fwd for callers that must not allocate device memory.  The paper
  * has no counterpart of this call; it exists for callers such as a plugin
  * inside a host framework that owns every device allocation, or a serving

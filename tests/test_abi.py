@@ -165,3 +165,15 @@ def test_noalloc_rejects_beyond_its_array(lib, B, H):
     assert _noalloc(lib, B, t_over, H) == kla.KLA_ERR_WORKSPACE
     # about 650 records of 25,344 bytes (fewer when the scan's maps share the array)
     assert B * H * t_fit <= 662 * 64
+
+
+def test_decode_step_checked_rejects(lib):
+    args = [P, P, P, P, P, ctypes.c_float(1e-6), P, P, 2, 2, 128, 128, kla.KLA_IO_BF16,
+            kla.KLA_BETA_KACZMARZ]
+    assert lib.kla_decode_step_checked(*args, WS + 16, None) == kla.KLA_ERR_WORKSPACE   # misaligned record
+    bad = list(args)
+    bad[13] = 7
+    assert lib.kla_decode_step_checked(*bad, WS, None) == kla.KLA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[6] = None
+    assert lib.kla_decode_step_checked(*bad, WS, None) == kla.KLA_ERR_INVALID_ARG
