@@ -182,3 +182,45 @@ def test_decode_empty_batch_is_noop():
     g = torch.empty((0, 4), device="cuda")
     S = torch.empty((0, 4, 128, 128), device="cuda")
     kla.decode_step(z, z, z, g, g, S)
+
+
+@pytest.mark.parametrize("io,B,H,T,segments", [("bf16", 2, 5, 300, 0), ("bf16", 1, 3, 4096, 4),
+                                               ("fp32", 2, 3, 130, 0), ("bf16", 4, 25, 2048, 0)])
+def test_permuting_heads_and_batch_permutes_outputs(io, B, H, T, segments):
+    """Heads and batch entries are independent: running the call on inputs
+    whose (b, h) are permuted gives the outputs permuted the same way, bit
+    for bit (each head's work does not depend on where it sits)."""
+    import chunked_delta_rule_kla_gb300 as kla
+    case = kla_inputs.TINY.with_(B=B, T=T, H=H, dk=128, dv=128, io=io, h0_std=0.05, seed=400 + H)
+    inp = kla_inputs.make_prefill(case, device="cuda")
+    gen = torch.Generator().manual_seed(7)
+    pb = torch.randperm(B, generator=gen).cuda()
+    ph = torch.randperm(H, generator=gen).cuda()
+
+    def perm_tok(x):   # [B, T, H, ...]
+        return x.index_select(0, pb).index_select(2, ph).contiguous()
+
+    def perm_state(x):  # [B, H, ...]
+        return x.index_select(0, pb).index_select(1, ph).contiguous()
+
+    def run(d):
+        o = torch.empty((B, T, H, 128), dtype=d["q"].dtype, device="cuda")
+        hT = torch.empty((B, H, 128, 128), device="cuda")
+        if segments:
+            ws = kla.alloc_workspace(B, T, H, 128, 128, segments=segments)
+            kla.kla_chunk_fwd_scan(d["q"], d["k"], d["v"], d["g"], d["eta"], d["eps"], d["h0"], o, hT, ws,
+                                   segments)
+        else:
+            ws = kla.alloc_workspace(B, T, H, 128, 128, io=kla.KLA_IO_BF16 if io == "bf16" else kla.KLA_IO_FP32)
+            kla.kla_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["eta"], d["eps"], d["h0"], o, hT, ws)
+        assert kla.kla_workspace_check(ws) == kla.KLA_OK
+        return o, hT
+
+    o, hT = run(inp)
+    pinp = dict(inp)
+    for n in ("q", "k", "v", "g", "eta"):
+        pinp[n] = perm_tok(inp[n])
+    pinp["h0"] = perm_state(inp["h0"])
+    o2, hT2 = run(pinp)
+    assert torch.equal(o2, perm_tok(o))
+    assert torch.equal(hT2, perm_state(hT))
