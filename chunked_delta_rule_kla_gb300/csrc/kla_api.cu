@@ -295,7 +295,7 @@ kla_status kla_psd_features(const void* x, void* y, int64_t rows, int p, int d_o
     if (!dim_ok(d_out) || p * (p + 1) / 2 > d_out) return KLA_ERR_UNSUPPORTED;
     if (rows == 0) return KLA_OK;
     if (!x || !y) return KLA_ERR_INVALID_ARG;
-    if (!aligned4(x) || !aligned4(y)) return KLA_ERR_INVALID_ARG;
+    if (!aligned4(x) || !aligned16(y)) return KLA_ERR_INVALID_ARG;   // features leave by 16-byte stores
     return to_status(kla::launch_psd_features(x, y, rows, p, d_out, io == KLA_IO_BF16,
                                               reinterpret_cast<cudaStream_t>(stream)));
 }

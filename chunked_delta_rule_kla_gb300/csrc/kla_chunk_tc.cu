@@ -60,6 +60,7 @@ constexpr int DVS = 64;        // state columns per carry CTA
 constexpr int kStages = 2;
 constexpr int LDF = 68;        // fp32 row stride of A / T / scratch
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s per wait
+constexpr long long kTimeoutCycles = 2000000000ll;  // about 1 s of SM clock, for waits timed by clock64
 // A carry's wait for a record's ready flag (another CTA's progress).  A
 // test-only build may shorten it (KLA_TEST_FLAG_WAIT_NS) and name one chunk
 // of head 0 whose flag the prep lanes never publish
@@ -183,10 +184,12 @@ struct PrepLayout {
     static constexpr uint32_t kXEnd = (kRw + 32 * LDF * 4 > kX + Rec<DK>::kGam) ? kRw + 32 * LDF * 4
                                                                               : kX + Rec<DK>::kGam;
     static constexpr uint32_t kAdT = kXEnd;                    // fp32 4 x [16][16]
-    static constexpr uint32_t kGam = kAdT + 4 * 256 * 4;       // gam[64], w[64], sc[64] (record tail)
-    static constexpr uint32_t kWf = kGam + 256;
-    static constexpr uint32_t kSc = kWf + 256;
-    static constexpr uint32_t kBet = kSc + 256;                // beta[64], betg[64]
+    // gam[64], w[64], sc[64] (the record tail), twice: item parity, so that
+    // the bulk store of one item's vectors may still be reading them while
+    // the next item writes its own
+    static constexpr uint32_t kGam = kAdT + 4 * 256 * 4;
+    static constexpr uint32_t kVecBytes = 768;
+    static constexpr uint32_t kBet = kGam + 2 * kVecBytes;     // beta[64], betg[64]
     static constexpr uint32_t kMisc = kBet + 2 * 256;
     static constexpr uint32_t kBars = kMisc + 64;
     static constexpr uint32_t kEnd = kBars + 6 * 8;
@@ -290,10 +293,8 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBars);
     float* misc = reinterpret_cast<float*>(sm + L::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 32);
-    float* gam = reinterpret_cast<float*>(sm + L::kGam);
     float* bet = reinterpret_cast<float*>(sm + L::kBet);
     float* betg = bet + C;
-    float* wf = reinterpret_cast<float*>(sm + L::kWf);
     float* Af = reinterpret_cast<float*>(sm + L::kAf);
     float* Tf = Af;  // T is formed in place: each block of T replaces the block of A it no longer needs
     float* Rw = reinterpret_cast<float*>(sm + L::kRw);
@@ -375,12 +376,22 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
         int it = 0;
         for (int item = item0; item < total; item += istride, ++it) {
         const uint32_t ph = it & 1;
+        float* gam = reinterpret_cast<float*>(sm + L::kGam + ph * L::kVecBytes);
+        float* wf = gam + C;
+        float* scv = gam + 2 * C;
         const int c = p.c_lo + item / nheads, hd = item % nheads;
         const int h = hd % H, b = hd / H;
         const int t0 = c * C;
         const int nvalid = min(C, T - t0);
         const float gv = gnext, ev = enext;
         fetch_gates(item + istride, gnext, enext);
+        // the next item's K tile is copied in only once this item's Wk has
+        // read the tile; bring it into L2 now so that copy is short
+        if (pt == 0 && item + istride < total) {
+            const int cn = p.c_lo + (item + istride) / nheads, hn = (item + istride) % nheads;
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb) tma_prefetch_l2_4d(tm_kp, kb * 64, hn % H, cn * C, hn / H);
+        }
 
         // (T's blocks above the diagonal are A's zeros.)
         // ---- gates and the decay cumsum (threads 0..63 hold rows 0..63)
@@ -432,8 +443,10 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
             const float gamm = gam[C / 2 - 1];
             if (pt < C) {
                 wf[pt] = __expf(gamm - gam[pt]);
-                reinterpret_cast<float*>(sm + L::kSc)[pt] = __expf(gam[C - 1] - gam[pt]);
+                scv[pt] = __expf(gam[C - 1] - gam[pt]);
             }
+            // the previous item's record store has read the tiles that A replaces
+            if (pt == kStorer) bulk_wait_read_le0();
             bar_sync(B1, 128);
             const bool fact = (gam[0] - gam[C - 1]) <= kSpanMax;
             // ---- A rows (64 threads) and the transposed diagonal blocks
@@ -597,19 +610,18 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
         if (pt == kStorer) {
             uint8_t* dst = p.rec + (((size_t)b * H + h) * p.nchunks + c) * Rec<DK>::kBytes;
             bulk_store(dst, sm + L::kX, Rec<DK>::kGam);
-            bulk_store(dst + Rec<DK>::kGam, sm + L::kGam, 768);
+            bulk_store(dst + Rec<DK>::kGam, gam, L::kVecBytes);
             bulk_commit();
             if (ln.flags && it == 0) {
                 // the first round's records are what the carries wait for
                 // at the start: publish at once
                 bulk_wait_all();
                 publish(item);
-            } else {
-                bulk_wait_read_le0();
-                if (ln.flags) pending = item;
+            } else if (ln.flags) {
+                pending = item;   // its reads are waited for before the next item's A rows
             }
         }
-        bar_sync(B1, 128);  // the record has been read out of shared memory
+        bar_sync(B1, 128);
         }
         if (pt == kStorer) {   // the last store completes (and is published) before exit
             bulk_wait_all();
@@ -1246,7 +1258,11 @@ __device__ __forceinline__ bool span_ok(const float* gam) { return (gam[0] - gam
 
 enum { SB_FULLA0 = 0, SB_FULLB0 = SB_FULLA0 + kStages, SB_EMPTYA0 = SB_FULLB0 + kStages,
        SB_EMPTYB0 = SB_EMPTYA0 + kStages, SB_QKB = SB_EMPTYB0 + kStages, SB_PR, SB_SR, SB_W,
-       SB_WCT, SB_WCB, SB_QSR, SB_S, SB_PW, SB_DRAIN, SB_SLD, SB_SFREE, SB_COUNT };
+       SB_WCT, SB_WCB, SB_QSR, SB_S, SB_PW, SB_DRAIN, SB_SLD, SB_SFREE,
+       SB_U,        // U(c) complete (issued by the MMA warp; W(c) accumulates onto it)
+       SB_SI,       // S(c) issued (U(c+1), which overwrites -W^T(c), may follow)
+       SB_DRAIN2,   // the MMAs issued by the state warps complete
+       SB_COUNT };
 
 // One carry CTA: warps 0..13 take the roles above; any further warp only
 // joins the CTA-wide barriers.  (bx, h, bz) play the roles of the grid
@@ -1275,7 +1291,13 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
     Waiter wt{bars, abort_flag, p.err};
 
     if (tid == 0) {
-        for (int i = 0; i < SB_COUNT; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < SB_COUNT; ++i) {
+            // without SUMMARY a stage's tiles are read by the MMAs of two
+            // issuing threads (the MMA warp and the state warps), and each
+            // commits its release
+            const bool two = !SUMMARY && i >= SB_EMPTYA0 && i < SB_QKB;
+            mbar_init(&bars[i], two ? 2 : 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         // a programmatic dependent (the next chunk range's prep) may start
@@ -1359,6 +1381,63 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
     // a no-op for an ordinary launch
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
+    // The MMAs of a chunk and the single thread that issues them: the MMA
+    // warp in SUMMARY mode, else the first thread of the state warps, which
+    // issues each product as soon as its own work has produced the operand.
+    const uint32_t st0 = smem_u32(sm);
+    constexpr int NW = SUMMARY ? 64 : 128;   // [Wk ; Q] rows
+    constexpr uint32_t id_u = idesc_bf16(128, NW, true, false, true);   // -(V^T [Tb ; 0]^T)
+    constexpr uint32_t id_w = idesc_bf16(128, NW, false, false);        // S0^T [Wk ; Q]^T
+    constexpr uint32_t id_s = idesc_bf16(128, 128, false, true);        // Wt^T K
+    constexpr uint32_t id_sp = idesc_bf16(128, 192, false, true);       // Wt^T [K | P'^T]
+    constexpr uint32_t id_pw = idesc_bf16(128, 64, false, false);       // Wb^T P^T
+    constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);
+    auto stage = [&](int cc) { return st0 + (cc % kStages) * L::kStageBytes; };
+    auto issue_u = [&](int cc) {
+        const uint32_t sb = stage(cc);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            mma_bf16(tmem + TS_D, sdesc_sw128(sb + L::kV + k * 2048, 8192, 1024),
+                     sdesc_sw128(sb + L::kTZ + k * 32, 16, 1024), id_u, k > 0);
+    };
+    auto issue_w = [&](int cc) {
+        const uint32_t sb = stage(cc);
+#pragma unroll
+        for (int k = 0; k < DK / 16; ++k)
+            mma_bf16_ta(tmem + TS_D, tmem + TS_S0B + k * 8,
+                        sdesc_sw128(sb + L::kWQ + (k / 4) * 16384 + (k % 4) * 32, 16, 1024), id_w,
+                        (vhalf || k > 0) ? 1u : 0u);
+        mma_commit(&bars[SB_W]);
+    };
+    // S_acc (and with `merged`, (P W)^T in the next 64 columns)
+    auto issue_s = [&](int cc, bool merged) {
+        const uint32_t sb = stage(cc);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            mma_bf16_ta(tmem + TS_SA, tmem + TS_WTB + k * 8, sdesc_sw128(sb + L::kK + k * 2048, 8192, 1024),
+                        merged ? id_sp : id_s, k > 0);
+        mma_commit(&bars[SB_S]);
+        if (merged) mma_commit(&bars[SB_PW]);
+    };
+    auto issue_qk = [&](int cc) {  // K Q^T (rows s, columns r)
+        const uint32_t sb = stage(cc);
+#pragma unroll
+        for (int k = 0; k < DK / 16; ++k)
+            mma_bf16(tmem + TS_QK, sdesc_sw128(sb + L::kK + (k / 4) * 8192 + (k % 4) * 32, 16, 1024),
+                     sdesc_sw128(sb + L::kWQ + (k / 4) * 16384 + 8192 + (k % 4) * 32, 16, 1024), id_qk, k > 0);
+        mma_commit(&bars[SB_QKB]);
+    };
+    auto issue_pw = [&](int cc) {
+        const uint32_t sPc = stage(cc) + L::kPT;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            mma_bf16_ta(tmem + TS_PW, tmem + TS_WBB + k * 8, sdesc_sw128(sPc + k * 32, 16, 1024), id_pw, k > 0);
+        mma_commit(&bars[SB_PW]);
+    };
+    auto chunk_span_ok = [&](int cc) {
+        return span_ok(reinterpret_cast<const float*>(sm + (cc % kStages) * L::kStageBytes + L::kVec));
+    };
+
     if (warp == 12) {
         // ================================================================ TMA producer
         if (lane == 0) {
@@ -1424,75 +1503,81 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
         }
     } else if (warp == 13) {
         // ================================================================ MMA schedule
-        const uint32_t st0 = smem_u32(sm);
-        constexpr int NW = SUMMARY ? 64 : 128;   // [Wk ; Q] rows
-        constexpr uint32_t id_u = idesc_bf16(128, NW, true, false, true);   // -(V^T [Tb ; 0]^T)
-        constexpr uint32_t id_w = idesc_bf16(128, NW, false, false);        // S0^T [Wk ; Q]^T
-        constexpr uint32_t id_s = idesc_bf16(128, 128, false, true);        // Wt^T K
-        constexpr uint32_t id_sp = idesc_bf16(128, 192, false, true);       // Wt^T [K | P'^T]
-        constexpr uint32_t id_pw = idesc_bf16(128, 64, false, false);       // Wb^T P^T
-        constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);
-        auto stage = [&](int cc) { return st0 + (cc % kStages) * L::kStageBytes; };
-        auto issue_u = [&](int cc) {
-            const uint32_t sb = stage(cc);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16(tmem + TS_D, sdesc_sw128(sb + L::kV + k * 2048, 8192, 1024),
-                         sdesc_sw128(sb + L::kTZ + k * 32, 16, 1024), id_u, k > 0);
-        };
-        auto issue_w = [&](int cc) {
-            const uint32_t sb = stage(cc);
-#pragma unroll
-            for (int k = 0; k < DK / 16; ++k)
-                mma_bf16_ta(tmem + TS_D, tmem + TS_S0B + k * 8,
-                            sdesc_sw128(sb + L::kWQ + (k / 4) * 16384 + (k % 4) * 32, 16, 1024), id_w,
-                            (vhalf || k > 0) ? 1u : 0u);
-            mma_commit(&bars[SB_W]);
-        };
-        // S_acc (and with `merged`, (P W)^T in the next 64 columns)
-        auto issue_s = [&](int cc, bool merged) {
-            const uint32_t sb = stage(cc);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16_ta(tmem + TS_SA, tmem + TS_WTB + k * 8, sdesc_sw128(sb + L::kK + k * 2048, 8192, 1024),
-                            merged ? id_sp : id_s, k > 0);
-            mma_commit(&bars[SB_S]);
-            if (merged) mma_commit(&bars[SB_PW]);
-        };
-        auto issue_qk = [&](int cc) {  // K Q^T (rows s, columns r)
-            const uint32_t sb = stage(cc);
-#pragma unroll
-            for (int k = 0; k < DK / 16; ++k)
-                mma_bf16(tmem + TS_QK, sdesc_sw128(sb + L::kK + (k / 4) * 8192 + (k % 4) * 32, 16, 1024),
-                         sdesc_sw128(sb + L::kWQ + (k / 4) * 16384 + 8192 + (k % 4) * 32, 16, 1024), id_qk, k > 0);
-            mma_commit(&bars[SB_QKB]);
-        };
-        auto issue_pw = [&](int cc) {
-            const uint32_t sPc = stage(cc) + L::kPT;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16_ta(tmem + TS_PW, tmem + TS_WBB + k * 8, sdesc_sw128(sPc + k * 32, 16, 1024), id_pw, k > 0);
-            mma_commit(&bars[SB_PW]);
-        };
-        auto chunk_span_ok = [&](int cc) {
-            return span_ok(reinterpret_cast<const float*>(sm + (cc % kStages) * L::kStageBytes + L::kVec));
-        };
-        // warp-uniform non-blocking test of a barrier phase
-        auto ready = [&](int slot, uint32_t parity) {
-            const bool r = mbar_test_wait(&bars[slot], parity);
-            return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
-        };
-        bool ok = nch > 0 && wt.warp(SB_FULLA0, 0, kWhereFull, 0);
-        if (ok && !SUMMARY) ok = wt.warp(SB_FULLB0, 0, kWhereFull, 0);   // Q K^T(0) reads K
-        if (ok) {
-            tc_fence_after();
+        if (!SUMMARY) {
+            // The side products, each issued by one elected lane once its
+            // inputs are ready: Q K^T(c+1) as soon as P(c) has been formed (Q
+            // K^T(c) read out of TMEM) and the next stage's tiles are in, so
+            // that P(c+1) is formed before S(c+1) needs it; U(c+1) once S(c)
+            // has been issued (-W^T(c) read out of TMEM) and S0^T Q^T(c) has
+            // been read.  The chain's products, W and S, are issued by the
+            // state warps.  Waits spin on non-blocking tests, uniformly over
+            // the warp, bounded in SM cycles.
+            auto wait1 = [&](int slot, uint32_t parity, unsigned where, int cc) -> bool {
+                if (__all_sync(0xffffffffu, mbar_test_wait(&bars[slot], parity))) return true;
+                const long long t0 = clock64();
+                for (uint32_t n = 1;; ++n) {
+                    if (__all_sync(0xffffffffu, mbar_test_wait(&bars[slot], parity))) return true;
+                    if ((n & 63) == 0) {
+                        if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
+                        if (__any_sync(0xffffffffu, clock64() - t0 > kTimeoutCycles)) {
+                            if (elect_one()) wt.fail(where, cc);
+                            __syncwarp();
+                            return false;
+                        }
+                    }
+                }
+            };
+            bool ok = nch > 0 && wait1(SB_FULLA0, 0, kWhereFull, 0) && wait1(SB_FULLB0, 0, kWhereFull, 0);
+            if (ok) {
+                tc_fence_after();
+                if (elect_one()) {
+                    issue_u(0);
+                    mma_commit(&bars[SB_U]);
+                    issue_qk(0);
+                    mma_commit(&bars[SB_EMPTYB0]);   // Q K^T(0) reads group B
+                    mma_commit(&bars[SB_EMPTYA0]);   // U(0), Q K^T(0) read group A
+                }
+                __syncwarp();
+            }
+            for (int c = 0; ok && c + 1 < nch; ++c) {
+                const uint32_t par = c & 1;
+                const int s1 = (c + 1) % kStages;
+                const uint32_t p1 = ((c + 1) / kStages) & 1;
+                if (!(ok = wait1(SB_PR, par, kWherePR, c))) break;
+                if (!(ok = wait1(SB_FULLA0 + s1, p1, kWhereFull, c + 1))) break;
+                if (!(ok = wait1(SB_FULLB0 + s1, p1, kWhereFull, c + 1))) break;
+                tc_fence_after();
+                if (elect_one()) {
+                    issue_qk(c + 1);
+                    mma_commit(&bars[SB_EMPTYB0 + s1]);   // Q K^T(c+1) reads group B
+                }
+                __syncwarp();
+                if (!(ok = wait1(SB_SI, par, kWhereS, c))) break;
+                if (!(ok = wait1(SB_QSR, par, kWhereEPI, c))) break;
+                tc_fence_after();
+                if (elect_one()) {
+                    issue_u(c + 1);
+                    mma_commit(&bars[SB_U]);
+                    mma_commit(&bars[SB_EMPTYA0 + s1]);   // Q K^T(c+1), U(c+1) read group A
+                }
+                __syncwarp();
+            }
             if (elect_one()) {
-                if (vhalf) issue_u(0);
-                if (!SUMMARY) issue_qk(0);
+                mma_commit(&bars[SB_DRAIN]);
+                const long long t0 = clock64();
+                while (!mbar_try_wait(&bars[SB_DRAIN], 0))
+                    if (clock64() - t0 > kTimeoutCycles) { wt.fail(kWhereDrain, -1); break; }
             }
             __syncwarp();
         }
+        // SUMMARY mode: this warp issues every product
         if (SUMMARY) {
+            bool ok = nch > 0 && wt.warp(SB_FULLA0, 0, kWhereFull, 0);
+            if (ok) {
+                tc_fence_after();
+                if (elect_one() && vhalf) issue_u(0);
+                __syncwarp();
+            }
             for (int c = 0; ok && c < nch; ++c) {
                 const uint32_t par = c & 1;
                 if (!(ok = wt.warp(SB_SR, par, kWhereSR, c))) break;
@@ -1519,95 +1604,15 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                     }
                 }
             }
-        } else {
-            // Per chunk c: W(c) [S_c ready] with the release of group A, and
-            // S(c) [Wt ready] first; then U(c+1) [-W^T and S0^T Q^T read],
-            // P W(c) [P(c) and Wb ready], Q K^T(c+1) [Q K^T(c) read], and the
-            // release of group B.
-            int c = 0;
-            bool fW = false, fS = false, fU = false, fPW = false, fQK = false, fE = false;
-            uint32_t idle = 0;
-            uint64_t t_last = globaltimer_ns();
-            while (ok && c < nch) {
-                const uint32_t par = c & 1;
-                const int s1 = (c + 1) % kStages;
-                const uint32_t p1 = ((c + 1) / kStages) & 1;
-                bool prog = false;
-                if (!fW && ready(SB_SR, par)) {
-                    tc_fence_after();
-                    if (elect_one()) {
-                        issue_w(c);
-                        // U(c), Q K^T(c) and W(c) are the readers of group A
-                        mma_commit(&bars[SB_EMPTYA0 + c % kStages]);
-                    }
-                    __syncwarp();
-                    fW = prog = true;
-                }
-                const bool merged = chunk_span_ok(c);
-                if (fW && !fS && ready(SB_WCT, par) && (!merged || ready(SB_PR, par))) {
-                    tc_fence_after();
-                    if (elect_one()) issue_s(c, merged);
-                    __syncwarp();
-                    fS = prog = true;
-                    if (merged) fPW = true;
-                }
-                if (fS && !fU) {
-                    if (c + 1 >= nch) {
-                        fU = true;
-                    } else if (ready(SB_QSR, par) && ready(SB_FULLA0 + s1, p1)) {
-                        tc_fence_after();
-                        if (elect_one()) issue_u(c + 1);
-                        __syncwarp();
-                        fU = prog = true;
-                    }
-                }
-                if (fW && !fPW && !merged && ready(SB_PR, par) && ready(SB_WCB, par)) {
-                    tc_fence_after();
-                    if (elect_one()) issue_pw(c);
-                    __syncwarp();
-                    fPW = prog = true;
-                }
-                if (fPW && !fQK) {
-                    if (c + 1 >= nch) {
-                        fQK = true;
-                    } else if (ready(SB_FULLA0 + s1, p1) && ready(SB_FULLB0 + s1, p1)) {
-                        tc_fence_after();
-                        if (elect_one()) issue_qk(c + 1);
-                        __syncwarp();
-                        fQK = prog = true;
-                    }
-                }
-                if (fS && fPW && !fE) {
-                    if (elect_one()) mma_commit(&bars[SB_EMPTYB0 + c % kStages]);
-                    __syncwarp();
-                    fE = prog = true;
-                }
-                if (fW && fS && fU && fPW && fQK && fE) {
-                    ++c;
-                    fW = fS = fU = fPW = fQK = fE = false;
-                    idle = 0;
-                    t_last = globaltimer_ns();
-                } else if (!prog) {
-                    // nothing issuable: sleep until the next state-path
-                    // barrier completes (or briefly), then look again
-                    if (!fW) mbar_try_wait_sleep(&bars[SB_SR], par, 1000);
-                    else if (!fS) mbar_try_wait_sleep(&bars[SB_WCT], par, 1000);
-                    __syncwarp();
-                    if ((++idle & 15) == 0) {
-                        if (*abort_flag) { ok = false; break; }
-                        if (globaltimer_ns() - t_last > kTimeoutNs) { wt.fail(kWhereSR, c); ok = false; break; }
-                    }
+            if (elect_one()) {
+                mma_commit(&bars[SB_DRAIN]);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait_sleep(&bars[SB_DRAIN], 0, kSuspendNs)) {
+                    if (globaltimer_ns() - t0 > kTimeoutNs) { wt.fail(kWhereDrain, -1); break; }
                 }
             }
+            __syncwarp();
         }
-        if (elect_one()) {
-            mma_commit(&bars[SB_DRAIN]);
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait_sleep(&bars[SB_DRAIN], 0, kSuspendNs)) {
-                if (globaltimer_ns() - t0 > kTimeoutNs) { wt.fail(kWhereDrain, -1); break; }
-            }
-        }
-        __syncwarp();
     } else if (warp >= 4 && warp < 12) {
         // ================================================================ state warps
         const int q = warp & 3, hh = (warp - 4) >> 2;
@@ -1615,6 +1620,56 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
         const uint32_t lf = (uint32_t)(q * 32) << 16;
         const int st_id = tid - 128;                      // 0..255
         float master[64];                                 // S^T[j][64 hh + i]
+        // (without SUMMARY) warp 4 issues the chain's products, W and S, one
+        // elected lane each, right after the state warps' barrier that makes
+        // the operand complete, so the chain needs no hand-off to another
+        // warp.  Its waits are warp-uniform and bounded; one that gives up
+        // records the error and sets the abort flag, so the group's next wait
+        // fails for every state thread alike.
+        auto wwait = [&](int slot, uint32_t parity, unsigned where, int cc) -> bool {
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
+            if (__all_sync(0xffffffffu, mbar_test_wait(&bars[slot], parity))) return true;
+            const long long t0 = clock64();
+            for (uint32_t n = 1;; ++n) {
+                if (__all_sync(0xffffffffu, mbar_test_wait(&bars[slot], parity))) return true;
+                if ((n & 63) == 0) {
+                    if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
+                    if (__any_sync(0xffffffffu, clock64() - t0 > kTimeoutCycles)) {
+                        if (elect_one()) wt.fail(where, cc);
+                        __syncwarp();
+                        return false;
+                    }
+                }
+            }
+        };
+        // S(c) (and P W(c) with strong decay) once Wt(c) is in TMEM and P(c)
+        // is formed; then the release of group B and the signal that lets the
+        // MMA warp overwrite -W^T(c) with U(c+1)
+        auto issue_s_chain = [&](int cc) {
+            tc_fence_after();
+            const bool merged = chunk_span_ok(cc);
+            if (!wwait(SB_PR, cc & 1, kWherePR, cc)) return;
+            if (elect_one()) {
+                issue_s(cc, merged);
+                if (!merged) issue_pw(cc);
+                mma_commit(&bars[SB_EMPTYB0 + cc % kStages]);
+                mbar_arrive(&bars[SB_SI]);
+            }
+            __syncwarp();
+        };
+        // W(c) once S_c is in TMEM (bf16) and U(c) is complete; then the
+        // release of group A
+        // W(c) once S_c is in TMEM (bf16) and U(c) is complete; then the
+        // release of group A
+        auto issue_w_chain = [&](int cc) {
+            if (!wwait(SB_U, cc & 1, kWhereW, cc)) return;
+            tc_fence_after();
+            if (elect_one()) {
+                issue_w(cc);
+                mma_commit(&bars[SB_EMPTYA0 + cc % kStages]);
+            }
+            __syncwarp();
+        };
         {
             // a failed wait leaves zeros; the abort flag then ends every loop
             const bool staged = s_start && wt.group(SB_SLD, 0, kWhereFull, -1, 3, 256);
@@ -1635,9 +1690,11 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
             tc_fence_before();
             bar_sync(1, 256);
             if (st_id == 0) {
-                mbar_arrive(&bars[SB_SR]);
+                if (SUMMARY) mbar_arrive(&bars[SB_SR]);
                 if (s_start) mbar_arrive(&bars[SB_SFREE]);
             }
+            __syncwarp();
+            if (!SUMMARY && warp == 4 && nch > 0) issue_w_chain(0);
         }
         for (int c = 0; c < nch; ++c) {
             const uint32_t par = c & 1;
@@ -1672,9 +1729,9 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
             }
             tc_fence_before();
             bar_sync(1, 256);
-            if (st_id == 0) mbar_arrive(&bars[SB_WCT]);
-            // ---- Wb^T (strong decay only), once P W of the previous chunk has read the last one
+            if (SUMMARY && st_id == 0) mbar_arrive(&bars[SB_WCT]);
             if (!SUMMARY) {
+                // ---- Wb^T (strong decay only), once P W of the previous chunk has read the last one
                 if (!span_ok(vec)) {
                     if (c > 0 && !wt.group(SB_PW, par ^ 1u, kWherePW, c, 3, 256)) break;
                     tc_fence_after();
@@ -1683,7 +1740,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                     tc_fence_before();
                     bar_sync(1, 256);
                 }
-                if (st_id == 0) mbar_arrive(&bars[SB_WCB]);
+                if (warp == 4) issue_s_chain(c);
             }
             // ---- S1^T = Gam_C S0^T + S_acc; bf16 copy for the next chunk
             if (!wt.group(SB_S, par, kWhereS, c, 3, 256)) break;
@@ -1704,7 +1761,18 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
             tmem_st_wait();
             tc_fence_before();
             bar_sync(1, 256);
-            if (st_id == 0) mbar_arrive(&bars[SB_SR]);
+            if (SUMMARY && st_id == 0) mbar_arrive(&bars[SB_SR]);
+            if (!SUMMARY && warp == 4 && c + 1 < nch) issue_w_chain(c + 1);
+        }
+        if (!SUMMARY && warp == 4) {
+            // every MMA this warp issued completes before TMEM is freed
+            if (elect_one()) {
+                mma_commit(&bars[SB_DRAIN2]);
+                const long long t0 = clock64();
+                while (!mbar_try_wait(&bars[SB_DRAIN2], 0))
+                    if (clock64() - t0 > kTimeoutCycles) { wt.fail(kWhereDrain, -1); break; }
+            }
+            __syncwarp();
         }
         const bool aborted = bar_or(3, 256, *abort_flag != 0);
         const bool write_final = SUMMARY || (p.s_out && seg == p.nseg - 1);

@@ -10,8 +10,9 @@
 // d_out in {64, 128} the chunked kernels take the features as keys and
 // queries unchanged (zero padding changes no product).
 //
-// The forward takes a half-warp per row, the derivative a warp per row; both
-// stream their rows once (HBM-bound).
+// The forward stages tiles of rows in shared memory and writes each row's
+// features as one contiguous run of 16-byte stores; the derivative takes a
+// warp per row; both stream their rows once (HBM-bound).
 #include "kla_internal.cuh"
 
 namespace kla {
@@ -40,81 +41,83 @@ __device__ __forceinline__ void feature_pair(int n, int p, int& i, int& j) {
     j = i + n;
 }
 
-// d_out / 16 consecutive features of one row, stored as one vector
-template <typename T, int PER> struct FeatStore;
-template <> struct FeatStore<__nv_bfloat16, 8> {
-    __device__ __forceinline__ static void st(__nv_bfloat16* p, const float* v) {
-        uint32_t w[4];
+// Eight features as one 16-byte store (bf16) or two (fp32).
+__device__ __forceinline__ void st8(__nv_bfloat16* p, const float* v) {
+    uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-            w[i] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
     }
-};
-template <> struct FeatStore<__nv_bfloat16, 4> {
-    __device__ __forceinline__ static void st(__nv_bfloat16* p, const float* v) {
-        const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
-        *reinterpret_cast<uint2*>(p) =
-            make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
-    }
-};
-template <> struct FeatStore<float, 8> {
-    __device__ __forceinline__ static void st(float* p, const float* v) {
-        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
-        *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
-    }
-};
-template <> struct FeatStore<float, 4> {
-    __device__ __forceinline__ static void st(float* p, const float* v) {
-        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
-    }
-};
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ void st8(float* p, const float* v) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+// Four features: one 8-byte store (bf16) or one 16-byte store (fp32).
+__device__ __forceinline__ void st4(__nv_bfloat16* p, const float* v) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+    *reinterpret_cast<uint2*>(p) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
+__device__ __forceinline__ void st4(float* p, const float* v) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
 
-// A half-warp per row: lane s of the half loads x[s] (s < p) and writes the
-// features PER*s .. PER*s + PER - 1 (PER = d_out / 16) as one vector.
-template <typename T, int PER>
+// Blocks of 256 threads walk tiles of kRows rows.  A tile's inputs (kRows x p
+// values, contiguous in memory) come in by coalesced loads into shared
+// memory; then 16 threads per row each write D_OUT / 16 consecutive features
+// with one 16-byte store (bf16, d_out = 128) or the equivalent, so a row's
+// features leave as one contiguous run.  A thread walks its features' (i, j)
+// pairs from the first one on, reading u_i and u_j from shared memory.
+constexpr int kRows = 64;
+
+template <typename T, int D_OUT>
 __global__ void __launch_bounds__(256) psd_features_kernel(const T* __restrict__ x, T* __restrict__ y,
                                                            int64_t rows, int p) {
-    constexpr int d_out = 16 * PER;
-    const int lane = threadIdx.x & 31, sub = lane & 15;
-    const unsigned mask = 0xffffu << (lane & 16);
+    constexpr int FPT = D_OUT / 16;   // features per thread (8 or 4)
+    __shared__ float sx[kRows * 16];
     const int nf = p * (p + 1) / 2;
-    int fi[PER], fj[PER];
-    float fs[PER];
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        const int n = PER * sub + u;
-        if (n < nf) {
-            feature_pair(n, p, fi[u], fj[u]);
-            fs[u] = fi[u] == fj[u] ? 1.f : kSqrt2;
-        } else {
-            fi[u] = fj[u] = 0;
-            fs[u] = 0.f;
+    const int part = threadIdx.x & 15, rsub = threadIdx.x >> 4;   // 16 rows per pass
+    const int n0 = part * FPT;
+    int i0 = 0, j0 = 0;
+    if (n0 < nf) feature_pair(n0, p, i0, j0);
+    for (int64_t r0 = (int64_t)blockIdx.x * kRows; r0 < rows; r0 += (int64_t)gridDim.x * kRows) {
+        const int nr = rows - r0 < kRows ? (int)(rows - r0) : kRows;
+        __syncthreads();   // the previous tile's values are read
+        const T* xs = x + r0 * p;
+        for (int e = threadIdx.x; e < nr * p; e += blockDim.x) {
+            const int r = e / p;
+            sx[r * 16 + (e - r * p)] = ldx<T>(xs + e);
         }
-    }
-    // four rows per half-warp in flight: their loads go out before any is used
-    const int64_t nhalf = ((int64_t)gridDim.x * blockDim.x) >> 4;
-    for (int64_t row0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4; row0 < rows;
-         row0 += 4 * nhalf) {
-        float xv[4];
+        __syncthreads();
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int64_t row = row0 + m * nhalf;
-            xv[m] = (sub < p && row < rows) ? ldx<T>(x + row * p + sub) : 0.f;
-        }
+        for (int pass = 0; pass < kRows / 16; ++pass) {
+            const int rr = pass * 16 + rsub;
+            if (rr < nr) {
+                const float* xr = sx + rr * 16;
+                float v[FPT];
+                int i = i0, j = j0;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int64_t row = row0 + m * nhalf;
-            float v[PER];
-#pragma unroll
-            for (int u = 0; u < PER; ++u) {
-                const float xi = __shfl_sync(mask, xv[m], fi[u], 16);
-                const float xj = __shfl_sync(mask, xv[m], fj[u], 16);
-                v[u] = fs[u] * xi * xj;
+                for (int u = 0; u < FPT; ++u) {
+                    // past the last feature (the zero padding) nothing is read
+                    // and (i, j) stay within the row
+                    float val = 0.f;
+                    if (n0 + u < nf) {
+                        val = (i == j ? 1.f : kSqrt2) * xr[i] * xr[j];
+                        if (++j == p) { ++i; j = i; }
+                    }
+                    v[u] = val;
+                }
+                T* yr = y + (r0 + rr) * D_OUT + n0;
+                if constexpr (FPT == 8) {
+                    st8(yr, v);
+                } else {
+                    float w[8] = {v[0], v[1], v[2], v[3], 0.f, 0.f, 0.f, 0.f};
+                    st4(yr, w);
+                }
             }
-            if (row < rows) FeatStore<T, PER>::st(y + row * d_out + PER * sub, v);
         }
     }
 }
@@ -160,17 +163,17 @@ int grid_for(int64_t rows) {
 cudaError_t launch_psd_features(const void* x, void* y, int64_t rows, int p, int d_out, bool bf16,
                                 cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
-    const int64_t blocks64 = (rows + 15) / 16;         // 16 half-warps per block, a row each
-    const int grid = (int)(blocks64 < 152 * 16 ? blocks64 : 152 * 16);
+    const int64_t tiles = (rows + kRows - 1) / kRows;
+    const int grid = (int)(tiles < 152 * 8 ? tiles : 152 * 8);
     using bf = __nv_bfloat16;
     if (bf16 && d_out == 128)
-        psd_features_kernel<bf, 8><<<grid, 256, 0, stream>>>(static_cast<const bf*>(x), static_cast<bf*>(y), rows, p);
+        psd_features_kernel<bf, 128><<<grid, 256, 0, stream>>>(static_cast<const bf*>(x), static_cast<bf*>(y), rows, p);
     else if (bf16)
-        psd_features_kernel<bf, 4><<<grid, 256, 0, stream>>>(static_cast<const bf*>(x), static_cast<bf*>(y), rows, p);
+        psd_features_kernel<bf, 64><<<grid, 256, 0, stream>>>(static_cast<const bf*>(x), static_cast<bf*>(y), rows, p);
     else if (d_out == 128)
-        psd_features_kernel<float, 8><<<grid, 256, 0, stream>>>(static_cast<const float*>(x), static_cast<float*>(y), rows, p);
+        psd_features_kernel<float, 128><<<grid, 256, 0, stream>>>(static_cast<const float*>(x), static_cast<float*>(y), rows, p);
     else
-        psd_features_kernel<float, 4><<<grid, 256, 0, stream>>>(static_cast<const float*>(x), static_cast<float*>(y), rows, p);
+        psd_features_kernel<float, 64><<<grid, 256, 0, stream>>>(static_cast<const float*>(x), static_cast<float*>(y), rows, p);
     return cudaGetLastError();
 }
 

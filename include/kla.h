@@ -269,7 +269,8 @@ KLA_API kla_status kla_loglinear_decode_step(const void* q, const void* k, const
  * psi(q) . psi(k) = (q . k)^2 and ||psi(k)||^2 = ||k||^4.  Feeding the
  * features of q and k to kla_chunk_fwd_ex / kla_chunk_bwd gives DeltaKATA.
  *
- *  x : [rows, p] I/O dtype;  y : [rows, d_out] I/O dtype (written in full)
+ *  x : [rows, p] I/O dtype, 4-byte aligned;  y : [rows, d_out] I/O dtype,
+ *      16-byte aligned (written in full, by 16-byte stores)
  *  1 <= p, p(p+1)/2 <= d_out, d_out in {64, 128} (p <= 10 or p <= 15)
  *
  * kla_psd_features_bwd maps grad_y [rows, d_out] to grad_x [rows, p].  Both
