@@ -318,7 +318,7 @@ def bench_prefill(case, K, W, flush, peaks, stream, e2e=True, direct=False):
     return res
 
 
-def e2e_prefill(kla, case, inp, ws, work, K, stream, sets=2):
+def e2e_prefill(kla, case, inp, ws, work, K, stream, sets=2, up_streams=3):
     names = ("q", "k", "v", "g", "eta")
     host = {n: inp[n].cpu().pin_memory() for n in names}
     B, T, H, dk, dv = case.B, case.T, case.H, case.dk, case.dv
@@ -327,22 +327,28 @@ def e2e_prefill(kla, case, inp, ws, work, K, stream, sets=2):
              torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")) for _ in range(sets)]
     outs_h = [(torch.empty(o.shape, dtype=o.dtype).pin_memory(),
                torch.empty(h.shape, dtype=h.dtype).pin_memory()) for o, h in outs]
-    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    # the large inputs go up on separate copy streams, so that their copies
+    # can run on different copy engines at once
+    ups = [torch.cuda.Stream() for _ in range(up_streams)]
+    up_of = {"q": 0, "k": 1 % up_streams, "v": 2 % up_streams, "g": 0, "eta": 1 % up_streams}
+    down = torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()  # noqa: E731
-    loaded = [ev() for _ in range(sets)]      # inputs of set j on the device
+    loaded = [[ev() for _ in ups] for _ in range(sets)]   # inputs of set j on the device
     consumed = [ev() for _ in range(sets)]    # the call has read set j's inputs and written its outputs
     fetched = [ev() for _ in range(sets)]     # set j's outputs are back on the host
     started = [False] * sets
 
     def e2e_step(i):
         j = i % sets
-        if started[j]:
-            up.wait_event(consumed[j])
-        with torch.cuda.stream(up):
-            for n in names:
-                dev[j][n].copy_(host[n], non_blocking=True)
-        loaded[j].record(up)
-        stream.wait_event(loaded[j])
+        for u, up in enumerate(ups):
+            if started[j]:
+                up.wait_event(consumed[j])
+            with torch.cuda.stream(up):
+                for n in names:
+                    if up_of[n] == u:
+                        dev[j][n].copy_(host[n], non_blocking=True)
+            loaded[j][u].record(up)
+            stream.wait_event(loaded[j][u])
         if started[j]:
             stream.wait_event(fetched[j])
         o, hT = outs[j]
@@ -372,8 +378,8 @@ def e2e_prefill(kla, case, inp, ws, work, K, stream, sets=2):
     d2h = sum(t.numel() * t.element_size() for t in outs_h[0])
     return dict(value=e2e_job, unit="tokens/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
                 ms_per_step=e2e_s * 1e3, steps=Ke,
-                pipeline=f"{sets} device buffer sets; H2D of step i+1 and D2H of step i-1 "
-                         "overlap step i (separate copy streams)")
+                pipeline=f"{sets} device buffer sets; H2D of step i+1 ({up_streams} copy streams) and D2H "
+                         "of step i-1 overlap step i")
 
 
 def bench_backward(case, K, W, flush, peaks, stream):
@@ -719,7 +725,7 @@ def main():
             r = bench_prefill(case, args.steps, args.warmup, flush, peaks, stream, e2e=e2e,
                               direct=args.only == "gdn")
             line = dict(workload=case.name, tokens_per_s=r["tokens_per_s"], ms_per_step=r["ms_per_step"],
-                        roofline=r["roofline"], gpu_launches=r["launches"])
+                        roofline=r["roofline"], gpu_launches=r["launches"], e2e=r.get("e2e"))
         clocks.stop()
         if rank == 0:
             print(json.dumps(dict(only=args.only, **line)), flush=True)

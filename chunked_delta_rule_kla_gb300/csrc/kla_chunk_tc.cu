@@ -1516,7 +1516,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                 if (__all_sync(0xffffffffu, mbar_test_wait(&bars[slot], parity))) return true;
                 const long long t0 = clock64();
                 for (uint32_t n = 1;; ++n) {
-                    if (__all_sync(0xffffffffu, mbar_test_wait(&bars[slot], parity))) return true;
+                    if (__all_sync(0xffffffffu, mbar_try_wait(&bars[slot], parity))) return true;
                     if ((n & 63) == 0) {
                         if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
                         if (__any_sync(0xffffffffu, clock64() - t0 > kTimeoutCycles)) {
@@ -1631,7 +1631,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
             if (__all_sync(0xffffffffu, mbar_test_wait(&bars[slot], parity))) return true;
             const long long t0 = clock64();
             for (uint32_t n = 1;; ++n) {
-                if (__all_sync(0xffffffffu, mbar_test_wait(&bars[slot], parity))) return true;
+                if (__all_sync(0xffffffffu, mbar_try_wait(&bars[slot], parity))) return true;
                 if ((n & 63) == 0) {
                     if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
                     if (__any_sync(0xffffffffu, clock64() - t0 > kTimeoutCycles)) {

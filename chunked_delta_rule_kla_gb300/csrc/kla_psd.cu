@@ -69,53 +69,78 @@ __device__ __forceinline__ void st4(float* p, const float* v) {
 // values, contiguous in memory) come in by coalesced loads into shared
 // memory; then 16 threads per row each write D_OUT / 16 consecutive features
 // with one 16-byte store (bf16, d_out = 128) or the equivalent, so a row's
-// features leave as one contiguous run.  A thread walks its features' (i, j)
-// pairs from the first one on, reading u_i and u_j from shared memory.
+// features leave as one contiguous run.  Which (i, j) pair and scale each of
+// a thread's features takes is worked out once, before the first tile: per
+// row a feature costs two shared-memory reads and two multiplies.
 constexpr int kRows = 64;
 
+// At least 6 blocks per SM: register use capped so that enough tiles are in
+// flight to cover the loads' latency (with the compiler's free choice only two
+// blocks fitted).
 template <typename T, int D_OUT>
-__global__ void __launch_bounds__(256) psd_features_kernel(const T* __restrict__ x, T* __restrict__ y,
-                                                           int64_t rows, int p) {
+__global__ void __launch_bounds__(256, 6) psd_features_kernel(const T* __restrict__ x, T* __restrict__ y,
+                                                              int64_t rows, int p) {
     constexpr int FPT = D_OUT / 16;   // features per thread (8 or 4)
-    __shared__ float sx[kRows * 16];
+    __shared__ float sx[2 * kRows * 16];
     const int nf = p * (p + 1) / 2;
     const int part = threadIdx.x & 15, rsub = threadIdx.x >> 4;   // 16 rows per pass
     const int n0 = part * FPT;
-    int i0 = 0, j0 = 0;
-    if (n0 < nf) feature_pair(n0, p, i0, j0);
-    for (int64_t r0 = (int64_t)blockIdx.x * kRows; r0 < rows; r0 += (int64_t)gridDim.x * kRows) {
-        const int nr = rows - r0 < kRows ? (int)(rows - r0) : kRows;
-        __syncthreads();   // the previous tile's values are read
-        const T* xs = x + r0 * p;
-        for (int e = threadIdx.x; e < nr * p; e += blockDim.x) {
-            const int r = e / p;
-            sx[r * 16 + (e - r * p)] = ldx<T>(xs + e);
-        }
-        __syncthreads();
+    int fi[FPT], fj[FPT];
+    float fs[FPT];
+    {
+        int i = 0, j = 0;
+        if (n0 < nf) feature_pair(n0, p, i, j);
 #pragma unroll
+        for (int u = 0; u < FPT; ++u) {
+            // past the last feature (the zero padding) the scale is 0 and
+            // (i, j) stay at (0, 0)
+            const bool on = n0 + u < nf;
+            fi[u] = on ? i : 0;
+            fj[u] = on ? j : 0;
+            fs[u] = on ? (i == j ? 1.f : kSqrt2) : 0.f;
+            if (on && ++j == p) { ++i; j = i; }
+        }
+    }
+    // Tiles are double-buffered: the next tile's values are loaded into
+    // registers while this one is written out.
+    constexpr int kPer = (kRows * 15 + 255) / 256;   // values a thread loads per tile (p <= 15)
+    const int64_t step = (int64_t)gridDim.x * kRows;
+    auto fetch = [&](int64_t t0, float (&vals)[kPer]) {
+        const int nr = rows - t0 < kRows ? (int)(rows - t0) : kRows;
+        const T* xs = x + t0 * p;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int e = threadIdx.x + u * 256;
+            vals[u] = (t0 < rows && e < nr * p) ? ldx<T>(xs + e) : 0.f;
+        }
+    };
+    float pre[kPer];
+    int buf = 0;
+    int64_t r0 = (int64_t)blockIdx.x * kRows;
+    fetch(r0, pre);
+    for (; r0 < rows; r0 += step, buf ^= 1) {
+        const int nr = rows - r0 < kRows ? (int)(rows - r0) : kRows;
+        float* sb = sx + buf * (kRows * 16);
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int e = threadIdx.x + u * 256;
+            if (e < nr * p) sb[e] = pre[u];
+        }
+        __syncthreads();   // this tile's values are in; the buffer written two tiles ago is no longer read
+        fetch(r0 + step, pre);
+#pragma unroll 1
         for (int pass = 0; pass < kRows / 16; ++pass) {
             const int rr = pass * 16 + rsub;
             if (rr < nr) {
-                const float* xr = sx + rr * 16;
+                const float* xr = sb + rr * p;
                 float v[FPT];
-                int i = i0, j = j0;
 #pragma unroll
-                for (int u = 0; u < FPT; ++u) {
-                    // past the last feature (the zero padding) nothing is read
-                    // and (i, j) stay within the row
-                    float val = 0.f;
-                    if (n0 + u < nf) {
-                        val = (i == j ? 1.f : kSqrt2) * xr[i] * xr[j];
-                        if (++j == p) { ++i; j = i; }
-                    }
-                    v[u] = val;
-                }
+                for (int u = 0; u < FPT; ++u) v[u] = fs[u] * xr[fi[u]] * xr[fj[u]];
                 T* yr = y + (r0 + rr) * D_OUT + n0;
                 if constexpr (FPT == 8) {
                     st8(yr, v);
                 } else {
-                    float w[8] = {v[0], v[1], v[2], v[3], 0.f, 0.f, 0.f, 0.f};
-                    st4(yr, w);
+                    st4(yr, v);
                 }
             }
         }
@@ -164,7 +189,7 @@ cudaError_t launch_psd_features(const void* x, void* y, int64_t rows, int p, int
                                 cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
     const int64_t tiles = (rows + kRows - 1) / kRows;
-    const int grid = (int)(tiles < 152 * 8 ? tiles : 152 * 8);
+    const int grid = (int)(tiles < 152 * 6 ? tiles : 152 * 6);
     using bf = __nv_bfloat16;
     if (bf16 && d_out == 128)
         psd_features_kernel<bf, 128><<<grid, 256, 0, stream>>>(static_cast<const bf*>(x), static_cast<bf*>(y), rows, p);
