@@ -372,3 +372,52 @@ def loglinear_decode(q, k, v, g, eta, lam, eps, *, beta_direct=False):
 
 __all__ = ["chunk_quantities", "chunk_step", "chunk_map", "chunk_forward", "chunk_scan_forward",
            "chunk_backward", "loglinear_chunk_forward", "loglinear_decode"]
+
+
+def loglinear_level_passes(q, k, v, g, eta, lam, eps, *, C=64, beta_direct=False):
+    """Log-Linear gated delta rule as independent passes of the ordinary
+    chunked recurrence, one per level above the chunk.
+
+    A token s is in bucket level l of token t > s when t and s first differ
+    at bit l - 1: s lies in the first half and t in the second half of the
+    aligned block of 2^l tokens that holds both.  So level l's contribution to
+    o_t is the ordinary recurrence restarted from zero at the block's start,
+    with writes from the first half only, read out at t after t's own
+    transition, weighted by lambda_t^(l).  With C = 2^m, levels l > m have
+    blocks of whole chunks: per block, the first-half chunks run the chunk
+    step with their values, the second-half chunks run it with zero values
+    (S1 = M S0, O = (diag(Gam) Q - P Wk) S0) and their outputs count.  Levels
+    0..m stay inside a chunk: O_in = ((P T diag(beta)) o Lam) V."""
+    q, k, v, g, eta, lam = map(_f64, (q, k, v, g, eta, lam))
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    assert C & (C - 1) == 0
+    m = (C - 1).bit_length()
+    L = (max(T, 1) - 1).bit_length() + 1
+    o = np.zeros((B, T, H, dv))
+    bounds = _bounds(T, C)
+    for b in range(B):
+        for h in range(H):
+            # in-chunk levels 0..m
+            for t0, t1 in bounds:
+                K, V, Q = k[b, t0:t1, h], v[b, t0:t1, h], q[b, t0:t1, h]
+                cq = chunk_quantities(K, V, g[b, t0:t1, h], eta[b, t0:t1, h], eps, beta_direct)
+                n = t1 - t0
+                P = cq["D"] * (Q @ K.T)
+                Lam = np.array([[lam[b, t0 + r, h, _level(t0 + r, t0 + s)] if s <= r else 0.0
+                                 for s in range(n)] for r in range(n)])
+                o[b, t0:t1, h] += ((P @ cq["T"]) * cq["beta"][None, :] * Lam) @ V
+            # one pass per level above the chunk: blocks of 2^(l - 1 - m) chunks per half
+            for lev in range(m + 1, L):
+                half = 1 << (lev - 1 - m)
+                for blk0 in range(0, len(bounds), 2 * half):
+                    S = np.zeros((dk, dv))
+                    for ci in range(blk0, min(blk0 + 2 * half, len(bounds))):
+                        t0, t1 = bounds[ci]
+                        writes = ci < blk0 + half
+                        Vc = v[b, t0:t1, h] if writes else np.zeros_like(v[b, t0:t1, h])
+                        O, S = chunk_step(q[b, t0:t1, h], k[b, t0:t1, h], Vc, g[b, t0:t1, h],
+                                          eta[b, t0:t1, h], eps, S, beta_direct)
+                        if not writes:
+                            o[b, t0:t1, h] += lam[b, t0:t1, h, lev][:, None] * O
+    return o

@@ -160,3 +160,19 @@ def test_loglinear_decoding_equals_the_by_origin_oracle(direct):
     ref = oracle.kla_oracle_loglinear_forward(q, k, v, g, eta, lam, 1e-6, beta_direct=direct)
     got = cm.loglinear_decode(q, k, v, g, eta, lam, 1e-6, beta_direct=direct)
     assert _rel(got, ref) <= 1e-11
+
+
+@pytest.mark.parametrize("C", [4, 16, 64])
+@pytest.mark.parametrize("T", [64, 130, 256, 333])
+@pytest.mark.parametrize("direct", [False, True])
+def test_loglinear_level_passes_equal_the_by_origin_oracle(C, T, direct):
+    """The Log-Linear output as one ordinary chunked pass per level above the
+    chunk (each aligned block restarted from zero, writes from its first half,
+    outputs in its second half) plus the in-chunk levels."""
+    q, k, v, g, eta, _ = _case(600 + T, B=1, T=T, dk=6, dv=4,
+                               knorm=(0.5, 1.2) if direct else (0.25, 4.0), h0_std=0.0)
+    L = oracle.loglinear_num_levels(T) + 1
+    lam = np.random.default_rng(T + 7).uniform(0.2, 1.5, (1, T, 2, L))
+    ref = oracle.kla_oracle_loglinear_forward(q, k, v, g, eta, lam, 1e-6, beta_direct=direct)
+    got = cm.loglinear_level_passes(q, k, v, g, eta, lam, 1e-6, C=C, beta_direct=direct)
+    assert _rel(got, ref) <= 1e-11
