@@ -26,6 +26,13 @@ bool sizes_fit(int B, int T, int H, int dk, int dv) {
     return toks <= (int64_t(1) << 46) / (dk > dv ? dk : dv);
 }
 
+// bf16 I/O at d_k = d_v = 128 runs on the tensor cores (the chunk records, an
+// in-chunk kernel and one carry pass per level above the chunk); the other
+// shapes keep the level states of every chunk start
+bool loglinear_on_tensor_cores(int dk, int dv, kla_io_dtype io) {
+    return io == KLA_IO_BF16 && dk == 128 && dv == 128;
+}
+
 }  // namespace
 
 extern "C" {
@@ -234,6 +241,7 @@ size_t kla_loglinear_workspace_bytes(int B, int T, int H, int dk, int dv, int ch
     if (B < 0 || T < 0 || H < 0 || check_io(io) != KLA_OK) return 0;
     if (!dim_ok(dk) || !dim_ok(dv) || chunk != 64) return 0;
     if (!sizes_fit(B, T, H, dk, dv) || (int64_t)B * H > 65535) return 0;
+    if (loglinear_on_tensor_cores(dk, dv, io)) return (kla::loglinear_tc_workspace_bytes(B, T, H) + 255) / 256 * 256;
     const size_t body = sizeof(float) * kla::loglinear_workspace_floats(B, T, H, dk, dv);
     return kla::kErrorRecordBytes + (body + 255) / 256 * 256;
 }
@@ -262,6 +270,9 @@ kla_status kla_loglinear_fwd(const void* q, const void* k, const void* v, const 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(workspace, 0, kla::kErrorRecordBytes, st);
     if (e != cudaSuccess) return KLA_ERR_CUDA;
+    if (loglinear_on_tensor_cores(dk, dv, io))
+        return to_status(kla::launch_loglinear_fwd_tc(q, k, v, g, eta, lambda, L, eps, o, B, T, H,
+                                                      beta == KLA_BETA_DIRECT, workspace, st));
     float* scratch = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kla::kErrorRecordBytes);
     return to_status(kla::launch_loglinear_fwd(q, k, v, g, eta, lambda, L, eps, o, B, T, H, dk, dv,
                                                io == KLA_IO_BF16, beta == KLA_BETA_DIRECT, scratch, st));

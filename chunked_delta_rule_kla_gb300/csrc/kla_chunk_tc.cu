@@ -728,6 +728,15 @@ struct CarryParams {
     // carrying, as in the scan's passes, the earlier requests only added to
     // the memory traffic in flight and the passes ran slower.
     int early_a;
+    // Log-Linear level pass (state_cta<false, true>): chunks are grouped in
+    // aligned blocks of lvl_bc chunks; the first half of a block writes (its
+    // values enter), the second half only takes the transitions and its
+    // outputs, scaled by lambda[b][t][h][lvl], are added into the fp32
+    // accumulator of tm_o; the state restarts from zero at each block.
+    int lvl_bc;             // block length in chunks (0: not a level pass)
+    int lvl;                // the level (index into lambda's last axis)
+    int L;                  // lambda's last extent
+    const float* lam;       // [B][T][H][L]
 };
 
 // mbarrier slots (all with arrival count 1)
@@ -1247,7 +1256,8 @@ struct StateLayout {
     static constexpr uint32_t kStageBytes = ((kVec + 768 + 1023) / 1024) * 1024;
     static constexpr uint32_t kO = 2 * kStageBytes;       // 2 x 2 boxes [64 tok][64] bf16
     static constexpr uint32_t kG = kO + 2 * 16384;        // 2 x (Gam_r, exp(gam_r - gam_C)) floats[64]
-    static constexpr uint32_t kMisc = kG + 1024;
+    static constexpr uint32_t kLam = kG + 1024;           // level pass: lambda of the chunk's tokens
+    static constexpr uint32_t kMisc = kLam + 256;
     static constexpr uint32_t kBars = kMisc + 64;
     static constexpr uint32_t kEnd = kBars + 32 * 8;
     static constexpr size_t kSmemBytes = kEnd + 1024;
@@ -1268,7 +1278,7 @@ enum { SB_FULLA0 = 0, SB_FULLB0 = SB_FULLA0 + kStages, SB_EMPTYA0 = SB_FULLB0 + 
 // joins the CTA-wide barriers.  (bx, h, bz) play the roles of the grid
 // coordinates (x: the SUMMARY half, y: head, z: batch * runs + run).  With
 // `flags`, the record of a chunk is copied only once its flag is set.
-template <bool SUMMARY>
+template <bool SUMMARY, bool LEVEL = false>
 __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                           const CUtensorMap& tm_v, const CUtensorMap& tm_o,
                                           const CarryParams& p, uint8_t* sm, const int bx, const int h,
@@ -1289,6 +1299,10 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
     const int nch = min(p.seg_chunks, p.c_end - c0);
     const size_t head = (size_t)b * H + h;
     Waiter wt{bars, abort_flag, p.err};
+    // level pass: chunk cc (relative) writes when it lies in the first half of
+    // its block, and the state restarts from zero after the block's last chunk
+    auto writes = [&](int cc) { return !LEVEL || ((c0 + cc) % p.lvl_bc) < (p.lvl_bc >> 1); };
+    auto block_end = [&](int cc) { return LEVEL && ((c0 + cc + 1) % p.lvl_bc) == 0; };
 
     if (tid == 0) {
         for (int i = 0; i < SB_COUNT; ++i) {
@@ -1406,7 +1420,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
         for (int k = 0; k < DK / 16; ++k)
             mma_bf16_ta(tmem + TS_D, tmem + TS_S0B + k * 8,
                         sdesc_sw128(sb + L::kWQ + (k / 4) * 16384 + (k % 4) * 32, 16, 1024), id_w,
-                        (vhalf || k > 0) ? 1u : 0u);
+                        ((vhalf && writes(cc)) || k > 0) ? 1u : 0u);   // onto U(c), which a no-write chunk skips
         mma_commit(&bars[SB_W]);
     };
     // S_acc (and with `merged`, (P W)^T in the next 64 columns)
@@ -1531,7 +1545,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
             if (ok) {
                 tc_fence_after();
                 if (elect_one()) {
-                    issue_u(0);
+                    if (writes(0)) issue_u(0);
                     mma_commit(&bars[SB_U]);
                     issue_qk(0);
                     mma_commit(&bars[SB_EMPTYB0]);   // Q K^T(0) reads group B
@@ -1556,7 +1570,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                 if (!(ok = wait1(SB_QSR, par, kWhereEPI, c))) break;
                 tc_fence_after();
                 if (elect_one()) {
-                    issue_u(c + 1);
+                    if (writes(c + 1)) issue_u(c + 1);
                     mma_commit(&bars[SB_U]);
                     mma_commit(&bars[SB_EMPTYA0 + s1]);   // Q K^T(c+1), U(c+1) read group A
                 }
@@ -1745,6 +1759,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
             // ---- S1^T = Gam_C S0^T + S_acc; bf16 copy for the next chunk
             if (!wt.group(SB_S, par, kWhereS, c, 3, 256)) break;
             tc_fence_after();
+            const bool keep = !block_end(c);   // level pass: the next block starts from zero
 #pragma unroll
             for (int hq = 0; hq < 2; ++hq) {
                 float acc[32];
@@ -1753,7 +1768,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                 tmem_ld_wait();
                 uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) master[32 * hq + i] = fmaf(GC, master[32 * hq + i], acc[i]);
+                for (int i = 0; i < 32; ++i) master[32 * hq + i] = keep ? fmaf(GC, master[32 * hq + i], acc[i]) : 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) pk[i] = pack2(master[32 * hq + 2 * i], master[32 * hq + 2 * i + 1]);
                 tmem_st_32x32b_x16u(tmem + lf + TS_S0B + 32 * hh + 16 * hq, pk);
@@ -1864,6 +1879,41 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
             // ---- o_r = Gam_r (S0^T Q^T)[., r] + (Wb^T P^T)[., r]: TMEM -> smem tile -> TMA store
             if (!wt.group(SB_PW, par, kWherePW, c, 4, 128)) break;
             tc_fence_after();
+            if constexpr (LEVEL) {
+                // level pass: only the second half of a block reads out; its
+                // rows, scaled by lambda_t^(lvl), are added into the fp32
+                // accumulator by a TMA reduction from a [64][32]-float box
+                // per 32 columns (one 32 KB tile, reused once the previous
+                // reduction has read it)
+                if (writes(c)) continue;
+                float* lamv = reinterpret_cast<float*>(sm + L::kLam);
+                if (at == 0) bulk_wait_read_le0();
+                if (at < C)
+                    lamv[at] = (t0 + at < p.T) ? p.lam[(((size_t)b * p.T + t0 + at) * H + h) * p.L + p.lvl] : 0.f;
+                bar_sync(2, 128);
+                float* ot = reinterpret_cast<float*>(sm + L::kO) + (j >> 5) * (C * 32) + (j & 31);
+#pragma unroll
+                for (int hq = 0; hq < 2; ++hq) {
+                    float b32[32];
+                    tmem_ld_32x32b_x32(tmem + lf + TS_PW + 32 * hq, b32);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int r = 32 * hq + i;
+                        ot[r * 32] = lamv[r] * (qs[r] + b32[i]);
+                    }
+                }
+                tc_fence_before();
+                fence_proxy_async_smem();
+                bar_sync(2, 128);
+                if (at == 0) {
+#pragma unroll
+                    for (int cb = 0; cb < 4; ++cb)
+                        tma_reduce_add_4d(&tm_o, sm + L::kO + cb * (C * 32 * 4), 32 * cb, h, t0, b);
+                    bulk_commit();
+                }
+                continue;
+            }
             if (at == 0) bulk_wait_read_le1();  // the store that last used this tile has read it
             bar_sync(2, 128);
             // o[r][j] goes to byte r*128 + ((j8 ^ (r & 7)) << 4) + (j & 7)*2 of
@@ -2282,7 +2332,348 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
     return cudaGetLastError();
 }
 
+// ============================================================================
+// Log-Linear gated delta rule on the tensor cores (bf16 I/O, d_k = d_v = 128).
+//
+// "Log-Linear Attention", technical summary section 2: token s lies in bucket
+// level l of token t > s when t and s first differ at bit l - 1, i.e. s is in
+// the first half and t in the second half of the aligned block of 2^l tokens
+// that holds both; o_t = sum_l lambda_t^(l) q_t^T S_t^(l).  With the delta
+// rule's transition acting on every bucket and each write kept in its token's
+// bucket, level l's contribution to o_t is the ordinary recurrence restarted
+// from zero at the block's start, with writes from the block's first half,
+// read out at t.  With chunks of C = 2^6 tokens:
+//   ll_inchunk_kernel  levels 0..6 (inside a chunk), every (chunk, head):
+//                      O_in = ((P T diag(beta)) o Lam) V, P = lower(D o Q K^T),
+//                      Lam[r][s] = lambda_r^(level(r, s)); writes the fp32
+//                      accumulator
+//   ll_level_kernel    levels 7..L-1: one ordinary carry pass per level over
+//                      aligned blocks of 2^(l-6) chunks (state_cta<false,
+//                      true>), writes in each block's first half, outputs of
+//                      its second half scaled by lambda^(l) and added into the
+//                      accumulator by TMA reductions
+//   ll_finish_kernel   o = bf16(accumulator)
+// The chunk records (T diag(beta), Wk, the decay vectors) come from the
+// ordinary prep kernel beforehand.
+// ============================================================================
+constexpr int kInThreads = 128;
+struct InLayout {
+    static constexpr uint32_t kQ = 0;          // 2 boxes [64][64] bf16
+    static constexpr uint32_t kK = 16384;
+    static constexpr uint32_t kV = 32768;
+    static constexpr uint32_t kTb = 49152;     // T diag(beta) [64][64] bf16 (the record's tile)
+    static constexpr uint32_t kP = 57344;      // P [r][s] bf16, then X [r][s]
+    static constexpr uint32_t kGam = 65536;    // gam[64] (the record's)
+    static constexpr uint32_t kLam = kGam + 256;             // lambda [64][8] (levels 0..6)
+    static constexpr uint32_t kBars = kLam + 64 * 8 * 4;
+    static constexpr uint32_t kMisc = kBars + 4 * 8;
+    static constexpr size_t kSmemBytes = kMisc + 64 + 1024;
+};
+
+__global__ void __launch_bounds__(kInThreads, 3)
+ll_inchunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const uint8_t* __restrict__ rec,
+                  const float* __restrict__ lam, int L, float* __restrict__ acc, int T, int H, int nchunks,
+                  DeviceErrorRecord* err) {
+    using IL = InLayout;
+    using R = Rec<128>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + IL::kBars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + IL::kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + IL::kMisc + 16);
+    float* gam = reinterpret_cast<float*>(sm + IL::kGam);
+    float* lamv = reinterpret_cast<float*>(sm + IL::kLam);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, hd = blockIdx.y, h = hd % H, b = hd / H;
+    const int t0 = c * C;
+    Waiter wt{bars, abort_flag, err};
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 128);
+        tmem_relinquish();
+    }
+    // lambda of the chunk's tokens at the in-chunk levels 0..6
+    for (int i = tid; i < C * 7; i += kInThreads) {
+        const int r = i / 7, l = i % 7;
+        lamv[r * 8 + l] = (t0 + r < T && l < L) ? lam[(((size_t)b * T + t0 + r) * H + h) * L + l] : 0.f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint8_t* rc = rec + ((size_t)hd * nchunks + c) * R::kBytes;
+    int armed = 1;   // (thread 0) barriers with a completion on the way: the copies, then each commit
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bars[0], 6 * 8192 + 8192 + 256);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            tma_load_4d(sm + IL::kQ + kb * 8192, &tm_q, &bars[0], kb * 64, h, t0, b);
+            tma_load_4d(sm + IL::kK + kb * 8192, &tm_k, &bars[0], kb * 64, h, t0, b);
+            tma_load_4d(sm + IL::kV + kb * 8192, &tm_v, &bars[0], kb * 64, h, t0, b);
+        }
+        bulk_load(sm + IL::kTb, rc + R::kTb, 8192, &bars[0]);
+        bulk_load(sm + IL::kGam, rc + R::kGam, 256, &bars[0]);
+    }
+    const int q = warp;                       // TMEM lane quadrant
+    const bool m64 = lane < 16;
+    const int r = q * 16 + lane;              // the M=64 row this thread holds
+    const uint32_t lf = (uint32_t)(q * 32) << 16;
+    bool ok = wt.group(0, 0, kWhereFull, c, 1, kInThreads);
+    // ---- Q K^T (M=64 N=64)
+    if (ok && tid == 0) {
+        tc_fence_after();
+        constexpr uint32_t id = idesc_bf16(64, 64, false, false);
+        const uint32_t sQ = smem_u32(sm + IL::kQ), sK = smem_u32(sm + IL::kK);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t off = (k / 4) * 8192 + (k % 4) * 32;
+            mma_bf16(tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), id, k > 0);
+        }
+        mma_commit(&bars[1]);
+        armed = 2;
+    }
+    ok = ok && wt.group(1, 0, kWherePrepG, c, 1, kInThreads);
+    if (ok) {
+        // ---- P[r][s] = exp(gam_r - gam_s) (q_r . k_s) for s <= r, bf16 A operand
+        tc_fence_after();
+        float row[64];
+        {
+            float lo[32], hi[32];
+            tmem_ld_32x32b_x32(tmem + lf, lo);
+            tmem_ld_32x32b_x32(tmem + lf + 32, hi);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) { row[i] = lo[i]; row[32 + i] = hi[i]; }
+        }
+        tc_fence_before();
+        if (m64) {
+            const float gr = gam[r];
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float v8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int s2 = c8 * 8 + i;
+                    v8[i] = s2 <= r ? __expf(gr - gam[s2]) * row[s2] : 0.f;
+                }
+                ST_CHUNK(sm + IL::kP, r, c8, v8, 0);
+            }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        // ---- P T diag(beta) (M=64 N=64; the record's tile as the MN-major B)
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc_bf16(64, 64, false, true);
+            const uint32_t sP = smem_u32(sm + IL::kP), sT = smem_u32(sm + IL::kTb);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16(tmem, sdesc_sw128(sP + k * 32, 16, 1024), sdesc_sw128(sT + k * 2048, 8192, 1024), id, k > 0);
+            mma_commit(&bars[2]);
+            armed = 3;
+        }
+    }
+    ok = ok && wt.group(2, 0, kWherePrepG, c, 1, kInThreads);
+    if (ok) {
+        // ---- X = (P T diag(beta)) o Lam, over P's tile
+        tc_fence_after();
+        float row[64];
+        {
+            float lo[32], hi[32];
+            tmem_ld_32x32b_x32(tmem + lf, lo);
+            tmem_ld_32x32b_x32(tmem + lf + 32, hi);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) { row[i] = lo[i]; row[32 + i] = hi[i]; }
+        }
+        tc_fence_before();
+        if (m64) {
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float v8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int s2 = c8 * 8 + i;
+                    const int lev = s2 == r ? 0 : 32 - __clz(r ^ s2);   // 1..6 inside a chunk
+                    v8[i] = s2 <= r ? row[s2] * lamv[r * 8 + lev] : 0.f;
+                }
+                ST_CHUNK(sm + IL::kP, r, c8, v8, 0);
+            }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        // ---- O_in = X V (M=64 N=128; V as the MN-major B)
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc_bf16(64, 128, false, true);
+            const uint32_t sX = smem_u32(sm + IL::kP), sV = smem_u32(sm + IL::kV);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16(tmem, sdesc_sw128(sX + k * 32, 16, 1024), sdesc_sw128(sV + k * 2048, 8192, 1024), id, k > 0);
+            mma_commit(&bars[3]);
+            armed = 4;
+        }
+    }
+    ok = ok && wt.group(3, 0, kWherePrepG, c, 1, kInThreads);
+    if (ok) {
+        tc_fence_after();
+        float* dst = acc + (((size_t)b * T + t0 + r) * H + h) * 128;
+#pragma unroll
+        for (int cc = 0; cc < 128; cc += 32) {
+            float v32[32];
+            tmem_ld_32x32b_x32(tmem + lf + cc, v32);
+            tmem_ld_wait();
+            if (m64 && t0 + r < T) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                    *reinterpret_cast<float4*>(dst + cc + i) = make_float4(v32[i], v32[i + 1], v32[i + 2], v32[i + 3]);
+            }
+        }
+        tc_fence_before();
+    }
+    if (tid == 0) {   // every MMA and copy of this CTA completes before TMEM is freed
+        for (int i = 0; i < armed; ++i) {
+            const uint64_t t1 = globaltimer_ns();
+            while (!mbar_try_wait_sleep(&bars[i], 0, kSuspendNs))
+                if (globaltimer_ns() - t1 > kTimeoutNs) break;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// One CTA per task: (level, head, group of whole blocks), the longest levels
+// first.  A task covers max(2^(l-6), group_min) chunks.
+__global__ void __launch_bounds__(kStateThreads, 1)
+ll_level_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_acc,
+                const CarryParams base, int nheads, int lvl_lo, int lvl_hi, int group_min) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    int i = blockIdx.x;
+    for (int lvl = lvl_hi - 1; lvl >= lvl_lo; --lvl) {
+        const int bc = 1 << (lvl - 6);
+        const int tc = bc > group_min ? bc : group_min;
+        const int nt = (base.nchunks + tc - 1) / tc;
+        if (i >= nt * nheads) {
+            i -= nt * nheads;
+            continue;
+        }
+        const int hd = i % nheads, t = i / nheads;
+        CarryParams cp = base;
+        cp.c_begin = t * tc;
+        cp.c_end = min(base.nchunks, cp.c_begin + tc);
+        cp.seg_chunks = tc;
+        cp.nseg = 1;
+        cp.lvl_bc = bc;
+        cp.lvl = lvl;
+        // a task that holds no second half of a block has nothing to read out
+        bool reads = false;
+        for (int cc = cp.c_begin; cc < cp.c_end && !reads; ++cc) reads = (cc % bc) >= (bc >> 1);
+        if (!reads) return;
+        state_cta<false, true>(tm_q, tm_k, tm_v, tm_acc, cp, sm, 0, hd % base.H, hd / base.H, nullptr);
+        return;
+    }
+}
+
+__global__ void __launch_bounds__(256) ll_finish_kernel(const float* __restrict__ acc,
+                                                       __nv_bfloat16* __restrict__ o, size_t n4) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+        const float4 v = reinterpret_cast<const float4*>(acc)[i];
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), c2 = __floats2bfloat162_rn(v.z, v.w);
+        reinterpret_cast<uint2*>(o)[i] =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&c2));
+    }
+}
+
+// the fp32 accumulator [B, T, H, 128] as 4-D (128, H, T, B); box 32 x 1 x 64 x 1
+bool make_acc_map(CUtensorMap* map, const float* base, int B, int T, int H) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {128, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+    cuuint64_t strides[3] = {128 * 4, (cuuint64_t)H * 128 * 4, (cuuint64_t)T * H * 128 * 4};
+    cuuint32_t box[4] = {32, 1, 64, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
+
+size_t loglinear_tc_workspace_bytes(int B, int T, int H) {
+    return kErrorRecordBytes + chunk_fwd_tc_record_bytes(B, T, H, 128) +
+           sizeof(float) * (size_t)B * T * H * 128;
+}
+
+cudaError_t launch_loglinear_fwd_tc(const void* q, const void* k, const void* v, const float* g,
+                                    const float* eta, const float* lam, int L, float eps, void* o, int B,
+                                    int T, int H, bool beta_direct, void* workspace, cudaStream_t stream) {
+    auto* err = reinterpret_cast<DeviceErrorRecord*>(workspace);
+    uint8_t* rec = reinterpret_cast<uint8_t*>(workspace) + kErrorRecordBytes;
+    float* acc = reinterpret_cast<float*>(rec + chunk_fwd_tc_record_bytes(B, T, H, 128));
+    CUtensorMap mq, mk, mv, macc;
+    if (!make_map(&mq, q, B, T, H, 128) || !make_map(&mk, k, B, T, H, 128) || !make_map(&mv, v, B, T, H, 128) ||
+        !make_acc_map(&macc, acc, B, T, H))
+        return cudaErrorInvalidValue;
+    static PerDevice attrs;
+    const cudaError_t attr_err = attrs.run([&](int, int&) {
+        cudaError_t r = cudaFuncSetAttribute(chunk_prep_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)PrepLayout<128>::kSmemBytes);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(ll_inchunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)InLayout::kSmemBytes);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(ll_level_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)StateLayout::kSmemBytes);
+        return r;
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int nchunks = (T + C - 1) / C;
+    const int nheads = B * H;
+    const int sms = sm_count();
+    cudaError_t e;
+    // chunk records: T diag(beta), Wk, the decay vectors
+    {
+        const int total = nchunks * nheads;
+        const int grid = total < kPrepPerSm * sms ? total : kPrepPerSm * sms;
+        PrepParams pp{g, eta, rec, err, eps, T, H, nchunks, B, 0, nchunks, 0, beta_direct ? 1 : 0};
+        chunk_prep_kernel<128><<<grid, kPrepThreads, PrepLayout<128>::kSmemBytes, stream>>>(mk, pp);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    ll_inchunk_kernel<<<dim3(nchunks, nheads), kInThreads, InLayout::kSmemBytes, stream>>>(
+        mq, mk, mv, rec, lam, L, acc, T, H, nchunks, err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // levels above the chunk: 7 .. top; a pair of tokens below T is at most
+    // at level ceil(log2 T), so higher entries of lambda are never read
+    int top = 0;
+    while (top < 31 && (1 << top) < T) ++top;
+    const int lvl_hi = L < top + 1 ? L : top + 1;
+    constexpr int kGroupMin = 16;
+    int64_t ntasks = 0;
+    for (int lvl = lvl_hi - 1; lvl >= 7; --lvl) {
+        const int64_t bc = int64_t(1) << (lvl - 6), tc = bc > kGroupMin ? bc : kGroupMin;
+        ntasks += (nchunks + tc - 1) / tc * nheads;
+    }
+    if (ntasks > INT32_MAX) return cudaErrorInvalidConfiguration;
+    if (ntasks > 0) {
+        CarryParams base{nullptr, rec, nullptr, nullptr, err, T, H, 128, nchunks, 1, nchunks, 0, nchunks, 0,
+                         0, 0, L, lam};
+        ll_level_kernel<<<(unsigned)ntasks, kStateThreads, StateLayout::kSmemBytes, stream>>>(mq, mk, mv, macc, base, nheads,
+                                                                                    7, lvl_hi, kGroupMin);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    const size_t n4 = (size_t)B * T * H * 128 / 4;
+    const size_t fb = (n4 + 255) / 256;
+    ll_finish_kernel<<<(unsigned)(fb < (size_t)sms * 16 ? fb : (size_t)sms * 16), 256, 0, stream>>>(
+        acc, reinterpret_cast<__nv_bfloat16*>(o), n4);
+    return cudaGetLastError();
+}
 
 size_t chunk_fwd_tc_record_bytes(int B, int T, int H, int dk) {
     const size_t nchunks = (size_t)((T + C - 1) / C);

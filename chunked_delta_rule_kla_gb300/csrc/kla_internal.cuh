@@ -132,6 +132,17 @@ cudaError_t launch_loglinear_fwd(const void* q, const void* k, const void* v, co
                                  int T, int H, int DK, int DV, bool bf16, bool beta_direct,
                                  float* scratch, cudaStream_t stream);
 
+// The same rule on the tensor cores for bf16 I/O with d_k = d_v = 128
+// (kla_chunk_tc.cu): the ordinary prep's chunk records, a per-chunk kernel
+// for the levels inside a chunk, one ordinary carry pass per level above the
+// chunk (outputs added into an fp32 accumulator), and a final conversion.
+// The workspace holds the error record, the chunk records and the
+// accumulator.
+size_t loglinear_tc_workspace_bytes(int B, int T, int H);
+cudaError_t launch_loglinear_fwd_tc(const void* q, const void* k, const void* v, const float* g,
+                                    const float* eta, const float* lam, int L, float eps, void* o, int B,
+                                    int T, int H, bool beta_direct, void* workspace, cudaStream_t stream);
+
 cudaError_t launch_loglinear_decode(const void* q, const void* k, const void* v, const float* g,
                                     const float* eta, const float* lam, int L, float eps, float* states,
                                     int t, void* o, int B, int H, int DK, int DV, bool bf16,

@@ -26,9 +26,11 @@ def _inputs(io, B, T, H, dk, dv, seed):
     return inp, lam
 
 
-def _check(io, B, T, H, dk, dv, seed, direct=False, heads=None):
+def _check(io, B, T, H, dk, dv, seed, direct=False, heads=None, tweak=None):
     kla = _kla()
     inp, lam = _inputs(io, B, T, H, dk, dv, seed)
+    if tweak is not None:
+        tweak(inp)
     beta = kla.KLA_BETA_DIRECT if direct else kla.KLA_BETA_KACZMARZ
     if direct:
         inp["k"] = torch.nn.functional.normalize(inp["k"].float(), dim=-1).to(inp["k"].dtype)
@@ -74,6 +76,22 @@ def test_loglinear_unit_weights_equal_chunk_fwd():
     o2, _ = kla.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["eta"], inp["eps"], None)
     torch.cuda.synchronize()
     assert rel_err(o, o2.double().cpu().numpy()) <= 1e-4
+
+
+def test_loglinear_batches_and_task_groups():
+    # bf16 d128 (the tensor-core path): 21 chunks, so the passes of levels
+    # 7..11 run several 16-chunk groups and end in a ragged chunk; B = 2
+    _check("bf16", 2, 1300, 3, 128, 128, 760)
+
+
+def test_loglinear_strong_decay_chunk():
+    # chunk 2 decays by about 2 per token (a span far above 80): the level
+    # passes take the direct P W branch there and the factorised one elsewhere
+    def strong(inp):
+        g = inp["g"].clone()
+        g[:, 128:192] *= 15.0
+        inp["g"] = g.contiguous()
+    _check("bf16", 1, 600, 2, 128, 128, 770, tweak=strong)
 
 
 def test_loglinear_training_shape_sampled_heads():
