@@ -374,7 +374,7 @@ __all__ = ["chunk_quantities", "chunk_step", "chunk_map", "chunk_forward", "chun
            "chunk_backward", "loglinear_chunk_forward", "loglinear_decode"]
 
 
-def loglinear_level_passes(q, k, v, g, eta, lam, eps, *, C=64, beta_direct=False):
+def loglinear_level_passes(q, k, v, g, eta, lam, eps, *, C=64, beta_direct=False, pair=False):
     """Log-Linear gated delta rule as independent passes of the ordinary
     chunked recurrence, one per level above the chunk.
 
@@ -387,7 +387,15 @@ def loglinear_level_passes(q, k, v, g, eta, lam, eps, *, C=64, beta_direct=False
     blocks of whole chunks: per block, the first-half chunks run the chunk
     step with their values, the second-half chunks run it with zero values
     (S1 = M S0, O = (diag(Gam) Q - P Wk) S0) and their outputs count.  Levels
-    0..m stay inside a chunk: O_in = ((P T diag(beta)) o Lam) V."""
+    0..m stay inside a chunk: O_in = ((P T diag(beta)) o Lam) V.
+
+    With ``pair``, levels 0..m+1 are taken over aligned pairs of chunks as
+    one chunk of 2C tokens, built from the two chunks' own quantities: with
+    A_21[r][s] = beta_r exp(gam_r - gam_s) (k_r . k_s) the block of A that
+    couples them (gam running over both), the inverse of the block lower
+    triangular I + A gives T diag(beta) = [[Tb_1, 0], [-Tb_2 A~_21 Tb_1,
+    Tb_2]] with Tb_i = T_i diag(beta_i) and A_21 = diag(beta_2) A~_21; the
+    passes then start at level m + 2."""
     q, k, v, g, eta, lam = map(_f64, (q, k, v, g, eta, lam))
     B, T, H, dk = k.shape
     dv = v.shape[-1]
@@ -398,8 +406,32 @@ def loglinear_level_passes(q, k, v, g, eta, lam, eps, *, C=64, beta_direct=False
     bounds = _bounds(T, C)
     for b in range(B):
         for h in range(H):
+            if pair:
+                for p0 in range(0, len(bounds), 2):
+                    t0 = bounds[p0][0]
+                    t1 = bounds[min(p0 + 1, len(bounds) - 1)][1]
+                    n = t1 - t0
+                    Q, K, V = q[b, t0:t1, h], k[b, t0:t1, h], v[b, t0:t1, h]
+                    n1 = bounds[p0][1] - t0
+                    c1 = chunk_quantities(K[:n1], V[:n1], g[b, t0:t0 + n1, h], eta[b, t0:t0 + n1, h], eps,
+                                          beta_direct)
+                    Tb = np.zeros((n, n))
+                    Tb[:n1, :n1] = c1["T"] * c1["beta"][None, :]
+                    gam = np.cumsum(g[b, t0:t1, h])
+                    if n > n1:
+                        c2 = chunk_quantities(K[n1:], V[n1:], g[b, t0 + n1:t1, h], eta[b, t0 + n1:t1, h], eps,
+                                              beta_direct)
+                        Tb2 = c2["T"] * c2["beta"][None, :]
+                        At = np.exp(gam[n1:, None] - gam[None, :n1]) * (K[n1:] @ K[:n1].T)
+                        Tb[n1:, n1:] = Tb2
+                        Tb[n1:, :n1] = -Tb2 @ At @ Tb[:n1, :n1]
+                    lower = np.tril(np.ones((n, n), dtype=bool))
+                    P = np.where(lower, np.exp(np.where(lower, gam[:, None] - gam[None, :], 0.0)), 0.0) * (Q @ K.T)
+                    Lam = np.array([[lam[b, t0 + r, h, _level(t0 + r, t0 + s)] if s <= r else 0.0
+                                     for s in range(n)] for r in range(n)])
+                    o[b, t0:t1, h] += ((P @ Tb) * Lam) @ V
             # in-chunk levels 0..m
-            for t0, t1 in bounds:
+            for t0, t1 in (() if pair else bounds):
                 K, V, Q = k[b, t0:t1, h], v[b, t0:t1, h], q[b, t0:t1, h]
                 cq = chunk_quantities(K, V, g[b, t0:t1, h], eta[b, t0:t1, h], eps, beta_direct)
                 n = t1 - t0
@@ -408,7 +440,7 @@ def loglinear_level_passes(q, k, v, g, eta, lam, eps, *, C=64, beta_direct=False
                                  for s in range(n)] for r in range(n)])
                 o[b, t0:t1, h] += ((P @ cq["T"]) * cq["beta"][None, :] * Lam) @ V
             # one pass per level above the chunk: blocks of 2^(l - 1 - m) chunks per half
-            for lev in range(m + 1, L):
+            for lev in range(m + 2 if pair else m + 1, L):
                 half = 1 << (lev - 1 - m)
                 for blk0 in range(0, len(bounds), 2 * half):
                     S = np.zeros((dk, dv))

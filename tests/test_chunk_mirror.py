@@ -176,3 +176,20 @@ def test_loglinear_level_passes_equal_the_by_origin_oracle(C, T, direct):
     ref = oracle.kla_oracle_loglinear_forward(q, k, v, g, eta, lam, 1e-6, beta_direct=direct)
     got = cm.loglinear_level_passes(q, k, v, g, eta, lam, 1e-6, C=C, beta_direct=direct)
     assert _rel(got, ref) <= 1e-11
+
+
+@pytest.mark.parametrize("C", [4, 16, 64])
+@pytest.mark.parametrize("T", [64, 100, 130, 256, 333])
+@pytest.mark.parametrize("direct", [False, True])
+def test_loglinear_chunk_pairs_equal_the_by_origin_oracle(C, T, direct):
+    """Levels 0..m+1 over aligned pairs of chunks, with the pair's
+    T diag(beta) assembled from the two chunks' own (the block inverse), and
+    the passes from level m + 2; ragged T leaves a pair with one chunk or a
+    short second chunk."""
+    q, k, v, g, eta, _ = _case(800 + T, B=1, T=T, dk=6, dv=4,
+                               knorm=(0.5, 1.2) if direct else (0.25, 4.0), h0_std=0.0)
+    L = oracle.loglinear_num_levels(T) + 1
+    lam = np.random.default_rng(T + 9).uniform(0.2, 1.5, (1, T, 2, L))
+    ref = oracle.kla_oracle_loglinear_forward(q, k, v, g, eta, lam, 1e-6, beta_direct=direct)
+    got = cm.loglinear_level_passes(q, k, v, g, eta, lam, 1e-6, C=C, beta_direct=direct, pair=True)
+    assert _rel(got, ref) <= 1e-11
