@@ -504,9 +504,10 @@ def bench_loglinear(case, K, W, flush, peaks, stream):
     mean_ms = slowest_s * 1e3
     res = dict(ms_per_step=mean_ms, tokens_per_s=work["tokens"] / (mean_ms * 1e-3), levels=L,
                roofline=dict(roofline(work, mean_ms * 1e-3, peaks, TRAFFIC_BYTES.get("loglinear_" + case.name)),
-                             scope="one kla_loglinear_fwd call: its three launches (chunk, carry, output)",
+                             scope="one kla_loglinear_fwd call: its four launches (chunk records, in-chunk levels, "
+                                   "one carry pass per level above the chunk, bf16 conversion)",
                              peak_kind="burst copy bandwidth"),
-               launches=3 * K, min_ms=min(ms))
+               launches=4 * K, min_ms=min(ms))
     del inp, lam, o, ws
     return res
 

@@ -1811,6 +1811,10 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
             const int t0 = (c0 + c) * C;
             const float* gam = reinterpret_cast<const float*>(sm + (c % kStages) * L::kStageBytes + L::kVec);
             float* Gp = reinterpret_cast<float*>(sm + L::kG) + par * C;  // Gam_r
+            // level pass: lambda of a read-out chunk's tokens, requested before its P is formed
+            float lam_at = 0.f;
+            if (LEVEL && !writes(c) && at < C && t0 + at < p.T)
+                lam_at = p.lam[(((size_t)b * p.T + t0 + at) * H + h) * p.L + p.lvl];
             // ---- from K Q^T (lane row s): P'^T [s][r] = exp(gam_r - gam_C) (k_s . q_r) for s <= r,
             // rows written whole; with strong decay P [r][s] = exp(gam_r - gam_s) (q_r . k_s),
             // columns written element by element.  Gam_r is kept for the epilogue.
@@ -1888,8 +1892,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                 if (writes(c)) continue;
                 float* lamv = reinterpret_cast<float*>(sm + L::kLam);
                 if (at == 0) bulk_wait_read_le0();
-                if (at < C)
-                    lamv[at] = (t0 + at < p.T) ? p.lam[(((size_t)b * p.T + t0 + at) * H + h) * p.L + p.lvl] : 0.f;
+                if (at < C) lamv[at] = lam_at;
                 bar_sync(2, 128);
                 float* ot = reinterpret_cast<float*>(sm + L::kO) + (j >> 5) * (C * 32) + (j & 31);
 #pragma unroll
@@ -2343,11 +2346,17 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
 // bucket, level l's contribution to o_t is the ordinary recurrence restarted
 // from zero at the block's start, with writes from the block's first half,
 // read out at t.  With chunks of C = 2^6 tokens:
-//   ll_inchunk_kernel  levels 0..6 (inside a chunk), every (chunk, head):
-//                      O_in = ((P T diag(beta)) o Lam) V, P = lower(D o Q K^T),
-//                      Lam[r][s] = lambda_r^(level(r, s)); writes the fp32
-//                      accumulator
-//   ll_level_kernel    levels 7..L-1: one ordinary carry pass per level over
+//   ll_pair_kernel     levels 0..7, every aligned pair of chunks (one chunk of
+//                      128 tokens) and head: O_in = ((P Tb) o Lam) V with P =
+//                      lower(D o Q K^T) over the pair, Lam[r][s] =
+//                      lambda_r^(level(r, s)) and Tb = T diag(beta) of the pair,
+//                      assembled from the two chunks' records: the inverse of
+//                      the block lower triangular I + A is
+//                      [[Tb_1, 0], [-Tb_2 A~_21 Tb_1, Tb_2]] with
+//                      A~_21[r][s] = exp(G_r - G_s) (k_r . k_s) the coupling
+//                      block (G the decay exponent running over the pair);
+//                      writes the fp32 accumulator
+//   ll_level_kernel    levels 8..: one ordinary carry pass per level over
 //                      aligned blocks of 2^(l-6) chunks (state_cta<false,
 //                      true>), writes in each block's first half, outputs of
 //                      its second half scaled by lambda^(l) and added into the
@@ -2356,195 +2365,366 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
 // The chunk records (T diag(beta), Wk, the decay vectors) come from the
 // ordinary prep kernel beforehand.
 // ============================================================================
-constexpr int kInThreads = 128;
-struct InLayout {
-    static constexpr uint32_t kQ = 0;          // 2 boxes [64][64] bf16
-    static constexpr uint32_t kK = 16384;
-    static constexpr uint32_t kV = 32768;
-    static constexpr uint32_t kTb = 49152;     // T diag(beta) [64][64] bf16 (the record's tile)
-    static constexpr uint32_t kP = 57344;      // P [r][s] bf16, then X [r][s]
-    static constexpr uint32_t kGam = 65536;    // gam[64] (the record's)
-    static constexpr uint32_t kLam = kGam + 256;             // lambda [64][8] (levels 0..6)
-    static constexpr uint32_t kBars = kLam + 64 * 8 * 4;
-    static constexpr uint32_t kMisc = kBars + 4 * 8;
+constexpr int kPairThreads = 256;
+struct PairLayout {
+    // operand tiles are 128-byte swizzled rows of 64 bf16
+    static constexpr uint32_t kQ = 0;          // Q boxes [d half][token half] (32 KB); then P, then X:
+                                               // [s half][128 rows][64]
+    static constexpr uint32_t kK = 32768;      // K boxes [d half][token half]; then V the same way
+    static constexpr uint32_t kTb1 = 65536;    // T diag(beta) of the first chunk [r][s]
+    static constexpr uint32_t kTb2 = 73728;    // of the second
+    static constexpr uint32_t kA = 81920;      // A~_21 [r][s], then X_21 = -Tb_2 A~_21 Tb_1 [r][s]
+    static constexpr uint32_t kY = 90112;      // A~_21 Tb_1 [r][s]
+    static constexpr uint32_t kGam = 98304;    // the two records' gam (float[64] each)
+    static constexpr uint32_t kG = kGam + 512;              // G[128], the exponent over the pair
+    static constexpr uint32_t kU = kG + 512;                // exp(G_r - G_m) [128]
+    static constexpr uint32_t kW = kU + 512;                // exp(G_m - G_s) [128]
+    static constexpr uint32_t kLam = kW + 512;              // lambda [8][128] (levels 0..7)
+    static constexpr uint32_t kBars = kLam + 128 * 8 * 4;
+    static constexpr uint32_t kMisc = kBars + 8 * 8;
     static constexpr size_t kSmemBytes = kMisc + 64 + 1024;
+    // the fp32 output is staged over Q and K's space as [col block][token half][64][32], 128-byte
+    // swizzled like the accumulator's store map
 };
+static_assert(2 * (PairLayout::kSmemBytes + 1024) <= 228 * 1024, "two pair CTAs per SM");
 
-__global__ void __launch_bounds__(kInThreads, 3)
-ll_inchunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const uint8_t* __restrict__ rec,
-                  const float* __restrict__ lam, int L, float* __restrict__ acc, int T, int H, int nchunks,
-                  DeviceErrorRecord* err) {
-    using IL = InLayout;
+// 8 bf16 of a P-like row chunk: row r, columns s0..s0+7, value f(s) for s <= r, else 0
+template <typename F>
+__device__ __forceinline__ void pair_chunk(uint8_t* tile, int r, int c8, int s0, F f) {
+    float v8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v8[i] = (s0 + i <= r) ? f(i) : 0.f;
+    ST_CHUNK(tile, r, c8, v8, 0);
+}
+
+__global__ void __launch_bounds__(kPairThreads, 2)
+ll_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_acc_sw,
+               const uint8_t* __restrict__ rec, const float* __restrict__ lam, int L, int T, int H,
+               int nchunks, DeviceErrorRecord* err) {
+    using PL = PairLayout;
     using R = Rec<128>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + IL::kBars);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + IL::kMisc);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + IL::kMisc + 16);
-    float* gam = reinterpret_cast<float*>(sm + IL::kGam);
-    float* lamv = reinterpret_cast<float*>(sm + IL::kLam);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PL::kBars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PL::kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + PL::kMisc + 16);
+    float* gam = reinterpret_cast<float*>(sm + PL::kGam);
+    float* G = reinterpret_cast<float*>(sm + PL::kG);
+    float* U = reinterpret_cast<float*>(sm + PL::kU);
+    float* Wf = reinterpret_cast<float*>(sm + PL::kW);
+    float* lamv = reinterpret_cast<float*>(sm + PL::kLam);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, hd = blockIdx.y, h = hd % H, b = hd / H;
-    const int t0 = c * C;
+    // warps q and q + 4 share TMEM lane quadrant q; ch picks the half of the columns
+    const int q = warp & 3, ch = warp >> 2;
+    const int r = 32 * q + lane;                          // row of the M = 128 products
+    const int pr = blockIdx.x, hd = blockIdx.y, h = hd % H, b = hd / H;
+    const int c1 = 2 * pr;
+    const bool has2 = c1 + 1 < nchunks;
+    const int t0 = c1 * C;
+    // barriers: Q, K and the records; V; Q K^T and K_2 K_1^T; Y; X_21; R = P Tb; O
+    enum { PB_IN = 0, PB_V, PB_QK, PB_Y, PB_X, PB_R, PB_O, PB_COUNT };
     Waiter wt{bars, abort_flag, err};
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < PB_COUNT; ++i) mbar_init(&bars[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, 128);
+        tmem_alloc(tmem_slot, 256);
         tmem_relinquish();
     }
-    // lambda of the chunk's tokens at the in-chunk levels 0..6
-    for (int i = tid; i < C * 7; i += kInThreads) {
-        const int r = i / 7, l = i % 7;
-        lamv[r * 8 + l] = (t0 + r < T && l < L) ? lam[(((size_t)b * T + t0 + r) * H + h) * L + l] : 0.f;
+    if (!has2) {   // no second chunk: its T diag(beta) is zero, so X_21 and its rows of R vanish
+        for (int i = tid; i < 2048; i += kPairThreads) reinterpret_cast<uint32_t*>(sm + PL::kTb2)[i] = 0u;
+        if (tid < 64) gam[64 + tid] = 0.f;
+        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint8_t* rc = rec + ((size_t)hd * nchunks + c) * R::kBytes;
-    int armed = 1;   // (thread 0) barriers with a completion on the way: the copies, then each commit
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&bars[0], 6 * 8192 + 8192 + 256);
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-            tma_load_4d(sm + IL::kQ + kb * 8192, &tm_q, &bars[0], kb * 64, h, t0, b);
-            tma_load_4d(sm + IL::kK + kb * 8192, &tm_k, &bars[0], kb * 64, h, t0, b);
-            tma_load_4d(sm + IL::kV + kb * 8192, &tm_v, &bars[0], kb * 64, h, t0, b);
-        }
-        bulk_load(sm + IL::kTb, rc + R::kTb, 8192, &bars[0]);
-        bulk_load(sm + IL::kGam, rc + R::kGam, 256, &bars[0]);
-    }
-    const int q = warp;                       // TMEM lane quadrant
-    const bool m64 = lane < 16;
-    const int r = q * 16 + lane;              // the M=64 row this thread holds
+    const uint32_t D0 = tmem, D1 = tmem + 128;             // [128 x 128] and [64 x 64] accumulators
     const uint32_t lf = (uint32_t)(q * 32) << 16;
-    bool ok = wt.group(0, 0, kWhereFull, c, 1, kInThreads);
-    // ---- Q K^T (M=64 N=64)
+    const uint32_t sQ = smem_u32(sm + PL::kQ), sK = smem_u32(sm + PL::kK);
+    const uint32_t sTb1 = smem_u32(sm + PL::kTb1), sTb2 = smem_u32(sm + PL::kTb2);
+    const uint32_t sA = smem_u32(sm + PL::kA), sY = smem_u32(sm + PL::kY);
+    const uint8_t* rc1 = rec + ((size_t)hd * nchunks + c1) * R::kBytes;
+    int armed = 1;   // (thread 0) barriers with a completion on the way: the inputs, then in order
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bars[PB_IN], 8 * 8192 + 8192 + 256 + (has2 ? 8192 + 256 : 0));
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+            for (int th = 0; th < 2; ++th) {
+                tma_load_4d(sm + PL::kQ + kb * 16384 + th * 8192, &tm_q, &bars[PB_IN], kb * 64, h, t0 + th * 64, b);
+                tma_load_4d(sm + PL::kK + kb * 16384 + th * 8192, &tm_k, &bars[PB_IN], kb * 64, h, t0 + th * 64, b);
+            }
+        bulk_load(sm + PL::kTb1, rc1 + R::kTb, 8192, &bars[PB_IN]);
+        bulk_load(sm + PL::kGam, rc1 + R::kGam, 256, &bars[PB_IN]);
+        if (has2) {
+            bulk_load(sm + PL::kTb2, rc1 + R::kBytes + R::kTb, 8192, &bars[PB_IN]);
+            bulk_load(sm + PL::kGam + 256, rc1 + R::kBytes + R::kGam, 256, &bars[PB_IN]);
+        }
+    }
+    {   // lambda of levels 0..7 as [level][token], all loads in flight together
+        float lv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = tid + j * kPairThreads, rr = i >> 3, l = i & 7;
+            lv[j] = (t0 + rr < T && l < L) ? lam[(((size_t)b * T + t0 + rr) * H + h) * L + l] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = tid + j * kPairThreads;
+            lamv[(i & 7) * 128 + (i >> 3)] = lv[j];
+        }
+    }
+    bool ok = wt.group(PB_IN, 0, kWhereFull, pr, 1, kPairThreads);
     if (ok && tid == 0) {
         tc_fence_after();
-        constexpr uint32_t id = idesc_bf16(64, 64, false, false);
-        const uint32_t sQ = smem_u32(sm + IL::kQ), sK = smem_u32(sm + IL::kK);
+        constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);
+        constexpr uint32_t id_g = idesc_bf16(64, 64, false, false);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const uint32_t off = (k / 4) * 8192 + (k % 4) * 32;
-            mma_bf16(tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), id, k > 0);
+            const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+            mma_bf16(D0, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), id_qk, k > 0);
         }
-        mma_commit(&bars[1]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {   // K_2 K_1^T: rows of the second token half against the first
+            const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+            mma_bf16(D1, sdesc_sw128(sK + off + 8192, 16, 1024), sdesc_sw128(sK + off, 16, 1024), id_g, k > 0);
+        }
+        mma_commit(&bars[PB_QK]);
         armed = 2;
     }
-    ok = ok && wt.group(1, 0, kWherePrepG, c, 1, kInThreads);
-    if (ok) {
-        // ---- P[r][s] = exp(gam_r - gam_s) (q_r . k_s) for s <= r, bf16 A operand
-        tc_fence_after();
-        float row[64];
-        {
-            float lo[32], hi[32];
-            tmem_ld_32x32b_x32(tmem + lf, lo);
-            tmem_ld_32x32b_x32(tmem + lf + 32, hi);
-            tmem_ld_wait();
+    if (ok && tid < 128) G[tid] = tid < C ? gam[tid] : gam[C - 1] + gam[tid];   // gam[64 + r2]: second record
+    ok = ok && !bar_or(1, kPairThreads, false);
+    // exp(G_r - G_s) = u_r w_s about the middle token when the pair's decay
+    // span allows it (every factor finite), else one exponential per entry
+    const bool fact = ok && (G[0] - G[127]) <= kSpanMax;
+    if (ok && tid < 128) {
+        U[tid] = __expf(G[tid] - G[63]);
+        Wf[tid] = __expf(G[63] - G[tid]);
+    }
+    ok = ok && wt.group(PB_QK, 0, kWherePrepG, pr, 1, kPairThreads);
+    if (ok && tid == 0) {   // V over K, which both products have read
+        mbar_arrive_expect_tx(&bars[PB_V], 4 * 8192);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) { row[i] = lo[i]; row[32 + i] = hi[i]; }
-        }
-        tc_fence_before();
-        if (m64) {
-            const float gr = gam[r];
+        for (int dh = 0; dh < 2; ++dh)
+#pragma unroll
+            for (int th = 0; th < 2; ++th)
+                tma_load_4d(sm + PL::kK + dh * 16384 + th * 8192, &tm_v, &bars[PB_V], dh * 64, h, t0 + th * 64, b);
+        armed = 3;
+    }
+    if (ok) {
+        // ---- P[r][s] = exp(G_r - G_s) (q_r . k_s) for s <= r, over Q's space;
+        // this warp: columns 64 ch .. 64 ch + 63
+        tc_fence_after();
+        uint8_t* Pt = sm + PL::kQ + ch * 16384;
+        const int s_base = 64 * ch;
+        if (s_base > 32 * q + 31) {   // the whole warp is above the diagonal
+            const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) ST_CHUNK(Pt, r, c8, z, 0);
+        } else {
+            float v[64];
+            tmem_ld_32x32b_x32(D0 + lf + s_base, *reinterpret_cast<float(*)[32]>(v));
+            tmem_ld_32x32b_x32(D0 + lf + s_base + 32, *reinterpret_cast<float(*)[32]>(v + 32));
+            tmem_ld_wait();
+            const float ur = U[r], Gr = G[r];
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {
-                float v8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int s2 = c8 * 8 + i;
-                    v8[i] = s2 <= r ? __expf(gr - gam[s2]) * row[s2] : 0.f;
-                }
-                ST_CHUNK(sm + IL::kP, r, c8, v8, 0);
+                const int s0 = s_base + 8 * c8;
+                const float4 w0 = *reinterpret_cast<const float4*>((fact ? Wf : G) + s0);
+                const float4 w1 = *reinterpret_cast<const float4*>((fact ? Wf : G) + s0 + 4);
+                const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                if (fact)
+                    pair_chunk(Pt, r, c8, s0, [&](int i) { return ur * v[8 * c8 + i] * wv[i]; });
+                else
+                    pair_chunk(Pt, r, c8, s0, [&](int i) { return __expf(Gr - wv[i]) * v[8 * c8 + i]; });
             }
         }
-        fence_proxy_async_smem();
-        __syncthreads();
-        // ---- P T diag(beta) (M=64 N=64; the record's tile as the MN-major B)
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id = idesc_bf16(64, 64, false, true);
-            const uint32_t sP = smem_u32(sm + IL::kP), sT = smem_u32(sm + IL::kTb);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16(tmem, sdesc_sw128(sP + k * 32, 16, 1024), sdesc_sw128(sT + k * 2048, 8192, 1024), id, k > 0);
-            mma_commit(&bars[2]);
-            armed = 3;
-        }
-    }
-    ok = ok && wt.group(2, 0, kWherePrepG, c, 1, kInThreads);
-    if (ok) {
-        // ---- X = (P T diag(beta)) o Lam, over P's tile
-        tc_fence_after();
-        float row[64];
+        // ---- A~_21[r2][s] = exp(G_{64+r2} - G_s) (k_{64+r2} . k_s): M = 64 rows in
+        // lanes 0..15; this warp: columns 32 ch .. 32 ch + 31
         {
-            float lo[32], hi[32];
-            tmem_ld_32x32b_x32(tmem + lf, lo);
-            tmem_ld_32x32b_x32(tmem + lf + 32, hi);
+            float a[32];
+            tmem_ld_32x32b_x32(D1 + lf + 32 * ch, a);
             tmem_ld_wait();
+            if (lane < 16) {
+                const int r2 = q * 16 + lane;
+                const float u2 = U[C + r2], G2 = G[C + r2];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) { row[i] = lo[i]; row[32 + i] = hi[i]; }
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    const int s0 = 32 * ch + 8 * c8;
+                    const float4 w0 = *reinterpret_cast<const float4*>((fact ? Wf : G) + s0);
+                    const float4 w1 = *reinterpret_cast<const float4*>((fact ? Wf : G) + s0 + 4);
+                    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                    float v8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        v8[i] = fact ? u2 * a[8 * c8 + i] * wv[i] : __expf(G2 - wv[i]) * a[8 * c8 + i];
+                    ST_CHUNK(sm + PL::kA, r2, 4 * ch + c8, v8, 0);
+                }
+            }
         }
         tc_fence_before();
-        if (m64) {
+        fence_proxy_async_smem();
+    }
+    ok = ok && !bar_or(1, kPairThreads, false);
+    if (ok && tid == 0) {   // Y = A~_21 Tb_1 (Tb_1 as the MN-major B)
+        tc_fence_after();
+        constexpr uint32_t id = idesc_bf16(64, 64, false, true);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            mma_bf16(D1, sdesc_sw128(sA + k * 32, 16, 1024), sdesc_sw128(sTb1 + k * 2048, 8192, 1024), id, k > 0);
+        mma_commit(&bars[PB_Y]);
+        armed = 4;
+    }
+    ok = ok && wt.group(PB_Y, 0, kWherePrepG, pr, 1, kPairThreads);
+    if (ok) {
+        tc_fence_after();
+        float y[32];
+        tmem_ld_32x32b_x32(D1 + lf + 32 * ch, y);
+        tmem_ld_wait();
+        if (lane < 16) {
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) ST_CHUNK(sm + PL::kY, q * 16 + lane, 4 * ch + c8, y, 8 * c8);
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+    }
+    ok = ok && !bar_or(1, kPairThreads, false);
+    if (ok && tid == 0) {   // Tb_2 Y (Y as the MN-major B)
+        tc_fence_after();
+        constexpr uint32_t id = idesc_bf16(64, 64, false, true);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            mma_bf16(D1, sdesc_sw128(sTb2 + k * 32, 16, 1024), sdesc_sw128(sY + k * 2048, 8192, 1024), id, k > 0);
+        mma_commit(&bars[PB_X]);
+        armed = 5;
+    }
+    ok = ok && wt.group(PB_X, 0, kWherePrepG, pr, 1, kPairThreads);
+    if (ok) {   // X_21 = -Tb_2 Y over A~_21 (read by the Y product, which is complete)
+        tc_fence_after();
+        float x[32];
+        tmem_ld_32x32b_x32(D1 + lf + 32 * ch, x);
+        tmem_ld_wait();
+        if (lane < 16) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = -x[i];
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) ST_CHUNK(sm + PL::kA, q * 16 + lane, 4 * ch + c8, x, 8 * c8);
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+    }
+    ok = ok && !bar_or(1, kPairThreads, false);
+    if (ok && tid == 0) {
+        // R = P Tb: columns 0..63 over K = 128 rows [Tb_1 ; X_21], columns
+        // 64..127 over the rows of Tb_2 (P is zero above its diagonal blocks)
+        tc_fence_after();
+        constexpr uint32_t id = idesc_bf16(128, 64, false, true);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t bo = k < 4 ? sTb1 + k * 2048 : sA + (k - 4) * 2048;
+            mma_bf16(D0, sdesc_sw128(sQ + (k / 4) * 16384 + (k % 4) * 32, 16, 1024), sdesc_sw128(bo, 8192, 1024),
+                     id, k > 0);
+        }
+#pragma unroll
+        for (int k = 4; k < 8; ++k)
+            mma_bf16(D0 + 64, sdesc_sw128(sQ + 16384 + (k % 4) * 32, 16, 1024),
+                     sdesc_sw128(sTb2 + (k - 4) * 2048, 8192, 1024), id, k > 4);
+        mma_commit(&bars[PB_R]);
+        armed = 6;
+    }
+    ok = ok && wt.group(PB_R, 0, kWherePrepG, pr, 1, kPairThreads);
+    if (ok) {
+        // ---- X = R o Lam over P (R, its last reader, is complete).  For s < r
+        // the level is 1 + floor(log2(r ^ s)): over a chunk of 8 columns away
+        // from the row's own it is 4 + floor(log2((r >> 3) ^ c)), one value
+        tc_fence_after();
+        uint8_t* Xt = sm + PL::kQ + ch * 16384;
+        const int s_base = 64 * ch;
+        if (s_base > 32 * q + 31) {
+            const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) ST_CHUNK(Xt, r, c8, z, 0);
+        } else {
+            float lr[8];
+#pragma unroll
+            for (int l = 0; l < 8; ++l) lr[l] = lamv[l * 128 + r];
+            float v[64];
+            tmem_ld_32x32b_x32(D0 + lf + s_base, *reinterpret_cast<float(*)[32]>(v));
+            tmem_ld_32x32b_x32(D0 + lf + s_base + 32, *reinterpret_cast<float(*)[32]>(v + 32));
+            tmem_ld_wait();
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {
-                float v8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int s2 = c8 * 8 + i;
-                    const int lev = s2 == r ? 0 : 32 - __clz(r ^ s2);   // 1..6 inside a chunk
-                    v8[i] = s2 <= r ? row[s2] * lamv[r * 8 + lev] : 0.f;
-                }
-                ST_CHUNK(sm + IL::kP, r, c8, v8, 0);
-            }
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-        // ---- O_in = X V (M=64 N=128; V as the MN-major B)
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id = idesc_bf16(64, 128, false, true);
-            const uint32_t sX = smem_u32(sm + IL::kP), sV = smem_u32(sm + IL::kV);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16(tmem, sdesc_sw128(sX + k * 32, 16, 1024), sdesc_sw128(sV + k * 2048, 8192, 1024), id, k > 0);
-            mma_commit(&bars[3]);
-            armed = 4;
-        }
-    }
-    ok = ok && wt.group(3, 0, kWherePrepG, c, 1, kInThreads);
-    if (ok) {
-        tc_fence_after();
-        float* dst = acc + (((size_t)b * T + t0 + r) * H + h) * 128;
-#pragma unroll
-        for (int cc = 0; cc < 128; cc += 32) {
-            float v32[32];
-            tmem_ld_32x32b_x32(tmem + lf + cc, v32);
-            tmem_ld_wait();
-            if (m64 && t0 + r < T) {
-#pragma unroll
-                for (int i = 0; i < 32; i += 4)
-                    *reinterpret_cast<float4*>(dst + cc + i) = make_float4(v32[i], v32[i + 1], v32[i + 2], v32[i + 3]);
+                const int s0 = s_base + 8 * c8;
+                const int hb = (r >> 3) ^ (s0 >> 3);               // 0 on the row's own chunk
+                const int lo = hb ? 31 - __clz(hb) : 0;            // 0..3
+                const float lam_far = lo == 0 ? lr[4] : lo == 1 ? lr[5] : lo == 2 ? lr[6] : lr[7];
+                pair_chunk(Xt, r, c8, s0, [&](int i) {
+                    const int d = r ^ (s0 + i);                    // < 8 on the row's own chunk
+                    const float lam_rs = hb ? lam_far
+                                            : (d == 0 ? lr[0] : d == 1 ? lr[1] : d < 4 ? lr[2] : lr[3]);
+                    return v[8 * c8 + i] * lam_rs;
+                });
             }
         }
         tc_fence_before();
+        fence_proxy_async_smem();
     }
-    if (tid == 0) {   // every MMA and copy of this CTA completes before TMEM is freed
+    ok = ok && wt.group(PB_V, 0, kWhereFull, pr, 1, kPairThreads);
+    if (ok && tid == 0) {   // O = X V (V as the MN-major B: two 64-column atoms 16 KB apart)
+        tc_fence_after();
+        constexpr uint32_t id = idesc_bf16(128, 128, false, true);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            mma_bf16(D0, sdesc_sw128(sQ + (k / 4) * 16384 + (k % 4) * 32, 16, 1024),
+                     sdesc_sw128(sK + k * 2048, 16384, 1024), id, k > 0);
+        mma_commit(&bars[PB_O]);
+        armed = 7;
+    }
+    ok = ok && wt.group(PB_O, 0, kWherePrepG, pr, 1, kPairThreads);
+    if (ok) {
+        // ---- fp32 rows -> [col block][token half][64][32] (128-byte rows, the
+        // 16-byte chunk f of row t at f ^ (t & 7)) over Q and K -> TMA stores
+        tc_fence_after();
+        const int th = r >> 6, rr = r & 63;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int cb = 2 * ch + j;
+            float v[32];
+            tmem_ld_32x32b_x32(D0 + lf + 32 * cb, v);
+            tmem_ld_wait();
+            uint8_t* rowp = sm + PL::kQ + (cb * 2 + th) * 8192 + rr * 128;
+#pragma unroll
+            for (int f = 0; f < 8; ++f)
+                *reinterpret_cast<float4*>(rowp + ((f ^ (rr & 7)) << 4)) =
+                    make_float4(v[4 * f], v[4 * f + 1], v[4 * f + 2], v[4 * f + 3]);
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+    }
+    ok = ok && !bar_or(1, kPairThreads, false);
+    if (ok && tid == 0) {
+        for (int cb = 0; cb < 4; ++cb)
+            for (int th = 0; th < 2; ++th)
+                if (t0 + 64 * th < T)
+                    tma_store_4d(&tm_acc_sw, sm + PL::kQ + (cb * 2 + th) * 8192, 32 * cb, h, t0 + 64 * th, b);
+        bulk_commit();
+    }
+    if (tid == 0) {   // every copy and MMA of this CTA completes before TMEM is freed and the CTA exits
+        bulk_wait_all();
         for (int i = 0; i < armed; ++i) {
+            const int slot = i == 0 ? PB_IN : i == 1 ? PB_QK : i == 2 ? PB_V : i;
             const uint64_t t1 = globaltimer_ns();
-            while (!mbar_try_wait_sleep(&bars[i], 0, kSuspendNs))
+            while (!mbar_try_wait_sleep(&bars[slot], 0, kSuspendNs))
                 if (globaltimer_ns() - t1 > kTimeoutNs) break;
         }
     }
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // One CTA per task: (level, head, group of whole blocks), the longest levels
@@ -2591,8 +2771,9 @@ __global__ void __launch_bounds__(256) ll_finish_kernel(const float* __restrict_
     }
 }
 
-// the fp32 accumulator [B, T, H, 128] as 4-D (128, H, T, B); box 32 x 1 x 64 x 1
-bool make_acc_map(CUtensorMap* map, const float* base, int B, int T, int H) {
+// the fp32 accumulator [B, T, H, 128] as 4-D (128, H, T, B); box 32 x 1 x 64 x 1,
+// shared-memory rows plain or 128-byte swizzled
+bool make_acc_map(CUtensorMap* map, const float* base, int B, int T, int H, bool swizzle = false) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[4] = {128, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
@@ -2600,8 +2781,8 @@ bool make_acc_map(CUtensorMap* map, const float* base, int B, int T, int H) {
     cuuint32_t box[4] = {32, 1, 64, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -2617,17 +2798,17 @@ cudaError_t launch_loglinear_fwd_tc(const void* q, const void* k, const void* v,
     auto* err = reinterpret_cast<DeviceErrorRecord*>(workspace);
     uint8_t* rec = reinterpret_cast<uint8_t*>(workspace) + kErrorRecordBytes;
     float* acc = reinterpret_cast<float*>(rec + chunk_fwd_tc_record_bytes(B, T, H, 128));
-    CUtensorMap mq, mk, mv, macc;
+    CUtensorMap mq, mk, mv, macc, macc_sw;
     if (!make_map(&mq, q, B, T, H, 128) || !make_map(&mk, k, B, T, H, 128) || !make_map(&mv, v, B, T, H, 128) ||
-        !make_acc_map(&macc, acc, B, T, H))
+        !make_acc_map(&macc, acc, B, T, H) || !make_acc_map(&macc_sw, acc, B, T, H, true))
         return cudaErrorInvalidValue;
     static PerDevice attrs;
     const cudaError_t attr_err = attrs.run([&](int, int&) {
         cudaError_t r = cudaFuncSetAttribute(chunk_prep_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)PrepLayout<128>::kSmemBytes);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(ll_inchunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)InLayout::kSmemBytes);
+            r = cudaFuncSetAttribute(ll_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)PairLayout::kSmemBytes);
         if (r == cudaSuccess)
             r = cudaFuncSetAttribute(ll_level_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)StateLayout::kSmemBytes);
@@ -2646,17 +2827,17 @@ cudaError_t launch_loglinear_fwd_tc(const void* q, const void* k, const void* v,
         chunk_prep_kernel<128><<<grid, kPrepThreads, PrepLayout<128>::kSmemBytes, stream>>>(mk, pp);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    ll_inchunk_kernel<<<dim3(nchunks, nheads), kInThreads, InLayout::kSmemBytes, stream>>>(
-        mq, mk, mv, rec, lam, L, acc, T, H, nchunks, err);
+    ll_pair_kernel<<<dim3((nchunks + 1) / 2, nheads), kPairThreads, PairLayout::kSmemBytes, stream>>>(
+        mq, mk, mv, macc_sw, rec, lam, L, T, H, nchunks, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // levels above the chunk: 7 .. top; a pair of tokens below T is at most
+    // levels above the chunk pair: 8 .. top; a pair of tokens below T is at most
     // at level ceil(log2 T), so higher entries of lambda are never read
     int top = 0;
     while (top < 31 && (1 << top) < T) ++top;
     const int lvl_hi = L < top + 1 ? L : top + 1;
     constexpr int kGroupMin = 16;
     int64_t ntasks = 0;
-    for (int lvl = lvl_hi - 1; lvl >= 7; --lvl) {
+    for (int lvl = lvl_hi - 1; lvl >= 8; --lvl) {
         const int64_t bc = int64_t(1) << (lvl - 6), tc = bc > kGroupMin ? bc : kGroupMin;
         ntasks += (nchunks + tc - 1) / tc * nheads;
     }
@@ -2665,7 +2846,7 @@ cudaError_t launch_loglinear_fwd_tc(const void* q, const void* k, const void* v,
         CarryParams base{nullptr, rec, nullptr, nullptr, err, T, H, 128, nchunks, 1, nchunks, 0, nchunks, 0,
                          0, 0, L, lam};
         ll_level_kernel<<<(unsigned)ntasks, kStateThreads, StateLayout::kSmemBytes, stream>>>(mq, mk, mv, macc, base, nheads,
-                                                                                    7, lvl_hi, kGroupMin);
+                                                                                    8, lvl_hi, kGroupMin);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     const size_t n4 = (size_t)B * T * H * 128 / 4;

@@ -133,9 +133,9 @@ cudaError_t launch_loglinear_fwd(const void* q, const void* k, const void* v, co
                                  float* scratch, cudaStream_t stream);
 
 // The same rule on the tensor cores for bf16 I/O with d_k = d_v = 128
-// (kla_chunk_tc.cu): the ordinary prep's chunk records, a per-chunk kernel
-// for the levels inside a chunk, one ordinary carry pass per level above the
-// chunk (outputs added into an fp32 accumulator), and a final conversion.
+// (kla_chunk_tc.cu): the ordinary prep's chunk records, a kernel for levels
+// 0..7 over aligned pairs of chunks, one ordinary carry pass per level above
+// the pair (outputs added into an fp32 accumulator), and a final conversion.
 // The workspace holds the error record, the chunk records and the
 // accumulator.
 size_t loglinear_tc_workspace_bytes(int B, int T, int H);
