@@ -2641,7 +2641,8 @@ ll_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (ok) {
         // ---- X = R o Lam over P (R, its last reader, is complete).  For s < r
         // the level is 1 + floor(log2(r ^ s)): over a chunk of 8 columns away
-        // from the row's own it is 4 + floor(log2((r >> 3) ^ c)), one value
+        // from the row's own it is 4 + floor(log2((r >> 3) ^ c)), one value;
+        // on the row's own chunk it depends on (r ^ s) & 7 alone
         tc_fence_after();
         uint8_t* Xt = sm + PL::kQ + ch * 16384;
         const int s_base = 64 * ch;
@@ -2653,6 +2654,12 @@ ll_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             float lr[8];
 #pragma unroll
             for (int l = 0; l < 8; ++l) lr[l] = lamv[l * 128 + r];
+            float dm[8];   // the row's own chunk: column i, zero above the diagonal
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int d = (r & 7) ^ i;
+                dm[i] = i > (r & 7) ? 0.f : d == 0 ? lr[0] : d == 1 ? lr[1] : d < 4 ? lr[2] : lr[3];
+            }
             float v[64];
             tmem_ld_32x32b_x32(D0 + lf + s_base, *reinterpret_cast<float(*)[32]>(v));
             tmem_ld_32x32b_x32(D0 + lf + s_base + 32, *reinterpret_cast<float(*)[32]>(v + 32));
@@ -2661,14 +2668,12 @@ ll_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int c8 = 0; c8 < 8; ++c8) {
                 const int s0 = s_base + 8 * c8;
                 const int hb = (r >> 3) ^ (s0 >> 3);               // 0 on the row's own chunk
-                const int lo = hb ? 31 - __clz(hb) : 0;            // 0..3
-                const float lam_far = lo == 0 ? lr[4] : lo == 1 ? lr[5] : lo == 2 ? lr[6] : lr[7];
-                pair_chunk(Xt, r, c8, s0, [&](int i) {
-                    const int d = r ^ (s0 + i);                    // < 8 on the row's own chunk
-                    const float lam_rs = hb ? lam_far
-                                            : (d == 0 ? lr[0] : d == 1 ? lr[1] : d < 4 ? lr[2] : lr[3]);
-                    return v[8 * c8 + i] * lam_rs;
-                });
+                const int lo = 31 - __clz(hb | 1);                 // floor(log2 hb), 0..3
+                const float far = s0 > r ? 0.f : lo == 0 ? lr[4] : lo == 1 ? lr[5] : lo == 2 ? lr[6] : lr[7];
+                float v8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v8[i] = v[8 * c8 + i] * (hb ? far : dm[i]);
+                ST_CHUNK(Xt, r, c8, v8, 0);
             }
         }
         tc_fence_before();
@@ -2715,7 +2720,7 @@ ll_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         bulk_commit();
     }
     if (tid == 0) {   // every copy and MMA of this CTA completes before TMEM is freed and the CTA exits
-        bulk_wait_all();
+        bulk_wait_read_le0();   // the stores have read shared memory (their writes complete with the grid)
         for (int i = 0; i < armed; ++i) {
             const int slot = i == 0 ? PB_IN : i == 1 ? PB_QK : i == 2 ? PB_V : i;
             const uint64_t t1 = globaltimer_ns();
