@@ -105,10 +105,11 @@ def load_peaks():
 # so writes still in L2 when a launch ends are not counted.  Refresh these
 # whenever the kernels change.
 TRAFFIC_BYTES = {
-    "train_prefill_bf16_B8H8T4096d128": 451.0e6,
+    "train_prefill_bf16_B8H8T4096d128": 453.5e6,
     "gdn_train_prefill_bf16_B8H8T4096d128_unitkeys": 452.5e6,
     "long_prefill_bf16_B1H16T131072d128": 6223.7e6,
     "decode_bf16_B64H16d128_x1024": 71.7e6,
+    "loglinear_train_prefill_bf16_B8H8T4096d128": 2573.0e6,
 }
 
 
@@ -119,11 +120,13 @@ def roofline(work, seconds, peaks, traffic=None):
         ach = work["bytes"] / seconds / 1e9
         return dict(bound="hbm", achieved=round(ach, 1), peak=peaks["hbm"], unit="GB/s",
                     frac=round(ach / peaks["hbm"], 4), traffic=traffic,
-                    peak_source=peaks["source"], roofline_us=round(t_mem * 1e6, 2))
+                    peak_source=peaks["source"], peak_kind="burst copy bandwidth",
+                    roofline_us=round(t_mem * 1e6, 2))
     ach = work["flops"] / seconds / 1e12
     return dict(bound="tensor", achieved=round(ach, 2), peak=peaks["bf16"], unit="TFLOP/s",
                 frac=round(ach / peaks["bf16"], 4), traffic=traffic,
-                peak_source=peaks["source"], roofline_us=round(t_flop * 1e6, 2))
+                peak_source=peaks["source"], peak_kind="burst bf16 GEMM",
+                roofline_us=round(t_flop * 1e6, 2))
 
 
 # ------------------------------------------------------------------- clocks
@@ -300,8 +303,7 @@ def bench_prefill(case, K, W, flush, peaks, stream, e2e=True, direct=False):
                tflops=work["flops"] / (mean_ms * 1e-3) / 1e12,
                gbps=work["bytes"] / (mean_ms * 1e-3) / 1e9,
                roofline=dict(roofline(work, mean_ms * 1e-3, peaks, TRAFFIC_BYTES.get(case.name)),
-                             scope="one kla_chunk_fwd call: all its launches (one fused prep-and-carry grid, or the prep, carry and combine kernels)",
-                             peak_kind="burst copy bandwidth"), work=work,
+                             scope="one kla_chunk_fwd call: all its launches (one fused prep-and-carry grid, or the prep, carry and combine kernels)"), work=work,
                launches=K * prefill_launches(kla, case), min_ms=min(ms),
                segments=kla.kla_chunk_fwd_auto_segments(B, T, H, dk, dv, case.chunk))
 
@@ -410,8 +412,7 @@ def bench_backward(case, K, W, flush, peaks, stream):
     mean_ms = slowest_s * 1e3
     res = dict(ms_per_step=mean_ms, tokens_per_s=work["tokens"] / (mean_ms * 1e-3),
                roofline=dict(roofline(work, mean_ms * 1e-3, peaks, TRAFFIC_BYTES.get("bwd_" + case.name)),
-                             scope="one kla_chunk_bwd call: its three launches (prep, the two carries in one grid, gradients)",
-                             peak_kind="burst copy bandwidth"),
+                             scope="one kla_chunk_bwd call: its three launches (prep, the two carries in one grid, gradients)"),
                launches=3 * K, min_ms=min(ms), workspace_bytes=ws.numel())
     del inp, do, dhT, ws, gq, gk, gv, gg, ge, gh0
     return res
@@ -460,8 +461,7 @@ def bench_deltakata(case, p, K, W, flush, peaks, stream):
     mean_ms = slowest_s * 1e3
     res = dict(ms_per_step=mean_ms, tokens_per_s=work["tokens"] / (mean_ms * 1e-3),
                roofline=dict(roofline(work, mean_ms * 1e-3, peaks, TRAFFIC_BYTES.get("deltakata_" + case.name)),
-                             scope="two kla_psd_features calls and one kla_chunk_fwd call",
-                             peak_kind="burst copy bandwidth"),
+                             scope="two kla_psd_features calls and one kla_chunk_fwd call"),
                launches=K * (2 + prefill_launches(kla, case)))
     del inp, q, k, fq, fk, o, hT, ws
     return res
@@ -505,8 +505,7 @@ def bench_loglinear(case, K, W, flush, peaks, stream):
     res = dict(ms_per_step=mean_ms, tokens_per_s=work["tokens"] / (mean_ms * 1e-3), levels=L,
                roofline=dict(roofline(work, mean_ms * 1e-3, peaks, TRAFFIC_BYTES.get("loglinear_" + case.name)),
                              scope="one kla_loglinear_fwd call: its four launches (chunk records, in-chunk levels, "
-                                   "one carry pass per level above the chunk, bf16 conversion)",
-                             peak_kind="burst copy bandwidth"),
+                                   "one carry pass per level above the chunk, bf16 conversion)"),
                launches=4 * K, min_ms=min(ms))
     del inp, lam, o, ws
     return res
@@ -558,8 +557,7 @@ def bench_loglinear_decode(case, steps, peaks, stream):
     work = dict(bytes=total, flops=0)
     res = dict(us_per_step=sec / steps * 1e6, tokens_per_s=B * steps / sec, levels=L,
                roofline=dict(roofline(work, sec, peaks),
-                             scope=f"{steps} kla_loglinear_decode_step calls from token 0, averaged",
-                             peak_kind="burst copy bandwidth"),
+                             scope=f"{steps} kla_loglinear_decode_step calls from token 0, averaged"),
                launches=steps)
     del q, k, v, g, eta, lam, states, o
     return res
@@ -588,8 +586,7 @@ def bench_decode(case, K_loops, W_loops, peaks, stream, n_states=4, e2e=True):
     res = dict(ms_per_call=per_call_s * 1e3, tokens_per_s=work["tokens"] / per_call_s,
                gbps=work["bytes"] / per_call_s / 1e9,
                roofline=dict(roofline(work, per_call_s, peaks, TRAFFIC_BYTES.get(case.name)),
-                             scope="one kla_decode_step call (decode_tma_kernel)",
-                             peak_kind="burst copy bandwidth"),
+                             scope="one kla_decode_step call (decode_tma_kernel)"),
                work=work, launches=K_loops * steps * LAUNCHES_PER_DECODE, calls_per_loop=steps,
                states_rotated=n_states)
 
