@@ -554,9 +554,9 @@ def bench_loglinear_decode(case, steps, peaks, stream):
     torch.cuda.synchronize()
     barrier()
     sec = e0.elapsed_time(e1) * 1e-3
-    work = dict(bytes=total, flops=0)
+    work = dict(bytes=total / steps, flops=0)    # per call, averaged over the calls
     res = dict(us_per_step=sec / steps * 1e6, tokens_per_s=B * steps / sec, levels=L,
-               roofline=dict(roofline(work, sec, peaks),
+               roofline=dict(roofline(work, sec / steps, peaks),
                              scope=f"{steps} kla_loglinear_decode_step calls from token 0, averaged"),
                launches=steps)
     del q, k, v, g, eta, lam, states, o

@@ -422,6 +422,17 @@ __global__ void __launch_bounds__(256) ll_decode_kernel(const TIO* __restrict__ 
     const int bh = blockIdx.y, col0 = blockIdx.x * 16;
     const int tid = threadIdx.x, col = tid & 15, rg = tid >> 4;
     const int rows = DK / 16, r0 = rg * rows;
+    const size_t SS = (size_t)DK * DV;
+    float* st = states + (size_t)bh * L * SS;
+    // this thread's column of the level-0 state, requested first (for t > 0)
+    float xn[8];
+    auto fetch = [&](int l) {
+        const float* S = st + (size_t)l * SS;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < rows) xn[i] = S[(size_t)(r0 + i) * DV + col0 + col];
+    };
+    if (t > 0) fetch(0);
     for (int i = tid; i < DK; i += blockDim.x) {
         sk[i] = ldf<TIO>(k + (size_t)bh * DK + i);
         sq[i] = ldf<TIO>(q + (size_t)bh * DK + i);
@@ -444,8 +455,6 @@ __global__ void __launch_bounds__(256) ll_decode_kernel(const TIO* __restrict__ 
     }
     __syncthreads();
     const float a = __expf(g[bh]), beta = sscal[0], qk = sscal[1];
-    const size_t SS = (size_t)DK * DV;
-    float* st = states + (size_t)bh * L * SS;
     // column reduction over the 16 row groups
     auto colsum = [&](float x) {
         sred[rg][col] = x;
@@ -463,19 +472,23 @@ __global__ void __launch_bounds__(256) ll_decode_kernel(const TIO* __restrict__ 
     const int b = t > 0 ? __ffs(t) - 1 : -1;
     if (t > 0) {
         const int prev = t - 1;
-        for (int l = 0; l < L; ++l) {
-            const bool present = l == 0 || ((prev >> (l - 1)) & 1);
-            if (!present) continue;
+        // the present levels: 0 and 1 + each set bit of t - 1; each level's
+        // column is requested while the previous level is reduced
+        auto next_present = [&](int l) {
+            for (++l; l < L; ++l)
+                if ((prev >> (l - 1)) & 1) return l;
+            return L;
+        };
+        for (int l = 0; l < L; l = next_present(l)) {
             float* S = st + (size_t)l * SS;
             float x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = xn[i];
+            if (next_present(l) < L) fetch(next_present(l));
             float dot = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if (i < rows) {
-                    x[i] = S[(size_t)(r0 + i) * DV + col0 + col];
-                    dot += sk[r0 + i] * x[i];
-                }
-            }
+            for (int i = 0; i < 8; ++i)
+                if (i < rows) dot += sk[r0 + i] * x[i];
             const float kx = colsum(dot);
             float y = 0.f;
 #pragma unroll
