@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(256) ll_decode_kernel(const TIO* __restrict__ 
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                     if (i < rows) S[(size_t)(r0 + i) * DV + col0 + col] = x[i];
-                out += slam[l] * colsum(y);
+                out += slam[l] * y;   // column-summed once, after the last level
             } else if (l > 0) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(256) ll_decode_kernel(const TIO* __restrict__ 
                 y += sq[r0 + i] * merged[i];
             }
         }
-        out += slam[b + 1] * colsum(y);
+        out = colsum(out + slam[b + 1] * y);   // sum_l lambda_l (S^(l)^T q), over the row groups
     }
     // the new write: level 0 = beta k v^T; its readout is beta (q . k) v
     const float vc = ldf<TIO>(v + (size_t)bh * DV + col0 + col);
