@@ -40,6 +40,7 @@ EXPORTED_SYMBOLS = (
     "kla_chunk_fwd_scan",
     "kla_chunk_fwd_auto_segments",
     "kla_chunk_fwd_noalloc",
+    "kla_chunk_fwd_noalloc_check",
     "kla_chunk_fwd_ex",
     "kla_decode_step",
     "kla_decode_step_ex",
@@ -98,6 +99,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kla_chunk_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp,
                                               i, i, i, i, i, i, i, vp]
         lib.kla_chunk_fwd_noalloc.restype = i
+        lib.kla_chunk_fwd_noalloc_check.argtypes = [vp]
+        lib.kla_chunk_fwd_noalloc_check.restype = i
         lib.kla_decode_step.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp]
         lib.kla_decode_step.restype = i
         lib.kla_chunk_fwd_ex.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp,
@@ -362,6 +365,12 @@ def kla_chunk_fwd_noalloc(q, k, v, g, eta, eps, h0, o, hT, chunk=64, stream=None
         raise KlaError(rc, "kla_chunk_fwd_noalloc")
 
 
+def kla_chunk_fwd_noalloc_check(stream=None) -> int:
+    """Synchronise and read the device error record of the last
+    kla_chunk_fwd_noalloc call on the current device (status code)."""
+    return int(load_library().kla_chunk_fwd_noalloc_check(_stream(stream)))
+
+
 def kla_decode_step(q, k, v, g, eta, eps, S, o, stream=None, beta=KLA_BETA_KACZMARZ,
                     status=None) -> None:
     """Enqueue one decode step (see include/kla.h); S [B,H,dk,dv] is updated in place.
@@ -547,7 +556,8 @@ def decode_step(q, k, v, g, eta, S, eps=1e-6, stream=None, beta=KLA_BETA_KACZMAR
 
 
 __all__ = [
-    "kla_chunk_fwd_workspace_bytes", "kla_chunk_fwd", "kla_chunk_fwd_noalloc", "kla_decode_step",
+    "kla_chunk_fwd_workspace_bytes", "kla_chunk_fwd", "kla_chunk_fwd_noalloc",
+    "kla_chunk_fwd_noalloc_check", "kla_decode_step",
     "kla_chunk_fwd_scan", "kla_chunk_fwd_scan_workspace_bytes", "kla_chunk_fwd_auto_segments",
     "kla_chunk_fwd_ex", "kla_decode_step_ex", "KLA_BETA_KACZMARZ", "KLA_BETA_DIRECT",
     "kla_chunk_bwd", "kla_chunk_bwd_workspace_bytes", "chunk_bwd", "kla_chunk", "KLAChunk",

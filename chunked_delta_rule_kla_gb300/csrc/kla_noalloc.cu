@@ -75,3 +75,12 @@ extern "C" kla_status kla_chunk_fwd_noalloc(const void* q, const void* k, const 
     return kla_chunk_fwd(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dk, dv, chunk, io, scratch,
                          kNoAllocScratchBytes, stream);
 }
+
+// The device error record of the last kla_chunk_fwd_noalloc call on the
+// current device: the same read as kla_workspace_check, on the built-in array.
+extern "C" kla_status kla_chunk_fwd_noalloc_check(void* stream) {
+    kla_status st = KLA_OK;
+    void* scratch = scratch_address(&st);
+    if (st != KLA_OK) return st;
+    return kla_workspace_check(scratch, kNoAllocScratchBytes, stream);
+}

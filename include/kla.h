@@ -357,13 +357,24 @@ KLA_API kla_status kla_decode_step_checked(const void* q, const void* k, const v
  *  - Every call shares the array and it keeps the last call's contents; the
  *    call clears what must start at zero.  Calls that overlap on the GPU
  *    (other streams or host threads) race on it.
- *  - A device-side wait timeout recorded in the array is not reported back.
+ *  - A device-side wait timeout is recorded in the array; read it back with
+ *    kla_chunk_fwd_noalloc_check before the next call.
  */
 KLA_API kla_status kla_chunk_fwd_noalloc(const void* q, const void* k, const void* v,
                                          const float* g, const float* eta, float eps,
                                          const float* h0, void* o, float* hT,
                                          int B, int T, int H, int dk, int dv, int chunk,
                                          kla_io_dtype io, void* stream);
+
+/*
+ * Synchronises `stream` and reads the device error record that the last
+ * kla_chunk_fwd_noalloc call on the current device left in the built-in
+ * array (the read kla_workspace_check makes on a workspace).  Returns
+ * KLA_ERR_DEVICE_TIMEOUT if a bounded device wait of that call gave up,
+ * KLA_OK otherwise, KLA_ERR_CUDA if the synchronisation or the read fails.
+ * Call it before the next kla_chunk_fwd_noalloc, which clears the record.
+ */
+KLA_API kla_status kla_chunk_fwd_noalloc_check(void* stream);
 
 /*
  * Synchronises `stream` and reads the device error record in `workspace`.

@@ -52,6 +52,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         torch.cuda.synchronize()
         assert rc == kla.KLA_OK, kla.kla_status_string(rc)
         assert torch.cuda.memory_allocated() == allocated
+        assert lib.kla_chunk_fwd_noalloc_check(None) == kla.KLA_OK   # no device wait ran out
         assert rel_err(o, o_ref.double().cpu().numpy()) <= TOL["bf16"]
         assert rel_err(hT, h_ref.double().cpu().numpy()) <= TOL["bf16"]
         assert rel_err(o, o_or) <= TOL["bf16"]
