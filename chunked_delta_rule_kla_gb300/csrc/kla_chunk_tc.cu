@@ -2732,8 +2732,12 @@ ll_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
-// One CTA per task: (level, head, group of whole blocks), the longest levels
-// first.  A task covers max(2^(l-6), group_min) chunks.
+// One CTA per task: (level, head, group of whole blocks).  A task covers
+// max(2^(l-6), group_min) chunks.  The levels with longer blocks come first,
+// the longest first; then the others, group_min chunks per task, side by side:
+// consecutive tasks share (group, head) and differ only in level, so they
+// start together and read the same chunks' q, k, v and records at about the
+// same time, which L2 then serves once.
 __global__ void __launch_bounds__(kStateThreads, 1)
 ll_level_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_acc,
@@ -2741,29 +2745,43 @@ ll_level_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     int i = blockIdx.x;
-    for (int lvl = lvl_hi - 1; lvl >= lvl_lo; --lvl) {
-        const int bc = 1 << (lvl - 6);
-        const int tc = bc > group_min ? bc : group_min;
-        const int nt = (base.nchunks + tc - 1) / tc;
-        if (i >= nt * nheads) {
+    int lvl = -1, hd = 0, t = 0, tc = group_min;
+    int short_hi = lvl_lo;   // levels [lvl_lo, short_hi) have blocks of at most group_min chunks
+    while (short_hi < lvl_hi && (1 << (short_hi - 6)) <= group_min) ++short_hi;
+    for (int l = lvl_hi - 1; l >= short_hi && lvl < 0; --l) {
+        const int bc = 1 << (l - 6);
+        const int nt = (base.nchunks + bc - 1) / bc;
+        if (i < nt * nheads) {
+            lvl = l;
+            tc = bc;
+            hd = i % nheads;
+            t = i / nheads;
+        } else {
             i -= nt * nheads;
-            continue;
         }
-        const int hd = i % nheads, t = i / nheads;
-        CarryParams cp = base;
-        cp.c_begin = t * tc;
-        cp.c_end = min(base.nchunks, cp.c_begin + tc);
-        cp.seg_chunks = tc;
-        cp.nseg = 1;
-        cp.lvl_bc = bc;
-        cp.lvl = lvl;
-        // a task that holds no second half of a block has nothing to read out
-        bool reads = false;
-        for (int cc = cp.c_begin; cc < cp.c_end && !reads; ++cc) reads = (cc % bc) >= (bc >> 1);
-        if (!reads) return;
-        state_cta<false, true>(tm_q, tm_k, tm_v, tm_acc, cp, sm, 0, hd % base.H, hd / base.H, nullptr);
-        return;
     }
+    if (lvl < 0) {
+        const int nshort = short_hi - lvl_lo;
+        if (nshort <= 0) return;
+        const int rest = i / nshort;
+        lvl = short_hi - 1 - i % nshort;
+        hd = rest % nheads;
+        t = rest / nheads;
+        if (t * group_min >= base.nchunks) return;
+    }
+    const int bc = 1 << (lvl - 6);
+    CarryParams cp = base;
+    cp.c_begin = t * tc;
+    cp.c_end = min(base.nchunks, cp.c_begin + tc);
+    cp.seg_chunks = tc;
+    cp.nseg = 1;
+    cp.lvl_bc = bc;
+    cp.lvl = lvl;
+    // a task that holds no second half of a block has nothing to read out
+    bool reads = false;
+    for (int cc = cp.c_begin; cc < cp.c_end && !reads; ++cc) reads = (cc % bc) >= (bc >> 1);
+    if (!reads) return;
+    state_cta<false, true>(tm_q, tm_k, tm_v, tm_acc, cp, sm, 0, hd % base.H, hd / base.H, nullptr);
 }
 
 __global__ void __launch_bounds__(256) ll_finish_kernel(const float* __restrict__ acc,
