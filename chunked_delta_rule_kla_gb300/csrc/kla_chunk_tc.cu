@@ -1832,9 +1832,14 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                     for (int i = 0; i < 32; ++i) { kq[i] = lo[i]; kq[32 + i] = hi[i]; }
                 }
                 const bool fact = span_ok(gam);
+                float* lamv = reinterpret_cast<float*>(sm + L::kLam);
                 if (at < C) {
-                    Gp[at] = __expf(gam[at]);
-                    Fr[at] = __expf(gam[at] - gam[C - 1]);
+                    // a level pass scales row r of the output, so both of its
+                    // terms, by lambda_r^(lvl): folded into Gam_r and into P's row
+                    const float lr = LEVEL ? lam_at : 1.f;
+                    Gp[at] = lr * __expf(gam[at]);
+                    Fr[at] = lr * __expf(gam[at] - gam[C - 1]);
+                    if (LEVEL) lamv[at] = lr;
                 }
                 bar_sync(2, 128);
                 uint8_t* Pt = sm + (c % kStages) * L::kStageBytes + L::kPT;
@@ -1855,7 +1860,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                         const float gs = gam[sr];
 #pragma unroll
                         for (int rr = 0; rr < C; ++rr) {
-                            const float pv = (sr <= rr) ? __expf(gam[rr] - gs) * kq[rr] : 0.f;
+                            const float pv = (sr <= rr) ? (LEVEL ? lamv[rr] : 1.f) * __expf(gam[rr] - gs) * kq[rr] : 0.f;
                             *reinterpret_cast<__nv_bfloat16*>(Pt + sw128_offset(rr, sr)) = __float2bfloat16_rn(pv);
                         }
                     }
@@ -1885,14 +1890,12 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
             tc_fence_after();
             if constexpr (LEVEL) {
                 // level pass: only the second half of a block reads out; its
-                // rows, scaled by lambda_t^(lvl), are added into the fp32
-                // accumulator by a TMA reduction from a [64][32]-float box
+                // rows (lambda_t^(lvl) already in Gam_r and P) are added into the
+                // fp32 accumulator by a TMA reduction from a [64][32]-float box
                 // per 32 columns (one 32 KB tile, reused once the previous
                 // reduction has read it)
                 if (writes(c)) continue;
-                float* lamv = reinterpret_cast<float*>(sm + L::kLam);
                 if (at == 0) bulk_wait_read_le0();
-                if (at < C) lamv[at] = lam_at;
                 bar_sync(2, 128);
                 float* ot = reinterpret_cast<float*>(sm + L::kO) + (j >> 5) * (C * 32) + (j & 31);
 #pragma unroll
@@ -1901,10 +1904,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
                     tmem_ld_32x32b_x32(tmem + lf + TS_PW + 32 * hq, b32);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int r = 32 * hq + i;
-                        ot[r * 32] = lamv[r] * (qs[r] + b32[i]);
-                    }
+                    for (int i = 0; i < 32; ++i) ot[(32 * hq + i) * 32] = qs[32 * hq + i] + b32[i];
                 }
                 tc_fence_before();
                 fence_proxy_async_smem();
