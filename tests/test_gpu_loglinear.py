@@ -89,6 +89,12 @@ def test_loglinear_batches_and_task_groups():
     _check("bf16", 2, 1300, 3, 128, 128, 760)
 
 
+def test_loglinear_more_level_tasks_than_sms():
+    # B4 H8 T2048: 224 level-pass tasks, more than one per SM, so tasks of all
+    # four levels queue behind one another; two heads checked
+    _check("bf16", 4, 2048, 8, 128, 128, 780, heads=[0, 5])
+
+
 def test_loglinear_strong_decay_chunk():
     # chunk 2 decays by about 2 per token (a span far above 80): the level
     # passes take the direct P W branch there and the factorised one elsewhere
