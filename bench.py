@@ -109,7 +109,7 @@ TRAFFIC_BYTES = {
     "gdn_train_prefill_bf16_B8H8T4096d128_unitkeys": 452.5e6,
     "long_prefill_bf16_B1H16T131072d128": 6223.7e6,
     "decode_bf16_B64H16d128_x1024": 71.7e6,
-    "loglinear_train_prefill_bf16_B8H8T4096d128": 2573.0e6,
+    "loglinear_train_prefill_bf16_B8H8T4096d128": 1760.5e6,
 }
 
 
