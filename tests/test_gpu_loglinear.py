@@ -130,3 +130,50 @@ def test_loglinear_decode_steps_match_oracle(io, dk, dv):
     ref = oracle.kla_oracle_loglinear_forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["eta"], lam,
                                               inp["eps"])
     assert rel_err(torch.stack(outs, 1), ref) <= TOL[io]
+
+
+def test_loglinear_bench_shape_sampled_sequences():
+    # B8 H8 T4096, the shape and launch configuration the bench times (960
+    # level-pass tasks, 2,048 chunk pairs); two (batch, head) sequences checked
+    kla = _kla()
+    case = kla_inputs.TRAIN
+    inp = kla_inputs.make_prefill(case, device="cuda")
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(790)
+    L = oracle.loglinear_num_levels(case.T)
+    lam = torch.empty((case.B, case.T, case.H, L), device="cuda").uniform_(0.2, 1.5, generator=gen)
+    ws = torch.empty(kla.kla_loglinear_workspace_bytes(case.B, case.T, case.H, 128, 128, 64, kla.KLA_IO_BF16),
+                     dtype=torch.uint8, device="cuda")
+    o = kla.loglinear_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["eta"], lam, inp["eps"], workspace=ws)
+    assert kla.kla_workspace_check(ws) == kla.KLA_OK
+    for b, h in ((0, 0), (7, 5)):
+        sl = lambda x: x[b:b + 1, :, h:h + 1]  # noqa: E731
+        ref = oracle.kla_oracle_loglinear_forward(*(sl(inp[n]) for n in ("q", "k", "v", "g", "eta")), sl(lam),
+                                                  inp["eps"])
+        e = rel_err(sl(o), ref)
+        assert e <= TOL["bf16"], f"(b={b}, h={h}) rel err {e:.3e}"
+
+
+def test_loglinear_decode_bench_shape_sampled_heads():
+    # B64 H16 d128, tokens 0..1023 from zero states (the bench's decode run);
+    # two heads checked against the oracle over the whole sequence
+    kla = _kla()
+    case = kla_inputs.DECODE
+    steps = 1024
+    dec = kla_inputs.make_decode(case, device="cuda", steps=steps)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(791)
+    L = oracle.loglinear_num_levels(steps)
+    lam = torch.empty((steps, case.B, case.H, L), device="cuda").uniform_(0.2, 1.5, generator=gen)
+    states = torch.zeros((case.B, case.H, L, 128, 128), device="cuda")
+    o = torch.empty((steps, case.B, case.H, 128), dtype=torch.bfloat16, device="cuda")
+    for t in range(steps):
+        kla.kla_loglinear_decode_step(dec["q"][t], dec["k"][t], dec["v"][t], dec["g"][t], dec["eta"][t], lam[t],
+                                      dec["eps"], states, t, o[t])
+    torch.cuda.synchronize()
+    for b, h in ((0, 0), (63, 15)):
+        seq = lambda x: x[:, b:b + 1, h:h + 1].transpose(0, 1).contiguous()  # noqa: E731  [1, T, 1, ...]
+        ref = oracle.kla_oracle_loglinear_forward(*(seq(dec[n]) for n in ("q", "k", "v", "g", "eta")), seq(lam),
+                                                  dec["eps"])
+        e = rel_err(seq(o), ref)
+        assert e <= TOL["bf16"], f"(b={b}, h={h}) rel err {e:.3e}"
