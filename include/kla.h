@@ -226,9 +226,13 @@ KLA_API kla_status kla_chunk_bwd(const void* q, const void* k, const void* v,
  *  o      : [B, T, H, dv] I/O dtype
  *  chunk = 64; dk, dv : 64 or 128; B*H <= 65535.
  *
- * Cost: O(T log T); the workspace (kla_loglinear_workspace_bytes) holds the
- * level states at every chunk start, ceil(log2(T / 64)) slots of dk x dv fp32
- * per (batch, head, chunk).  Errors as kla_chunk_fwd_ex.
+ * Cost: O(T log T).  The workspace (kla_loglinear_workspace_bytes, 256-byte
+ * aligned, caller owned) holds, with bf16 I/O and dk = dv = 128 (the
+ * tensor-core path), the per-chunk records of kla_chunk_fwd (25,344 bytes per
+ * batch, head and chunk) and an fp32 [B, T, H, dv] output accumulator; for
+ * the other shapes, the level states at every chunk start, ceil(log2(T / 64))
+ * slots of dk x dv fp32 per (batch, head, chunk).  B*T*H = 0 returns KLA_OK
+ * without reading any pointer.  Errors as kla_chunk_fwd_ex.
  */
 KLA_API int kla_loglinear_num_levels(int T);
 KLA_API size_t kla_loglinear_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk,

@@ -177,3 +177,63 @@ def test_decode_step_checked_rejects(lib):
     bad = list(args)
     bad[6] = None
     assert lib.kla_decode_step_checked(*bad, WS, None) == kla.KLA_ERR_INVALID_ARG
+
+
+# ---- kla_loglinear_fwd: sizes and argument checks (host side, no launch)
+
+def _ll(lib, **kw):
+    a = dict(q=P, k=P, v=P, g=P, eta=P, lam=P, L=None, eps=1e-6, o=P, B=1, T=300, H=2, dk=128, dv=128,
+             chunk=64, io=kla.KLA_IO_BF16, beta=kla.KLA_BETA_KACZMARZ, ws=WS, wsb=None, stream=None)
+    a.update(kw)
+    if a["L"] is None:
+        a["L"] = lib.kla_loglinear_num_levels(max(a["T"], 0))
+    if a["wsb"] is None:
+        a["wsb"] = lib.kla_loglinear_workspace_bytes(a["B"], a["T"], a["H"], 128, 128, 64, kla.KLA_IO_BF16)
+    return lib.kla_loglinear_fwd(a["q"], a["k"], a["v"], a["g"], a["eta"], a["lam"], a["L"],
+                                 ctypes.c_float(a["eps"]), a["o"], a["B"], a["T"], a["H"], a["dk"], a["dv"],
+                                 a["chunk"], a["io"], a["beta"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_loglinear_levels(lib):
+    # 1 + ceil(log2 T): a pair of tokens below T is at most at level ceil(log2 T)
+    for T, want in ((1, 1), (2, 2), (3, 3), (64, 7), (65, 8), (128, 8), (129, 9), (4096, 13)):
+        assert lib.kla_loglinear_num_levels(T) == want, T
+
+
+def test_loglinear_workspace_bytes(lib):
+    # bf16, d = 128 (the tensor-core path): the error record, one 25,344-byte
+    # chunk record per (b, h, chunk) and the fp32 accumulator [B, T, H, 128]
+    B, T, H = 2, 300, 3
+    n = lib.kla_loglinear_workspace_bytes(B, T, H, 128, 128, 64, kla.KLA_IO_BF16)
+    nch = (T + 63) // 64
+    want = 256 + B * H * nch * 25344 + 4 * B * T * H * 128
+    assert n == (want + 255) // 256 * 256
+    assert lib.kla_loglinear_workspace_bytes(B, T, H, 128, 128, 64, kla.KLA_IO_FP32) >= 256
+    assert lib.kla_loglinear_workspace_bytes(B, T, H, 64, 128, 64, kla.KLA_IO_BF16) >= 256
+    assert lib.kla_loglinear_workspace_bytes(B, T, H, 96, 128, 64, kla.KLA_IO_BF16) == 0
+    assert lib.kla_loglinear_workspace_bytes(B, T, H, 128, 128, 32, kla.KLA_IO_BF16) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), kla.KLA_ERR_INVALID_ARG),
+    (dict(lam=None), kla.KLA_ERR_INVALID_ARG),
+    (dict(o=None), kla.KLA_ERR_INVALID_ARG),
+    (dict(L=8), kla.KLA_ERR_INVALID_ARG),             # T = 300 needs 10 levels
+    (dict(eps=-1.0), kla.KLA_ERR_INVALID_ARG),
+    (dict(beta=7), kla.KLA_ERR_INVALID_ARG),
+    (dict(q=P + 8), kla.KLA_ERR_INVALID_ARG),          # not 16-byte aligned
+    (dict(lam=P + 2), kla.KLA_ERR_INVALID_ARG),        # not 4-byte aligned
+    (dict(dk=96), kla.KLA_ERR_UNSUPPORTED),
+    (dict(chunk=32), kla.KLA_ERR_UNSUPPORTED),
+    (dict(ws=None), kla.KLA_ERR_WORKSPACE),
+    (dict(ws=WS + 16), kla.KLA_ERR_WORKSPACE),         # not 256-byte aligned
+    (dict(wsb=256), kla.KLA_ERR_WORKSPACE),            # too small
+])
+def test_loglinear_fwd_rejects(lib, kw, code):
+    assert _ll(lib, **kw) == code
+
+
+def test_loglinear_fwd_empty_problem_is_a_no_op(lib):
+    # no tokens: nothing to compute, the pointers and the workspace are not read
+    assert _ll(lib, T=0, q=None, ws=None, wsb=0) == kla.KLA_OK
+    assert _ll(lib, B=0, q=None, ws=None, wsb=0) == kla.KLA_OK
