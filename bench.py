@@ -431,8 +431,10 @@ def deltakata_work(case, p):
 
 
 def bench_deltakata(case, p, K, W, flush, peaks, stream):
-    """Time DeltaKATA on ``case``: the PSD features of q and k (p values per
-    token-head, case.dk features) and kla_chunk_fwd on them."""
+    """Time DeltaKATA on ``case`` from q, k with p values per token-head:
+    kla_deltakata_fwd, which forms the case.dk PSD features inside the prefill
+    (or, for a shape it does not take, kla_psd_features of q and k and then
+    kla_chunk_fwd on them)."""
     import chunked_delta_rule_kla_gb300 as kla
     inp = kla_inputs.make_prefill(case, device="cuda")
     B, T, H, dk, dv = case.B, case.T, case.H, case.dk, case.dv
@@ -442,17 +444,28 @@ def bench_deltakata(case, p, K, W, flush, peaks, stream):
     q = torch.randn((B, T, H, p), generator=gen, device="cuda").mul(0.4).to(dt)
     u = torch.randn((B, T, H, p), generator=gen, device="cuda")
     k = (u / u.norm(dim=-1, keepdim=True)).to(dt)
-    fq = torch.empty((B, T, H, dk), dtype=dt, device="cuda")
-    fk = torch.empty_like(fq)
     o = torch.empty((B, T, H, dv), dtype=dt, device="cuda")
     hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
-    ws = kla.alloc_workspace(B, T, H, dk, dv, case.chunk, kla.KLA_IO_BF16 if case.io == "bf16" else kla.KLA_IO_FP32)
+    io = kla.KLA_IO_BF16 if case.io == "bf16" else kla.KLA_IO_FP32
+    n_fused = kla.kla_deltakata_fwd_workspace_bytes(B, T, H, p, dv, case.chunk, io) if dk == 128 else 0
+    if n_fused:
+        ws = torch.empty(n_fused, dtype=torch.uint8, device="cuda")
 
-    def step():
-        kla.kla_psd_features(q, fq, stream)
-        kla.kla_psd_features(k, fk, stream)
-        kla.kla_chunk_fwd(fq, fk, inp["v"], inp["g"], inp["eta"], inp["eps"], None, o, hT, ws,
-                          case.chunk, stream)
+        def step():
+            kla.kla_deltakata_fwd(q, k, inp["v"], inp["g"], inp["eta"], inp["eps"], None, o, hT, ws,
+                                  chunk=case.chunk, stream=stream)
+        scope, launches = "one kla_deltakata_fwd call (features formed in the prep lanes)", prefill_launches(kla, case)
+    else:
+        fq = torch.empty((B, T, H, dk), dtype=dt, device="cuda")
+        fk = torch.empty_like(fq)
+        ws = kla.alloc_workspace(B, T, H, dk, dv, case.chunk, io)
+
+        def step():
+            kla.kla_psd_features(q, fq, stream)
+            kla.kla_psd_features(k, fk, stream)
+            kla.kla_chunk_fwd(fq, fk, inp["v"], inp["g"], inp["eta"], inp["eps"], None, o, hT, ws,
+                              case.chunk, stream)
+        scope, launches = "two kla_psd_features calls and one kla_chunk_fwd call", 2 + prefill_launches(kla, case)
 
     barrier()
     ms = timed_steps(step, K, W, flush, stream)
@@ -462,9 +475,9 @@ def bench_deltakata(case, p, K, W, flush, peaks, stream):
     mean_ms = slowest_s * 1e3
     res = dict(ms_per_step=mean_ms, tokens_per_s=work["tokens"] / (mean_ms * 1e-3),
                roofline=dict(roofline(work, mean_ms * 1e-3, peaks, TRAFFIC_BYTES.get("deltakata_" + case.name)),
-                             scope="two kla_psd_features calls and one kla_chunk_fwd call"),
-               launches=K * (2 + prefill_launches(kla, case)))
-    del inp, q, k, fq, fk, o, hT, ws
+                             scope=scope),
+               launches=K * launches)
+    del inp, q, k, o, hT, ws
     return res
 
 

@@ -49,6 +49,8 @@ EXPORTED_SYMBOLS = (
     "kla_chunk_bwd",
     "kla_psd_features",
     "kla_psd_features_bwd",
+    "kla_deltakata_fwd_workspace_bytes",
+    "kla_deltakata_fwd",
     "kla_loglinear_num_levels",
     "kla_loglinear_workspace_bytes",
     "kla_loglinear_fwd",
@@ -121,6 +123,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kla_psd_features.restype = i
         lib.kla_psd_features_bwd.argtypes = [vp, vp, vp, i64, i, i, i, vp]
         lib.kla_psd_features_bwd.restype = i
+        lib.kla_deltakata_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+        lib.kla_deltakata_fwd_workspace_bytes.restype = sz
+        lib.kla_deltakata_fwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp,
+                                          i, i, i, i, i, i, i, i, vp, sz, vp]
+        lib.kla_deltakata_fwd.restype = i
         lib.kla_loglinear_num_levels.argtypes = [i]
         lib.kla_loglinear_num_levels.restype = i
         lib.kla_loglinear_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
@@ -308,6 +315,38 @@ def kla_psd_features_bwd(x, grad_y, grad_x, stream=None) -> None:
                                              _stream(stream))
     if rc != KLA_OK:
         raise KlaError(rc, "kla_psd_features_bwd")
+
+
+def kla_deltakata_fwd_workspace_bytes(B, T, H, p, dv, chunk=64, io=KLA_IO_BF16) -> int:
+    """Workspace of kla_deltakata_fwd; 0 where that shape is not supported."""
+    return int(load_library().kla_deltakata_fwd_workspace_bytes(B, T, H, p, dv, chunk, io))
+
+
+def kla_deltakata_fwd(xq, xk, v, g, eta, eps, h0, o, hT, workspace, beta=KLA_BETA_KACZMARZ,
+                      chunk=64, stream=None) -> None:
+    """Enqueue DeltaKATA's forward with the features formed inside (see
+    include/kla.h): xq, xk [B,T,H,p] bf16; v, o [B,T,H,128] bf16; g, eta
+    [B,T,H] fp32; h0, hT [B,H,128,128] fp32 or None."""
+    B, T, H, p = xk.shape
+    dv = v.shape[-1]
+    for name, t in (("xk", xk), ("v", v), ("o", o)):
+        if t.dtype != xq.dtype:
+            raise TypeError(f"{name} must have xq's dtype {xq.dtype}")
+    if xq.shape != xk.shape or v.shape[:3] != xk.shape[:3] or o.shape != v.shape:
+        raise ValueError("shape mismatch among xq, xk, v, o")
+    if g.shape != (B, T, H) or eta.shape != (B, T, H):
+        raise ValueError("g and eta must be [B,T,H]")
+    for name, t in (("h0", h0), ("hT", hT)):
+        if t is not None and tuple(t.shape) != (B, H, 128, dv):
+            raise ValueError(f"{name} must be [B,H,128,dv]")
+    rc = load_library().kla_deltakata_fwd(
+        _ptr(xq, "xq"), _ptr(xk, "xk"), _ptr(v, "v"), _ptr(g, "g", torch.float32),
+        _ptr(eta, "eta", torch.float32), float(eps), _ptr(h0, "h0", torch.float32),
+        _ptr(o, "o"), _ptr(hT, "hT", torch.float32), B, T, H, p, dv, int(chunk), _io_of(xq),
+        int(beta), _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    if rc != KLA_OK:
+        raise KlaError(rc, "kla_deltakata_fwd")
 
 
 def kla_loglinear_num_levels(T) -> int:
@@ -520,14 +559,57 @@ class PSDFeatures(torch.autograd.Function):
         return gx, None
 
 
+class DeltaKATAFused(torch.autograd.Function):
+    """DeltaKATA with 128 features through kla_deltakata_fwd: the forward forms
+    the features inside the prefill; the backward forms them again
+    (kla_psd_features), runs kla_chunk_bwd on them and maps the feature
+    gradients back with kla_psd_features_bwd."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, g, eta, h0, eps, beta):
+        B, T, H, p = k.shape
+        dv = v.shape[-1]
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+        hT = torch.empty((B, H, 128, dv), dtype=torch.float32, device=q.device)
+        n = kla_deltakata_fwd_workspace_bytes(B, T, H, p, dv, 64, _io_of(q))
+        if n == 0:
+            raise KlaError(KLA_ERR_UNSUPPORTED, "kla_deltakata_fwd_workspace_bytes")
+        ws = torch.empty(n, dtype=torch.uint8, device=q.device)
+        kla_deltakata_fwd(q, k, v, g, eta, eps, h0, o, hT, ws, beta=beta)
+        ctx.save_for_backward(q, k, v, g, eta, h0)
+        ctx.eps, ctx.beta = eps, beta
+        return o, hT
+
+    @staticmethod
+    def backward(ctx, do, dhT):
+        q, k, v, g, eta, h0 = ctx.saved_tensors
+        fq, fk = psd_features(q, 128), psd_features(k, 128)
+        do = torch.zeros_like(v) if do is None else do
+        grads = chunk_bwd(fq, fk, v, g, eta, do.contiguous(),
+                          None if dhT is None else dhT.contiguous(), ctx.eps, h0, ctx.beta)
+        gq, gk = torch.empty_like(q), torch.empty_like(k)
+        kla_psd_features_bwd(q, grads["dq"], gq)
+        kla_psd_features_bwd(k, grads["dk"], gk)
+        return (gq, gk, grads["dv"], grads["dg"], grads["deta"],
+                grads["dh0"] if h0 is not None else None, None, None)
+
+
 def deltakata(q, k, v, g, eta, eps=1e-6, h0=None, d_feat=None, beta=KLA_BETA_KACZMARZ):
     """DeltaKATA: the KLA recurrence on the rank-one PSD features of q and k.
 
     q, k [B,T,H,p] with p(p+1)/2 <= d_feat in {64, 128} (default: the smaller
-    that fits); v [B,T,H,dv].  Differentiable; returns (o, hT)."""
-    p = k.shape[-1]
+    that fits); v [B,T,H,dv].  Differentiable; returns (o, hT).  With 128
+    features, bf16 and a shape kla_deltakata_fwd supports, the features are
+    formed inside the prefill (DeltaKATAFused); otherwise kla_psd_features
+    writes them first."""
+    B, T, H, p = k.shape
     if d_feat is None:
         d_feat = 64 if p * (p + 1) // 2 <= 64 else 128
+    if (d_feat == 128 and q.dtype == torch.bfloat16 and
+            kla_deltakata_fwd_workspace_bytes(B, T, H, p, v.shape[-1], 64, KLA_IO_BF16) > 0):
+        return DeltaKATAFused.apply(q.contiguous(), k.contiguous(), v.contiguous(), g.contiguous(),
+                                    eta.contiguous(), None if h0 is None else h0.contiguous(),
+                                    float(eps), int(beta))
     return kla_chunk(PSDFeatures.apply(q, d_feat), PSDFeatures.apply(k, d_feat), v, g, eta, eps,
                      h0, beta)
 
@@ -562,6 +644,7 @@ __all__ = [
     "kla_chunk_fwd_ex", "kla_decode_step_ex", "KLA_BETA_KACZMARZ", "KLA_BETA_DIRECT",
     "kla_chunk_bwd", "kla_chunk_bwd_workspace_bytes", "chunk_bwd", "kla_chunk", "KLAChunk",
     "kla_psd_features", "kla_psd_features_bwd", "psd_features", "PSDFeatures", "deltakata",
+    "kla_deltakata_fwd_workspace_bytes", "kla_deltakata_fwd", "DeltaKATAFused",
     "kla_loglinear_num_levels", "kla_loglinear_workspace_bytes", "kla_loglinear_fwd", "loglinear_fwd",
     "kla_loglinear_decode_step",
     "kla_workspace_check",

@@ -323,6 +323,57 @@ kla_status kla_psd_features_bwd(const void* x, const void* grad_y, void* grad_x,
                                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t kla_deltakata_fwd_workspace_bytes(int B, int T, int H, int p, int dv, int chunk,
+                                         kla_io_dtype io) {
+    if (B < 0 || T < 0 || H < 0 || p < 1 || check_io(io) != KLA_OK) return 0;
+    if (io != KLA_IO_BF16 || dv != 128 || chunk != 64 || p * (p + 1) / 2 > 128) return 0;
+    if (!sizes_fit(B, T, H, 128, 128) || !kla::deltakata_fwd_tc_supported(B, T, H)) return 0;
+    return kla::kErrorRecordBytes + kla::deltakata_fwd_tc_workspace_bytes(B, T, H);
+}
+
+kla_status kla_deltakata_fwd(const void* xq, const void* xk, const void* v, const float* g,
+                             const float* eta, float eps, const float* h0, void* o, float* hT,
+                             int B, int T, int H, int p, int dv, int chunk, kla_io_dtype io,
+                             kla_beta_mode beta, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+    if (B < 0 || T < 0 || H < 0 || p < 1 || dv <= 0 || chunk <= 0) return KLA_ERR_INVALID_ARG;
+    if (check_io(io) != KLA_OK) return KLA_ERR_INVALID_ARG;
+    if (beta != KLA_BETA_KACZMARZ && beta != KLA_BETA_DIRECT) return KLA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f)) return KLA_ERR_INVALID_ARG;
+    if (io != KLA_IO_BF16 || dv != 128 || chunk != 64 || p * (p + 1) / 2 > 128) return KLA_ERR_UNSUPPORTED;
+    if (!sizes_fit(B, T, H, 128, 128) || !kla::deltakata_fwd_tc_supported(B, T, H))
+        return KLA_ERR_UNSUPPORTED;
+    const bool have_tokens = (int64_t)B * H * T > 0;
+    if (have_tokens && (!xq || !xk || !v || !g || !eta || !o)) return KLA_ERR_INVALID_ARG;
+    if ((xq && !aligned4(xq)) || (xk && !aligned4(xk))) return KLA_ERR_INVALID_ARG;
+    const void* ptrs[] = {v, h0, o, hT};
+    for (const void* ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return KLA_ERR_INVALID_ARG;
+    if ((g && !aligned4(g)) || (eta && !aligned4(eta))) return KLA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kla::kErrorRecordBytes) return KLA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KLA_ERR_WORKSPACE;
+    if ((int64_t)B * H == 0) return KLA_OK;
+    if (workspace_bytes < kla_deltakata_fwd_workspace_bytes(B, T, H, p, dv, chunk, io))
+        return KLA_ERR_WORKSPACE;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, kla::kErrorRecordBytes, st);
+    if (e != cudaSuccess) return KLA_ERR_CUDA;
+    if (T == 0) {
+        if (!hT) return KLA_OK;
+        const size_t bytes = sizeof(float) * (size_t)B * H * 128 * 128;
+        if (h0) {
+            if (h0 == hT) return KLA_OK;
+            return to_status(cudaMemcpyAsync(hT, h0, bytes, cudaMemcpyDeviceToDevice, st));
+        }
+        return to_status(cudaMemsetAsync(hT, 0, bytes, st));
+    }
+    auto* rec = reinterpret_cast<kla::DeviceErrorRecord*>(workspace);
+    uint8_t* records = reinterpret_cast<uint8_t*>(workspace) + kla::kErrorRecordBytes;
+    return to_status(kla::launch_deltakata_fwd_tc(xq, xk, p, v, g, eta, eps, h0, o, hT, B, T, H,
+                                                  beta == KLA_BETA_DIRECT, rec, records, st));
+}
+
 kla_status kla_workspace_check(const void* workspace, size_t workspace_bytes, void* stream) {
     if (!workspace || workspace_bytes < kla::kErrorRecordBytes) return KLA_ERR_WORKSPACE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -166,6 +166,10 @@ struct Waiter {
 constexpr int kPrepThreads = 128;
 constexpr int kPrepPerSm = 4;   // resident prep CTAs per SM (49 KB shared memory, 128 TMEM columns each)
 
+// row stride (words) of the staged DeltaKATA values: odd, so that the 16
+// tokens a warp reads at once fall in distinct banks
+constexpr int kXsLd = 17;
+
 template <int DK>
 struct PrepLayout {
     static constexpr int KB = DK / 64;
@@ -192,7 +196,11 @@ struct PrepLayout {
     static constexpr uint32_t kBet = kGam + 2 * kVecBytes;     // beta[64], betg[64]
     static constexpr uint32_t kMisc = kBet + 2 * 256;
     static constexpr uint32_t kBars = kMisc + 64;
-    static constexpr uint32_t kEnd = kBars + 6 * 8;
+    // DeltaKATA (DK = 128): the values of an item's keys and queries, one
+    // 32-bit word per (token, value): key bits low, query bits high
+    static constexpr uint32_t kXs = kBars + 6 * 8;
+    static constexpr uint32_t kXsBytes = DK == 128 ? C * kXsLd * 4 : 0;
+    static constexpr uint32_t kEnd = kXs + kXsBytes;
     static constexpr size_t kSmemBytes = kEnd + 1024;
     static_assert(Rec<DK>::kWk + 8192 <= C * LDF * 4, "Tb, Tg fit in A's space");
 };
@@ -207,7 +215,40 @@ struct PrepParams {
     int B, c_lo, c_hi;      // work items: chunks [c_lo, c_hi) of every (b, h), chunk-major
     int pdl_wait;           // launched as a programmatic dependent: wait for the primary at exit
     int beta_direct;        // beta_t = eta_t instead of eta_t / (||k_t||^2 + eps)
+    // DeltaKATA (DK = 128): keys and queries given as fp values per
+    // token-head [B][T][H][fp] bf16; the lane forms their rank-one PSD
+    // features itself (the K tile of its products) and stores both feature
+    // tiles in the record after its other parts (null: keys through tm_k)
+    const __nv_bfloat16* xq = nullptr;
+    const __nv_bfloat16* xk = nullptr;
+    int fp = 0;
+    uint32_t rec_bytes = 0;  // record stride (0: Rec<DK>::kBytes)
 };
+
+// DeltaKATA's feature map ("Kernelized Linear Attention: breaking the
+// capacity wall via symmetric cones", section 2.2: psi(u) = u u^T), as a
+// vector: feature n is s * u_i * u_j over the upper triangle (i <= j,
+// row-major), s = 1 on the diagonal and sqrt(2) off it, then zeros up to 128,
+// so that psi(q) . psi(k) = (q . k)^2.  Each product is (s * u_i) * u_j in
+// fp32, rounded to bf16 once: the same values kla_psd_features writes.
+constexpr float kPsdSqrt2 = 1.41421356237309515f;
+// The pairs of features 8 part .. 8 part + 7 (part = 0..15): feature n is
+// s_n * u_i * u_j; past the last feature s = 0 with i = j = 0, which gives
+// +0 for any u.
+__device__ __forceinline__ void psd_pairs(int fp, int part, int (&fi)[8], int (&fj)[8], float (&fs)[8]) {
+    const int nf = fp * (fp + 1) / 2, n0 = 8 * part;
+    int i = 0, m = n0;   // row i of the triangle, then the offset in it
+    while (i < fp && m >= fp - i) { m -= fp - i; ++i; }
+    int j = i + m;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const bool on = n0 + u < nf;
+        fi[u] = on ? i : 0;
+        fj[u] = on ? j : 0;
+        fs[u] = on ? (i == j ? 1.f : kPsdSqrt2) : 0.f;
+        if (on && ++j == fp) { ++i; j = i; }
+    }
+}
 
 // D = P Q for a 16 x 16 tile of D with K = 8 * KS: P (16 x K) and Q (K x 16)
 // row-major fp32 in shared memory with row stride LDF, rounded to tf32 for
@@ -285,7 +326,8 @@ __device__ __forceinline__ void prep_lane_init(uint8_t* sm) {
     fence_mbar_init();
 }
 
-template <int DK>
+// FEAT: DeltaKATA inputs (p.xk, p.xq), DK = 128
+template <int DK, bool FEAT = false>
 __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepParams& p, uint8_t* sm,
                                           const uint32_t tmem, const PrepLane& ln) {
     using L = PrepLayout<DK>;
@@ -315,6 +357,9 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
     const uint32_t lf = (uint32_t)(q * 32) << 16;
     uint8_t* Tbt = sm + L::kTb;
     uint8_t* Tgt = sm + L::kTg;
+    static_assert(!FEAT || DK == 128, "DeltaKATA features are 128 wide");
+    constexpr bool feat = FEAT;
+    const uint32_t rec_bytes = p.rec_bytes ? p.rec_bytes : Rec<DK>::kBytes;
     {
         // Thread 0 issues the K copies and the MMAs: the next item's K as
         // soon as this item's Wk product has read the tile, and the next
@@ -328,10 +373,13 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
                 tma_load_4d(sm + L::kK + kb * 8192, tm_kp, &bars[0], kb * 64, hd % H, c * C, hd / H);
             ++loads;
         };
-        // K K^T (M=64, N=64) of the item whose tile was requested last
+        // K K^T (M=64, N=64) of the item whose tile was requested last (or,
+        // with DeltaKATA inputs, formed last)
         auto issue_gram = [&](int c) -> bool {
-            if (!wt.poll(0, waited & 1, kWherePrepK, c)) return false;
-            ++waited;
+            if (!feat) {
+                if (!wt.poll(0, waited & 1, kWherePrepK, c)) return false;
+                ++waited;
+            }
             tc_fence_after();
             constexpr uint32_t id_g = idesc_bf16(64, 64, false, false);
             const uint32_t sK = smem_u32(sm + L::kK);
@@ -343,8 +391,83 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
             mma_commit(&bars[1]);
             return true;
         };
+        // DeltaKATA: an item's values, fetched an item ahead: thread pt holds
+        // value pt % 16 of tokens pt / 16 + 8 u (u = 0..7) of the keys (kraw)
+        // and the queries (qraw), as bf16 bits (zero past fp and past T).
+        // They are requested before the triangular inverse and first read
+        // when the features are formed, after the Wk product.
+        unsigned short kraw[8], qraw[8];
+        auto psd_fetch = [&](int it_) {
+            const int ci = p.c_lo + it_ / nheads, hdi = it_ % nheads;
+            const int hi = hdi % H, bi = hdi / H;
+            const int i = pt & 15;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = ci * C + (pt >> 4) + 8 * u;
+                kraw[u] = 0;
+                qraw[u] = 0;
+                if (i < p.fp && t < T) {
+                    // issued here, an item before their use (volatile: not sunk to it)
+                    const size_t off = (((size_t)bi * T + t) * H + hi) * p.fp + i;
+                    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(kraw[u]) : "l"(p.xk + off));
+                    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(qraw[u]) : "l"(p.xq + off));
+                }
+            }
+        };
+        // Thread kStorer stores the records and publishes their flags; its
+        // warp is idle while T's diagonal blocks are inverted, which is when
+        // it waits for the previous record's store to complete.
+        constexpr int kStorer = 64;
+        // DeltaKATA: the features of the item fetched last.  The values are
+        // staged as (key, query) words; thread pt then forms the 16-byte
+        // chunk pt % 16 (features 8 (pt % 16) ..) of tokens pt / 16 + 8 u of
+        // both tensors from the same two reads per feature, and writes psi(k)
+        // to the K tile and the record, psi(q) to the record.  The writers'
+        // proxy fences let the tensor core and the carry's bulk copies read
+        // the tiles after the lane's next barrier (the records after the
+        // item's flag).
+        auto psd_form = [&](int it_) {
+            uint32_t* xw = reinterpret_cast<uint32_t*>(sm + L::kXs);
+            const int part = pt & 15;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                xw[((pt >> 4) + 8 * u) * kXsLd + part] = (uint32_t)kraw[u] | ((uint32_t)qraw[u] << 16);
+            int fi[8], fj[8];
+            float fs[8];
+            psd_pairs(p.fp, part, fi, fj, fs);
+            uint8_t* gq = p.rec + ((size_t)(it_ % nheads) * p.nchunks + p.c_lo + it_ / nheads) * rec_bytes +
+                          Rec<DK>::kBytes;
+            bar_sync(B1, 128);
+#pragma unroll 2
+            for (int u = 0; u < 8; ++u) {
+                const int r = (pt >> 4) + 8 * u;
+                const uint32_t* xr = xw + r * kXsLd;
+                float vk[8], vq[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t wi = xr[fi[e]], wj = xr[fj[e]];
+                    vk[e] = fs[e] * __uint_as_float(wi << 16) * __uint_as_float(wj << 16);
+                    vq[e] = fs[e] * __uint_as_float(wi & 0xffff0000u) * __uint_as_float(wj & 0xffff0000u);
+                }
+                const uint32_t off = 8192u * (uint32_t)(part >> 3) + sw128_offset(r, (part & 7) * 8);
+                const uint4 pk = make_uint4(pack2(vk[0], vk[1]), pack2(vk[2], vk[3]), pack2(vk[4], vk[5]),
+                                            pack2(vk[6], vk[7]));
+                const uint4 pq = make_uint4(pack2(vq[0], vq[1]), pack2(vq[2], vq[3]), pack2(vq[4], vq[5]),
+                                            pack2(vq[6], vq[7]));
+                *reinterpret_cast<uint4*>(sm + L::kK + off) = pk;
+                *reinterpret_cast<uint4*>(gq + 16384u + off) = pk;
+                *reinterpret_cast<uint4*>(gq + off) = pq;
+            }
+            fence_proxy_async_smem();
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        };
+        if (feat && item0 < total) {
+            psd_fetch(item0);
+            psd_form(item0);
+            bar_sync(B1, 128);   // the K tile is complete
+        }
         if (pt == 0 && item0 < total) {
-            load_k(item0);
+            if (!feat) load_k(item0);
             issue_gram(p.c_lo + item0 / nheads);
         }
         // gates of an item, fetched one item ahead (threads 0..63, one token each)
@@ -361,10 +484,6 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
         };
         float gnext, enext;
         fetch_gates(item0, gnext, enext);
-        // Thread kStorer stores the records and publishes their flags; its
-        // warp is idle while T's diagonal blocks are inverted, which is when
-        // it waits for the previous record's store to complete.
-        constexpr int kStorer = 64;
         int pending = -1;  // (kStorer) item whose record store is not yet published
         auto publish = [&](int item) {
             const int c = p.c_lo + item / nheads, hd = item % nheads;
@@ -387,7 +506,7 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
         fetch_gates(item + istride, gnext, enext);
         // the next item's K tile is copied in only once this item's Wk has
         // read the tile; bring it into L2 now so that copy is short
-        if (pt == 0 && item + istride < total) {
+        if (!feat && pt == 0 && item + istride < total) {
             const int cn = p.c_lo + (item + istride) / nheads, hn = (item + istride) % nheads;
 #pragma unroll
             for (int kb = 0; kb < KB; ++kb) tma_prefetch_l2_4d(tm_kp, kb * 64, hn % H, cn * C, hn / H);
@@ -491,6 +610,8 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
             publish(pending);
             pending = -1;
         }
+        // DeltaKATA: the next item's values, requested while T is formed
+        if (feat && item + istride < total) psd_fetch(item + istride);
         // ---- T = (I + A)^{-1}: diagonal 16x16 blocks, right-looking
         if (pt < 64) {
             const int I = pt >> 4, j = pt & 15;
@@ -588,7 +709,7 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
         }
         if (!wt.group(2, ph, kWherePrepG, c, B3, 128)) break;
         tc_fence_after();
-        if (pt == 0 && item + istride < total) load_k(item + istride);   // Wk has read the tile
+        if (!feat && pt == 0 && item + istride < total) load_k(item + istride);   // Wk has read the tile
         {
             uint8_t* Wkt = sm + L::kWk;
 #pragma unroll
@@ -602,13 +723,14 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
                 }
             }
         }
+        if (feat && item + istride < total) psd_form(item + istride);   // Wk has read the K tile
         tc_fence_before();
         fence_proxy_async_smem();
         bar_sync(B1, 128);
         // Wk is out of TMEM: the next item's K K^T may overwrite it
         if (pt == 0 && item + istride < total) issue_gram(p.c_lo + (item + istride) / nheads);
         if (pt == kStorer) {
-            uint8_t* dst = p.rec + (((size_t)b * H + h) * p.nchunks + c) * Rec<DK>::kBytes;
+            uint8_t* dst = p.rec + (((size_t)b * H + h) * p.nchunks + c) * rec_bytes;
             bulk_store(dst, sm + L::kX, Rec<DK>::kGam);
             bulk_store(dst + Rec<DK>::kGam, gam, L::kVecBytes);
             bulk_commit();
@@ -642,7 +764,7 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
 }
 
 // Persistent prep grid: one lane per CTA; CTA i walks items i, i + gridDim.x, ...
-template <int DK>
+template <int DK, bool FEAT = false>
 __global__ void __launch_bounds__(kPrepThreads, kPrepPerSm)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) {
     using L = PrepLayout<DK>;
@@ -662,7 +784,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const PrepParams p) 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    prep_lane<DK>(&tm_k, p, sm, tmem, PrepLane{tid, 0, 1, (int)blockIdx.x, (int)gridDim.x, nullptr});
+    prep_lane<DK, FEAT>(&tm_k, p, sm, tmem, PrepLane{tid, 0, 1, (int)blockIdx.x, (int)gridDim.x, nullptr});
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -737,6 +859,9 @@ struct CarryParams {
     int lvl;                // the level (index into lambda's last axis)
     int L;                  // lambda's last extent
     const float* lam;       // [B][T][H][L]
+    // record stride (0: Rec<DK>::kBytes); larger when the records also hold
+    // DeltaKATA's feature tiles (state_cta<..., FEAT>)
+    uint32_t rec_bytes = 0;
 };
 
 // mbarrier slots (all with arrival count 1)
@@ -1278,7 +1403,8 @@ enum { SB_FULLA0 = 0, SB_FULLB0 = SB_FULLA0 + kStages, SB_EMPTYA0 = SB_FULLB0 + 
 // joins the CTA-wide barriers.  (bx, h, bz) play the roles of the grid
 // coordinates (x: the SUMMARY half, y: head, z: batch * runs + run).  With
 // `flags`, the record of a chunk is copied only once its flag is set.
-template <bool SUMMARY, bool LEVEL = false>
+// FEAT: the Q and K tiles come from the chunk records (DeltaKATA features)
+template <bool SUMMARY, bool LEVEL = false, bool FEAT = false>
 __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                           const CUtensorMap& tm_v, const CUtensorMap& tm_o,
                                           const CarryParams& p, uint8_t* sm, const int bx, const int h,
@@ -1343,6 +1469,8 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
     // chunk's S and P W.
     const uint32_t a_bytes = (SUMMARY ? 0u : 16384u) + (vhalf ? 16384u : 0u) + 16384u + 8192u;
     const uint32_t b_bytes = 16384u + 768u;
+    constexpr bool feat = FEAT;   // Q and K from the record (same bytes per group)
+    const uint32_t rec_bytes = p.rec_bytes ? p.rec_bytes : R::kBytes;
     auto load_inputs = [&](int c, bool group_a) {
         uint8_t* st = sm + (c % kStages) * L::kStageBytes;
         uint64_t* full = &bars[(group_a ? SB_FULLA0 : SB_FULLB0) + c % kStages];
@@ -1350,23 +1478,33 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
             if (!group_a) {
-                tma_load_4d(st + L::kK + kb * 8192, &tm_k, full, kb * 64, h, t0, b);
+                if (!feat) tma_load_4d(st + L::kK + kb * 8192, &tm_k, full, kb * 64, h, t0, b);
                 continue;
             }
-            if (!SUMMARY) tma_load_4d(st + L::kWQ + kb * 16384 + 8192, &tm_q, full, kb * 64, h, t0, b);
+            if (!SUMMARY && !feat) tma_load_4d(st + L::kWQ + kb * 16384 + 8192, &tm_q, full, kb * 64, h, t0, b);
             if (vhalf) tma_load_4d(st + L::kV + kb * 8192, &tm_v, full, kb * 64, h, t0, b);
         }
     };
     auto load_record = [&](int c, bool group_a) {
         uint8_t* st = sm + (c % kStages) * L::kStageBytes;
         uint64_t* full = &bars[(group_a ? SB_FULLA0 : SB_FULLB0) + c % kStages];
-        const uint8_t* rec = p.rec + (head * nchunks + c0 + c) * R::kBytes;
+        const uint8_t* rec = p.rec + (head * nchunks + c0 + c) * rec_bytes;
         if (!group_a) {
             bulk_load(st + L::kVec, rec + R::kGam, 768, full);
+            if (feat) {   // the features of K: the record's second appended tile
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+                    bulk_load(st + L::kK + kb * 8192, rec + R::kBytes + 16384 + kb * 8192, 8192, full);
+            }
             return;
         }
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) bulk_load(st + L::kWQ + kb * 16384, rec + R::kWk + kb * 8192, 8192, full);
+        if (feat && !SUMMARY) {   // the features of Q: the first appended tile
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb)
+                bulk_load(st + L::kWQ + kb * 16384 + 8192, rec + R::kBytes + kb * 8192, 8192, full);
+        }
         bulk_load(st + L::kTZ, rec + R::kTb, 8192, full);
     };
     // The start state (fp32 [DK][dv], 64 KB) comes in through stage 1 with a
@@ -1380,8 +1518,8 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
         // No grid of this call writes q, k or v, so the first stages' input
         // tiles are requested before the dependency wait below and arrive
         // while the grids before this one finish.
-        tma_prefetch_desc(&tm_k);
-        if (!SUMMARY) tma_prefetch_desc(&tm_q);
+        if (!feat) tma_prefetch_desc(&tm_k);
+        if (!SUMMARY && !feat) tma_prefetch_desc(&tm_q);
         if (vhalf) tma_prefetch_desc(&tm_v);
         for (int c = 0; c < first; ++c) {
             mbar_arrive_expect_tx(&bars[SB_FULLA0 + c], a_bytes);
@@ -1957,14 +2095,14 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
     if (warp == 13) tmem_dealloc(tmem, 512);
 }
 
-template <bool SUMMARY>
+template <bool SUMMARY, bool FEAT = false>
 __global__ void __launch_bounds__(kStateThreads, 1)
 chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                    const CarryParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    state_cta<SUMMARY>(tm_q, tm_k, tm_v, tm_o, p, sm, blockIdx.x, blockIdx.y, blockIdx.z, nullptr);
+    state_cta<SUMMARY, false, FEAT>(tm_q, tm_k, tm_v, tm_o, p, sm, blockIdx.x, blockIdx.y, blockIdx.z, nullptr);
 }
 
 // ============================================================================
@@ -1994,7 +2132,10 @@ constexpr size_t kFusedSmemBytes =
 // more than half of an SM's shared memory: one CTA per SM, so the SM ids of
 // a full grid are distinct
 static_assert(kFusedSmemBytes > 116 * 1024, "the fused grid relies on one CTA per SM");
-// register budget of a 14-warp carry: 128 per thread (65536 / 512)
+// register budget of a 14-warp carry: 128 per thread (65536 / 512).  FEAT:
+// DeltaKATA inputs (the prep lanes form the features, the carries copy them
+// from the records)
+template <bool FEAT = false>
 __global__ void __launch_bounds__(512, 1)
 chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -2018,7 +2159,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __syncthreads();
     if (role[0]) {
         const int hd = role[1];
-        state_cta<false>(tm_q, tm_k, tm_v, tm_o, cp, sm, 0, hd % cp.H, hd / cp.H, flags);
+        state_cta<false, false, FEAT>(tm_q, tm_k, tm_v, tm_o, cp, sm, 0, hd % cp.H, hd / cp.H, flags);
         return;
     }
     const int pidx = role[1];
@@ -2035,7 +2176,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    prep_lane<128>(&tm_k, pp, lsm, tmem + 128u * ln,
+    prep_lane<128, FEAT>(&tm_k, pp, lsm, tmem + 128u * ln,
                    PrepLane{tid - ln * kPrepThreads, ln * 4, 1 + 3 * ln, pidx * kFusedLanes + ln,
                             nprep * kFusedLanes, flags});
     tc_fence_before();
@@ -2156,16 +2297,40 @@ int sm_count() {
     return (e == cudaSuccess && n > 0) ? n : kScanTargetCtas;
 }
 
+// DeltaKATA inputs of a forward call: q and k as fp values per token-head,
+// their features formed by the prep lanes and kept in records of rec_bytes
+struct FeatIn {
+    const __nv_bfloat16* xq;
+    const __nv_bfloat16* xk;
+    int fp;
+    uint32_t rec_bytes;
+};
+constexpr uint32_t kFeatRecBytes = Rec<128>::kBytes + 2 * 16384;   // + psi(q), psi(k) tiles
+
 template <int DK>
 cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* g, const float* eta,
                       float eps, const float* h0, void* o, float* hT, int B, int T, int H, int dv,
                       DeviceErrorRecord* err, uint8_t* rec, int nseg, int seg_chunks, float* seg_x,
-                      float* seg_start, float* handoff, bool beta_direct, cudaStream_t stream) {
-    CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, B, T, H, DK) || !make_map(&mk, k, B, T, H, DK) ||
+                      float* seg_start, float* handoff, bool beta_direct, cudaStream_t stream,
+                      const FeatIn* feat = nullptr) {
+    // with DeltaKATA inputs (DK = 128, no scan, no chunk ranges) q and k are
+    // not read: their maps stay empty
+    CUtensorMap mq{}, mk{}, mv;
+    if ((!feat && (!make_map(&mq, q, B, T, H, DK) || !make_map(&mk, k, B, T, H, DK))) ||
         !make_map(&mv, v, B, T, H, dv))
         return cudaErrorInvalidValue;
-    auto prep = chunk_prep_kernel<DK>;
+    if (feat && (DK != 128 || dv != 128 || nseg != 1)) return cudaErrorNotSupported;
+    auto with_feat = [&](PrepParams pp) {
+        if (feat) { pp.xq = feat->xq; pp.xk = feat->xk; pp.fp = feat->fp; pp.rec_bytes = feat->rec_bytes; }
+        return pp;
+    };
+    auto with_feat_c = [&](CarryParams cp) {
+        if (feat) cp.rec_bytes = feat->rec_bytes;
+        return cp;
+    };
+    auto prep_plain = chunk_prep_kernel<DK, false>;
+    auto prep_feat = chunk_prep_kernel<DK, DK == 128>;
+    auto prep = feat ? prep_feat : prep_plain;
     auto carry = chunk_carry_kernel<DK, false>;
     auto summary = chunk_carry_kernel<DK, true>;
     auto combine = segment_combine_kernel<DK>;
@@ -2174,7 +2339,9 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
     // shared-memory limits, set on each device the first time it launches
     static PerDevice attrs;
     const cudaError_t attr_err = attrs.run([&](int, int&) {
-        cudaError_t r = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_prep);
+        cudaError_t r = cudaFuncSetAttribute(prep_plain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_prep);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(prep_feat, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_prep);
         if (r == cudaSuccess)
             r = cudaFuncSetAttribute(carry, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_carry);
         if (r == cudaSuccess)
@@ -2191,7 +2358,8 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
     auto launch_prep = [&](int c_lo, int c_hi, int max_ctas, bool pdl) -> cudaError_t {
         const int total = (c_hi - c_lo) * B * H;
         const int grid = total < max_ctas ? total : max_ctas;
-        PrepParams pp{g, eta, rec, err, eps, T, H, nchunks, B, c_lo, c_hi, pdl ? 1 : 0, beta_direct ? 1 : 0};
+        const PrepParams pp =
+            with_feat(PrepParams{g, eta, rec, err, eps, T, H, nchunks, B, c_lo, c_hi, pdl ? 1 : 0, beta_direct ? 1 : 0});
         if (!pdl) {
             prep<<<grid, kPrepThreads, smem_prep, stream>>>(mk, pp);
             return cudaGetLastError();
@@ -2214,9 +2382,11 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
     int fused_per_sm = 0;   // resident fused CTAs per SM on this device (0: the grid cannot be formed)
     if (DK == 128 && dv == 128 && chunk_fused(B, H, DK, dv, nseg)) {
         (void)fused_setup.run([&](int, int& per_sm) {
-            if (cudaFuncSetAttribute(chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(chunk_fused_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kFusedSmemBytes) != cudaSuccess ||
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chunk_fused_kernel, kFusedThreads,
+                cudaFuncSetAttribute(chunk_fused_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kFusedSmemBytes) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chunk_fused_kernel<false>, kFusedThreads,
                                                               kFusedSmemBytes) != cudaSuccess)
                 per_sm = 0;
             (void)cudaGetLastError();
@@ -2233,8 +2403,8 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
         int* flags = tickets + 2;
         if ((e = cudaMemsetAsync(tickets, 0, sizeof(int) * (2 + (size_t)B * H * nchunks), stream)) != cudaSuccess)
             return e;
-        CarryParams cp{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks, 0, nchunks, 1};
-        PrepParams pp{g, eta, rec, err, eps, T, H, nchunks, B, 0, nchunks, 0, beta_direct ? 1 : 0};
+        const CarryParams cp = with_feat_c(CarryParams{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks, 0, nchunks, 1});
+        const PrepParams pp = with_feat(PrepParams{g, eta, rec, err, eps, T, H, nchunks, B, 0, nchunks, 0, beta_direct ? 1 : 0});
         const int ncarry = B * H;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(sms);
@@ -2246,31 +2416,37 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
         at[0].val.cooperative = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, chunk_fused_kernel, mq, mk, mv, mo, cp, pp, tickets, flags, ncarry);
+        e = cudaLaunchKernelEx(&cfg, feat ? chunk_fused_kernel<true> : chunk_fused_kernel<false>, mq, mk, mv, mo, cp,
+                               pp, tickets, flags, ncarry);
         if (e != cudaErrorCooperativeLaunchTooLarge) return e;
         // fewer SMs usable than the device has (another context holds some):
         // the prep grid and then one carry grid instead
         (void)cudaGetLastError();
     }
     const int ranges = (DK == 128 && dv == 128) ? chunk_ranges(B, H, nchunks, nseg) : 1;  // >= 1
+    if (feat && ranges != 1) return cudaErrorNotSupported;
     if (ranges == 1 && (e = launch_prep(0, nchunks, kPrepPerSm * sms, false)) != cudaSuccess) return e;
     if (DK == 128 && dv == 128) {
         // transposed-state carry: one CTA per (head, run)
         CUtensorMap mo;
         if (!make_map(&mo, o, B, T, H, dv)) return cudaErrorInvalidValue;
-        auto state = chunk_state_kernel<false>;
+        auto state_plain = chunk_state_kernel<false>;
+        auto state_feat = chunk_state_kernel<false, true>;
+        auto state = feat ? state_feat : state_plain;
         auto state_sum = chunk_state_kernel<true>;
         constexpr size_t smem_state = StateLayout::kSmemBytes;
         static PerDevice state_attrs;
         const cudaError_t attr_s = state_attrs.run([&](int, int&) {
-            cudaError_t r = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_state);
+            cudaError_t r = cudaFuncSetAttribute(state_plain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_state);
+            if (r == cudaSuccess)
+                r = cudaFuncSetAttribute(state_feat, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_state);
             if (r == cudaSuccess)
                 r = cudaFuncSetAttribute(state_sum, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_state);
             return r;
         });
         if (attr_s != cudaSuccess) return attr_s;
         if (nseg == 1 && ranges == 1) {
-            CarryParams cp{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks, 0, nchunks};
+            const CarryParams cp = with_feat_c(CarryParams{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks, 0, nchunks});
             state<<<dim3(1, H, B), kStateThreads, smem_state, stream>>>(mq, mk, mv, mo, cp);
             return cudaGetLastError();
         }
@@ -2932,6 +3108,7 @@ size_t chunk_fwd_tc_extra_bytes(int B, int T, int H, int dk, int dv, int nseg) {
 int chunk_fwd_tc_auto_segments(int B, int T, int H, int dk, int dv) {
     const int nchunks = (T + C - 1) / C;
     const long long heads = (long long)B * H;
+    if (heads <= 0 || nchunks <= 0) return 1;   // nothing to split
     long long nseg;
     if (dk == 128 && dv == 128) {
         // one carry CTA per (head, run): enough runs for one full wave of the
@@ -2963,6 +3140,29 @@ cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, con
                               sh.seg_chunks, seg_x, seg_start, handoff, beta_direct, stream);
     return launch_dk<64>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, err, records, sh.nseg,
                          sh.seg_chunks, seg_x, seg_start, handoff, beta_direct, stream);
+}
+
+bool deltakata_fwd_tc_supported(int B, int T, int H) {
+    const int nchunks = (T + C - 1) / C;
+    return chunk_fwd_tc_auto_segments(B, T, H, 128, 128) == 1 && chunk_ranges(B, H, nchunks, 1) == 1;
+}
+
+size_t deltakata_fwd_tc_workspace_bytes(int B, int T, int H) {
+    const size_t nchunks = (size_t)((T + C - 1) / C);
+    return (size_t)B * H * nchunks * kFeatRecBytes + chunk_fwd_tc_extra_bytes(B, T, H, 128, 128, 1);
+}
+
+cudaError_t launch_deltakata_fwd_tc(const void* xq, const void* xk, int fp, const void* v, const float* g,
+                                    const float* eta, float eps, const float* h0, void* o, float* hT,
+                                    int B, int T, int H, bool beta_direct, DeviceErrorRecord* err,
+                                    uint8_t* records, cudaStream_t stream) {
+    const int nchunks = (T + C - 1) / C;
+    const FeatIn f{reinterpret_cast<const __nv_bfloat16*>(xq), reinterpret_cast<const __nv_bfloat16*>(xk), fp,
+                   kFeatRecBytes};
+    // after the records: the fused grid's counters and flags
+    float* after = reinterpret_cast<float*>(records + (size_t)B * H * nchunks * kFeatRecBytes);
+    return launch_dk<128>(nullptr, nullptr, v, g, eta, eps, h0, o, hT, B, T, H, 128, err, records, 1,
+                          nchunks > 0 ? nchunks : 1, after, after, after, beta_direct, stream, &f);
 }
 
 }  // namespace kla

@@ -288,6 +288,38 @@ KLA_API kla_status kla_psd_features_bwd(const void* x, const void* grad_y, void*
                                         void* stream);
 
 /*
+ * DeltaKATA forward in one call ("Kernelized Linear Attention: breaking the
+ * capacity wall via symmetric cones", sections 2.2 and 4): the
+ * recurrence of kla_chunk_fwd_ex run on psi(q_t), psi(k_t), where psi is
+ * kla_psd_features' map to 128 features.  The features are formed inside the
+ * prefill from the p values per token-head and never written to a tensor;
+ * o and hT equal, bit for bit, kla_psd_features of q and k (d_out = 128)
+ * followed by kla_chunk_fwd_ex with the same arguments.
+ *
+ *  xq, xk : [B, T, H, p] bf16, 4-byte aligned, 1 <= p <= 15
+ *  v, o   : [B, T, H, 128] bf16;  g, eta, eps, beta, h0, hT : as
+ *           kla_chunk_fwd_ex, with d_k = d_v = 128
+ *  chunk = 64; io = KLA_IO_BF16
+ *
+ * Supported where kla_chunk_fwd runs without the chunk-level scan and
+ * without chunk ranges (kla_deltakata_fwd_workspace_bytes > 0): for
+ * instance 39 <= B*H <= 76 heads of any length, or fewer heads with at most
+ * 63 chunks; otherwise KLA_ERR_UNSUPPORTED, and the caller forms the
+ * features with kla_psd_features.  The workspace (256-byte aligned, caller
+ * owned) holds the error record, then one 58,112-byte record per (batch,
+ * head, chunk): the 25,344 bytes of kla_chunk_fwd's record and the two
+ * feature tiles.  Errors as kla_chunk_fwd_ex; asynchronous on `stream`.
+ */
+KLA_API size_t kla_deltakata_fwd_workspace_bytes(int B, int T, int H, int p, int dv, int chunk,
+                                                 kla_io_dtype io);
+KLA_API kla_status kla_deltakata_fwd(const void* xq, const void* xk, const void* v,
+                                     const float* g, const float* eta, float eps,
+                                     const float* h0, void* o, float* hT, int B, int T, int H,
+                                     int p, int dv, int chunk, kla_io_dtype io,
+                                     kla_beta_mode beta, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/*
  * Segment count kla_chunk_fwd uses for this shape (1 = no scan).  With bf16
  * I/O and dk = dv = 128, when 4*B*H <= 152 (a GB300's SMs), it is
  * floor(152 / (B*H)): one full wave of per-(head, run) carry CTAs.  For the

@@ -237,3 +237,79 @@ def test_loglinear_fwd_empty_problem_is_a_no_op(lib):
     # no tokens: nothing to compute, the pointers and the workspace are not read
     assert _ll(lib, T=0, q=None, ws=None, wsb=0) == kla.KLA_OK
     assert _ll(lib, B=0, q=None, ws=None, wsb=0) == kla.KLA_OK
+
+
+# ---- kla_deltakata_fwd: sizes and argument checks (host side, no launch)
+
+def _dk_ws_want(B, T, H):
+    nch = (T + 63) // 64
+    flags = 0
+    if 2 * B * H <= 152:   # the fused grid's role counters and ready flags
+        flags = (4 * (2 + B * H * nch) + 255) // 256 * 256
+    return 256 + B * H * nch * 58112 + flags
+
+
+@pytest.mark.parametrize("B,T,H", [(1, 300, 2), (8, 4096, 8), (1, 2100, 40), (1, 128, 140)])
+def test_deltakata_workspace_bytes(lib, B, T, H):
+    # the error record, one 58,112-byte record per (b, h, chunk) (the prefill's
+    # 25,344 bytes and two 16 KB feature tiles), then the fused grid's flags
+    assert lib.kla_deltakata_fwd_workspace_bytes(B, T, H, 15, 128, 64, kla.KLA_IO_BF16) == _dk_ws_want(B, T, H)
+
+
+@pytest.mark.parametrize("args", [
+    (1, 300, 2, 16, 128, 64, kla.KLA_IO_BF16),     # p(p+1)/2 > 128
+    (1, 300, 2, 0, 128, 64, kla.KLA_IO_BF16),
+    (1, 300, 2, 15, 64, 64, kla.KLA_IO_BF16),      # d_v = 64
+    (1, 300, 2, 15, 128, 32, kla.KLA_IO_BF16),
+    (1, 300, 2, 15, 128, 64, kla.KLA_IO_FP32),
+    (1, 4096, 2, 15, 128, 64, kla.KLA_IO_BF16),    # runs with the chunk-level scan
+    (1, 4096, 100, 15, 128, 64, kla.KLA_IO_BF16),  # runs in chunk ranges
+])
+def test_deltakata_workspace_bytes_unsupported(lib, args):
+    assert lib.kla_deltakata_fwd_workspace_bytes(*args) == 0
+
+
+def _dkf(lib, **kw):
+    a = dict(xq=P, xk=P, v=P, g=P, eta=P, eps=1e-6, h0=None, o=P, hT=None, B=1, T=300, H=2, p=15,
+             dv=128, chunk=64, io=kla.KLA_IO_BF16, beta=kla.KLA_BETA_KACZMARZ, ws=WS, wsb=None)
+    a.update(kw)
+    if a["wsb"] is None:
+        a["wsb"] = _dk_ws_want(a["B"], a["T"], a["H"])
+    return lib.kla_deltakata_fwd(a["xq"], a["xk"], a["v"], a["g"], a["eta"], ctypes.c_float(a["eps"]),
+                                 a["h0"], a["o"], a["hT"], a["B"], a["T"], a["H"], a["p"], a["dv"],
+                                 a["chunk"], a["io"], a["beta"], a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(xq=None), kla.KLA_ERR_INVALID_ARG),
+    (dict(xk=None), kla.KLA_ERR_INVALID_ARG),
+    (dict(v=None), kla.KLA_ERR_INVALID_ARG),
+    (dict(xq=P + 2), kla.KLA_ERR_INVALID_ARG),        # not 4-byte aligned
+    (dict(v=P + 4), kla.KLA_ERR_INVALID_ARG),         # not 16-byte aligned
+    (dict(eps=-1.0), kla.KLA_ERR_INVALID_ARG),
+    (dict(beta=5), kla.KLA_ERR_INVALID_ARG),
+    (dict(p=0), kla.KLA_ERR_INVALID_ARG),
+    (dict(p=16), kla.KLA_ERR_UNSUPPORTED),
+    (dict(dv=64), kla.KLA_ERR_UNSUPPORTED),
+    (dict(io=kla.KLA_IO_FP32), kla.KLA_ERR_UNSUPPORTED),
+    (dict(T=4096), kla.KLA_ERR_UNSUPPORTED),          # the scan's shape
+    (dict(ws=None), kla.KLA_ERR_WORKSPACE),
+    (dict(ws=WS + 64), kla.KLA_ERR_WORKSPACE),
+    (dict(wsb=4096), kla.KLA_ERR_WORKSPACE),
+])
+def test_deltakata_fwd_rejects(lib, kw, code):
+    assert _dkf(lib, **kw) == code
+
+
+def test_deltakata_fwd_no_heads_is_a_no_op(lib):
+    assert _dkf(lib, B=0, xq=None, xk=None, v=None, g=None, eta=None, o=None, wsb=256) == kla.KLA_OK
+
+
+@pytest.mark.parametrize("B,T,H", [(0, 300, 2), (2, 300, 0), (2, 0, 3)])
+def test_segment_policy_and_workspace_of_empty_problems(lib, B, T, H):
+    # no heads or no tokens: one segment, and a workspace of the error record
+    # plus whatever the path keeps per chunk (nothing here)
+    assert lib.kla_chunk_fwd_auto_segments(B, T, H, 128, 128, 64, kla.KLA_IO_BF16) == 1
+    assert lib.kla_chunk_fwd_auto_segments(B, T, H, 64, 64, 64, kla.KLA_IO_BF16) == 1
+    assert lib.kla_chunk_fwd_workspace_bytes(B, T, H, 128, 128, 64, kla.KLA_IO_BF16) >= 256
+    assert lib.kla_deltakata_fwd_workspace_bytes(B, T, H, 15, 128, 64, kla.KLA_IO_BF16) >= 256

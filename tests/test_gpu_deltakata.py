@@ -112,3 +112,78 @@ def test_deltakata_end_to_end_forward_and_backward(io):
     for n, leaf in leaves.items():
         e = rel_err(leaf.grad, want[n])
         assert e <= TOL[io], f"d{n}: {e:.3e}"
+
+
+def _fused_vs_features(B, T, H, p, seed, h0=False, beta=0):
+    """kla_deltakata_fwd (features formed inside the prefill) against
+    kla_psd_features + kla_chunk_fwd_ex on the same inputs."""
+    kla = _kla()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    dt = torch.bfloat16
+    q = torch.randn((B, T, H, p), generator=gen, device="cuda").mul(0.4).to(dt)
+    u = torch.randn((B, T, H, p), generator=gen, device="cuda")
+    k = (u / u.norm(dim=-1, keepdim=True) * torch.empty((B, T, H, 1), device="cuda").uniform_(
+        0.5, 2.0, generator=gen)).to(dt)
+    v = torch.randn((B, T, H, 128), generator=gen, device="cuda").to(dt)
+    g = torch.nn.functional.logsigmoid(torch.randn((B, T, H), generator=gen, device="cuda") + 2.0)
+    eta = torch.sigmoid(torch.randn((B, T, H), generator=gen, device="cuda"))
+    s0 = torch.randn((B, H, 128, 128), generator=gen, device="cuda") * 0.05 if h0 else None
+    n = kla.kla_deltakata_fwd_workspace_bytes(B, T, H, p, 128)
+    assert n > 0
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    o = torch.empty((B, T, H, 128), dtype=dt, device="cuda")
+    hT = torch.empty((B, H, 128, 128), dtype=torch.float32, device="cuda")
+    kla.kla_deltakata_fwd(q, k, v, g, eta, 1e-6, s0, o, hT, ws, beta=beta)
+    assert kla.kla_workspace_check(ws) == kla.KLA_OK
+    fq, fk = kla.psd_features(q, 128), kla.psd_features(k, 128)
+    o2 = torch.empty_like(o)
+    h2 = torch.empty_like(hT)
+    ws2 = kla.alloc_workspace(B, T, H, 128, 128, 64, kla.KLA_IO_BF16, q.device)
+    kla.kla_chunk_fwd_ex(fq, fk, v, g, eta, 1e-6, s0, o2, h2, ws2, beta=beta)
+    torch.cuda.synchronize()
+    return (q, k, v, g, eta, s0), (o, hT), (o2, h2)
+
+
+@pytest.mark.parametrize("B,T,H,p,h0,beta", [
+    (1, 300, 2, 15, False, 0),     # ragged last chunk, fused grid
+    (2, 1000, 3, 11, True, 0),     # start state
+    (1, 64, 1, 1, False, 0),       # one value per token, one chunk
+    (3, 129, 5, 12, True, 1),      # direct step size, a one-token chunk
+    (1, 2100, 40, 15, False, 0),   # 40 heads of 33 chunks (fused grid, no scan)
+    (1, 128, 140, 15, True, 0),    # 140 heads: the prep grid and one carry grid
+])
+def test_fused_features_equal_features_then_prefill(B, T, H, p, h0, beta):
+    # the same feature bytes reach the same kernels: o and hT agree bit for bit
+    _, (o, hT), (o2, h2) = _fused_vs_features(B, T, H, p, 700 + 13 * p + H, h0, beta)
+    assert torch.equal(o, o2)
+    assert torch.equal(hT, h2)
+
+
+def test_fused_forward_matches_oracle():
+    # and against the oracle directly (features and recurrence in fp64)
+    (q, k, v, g, eta, s0), (o, hT), _ = _fused_vs_features(2, 200, 2, 15, 790, True)
+    fq, fk = oracle.kla_oracle_psd_features(q, 128), oracle.kla_oracle_psd_features(k, 128)
+    o_ref, h_ref = oracle.kla_oracle_forward(fq, fk, v, g, eta, 1e-6, s0)
+    assert rel_err(o, o_ref) <= TOL["bf16"]
+    assert rel_err(hT, h_ref) <= TOL["bf16"]
+
+
+def test_fused_forward_unsupported_shape_falls_back():
+    # few heads of a long sequence run with the chunk-level scan: the fused
+    # entry declines and deltakata() forms the features first
+    kla = _kla()
+    B, T, H, p = 1, 4096, 2, 15
+    assert kla.kla_deltakata_fwd_workspace_bytes(B, T, H, p, 128) == 0
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(800)
+    q = torch.randn((B, T, H, p), generator=gen, device="cuda").mul(0.4).to(torch.bfloat16)
+    u = torch.randn((B, T, H, p), generator=gen, device="cuda")
+    k = (u / u.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    v = torch.randn((B, T, H, 128), generator=gen, device="cuda").to(torch.bfloat16)
+    g = torch.nn.functional.logsigmoid(torch.randn((B, T, H), generator=gen, device="cuda") + 2.0)
+    eta = torch.sigmoid(torch.randn((B, T, H), generator=gen, device="cuda"))
+    o, hT = kla.deltakata(q, k, v, g, eta)
+    o2, h2 = kla.chunk_fwd(kla.psd_features(q, 128), kla.psd_features(k, 128), v, g, eta)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(hT, h2)
