@@ -103,7 +103,12 @@ kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v, const f
         return KLA_ERR_WORKSPACE;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(workspace, 0, kla::kErrorRecordBytes, st);
+    // the error record and, on the fused grid's path, its counters and flags
+    const size_t zero = kla::kErrorRecordBytes +
+        ((io == KLA_IO_BF16 && T > 0)
+             ? kla::chunk_fwd_tc_lead_bytes(B, T, H, dk, dv, kla::chunk_fwd_tc_scan_shape(T, segments).nseg)
+             : 0);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, zero, st);
     if (e != cudaSuccess) return KLA_ERR_CUDA;
     if (T == 0) {
         if (!hT) return KLA_OK;
@@ -357,7 +362,9 @@ kla_status kla_deltakata_fwd(const void* xq, const void* xk, const void* v, cons
         return KLA_ERR_WORKSPACE;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(workspace, 0, kla::kErrorRecordBytes, st);
+    // the error record and, on the fused grid's path, its counters and flags
+    const size_t zero = kla::kErrorRecordBytes + (T > 0 ? kla::chunk_fwd_tc_lead_bytes(B, T, H, 128, 128, 1) : 0);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, zero, st);
     if (e != cudaSuccess) return KLA_ERR_CUDA;
     if (T == 0) {
         if (!hT) return KLA_OK;

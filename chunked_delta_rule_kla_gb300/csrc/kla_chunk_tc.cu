@@ -2399,10 +2399,10 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
         // one cooperative grid: a carry CTA per head, prep lanes on the rest
         CUtensorMap mo;
         if (!make_map(&mo, o, B, T, H, dv)) return cudaErrorInvalidValue;
-        int* tickets = reinterpret_cast<int*>(handoff);   // 2 role counters, then the flags
+        // 2 role counters, then the flags: right after the error record,
+        // zeroed with it by the caller's one memset
+        int* tickets = reinterpret_cast<int*>(handoff);
         int* flags = tickets + 2;
-        if ((e = cudaMemsetAsync(tickets, 0, sizeof(int) * (2 + (size_t)B * H * nchunks), stream)) != cudaSuccess)
-            return e;
         const CarryParams cp = with_feat_c(CarryParams{h0, rec, ob, hT, err, T, H, dv, nchunks, 1, nchunks, 0, nchunks, 1});
         const PrepParams pp = with_feat(PrepParams{g, eta, rec, err, eps, T, H, nchunks, B, 0, nchunks, 0, beta_direct ? 1 : 0});
         const int ncarry = B * H;
@@ -3125,16 +3125,24 @@ int chunk_fwd_tc_auto_segments(int B, int T, int H, int dk, int dv) {
     return nseg > 1 ? (int)nseg : 1;
 }
 
+size_t chunk_fwd_tc_lead_bytes(int B, int T, int H, int dk, int dv, int nseg) {
+    return chunk_fused(B, H, dk, dv, nseg) ? chunk_fwd_tc_extra_bytes(B, T, H, dk, dv, nseg) : 0;
+}
+
 cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, const float* g,
                                 const float* eta, float eps, const float* h0, void* o, float* hT,
                                 int B, int T, int H, int dk, int dv, int segments, bool beta_direct,
                                 DeviceErrorRecord* err, uint8_t* records, cudaStream_t stream) {
     const ScanShape sh = chunk_fwd_tc_scan_shape(T, segments);
-    // after the records: the scan's maps and start states, or (without a
-    // scan) the state handed between chunk ranges
-    float* seg_x = reinterpret_cast<float*>(records + chunk_fwd_tc_record_bytes(B, T, H, dk));
+    // the fused grid's counters and flags come first (zeroed by the caller),
+    // then the records; after the records: the scan's maps and start states,
+    // or (without a scan) the state handed between chunk ranges
+    const size_t lead = chunk_fwd_tc_lead_bytes(B, T, H, dk, dv, sh.nseg);
+    uint8_t* recs = records + lead;
+    float* seg_x = reinterpret_cast<float*>(recs + chunk_fwd_tc_record_bytes(B, T, H, dk));
     float* seg_start = seg_x + (size_t)B * H * sh.nseg * dk * (dv + dk);
-    float* handoff = seg_x;
+    float* handoff = lead ? reinterpret_cast<float*>(records) : seg_x;
+    records = recs;
     if (dk == 128)
         return launch_dk<128>(q, k, v, g, eta, eps, h0, o, hT, B, T, H, dv, err, records, sh.nseg,
                               sh.seg_chunks, seg_x, seg_start, handoff, beta_direct, stream);
@@ -3159,10 +3167,11 @@ cudaError_t launch_deltakata_fwd_tc(const void* xq, const void* xk, int fp, cons
     const int nchunks = (T + C - 1) / C;
     const FeatIn f{reinterpret_cast<const __nv_bfloat16*>(xq), reinterpret_cast<const __nv_bfloat16*>(xk), fp,
                    kFeatRecBytes};
-    // after the records: the fused grid's counters and flags
-    float* after = reinterpret_cast<float*>(records + (size_t)B * H * nchunks * kFeatRecBytes);
-    return launch_dk<128>(nullptr, nullptr, v, g, eta, eps, h0, o, hT, B, T, H, 128, err, records, 1,
-                          nchunks > 0 ? nchunks : 1, after, after, after, beta_direct, stream, &f);
+    // the fused grid's counters and flags first (zeroed by the caller), then the records
+    const size_t lead = chunk_fwd_tc_lead_bytes(B, T, H, 128, 128, 1);
+    float* flags = reinterpret_cast<float*>(records);
+    return launch_dk<128>(nullptr, nullptr, v, g, eta, eps, h0, o, hT, B, T, H, 128, err, records + lead, 1,
+                          nchunks > 0 ? nchunks : 1, flags, flags, flags, beta_direct, stream, &f);
 }
 
 }  // namespace kla

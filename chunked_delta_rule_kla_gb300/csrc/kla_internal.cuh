@@ -108,6 +108,11 @@ cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, con
 size_t chunk_fwd_tc_record_bytes(int B, int T, int H, int dk);
 ScanShape chunk_fwd_tc_scan_shape(int T, int segments);
 size_t chunk_fwd_tc_extra_bytes(int B, int T, int H, int dk, int dv, int nseg);
+// The part of chunk_fwd_tc_extra_bytes that sits before the records, right
+// after the error record, and must start at zero: the fused grid's counters
+// and flags (0 on the other paths).  The caller zeroes it with the error
+// record in one memset.
+size_t chunk_fwd_tc_lead_bytes(int B, int T, int H, int dk, int dv, int nseg);
 // Unsegmented d_k = d_v = 128 with at most kScanTargetCtas / 2 heads: prep and
 // carry run in one cooperative grid (per-chunk ready flags in the workspace).
 bool chunk_fused(int B, int H, int dk, int dv, int nseg);
