@@ -105,8 +105,8 @@ def load_peaks():
 # so writes still in L2 when a launch ends are not counted.  Refresh these
 # whenever the kernels change.
 TRAFFIC_BYTES = {
-    "train_prefill_bf16_B8H8T4096d128": 453.5e6,
-    "gdn_train_prefill_bf16_B8H8T4096d128_unitkeys": 455.0e6,
+    "train_prefill_bf16_B8H8T4096d128": 453.4e6,
+    "gdn_train_prefill_bf16_B8H8T4096d128_unitkeys": 453.2e6,
     "long_prefill_bf16_B1H16T131072d128": 6223.7e6,
     "decode_bf16_B64H16d128_x1024": 73.9e6,
     "loglinear_train_prefill_bf16_B8H8T4096d128": 1760.5e6,
