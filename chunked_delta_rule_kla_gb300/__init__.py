@@ -599,9 +599,8 @@ def deltakata(q, k, v, g, eta, eps=1e-6, h0=None, d_feat=None, beta=KLA_BETA_KAC
 
     q, k [B,T,H,p] with p(p+1)/2 <= d_feat in {64, 128} (default: the smaller
     that fits); v [B,T,H,dv].  Differentiable; returns (o, hT).  With 128
-    features, bf16 and a shape kla_deltakata_fwd supports, the features are
-    formed inside the prefill (DeltaKATAFused); otherwise kla_psd_features
-    writes them first."""
+    features, bf16 and d_v = 128 the features are formed inside the prefill
+    (DeltaKATAFused); otherwise kla_psd_features writes them first."""
     B, T, H, p = k.shape
     if d_feat is None:
         d_feat = 64 if p * (p + 1) // 2 <= 64 else 128

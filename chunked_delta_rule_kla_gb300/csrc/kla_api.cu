@@ -332,7 +332,7 @@ size_t kla_deltakata_fwd_workspace_bytes(int B, int T, int H, int p, int dv, int
                                          kla_io_dtype io) {
     if (B < 0 || T < 0 || H < 0 || p < 1 || check_io(io) != KLA_OK) return 0;
     if (io != KLA_IO_BF16 || dv != 128 || chunk != 64 || p * (p + 1) / 2 > 128) return 0;
-    if (!sizes_fit(B, T, H, 128, 128) || !kla::deltakata_fwd_tc_supported(B, T, H)) return 0;
+    if (!sizes_fit(B, T, H, 128, 128)) return 0;
     return kla::kErrorRecordBytes + kla::deltakata_fwd_tc_workspace_bytes(B, T, H);
 }
 
@@ -346,8 +346,7 @@ kla_status kla_deltakata_fwd(const void* xq, const void* xk, const void* v, cons
     if (beta != KLA_BETA_KACZMARZ && beta != KLA_BETA_DIRECT) return KLA_ERR_INVALID_ARG;
     if (!(eps >= 0.f)) return KLA_ERR_INVALID_ARG;
     if (io != KLA_IO_BF16 || dv != 128 || chunk != 64 || p * (p + 1) / 2 > 128) return KLA_ERR_UNSUPPORTED;
-    if (!sizes_fit(B, T, H, 128, 128) || !kla::deltakata_fwd_tc_supported(B, T, H))
-        return KLA_ERR_UNSUPPORTED;
+    if (!sizes_fit(B, T, H, 128, 128)) return KLA_ERR_UNSUPPORTED;
     const bool have_tokens = (int64_t)B * H * T > 0;
     if (have_tokens && (!xq || !xk || !v || !g || !eta || !o)) return KLA_ERR_INVALID_ARG;
     if ((xq && !aligned4(xq)) || (xk && !aligned4(xk))) return KLA_ERR_INVALID_ARG;
@@ -363,7 +362,7 @@ kla_status kla_deltakata_fwd(const void* xq, const void* xk, const void* v, cons
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // the error record and, on the fused grid's path, its counters and flags
-    const size_t zero = kla::kErrorRecordBytes + (T > 0 ? kla::chunk_fwd_tc_lead_bytes(B, T, H, 128, 128, 1) : 0);
+    const size_t zero = kla::kErrorRecordBytes + (T > 0 ? kla::deltakata_fwd_tc_lead_bytes(B, T, H) : 0);
     cudaError_t e = cudaMemsetAsync(workspace, 0, zero, st);
     if (e != cudaSuccess) return KLA_ERR_CUDA;
     if (T == 0) {

@@ -2319,7 +2319,7 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
     if ((!feat && (!make_map(&mq, q, B, T, H, DK) || !make_map(&mk, k, B, T, H, DK))) ||
         !make_map(&mv, v, B, T, H, dv))
         return cudaErrorInvalidValue;
-    if (feat && (DK != 128 || dv != 128 || nseg != 1)) return cudaErrorNotSupported;
+    if (feat && (DK != 128 || dv != 128)) return cudaErrorNotSupported;
     auto with_feat = [&](PrepParams pp) {
         if (feat) { pp.xq = feat->xq; pp.xk = feat->xk; pp.fp = feat->fp; pp.rec_bytes = feat->rec_bytes; }
         return pp;
@@ -2424,7 +2424,6 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
         (void)cudaGetLastError();
     }
     const int ranges = (DK == 128 && dv == 128) ? chunk_ranges(B, H, nchunks, nseg) : 1;  // >= 1
-    if (feat && ranges != 1) return cudaErrorNotSupported;
     if (ranges == 1 && (e = launch_prep(0, nchunks, kPrepPerSm * sms, false)) != cudaSuccess) return e;
     if (DK == 128 && dv == 128) {
         // transposed-state carry: one CTA per (head, run)
@@ -2433,7 +2432,9 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
         auto state_plain = chunk_state_kernel<false>;
         auto state_feat = chunk_state_kernel<false, true>;
         auto state = feat ? state_feat : state_plain;
-        auto state_sum = chunk_state_kernel<true>;
+        auto state_sum_plain = chunk_state_kernel<true>;
+        auto state_sum_feat = chunk_state_kernel<true, true>;
+        auto state_sum = feat ? state_sum_feat : state_sum_plain;
         constexpr size_t smem_state = StateLayout::kSmemBytes;
         static PerDevice state_attrs;
         const cudaError_t attr_s = state_attrs.run([&](int, int&) {
@@ -2441,7 +2442,9 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
             if (r == cudaSuccess)
                 r = cudaFuncSetAttribute(state_feat, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_state);
             if (r == cudaSuccess)
-                r = cudaFuncSetAttribute(state_sum, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_state);
+                r = cudaFuncSetAttribute(state_sum_plain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_state);
+            if (r == cudaSuccess)
+                r = cudaFuncSetAttribute(state_sum_feat, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_state);
             return r;
         });
         if (attr_s != cudaSuccess) return attr_s;
@@ -2477,20 +2480,23 @@ cudaError_t launch_dk(const void* q, const void* k, const void* v, const float* 
             if ((e = launch_prep(bounds[0], bounds[1], kPrepPerSm * sms, false)) != cudaSuccess) return e;
             for (int r = 0; r < nr; ++r) {
                 const bool last = r == nr - 1;
-                CarryParams cp{r == 0 ? h0 : handoff, rec, ob, last ? hT : handoff, err, T, H, dv, nchunks,
-                               1, bounds[r + 1] - bounds[r], bounds[r], bounds[r + 1]};
+                const CarryParams cp = with_feat_c(CarryParams{r == 0 ? h0 : handoff, rec, ob, last ? hT : handoff, err,
+                                                               T, H, dv, nchunks, 1, bounds[r + 1] - bounds[r],
+                                                               bounds[r], bounds[r + 1]});
                 if ((e = launch_state(cp, r > 0)) != cudaSuccess) return e;
                 if (!last && (e = launch_prep(bounds[r + 1], bounds[r + 2], kPrepPerSm * free_sms, true)) != cudaSuccess)
                     return e;
             }
             return cudaSuccess;
         }
-        CarryParams c1{nullptr, rec, nullptr, seg_x, err, T, H, dv, nchunks, nseg, seg_chunks, 0, nchunks};
+        const CarryParams c1 =
+            with_feat_c(CarryParams{nullptr, rec, nullptr, seg_x, err, T, H, dv, nchunks, nseg, seg_chunks, 0, nchunks});
         state_sum<<<dim3(2, H, B * nseg), kStateThreads, smem_state, stream>>>(mq, mk, mv, mo, c1);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         combine<<<dim3(dv / 16, H, B), 2 * DK, smem_comb, stream>>>(seg_x, h0, seg_start, H, nseg, dv);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        CarryParams c3{seg_start, rec, ob, hT, err, T, H, dv, nchunks, nseg, seg_chunks, 0, nchunks};
+        const CarryParams c3 =
+            with_feat_c(CarryParams{seg_start, rec, ob, hT, err, T, H, dv, nchunks, nseg, seg_chunks, 0, nchunks});
         state<<<dim3(1, H, B * nseg), kStateThreads, smem_state, stream>>>(mq, mk, mv, mo, c3);
         return cudaGetLastError();
     }
@@ -3150,28 +3156,34 @@ cudaError_t launch_chunk_fwd_tc(const void* q, const void* k, const void* v, con
                          sh.seg_chunks, seg_x, seg_start, handoff, beta_direct, stream);
 }
 
-bool deltakata_fwd_tc_supported(int B, int T, int H) {
-    const int nchunks = (T + C - 1) / C;
-    return chunk_fwd_tc_auto_segments(B, T, H, 128, 128) == 1 && chunk_ranges(B, H, nchunks, 1) == 1;
-}
-
 size_t deltakata_fwd_tc_workspace_bytes(int B, int T, int H) {
     const size_t nchunks = (size_t)((T + C - 1) / C);
-    return (size_t)B * H * nchunks * kFeatRecBytes + chunk_fwd_tc_extra_bytes(B, T, H, 128, 128, 1);
+    const int nseg = chunk_fwd_tc_scan_shape(T, chunk_fwd_tc_auto_segments(B, T, H, 128, 128)).nseg;
+    return (size_t)B * H * nchunks * kFeatRecBytes + chunk_fwd_tc_extra_bytes(B, T, H, 128, 128, nseg);
+}
+
+size_t deltakata_fwd_tc_lead_bytes(int B, int T, int H) {
+    const int nseg = chunk_fwd_tc_scan_shape(T, chunk_fwd_tc_auto_segments(B, T, H, 128, 128)).nseg;
+    return chunk_fwd_tc_lead_bytes(B, T, H, 128, 128, nseg);
 }
 
 cudaError_t launch_deltakata_fwd_tc(const void* xq, const void* xk, int fp, const void* v, const float* g,
                                     const float* eta, float eps, const float* h0, void* o, float* hT,
                                     int B, int T, int H, bool beta_direct, DeviceErrorRecord* err,
                                     uint8_t* records, cudaStream_t stream) {
-    const int nchunks = (T + C - 1) / C;
+    const ScanShape sh = chunk_fwd_tc_scan_shape(T, chunk_fwd_tc_auto_segments(B, T, H, 128, 128));
     const FeatIn f{reinterpret_cast<const __nv_bfloat16*>(xq), reinterpret_cast<const __nv_bfloat16*>(xk), fp,
                    kFeatRecBytes};
-    // the fused grid's counters and flags first (zeroed by the caller), then the records
-    const size_t lead = chunk_fwd_tc_lead_bytes(B, T, H, 128, 128, 1);
-    float* flags = reinterpret_cast<float*>(records);
-    return launch_dk<128>(nullptr, nullptr, v, g, eta, eps, h0, o, hT, B, T, H, 128, err, records + lead, 1,
-                          nchunks > 0 ? nchunks : 1, flags, flags, flags, beta_direct, stream, &f);
+    // as kla_chunk_fwd's workspace, with the larger records: the fused grid's
+    // counters and flags first (zeroed by the caller), then the records, then
+    // the scan's maps and start states or the state handed between chunk ranges
+    const size_t lead = chunk_fwd_tc_lead_bytes(B, T, H, 128, 128, sh.nseg);
+    uint8_t* recs = records + lead;
+    float* seg_x = reinterpret_cast<float*>(recs + (size_t)B * H * ((T + C - 1) / C) * kFeatRecBytes);
+    float* seg_start = seg_x + (size_t)B * H * sh.nseg * 128 * (128 + 128);
+    float* handoff = lead ? reinterpret_cast<float*>(records) : seg_x;
+    return launch_dk<128>(nullptr, nullptr, v, g, eta, eps, h0, o, hT, B, T, H, 128, err, recs, sh.nseg,
+                          sh.seg_chunks, seg_x, seg_start, handoff, beta_direct, stream, &f);
 }
 
 }  // namespace kla

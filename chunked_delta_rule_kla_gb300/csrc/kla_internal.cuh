@@ -121,14 +121,15 @@ int chunk_ranges(int B, int H, int nchunks, int nseg);
 // bounds[n] = nchunks) and returns n <= kMaxRanges.
 int chunk_range_bounds(int nchunks, int* bounds);
 int chunk_fwd_tc_auto_segments(int B, int T, int H, int dk, int dv);
-// DeltaKATA forward on the same path (bf16, 128 features, d_v = 128): the
-// prep lanes form psi(k) and psi(q) from xk, xq [B][T][H][fp] (fp <= 15) and
-// keep both tiles in the chunk records, which the carries copy in place of
-// TMA loads of q and k.  Shapes that the automatic policy runs with a scan or
-// with chunk ranges are not supported.  The records, then the fused grid's
-// flags, take deltakata_fwd_tc_workspace_bytes after the error record.
-bool deltakata_fwd_tc_supported(int B, int T, int H);
+// DeltaKATA forward on the same paths (bf16, 128 features, d_v = 128; the
+// automatic segment count): the prep lanes form psi(k) and psi(q) from xk,
+// xq [B][T][H][fp] (fp <= 15) and keep both tiles in the chunk records, which
+// the carries copy in place of TMA loads of q and k.  The workspace after
+// the error record is laid out as kla_chunk_fwd's with the larger records
+// (deltakata_fwd_tc_workspace_bytes); its first deltakata_fwd_tc_lead_bytes
+// must be zeroed with the error record.
 size_t deltakata_fwd_tc_workspace_bytes(int B, int T, int H);
+size_t deltakata_fwd_tc_lead_bytes(int B, int T, int H);
 cudaError_t launch_deltakata_fwd_tc(const void* xq, const void* xk, int fp, const void* v, const float* g,
                                     const float* eta, float eps, const float* h0, void* o, float* hT,
                                     int B, int T, int H, bool beta_direct, DeviceErrorRecord* err,

@@ -301,14 +301,12 @@ KLA_API kla_status kla_psd_features_bwd(const void* x, const void* grad_y, void*
  *           kla_chunk_fwd_ex, with d_k = d_v = 128
  *  chunk = 64; io = KLA_IO_BF16
  *
- * Supported where kla_chunk_fwd runs without the chunk-level scan and
- * without chunk ranges (kla_deltakata_fwd_workspace_bytes > 0): for
- * instance 39 <= B*H <= 76 heads of any length, or fewer heads with at most
- * 63 chunks; otherwise KLA_ERR_UNSUPPORTED, and the caller forms the
- * features with kla_psd_features.  The workspace (256-byte aligned, caller
- * owned) holds the error record, then one 58,112-byte record per (batch,
- * head, chunk): the 25,344 bytes of kla_chunk_fwd's record and the two
- * feature tiles.  Errors as kla_chunk_fwd_ex; asynchronous on `stream`.
+ * The call takes kla_chunk_fwd's paths for the shape (the automatic segment
+ * count: the fused grid, chunk ranges or the chunk-level scan).  The
+ * workspace (kla_deltakata_fwd_workspace_bytes, 256-byte aligned, caller
+ * owned) is kla_chunk_fwd's with each 25,344-byte chunk record grown to
+ * 58,112 bytes by the two feature tiles.  Errors as kla_chunk_fwd_ex;
+ * asynchronous on `stream`.
  */
 KLA_API size_t kla_deltakata_fwd_workspace_bytes(int B, int T, int H, int p, int dv, int chunk,
                                                  kla_io_dtype io);

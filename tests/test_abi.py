@@ -256,14 +256,22 @@ def test_deltakata_workspace_bytes(lib, B, T, H):
     assert lib.kla_deltakata_fwd_workspace_bytes(B, T, H, 15, 128, 64, kla.KLA_IO_BF16) == _dk_ws_want(B, T, H)
 
 
+@pytest.mark.parametrize("B,T,H", [(1, 4096, 2), (1, 131072, 16), (1, 4096, 100), (2, 300, 70)])
+def test_deltakata_workspace_is_the_prefills_with_larger_records(lib, B, T, H):
+    # the chunk-level scan, chunk ranges and the prep-then-carry shapes: the
+    # prefill's workspace with each record grown by the two feature tiles
+    nch = (T + 63) // 64
+    plain = lib.kla_chunk_fwd_workspace_bytes(B, T, H, 128, 128, 64, kla.KLA_IO_BF16)
+    fused = lib.kla_deltakata_fwd_workspace_bytes(B, T, H, 15, 128, 64, kla.KLA_IO_BF16)
+    assert fused - plain == B * H * nch * (58112 - 25344)
+
+
 @pytest.mark.parametrize("args", [
     (1, 300, 2, 16, 128, 64, kla.KLA_IO_BF16),     # p(p+1)/2 > 128
     (1, 300, 2, 0, 128, 64, kla.KLA_IO_BF16),
     (1, 300, 2, 15, 64, 64, kla.KLA_IO_BF16),      # d_v = 64
     (1, 300, 2, 15, 128, 32, kla.KLA_IO_BF16),
     (1, 300, 2, 15, 128, 64, kla.KLA_IO_FP32),
-    (1, 4096, 2, 15, 128, 64, kla.KLA_IO_BF16),    # runs with the chunk-level scan
-    (1, 4096, 100, 15, 128, 64, kla.KLA_IO_BF16),  # runs in chunk ranges
 ])
 def test_deltakata_workspace_bytes_unsupported(lib, args):
     assert lib.kla_deltakata_fwd_workspace_bytes(*args) == 0
@@ -292,7 +300,6 @@ def _dkf(lib, **kw):
     (dict(p=16), kla.KLA_ERR_UNSUPPORTED),
     (dict(dv=64), kla.KLA_ERR_UNSUPPORTED),
     (dict(io=kla.KLA_IO_FP32), kla.KLA_ERR_UNSUPPORTED),
-    (dict(T=4096), kla.KLA_ERR_UNSUPPORTED),          # the scan's shape
     (dict(ws=None), kla.KLA_ERR_WORKSPACE),
     (dict(ws=WS + 64), kla.KLA_ERR_WORKSPACE),
     (dict(wsb=4096), kla.KLA_ERR_WORKSPACE),

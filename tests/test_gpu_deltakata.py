@@ -169,21 +169,13 @@ def test_fused_forward_matches_oracle():
     assert rel_err(hT, h_ref) <= TOL["bf16"]
 
 
-def test_fused_forward_unsupported_shape_falls_back():
-    # few heads of a long sequence run with the chunk-level scan: the fused
-    # entry declines and deltakata() forms the features first
+@pytest.mark.parametrize("B,T,H,p,h0", [
+    (1, 4096, 2, 15, True),      # two heads: the chunk-level scan (2 runs), a start state
+    (1, 2100, 100, 12, False),   # 100 heads of 33 chunks: chunk ranges
+])
+def test_fused_features_on_the_scan_and_range_paths(B, T, H, p, h0):
     kla = _kla()
-    B, T, H, p = 1, 4096, 2, 15
-    assert kla.kla_deltakata_fwd_workspace_bytes(B, T, H, p, 128) == 0
-    gen = torch.Generator(device="cuda")
-    gen.manual_seed(800)
-    q = torch.randn((B, T, H, p), generator=gen, device="cuda").mul(0.4).to(torch.bfloat16)
-    u = torch.randn((B, T, H, p), generator=gen, device="cuda")
-    k = (u / u.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
-    v = torch.randn((B, T, H, 128), generator=gen, device="cuda").to(torch.bfloat16)
-    g = torch.nn.functional.logsigmoid(torch.randn((B, T, H), generator=gen, device="cuda") + 2.0)
-    eta = torch.sigmoid(torch.randn((B, T, H), generator=gen, device="cuda"))
-    o, hT = kla.deltakata(q, k, v, g, eta)
-    o2, h2 = kla.chunk_fwd(kla.psd_features(q, 128), kla.psd_features(k, 128), v, g, eta)
-    torch.cuda.synchronize()
-    assert torch.equal(o, o2) and torch.equal(hT, h2)
+    assert kla.kla_chunk_fwd_auto_segments(B, T, H, 128, 128) == (2 if H == 2 else 1)
+    _, (o, hT), (o2, h2) = _fused_vs_features(B, T, H, p, 900 + H, h0)
+    assert torch.equal(o, o2)
+    assert torch.equal(hT, h2)
