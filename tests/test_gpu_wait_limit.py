@@ -76,6 +76,56 @@ def test_flag_wait_runs_out_and_is_reported():
     assert res["again"] == kla.KLA_ERR_DEVICE_TIMEOUT     # the variant never publishes that flag
 
 
+CHILD_DELTAKATA = r"""
+import json, sys
+import torch
+import chunked_delta_rule_kla_gb300 as kla
+import oracle
+from tests.parity_utils import rel_err
+
+kla.load_library(sys.argv[1])
+B, T, H, p = 1, 512, 4, 15
+gen = torch.Generator(device="cuda")
+gen.manual_seed(6)
+xq = (torch.randn((B, T, H, p), generator=gen, device="cuda") * 0.4).to(torch.bfloat16)
+u = torch.randn((B, T, H, p), generator=gen, device="cuda")
+xk = (u / u.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+v = torch.randn((B, T, H, 128), generator=gen, device="cuda").to(torch.bfloat16)
+g = torch.nn.functional.logsigmoid(torch.randn((B, T, H), generator=gen, device="cuda") + 2.0)
+eta = torch.sigmoid(torch.randn((B, T, H), generator=gen, device="cuda"))
+ws = torch.empty(kla.kla_deltakata_fwd_workspace_bytes(B, T, H, p, 128), dtype=torch.uint8, device="cuda")
+o = torch.zeros((B, T, H, 128), dtype=torch.bfloat16, device="cuda")
+hT = torch.zeros((B, H, 128, 128), device="cuda")
+kla.kla_deltakata_fwd(xq, xk, v, g, eta, 1e-6, None, o, hT, ws)
+status = kla.kla_workspace_check(ws)
+record = ws[:16].view(torch.int32).cpu().tolist()
+hs = slice(1, 4)
+fq = oracle.kla_oracle_psd_features(xq[:, :, hs], 128)
+fk = oracle.kla_oracle_psd_features(xk[:, :, hs], 128)
+o_ref, h_ref = oracle.kla_oracle_forward(fq, fk, v[:, :, hs], g[:, :, hs], eta[:, :, hs], 1e-6)
+other_heads = max(rel_err(o[:, :, hs], o_ref), rel_err(hT[:, hs], h_ref))
+torch.cuda.synchronize()
+print(json.dumps(dict(status=status, record=record[:4], other_heads=other_heads)))
+"""
+
+
+def test_flag_wait_runs_out_with_deltakata_inputs():
+    # the same bounded flag wait on the feature path (kla_deltakata_fwd)
+    import chunked_delta_rule_kla_gb300 as kla
+    from chunked_delta_rule_kla_gb300 import _build
+    variant = _build.build(
+        extra_flags=["-DKLA_TEST_FLAG_WAIT_NS=2000000ull", f"-DKLA_TEST_UNPUBLISHED_CHUNK={UNPUBLISHED}"],
+        build_dir=os.path.join(_build.BUILD_DIR, "wait_test"))
+    r = subprocess.run([sys.executable, "-c", CHILD_DELTAKATA, variant], cwd=ROOT, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    assert res["status"] == kla.KLA_ERR_DEVICE_TIMEOUT
+    code, where, block, detail = res["record"]
+    assert code == 1 and where == WHERE_FLAG and detail == UNPUBLISHED
+    assert res["other_heads"] <= TOL["bf16"]
+
+
 def test_decode_step_checked_matches_and_reports_no_error():
     import chunked_delta_rule_kla_gb300 as kla
     case = kla_inputs.DECODE.with_(B=3, H=5, dk=128, dv=128, steps=4, io="bf16", seed=17)
