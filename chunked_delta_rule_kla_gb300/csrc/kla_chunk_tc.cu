@@ -399,18 +399,20 @@ __device__ __forceinline__ void prep_lane(const CUtensorMap* tm_kp, const PrepPa
         unsigned short kraw[8], qraw[8];
         auto psd_fetch = [&](int it_) {
             const int ci = p.c_lo + it_ / nheads, hdi = it_ % nheads;
-            const int hi = hdi % H, bi = hdi / H;
-            const int i = pt & 15;
+            const int i = pt & 15, t = ci * C + (pt >> 4);
+            // element offset of value i of token t, then 8 tokens further per u
+            const size_t off = (((size_t)(hdi / H) * T + t) * H + hdi % H) * p.fp + i;
+            const size_t step = (size_t)8 * H * p.fp;
+            const __nv_bfloat16* xk = p.xk + off;
+            const __nv_bfloat16* xq = p.xq + off;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int t = ci * C + (pt >> 4) + 8 * u;
                 kraw[u] = 0;
                 qraw[u] = 0;
-                if (i < p.fp && t < T) {
+                if (i < p.fp && t + 8 * u < T) {
                     // issued here, an item before their use (volatile: not sunk to it)
-                    const size_t off = (((size_t)bi * T + t) * H + hi) * p.fp + i;
-                    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(kraw[u]) : "l"(p.xk + off));
-                    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(qraw[u]) : "l"(p.xq + off));
+                    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(kraw[u]) : "l"(xk + u * step));
+                    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(qraw[u]) : "l"(xq + u * step));
                 }
             }
         };
