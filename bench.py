@@ -526,11 +526,30 @@ def bench_loglinear(case, K, W, flush, peaks, stream):
     return res
 
 
+def loglinear_decode_bytes(B, H, dk, dv, L, steps, esz):
+    """Algorithmic bytes of Log-Linear decoding tokens 0 .. steps-1: at token
+    t > 0, with b the lowest set bit of t, each non-empty level is read
+    (popcount(t-1) + 1 of them), the levels above b + 1 are written back, and
+    the merged level b + 1 and the new level 0 are written; plus each token's
+    q, k, v, o, g, eta and lambda."""
+    sbytes = dk * dv * 4
+    total = 0
+    for t in range(steps):
+        touched = 0
+        if t > 0:
+            present = bin(t - 1).count("1") + 1
+            b = (t & -t).bit_length() - 1          # levels 0 .. b merge into b + 1
+            touched = present * sbytes + (present - (b + 1)) * sbytes + sbytes
+        total += B * H * (touched + sbytes + esz * (2 * dk + 2 * dv) + 8 + 4 * L)
+    return total
+
+
 def bench_loglinear_decode(case, steps, peaks, stream):
     """Time kla_loglinear_decode_step over tokens 0 .. steps-1 of ``case``'s
-    heads (states zero at token 0).  Algorithmic bytes of token t: each
-    non-empty bucket state read and written (popcount(t-1) + 1 of them for
-    t > 0), the merged and new states written, q, k, v, o, g, eta, lambda."""
+    heads (states zero at token 0).  Algorithmic bytes of token t > 0, with b
+    the lowest set bit of t: each non-empty bucket state read (popcount(t-1)
+    + 1 of them), those above level b + 1 written back, the merged level b + 1
+    and the new level 0 written; q, k, v, o, g, eta, lambda."""
     import chunked_delta_rule_kla_gb300 as kla
     B, H, dk, dv = case.B, case.H, case.dk, case.dv
     L = kla.kla_loglinear_num_levels(steps)
@@ -546,11 +565,7 @@ def bench_loglinear_decode(case, steps, peaks, stream):
     states = torch.zeros((B, H, L, dk, dv), device="cuda")
     o = torch.empty((B, H, dv), dtype=dt, device="cuda")
     esz = 2 if case.io == "bf16" else 4
-    sbytes = dk * dv * 4
-    total = 0
-    for t in range(steps):
-        touched = (bin(t - 1).count("1") + 1) * 2 * sbytes + sbytes if t > 0 else 0
-        total += B * H * (touched + sbytes + esz * (2 * dk + 2 * dv) + 8 + 4 * L)
+    total = loglinear_decode_bytes(B, H, dk, dv, L, steps, esz)
 
     def run():
         for t in range(steps):

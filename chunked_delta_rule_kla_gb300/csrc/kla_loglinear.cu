@@ -504,11 +504,9 @@ __global__ void __launch_bounds__(256) ll_decode_kernel(const TIO* __restrict__ 
                 for (int i = 0; i < 8; ++i)
                     if (i < rows) S[(size_t)(r0 + i) * DV + col0 + col] = x[i];
                 out += slam[l] * y;   // column-summed once, after the last level
-            } else if (l > 0) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (i < rows) S[(size_t)(r0 + i) * DV + col0 + col] = 0.f;   // merged away
             }
+            // levels 1 .. b are merged away and left as they are: an empty
+            // level is read again only after a merge has overwritten it
         }
         // the merged level b + 1
         float* S = st + (size_t)(b + 1) * SS;

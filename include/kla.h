@@ -247,8 +247,9 @@ KLA_API kla_status kla_loglinear_fwd(const void* q, const void* k, const void* v
  * One Log-Linear decode step (token t) for B*H heads, O(log T) per token: the
  * Fenwick update of the Log-Linear page.  `states` [B, H, L, dk, dv] fp32
  * holds the bucket states relative to token t - 1 (level 0: token t - 1;
- * level j + 1: non-empty when bit j of t - 1 is set); the caller zero-fills it
- * before t = 0 and passes t = 0, 1, 2, ... in order.  Every non-empty state
+ * level j + 1: non-empty when bit j of t - 1 is set; the contents of an empty
+ * level are unspecified); the caller zero-fills it before t = 0 and passes
+ * t = 0, 1, 2, ... in order.  Every non-empty state
  * takes the transition a_t (I - beta_t k_t k_t^T); with b the lowest set bit
  * of t, levels 0..b merge into level b + 1, the write beta_t k_t v_t^T becomes
  * level 0, and o_t = sum_l lambda_t^(l) S^(l)^T q_t.  Decoding a whole

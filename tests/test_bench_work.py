@@ -48,3 +48,26 @@ def test_decode_bytes():
     # the fp32 state read and written, q, k, v, o in bf16, g and eta
     assert w["bytes"] == heads * (2 * c.dk * c.dv * 4 + 2 * (2 * c.dk + 2 * c.dv) + 8)
     assert round(w["bytes"] / 1e6, 1) == 135.3
+
+
+def test_loglinear_decode_bytes_against_a_simulated_bucket_set():
+    # replay the buckets token by token (the set of non-empty levels as the
+    # decode step defines it) and count the state tiles read and written
+    import bench
+    B, H, dk, dv, L, steps, esz = 2, 3, 128, 64, 11, 300, 2
+    tile = dk * dv * 4
+    nonempty = set()
+    want = 0
+    for t in range(steps):
+        reads = writes = 0
+        if t > 0:
+            reads = len(nonempty)                    # every non-empty level takes the transition
+            b = (t & -t).bit_length() - 1
+            assert b + 1 not in nonempty
+            merged = {l for l in nonempty if l <= b}
+            writes = len(nonempty - merged) + 1       # the rest written back, the merge target written
+            nonempty = (nonempty - merged) | {b + 1}
+        writes += 1                                   # the new level 0
+        nonempty.add(0)
+        want += B * H * ((reads + writes) * tile + esz * (2 * dk + 2 * dv) + 8 + 4 * L)
+    assert bench.loglinear_decode_bytes(B, H, dk, dv, L, steps, esz) == want
