@@ -368,22 +368,27 @@ def e2e_prefill(kla, case, inp, ws, work, K, stream, sets=2, up_streams=3):
         started[j] = True
 
     Ke = max(3, min(K, 20))
-    for i in range(2):
+    for i in range(4):
         e2e_step(i)
     torch.cuda.synchronize()
-    barrier()
-    t0 = time.perf_counter()
-    for i in range(Ke):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e2e_job, e2e_s = job_throughput(work["tokens"], (time.perf_counter() - t0) / Ke)
+    # three timed windows of Ke steps; the median window is reported, so that
+    # one stall of the host (another process, the clock sampler) does not set it
+    windows = []
+    for w in range(3):
+        barrier()
+        t0 = time.perf_counter()
+        for i in range(Ke):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        windows.append((time.perf_counter() - t0) / Ke)
+    e2e_job, e2e_s = job_throughput(work["tokens"], sorted(windows)[1])
     assert kla.kla_workspace_check(ws, stream) == kla.KLA_OK
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in outs_h[0])
     return dict(value=e2e_job, unit="tokens/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
-                ms_per_step=e2e_s * 1e3, steps=Ke,
+                ms_per_step=e2e_s * 1e3, steps=Ke, windows=3,
                 pipeline=f"{sets} device buffer sets; H2D of step i+1 ({up_streams} copy streams) and D2H "
-                         "of step i-1 overlap step i")
+                         "of step i-1 overlap step i; median of 3 timed windows")
 
 
 def bench_backward(case, K, W, flush, peaks, stream):
