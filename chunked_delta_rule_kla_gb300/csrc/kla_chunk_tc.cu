@@ -1469,7 +1469,8 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
     // it is released early and (with p.early_a) refilled then, two chunks
     // ahead.  Group B: the K tiles and the gate vectors, read until the
     // chunk's S and P W.
-    const uint32_t a_bytes = (SUMMARY ? 0u : 16384u) + (vhalf ? 16384u : 0u) + 16384u + 8192u;
+    // (the [M] half of a summary takes no values: neither V nor T diag(beta))
+    const uint32_t a_bytes = (SUMMARY ? 0u : 16384u) + (vhalf ? 16384u + 8192u : 0u) + 16384u;
     const uint32_t b_bytes = 16384u + 768u;
     constexpr bool feat = FEAT;   // Q and K from the record (same bytes per group)
     const uint32_t rec_bytes = p.rec_bytes ? p.rec_bytes : R::kBytes;
@@ -1507,7 +1508,7 @@ __device__ __forceinline__ void state_cta(const CUtensorMap& tm_q, const CUtenso
             for (int kb = 0; kb < 2; ++kb)
                 bulk_load(st + L::kWQ + kb * 16384 + 8192, rec + R::kBytes + kb * 8192, 8192, full);
         }
-        bulk_load(st + L::kTZ, rec + R::kTb, 8192, full);
+        if (vhalf) bulk_load(st + L::kTZ, rec + R::kTb, 8192, full);
     };
     // The start state (fp32 [DK][dv], 64 KB) comes in through stage 1 with a
     // bulk copy: plain loads of it by the state warps were limited by the
