@@ -231,7 +231,8 @@ kla_status kla_chunk_bwd(const void* q, const void* k, const void* v, const floa
     float* scratch = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kla::kErrorRecordBytes);
     return to_status(kla::launch_chunk_bwd(q, k, v, g, eta, eps, h0, grad_o, grad_hT, grad_q, grad_k,
                                            grad_v, grad_g, grad_eta, grad_h0, B, T, H, dk, dv,
-                                           io == KLA_IO_BF16, beta == KLA_BETA_DIRECT, scratch, st));
+                                           io == KLA_IO_BF16, beta == KLA_BETA_DIRECT, scratch,
+                                           static_cast<kla::DeviceErrorRecord*>(workspace), st));
 }
 
 int kla_loglinear_num_levels(int T) {

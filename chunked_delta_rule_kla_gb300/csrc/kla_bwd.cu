@@ -41,6 +41,7 @@
 // (hi*hi + hi*lo + lo*hi), which keeps fp32-level accuracy.
 #include "kla_internal.cuh"
 #include "kla_tile.cuh"
+#include "tc_common.cuh"
 
 #include <algorithm>
 
@@ -76,6 +77,7 @@ struct BwdParams {
     float* wbuf;     // [B*H][nchunks][64][dv]   W of each chunk
     float* dstates;  // [B*H][nchunks][dk][dv]   dS1 of each chunk
     float* dwbuf;    // [B*H][nchunks][64][dv]   dW of each chunk
+    DeviceErrorRecord* err;  // where a bounded wait that gives up is recorded (nullable)
 };
 
 __device__ __forceinline__ size_t tok_index(const BwdParams& p, int bh, int c, int r) {
@@ -390,6 +392,288 @@ __global__ void __launch_bounds__(512) bwd_carry_kernel(BwdParams p) {
         }
 }
 
+// ------------------------------------------------------- carries (tcgen05)
+// bf16 I/O with d_k = d_v = 128: the same two carries on the tensor cores
+// (tcgen05, accumulators in tensor memory).  One CTA per (head, direction):
+// TMEM lane j holds column j of the state (S^T, or dS^T in reverse); its
+// fp32 master stays in registers of the eight state warps (warp w: lanes
+// 32 (w % 4).., state rows 64 (w / 4)..), and a bf16 copy written to TMEM is
+// the A operand of the first product:
+//   forward:  D = S0^T Wk^T,  W = U - D^T,  S_acc = Wt^T K with Wt = diag(exp(gam_C - gam)) W,
+//             S^T <- Gam_C S^T + S_acc
+//   reverse:  D = dS1^T K^T,  dW = diag(exp(gam_C - gam)) D^T + P^T dO,  S_acc = dW^T Wk,
+//             dS^T <- Gam_C dS^T + L^T - S_acc
+// Operands are bf16, accumulation fp32.  Warps 8..11 stage the next chunk
+// while the state warps run this one: Wk (from the fp32 record) and K as
+// 128-byte-swizzled bf16 tiles and the decay factors, with U (or P^T dO)
+// and, in reverse, L brought in by bulk copies.
+namespace bct {
+constexpr int kThreads = 384;
+constexpr int kStateThreads = 256;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t TC_D = 0;     // D (fp32, 64 columns); shares columns with S_acc
+constexpr uint32_t TC_SA = 0;    // S_acc (fp32, 128 columns)
+constexpr uint32_t TC_WB = 128;  // Wt^T or dW^T (bf16 pairs, 32 columns)
+constexpr uint32_t TC_SB = 160;  // S^T or dS^T (bf16 pairs, 64 columns)
+// shared memory: two stages, then L (reverse), then the barriers
+constexpr uint32_t kWk = 0;          // Wk, [64 tok][128] bf16 as two 64-column boxes
+constexpr uint32_t kK = 16384;       // K, same layout
+constexpr uint32_t kU = 32768;       // U or P^T dO, fp32 [64][128]
+constexpr uint32_t kSc = 65536;      // exp(gam_C - gam_r) [64], then gam_C
+constexpr uint32_t kStage = 66560;
+constexpr uint32_t kL = 2 * kStage;  // L, fp32 [128][128]
+constexpr uint32_t kBars = kL + 65536;
+constexpr size_t kSmem = kBars + 128 + 1024;
+enum { BAR_W = 0, BAR_S, BAR_LD0, BAR_LD1, BAR_L, BAR_COUNT };
+enum : unsigned { kWhereW = 40, kWhereS, kWhereLd, kWhereL };
+constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s per wait
+constexpr int kBarState = 1;                      // named barrier of the state warps
+}  // namespace bct
+
+__device__ __forceinline__ void bct_bar(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// true on every thread of named barrier `id` if `pred` holds on any of them
+__device__ __forceinline__ bool bct_bar_or(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ uint32_t bct_pack2(float a, float b) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&p);
+}
+
+__global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParams p) {
+    using namespace bct;
+    extern __shared__ uint8_t smraw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    constexpr int D = 128;
+    const int heads = p.B * p.H;
+    const bool rev = (int)blockIdx.x >= heads;
+    const int bh = rev ? (int)blockIdx.x - heads : (int)blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = p.nchunks;
+    const RecLayout L(D, D);
+    const size_t SS = (size_t)D * D, WS = (size_t)C * D;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBars + 64);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kBars + 72);
+    auto chunk_of = [&](int it) { return rev ? n - 1 - it : it; };
+    auto record = [&](int c) { return p.rec + ((size_t)bh * n + c) * L.floats; };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < BAR_COUNT; ++i) tc::mbar_init(&bars[i], 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    __syncthreads();   // the barriers are initialised before the first copy
+
+    // Loader warps: the record tiles of chunk `it` into stage it % 2.
+    const int lt = (int)threadIdx.x - kStateThreads;
+    auto stage_chunk = [&](int it) {
+        const int c = chunk_of(it), s = it & 1;
+        uint8_t* st = sm + s * kStage;
+        const float* rec = record(c);
+        if (lt == 0) {
+            tc::mbar_arrive_expect_tx(&bars[BAR_LD0 + s], (uint32_t)(sizeof(float) * C * D));
+            tc::bulk_load(st + kU, rec + (rev ? L.PdO : L.U), (uint32_t)(sizeof(float) * C * D),
+                          &bars[BAR_LD0 + s]);
+        }
+        const int nvalid = chunk_valid(p, c);
+        const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(p.k) + tok_index(p, bh, c, 0) * D;
+        const size_t ldk = (size_t)p.H * D;
+        float4 w[16];
+        uint4 kv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int unit = lt + 128 * u, r = unit >> 4, c8 = unit & 15;
+            const float4* src = reinterpret_cast<const float4*>(rec + L.Wk + r * D + 8 * c8);
+            w[2 * u] = __ldg(src);
+            w[2 * u + 1] = __ldg(src + 1);
+            kv[u] = r < nvalid ? __ldg(reinterpret_cast<const uint4*>(K + r * ldk + 8 * c8))
+                               : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int unit = lt + 128 * u, r = unit >> 4, c8 = unit & 15;
+            const uint32_t off = (uint32_t)(c8 >> 3) * 8192u + tc::sw128_offset(r, (c8 & 7) * 8);
+            uint4 pk;
+            pk.x = bct_pack2(w[2 * u].x, w[2 * u].y);
+            pk.y = bct_pack2(w[2 * u].z, w[2 * u].w);
+            pk.z = bct_pack2(w[2 * u + 1].x, w[2 * u + 1].y);
+            pk.w = bct_pack2(w[2 * u + 1].z, w[2 * u + 1].w);
+            *reinterpret_cast<uint4*>(st + kWk + off) = pk;
+            *reinterpret_cast<uint4*>(st + kK + off) = kv[u];
+        }
+        if (lt < C) {
+            float* sc = reinterpret_cast<float*>(st + kSc);
+            const float gC = __ldg(rec + L.gamma + C - 1);
+            sc[lt] = __expf(gC - __ldg(rec + L.gamma + lt));
+            if (lt == 0) sc[C] = gC;
+        }
+        tc::fence_proxy_async_smem();   // the tiles are read by the tensor cores
+    };
+
+    // State warps: the master state and its first bf16 copy.
+    const int hs = (warp >> 2) & 1, qd = warp & 3;
+    const int j = 32 * qd + lane;                        // state column (d_v index)
+    const uint32_t lf = (uint32_t)(32 * qd) << 16;       // TMEM lane field
+    float m[64];                                         // S[64 hs + i][j] (or dS)
+    if (warp < 8) {
+        const float* init = rev ? p.dhT : p.h0;
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+            m[i] = init ? __ldg(init + (size_t)bh * SS + (size_t)(64 * hs + i) * D + j) : 0.f;
+    } else {
+        stage_chunk(0);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (warp < 8) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = bct_pack2(m[32 * hh + 2 * i], m[32 * hh + 2 * i + 1]);
+            tc::tmem_st_32x32b_x16u(tmem + lf + TC_SB + 32 * hs + 16 * hh, pk);
+        }
+        tc::tmem_st_wait();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+
+    // one bounded mbarrier wait with an outcome shared by the state warps
+    auto group_wait = [&](int slot, uint32_t parity, unsigned where, int c, bool ok) {
+        bool good = ok;
+        if (good && !tc::mbar_wait(&bars[slot], parity, kTimeoutNs)) {
+            record_error(p.err, where, (unsigned)c);
+            *abort_flag = 1;
+            good = false;
+        }
+        return !bct_bar_or(kBarState, kStateThreads, !good);
+    };
+    constexpr uint32_t id1 = tc::idesc_bf16(128, 64, false, false);   // [128 x 64] = A(TMEM) B^T, B K-major
+    constexpr uint32_t id2 = tc::idesc_bf16(128, 128, false, true);   // [128 x 128] = A(TMEM) B, B N-major
+    int it = 0;
+    for (; it < n; ++it) {
+        const int c = chunk_of(it), s = it & 1;
+        uint8_t* st = sm + s * kStage;
+        const size_t item = (size_t)bh * n + c;
+        if (warp < 8) {
+            tc::tc_fence_after();
+            if (threadIdx.x == 0) {
+                const uint32_t bt = tc::smem_u32(st + (rev ? kK : kWk));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tc::mma_bf16_ta(tmem + TC_D, tmem + TC_SB + kk * 8,
+                                    tc::sdesc_sw128(bt + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id1,
+                                    kk > 0 ? 1u : 0u);
+                tc::mma_commit(&bars[BAR_W]);
+            }
+            // keep the state this chunk starts from (S0, or dS1 in reverse)
+            {
+                float* ks = (rev ? p.dstates : p.states) + item * SS + (size_t)(64 * hs) * D + j;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) ks[(size_t)i * D] = m[i];
+            }
+            bool ok = group_wait(BAR_W, it & 1, kWhereW, c, true);
+            ok = group_wait(BAR_LD0 + s, (it >> 1) & 1, kWhereLd, c, ok);
+            tc::tc_fence_after();
+            const float* sc = reinterpret_cast<const float*>(st + kSc);
+            if (ok) {
+                float v[32];
+                tc::tmem_ld_32x32b_x32(tmem + lf + TC_D + 32 * hs, v);
+                tc::tmem_ld_wait();
+                const float* sU = reinterpret_cast<const float*>(st + kU);
+                float* kw = (rev ? p.dwbuf : p.wbuf) + item * WS + j;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int r = 32 * hs + i;
+                    const float w = rev ? fmaf(sc[r], v[i], sU[r * D + j]) : sU[r * D + j] - v[i];
+                    kw[(size_t)r * D] = w;
+                    v[i] = rev ? w : sc[r] * w;
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pk[i] = bct_pack2(v[2 * i], v[2 * i + 1]);
+                tc::tmem_st_32x32b_x16u(tmem + lf + TC_WB + 16 * hs, pk);
+                tc::tmem_st_wait();
+            }
+            tc::tc_fence_before();
+            bct_bar(kBarState, kStateThreads);
+            tc::tc_fence_after();
+            if (threadIdx.x == 0 && ok) {
+                const uint32_t bt = tc::smem_u32(st + (rev ? kWk : kK));
+#pragma unroll
+                for (int kk = 0; kk < C / 16; ++kk)
+                    tc::mma_bf16_ta(tmem + TC_SA, tmem + TC_WB + kk * 8,
+                                    tc::sdesc_sw128(bt + kk * 2048, 8192, 1024), id2, kk > 0 ? 1u : 0u);
+                tc::mma_commit(&bars[BAR_S]);
+            }
+            ok = group_wait(BAR_S, it & 1, kWhereS, c, ok);
+            if (rev) ok = group_wait(BAR_L, it & 1, kWhereL, c, ok);
+            tc::tc_fence_after();
+            if (ok) {
+                const float GC = __expf(sc[C]);
+                const float* sL = reinterpret_cast<const float*>(sm + kL) + (size_t)(64 * hs) * D + j;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float a[32];
+                    tc::tmem_ld_32x32b_x32(tmem + lf + TC_SA + 64 * hs + 32 * hh, a);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int x = 32 * hh + i;
+                        m[x] = rev ? fmaf(GC, m[x], sL[x * D] - a[i]) : fmaf(GC, m[x], a[i]);
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pk[i] = bct_pack2(m[32 * hh + 2 * i], m[32 * hh + 2 * i + 1]);
+                    tc::tmem_st_32x32b_x16u(tmem + lf + TC_SB + 32 * hs + 16 * hh, pk);
+                }
+                tc::tmem_st_wait();
+            }
+            tc::tc_fence_before();
+        } else {
+            if (rev && lt == 0) {
+                const float* rec = record(c);
+                tc::mbar_arrive_expect_tx(&bars[BAR_L], (uint32_t)(sizeof(float) * SS));
+                tc::bulk_load(sm + kL, rec + L.L, (uint32_t)(sizeof(float) * SS), &bars[BAR_L]);
+                if (it + 1 < n) prefetch_l2(record(chunk_of(it + 1)) + L.L, (uint32_t)(sizeof(float) * SS));
+            }
+            if (it + 1 < n) stage_chunk(it + 1);
+        }
+        __syncthreads();
+        if (*abort_flag) break;
+    }
+    if (it < n && lt == 0) {
+        // given up: let the bulk copies still in flight land before the CTA leaves
+        tc::mbar_wait(&bars[BAR_LD0 + (it & 1)], (it >> 1) & 1, kTimeoutNs);
+        if (it + 1 < n) tc::mbar_wait(&bars[BAR_LD0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1, kTimeoutNs);
+        if (rev) tc::mbar_wait(&bars[BAR_L], it & 1, kTimeoutNs);
+    }
+    if (it == n && rev && p.dh0 && warp < 8) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) p.dh0[(size_t)bh * SS + (size_t)(64 * hs + i) * D + j] = m[i];
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
 // ------------------------------------------------------------ gradients
 
 // Shared memory of the gradient kernel (floats, in order): dX, E, dQ, dK
@@ -683,7 +967,14 @@ cudaError_t launch_all(const BwdParams& p, cudaStream_t st) {
     const dim3 items(p.nchunks, p.B * p.H);
     bwd_prep_kernel<TIO, PRECISE><<<items, 256, s_prep, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_carry_kernel<TIO, PRECISE><<<2 * p.B * p.H, 512, s_carry, st>>>(p);
+    if (sizeof(TIO) == 2 && p.DK == 128 && p.DV == 128) {
+        if ((e = cudaFuncSetAttribute(bwd_carry_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)bct::kSmem)) != cudaSuccess)
+            return e;
+        bwd_carry_tc_kernel<<<2 * p.B * p.H, bct::kThreads, bct::kSmem, st>>>(p);
+    } else {
+        bwd_carry_kernel<TIO, PRECISE><<<2 * p.B * p.H, 512, s_carry, st>>>(p);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bwd_grad_kernel<TIO, PRECISE><<<items, 512, s_grad, st>>>(p);
     return cudaGetLastError();
@@ -702,7 +993,8 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
                              const float* eta, float eps, const float* h0, const void* dout,
                              const float* dhT, void* dq, void* dk, void* dv, float* dg, float* deta,
                              float* dh0, int B, int T, int H, int DK, int DV, bool bf16,
-                             bool beta_direct, float* scratch, cudaStream_t stream) {
+                             bool beta_direct, float* scratch, DeviceErrorRecord* err,
+                             cudaStream_t stream) {
     BwdParams p;
     p.q = q; p.k = k; p.v = v; p.dout = dout;
     p.g = g; p.eta = eta; p.h0 = h0; p.dhT = dhT;
@@ -717,6 +1009,7 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
     p.wbuf = p.states + items * DK * DV;
     p.dstates = p.wbuf + items * C * DV;
     p.dwbuf = p.dstates + items * DK * DV;
+    p.err = err;
     if (bf16) return launch_all<__nv_bfloat16, false>(p, stream);
     return launch_all<float, true>(p, stream);
 }

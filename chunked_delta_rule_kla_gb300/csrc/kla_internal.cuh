@@ -176,6 +176,7 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
                              const float* eta, float eps, const float* h0, const void* dout,
                              const float* dhT, void* dq, void* dk, void* dv, float* dg, float* deta,
                              float* dh0, int B, int T, int H, int DK, int DV, bool bf16,
-                             bool beta_direct, float* scratch, cudaStream_t stream);
+                             bool beta_direct, float* scratch, DeviceErrorRecord* err,
+                             cudaStream_t stream);
 
 }  // namespace kla
