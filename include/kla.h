@@ -194,8 +194,12 @@ KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
  *  grad_h0 : fp32 [B, H, dk, dv], or NULL when not wanted
  *  chunk = 64; dk, dv : 64 or 128 each; B*H <= 65535.
  *
- * Products are tf32 tensor-core tiles with fp32 accumulation; with fp32 I/O
- * each product is split into three tf32 products (fp32-level accuracy).
+ * With bf16 I/O and dk = dv = 128 the two state carries are bf16 tcgen05
+ * products with fp32 accumulation and an fp32 master state; their waits are
+ * bounded (1 s) and a wait that runs out is recorded in the workspace
+ * (kla_workspace_check returns KLA_ERR_DEVICE_TIMEOUT).  Other products are
+ * tf32 tensor-core tiles with fp32 accumulation; with fp32 I/O each is split
+ * into three tf32 products (fp32-level accuracy).
  * The workspace (kla_chunk_bwd_workspace_bytes, 256-byte aligned, caller
  * owned) holds per-chunk records, every chunk's start state and state
  * gradient: about 373 KB per (batch, head, chunk) at dk = dv = 128.  Errors
