@@ -78,6 +78,7 @@ struct BwdParams {
     float* dstates;  // [B*H][nchunks][dk][dv]   dS1 of each chunk
     float* dwbuf;    // [B*H][nchunks][64][dv]   dW of each chunk
     DeviceErrorRecord* err;  // where a bounded wait that gives up is recorded (nullable)
+    int tc_carry;            // the tensor-core carries run: the records need no U and no L
 };
 
 __device__ __forceinline__ size_t tok_index(const BwdParams& p, int bh, int c, int r) {
@@ -190,11 +191,13 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdParams p) {
     // Wk = T diag(beta Gam) K
     mm<PRECISE>(C, DK, C, opnd<false>(sT, kLdCC), opnd<true>(b2, kLdCC), rec + L.Wk, DK, 1.f, false);
     __syncthreads();
-    // U = T diag(beta) V
-    stage_cols<TIO>(b2, kLdCC, V, ldv, C, DV, nvalid, sbeta);
-    __syncthreads();
-    mm<PRECISE>(C, DV, C, opnd<false>(sT, kLdCC), opnd<true>(b2, kLdCC), rec + L.U, DV, 1.f, false);
-    __syncthreads();
+    // U = T diag(beta) V (the tensor-core carry forms U itself)
+    if (!p.tc_carry) {
+        stage_cols<TIO>(b2, kLdCC, V, ldv, C, DV, nvalid, sbeta);
+        __syncthreads();
+        mm<PRECISE>(C, DV, C, opnd<false>(sT, kLdCC), opnd<true>(b2, kLdCC), rec + L.U, DV, 1.f, false);
+        __syncthreads();
+    }
     // P^T = upper(D^T o K Q^T), Q row-major in b2
     stage_rows<TIO>(b2, ldR, Q, ldk, C, DK, nvalid, nullptr);
     __syncthreads();
@@ -204,16 +207,18 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdParams p) {
         const int s2 = i / C, r = i % C;
         sG[s2 * kLdCC + r] = s2 <= r ? __expf(sgam[r] - sgam[s2]) * sG[s2 * kLdCC + r] : 0.f;
     }
-    for (int i = tid; i < C * DK; i += nt) {     // (Gam Q)^T over K (K is no longer needed)
-        const int r = i % C, j = i / C;
-        b1[j * kLdCC + r] = __expf(sgam[r]) * b2[r * ldR + j];
-    }
+    if (!p.tc_carry)
+        for (int i = tid; i < C * DK; i += nt) {     // (Gam Q)^T over K (K is no longer needed)
+            const int r = i % C, j = i / C;
+            b1[j * kLdCC + r] = __expf(sgam[r]) * b2[r * ldR + j];
+        }
     __syncthreads();
     stage_cols<TIO>(b2, kLdCC, dO, ldv, C, DV, nvalid, nullptr);   // dO^T
     __syncthreads();
-    // P^T dO and L = (Gam Q)^T dO
+    // P^T dO and L = (Gam Q)^T dO (the tensor-core carry forms L itself)
     mm<PRECISE>(C, DV, C, opnd<false>(sG, kLdCC), opnd<true>(b2, kLdCC), rec + L.PdO, DV, 1.f, false);
-    mm<PRECISE>(DK, DV, C, opnd<false>(b1, kLdCC), opnd<true>(b2, kLdCC), rec + L.L, DV, 1.f, false);
+    if (!p.tc_carry)
+        mm<PRECISE>(DK, DV, C, opnd<false>(b1, kLdCC), opnd<true>(b2, kLdCC), rec + L.L, DV, 1.f, false);
     // vectors and T
     for (int i = tid; i < C; i += nt) {
         rec[L.gamma + i] = sgam[i];
@@ -394,38 +399,41 @@ __global__ void __launch_bounds__(512) bwd_carry_kernel(BwdParams p) {
 
 // ------------------------------------------------------- carries (tcgen05)
 // bf16 I/O with d_k = d_v = 128: the same two carries on the tensor cores
-// (tcgen05, accumulators in tensor memory).  One CTA per (head, direction):
-// TMEM lane j holds column j of the state (S^T, or dS^T in reverse); its
-// fp32 master stays in registers of the eight state warps (warp w: lanes
-// 32 (w % 4).., state rows 64 (w / 4)..), and a bf16 copy written to TMEM is
-// the A operand of the first product:
-//   forward:  D = S0^T Wk^T,  W = U - D^T,  S_acc = Wt^T K with Wt = diag(exp(gam_C - gam)) W,
-//             S^T <- Gam_C S^T + S_acc
-//   reverse:  D = dS1^T K^T,  dW = diag(exp(gam_C - gam)) D^T + P^T dO,  S_acc = dW^T Wk,
-//             dS^T <- Gam_C dS^T + L^T - S_acc
+// (tcgen05, accumulators in tensor memory), which also form the records' U
+// and L themselves (the prep leaves both out).  One CTA per (head,
+// direction): TMEM lane j holds column j of the state (S^T, or dS^T in
+// reverse); its fp32 master stays in registers of the eight state warps
+// (warp w: lanes 32 (w % 4).., state rows 64 (w / 4)..), and a bf16 copy
+// written to TMEM is the A operand of the chain's first product:
+//   forward:  D = -V^T Tb^T + S0^T Wk^T = -W^T     (Tb = T diag(beta), so V^T Tb^T = U^T)
+//             S_acc = Wt^T K,  Wt = diag(exp(gam_C - gam)) W
+//   reverse:  D = dS1^T K^T,  dW = diag(exp(gam_C - gam)) D^T + P^T dO
+//             S_acc = dO^T diag(Gam) Q - dW^T Wk     (L^T - dW^T Wk)
+//   S^T <- Gam_C S^T + S_acc
 // Operands are bf16, accumulation fp32.  Warps 8..11 stage the next chunk
-// while the state warps run this one: Wk (from the fp32 record) and K as
-// 128-byte-swizzled bf16 tiles and the decay factors, with U (or P^T dO)
-// and, in reverse, L brought in by bulk copies.
+// while the state warps run this one, as 128-byte-swizzled bf16 tiles: Wk
+// (from the fp32 record) and K; forward V and Tb; reverse dO and diag(Gam) Q;
+// the decay factors; and in reverse P^T dO by a bulk copy.
 namespace bct {
 constexpr int kThreads = 384;
 constexpr int kStateThreads = 256;
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t TC_D = 0;     // D (fp32, 64 columns); shares columns with S_acc
-constexpr uint32_t TC_SA = 0;    // S_acc (fp32, 128 columns)
-constexpr uint32_t TC_WB = 128;  // Wt^T or dW^T (bf16 pairs, 32 columns)
-constexpr uint32_t TC_SB = 160;  // S^T or dS^T (bf16 pairs, 64 columns)
-// shared memory: two stages, then L (reverse), then the barriers
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t TC_D = 0;     // D (fp32, 64 columns)
+constexpr uint32_t TC_SA = 128;  // S_acc (fp32, 128 columns)
+constexpr uint32_t TC_WB = 256;  // Wt^T or -dW^T (bf16 pairs, 32 columns)
+constexpr uint32_t TC_SB = 288;  // S^T or dS^T (bf16 pairs, 64 columns)
+// shared memory: two stages, then the barriers
 constexpr uint32_t kWk = 0;          // Wk, [64 tok][128] bf16 as two 64-column boxes
 constexpr uint32_t kK = 16384;       // K, same layout
-constexpr uint32_t kU = 32768;       // U or P^T dO, fp32 [64][128]
-constexpr uint32_t kSc = 65536;      // exp(gam_C - gam_r) [64], then gam_C
-constexpr uint32_t kStage = 66560;
-constexpr uint32_t kL = 2 * kStage;  // L, fp32 [128][128]
-constexpr uint32_t kBars = kL + 65536;
+constexpr uint32_t kX1 = 32768;      // forward V, reverse dO: same layout
+constexpr uint32_t kX2 = 49152;      // forward Tb [64][64] (one box), reverse diag(Gam) Q [64][128]
+constexpr uint32_t kU = 65536;       // reverse P^T dO, fp32 [64][128]
+constexpr uint32_t kSc = 98304;      // exp(gam_C - gam_r) [64], then gam_C
+constexpr uint32_t kStage = 99328;
+constexpr uint32_t kBars = 2 * kStage;
 constexpr size_t kSmem = kBars + 128 + 1024;
-enum { BAR_W = 0, BAR_S, BAR_LD0, BAR_LD1, BAR_L, BAR_COUNT };
-enum : unsigned { kWhereW = 40, kWhereS, kWhereLd, kWhereL };
+enum { BAR_W = 0, BAR_S, BAR_LD0, BAR_LD1, BAR_COUNT };
+enum : unsigned { kWhereW = 40, kWhereS, kWhereLd };
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s per wait
 constexpr int kBarState = 1;                      // named barrier of the state warps
 }  // namespace bct
@@ -447,6 +455,11 @@ __device__ __forceinline__ bool bct_bar_or(int id, int n, bool pred) {
 __device__ __forceinline__ uint32_t bct_pack2(float a, float b) {
     __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&p);
+}
+// byte offset of the 16-byte chunk (row r, columns 8 c8 .. 8 c8 + 7) in a
+// [64][128] bf16 tile stored as two swizzled 64-column boxes
+__device__ __forceinline__ uint32_t bct_off(int r, int c8) {
+    return (uint32_t)(c8 >> 3) * 8192u + tc::sw128_offset(r, (c8 & 7) * 8);
 }
 
 __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParams p) {
@@ -478,48 +491,100 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
     }
     __syncthreads();   // the barriers are initialised before the first copy
 
-    // Loader warps: the record tiles of chunk `it` into stage it % 2.
+    // Loader warps: the tiles of chunk `it` into stage it % 2.
     const int lt = (int)threadIdx.x - kStateThreads;
     auto stage_chunk = [&](int it) {
         const int c = chunk_of(it), s = it & 1;
         uint8_t* st = sm + s * kStage;
         const float* rec = record(c);
-        if (lt == 0) {
+        if (rev && lt == 0) {
             tc::mbar_arrive_expect_tx(&bars[BAR_LD0 + s], (uint32_t)(sizeof(float) * C * D));
-            tc::bulk_load(st + kU, rec + (rev ? L.PdO : L.U), (uint32_t)(sizeof(float) * C * D),
-                          &bars[BAR_LD0 + s]);
+            tc::bulk_load(st + kU, rec + L.PdO, (uint32_t)(sizeof(float) * C * D), &bars[BAR_LD0 + s]);
         }
         const int nvalid = chunk_valid(p, c);
-        const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(p.k) + tok_index(p, bh, c, 0) * D;
-        const size_t ldk = (size_t)p.H * D;
-        float4 w[16];
-        uint4 kv[8];
+        const size_t t0 = tok_index(p, bh, c, 0);
+        const size_t ld = (size_t)p.H * D;
+        const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(p.k) + t0 * D;
+        const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(rev ? p.dout : p.v) + t0 * D;
+        {   // Wk (fp32 -> bf16), K and V or dO (bf16 rows, zero past nvalid)
+            float4 w[16];
+            uint4 kv[8], xv[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int unit = lt + 128 * u, r = unit >> 4, c8 = unit & 15;
-            const float4* src = reinterpret_cast<const float4*>(rec + L.Wk + r * D + 8 * c8);
-            w[2 * u] = __ldg(src);
-            w[2 * u + 1] = __ldg(src + 1);
-            kv[u] = r < nvalid ? __ldg(reinterpret_cast<const uint4*>(K + r * ldk + 8 * c8))
-                               : make_uint4(0u, 0u, 0u, 0u);
-        }
+            for (int u = 0; u < 8; ++u) {
+                const int unit = lt + 128 * u, r = unit >> 4, c8 = unit & 15;
+                const float4* src = reinterpret_cast<const float4*>(rec + L.Wk + r * D + 8 * c8);
+                w[2 * u] = __ldg(src);
+                w[2 * u + 1] = __ldg(src + 1);
+                const bool in = r < nvalid;
+                kv[u] = in ? __ldg(reinterpret_cast<const uint4*>(K + r * ld + 8 * c8)) : make_uint4(0u, 0u, 0u, 0u);
+                xv[u] = in ? __ldg(reinterpret_cast<const uint4*>(X + r * ld + 8 * c8)) : make_uint4(0u, 0u, 0u, 0u);
+            }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int unit = lt + 128 * u, r = unit >> 4, c8 = unit & 15;
-            const uint32_t off = (uint32_t)(c8 >> 3) * 8192u + tc::sw128_offset(r, (c8 & 7) * 8);
-            uint4 pk;
-            pk.x = bct_pack2(w[2 * u].x, w[2 * u].y);
-            pk.y = bct_pack2(w[2 * u].z, w[2 * u].w);
-            pk.z = bct_pack2(w[2 * u + 1].x, w[2 * u + 1].y);
-            pk.w = bct_pack2(w[2 * u + 1].z, w[2 * u + 1].w);
-            *reinterpret_cast<uint4*>(st + kWk + off) = pk;
-            *reinterpret_cast<uint4*>(st + kK + off) = kv[u];
+            for (int u = 0; u < 8; ++u) {
+                const int unit = lt + 128 * u, r = unit >> 4, c8 = unit & 15;
+                const uint32_t off = bct_off(r, c8);
+                uint4 pk;
+                pk.x = bct_pack2(w[2 * u].x, w[2 * u].y);
+                pk.y = bct_pack2(w[2 * u].z, w[2 * u].w);
+                pk.z = bct_pack2(w[2 * u + 1].x, w[2 * u + 1].y);
+                pk.w = bct_pack2(w[2 * u + 1].z, w[2 * u + 1].w);
+                *reinterpret_cast<uint4*>(st + kWk + off) = pk;
+                *reinterpret_cast<uint4*>(st + kK + off) = kv[u];
+                *reinterpret_cast<uint4*>(st + kX1 + off) = xv[u];
+            }
         }
+        float* sc = reinterpret_cast<float*>(st + kSc);
         if (lt < C) {
-            float* sc = reinterpret_cast<float*>(st + kSc);
             const float gC = __ldg(rec + L.gamma + C - 1);
             sc[lt] = __expf(gC - __ldg(rec + L.gamma + lt));
             if (lt == 0) sc[C] = gC;
+        }
+        if (rev) {
+            // diag(Gam) Q, rounded to bf16 once
+            const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(p.q) + t0 * D;
+            uint4 qv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int unit = lt + 128 * u, r = unit >> 4, c8 = unit & 15;
+                qv[u] = r < nvalid ? __ldg(reinterpret_cast<const uint4*>(Q + r * ld + 8 * c8)) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int unit = lt + 128 * u, r = unit >> 4, c8 = unit & 15;
+                const float G = __expf(__ldg(rec + L.gamma + r));
+                const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&qv[u]);
+                uint4 pk;
+                uint32_t* o = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(h[e]);
+                    o[e] = bct_pack2(G * f.x, G * f.y);
+                }
+                *reinterpret_cast<uint4*>(st + kX2 + bct_off(r, c8)) = pk;
+            }
+        } else {
+            // Tb = T diag(beta): 64 x 64, one box
+            float4 tv[8];
+            float bt[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int unit = lt + 128 * u, r = unit >> 3, c8 = unit & 7;
+                const float4* src = reinterpret_cast<const float4*>(rec + L.T + r * C + 8 * c8);
+                tv[2 * u] = __ldg(src);
+                tv[2 * u + 1] = __ldg(src + 1);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) bt[u][e] = __ldg(rec + L.beta + 8 * c8 + e);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int unit = lt + 128 * u, r = unit >> 3, c8 = unit & 7;
+                uint4 pk;
+                pk.x = bct_pack2(tv[2 * u].x * bt[u][0], tv[2 * u].y * bt[u][1]);
+                pk.y = bct_pack2(tv[2 * u].z * bt[u][2], tv[2 * u].w * bt[u][3]);
+                pk.z = bct_pack2(tv[2 * u + 1].x * bt[u][4], tv[2 * u + 1].y * bt[u][5]);
+                pk.w = bct_pack2(tv[2 * u + 1].z * bt[u][6], tv[2 * u + 1].w * bt[u][7]);
+                *reinterpret_cast<uint4*>(st + kX2 + tc::sw128_offset(r, 8 * c8)) = pk;
+            }
         }
         tc::fence_proxy_async_smem();   // the tiles are read by the tensor cores
     };
@@ -564,8 +629,10 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
         }
         return !bct_bar_or(kBarState, kStateThreads, !good);
     };
-    constexpr uint32_t id1 = tc::idesc_bf16(128, 64, false, false);   // [128 x 64] = A(TMEM) B^T, B K-major
-    constexpr uint32_t id2 = tc::idesc_bf16(128, 128, false, true);   // [128 x 128] = A(TMEM) B, B N-major
+    constexpr uint32_t id1 = tc::idesc_bf16(128, 64, false, false);         // A(TMEM) B^T, B K-major
+    constexpr uint32_t id_u = tc::idesc_bf16(128, 64, true, false, true);   // -(V^T Tb^T), A N-major
+    constexpr uint32_t id2 = tc::idesc_bf16(128, 128, false, true);         // A(TMEM) B, B N-major
+    constexpr uint32_t id_l = tc::idesc_bf16(128, 128, true, true);         // dO^T (Gam Q)
     int it = 0;
     for (; it < n; ++it) {
         const int c = chunk_of(it), s = it & 1;
@@ -574,12 +641,24 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
         if (warp < 8) {
             tc::tc_fence_after();
             if (threadIdx.x == 0) {
+                const uint32_t x1 = tc::smem_u32(st + kX1), x2 = tc::smem_u32(st + kX2);
+                if (rev) {
+#pragma unroll
+                    for (int kk = 0; kk < C / 16; ++kk)
+                        tc::mma_bf16(tmem + TC_SA, tc::sdesc_sw128(x1 + kk * 2048, 8192, 1024),
+                                     tc::sdesc_sw128(x2 + kk * 2048, 8192, 1024), id_l, kk > 0 ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < C / 16; ++kk)
+                        tc::mma_bf16(tmem + TC_D, tc::sdesc_sw128(x1 + kk * 2048, 8192, 1024),
+                                     tc::sdesc_sw128(x2 + kk * 32, 16, 1024), id_u, kk > 0 ? 1u : 0u);
+                }
                 const uint32_t bt = tc::smem_u32(st + (rev ? kK : kWk));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     tc::mma_bf16_ta(tmem + TC_D, tmem + TC_SB + kk * 8,
                                     tc::sdesc_sw128(bt + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id1,
-                                    kk > 0 ? 1u : 0u);
+                                    (rev && kk == 0) ? 0u : 1u);
                 tc::mma_commit(&bars[BAR_W]);
             }
             // keep the state this chunk starts from (S0, or dS1 in reverse)
@@ -589,7 +668,7 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
                 for (int i = 0; i < 64; ++i) ks[(size_t)i * D] = m[i];
             }
             bool ok = group_wait(BAR_W, it & 1, kWhereW, c, true);
-            ok = group_wait(BAR_LD0 + s, (it >> 1) & 1, kWhereLd, c, ok);
+            if (rev) ok = group_wait(BAR_LD0 + s, (it >> 1) & 1, kWhereLd, c, ok);
             tc::tc_fence_after();
             const float* sc = reinterpret_cast<const float*>(st + kSc);
             if (ok) {
@@ -601,9 +680,9 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int r = 32 * hs + i;
-                    const float w = rev ? fmaf(sc[r], v[i], sU[r * D + j]) : sU[r * D + j] - v[i];
+                    const float w = rev ? fmaf(sc[r], v[i], sU[r * D + j]) : -v[i];
                     kw[(size_t)r * D] = w;
-                    v[i] = rev ? w : sc[r] * w;
+                    v[i] = rev ? -w : sc[r] * w;
                 }
                 uint32_t pk[16];
 #pragma unroll
@@ -619,25 +698,21 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
 #pragma unroll
                 for (int kk = 0; kk < C / 16; ++kk)
                     tc::mma_bf16_ta(tmem + TC_SA, tmem + TC_WB + kk * 8,
-                                    tc::sdesc_sw128(bt + kk * 2048, 8192, 1024), id2, kk > 0 ? 1u : 0u);
+                                    tc::sdesc_sw128(bt + kk * 2048, 8192, 1024), id2,
+                                    (rev || kk > 0) ? 1u : 0u);
                 tc::mma_commit(&bars[BAR_S]);
             }
             ok = group_wait(BAR_S, it & 1, kWhereS, c, ok);
-            if (rev) ok = group_wait(BAR_L, it & 1, kWhereL, c, ok);
             tc::tc_fence_after();
             if (ok) {
                 const float GC = __expf(sc[C]);
-                const float* sL = reinterpret_cast<const float*>(sm + kL) + (size_t)(64 * hs) * D + j;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     float a[32];
                     tc::tmem_ld_32x32b_x32(tmem + lf + TC_SA + 64 * hs + 32 * hh, a);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int x = 32 * hh + i;
-                        m[x] = rev ? fmaf(GC, m[x], sL[x * D] - a[i]) : fmaf(GC, m[x], a[i]);
-                    }
+                    for (int i = 0; i < 32; ++i) m[32 * hh + i] = fmaf(GC, m[32 * hh + i], a[i]);
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) pk[i] = bct_pack2(m[32 * hh + 2 * i], m[32 * hh + 2 * i + 1]);
@@ -646,23 +721,16 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
                 tc::tmem_st_wait();
             }
             tc::tc_fence_before();
-        } else {
-            if (rev && lt == 0) {
-                const float* rec = record(c);
-                tc::mbar_arrive_expect_tx(&bars[BAR_L], (uint32_t)(sizeof(float) * SS));
-                tc::bulk_load(sm + kL, rec + L.L, (uint32_t)(sizeof(float) * SS), &bars[BAR_L]);
-                if (it + 1 < n) prefetch_l2(record(chunk_of(it + 1)) + L.L, (uint32_t)(sizeof(float) * SS));
-            }
-            if (it + 1 < n) stage_chunk(it + 1);
+        } else if (it + 1 < n) {
+            stage_chunk(it + 1);
         }
         __syncthreads();
         if (*abort_flag) break;
     }
-    if (it < n && lt == 0) {
+    if (it < n && rev && lt == 0) {
         // given up: let the bulk copies still in flight land before the CTA leaves
         tc::mbar_wait(&bars[BAR_LD0 + (it & 1)], (it >> 1) & 1, kTimeoutNs);
         if (it + 1 < n) tc::mbar_wait(&bars[BAR_LD0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1, kTimeoutNs);
-        if (rev) tc::mbar_wait(&bars[BAR_L], it & 1, kTimeoutNs);
     }
     if (it == n && rev && p.dh0 && warp < 8) {
 #pragma unroll
@@ -953,7 +1021,7 @@ size_t grad_smem(int DK, int DV, bool bf16) {
 }
 
 template <typename TIO, bool PRECISE>
-cudaError_t launch_all(const BwdParams& p, cudaStream_t st) {
+cudaError_t launch_all(BwdParams p, cudaStream_t st) {
     const size_t s_prep = prep_smem(p.DK, p.DV), s_carry = carry_smem(p.DK, p.DV);
     const size_t s_grad = grad_smem(p.DK, p.DV, sizeof(TIO) == 2);
     cudaError_t e;
@@ -965,9 +1033,10 @@ cudaError_t launch_all(const BwdParams& p, cudaStream_t st) {
     if ((e = cudaFuncSetAttribute(bwd_grad_kernel<TIO, PRECISE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)s_grad)) != cudaSuccess) return e;
     const dim3 items(p.nchunks, p.B * p.H);
+    p.tc_carry = sizeof(TIO) == 2 && p.DK == 128 && p.DV == 128;
     bwd_prep_kernel<TIO, PRECISE><<<items, 256, s_prep, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (sizeof(TIO) == 2 && p.DK == 128 && p.DV == 128) {
+    if (p.tc_carry) {
         if ((e = cudaFuncSetAttribute(bwd_carry_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)bct::kSmem)) != cudaSuccess)
             return e;
@@ -1010,6 +1079,7 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
     p.dstates = p.wbuf + items * C * DV;
     p.dwbuf = p.dstates + items * DK * DV;
     p.err = err;
+    p.tc_carry = 0;
     if (bf16) return launch_all<__nv_bfloat16, false>(p, stream);
     return launch_all<float, true>(p, stream);
 }
