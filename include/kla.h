@@ -194,7 +194,8 @@ KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
  *  grad_h0 : fp32 [B, H, dk, dv], or NULL when not wanted
  *  chunk = 64; dk, dv : 64 or 128 each; B*H <= 65535.
  *
- * With bf16 I/O and dk = dv = 128 the two state carries are bf16 tcgen05
+ * With bf16 I/O and dk = dv = 128 the two state carries (and the per-chunk
+ * U = T diag(beta) V and L = (diag(Gam) Q)^T dO they use) are bf16 tcgen05
  * products with fp32 accumulation and an fp32 master state; their waits are
  * bounded (1 s) and a wait that runs out is recorded in the workspace
  * (kla_workspace_check returns KLA_ERR_DEVICE_TIMEOUT).  Other products are
