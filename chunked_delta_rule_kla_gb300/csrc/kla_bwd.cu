@@ -742,6 +742,579 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
     if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------- gradients (tcgen05)
+// bf16 I/O with d_k = d_v = 128: the gradient kernel's fifteen products on
+// the tensor cores, accumulators in TMEM, operands as 128-byte-swizzled bf16
+// tiles.  Two 64-row operands that multiply the same B are stacked into one
+// M = 128 product: [Q ; K] K^T = [P' ; G], [dO ; dX] S0^T = [X1 ; Y1],
+// [dO ; dX] W^T = [dP ; -dA].  Phases (one CTA per chunk and head):
+//   1  dX = T^T dW,  [P' ; G],  E1 = K S0,  Z1 = W dS1^T;  T, dW and S0 enter
+//      dX and E1 as bf16 pairs (hi + lo: hi lo, lo hi and hi hi products for dX),
+//      so that dX and the residual e keep fp32-level accuracy
+//   2  dX -> dv and the [dO ; dX] tile;  P = D o P' (s <= r) and At = D o G
+//      (s < r) kept by the threads that will hold dP and dA;  diag(Gam) E1 kept
+//   3  [X1 ; Y1],  [dP ; -dA],  E2 = At W
+//   4  e = V - diag(Gam) E1 - E2 and dbeta;  the dgamma terms;  diag(eC) Z1 kept;
+//      dP o D and F = diag(beta)(dA o D)
+//   5  X2 = (dP o D) K;  Z5 = (dP o D)^T Q + F K + F^T K
+//   6  dq = diag(Gam) X1 + X2,  dk = -diag(Gam beta) Y1 + diag(eC) Z1 + Z5 + (beta chain) k
+// (eC_r = exp(gam_C - gam_r), D_rs = exp(gam_r - gam_s).)
+namespace bgt {
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns
+constexpr uint32_t TD_X = 0;      // phase 1: dX (M=64, N=128);  phase 3: [X1 ; Y1] (M=128, N=128)
+constexpr uint32_t TD_PG = 128;   // phase 1: [P' ; G] (M=128, N=64);  phase 3: [dP ; -dA]
+constexpr uint32_t TD_E = 192;    // E1, then E2 (M=64, N=128);  phase 5: X2
+constexpr uint32_t TD_Z = 320;    // Z1, then Z5 (M=64, N=128)
+// shared memory
+constexpr uint32_t kKQ = 0;         // [Q box b | K box b] at 16384 b  (A = [Q ; K], B = K)
+constexpr uint32_t kOX = 32768;     // [dO box b | dX box b] at kOX + 16384 b (phase 1: dW - bf16(dW) in the dX boxes)
+constexpr uint32_t kS0 = 65536;     // S0 [128 a][128 j], box b = columns 64 b.. (16 KB each)
+constexpr uint32_t kW = 98304;      // W [64 s][128 j], boxes 8 KB apart
+constexpr uint32_t kR1 = 114688;    // phase 1: dS1 like S0;  then dX (fp32, per thread);  phase 6: X2^T
+constexpr uint32_t kR2 = 147456;    // phase 1: S0 - bf16(S0) like S0;  then diag(Gam) E1, diag(eC) Z1 (per thread);  phase 6: Z^T
+constexpr uint32_t kR3 = 180224;    // phase 1: dW (16 KB), T [64 s][64 r] at +16384;  then At, dP o D, F
+constexpr uint32_t kTlo = 204800;   // phase 1: T - bf16(T), like T
+constexpr uint32_t kVec = 212992;   // gam, Gam, eC, beta, kk, dbeta, dgamma (float[64] each), misc
+constexpr uint32_t kBars = kVec + 8 * 256;
+constexpr size_t kSmem = kBars + 64 + 1024;
+constexpr uint64_t kTimeoutNs = 1000000000ull;
+enum : unsigned { kWhere1 = 48, kWhere3, kWhere5 };
+}  // namespace bgt
+
+// 8 fp32 -> one 16-byte chunk of bf16
+__device__ __forceinline__ uint4 bgt_pack8(const float* x) {
+    uint4 pk;
+    pk.x = bct_pack2(x[0], x[1]);
+    pk.y = bct_pack2(x[2], x[3]);
+    pk.z = bct_pack2(x[4], x[5]);
+    pk.w = bct_pack2(x[6], x[7]);
+    return pk;
+}
+__device__ __forceinline__ void bgt_unpack8(uint4 v, float* x) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+    }
+}
+// Sum over the warp's lanes of column c of x[32], delivered to lane c.
+__device__ __forceinline__ float bgt_col_sums(float (&x)[32], int lane) {
+#pragma unroll
+    for (int st = 0; st < 5; ++st) {
+        const int off = 16 >> st, n = 32 >> st;
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int k = 0; k < n / 2; ++k) {
+            const float send = upper ? x[k] : x[k + n / 2];
+            const float keep = upper ? x[k + n / 2] : x[k];
+            x[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    return x[0];
+}
+
+__global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams p) {
+    using namespace bgt;
+    extern __shared__ uint8_t smraw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    constexpr int D = 128;
+    const int c = blockIdx.x, bh = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, hh = warp >> 2;                  // TMEM lane quadrant, column half
+    const uint32_t lf = (uint32_t)(32 * q4) << 16;
+    const int r64 = 16 * q4 + lane;                           // row of an M = 64 accumulator (lane < 16)
+    const bool m64 = lane < 16;
+    const int rr = (32 * q4 + lane) & 63;                     // row of an M = 128 accumulator's half
+    const bool top = q4 < 2;                                  // first operand of the stacked pair
+    const int nvalid = chunk_valid(p, c);
+    const RecLayout L(D, D);
+    const size_t item = (size_t)bh * p.nchunks + c;
+    const float* rec = p.rec + item * L.floats;
+    const size_t SS = (size_t)D * D, WS = (size_t)C * D;
+    const float* S0 = p.states + item * SS;
+    const float* dS1 = p.dstates + item * SS;
+    const float* W = p.wbuf + item * WS;
+    const float* dW = p.dwbuf + item * WS;
+    const size_t t0 = tok_index(p, bh, c, 0);
+    const size_t ld = (size_t)p.H * D;
+    float* vgam = reinterpret_cast<float*>(sm + kVec);
+    float* vG = vgam + C;       // Gam
+    float* veC = vG + C;        // exp(gam_C - gam)
+    float* vbeta = veC + C;
+    float* vkk = vbeta + C;
+    float* vdb = vkk + C;       // dbeta
+    float* vdg = vdb + C;       // dgamma
+    float* vmisc = vdg + C;     // [0] the dgamma total added at the chunk's last token
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBars + 32);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kBars + 40);
+
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) tc::mbar_init(&bars[i], 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    if (tid < C) {
+        const float gr = __ldg(rec + L.gamma + tid), gC = __ldg(rec + L.gamma + C - 1);
+        vgam[tid] = gr;
+        vG[tid] = __expf(gr);
+        veC[tid] = __expf(gC - gr);
+        vbeta[tid] = __ldg(rec + L.beta + tid);
+        vkk[tid] = __ldg(rec + L.kk + tid);
+        vdb[tid] = 0.f;
+        vdg[tid] = 0.f;
+        if (tid == 0) vmisc[0] = 0.f;
+    }
+    __syncthreads();
+
+    // ---- phase 0: the operand tiles
+    {
+        const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(p.k) + t0 * D;
+        const __nv_bfloat16* Qg = static_cast<const __nv_bfloat16*>(p.q) + t0 * D;
+        const __nv_bfloat16* Og = static_cast<const __nv_bfloat16*>(p.dout) + t0 * D;
+        // bf16 rows: K, Q, dO and diag(Gam) K (1024 chunks each)
+#pragma unroll 2
+        for (int u = tid; u < 1024; u += kThreads) {
+            const int r = u >> 4, c8 = u & 15, b = c8 >> 3;
+            const uint32_t so = tc::sw128_offset(r, (c8 & 7) * 8);
+            const bool in = r < nvalid;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            const uint4 kv = in ? __ldg(reinterpret_cast<const uint4*>(Kg + r * ld + 8 * c8)) : z;
+            const uint4 qv = in ? __ldg(reinterpret_cast<const uint4*>(Qg + r * ld + 8 * c8)) : z;
+            const uint4 ov = in ? __ldg(reinterpret_cast<const uint4*>(Og + r * ld + 8 * c8)) : z;
+            *reinterpret_cast<uint4*>(sm + kKQ + 16384 * b + so) = qv;
+            *reinterpret_cast<uint4*>(sm + kKQ + 16384 * b + 8192 + so) = kv;
+            *reinterpret_cast<uint4*>(sm + kOX + 16384 * b + so) = ov;
+        }
+        // fp32 -> bf16: S0 (and its remainder), dS1 (2048 chunks each), W, dW (1024), T (512)
+#pragma unroll 2
+        for (int u = tid; u < 2048; u += kThreads) {
+            const int r = u >> 4, c8 = u & 15, b = c8 >> 3;
+            const uint32_t so = 16384 * b + tc::sw128_offset(r, (c8 & 7) * 8);
+            float x[8], y[8];
+            const float4* s4 = reinterpret_cast<const float4*>(S0 + r * D + 8 * c8);
+            const float4* d4 = reinterpret_cast<const float4*>(dS1 + r * D + 8 * c8);
+            *reinterpret_cast<float4*>(x) = __ldg(s4);
+            *reinterpret_cast<float4*>(x + 4) = __ldg(s4 + 1);
+            *reinterpret_cast<float4*>(y) = __ldg(d4);
+            *reinterpret_cast<float4*>(y + 4) = __ldg(d4 + 1);
+            const uint4 hi = bgt_pack8(x);
+            float xh[8];
+            bgt_unpack8(hi, xh);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xh[e] = x[e] - xh[e];
+            *reinterpret_cast<uint4*>(sm + kS0 + so) = hi;
+            *reinterpret_cast<uint4*>(sm + kR2 + so) = bgt_pack8(xh);
+            *reinterpret_cast<uint4*>(sm + kR1 + so) = bgt_pack8(y);
+        }
+#pragma unroll 2
+        for (int u = tid; u < 1024; u += kThreads) {
+            const int r = u >> 4, c8 = u & 15, b = c8 >> 3;
+            const uint32_t so = 8192 * b + tc::sw128_offset(r, (c8 & 7) * 8);
+            float x[8], y[8];
+            const float4* w4 = reinterpret_cast<const float4*>(W + r * D + 8 * c8);
+            const float4* d4 = reinterpret_cast<const float4*>(dW + r * D + 8 * c8);
+            *reinterpret_cast<float4*>(x) = __ldg(w4);
+            *reinterpret_cast<float4*>(x + 4) = __ldg(w4 + 1);
+            *reinterpret_cast<float4*>(y) = __ldg(d4);
+            *reinterpret_cast<float4*>(y + 4) = __ldg(d4 + 1);
+            *reinterpret_cast<uint4*>(sm + kW + so) = bgt_pack8(x);
+            const uint4 hi = bgt_pack8(y);
+            float yh[8];
+            bgt_unpack8(hi, yh);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) yh[e] = y[e] - yh[e];
+            *reinterpret_cast<uint4*>(sm + kR3 + so) = hi;
+            *reinterpret_cast<uint4*>(sm + kOX + 16384 * b + 8192 + tc::sw128_offset(r, (c8 & 7) * 8)) =
+                bgt_pack8(yh);
+        }
+        for (int u = tid; u < 512; u += kThreads) {
+            const int r = u >> 3, c8 = u & 7;
+            float x[8];
+            const float4* t4 = reinterpret_cast<const float4*>(rec + L.T + r * C + 8 * c8);
+            *reinterpret_cast<float4*>(x) = __ldg(t4);
+            *reinterpret_cast<float4*>(x + 4) = __ldg(t4 + 1);
+            const uint4 hi = bgt_pack8(x);
+            float xh[8];
+            bgt_unpack8(hi, xh);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xh[e] = x[e] - xh[e];
+            *reinterpret_cast<uint4*>(sm + kR3 + 16384 + tc::sw128_offset(r, 8 * c8)) = hi;
+            *reinterpret_cast<uint4*>(sm + kTlo + tc::sw128_offset(r, 8 * c8)) = bgt_pack8(xh);
+        }
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t s0 = tc::smem_u32(sm);
+
+    auto wait_all = [&](int slot, unsigned where) {
+        bool good = !*abort_flag;
+        if (good && !tc::mbar_wait(&bars[slot], 0, kTimeoutNs)) {
+            record_error(p.err, where, (unsigned)c);
+            *abort_flag = 1;
+            good = false;
+        }
+        const bool ok = !__syncthreads_or(!good);
+        tc::tc_fence_after();
+        return ok;
+    };
+
+    // 64 columns of this warp's TMEM lanes into two register arrays
+    auto ld64 = [&](uint32_t col, float (&a)[32], float (&b)[32]) {
+        tc::tmem_ld_32x32b_x32(tmem + lf + col + 64 * hh, a);
+        tc::tmem_ld_32x32b_x32(tmem + lf + col + 64 * hh + 32, b);
+        tc::tmem_ld_wait();
+    };
+#define V64(i) ((i) < 32 ? va[(i)] : vb[(i) - 32])
+
+    // ---- phase 1 products
+    if (tid == 0) {
+        using tc::sdesc_sw128;
+        constexpr uint32_t i_dx = tc::idesc_bf16(64, 128, true, true);
+        constexpr uint32_t i_pg = tc::idesc_bf16(128, 64, false, false);
+        constexpr uint32_t i_e = tc::idesc_bf16(64, 128, false, true);
+        constexpr uint32_t i_z = tc::idesc_bf16(64, 128, false, false);
+#pragma unroll
+        for (int kk = 0; kk < 12; ++kk) {   // dX = T^T dW: A = T^T (M-major), B = dW (N-major)
+            const int k4 = kk & 3, part = kk >> 2;   // hi hi, hi lo, lo hi
+            const uint32_t a = (part == 2 ? kTlo : kR3 + 16384) + k4 * 2048;
+            const uint64_t bd = part == 1 ? sdesc_sw128(s0 + kOX + 8192 + k4 * 2048, 16384, 1024)
+                                          : sdesc_sw128(s0 + kR3 + k4 * 2048, 8192, 1024);
+            tc::mma_bf16(tmem + TD_X, sdesc_sw128(s0 + a, 8192, 1024), bd, i_dx, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+            // [P' ; G] = [Q ; K] K^T
+            tc::mma_bf16(tmem + TD_PG, sdesc_sw128(s0 + kKQ + ko, 16, 1024),
+                         sdesc_sw128(s0 + kKQ + 8192 + ko, 16, 1024), i_pg, kk > 0);
+            // Z1 = W dS1^T: B = dS1 rows (K-major)
+            tc::mma_bf16(tmem + TD_Z, sdesc_sw128(s0 + kW + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                         sdesc_sw128(s0 + kR1 + ko, 16, 1024), i_z, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            // E1 = K S0 = K hi + K lo: B = S0 (N-major), A = the K rows of [Q ; K]
+            const int k8 = kk & 7;
+            tc::mma_bf16(tmem + TD_E, sdesc_sw128(s0 + kKQ + 8192 + (k8 >> 2) * 16384 + (k8 & 3) * 32, 16, 1024),
+                         sdesc_sw128(s0 + (kk < 8 ? kS0 : kR2) + k8 * 2048, 16384, 1024), i_e, kk > 0);
+        }
+        tc::mma_commit(&bars[0]);
+    }
+    bool ok = wait_all(0, kWhere1);
+
+    // ---- phase 2
+    float* dxp = reinterpret_cast<float*>(sm + kR1);   // dX, 64 values per M=64 row thread
+    float* eke = reinterpret_cast<float*>(sm + kR2);   // diag(Gam) E1, later diag(eC) Z1, the same way
+    const int pslot = warp * 16 + lane;                // 0..127 for the M = 64 row threads
+    float PA[32];                                       // P (top) or At (bottom), columns 32 hh..
+    if (ok) {
+        {   // dX: rows r64, columns 64 hh..
+            float va[32], vb[32];
+            ld64(TD_X, va, vb);
+            if (m64) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) dxp[i * 128 + pslot] = V64(i);
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8)
+                    *reinterpret_cast<uint4*>(sm + kOX + 16384 * hh + 8192 + tc::sw128_offset(r64, 8 * c8)) =
+                        bgt_pack8(c8 < 4 ? va + 8 * c8 : vb + 8 * (c8 - 4));
+                if (r64 < nvalid) {
+                    const float b = vbeta[r64];
+                    __nv_bfloat16* gv = static_cast<__nv_bfloat16*>(p.dv) + (t0 + (size_t)r64 * p.H) * D + 64 * hh;
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        float x[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[e] = b * V64(8 * c8 + e);
+                        *reinterpret_cast<uint4*>(gv + 8 * c8) = bgt_pack8(x);
+                    }
+                }
+            }
+        }
+        {   // diag(Gam) E1, per M = 64 row thread (the remainder tile is consumed)
+            float va[32], vb[32];
+            ld64(TD_E, va, vb);
+            if (m64) {
+                const float G = vG[r64];
+#pragma unroll
+                for (int i = 0; i < 64; ++i) eke[i * 128 + pslot] = G * V64(i);
+            }
+        }
+        {   // [P' ; G]: row rr, columns s = 32 hh + i
+            float v[32];
+            tc::tmem_ld_32x32b_x32(tmem + lf + TD_PG + 32 * hh, v);
+            tc::tmem_ld_wait();
+            const float gr = vgam[rr];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int s = 32 * hh + i;
+                const bool in = top ? s <= rr : s < rr;
+                PA[i] = in ? __expf(gr - vgam[s]) * v[i] : 0.f;
+            }
+            if (!top) {
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8)
+                    *reinterpret_cast<uint4*>(sm + kR3 + tc::sw128_offset(rr, 32 * hh + 8 * c8)) =
+                        bgt_pack8(PA + 8 * c8);
+            }
+        }
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+
+    // ---- phase 3 products
+    if (tid == 0 && ok) {
+        using tc::sdesc_sw128;
+        constexpr uint32_t i_xy = tc::idesc_bf16(128, 128, false, false);
+        constexpr uint32_t i_pa = tc::idesc_bf16(128, 64, false, false);
+        constexpr uint32_t i_aw = tc::idesc_bf16(64, 128, false, true);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+            // [X1 ; Y1] = [dO ; dX] S0^T: B = S0 rows (K-major)
+            tc::mma_bf16(tmem + TD_X, sdesc_sw128(s0 + kOX + ko, 16, 1024), sdesc_sw128(s0 + kS0 + ko, 16, 1024),
+                         i_xy, kk > 0);
+            // [dP ; -dA] = [dO ; dX] W^T: B = W rows (K-major)
+            tc::mma_bf16(tmem + TD_PG, sdesc_sw128(s0 + kOX + ko, 16, 1024),
+                         sdesc_sw128(s0 + kW + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), i_pa, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)   // E2 = At W: B = W (N-major)
+            tc::mma_bf16(tmem + TD_E, sdesc_sw128(s0 + kR3 + kk * 32, 16, 1024),
+                         sdesc_sw128(s0 + kW + kk * 2048, 8192, 1024), i_aw, kk > 0);
+        tc::mma_commit(&bars[1]);
+    }
+    // V rows for the residuals, loaded while the products run
+    uint4 vrow[8];
+    if (m64) {
+        const __nv_bfloat16* Vg = static_cast<const __nv_bfloat16*>(p.v) + (t0 + (size_t)r64 * p.H) * D + 64 * hh;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8)
+            vrow[c8] = r64 < nvalid ? __ldg(reinterpret_cast<const uint4*>(Vg + 8 * c8)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // <dS1, S0> (fp32)
+    float sdot = 0.f;
+    {
+        const float4* a4 = reinterpret_cast<const float4*>(dS1);
+        const float4* b4 = reinterpret_cast<const float4*>(S0);
+        for (int i = tid; i < D * D / 4; i += kThreads) {
+            const float4 a = __ldg(a4 + i), b = __ldg(b4 + i);
+            sdot += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+        }
+        sdot = warp_sum(sdot);
+    }
+    ok = ok && wait_all(1, kWhere3);
+    if (ok) {   // uniform: every thread takes the same branch
+        if (lane == 0) atomicAdd(&vmisc[0], __expf(vgam[C - 1]) * sdot);
+        {   // E: residuals and dbeta (rows r64, columns 64 hh..)
+            float va[32], vb[32];
+            ld64(TD_E, va, vb);
+            if (m64) {
+                float db = 0.f;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    float x[8];
+                    bgt_unpack8(vrow[c8], x);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int i = 8 * c8 + e;
+                        db += dxp[i * 128 + pslot] * (x[e] - eke[i * 128 + pslot] - V64(i));
+                    }
+                }
+                atomicAdd(&vdb[r64], db);
+            }
+        }
+        {   // diag(eC) Z1: the Kt term of dgamma (rows r64), kept for dk
+            float va[32], vb[32];
+            ld64(TD_Z, va, vb);
+            if (m64) {
+                float z = 0.f;
+                const float ec = veC[r64];
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    float x[8];
+                    bgt_unpack8(*reinterpret_cast<const uint4*>(sm + kKQ + 16384 * hh + 8192 +
+                                                                tc::sw128_offset(r64, 8 * c8)), x);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int i = 8 * c8 + e;
+                        const float zz = ec * V64(i);
+                        z += x[e] * zz;
+                        eke[i * 128 + pslot] = zz;
+                    }
+                }
+                atomicAdd(&vdg[r64], -z);
+                atomicAdd(&vmisc[0], z);
+            }
+        }
+        {   // [X1 ; Y1]: the O term (q . Gam X1) and the Y term (k . -Gam beta Y1) of dgamma
+            float va[32], vb[32];
+            ld64(TD_X, va, vb);
+            const uint32_t rowb = kKQ + 16384 * hh + (top ? 0u : 8192u);
+            float a = 0.f;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float x[8];
+                bgt_unpack8(*reinterpret_cast<const uint4*>(sm + rowb + tc::sw128_offset(rr, 8 * c8)), x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a += x[e] * V64(8 * c8 + e);
+            }
+            atomicAdd(&vdg[rr], top ? vG[rr] * a : -vG[rr] * vbeta[rr] * a);
+        }
+        {   // [dP ; -dA]: P and A terms of dgamma, dP o D and F
+            float v[32];
+            tc::tmem_ld_32x32b_x32(tmem + lf + TD_PG + 32 * hh, v);
+            tc::tmem_ld_wait();
+            const float gr = vgam[rr], br = vbeta[rr];
+            float row = 0.f, col[32], t[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int s = 32 * hh + i;
+                // top: dP (s <= r), P in PA;  bottom: dA = -(dX W^T) (s < r), At in PA
+                const float m = top ? (s <= rr ? v[i] : 0.f) : (s < rr ? -v[i] : 0.f);
+                const float prod = m * PA[i];
+                row += prod;
+                col[i] = top ? prod : br * prod;
+                const float dd = (top ? s <= rr : s < rr) ? __expf(gr - vgam[s]) : 0.f;
+                t[i] = top ? dd * m : br * dd * m;
+            }
+            atomicAdd(&vdg[rr], top ? row : br * row);
+            const float cs = bgt_col_sums(col, lane);
+            atomicAdd(&vdg[32 * hh + lane], -cs);
+            const uint32_t dst = kR3 + (top ? 8192u : 16384u);
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8)
+                *reinterpret_cast<uint4*>(sm + dst + tc::sw128_offset(rr, 32 * hh + 8 * c8)) = bgt_pack8(t + 8 * c8);
+        }
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        __syncthreads();
+        tc::tc_fence_after();
+        // ---- phase 5 products
+        if (tid == 0) {
+            using tc::sdesc_sw128;
+            constexpr uint32_t i_k = tc::idesc_bf16(64, 128, false, true);   // A K-major, B = K or Q rows (N-major)
+            constexpr uint32_t i_kt = tc::idesc_bf16(64, 128, true, true);   // A^T (M-major)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t kb = s0 + kKQ + 8192 + kk * 2048, qb = s0 + kKQ + kk * 2048;
+                // X2 = (dP o D) K
+                tc::mma_bf16(tmem + TD_E, sdesc_sw128(s0 + kR3 + 8192 + kk * 32, 16, 1024),
+                             sdesc_sw128(kb, 16384, 1024), i_k, kk > 0);
+                // Z5 = (dP o D)^T Q + F K + F^T K
+                tc::mma_bf16(tmem + TD_Z, sdesc_sw128(s0 + kR3 + 8192 + kk * 2048, 8192, 1024),
+                             sdesc_sw128(qb, 16384, 1024), i_kt, kk > 0);
+                tc::mma_bf16(tmem + TD_Z, sdesc_sw128(s0 + kR3 + 16384 + kk * 32, 16, 1024),
+                             sdesc_sw128(kb, 16384, 1024), i_k, 1u);
+                tc::mma_bf16(tmem + TD_Z, sdesc_sw128(s0 + kR3 + 16384 + kk * 2048, 8192, 1024),
+                             sdesc_sw128(kb, 16384, 1024), i_kt, 1u);
+            }
+            tc::mma_commit(&bars[2]);
+        }
+        __syncthreads();   // dbeta and dgamma complete
+    }
+    ok = ok && wait_all(2, kWhere5);
+    // ---- phase 6: stage X2^T and Z^T ([column][row]), then the outputs
+    float* x2t = reinterpret_cast<float*>(sm + kR1);
+    float* zt = reinterpret_cast<float*>(sm + kR2);
+    {
+        float za[32], zb[32];
+        if (ok) {
+            float va[32], vb[32];
+            ld64(TD_Z, va, vb);
+            if (m64) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    za[i] = va[i] + eke[i * 128 + pslot];
+                    zb[i] = vb[i] + eke[(i + 32) * 128 + pslot];
+                }
+            }
+        }
+        __syncthreads();   // the kept values are read before the staging overwrites them
+        if (ok) {
+            float va[32], vb[32];
+            ld64(TD_E, va, vb);
+            if (m64) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) x2t[(64 * hh + i) * 64 + r64] = V64(i);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    zt[(64 * hh + i) * 64 + r64] = za[i];
+                    zt[(64 * hh + i + 32) * 64 + r64] = zb[i];
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (ok) {
+        float va[32], vb[32];
+        ld64(TD_X, va, vb);
+        if (rr < nvalid) {
+            const float G = vG[rr], br = vbeta[rr];
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(top ? p.dq : p.dk) + (t0 + (size_t)rr * p.H) * D + 64 * hh;
+            if (top) {
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int a = 64 * hh + 8 * c8 + e;
+                        x[e] = fmaf(G, V64(8 * c8 + e), x2t[a * 64 + rr]);
+                    }
+                    *reinterpret_cast<uint4*>(out + 8 * c8) = bgt_pack8(x);
+                }
+            } else {
+                const float den = vkk[rr] + p.eps;
+                const float vrs = p.beta_direct ? 0.f : -2.f * br * vdb[rr] / den;
+                const float ys = -G * br;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    float x[8], kx[8];
+                    bgt_unpack8(*reinterpret_cast<const uint4*>(sm + kKQ + 16384 * hh + 8192 +
+                                                                tc::sw128_offset(rr, 8 * c8)), kx);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int a = 64 * hh + 8 * c8 + e;
+                        x[e] = fmaf(ys, V64(8 * c8 + e), zt[a * 64 + rr]) + vrs * kx[e];
+                    }
+                    *reinterpret_cast<uint4*>(out + 8 * c8) = bgt_pack8(x);
+                }
+            }
+        }
+        if (tid == 0) {
+            // dg: the reverse cumulative sum of dgamma, with the chunk-end total at its last token
+            float acc = vmisc[0];
+            for (int r = C - 1; r >= 0; --r) {
+                acc += vdg[r];
+                if (r < nvalid) p.dg[t0 + (size_t)r * p.H] = acc;
+            }
+        }
+        if (tid < nvalid) {
+            const float den = vkk[tid] + p.eps;
+            p.deta[t0 + (size_t)tid * p.H] = p.beta_direct ? vdb[tid] : vdb[tid] / den;
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+#undef V64
+}
+
 // ------------------------------------------------------------ gradients
 
 // Shared memory of the gradient kernel (floats, in order): dX, E, dQ, dK
@@ -1045,7 +1618,14 @@ cudaError_t launch_all(BwdParams p, cudaStream_t st) {
         bwd_carry_kernel<TIO, PRECISE><<<2 * p.B * p.H, 512, s_carry, st>>>(p);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_grad_kernel<TIO, PRECISE><<<items, 512, s_grad, st>>>(p);
+    if (p.tc_carry) {
+        if ((e = cudaFuncSetAttribute(bwd_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)bgt::kSmem)) != cudaSuccess)
+            return e;
+        bwd_grad_tc_kernel<<<items, bgt::kThreads, bgt::kSmem, st>>>(p);
+    } else {
+        bwd_grad_kernel<TIO, PRECISE><<<items, 512, s_grad, st>>>(p);
+    }
     return cudaGetLastError();
 }
 
