@@ -875,13 +875,14 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
     }
     __syncthreads();
 
-    // ---- phase 0: the operand tiles
+    // ---- phase 0: the operand tiles (and <dS1, S0> from the same loads)
+    float sdot = 0.f;
     {
         const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(p.k) + t0 * D;
         const __nv_bfloat16* Qg = static_cast<const __nv_bfloat16*>(p.q) + t0 * D;
         const __nv_bfloat16* Og = static_cast<const __nv_bfloat16*>(p.dout) + t0 * D;
-        // bf16 rows: K, Q, dO and diag(Gam) K (1024 chunks each)
-#pragma unroll 2
+        // bf16 rows: K, Q, dO (1024 chunks each)
+#pragma unroll 4
         for (int u = tid; u < 1024; u += kThreads) {
             const int r = u >> 4, c8 = u & 15, b = c8 >> 3;
             const uint32_t so = tc::sw128_offset(r, (c8 & 7) * 8);
@@ -895,7 +896,7 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
             *reinterpret_cast<uint4*>(sm + kOX + 16384 * b + so) = ov;
         }
         // fp32 -> bf16: S0 (and its remainder), dS1 (2048 chunks each), W, dW (1024), T (512)
-#pragma unroll 2
+#pragma unroll 4
         for (int u = tid; u < 2048; u += kThreads) {
             const int r = u >> 4, c8 = u & 15, b = c8 >> 3;
             const uint32_t so = 16384 * b + tc::sw128_offset(r, (c8 & 7) * 8);
@@ -906,6 +907,8 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
             *reinterpret_cast<float4*>(x + 4) = __ldg(s4 + 1);
             *reinterpret_cast<float4*>(y) = __ldg(d4);
             *reinterpret_cast<float4*>(y + 4) = __ldg(d4 + 1);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sdot = fmaf(x[e], y[e], sdot);
             const uint4 hi = bgt_pack8(x);
             float xh[8];
             bgt_unpack8(hi, xh);
@@ -915,7 +918,7 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
             *reinterpret_cast<uint4*>(sm + kR2 + so) = bgt_pack8(xh);
             *reinterpret_cast<uint4*>(sm + kR1 + so) = bgt_pack8(y);
         }
-#pragma unroll 2
+#pragma unroll 4
         for (int u = tid; u < 1024; u += kThreads) {
             const int r = u >> 4, c8 = u & 15, b = c8 >> 3;
             const uint32_t so = 8192 * b + tc::sw128_offset(r, (c8 & 7) * 8);
@@ -1106,17 +1109,7 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
         for (int c8 = 0; c8 < 8; ++c8)
             vrow[c8] = r64 < nvalid ? __ldg(reinterpret_cast<const uint4*>(Vg + 8 * c8)) : make_uint4(0u, 0u, 0u, 0u);
     }
-    // <dS1, S0> (fp32)
-    float sdot = 0.f;
-    {
-        const float4* a4 = reinterpret_cast<const float4*>(dS1);
-        const float4* b4 = reinterpret_cast<const float4*>(S0);
-        for (int i = tid; i < D * D / 4; i += kThreads) {
-            const float4 a = __ldg(a4 + i), b = __ldg(b4 + i);
-            sdot += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
-        }
-        sdot = warp_sum(sdot);
-    }
+    sdot = warp_sum(sdot);
     ok = ok && wait_all(1, kWhere3);
     if (ok) {   // uniform: every thread takes the same branch
         if (lane == 0) atomicAdd(&vmisc[0], __expf(vgam[C - 1]) * sdot);

@@ -99,13 +99,23 @@ def test_backward_deltanet_without_decay():
     _check(inp, "bf16", do, dh, direct=True)
 
 
-def test_backward_strong_decay():
+@pytest.mark.parametrize("io", ["fp32", "bf16"])
+def test_backward_strong_decay(io):
     # log-decays near -3 per token: spans of about 190 inside a chunk
-    case = kla_inputs.TINY.with_(B=1, T=130, H=2, dk=128, dv=128, io="fp32", h0_std=0.05, seed=350)
+    case = kla_inputs.TINY.with_(B=1, T=130, H=2, dk=128, dv=128, io=io, h0_std=0.05, seed=350)
     inp = kla_inputs.make_prefill(case, device="cuda")
     inp["g"] = torch.full_like(inp["g"], -3.0)
     do, dh = _grad_inputs(inp, 450)
-    _check(inp, "fp32", do, dh)
+    _check(inp, io, do, dh)
+
+
+def test_backward_large_start_state():
+    # h0 of unit scale: the residual e = v - Gam k S0 - ... is dominated by the
+    # start state, the case that needs S0 at fp32-level accuracy in the products
+    case = kla_inputs.TINY.with_(B=1, T=200, H=2, dk=128, dv=128, io="bf16", h0_std=1.0, seed=360)
+    inp = kla_inputs.make_prefill(case, device="cuda")
+    do, dh = _grad_inputs(inp, 460)
+    _check(inp, "bf16", do, dh)
 
 
 def test_backward_empty_sequence():
