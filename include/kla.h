@@ -195,12 +195,14 @@ KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
  *  chunk = 64; dk, dv : 64 or 128 each; B*H <= 65535.
  *
  * With bf16 I/O and dk = dv = 128 the two state carries (and the per-chunk
- * U = T diag(beta) V and L = (diag(Gam) Q)^T dO they use) are bf16 tcgen05
- * products with fp32 accumulation and an fp32 master state; their waits are
- * bounded (1 s) and a wait that runs out is recorded in the workspace
- * (kla_workspace_check returns KLA_ERR_DEVICE_TIMEOUT).  Other products are
- * tf32 tensor-core tiles with fp32 accumulation; with fp32 I/O each is split
- * into three tf32 products (fp32-level accuracy).
+ * U = T diag(beta) V and L = (diag(Gam) Q)^T dO they use) and the gradient
+ * products are bf16 tcgen05 products with fp32 accumulation (the carries'
+ * master state is fp32; T, dW and S0 enter the residual and dX as bf16
+ * pairs); their waits are bounded (1 s) and a wait that runs out is recorded
+ * in the workspace (kla_workspace_check returns KLA_ERR_DEVICE_TIMEOUT).  The
+ * prep's products, and every product of the other shapes, are tf32
+ * tensor-core tiles with fp32 accumulation; with fp32 I/O each is split into
+ * three tf32 products (fp32-level accuracy).
  * The workspace (kla_chunk_bwd_workspace_bytes, 256-byte aligned, caller
  * owned) holds per-chunk records, every chunk's start state and state
  * gradient: about 373 KB per (batch, head, chunk) at dk = dv = 128.  Errors
