@@ -742,6 +742,261 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
     if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------- prep (tcgen05)
+// bf16 I/O with d_k = d_v = 128, for the tensor-core carries and gradients:
+// per (chunk, head) the record's gamma, beta, ||k||^2, T (fp32), Wk and P^T dO,
+// with the products on tcgen05 (bf16 operands, fp32 accumulation):
+//   G = K K^T (beta and ||k||^2 from its diagonal),  K Q^T  (M = 64, N = 64)
+//   T = (I + diag(beta) strict_lower(D o G))^{-1} by forward substitution (fp32)
+//   Wk = T diag(beta Gam) K,  P^T dO with P^T_rs = exp(gam_s - gam_r) (k_r . q_s), s >= r
+// U and L are left out (the carries form them).  Two CTAs fit on an SM.
+namespace bpt {
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t TP_G = 0, TP_KQ = 64;      // phase 1 (M = 64, N = 64)
+constexpr uint32_t TP_WK = 0, TP_PDO = 128;   // phase 2 (M = 64, N = 128)
+constexpr uint32_t kK = 0;        // K [64][128] bf16, boxes 8 KB apart
+constexpr uint32_t kQ = 16384;    // Q, same layout
+constexpr uint32_t kO = 32768;    // dO, same layout
+constexpr uint32_t kTg = 49152;   // T diag(beta Gam) [64 r][64 s] bf16
+constexpr uint32_t kPT = 57344;   // P^T [64 r][64 s] bf16
+constexpr uint32_t kA = 65536;    // A, then T: fp32 [64][kLdA]
+constexpr int kLdA = 65;
+constexpr uint32_t kT = kA + 64 * kLdA * 4;        // T fp32 [64][kLdA]
+constexpr uint32_t kVec = kT + 64 * kLdA * 4;      // gam, beta, kk, bg (float[64] each)
+constexpr uint32_t kBars = kVec + 4 * 256;
+constexpr size_t kSmem = kBars + 32 + 1024;
+constexpr uint64_t kTimeoutNs = 1000000000ull;
+enum : unsigned { kWhere1 = 56, kWhere2 };
+}  // namespace bpt
+
+__global__ void __launch_bounds__(bpt::kThreads, 2) bwd_prep_tc_kernel(BwdParams p) {
+    using namespace bpt;
+    extern __shared__ uint8_t smraw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    constexpr int D = 128;
+    const int c = blockIdx.x, bh = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, hh = warp >> 2;
+    const uint32_t lf = (uint32_t)(32 * q4) << 16;
+    const int r64 = 16 * q4 + lane;   // row of an M = 64 accumulator (lane < 16)
+    const bool m64 = lane < 16;
+    const int nvalid = chunk_valid(p, c);
+    const RecLayout L(D, D);
+    float* rec = p.rec + ((size_t)bh * p.nchunks + c) * L.floats;
+    const size_t t0 = tok_index(p, bh, c, 0);
+    const size_t ld = (size_t)p.H * D;
+    float* sA = reinterpret_cast<float*>(sm + kA);
+    float* sT = reinterpret_cast<float*>(sm + kT);
+    float* vgam = reinterpret_cast<float*>(sm + kVec);
+    float* vbeta = vgam + C;
+    float* vkk = vbeta + C;
+    float* vbg = vkk + C;   // beta Gam
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBars + 16);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kBars + 24);
+
+    if (tid == 0) {
+        tc::mbar_init(&bars[0], 1);
+        tc::mbar_init(&bars[1], 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    // K, Q, dO rows as swizzled bf16 tiles (zero past nvalid); g and eta
+    {
+        const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(p.k) + t0 * D;
+        const __nv_bfloat16* Qg = static_cast<const __nv_bfloat16*>(p.q) + t0 * D;
+        const __nv_bfloat16* Og = static_cast<const __nv_bfloat16*>(p.dout) + t0 * D;
+#pragma unroll 4
+        for (int u = tid; u < 1024; u += kThreads) {
+            const int r = u >> 4, c8 = u & 15;
+            const uint32_t so = (uint32_t)(c8 >> 3) * 8192u + tc::sw128_offset(r, (c8 & 7) * 8);
+            const bool in = r < nvalid;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            const uint4 kv = in ? __ldg(reinterpret_cast<const uint4*>(Kg + r * ld + 8 * c8)) : z;
+            const uint4 qv = in ? __ldg(reinterpret_cast<const uint4*>(Qg + r * ld + 8 * c8)) : z;
+            const uint4 ov = in ? __ldg(reinterpret_cast<const uint4*>(Og + r * ld + 8 * c8)) : z;
+            *reinterpret_cast<uint4*>(sm + kK + so) = kv;
+            *reinterpret_cast<uint4*>(sm + kQ + so) = qv;
+            *reinterpret_cast<uint4*>(sm + kO + so) = ov;
+        }
+    }
+    load_row_scalars(vgam, p.g, p, bh, c, nvalid);
+    load_row_scalars(vbeta, p.eta, p, bh, c, nvalid);
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t s0 = tc::smem_u32(sm);
+    auto wait_all = [&](int slot, unsigned where) {
+        bool good = !*abort_flag;
+        if (good && !tc::mbar_wait(&bars[slot], 0, kTimeoutNs)) {
+            record_error(p.err, where, (unsigned)c);
+            *abort_flag = 1;
+            good = false;
+        }
+        const bool ok = !__syncthreads_or(!good);
+        tc::tc_fence_after();
+        return ok;
+    };
+    if (tid == 0) {
+        constexpr uint32_t id = tc::idesc_bf16(64, 64, false, false);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ko = (kk >> 2) * 8192 + (kk & 3) * 32;
+            tc::mma_bf16(tmem + TP_G, tc::sdesc_sw128(s0 + kK + ko, 16, 1024), tc::sdesc_sw128(s0 + kK + ko, 16, 1024),
+                         id, kk > 0);
+            tc::mma_bf16(tmem + TP_KQ, tc::sdesc_sw128(s0 + kK + ko, 16, 1024), tc::sdesc_sw128(s0 + kQ + ko, 16, 1024),
+                         id, kk > 0);
+        }
+        tc::mma_commit(&bars[0]);
+    }
+    if (tid < 32) {
+        // gamma = inclusive cumulative sum of g: two rows per lane, then a warp scan
+        const float a0 = vgam[2 * tid], a1 = a0 + vgam[2 * tid + 1];
+        float x = a1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, o);
+            if (tid >= o) x += y;
+        }
+        vgam[2 * tid] = x - a1 + a0;
+        vgam[2 * tid + 1] = x;
+    }
+    bool ok = wait_all(0, kWhere1);   // also orders the scan before its readers
+    float g[32];
+    if (ok) {
+        // G into A's place first: ||k_r||^2 is its diagonal
+        tc::tmem_ld_32x32b_x32(tmem + lf + TP_G + 32 * hh, g);
+        tc::tmem_ld_wait();
+        if (m64)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sA[r64 * kLdA + 32 * hh + i] = g[i];
+    }
+    __syncthreads();
+    if (tid < C) {
+        vkk[tid] = sA[tid * kLdA + tid];
+        const float e = vbeta[tid];
+        const float b = tid < nvalid ? (p.beta_direct ? e : e / (sA[tid * kLdA + tid] + p.eps)) : 0.f;
+        vbeta[tid] = b;
+        vbg[tid] = b * __expf(vgam[tid]);
+    }
+    __syncthreads();
+    if (ok) {
+        // A = diag(beta) strict_lower(D o G);  P^T from K Q^T
+        if (m64) {
+            const float gr = vgam[r64], br = vbeta[r64];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int s = 32 * hh + i;
+                sA[r64 * kLdA + s] = s < r64 ? br * __expf(gr - vgam[s]) * g[i] : 0.f;
+            }
+        }
+        float v[32];
+        tc::tmem_ld_32x32b_x32(tmem + lf + TP_KQ + 32 * hh, v);
+        tc::tmem_ld_wait();
+        if (m64) {
+            const float gr = vgam[r64];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int s = 32 * hh + i;
+                v[i] = s >= r64 ? __expf(vgam[s] - gr) * v[i] : 0.f;
+            }
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+                uint4 pk;
+                pk.x = bct_pack2(v[8 * c8], v[8 * c8 + 1]);
+                pk.y = bct_pack2(v[8 * c8 + 2], v[8 * c8 + 3]);
+                pk.z = bct_pack2(v[8 * c8 + 4], v[8 * c8 + 5]);
+                pk.w = bct_pack2(v[8 * c8 + 6], v[8 * c8 + 7]);
+                *reinterpret_cast<uint4*>(sm + kPT + tc::sw128_offset(r64, 32 * hh + 8 * c8)) = pk;
+            }
+        }
+    }
+    __syncthreads();
+    // T = (I + A)^{-1}: column j by four lanes of one warp, forward substitution
+    {
+        const int j = tid >> 2, part = tid & 3;
+        if (j < C) {
+            for (int r = 0; r < C; ++r) {
+                float a = 0.f;
+                for (int s2 = j + part; s2 < r; s2 += 4) a += sA[r * kLdA + s2] * sT[s2 * kLdA + j];
+                a += __shfl_xor_sync(0xffffffffu, a, 1);
+                a += __shfl_xor_sync(0xffffffffu, a, 2);
+                if (part == 0) sT[r * kLdA + j] = r == j ? 1.f : (r < j ? 0.f : -a);
+                __syncwarp();
+            }
+        }
+    }
+    __syncthreads();
+    // T diag(beta Gam) as bf16 (rows r, columns s); T (fp32) and the vectors to the record
+    for (int u = tid; u < 512; u += kThreads) {
+        const int r = u >> 3, c8 = u & 7;
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = sT[r * kLdA + 8 * c8 + e] * vbg[8 * c8 + e];
+        uint4 pk;
+        pk.x = bct_pack2(x[0], x[1]);
+        pk.y = bct_pack2(x[2], x[3]);
+        pk.z = bct_pack2(x[4], x[5]);
+        pk.w = bct_pack2(x[6], x[7]);
+        *reinterpret_cast<uint4*>(sm + kTg + tc::sw128_offset(r, 8 * c8)) = pk;
+        float4* dst = reinterpret_cast<float4*>(rec + L.T + r * C + 8 * c8);
+        dst[0] = make_float4(sT[r * kLdA + 8 * c8], sT[r * kLdA + 8 * c8 + 1], sT[r * kLdA + 8 * c8 + 2],
+                             sT[r * kLdA + 8 * c8 + 3]);
+        dst[1] = make_float4(sT[r * kLdA + 8 * c8 + 4], sT[r * kLdA + 8 * c8 + 5], sT[r * kLdA + 8 * c8 + 6],
+                             sT[r * kLdA + 8 * c8 + 7]);
+    }
+    if (tid < C) {
+        rec[L.gamma + tid] = vgam[tid];
+        rec[L.beta + tid] = vbeta[tid];
+        rec[L.kk + tid] = vkk[tid];
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (tid == 0 && ok) {
+        constexpr uint32_t id = tc::idesc_bf16(64, 128, false, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            // Wk = (T diag(beta Gam)) K;  P^T dO: B = K or dO rows (N-major)
+            tc::mma_bf16(tmem + TP_WK, tc::sdesc_sw128(s0 + kTg + kk * 32, 16, 1024),
+                         tc::sdesc_sw128(s0 + kK + kk * 2048, 8192, 1024), id, kk > 0);
+            tc::mma_bf16(tmem + TP_PDO, tc::sdesc_sw128(s0 + kPT + kk * 32, 16, 1024),
+                         tc::sdesc_sw128(s0 + kO + kk * 2048, 8192, 1024), id, kk > 0);
+        }
+        tc::mma_commit(&bars[1]);
+    }
+    ok = ok && wait_all(1, kWhere2);
+    if (ok) {
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            float a[32], b[32];
+            const uint32_t col = (part ? TP_PDO : TP_WK) + 64 * hh;
+            tc::tmem_ld_32x32b_x32(tmem + lf + col, a);
+            tc::tmem_ld_32x32b_x32(tmem + lf + col + 32, b);
+            tc::tmem_ld_wait();
+            if (m64) {
+                float4* dst = reinterpret_cast<float4*>(rec + (part ? L.PdO : L.Wk) + r64 * D + 64 * hh);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dst[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dst[8 + i] = make_float4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
+            }
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
 // ------------------------------------------------------- gradients (tcgen05)
 // bf16 I/O with d_k = d_v = 128: the gradient kernel's fifteen products on
 // the tensor cores, accumulators in TMEM, operands as 128-byte-swizzled bf16
@@ -1600,7 +1855,14 @@ cudaError_t launch_all(BwdParams p, cudaStream_t st) {
                                   (int)s_grad)) != cudaSuccess) return e;
     const dim3 items(p.nchunks, p.B * p.H);
     p.tc_carry = sizeof(TIO) == 2 && p.DK == 128 && p.DV == 128;
-    bwd_prep_kernel<TIO, PRECISE><<<items, 256, s_prep, st>>>(p);
+    if (p.tc_carry) {
+        if ((e = cudaFuncSetAttribute(bwd_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)bpt::kSmem)) != cudaSuccess)
+            return e;
+        bwd_prep_tc_kernel<<<items, bpt::kThreads, bpt::kSmem, st>>>(p);
+    } else {
+        bwd_prep_kernel<TIO, PRECISE><<<items, 256, s_prep, st>>>(p);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (p.tc_carry) {
         if ((e = cudaFuncSetAttribute(bwd_carry_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
