@@ -919,21 +919,47 @@ __global__ void __launch_bounds__(bpt::kThreads, 2) bwd_prep_tc_kernel(BwdParams
         }
     }
     __syncthreads();
-    // T = (I + A)^{-1}: column j by four lanes of one warp, forward substitution
+    // T = (I + A)^{-1} (A strictly lower triangular) in 16 x 16 blocks: the
+    // diagonal blocks T_ii = (I + A_ii)^{-1} by forward substitution, four at
+    // once (a column by four lanes), then block row by block row
+    // T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
     {
-        const int j = tid >> 2, part = tid & 3;
-        if (j < C) {
-            for (int r = 0; r < C; ++r) {
-                float a = 0.f;
-                for (int s2 = j + part; s2 < r; s2 += 4) a += sA[r * kLdA + s2] * sT[s2 * kLdA + j];
-                a += __shfl_xor_sync(0xffffffffu, a, 1);
-                a += __shfl_xor_sync(0xffffffffu, a, 2);
-                if (part == 0) sT[r * kLdA + j] = r == j ? 1.f : (r < j ? 0.f : -a);
-                __syncwarp();
-            }
+        const int b = tid >> 6, j = 16 * b + ((tid >> 2) & 15), part = tid & 3;
+        for (int i = 0; i < 16; ++i) {
+            const int r = 16 * b + i;
+            float a = 0.f;
+            for (int s2 = j + part; s2 < r; s2 += 4) a = fmaf(sA[r * kLdA + s2], sT[s2 * kLdA + j], a);
+            a += __shfl_xor_sync(0xffffffffu, a, 1);
+            a += __shfl_xor_sync(0xffffffffu, a, 2);
+            if (part == 0) sT[r * kLdA + j] = r == j ? 1.f : (r < j ? 0.f : -a);
+            __syncwarp();
+        }
+        for (int e = tid; e < C * C; e += kThreads) {   // the blocks above the diagonal
+            const int r = e >> 6, col = e & 63;
+            if ((r >> 4) < (col >> 4)) sT[r * kLdA + col] = 0.f;
         }
     }
     __syncthreads();
+    {
+        float* sY = reinterpret_cast<float*>(sm + kTg);   // [j block][16][16] scratch, before Tg
+        for (int i = 1; i < 4; ++i) {
+            for (int e = tid; e < 256 * i; e += kThreads) {
+                const int jb = e >> 8, r = 16 * i + ((e >> 4) & 15), col = 16 * jb + (e & 15);
+                float y = 0.f;
+                for (int s2 = 16 * jb; s2 < 16 * i; ++s2) y = fmaf(sA[r * kLdA + s2], sT[s2 * kLdA + col], y);
+                sY[e] = y;
+            }
+            __syncthreads();
+            for (int e = tid; e < 256 * i; e += kThreads) {
+                const int jb = e >> 8, i2 = (e >> 4) & 15, cc = e & 15;
+                const int r = 16 * i + i2;
+                float t = 0.f;
+                for (int m = 0; m <= i2; ++m) t = fmaf(sT[r * kLdA + 16 * i + m], sY[(jb << 8) + (m << 4) + cc], t);
+                sT[r * kLdA + 16 * jb + cc] = -t;
+            }
+            __syncthreads();
+        }
+    }
     // T diag(beta Gam) as bf16 (rows r, columns s); T (fp32) and the vectors to the record
     for (int u = tid; u < 512; u += kThreads) {
         const int r = u >> 3, c8 = u & 7;
