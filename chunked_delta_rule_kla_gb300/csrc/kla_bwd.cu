@@ -1156,83 +1156,106 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
     }
     __syncthreads();
 
-    // ---- phase 0: the operand tiles (and <dS1, S0> from the same loads)
+    // ---- phase 0: the operand tiles (and <dS1, S0> from the same loads), in two
+    // rounds of loads issued together: S0 and dS1; then K, Q, dO, W, dW and T
     float sdot = 0.f;
     {
-        const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(p.k) + t0 * D;
-        const __nv_bfloat16* Qg = static_cast<const __nv_bfloat16*>(p.q) + t0 * D;
-        const __nv_bfloat16* Og = static_cast<const __nv_bfloat16*>(p.dout) + t0 * D;
-        // bf16 rows: K, Q, dO (1024 chunks each)
-#pragma unroll 4
-        for (int u = tid; u < 1024; u += kThreads) {
-            const int r = u >> 4, c8 = u & 15, b = c8 >> 3;
-            const uint32_t so = tc::sw128_offset(r, (c8 & 7) * 8);
-            const bool in = r < nvalid;
-            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-            const uint4 kv = in ? __ldg(reinterpret_cast<const uint4*>(Kg + r * ld + 8 * c8)) : z;
-            const uint4 qv = in ? __ldg(reinterpret_cast<const uint4*>(Qg + r * ld + 8 * c8)) : z;
-            const uint4 ov = in ? __ldg(reinterpret_cast<const uint4*>(Og + r * ld + 8 * c8)) : z;
-            *reinterpret_cast<uint4*>(sm + kKQ + 16384 * b + so) = qv;
-            *reinterpret_cast<uint4*>(sm + kKQ + 16384 * b + 8192 + so) = kv;
-            *reinterpret_cast<uint4*>(sm + kOX + 16384 * b + so) = ov;
+        {
+            float4 xs[8][2], ys[8][2];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int u = tid + kThreads * k, r = u >> 4, c8 = u & 15;
+                const float4* s4 = reinterpret_cast<const float4*>(S0 + r * D + 8 * c8);
+                const float4* d4 = reinterpret_cast<const float4*>(dS1 + r * D + 8 * c8);
+                xs[k][0] = __ldg(s4);
+                xs[k][1] = __ldg(s4 + 1);
+                ys[k][0] = __ldg(d4);
+                ys[k][1] = __ldg(d4 + 1);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int u = tid + kThreads * k, r = u >> 4, c8 = u & 15, b = c8 >> 3;
+                const uint32_t so = 16384 * b + tc::sw128_offset(r, (c8 & 7) * 8);
+                float x[8], y[8];
+                *reinterpret_cast<float4*>(x) = xs[k][0];
+                *reinterpret_cast<float4*>(x + 4) = xs[k][1];
+                *reinterpret_cast<float4*>(y) = ys[k][0];
+                *reinterpret_cast<float4*>(y + 4) = ys[k][1];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) sdot = fmaf(x[e], y[e], sdot);
+                const uint4 hi = bgt_pack8(x);
+                float xh[8];
+                bgt_unpack8(hi, xh);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xh[e] = x[e] - xh[e];
+                *reinterpret_cast<uint4*>(sm + kS0 + so) = hi;
+                *reinterpret_cast<uint4*>(sm + kR2 + so) = bgt_pack8(xh);
+                *reinterpret_cast<uint4*>(sm + kR1 + so) = bgt_pack8(y);
+            }
         }
-        // fp32 -> bf16: S0 (and its remainder), dS1 (2048 chunks each), W, dW (1024), T (512)
-#pragma unroll 4
-        for (int u = tid; u < 2048; u += kThreads) {
-            const int r = u >> 4, c8 = u & 15, b = c8 >> 3;
-            const uint32_t so = 16384 * b + tc::sw128_offset(r, (c8 & 7) * 8);
-            float x[8], y[8];
-            const float4* s4 = reinterpret_cast<const float4*>(S0 + r * D + 8 * c8);
-            const float4* d4 = reinterpret_cast<const float4*>(dS1 + r * D + 8 * c8);
-            *reinterpret_cast<float4*>(x) = __ldg(s4);
-            *reinterpret_cast<float4*>(x + 4) = __ldg(s4 + 1);
-            *reinterpret_cast<float4*>(y) = __ldg(d4);
-            *reinterpret_cast<float4*>(y + 4) = __ldg(d4 + 1);
+        {
+            const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(p.k) + t0 * D;
+            const __nv_bfloat16* Qg = static_cast<const __nv_bfloat16*>(p.q) + t0 * D;
+            const __nv_bfloat16* Og = static_cast<const __nv_bfloat16*>(p.dout) + t0 * D;
+            uint4 kv[4], qv[4], ov[4];
+            float4 ws[4][2], dws[4][2], ts[2][2];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) sdot = fmaf(x[e], y[e], sdot);
-            const uint4 hi = bgt_pack8(x);
-            float xh[8];
-            bgt_unpack8(hi, xh);
+            for (int k = 0; k < 4; ++k) {
+                const int u = tid + kThreads * k, r = u >> 4, c8 = u & 15;
+                const bool in = r < nvalid;
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                kv[k] = in ? __ldg(reinterpret_cast<const uint4*>(Kg + r * ld + 8 * c8)) : z;
+                qv[k] = in ? __ldg(reinterpret_cast<const uint4*>(Qg + r * ld + 8 * c8)) : z;
+                ov[k] = in ? __ldg(reinterpret_cast<const uint4*>(Og + r * ld + 8 * c8)) : z;
+                const float4* w4 = reinterpret_cast<const float4*>(W + r * D + 8 * c8);
+                const float4* d4 = reinterpret_cast<const float4*>(dW + r * D + 8 * c8);
+                ws[k][0] = __ldg(w4);
+                ws[k][1] = __ldg(w4 + 1);
+                dws[k][0] = __ldg(d4);
+                dws[k][1] = __ldg(d4 + 1);
+            }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xh[e] = x[e] - xh[e];
-            *reinterpret_cast<uint4*>(sm + kS0 + so) = hi;
-            *reinterpret_cast<uint4*>(sm + kR2 + so) = bgt_pack8(xh);
-            *reinterpret_cast<uint4*>(sm + kR1 + so) = bgt_pack8(y);
-        }
-#pragma unroll 4
-        for (int u = tid; u < 1024; u += kThreads) {
-            const int r = u >> 4, c8 = u & 15, b = c8 >> 3;
-            const uint32_t so = 8192 * b + tc::sw128_offset(r, (c8 & 7) * 8);
-            float x[8], y[8];
-            const float4* w4 = reinterpret_cast<const float4*>(W + r * D + 8 * c8);
-            const float4* d4 = reinterpret_cast<const float4*>(dW + r * D + 8 * c8);
-            *reinterpret_cast<float4*>(x) = __ldg(w4);
-            *reinterpret_cast<float4*>(x + 4) = __ldg(w4 + 1);
-            *reinterpret_cast<float4*>(y) = __ldg(d4);
-            *reinterpret_cast<float4*>(y + 4) = __ldg(d4 + 1);
-            *reinterpret_cast<uint4*>(sm + kW + so) = bgt_pack8(x);
-            const uint4 hi = bgt_pack8(y);
-            float yh[8];
-            bgt_unpack8(hi, yh);
+            for (int k = 0; k < 2; ++k) {
+                const int u = tid + kThreads * k, r = u >> 3, c8 = u & 7;
+                const float4* t4 = reinterpret_cast<const float4*>(rec + L.T + r * C + 8 * c8);
+                ts[k][0] = __ldg(t4);
+                ts[k][1] = __ldg(t4 + 1);
+            }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) yh[e] = y[e] - yh[e];
-            *reinterpret_cast<uint4*>(sm + kR3 + so) = hi;
-            *reinterpret_cast<uint4*>(sm + kOX + 16384 * b + 8192 + tc::sw128_offset(r, (c8 & 7) * 8)) =
-                bgt_pack8(yh);
-        }
-        for (int u = tid; u < 512; u += kThreads) {
-            const int r = u >> 3, c8 = u & 7;
-            float x[8];
-            const float4* t4 = reinterpret_cast<const float4*>(rec + L.T + r * C + 8 * c8);
-            *reinterpret_cast<float4*>(x) = __ldg(t4);
-            *reinterpret_cast<float4*>(x + 4) = __ldg(t4 + 1);
-            const uint4 hi = bgt_pack8(x);
-            float xh[8];
-            bgt_unpack8(hi, xh);
+            for (int k = 0; k < 4; ++k) {
+                const int u = tid + kThreads * k, r = u >> 4, c8 = u & 15, b = c8 >> 3;
+                const uint32_t so = tc::sw128_offset(r, (c8 & 7) * 8);
+                *reinterpret_cast<uint4*>(sm + kKQ + 16384 * b + so) = qv[k];
+                *reinterpret_cast<uint4*>(sm + kKQ + 16384 * b + 8192 + so) = kv[k];
+                *reinterpret_cast<uint4*>(sm + kOX + 16384 * b + so) = ov[k];
+                float x[8], y[8];
+                *reinterpret_cast<float4*>(x) = ws[k][0];
+                *reinterpret_cast<float4*>(x + 4) = ws[k][1];
+                *reinterpret_cast<float4*>(y) = dws[k][0];
+                *reinterpret_cast<float4*>(y + 4) = dws[k][1];
+                *reinterpret_cast<uint4*>(sm + kW + 8192 * b + so) = bgt_pack8(x);
+                const uint4 hi = bgt_pack8(y);
+                float yh[8];
+                bgt_unpack8(hi, yh);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xh[e] = x[e] - xh[e];
-            *reinterpret_cast<uint4*>(sm + kR3 + 16384 + tc::sw128_offset(r, 8 * c8)) = hi;
-            *reinterpret_cast<uint4*>(sm + kTlo + tc::sw128_offset(r, 8 * c8)) = bgt_pack8(xh);
+                for (int e = 0; e < 8; ++e) yh[e] = y[e] - yh[e];
+                *reinterpret_cast<uint4*>(sm + kR3 + 8192 * b + so) = hi;
+                *reinterpret_cast<uint4*>(sm + kOX + 16384 * b + 8192 + so) = bgt_pack8(yh);
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int u = tid + kThreads * k, r = u >> 3, c8 = u & 7;
+                float x[8];
+                *reinterpret_cast<float4*>(x) = ts[k][0];
+                *reinterpret_cast<float4*>(x + 4) = ts[k][1];
+                const uint4 hi = bgt_pack8(x);
+                float xh[8];
+                bgt_unpack8(hi, xh);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xh[e] = x[e] - xh[e];
+                *reinterpret_cast<uint4*>(sm + kR3 + 16384 + tc::sw128_offset(r, 8 * c8)) = hi;
+                *reinterpret_cast<uint4*>(sm + kTlo + tc::sw128_offset(r, 8 * c8)) = bgt_pack8(xh);
+            }
         }
     }
     tc::fence_proxy_async_smem();
