@@ -194,14 +194,14 @@ KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
  *  grad_h0 : fp32 [B, H, dk, dv], or NULL when not wanted
  *  chunk = 64; dk, dv : 64 or 128 each; B*H <= 65535.
  *
- * With bf16 I/O and dk = dv = 128 the two state carries (and the per-chunk
- * U = T diag(beta) V and L = (diag(Gam) Q)^T dO they use) and the gradient
- * products are bf16 tcgen05 products with fp32 accumulation (the carries'
- * master state is fp32; T, dW and S0 enter the residual and dX as bf16
- * pairs); their waits are bounded (1 s) and a wait that runs out is recorded
- * in the workspace (kla_workspace_check returns KLA_ERR_DEVICE_TIMEOUT).  The
- * prep's products, and every product of the other shapes, are tf32
- * tensor-core tiles with fp32 accumulation; with fp32 I/O each is split into
+ * With bf16 I/O and dk = dv = 128 every product (the prep's, the two state
+ * carries' with the per-chunk U = T diag(beta) V and L = (diag(Gam) Q)^T dO,
+ * and the gradients') is a bf16 tcgen05 product with fp32 accumulation; the
+ * carries' master state and the triangular inverse are fp32, and T, dW and
+ * S0 enter the residual and dX as bf16 pairs.  Their waits are bounded (1 s)
+ * and a wait that runs out is recorded in the workspace (kla_workspace_check
+ * returns KLA_ERR_DEVICE_TIMEOUT).  The other shapes use tf32 tensor-core
+ * tiles with fp32 accumulation; with fp32 I/O each product is split into
  * three tf32 products (fp32-level accuracy).
  * The workspace (kla_chunk_bwd_workspace_bytes, 256-byte aligned, caller
  * owned) holds per-chunk records, every chunk's start state and state
