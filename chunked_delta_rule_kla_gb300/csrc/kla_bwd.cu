@@ -411,9 +411,9 @@ __global__ void __launch_bounds__(512) bwd_carry_kernel(BwdParams p) {
 //             S_acc = dO^T diag(Gam) Q - dW^T Wk     (L^T - dW^T Wk)
 //   S^T <- Gam_C S^T + S_acc
 // Operands are bf16, accumulation fp32.  Warps 8..11 stage the next chunk
-// while the state warps run this one, as 128-byte-swizzled bf16 tiles: Wk
-// (from the fp32 record) and K; forward V and Tb; reverse dO and diag(Gam) Q;
-// the decay factors; and in reverse P^T dO by a bulk copy.
+// while the state warps run this one, as 128-byte-swizzled bf16 tiles: K;
+// forward V, reverse dO and diag(Gam) Q; the decay factors; and by bulk copies
+// the prep's bf16 Wk tile with Tb (forward) or the fp32 P^T dO (reverse).
 namespace bct {
 constexpr int kThreads = 384;
 constexpr int kStateThreads = 256;
@@ -497,24 +497,27 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
         const int c = chunk_of(it), s = it & 1;
         uint8_t* st = sm + s * kStage;
         const float* rec = record(c);
-        if (rev && lt == 0) {
-            tc::mbar_arrive_expect_tx(&bars[BAR_LD0 + s], (uint32_t)(sizeof(float) * C * D));
-            tc::bulk_load(st + kU, rec + L.PdO, (uint32_t)(sizeof(float) * C * D), &bars[BAR_LD0 + s]);
+        if (lt == 0) {
+            // the prep's bf16 Wk tile, and T diag(beta) (forward) or P^T dO (reverse)
+            const uint8_t* rb = reinterpret_cast<const uint8_t*>(rec);
+            const uint32_t bytes = 16384u + (rev ? (uint32_t)(sizeof(float) * C * D) : 8192u);
+            tc::mbar_arrive_expect_tx(&bars[BAR_LD0 + s], bytes);
+            tc::bulk_load(st + kWk, rb + sizeof(float) * L.Wk, 16384u, &bars[BAR_LD0 + s]);
+            if (rev)
+                tc::bulk_load(st + kU, rec + L.PdO, (uint32_t)(sizeof(float) * C * D), &bars[BAR_LD0 + s]);
+            else
+                tc::bulk_load(st + kX2, rb + sizeof(float) * L.U, 8192u, &bars[BAR_LD0 + s]);
         }
         const int nvalid = chunk_valid(p, c);
         const size_t t0 = tok_index(p, bh, c, 0);
         const size_t ld = (size_t)p.H * D;
         const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(p.k) + t0 * D;
         const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(rev ? p.dout : p.v) + t0 * D;
-        {   // Wk (fp32 -> bf16), K and V or dO (bf16 rows, zero past nvalid)
-            float4 w[16];
+        {   // K and V or dO (bf16 rows, zero past nvalid)
             uint4 kv[8], xv[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int unit = lt + 128 * u, r = unit >> 4, c8 = unit & 15;
-                const float4* src = reinterpret_cast<const float4*>(rec + L.Wk + r * D + 8 * c8);
-                w[2 * u] = __ldg(src);
-                w[2 * u + 1] = __ldg(src + 1);
                 const bool in = r < nvalid;
                 kv[u] = in ? __ldg(reinterpret_cast<const uint4*>(K + r * ld + 8 * c8)) : make_uint4(0u, 0u, 0u, 0u);
                 xv[u] = in ? __ldg(reinterpret_cast<const uint4*>(X + r * ld + 8 * c8)) : make_uint4(0u, 0u, 0u, 0u);
@@ -523,12 +526,6 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
             for (int u = 0; u < 8; ++u) {
                 const int unit = lt + 128 * u, r = unit >> 4, c8 = unit & 15;
                 const uint32_t off = bct_off(r, c8);
-                uint4 pk;
-                pk.x = bct_pack2(w[2 * u].x, w[2 * u].y);
-                pk.y = bct_pack2(w[2 * u].z, w[2 * u].w);
-                pk.z = bct_pack2(w[2 * u + 1].x, w[2 * u + 1].y);
-                pk.w = bct_pack2(w[2 * u + 1].z, w[2 * u + 1].w);
-                *reinterpret_cast<uint4*>(st + kWk + off) = pk;
                 *reinterpret_cast<uint4*>(st + kK + off) = kv[u];
                 *reinterpret_cast<uint4*>(st + kX1 + off) = xv[u];
             }
@@ -561,29 +558,6 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
                     o[e] = bct_pack2(G * f.x, G * f.y);
                 }
                 *reinterpret_cast<uint4*>(st + kX2 + bct_off(r, c8)) = pk;
-            }
-        } else {
-            // Tb = T diag(beta): 64 x 64, one box
-            float4 tv[8];
-            float bt[4][8];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int unit = lt + 128 * u, r = unit >> 3, c8 = unit & 7;
-                const float4* src = reinterpret_cast<const float4*>(rec + L.T + r * C + 8 * c8);
-                tv[2 * u] = __ldg(src);
-                tv[2 * u + 1] = __ldg(src + 1);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) bt[u][e] = __ldg(rec + L.beta + 8 * c8 + e);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int unit = lt + 128 * u, r = unit >> 3, c8 = unit & 7;
-                uint4 pk;
-                pk.x = bct_pack2(tv[2 * u].x * bt[u][0], tv[2 * u].y * bt[u][1]);
-                pk.y = bct_pack2(tv[2 * u].z * bt[u][2], tv[2 * u].w * bt[u][3]);
-                pk.z = bct_pack2(tv[2 * u + 1].x * bt[u][4], tv[2 * u + 1].y * bt[u][5]);
-                pk.w = bct_pack2(tv[2 * u + 1].z * bt[u][6], tv[2 * u + 1].w * bt[u][7]);
-                *reinterpret_cast<uint4*>(st + kX2 + tc::sw128_offset(r, 8 * c8)) = pk;
             }
         }
         tc::fence_proxy_async_smem();   // the tiles are read by the tensor cores
@@ -639,8 +613,9 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
         uint8_t* st = sm + s * kStage;
         const size_t item = (size_t)bh * n + c;
         if (warp < 8) {
+            bool ok = group_wait(BAR_LD0 + s, (it >> 1) & 1, kWhereLd, c, true);
             tc::tc_fence_after();
-            if (threadIdx.x == 0) {
+            if (threadIdx.x == 0 && ok) {
                 const uint32_t x1 = tc::smem_u32(st + kX1), x2 = tc::smem_u32(st + kX2);
                 if (rev) {
 #pragma unroll
@@ -667,8 +642,7 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
 #pragma unroll
                 for (int i = 0; i < 64; ++i) ks[(size_t)i * D] = m[i];
             }
-            bool ok = group_wait(BAR_W, it & 1, kWhereW, c, true);
-            if (rev) ok = group_wait(BAR_LD0 + s, (it >> 1) & 1, kWhereLd, c, ok);
+            ok = group_wait(BAR_W, it & 1, kWhereW, c, ok);
             tc::tc_fence_after();
             const float* sc = reinterpret_cast<const float*>(st + kSc);
             if (ok) {
@@ -727,7 +701,7 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
         __syncthreads();
         if (*abort_flag) break;
     }
-    if (it < n && rev && lt == 0) {
+    if (it < n && lt == 0) {
         // given up: let the bulk copies still in flight land before the CTA leaves
         tc::mbar_wait(&bars[BAR_LD0 + (it & 1)], (it >> 1) & 1, kTimeoutNs);
         if (it + 1 < n) tc::mbar_wait(&bars[BAR_LD0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1, kTimeoutNs);
@@ -744,8 +718,10 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
 
 // ------------------------------------------------------- prep (tcgen05)
 // bf16 I/O with d_k = d_v = 128, for the tensor-core carries and gradients:
-// per (chunk, head) the record's gamma, beta, ||k||^2, T (fp32), Wk and P^T dO,
-// with the products on tcgen05 (bf16 operands, fp32 accumulation):
+// per (chunk, head) the record's gamma, beta, ||k||^2, T (fp32), P^T dO (fp32)
+// and, as the 128-byte-swizzled bf16 tiles the tensor-core carries copy as
+// they are, Wk (in Wk's place) and T diag(beta) (in U's place), with the
+// products on tcgen05 (bf16 operands, fp32 accumulation):
 //   G = K K^T (beta and ||k||^2 from its diagonal),  K Q^T  (M = 64, N = 64)
 //   T = (I + diag(beta) strict_lower(D o G))^{-1} by forward substitution (fp32)
 //   Wk = T diag(beta Gam) K,  P^T dO with P^T_rs = exp(gam_s - gam_r) (k_r . q_s), s >= r
@@ -972,6 +948,13 @@ __global__ void __launch_bounds__(bpt::kThreads, 2) bwd_prep_tc_kernel(BwdParams
         pk.z = bct_pack2(x[4], x[5]);
         pk.w = bct_pack2(x[6], x[7]);
         *reinterpret_cast<uint4*>(sm + kTg + tc::sw128_offset(r, 8 * c8)) = pk;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = sT[r * kLdA + 8 * c8 + e] * vbeta[8 * c8 + e];
+        pk.x = bct_pack2(x[0], x[1]);
+        pk.y = bct_pack2(x[2], x[3]);
+        pk.z = bct_pack2(x[4], x[5]);
+        pk.w = bct_pack2(x[6], x[7]);
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(rec + L.U) + tc::sw128_offset(r, 8 * c8)) = pk;
         float4* dst = reinterpret_cast<float4*>(rec + L.T + r * C + 8 * c8);
         dst[0] = make_float4(sT[r * kLdA + 8 * c8], sT[r * kLdA + 8 * c8 + 1], sT[r * kLdA + 8 * c8 + 2],
                              sT[r * kLdA + 8 * c8 + 3]);
@@ -1008,12 +991,25 @@ __global__ void __launch_bounds__(bpt::kThreads, 2) bwd_prep_tc_kernel(BwdParams
             tc::tmem_ld_32x32b_x32(tmem + lf + col, a);
             tc::tmem_ld_32x32b_x32(tmem + lf + col + 32, b);
             tc::tmem_ld_wait();
-            if (m64) {
-                float4* dst = reinterpret_cast<float4*>(rec + (part ? L.PdO : L.Wk) + r64 * D + 64 * hh);
+            if (m64 && part) {
+                float4* dst = reinterpret_cast<float4*>(rec + L.PdO + r64 * D + 64 * hh);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) dst[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) dst[8 + i] = make_float4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
+            } else if (m64) {
+                // Wk as the bf16 tile: row r64 of box hh
+                uint8_t* dst = reinterpret_cast<uint8_t*>(rec + L.Wk) + 8192 * hh;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const float* x = c8 < 4 ? a + 8 * c8 : b + 8 * (c8 - 4);
+                    uint4 pk;
+                    pk.x = bct_pack2(x[0], x[1]);
+                    pk.y = bct_pack2(x[2], x[3]);
+                    pk.z = bct_pack2(x[4], x[5]);
+                    pk.w = bct_pack2(x[6], x[7]);
+                    *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r64, 8 * c8)) = pk;
+                }
             }
         }
     }
