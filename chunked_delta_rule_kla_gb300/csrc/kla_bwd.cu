@@ -919,19 +919,31 @@ __global__ void __launch_bounds__(bpt::kThreads, 2) bwd_prep_tc_kernel(BwdParams
     {
         float* sY = reinterpret_cast<float*>(sm + kTg);   // [j block][16][16] scratch, before Tg
         for (int i = 1; i < 4; ++i) {
+            // (four partial sums a thread: the sums are chains of shared-memory loads)
             for (int e = tid; e < 256 * i; e += kThreads) {
                 const int jb = e >> 8, r = 16 * i + ((e >> 4) & 15), col = 16 * jb + (e & 15);
-                float y = 0.f;
-                for (int s2 = 16 * jb; s2 < 16 * i; ++s2) y = fmaf(sA[r * kLdA + s2], sT[s2 * kLdA + col], y);
-                sY[e] = y;
+                float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+                for (int s2 = 16 * jb; s2 < 16 * i; s2 += 4) {   // multiples of 16 long
+                    y0 = fmaf(sA[r * kLdA + s2], sT[s2 * kLdA + col], y0);
+                    y1 = fmaf(sA[r * kLdA + s2 + 1], sT[(s2 + 1) * kLdA + col], y1);
+                    y2 = fmaf(sA[r * kLdA + s2 + 2], sT[(s2 + 2) * kLdA + col], y2);
+                    y3 = fmaf(sA[r * kLdA + s2 + 3], sT[(s2 + 3) * kLdA + col], y3);
+                }
+                sY[e] = (y0 + y1) + (y2 + y3);
             }
             __syncthreads();
             for (int e = tid; e < 256 * i; e += kThreads) {
                 const int jb = e >> 8, i2 = (e >> 4) & 15, cc = e & 15;
                 const int r = 16 * i + i2;
-                float t = 0.f;
-                for (int m = 0; m <= i2; ++m) t = fmaf(sT[r * kLdA + 16 * i + m], sY[(jb << 8) + (m << 4) + cc], t);
-                sT[r * kLdA + 16 * jb + cc] = -t;
+                float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; m += 4) {   // T_ii is lower triangular: T_ii[i2][m] = 0 for m > i2
+                    t0 = fmaf(sT[r * kLdA + 16 * i + m], sY[(jb << 8) + (m << 4) + cc], t0);
+                    t1 = fmaf(sT[r * kLdA + 16 * i + m + 1], sY[(jb << 8) + ((m + 1) << 4) + cc], t1);
+                    t2 = fmaf(sT[r * kLdA + 16 * i + m + 2], sY[(jb << 8) + ((m + 2) << 4) + cc], t2);
+                    t3 = fmaf(sT[r * kLdA + 16 * i + m + 3], sY[(jb << 8) + ((m + 3) << 4) + cc], t3);
+                }
+                sT[r * kLdA + 16 * jb + cc] = -((t0 + t1) + (t2 + t3));
             }
             __syncthreads();
         }
@@ -1588,13 +1600,20 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
                 }
             }
         }
-        if (tid == 0) {
-            // dg: the reverse cumulative sum of dgamma, with the chunk-end total at its last token
-            float acc = vmisc[0];
-            for (int r = C - 1; r >= 0; --r) {
-                acc += vdg[r];
-                if (r < nvalid) p.dg[t0 + (size_t)r * p.H] = acc;
+        if (warp == 0) {
+            // dg: the reverse cumulative sum of dgamma, with the chunk-end total at its
+            // last token; lane l holds rows 62 - 2l and 63 - 2l, then a warp scan
+            const int ra = 63 - 2 * lane, rb = ra - 1;
+            const float xa = vdg[ra] + (lane == 0 ? vmisc[0] : 0.f), xb = vdg[rb];
+            float x = xa + xb;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
             }
+            const float before = x - (xa + xb);
+            if (ra < nvalid) p.dg[t0 + (size_t)ra * p.H] = before + xa;
+            if (rb < nvalid) p.dg[t0 + (size_t)rb * p.H] = x;
         }
         if (tid < nvalid) {
             const float den = vkk[tid] + p.eps;
