@@ -74,8 +74,8 @@ struct BwdParams {
     int B, T, H, DK, DV, nchunks;
     float* rec;      // [B*H][nchunks] records
     float* states;   // [B*H][nchunks][dk][dv]   S0 of each chunk
-    float* wbuf;     // [B*H][nchunks][64][dv]   W of each chunk
-    float* dstates;  // [B*H][nchunks][dk][dv]   dS1 of each chunk
+    float* wbuf;     // [B*H][nchunks][64][dv]   W of each chunk (bf16 in the first half with the tcgen05 kernels)
+    float* dstates;  // [B*H][nchunks][dk][dv]   dS1 of each chunk (likewise bf16 with the tcgen05 kernels)
     float* dwbuf;    // [B*H][nchunks][64][dv]   dW of each chunk
     DeviceErrorRecord* err;  // where a bounded wait that gives up is recorded (nullable)
     int tc_carry;            // the tensor-core carries run: the records need no U and no L
@@ -636,11 +636,20 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
                                     (rev && kk == 0) ? 0u : 1u);
                 tc::mma_commit(&bars[BAR_W]);
             }
-            // keep the state this chunk starts from (S0, or dS1 in reverse)
-            {
-                float* ks = (rev ? p.dstates : p.states) + item * SS + (size_t)(64 * hs) * D + j;
+            // keep the state this chunk starts from: S0 in fp32; dS1 in bf16 (the
+            // gradient products take it in bf16), two columns a store
+            if (!rev) {
+                float* ks = p.states + item * SS + (size_t)(64 * hs) * D + j;
 #pragma unroll
                 for (int i = 0; i < 64; ++i) ks[(size_t)i * D] = m[i];
+            } else {
+                __nv_bfloat16* ks = reinterpret_cast<__nv_bfloat16*>(p.dstates) + item * SS + (size_t)(64 * hs) * D + j;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    const float nb = __shfl_down_sync(0xffffffffu, m[i], 1);
+                    if ((lane & 1) == 0)
+                        *reinterpret_cast<__nv_bfloat162*>(ks + (size_t)i * D) = __floats2bfloat162_rn(m[i], nb);
+                }
             }
             ok = group_wait(BAR_W, it & 1, kWhereW, c, ok);
             tc::tc_fence_after();
@@ -650,12 +659,20 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
                 tc::tmem_ld_32x32b_x32(tmem + lf + TC_D + 32 * hs, v);
                 tc::tmem_ld_wait();
                 const float* sU = reinterpret_cast<const float*>(st + kU);
-                float* kw = (rev ? p.dwbuf : p.wbuf) + item * WS + j;
+                // keep dW in fp32 (the gradients split it into a bf16 pair) and W in bf16
+                float* kw = p.dwbuf + item * WS + j;
+                __nv_bfloat16* kwb = reinterpret_cast<__nv_bfloat16*>(p.wbuf) + item * WS + j;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int r = 32 * hs + i;
                     const float w = rev ? fmaf(sc[r], v[i], sU[r * D + j]) : -v[i];
-                    kw[(size_t)r * D] = w;
+                    if (rev) {
+                        kw[(size_t)r * D] = w;
+                    } else {
+                        const float nb = __shfl_down_sync(0xffffffffu, w, 1);
+                        if ((lane & 1) == 0)
+                            *reinterpret_cast<__nv_bfloat162*>(kwb + (size_t)r * D) = __floats2bfloat162_rn(w, nb);
+                    }
                     v[i] = rev ? -w : sc[r] * w;
                 }
                 uint32_t pk[16];
@@ -1125,8 +1142,8 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
     const float* rec = p.rec + item * L.floats;
     const size_t SS = (size_t)D * D, WS = (size_t)C * D;
     const float* S0 = p.states + item * SS;
-    const float* dS1 = p.dstates + item * SS;
-    const float* W = p.wbuf + item * WS;
+    const __nv_bfloat16* dS1 = reinterpret_cast<const __nv_bfloat16*>(p.dstates) + item * SS;   // bf16
+    const __nv_bfloat16* W = reinterpret_cast<const __nv_bfloat16*>(p.wbuf) + item * WS;        // bf16
     const float* dW = p.dwbuf + item * WS;
     const size_t t0 = tok_index(p, bh, c, 0);
     const size_t ld = (size_t)p.H * D;
@@ -1169,16 +1186,15 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
     float sdot = 0.f;
     {
         {
-            float4 xs[8][2], ys[8][2];
+            float4 xs[8][2];
+            uint4 ys[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int u = tid + kThreads * k, r = u >> 4, c8 = u & 15;
                 const float4* s4 = reinterpret_cast<const float4*>(S0 + r * D + 8 * c8);
-                const float4* d4 = reinterpret_cast<const float4*>(dS1 + r * D + 8 * c8);
                 xs[k][0] = __ldg(s4);
                 xs[k][1] = __ldg(s4 + 1);
-                ys[k][0] = __ldg(d4);
-                ys[k][1] = __ldg(d4 + 1);
+                ys[k] = __ldg(reinterpret_cast<const uint4*>(dS1 + r * D + 8 * c8));
             }
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -1187,8 +1203,7 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
                 float x[8], y[8];
                 *reinterpret_cast<float4*>(x) = xs[k][0];
                 *reinterpret_cast<float4*>(x + 4) = xs[k][1];
-                *reinterpret_cast<float4*>(y) = ys[k][0];
-                *reinterpret_cast<float4*>(y + 4) = ys[k][1];
+                bgt_unpack8(ys[k], y);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) sdot = fmaf(x[e], y[e], sdot);
                 const uint4 hi = bgt_pack8(x);
@@ -1198,15 +1213,15 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
                 for (int e = 0; e < 8; ++e) xh[e] = x[e] - xh[e];
                 *reinterpret_cast<uint4*>(sm + kS0 + so) = hi;
                 *reinterpret_cast<uint4*>(sm + kR2 + so) = bgt_pack8(xh);
-                *reinterpret_cast<uint4*>(sm + kR1 + so) = bgt_pack8(y);
+                *reinterpret_cast<uint4*>(sm + kR1 + so) = ys[k];
             }
         }
         {
             const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(p.k) + t0 * D;
             const __nv_bfloat16* Qg = static_cast<const __nv_bfloat16*>(p.q) + t0 * D;
             const __nv_bfloat16* Og = static_cast<const __nv_bfloat16*>(p.dout) + t0 * D;
-            uint4 kv[4], qv[4], ov[4];
-            float4 ws[4][2], dws[4][2], ts[2][2];
+            uint4 kv[4], qv[4], ov[4], wv[4];
+            float4 dws[4][2], ts[2][2];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int u = tid + kThreads * k, r = u >> 4, c8 = u & 15;
@@ -1215,10 +1230,8 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
                 kv[k] = in ? __ldg(reinterpret_cast<const uint4*>(Kg + r * ld + 8 * c8)) : z;
                 qv[k] = in ? __ldg(reinterpret_cast<const uint4*>(Qg + r * ld + 8 * c8)) : z;
                 ov[k] = in ? __ldg(reinterpret_cast<const uint4*>(Og + r * ld + 8 * c8)) : z;
-                const float4* w4 = reinterpret_cast<const float4*>(W + r * D + 8 * c8);
                 const float4* d4 = reinterpret_cast<const float4*>(dW + r * D + 8 * c8);
-                ws[k][0] = __ldg(w4);
-                ws[k][1] = __ldg(w4 + 1);
+                wv[k] = __ldg(reinterpret_cast<const uint4*>(W + r * D + 8 * c8));
                 dws[k][0] = __ldg(d4);
                 dws[k][1] = __ldg(d4 + 1);
             }
@@ -1236,12 +1249,10 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
                 *reinterpret_cast<uint4*>(sm + kKQ + 16384 * b + so) = qv[k];
                 *reinterpret_cast<uint4*>(sm + kKQ + 16384 * b + 8192 + so) = kv[k];
                 *reinterpret_cast<uint4*>(sm + kOX + 16384 * b + so) = ov[k];
-                float x[8], y[8];
-                *reinterpret_cast<float4*>(x) = ws[k][0];
-                *reinterpret_cast<float4*>(x + 4) = ws[k][1];
+                float y[8];
                 *reinterpret_cast<float4*>(y) = dws[k][0];
                 *reinterpret_cast<float4*>(y + 4) = dws[k][1];
-                *reinterpret_cast<uint4*>(sm + kW + 8192 * b + so) = bgt_pack8(x);
+                *reinterpret_cast<uint4*>(sm + kW + 8192 * b + so) = wv[k];
                 const uint4 hi = bgt_pack8(y);
                 float yh[8];
                 bgt_unpack8(hi, yh);
