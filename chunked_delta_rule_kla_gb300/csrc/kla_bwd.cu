@@ -1060,9 +1060,10 @@ __global__ void __launch_bounds__(bpt::kThreads, 2) bwd_prep_tc_kernel(BwdParams
 //   2  dX -> dv and the [dO ; dX] tile;  P = D o P' (s <= r) and At = D o G
 //      (s < r) kept by the threads that will hold dP and dA;  diag(Gam) E1 kept
 //   3  [X1 ; Y1],  [dP ; -dA],  E2 = At W
-//   4  e = V - diag(Gam) E1 - E2 and dbeta;  the dgamma terms;  diag(eC) Z1 kept;
-//      dP o D and F = diag(beta)(dA o D)
-//   5  X2 = (dP o D) K;  Z5 = (dP o D)^T Q + F K + F^T K
+//   4  e = V - diag(Gam) E1 - E2 and dbeta;  the dgamma terms;  diag(eC) Z1 staged
+//      in shared memory for the dk rows;  dP o D and F = diag(beta)(dA o D)
+//   5  [X2 ; Z5] = [dP o D ; F] K + [0 ; (dP o D)^T] Q + [0 ; F^T] K  (M = 128, so that
+//      X2 and Z5 sit in the lanes of X1 and Y1)
 //   6  dq = diag(Gam) X1 + X2,  dk = -diag(Gam beta) Y1 + diag(eC) Z1 + Z5 + (beta chain) k
 // (eC_r = exp(gam_C - gam_r), D_rs = exp(gam_r - gam_s).)
 namespace bgt {
@@ -1071,16 +1072,16 @@ constexpr uint32_t kTmemCols = 512;
 // TMEM columns
 constexpr uint32_t TD_X = 0;      // phase 1: dX (M=64, N=128);  phase 3: [X1 ; Y1] (M=128, N=128)
 constexpr uint32_t TD_PG = 128;   // phase 1: [P' ; G] (M=128, N=64);  phase 3: [dP ; -dA]
-constexpr uint32_t TD_E = 192;    // E1, then E2 (M=64, N=128);  phase 5: X2
-constexpr uint32_t TD_Z = 320;    // Z1, then Z5 (M=64, N=128)
+constexpr uint32_t TD_E = 192;    // E1, then E2 (M=64, N=128);  phase 5: [X2 ; Z5] (M=128, N=128)
+constexpr uint32_t TD_Z = 320;    // Z1 (M=64, N=128)
 // shared memory
 constexpr uint32_t kKQ = 0;         // [Q box b | K box b] at 16384 b  (A = [Q ; K], B = K)
 constexpr uint32_t kOX = 32768;     // [dO box b | dX box b] at kOX + 16384 b (phase 1: dW - bf16(dW) in the dX boxes)
 constexpr uint32_t kS0 = 65536;     // S0 [128 a][128 j], box b = columns 64 b.. (16 KB each)
 constexpr uint32_t kW = 98304;      // W [64 s][128 j], boxes 8 KB apart
 constexpr uint32_t kR1 = 114688;    // phase 1: dS1 like S0;  then dX (fp32, per thread);  phase 6: X2^T
-constexpr uint32_t kR2 = 147456;    // phase 1: S0 - bf16(S0) like S0;  then diag(Gam) E1, diag(eC) Z1 (per thread);  phase 6: Z^T
-constexpr uint32_t kR3 = 180224;    // phase 1: dW (16 KB), T [64 s][64 r] at +16384;  then At, dP o D, F
+constexpr uint32_t kR2 = 147456;    // phase 1: S0 - bf16(S0) like S0;  then diag(Gam) E1 (per thread);  phase 4: (diag(eC) Z1)^T
+constexpr uint32_t kR3 = 180224;    // phase 1: dW (16 KB), T [64 s][64 r] at +16384;  then At (zeros in phase 5), dP o D, F
 constexpr uint32_t kTlo = 204800;   // phase 1: T - bf16(T), like T
 constexpr uint32_t kVec = 212992;   // gam, Gam, eC, beta, kk, dbeta, dgamma (float[64] each), misc
 constexpr uint32_t kBars = kVec + 8 * 256;
@@ -1342,7 +1343,8 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
 
     // ---- phase 2
     float* dxp = reinterpret_cast<float*>(sm + kR1);   // dX, 64 values per M=64 row thread
-    float* eke = reinterpret_cast<float*>(sm + kR2);   // diag(Gam) E1, later diag(eC) Z1, the same way
+    float* eke = reinterpret_cast<float*>(sm + kR2);   // diag(Gam) E1, the same way
+    float* zt = reinterpret_cast<float*>(sm + kR2);    // later (diag(eC) Z1)^T: [column][row]
     const int pslot = warp * 16 + lane;                // 0..127 for the M = 64 row threads
     float PA[32];                                       // P (top) or At (bottom), columns 32 hh..
     if (ok) {
@@ -1454,7 +1456,8 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
                 atomicAdd(&vdb[r64], db);
             }
         }
-        {   // diag(eC) Z1: the Kt term of dgamma (rows r64), kept for dk
+        __syncthreads();   // every thread has read its diag(Gam) E1 before the staging below
+        {   // diag(eC) Z1: the Kt term of dgamma (rows r64), staged for dk
             float va[32], vb[32];
             ld64(TD_Z, va, vb);
             if (m64) {
@@ -1470,7 +1473,7 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
                         const int i = 8 * c8 + e;
                         const float zz = ec * V64(i);
                         z += x[e] * zz;
-                        eke[i * 128 + pslot] = zz;
+                        zt[(64 * hh + i) * 64 + r64] = zz;
                     }
                 }
                 atomicAdd(&vdg[r64], -z);
@@ -1516,6 +1519,10 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
             for (int c8 = 0; c8 < 4; ++c8)
                 *reinterpret_cast<uint4*>(sm + dst + tc::sw128_offset(rr, 32 * hh + 8 * c8)) = bgt_pack8(t + 8 * c8);
         }
+        // At is consumed (E2 is complete): its tile becomes the zero top half of
+        // the M = 128 operands [0 ; (dP o D)^T] and [0 ; F^T]
+        *reinterpret_cast<uint4*>(sm + kR3 + 32 * tid) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(sm + kR3 + 32 * tid + 16) = make_uint4(0u, 0u, 0u, 0u);
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
         __syncthreads();
@@ -1523,62 +1530,31 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
         // ---- phase 5 products
         if (tid == 0) {
             using tc::sdesc_sw128;
-            constexpr uint32_t i_k = tc::idesc_bf16(64, 128, false, true);   // A K-major, B = K or Q rows (N-major)
-            constexpr uint32_t i_kt = tc::idesc_bf16(64, 128, true, true);   // A^T (M-major)
+            constexpr uint32_t i_a = tc::idesc_bf16(128, 128, false, true);   // A K-major, B = K or Q rows (N-major)
+            constexpr uint32_t i_t = tc::idesc_bf16(128, 128, true, true);    // A M-major
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t kb = s0 + kKQ + 8192 + kk * 2048, qb = s0 + kKQ + kk * 2048;
-                // X2 = (dP o D) K
+                // [dP o D ; F] K: the two 64-row tiles are adjacent
                 tc::mma_bf16(tmem + TD_E, sdesc_sw128(s0 + kR3 + 8192 + kk * 32, 16, 1024),
-                             sdesc_sw128(kb, 16384, 1024), i_k, kk > 0);
-                // Z5 = (dP o D)^T Q + F K + F^T K
-                tc::mma_bf16(tmem + TD_Z, sdesc_sw128(s0 + kR3 + 8192 + kk * 2048, 8192, 1024),
-                             sdesc_sw128(qb, 16384, 1024), i_kt, kk > 0);
-                tc::mma_bf16(tmem + TD_Z, sdesc_sw128(s0 + kR3 + 16384 + kk * 32, 16, 1024),
-                             sdesc_sw128(kb, 16384, 1024), i_k, 1u);
-                tc::mma_bf16(tmem + TD_Z, sdesc_sw128(s0 + kR3 + 16384 + kk * 2048, 8192, 1024),
-                             sdesc_sw128(kb, 16384, 1024), i_kt, 1u);
+                             sdesc_sw128(kb, 16384, 1024), i_a, kk > 0);
+                // [0 ; (dP o D)^T] Q and [0 ; F^T] K: M-major A, the zero tile as its first 64 rows
+                tc::mma_bf16(tmem + TD_E, sdesc_sw128(s0 + kR3 + kk * 2048, 8192, 1024),
+                             sdesc_sw128(qb, 16384, 1024), i_t, 1u);
+                tc::mma_bf16(tmem + TD_E, sdesc_sw128(s0 + kR3 + kk * 2048, 16384, 1024),
+                             sdesc_sw128(kb, 16384, 1024), i_t, 1u);
             }
             tc::mma_commit(&bars[2]);
         }
         __syncthreads();   // dbeta and dgamma complete
     }
     ok = ok && wait_all(2, kWhere5);
-    // ---- phase 6: stage X2^T and Z^T ([column][row]), then the outputs
-    float* x2t = reinterpret_cast<float*>(sm + kR1);
-    float* zt = reinterpret_cast<float*>(sm + kR2);
-    {
-        float za[32], zb[32];
-        if (ok) {
-            float va[32], vb[32];
-            ld64(TD_Z, va, vb);
-            if (m64) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    za[i] = va[i] + eke[i * 128 + pslot];
-                    zb[i] = vb[i] + eke[(i + 32) * 128 + pslot];
-                }
-            }
-        }
-        __syncthreads();   // the kept values are read before the staging overwrites them
-        if (ok) {
-            float va[32], vb[32];
-            ld64(TD_E, va, vb);
-            if (m64) {
-#pragma unroll
-                for (int i = 0; i < 64; ++i) x2t[(64 * hh + i) * 64 + r64] = V64(i);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    zt[(64 * hh + i) * 64 + r64] = za[i];
-                    zt[(64 * hh + i + 32) * 64 + r64] = zb[i];
-                }
-            }
-        }
-    }
-    __syncthreads();
+    // ---- phase 6: dq and dk from [X1 ; Y1], [X2 ; Z5] and the staged (diag(eC) Z1)^T
     if (ok) {
-        float va[32], vb[32];
+        float va[32], vb[32], wa[32], wb[32];
         ld64(TD_X, va, vb);
+        ld64(TD_E, wa, wb);
+#define W64(i) ((i) < 32 ? wa[(i)] : wb[(i) - 32])
         if (rr < nvalid) {
             const float G = vG[rr], br = vbeta[rr];
             __nv_bfloat16* out = static_cast<__nv_bfloat16*>(top ? p.dq : p.dk) + (t0 + (size_t)rr * p.H) * D + 64 * hh;
@@ -1587,10 +1563,7 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
                 for (int c8 = 0; c8 < 8; ++c8) {
                     float x[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int a = 64 * hh + 8 * c8 + e;
-                        x[e] = fmaf(G, V64(8 * c8 + e), x2t[a * 64 + rr]);
-                    }
+                    for (int e = 0; e < 8; ++e) x[e] = fmaf(G, V64(8 * c8 + e), W64(8 * c8 + e));
                     *reinterpret_cast<uint4*>(out + 8 * c8) = bgt_pack8(x);
                 }
             } else {
@@ -1605,12 +1578,13 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int a = 64 * hh + 8 * c8 + e;
-                        x[e] = fmaf(ys, V64(8 * c8 + e), zt[a * 64 + rr]) + vrs * kx[e];
+                        x[e] = fmaf(ys, V64(8 * c8 + e), W64(8 * c8 + e) + zt[a * 64 + rr]) + vrs * kx[e];
                     }
                     *reinterpret_cast<uint4*>(out + 8 * c8) = bgt_pack8(x);
                 }
             }
         }
+#undef W64
         if (warp == 0) {
             // dg: the reverse cumulative sum of dgamma, with the chunk-end total at its
             // last token; lane l holds rows 62 - 2l and 63 - 2l, then a warp scan
