@@ -1054,18 +1054,21 @@ __global__ void __launch_bounds__(bpt::kThreads, 2) bwd_prep_tc_kernel(BwdParams
 // tiles.  Two 64-row operands that multiply the same B are stacked into one
 // M = 128 product: [Q ; K] K^T = [P' ; G], [dO ; dX] S0^T = [X1 ; Y1],
 // [dO ; dX] W^T = [dP ; -dA].  Phases (one CTA per chunk and head):
-//   1  dX = T^T dW,  [P' ; G],  E1 = K S0,  Z1 = W dS1^T;  T, dW and S0 enter
+//   1  dX = T^T dW,  [P' ; G],  E1 = K S0,  [- ; Z1] = [- ; W] dS1^T;  T, dW and S0 enter
 //      dX and E1 as bf16 pairs (hi + lo: hi lo, lo hi and hi hi products for dX),
 //      so that dX and the residual e keep fp32-level accuracy
 //   2  dX -> dv and the [dO ; dX] tile;  P = D o P' (s <= r) and At = D o G
 //      (s < r) kept by the threads that will hold dP and dA;  diag(Gam) E1 kept
 //   3  [X1 ; Y1],  [dP ; -dA],  E2 = At W
-//   4  e = V - diag(Gam) E1 - E2 and dbeta;  the dgamma terms;  diag(eC) Z1 staged
-//      in shared memory for the dk rows;  dP o D and F = diag(beta)(dA o D)
+//   4  e = V - diag(Gam) E1 - E2 and dbeta;  the dgamma terms;  dP o D and
+//      F = diag(beta)(dA o D)
 //   5  [X2 ; Z5] = [dP o D ; F] K + [0 ; (dP o D)^T] Q + [0 ; F^T] K  (M = 128, so that
 //      X2 and Z5 sit in the lanes of X1 and Y1)
 //   6  dq = diag(Gam) X1 + X2,  dk = -diag(Gam beta) Y1 + diag(eC) Z1 + Z5 + (beta chain) k
-// (eC_r = exp(gam_C - gam_r), D_rs = exp(gam_r - gam_s).)
+// (eC_r = exp(gam_C - gam_r), D_rs = exp(gam_r - gam_s).)  Z1 is an M = 128
+// product with W as its second 64 rows (the first 64 are whatever precedes W
+// in shared memory; their result rows are never read), so that Z1 sits in
+// the lanes of Y1 and Z5.
 namespace bgt {
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
@@ -1073,14 +1076,14 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TD_X = 0;      // phase 1: dX (M=64, N=128);  phase 3: [X1 ; Y1] (M=128, N=128)
 constexpr uint32_t TD_PG = 128;   // phase 1: [P' ; G] (M=128, N=64);  phase 3: [dP ; -dA]
 constexpr uint32_t TD_E = 192;    // E1, then E2 (M=64, N=128);  phase 5: [X2 ; Z5] (M=128, N=128)
-constexpr uint32_t TD_Z = 320;    // Z1 (M=64, N=128)
+constexpr uint32_t TD_Z = 320;    // [- ; Z1] (M=128, N=128)
 // shared memory
 constexpr uint32_t kKQ = 0;         // [Q box b | K box b] at 16384 b  (A = [Q ; K], B = K)
 constexpr uint32_t kOX = 32768;     // [dO box b | dX box b] at kOX + 16384 b (phase 1: dW - bf16(dW) in the dX boxes)
 constexpr uint32_t kS0 = 65536;     // S0 [128 a][128 j], box b = columns 64 b.. (16 KB each)
 constexpr uint32_t kW = 98304;      // W [64 s][128 j], boxes 8 KB apart
 constexpr uint32_t kR1 = 114688;    // phase 1: dS1 like S0;  then dX (fp32, per thread);  phase 6: X2^T
-constexpr uint32_t kR2 = 147456;    // phase 1: S0 - bf16(S0) like S0;  then diag(Gam) E1 (per thread);  phase 4: (diag(eC) Z1)^T
+constexpr uint32_t kR2 = 147456;    // phase 1: S0 - bf16(S0) like S0;  then diag(Gam) E1 (per thread)
 constexpr uint32_t kR3 = 180224;    // phase 1: dW (16 KB), T [64 s][64 r] at +16384;  then At (zeros in phase 5), dP o D, F
 constexpr uint32_t kTlo = 204800;   // phase 1: T - bf16(T), like T
 constexpr uint32_t kVec = 212992;   // gam, Gam, eC, beta, kk, dbeta, dgamma (float[64] each), misc
@@ -1311,7 +1314,7 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
         constexpr uint32_t i_dx = tc::idesc_bf16(64, 128, true, true);
         constexpr uint32_t i_pg = tc::idesc_bf16(128, 64, false, false);
         constexpr uint32_t i_e = tc::idesc_bf16(64, 128, false, true);
-        constexpr uint32_t i_z = tc::idesc_bf16(64, 128, false, false);
+        constexpr uint32_t i_z = tc::idesc_bf16(128, 128, false, false);
 #pragma unroll
         for (int kk = 0; kk < 12; ++kk) {   // dX = T^T dW: A = T^T (M-major), B = dW (N-major)
             const int k4 = kk & 3, part = kk >> 2;   // hi hi, hi lo, lo hi
@@ -1326,8 +1329,8 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
             // [P' ; G] = [Q ; K] K^T
             tc::mma_bf16(tmem + TD_PG, sdesc_sw128(s0 + kKQ + ko, 16, 1024),
                          sdesc_sw128(s0 + kKQ + 8192 + ko, 16, 1024), i_pg, kk > 0);
-            // Z1 = W dS1^T: B = dS1 rows (K-major)
-            tc::mma_bf16(tmem + TD_Z, sdesc_sw128(s0 + kW + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+            // [- ; Z1] = [- ; W] dS1^T: A's rows 64..127 are W's box, B = dS1 rows (K-major)
+            tc::mma_bf16(tmem + TD_Z, sdesc_sw128(s0 + kW - 8192 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
                          sdesc_sw128(s0 + kR1 + ko, 16, 1024), i_z, kk > 0);
         }
 #pragma unroll
@@ -1344,7 +1347,6 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
     // ---- phase 2
     float* dxp = reinterpret_cast<float*>(sm + kR1);   // dX, 64 values per M=64 row thread
     float* eke = reinterpret_cast<float*>(sm + kR2);   // diag(Gam) E1, the same way
-    float* zt = reinterpret_cast<float*>(sm + kR2);    // later (diag(eC) Z1)^T: [column][row]
     const int pslot = warp * 16 + lane;                // 0..127 for the M = 64 row threads
     float PA[32];                                       // P (top) or At (bottom), columns 32 hh..
     if (ok) {
@@ -1456,29 +1458,22 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
                 atomicAdd(&vdb[r64], db);
             }
         }
-        __syncthreads();   // every thread has read its diag(Gam) E1 before the staging below
-        {   // diag(eC) Z1: the Kt term of dgamma (rows r64), staged for dk
+        if (!top) {   // diag(eC) Z1: the Kt term of dgamma (the dk rows rr, lanes 64..127)
             float va[32], vb[32];
             ld64(TD_Z, va, vb);
-            if (m64) {
-                float z = 0.f;
-                const float ec = veC[r64];
+            float z = 0.f;
+            const float ec = veC[rr];
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    float x[8];
-                    bgt_unpack8(*reinterpret_cast<const uint4*>(sm + kKQ + 16384 * hh + 8192 +
-                                                                tc::sw128_offset(r64, 8 * c8)), x);
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float x[8];
+                bgt_unpack8(*reinterpret_cast<const uint4*>(sm + kKQ + 16384 * hh + 8192 +
+                                                            tc::sw128_offset(rr, 8 * c8)), x);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int i = 8 * c8 + e;
-                        const float zz = ec * V64(i);
-                        z += x[e] * zz;
-                        zt[(64 * hh + i) * 64 + r64] = zz;
-                    }
-                }
-                atomicAdd(&vdg[r64], -z);
-                atomicAdd(&vmisc[0], z);
+                for (int e = 0; e < 8; ++e) z += x[e] * V64(8 * c8 + e);
             }
+            z *= ec;
+            atomicAdd(&vdg[rr], -z);
+            atomicAdd(&vmisc[0], z);
         }
         {   // [X1 ; Y1]: the O term (q . Gam X1) and the Y term (k . -Gam beta Y1) of dgamma
             float va[32], vb[32];
@@ -1549,11 +1544,21 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
         __syncthreads();   // dbeta and dgamma complete
     }
     ok = ok && wait_all(2, kWhere5);
-    // ---- phase 6: dq and dk from [X1 ; Y1], [X2 ; Z5] and the staged (diag(eC) Z1)^T
+    // ---- phase 6: dq and dk from [X1 ; Y1], [X2 ; Z5] and [- ; Z1]
     if (ok) {
         float va[32], vb[32], wa[32], wb[32];
         ld64(TD_X, va, vb);
         ld64(TD_E, wa, wb);
+        if (!top) {   // Z5 + diag(eC) Z1 into wa / wb
+            float za[32], zb[32];
+            ld64(TD_Z, za, zb);
+            const float ec = veC[rr];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                wa[i] = fmaf(ec, za[i], wa[i]);
+                wb[i] = fmaf(ec, zb[i], wb[i]);
+            }
+        }
 #define W64(i) ((i) < 32 ? wa[(i)] : wb[(i) - 32])
         if (rr < nvalid) {
             const float G = vG[rr], br = vbeta[rr];
@@ -1576,10 +1581,7 @@ __global__ void __launch_bounds__(bgt::kThreads, 1) bwd_grad_tc_kernel(BwdParams
                     bgt_unpack8(*reinterpret_cast<const uint4*>(sm + kKQ + 16384 * hh + 8192 +
                                                                 tc::sw128_offset(rr, 8 * c8)), kx);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int a = 64 * hh + 8 * c8 + e;
-                        x[e] = fmaf(ys, V64(8 * c8 + e), W64(8 * c8 + e) + zt[a * 64 + rr]) + vrs * kx[e];
-                    }
+                    for (int e = 0; e < 8; ++e) x[e] = fmaf(ys, V64(8 * c8 + e), W64(8 * c8 + e)) + vrs * kx[e];
                     *reinterpret_cast<uint4*>(out + 8 * c8) = bgt_pack8(x);
                 }
             }
