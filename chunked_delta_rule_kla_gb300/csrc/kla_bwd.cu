@@ -20,13 +20,18 @@
 //   dS0 = Gam_C dS1 + (diag(Gam) Q)^T dO - Wk^T dW
 //
 // Three launches:
-//   bwd_prep_kernel   every (chunk, head): beta, gamma, T, Wk, U, P^T dO and
-//                     L = (diag(Gam) Q)^T dO
-//   bwd_carry_kernel  every head twice, at the same time: the forward carry
-//                     (chunks in order) keeps S0 and W of each chunk; the
-//                     reverse carry (chunks in reverse, dS0 = Gam_C dS1 + L -
-//                     Wk^T dW) keeps dS1 and dW.  Neither needs the other.
-//   bwd_grad_kernel   every (chunk, head): dq, dk, dv, dg, deta
+//   prep    every (chunk, head): beta, gamma, T, Wk, P^T dO (and U and
+//           L = (diag(Gam) Q)^T dO where the carries do not form them)
+//   carry   every head twice, at the same time: the forward carry (chunks in
+//           order) keeps S0 and W of each chunk; the reverse carry (chunks in
+//           reverse, dS0 = Gam_C dS1 + L - Wk^T dW) keeps dS1 and dW.
+//           Neither needs the other.
+//   grad    every (chunk, head): dq, dk, dv, dg, deta
+// With bf16 I/O and d_k = d_v = 128 the three are tcgen05 kernels
+// (bwd_prep_tc_kernel, bwd_carry_tc_kernel, bwd_grad_tc_kernel: bf16 operand
+// tiles in shared memory, fp32 accumulators in tensor memory, each described
+// where it is defined); every other shape and fp32 I/O use bwd_prep_kernel,
+// bwd_carry_kernel and bwd_grad_kernel, described next.
 //
 // Given S0, dS1, W and dW, the gradient kernel works out the rest:
 //   - dX = T^T dW, dv = diag(beta) dX;
@@ -35,10 +40,10 @@
 //   - dg, the reverse cumulative sum of dgamma inside the chunk;
 //   - the chain through beta (deta, and with the Kaczmarz rule a term of dk).
 //
-// All products are CTA-wide tf32 mma.sync tiles (m16n8k8, fp32 accumulate).
-// Operands come from shared memory, or straight from global memory through
-// L1/L2.  With fp32 I/O each product is split into three tf32 products
-// (hi*hi + hi*lo + lo*hi), which keeps fp32-level accuracy.
+// In those three kernels all products are CTA-wide tf32 mma.sync tiles
+// (m16n8k8, fp32 accumulate).  Operands come from shared memory, or straight
+// from global memory through L1/L2.  With fp32 I/O each product is split into
+// three tf32 products (hi*hi + hi*lo + lo*hi), which keeps fp32-level accuracy.
 #include "kla_internal.cuh"
 #include "kla_tile.cuh"
 #include "tc_common.cuh"
@@ -740,7 +745,7 @@ __global__ void __launch_bounds__(bct::kThreads, 1) bwd_carry_tc_kernel(BwdParam
 // they are, Wk (in Wk's place) and T diag(beta) (in U's place), with the
 // products on tcgen05 (bf16 operands, fp32 accumulation):
 //   G = K K^T (beta and ||k||^2 from its diagonal),  K Q^T  (M = 64, N = 64)
-//   T = (I + diag(beta) strict_lower(D o G))^{-1} by forward substitution (fp32)
+//   T = (I + diag(beta) strict_lower(D o G))^{-1} in fp32 by 16 x 16 blocks
 //   Wk = T diag(beta Gam) K,  P^T dO with P^T_rs = exp(gam_s - gam_r) (k_r . q_s), s >= r
 // U and L are left out (the carries form them).  Two CTAs fit on an SM.
 namespace bpt {
@@ -753,7 +758,7 @@ constexpr uint32_t kQ = 16384;    // Q, same layout
 constexpr uint32_t kO = 32768;    // dO, same layout
 constexpr uint32_t kTg = 49152;   // T diag(beta Gam) [64 r][64 s] bf16
 constexpr uint32_t kPT = 57344;   // P^T [64 r][64 s] bf16
-constexpr uint32_t kA = 65536;    // A, then T: fp32 [64][kLdA]
+constexpr uint32_t kA = 65536;    // G, then A = diag(beta) strict_lower(D o G): fp32 [64][kLdA]
 constexpr int kLdA = 65;
 constexpr uint32_t kT = kA + 64 * kLdA * 4;        // T fp32 [64][kLdA]
 constexpr uint32_t kVec = kT + 64 * kLdA * 4;      // gam, beta, kk, bg (float[64] each)
