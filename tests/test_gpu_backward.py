@@ -109,6 +109,15 @@ def test_backward_strong_decay(io):
     _check(inp, io, do, dh)
 
 
+def test_backward_odd_batch_and_heads():
+    # B = 3, H = 3 with d_k = d_v = 128 in bf16 (the tensor-core kernels): token
+    # rows interleave three heads, and the carries' grid has 18 CTAs
+    case = kla_inputs.TINY.with_(B=3, T=190, H=3, dk=128, dv=128, io="bf16", h0_std=0.05, seed=365)
+    inp = kla_inputs.make_prefill(case, device="cuda")
+    do, dh = _grad_inputs(inp, 465)
+    _check(inp, "bf16", do, dh)
+
+
 def test_backward_large_start_state():
     # h0 of unit scale: the residual e = v - Gam k S0 - ... is dominated by the
     # start state, the case that needs S0 at fp32-level accuracy in the products
