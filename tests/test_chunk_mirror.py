@@ -193,3 +193,107 @@ def test_loglinear_chunk_pairs_equal_the_by_origin_oracle(C, T, direct):
     ref = oracle.kla_oracle_loglinear_forward(q, k, v, g, eta, lam, 1e-6, beta_direct=direct)
     got = cm.loglinear_level_passes(q, k, v, g, eta, lam, 1e-6, C=C, beta_direct=direct, pair=True)
     assert _rel(got, ref) <= 1e-11
+
+
+# ------------------------------------------------------------------
+# The tensor-core backward's arrangement of the chunk algebra (bf16 I/O,
+# d_k = d_v = 128 in the library), restated in fp64: the carries form U from
+# T diag(beta) and L = dO^T diag(Gam) Q themselves and keep W, dW, S0 and dS1;
+# the gradient kernel stacks its products ([P' ; G], [X1 ; Y1], [dP ; -dA],
+# [X2 ; Z5]) and takes dgamma's column sums separately.  Every step is an
+# exact rewrite of the chunk reverse mode, so it must equal the oracle's
+# sequential reverse mode to rounding.
+
+def _tc_backward(q, k, v, g, eta, eps, h0, dout, dhT, C=64, beta_direct=False):
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    out = dict(dq=np.zeros_like(q), dk=np.zeros_like(k), dv=np.zeros_like(v),
+               dg=np.zeros_like(g), deta=np.zeros_like(eta), dh0=np.zeros((B, H, dk, dv)))
+    for b in range(B):
+        for h in range(H):
+            recs, S = [], (np.zeros((dk, dv)) if h0 is None else h0[b, h].copy())
+            for t0 in range(0, T, C):
+                t1 = min(t0 + C, T)
+                Q, K, V, O = q[b, t0:t1, h], k[b, t0:t1, h], v[b, t0:t1, h], dout[b, t0:t1, h]
+                gam = np.cumsum(g[b, t0:t1, h])
+                G = K @ K.T
+                kk = np.diag(G).copy()
+                beta = eta[b, t0:t1, h] if beta_direct else eta[b, t0:t1, h] / (kk + eps)
+                Dm = np.exp(gam[:, None] - gam[None, :])
+                n = len(gam)
+                strict, incl = np.tril(np.ones((n, n)), -1), np.tril(np.ones((n, n)))
+                At = strict * Dm * G                       # D o G, s < r
+                Tm = np.linalg.inv(np.eye(n) + beta[:, None] * At)
+                Wk = Tm @ ((beta * np.exp(gam))[:, None] * K)
+                sc = np.exp(gam[-1] - gam)
+                PT = np.triu(np.exp(gam[None, :] - gam[:, None]) * (K @ Q.T))   # P^T from K Q^T, s >= r
+                # forward carry: D = -V^T Tb^T + S0^T Wk^T = -W^T
+                W = -(-(V.T @ (Tm * beta[None, :]).T) + S.T @ Wk.T).T
+                recs.append(dict(Q=Q, K=K, V=V, O=O, gam=gam, G=G, kk=kk, beta=beta, Dm=Dm, At=At, Tm=Tm,
+                                 Wk=Wk, sc=sc, PT=PT, S0=S.copy(), W=W, n=n, strict=strict, incl=incl, t0=t0))
+                S = np.exp(gam[-1]) * S + K.T @ (sc[:, None] * W)
+            dS = np.zeros((dk, dv)) if dhT is None else dhT[b, h].copy()
+            for r in reversed(recs):
+                Q, K, V, O, gam, beta, Dm, n = r["Q"], r["K"], r["V"], r["O"], r["gam"], r["beta"], r["Dm"], r["n"]
+                S0, W, Tm, At, Wk, sc = r["S0"], r["W"], r["Tm"], r["At"], r["Wk"], r["sc"]
+                Gam = np.exp(gam)
+                # reverse carry: D = dS1^T K^T, dW = diag(sc) D^T + P^T dO;  S_acc = dO^T diag(Gam) Q - dW^T Wk
+                dW = sc[:, None] * (dS.T @ K.T).T + r["PT"] @ O
+                dS1 = dS
+                dS = np.exp(gam[-1]) * dS + (O.T @ (Gam[:, None] * Q) - dW.T @ Wk).T
+                # gradient kernel, phase 1
+                dX = Tm.T @ dW
+                PG = np.vstack([Q, K]) @ K.T
+                P = r["incl"] * Dm * PG[:n]
+                At_ = r["strict"] * Dm * PG[n:]
+                E1 = K @ S0
+                Z1 = W @ dS1.T
+                # phases 3 and 4
+                XY = np.vstack([O, dX]) @ S0.T
+                dPA = np.vstack([O, dX]) @ W.T
+                E2 = At_ @ W
+                e = V - Gam[:, None] * E1 - E2
+                dbeta = (dX * e).sum(1)
+                dgam = Gam * (Q * XY[:n]).sum(1) - Gam * beta * (K * XY[n:]).sum(1)
+                z = sc * (K * Z1).sum(1)
+                dgam -= z
+                total = z.sum() + np.exp(gam[-1]) * (dS1 * S0).sum()
+                dPm = r["incl"] * dPA[:n]
+                dA = -r["strict"] * dPA[n:]
+                dgam += (dPm * P).sum(1) - (dPm * P).sum(0)
+                dgam += beta * (dA * At_).sum(1) - (beta[:, None] * dA * At_).sum(0)
+                dPD = dPm * Dm
+                F = beta[:, None] * r["strict"] * Dm * dA
+                # phase 5: [X2 ; Z5] = [dPD ; F] K + [0 ; dPD^T] Q + [0 ; F^T] K
+                Z = np.zeros((n, n))
+                X2Z5 = np.vstack([dPD, F]) @ K + np.vstack([Z, dPD.T]) @ Q + np.vstack([Z, F.T]) @ K
+                den = r["kk"] + eps
+                vrs = np.zeros(n) if beta_direct else -2 * beta * dbeta / den
+                dQ = Gam[:, None] * XY[:n] + X2Z5[:n]
+                dK = -(Gam * beta)[:, None] * XY[n:] + sc[:, None] * Z1 + X2Z5[n:] + vrs[:, None] * K
+                dgam[-1] += total
+                t0, t1 = r["t0"], r["t0"] + n
+                out["dq"][b, t0:t1, h] = dQ
+                out["dk"][b, t0:t1, h] = dK
+                out["dv"][b, t0:t1, h] = beta[:, None] * dX
+                out["dg"][b, t0:t1, h] = np.cumsum(dgam[::-1])[::-1]
+                out["deta"][b, t0:t1, h] = dbeta if beta_direct else dbeta / den
+            out["dh0"][b, h] = dS
+    return out
+
+
+@pytest.mark.parametrize("C", [16, 64, "T"])
+@pytest.mark.parametrize("T", [1, 65, 130])
+@pytest.mark.parametrize("direct", [False, True])
+def test_tensor_core_backward_arrangement_equals_the_sequential_reverse_mode(C, T, direct):
+    q, k, v, g, eta, h0 = _case(300 + T, B=1, T=T, dk=8, dv=5,
+                                knorm=(0.5, 1.2) if direct else (0.25, 4.0))
+    rng = np.random.default_rng(3 + T)
+    dout = rng.standard_normal(v.shape)
+    dhT = rng.standard_normal((1, 2, 8, 5))
+    eps = 1e-3
+    ref = oracle.kla_oracle_backward(q, k, v, g, eta, eps, h0, dout, dhT, beta_direct=direct)
+    got = _tc_backward(*(np.asarray(x, np.float64) for x in (q, k, v, g, eta)), eps,
+                       np.asarray(h0, np.float64), dout, dhT, C=T if C == "T" else C, beta_direct=direct)
+    for name in ("dq", "dk", "dv", "dg", "deta", "dh0"):
+        assert _rel(got[name], ref[name]) <= 1e-10, name
