@@ -940,12 +940,17 @@ __global__ void __launch_bounds__(bpt::kThreads, 2) bwd_prep_tc_kernel(BwdParams
     __syncthreads();
     {
         float* sY = reinterpret_cast<float*>(sm + kTg);   // [j block][16][16] scratch, before Tg
+        // (block row i, block column jb: both compile-time once unrolled, so the
+        // sums have fixed lengths; four partial sums a thread)
+#pragma unroll
         for (int i = 1; i < 4; ++i) {
-            // (four partial sums a thread: the sums are chains of shared-memory loads)
-            for (int e = tid; e < 256 * i; e += kThreads) {
-                const int jb = e >> 8, r = 16 * i + ((e >> 4) & 15), col = 16 * jb + (e & 15);
+#pragma unroll
+            for (int jb = 0; jb < i; ++jb) {
+                const int e = (jb << 8) + tid;
+                const int r = 16 * i + ((e >> 4) & 15), col = 16 * jb + (e & 15);
                 float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
-                for (int s2 = 16 * jb; s2 < 16 * i; s2 += 4) {   // multiples of 16 long
+#pragma unroll
+                for (int s2 = 16 * jb; s2 < 16 * i; s2 += 4) {
                     y0 = fmaf(sA[r * kLdA + s2], sT[s2 * kLdA + col], y0);
                     y1 = fmaf(sA[r * kLdA + s2 + 1], sT[(s2 + 1) * kLdA + col], y1);
                     y2 = fmaf(sA[r * kLdA + s2 + 2], sT[(s2 + 2) * kLdA + col], y2);
@@ -954,8 +959,10 @@ __global__ void __launch_bounds__(bpt::kThreads, 2) bwd_prep_tc_kernel(BwdParams
                 sY[e] = (y0 + y1) + (y2 + y3);
             }
             __syncthreads();
-            for (int e = tid; e < 256 * i; e += kThreads) {
-                const int jb = e >> 8, i2 = (e >> 4) & 15, cc = e & 15;
+#pragma unroll
+            for (int jb = 0; jb < i; ++jb) {
+                const int e = (jb << 8) + tid;
+                const int i2 = (e >> 4) & 15, cc = e & 15;
                 const int r = 16 * i + i2;
                 float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
 #pragma unroll
