@@ -926,7 +926,11 @@ __global__ void __launch_bounds__(bpt::kThreads, 2) bwd_prep_tc_kernel(BwdParams
         for (int i = 0; i < 16; ++i) {
             const int r = 16 * b + i;
             float a = 0.f;
-            for (int s2 = j + part; s2 < r; s2 += 4) a = fmaf(sA[r * kLdA + s2], sT[s2 * kLdA + j], a);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {   // s2 < r <= j + 15: at most four terms a lane
+                const int s2 = j + part + 4 * u;
+                if (s2 < r) a = fmaf(sA[r * kLdA + s2], sT[s2 * kLdA + j], a);
+            }
             a += __shfl_xor_sync(0xffffffffu, a, 1);
             a += __shfl_xor_sync(0xffffffffu, a, 2);
             if (part == 0) sT[r * kLdA + j] = r == j ? 1.f : (r < j ? 0.f : -a);
