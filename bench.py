@@ -110,7 +110,7 @@ TRAFFIC_BYTES = {
     "long_prefill_bf16_B1H16T131072d128": 6223.5e6,
     "decode_bf16_B64H16d128_x1024": 73.9e6,
     "loglinear_train_prefill_bf16_B8H8T4096d128": 1760.5e6,
-    "bwd_train_prefill_bf16_B8H8T4096d128": 2773.0e6,
+    "bwd_train_prefill_bf16_B8H8T4096d128": 2772.8e6,
     "deltakata_train_prefill_bf16_B8H8T4096d128": 413.7e6,
 }
 
