@@ -936,8 +936,9 @@ __global__ void __launch_bounds__(bpt::kThreads, 2) bwd_prep_tc_kernel(BwdParams
             if (part == 0) sT[r * kLdA + j] = r == j ? 1.f : (r < j ? 0.f : -a);
             __syncwarp();
         }
-        for (int e = tid; e < C * C; e += kThreads) {   // the blocks above the diagonal
-            const int r = e >> 6, col = e & 63;
+#pragma unroll
+        for (int k = 0; k < C * C / kThreads; ++k) {   // the blocks above the diagonal
+            const int e = tid + kThreads * k, r = e >> 6, col = e & 63;
             if ((r >> 4) < (col >> 4)) sT[r * kLdA + col] = 0.f;
         }
     }
@@ -982,8 +983,9 @@ __global__ void __launch_bounds__(bpt::kThreads, 2) bwd_prep_tc_kernel(BwdParams
         }
     }
     // T diag(beta Gam) as bf16 (rows r, columns s); T (fp32) and the vectors to the record
-    for (int u = tid; u < 512; u += kThreads) {
-        const int r = u >> 3, c8 = u & 7;
+#pragma unroll
+    for (int k = 0; k < 512 / kThreads; ++k) {
+        const int u = tid + kThreads * k, r = u >> 3, c8 = u & 7;
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = sT[r * kLdA + 8 * c8 + e] * vbg[8 * c8 + e];
